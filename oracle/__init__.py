@@ -1,0 +1,218 @@
+"""Python access to the scalar C oracle (fp8opt_oracle.c).
+
+TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library
+never calls it, and it never calls the CUDA library.
+
+Arrays are numpy: FP8 codes ``uint8``; FP16 and BF16 as their ``uint16`` bit
+patterns; FP32 as ``float32``.  ``build()`` compiles the C file with gcc
+(``-ffp-contract=off``, no fast-math) into ``oracle/_build``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+from typing import List, Sequence
+
+import numpy as np
+
+E4M3, E5M2 = 0, 1
+F32, BF16, F16 = 0, 1, 2
+FMT = {"e4m3": E4M3, "e5m2": E5M2}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp8opt_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "liboracle_fp8opt.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into a shared library (gcc); return its path."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call([
+        "gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
+        "-fno-fast-math", "-fno-finite-math-only", "-Wall", "-o", tmp, _SRC,
+        "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class Param(C.Structure):
+    _fields_ = [
+        ("numel", C.c_int64), ("g", C.c_void_p), ("g_scale", C.c_float),
+        ("g_fmt", C.c_int), ("m", C.c_void_p), ("m_scale", C.c_void_p),
+        ("v", C.c_void_p), ("w", C.c_void_p), ("w8", C.c_void_p),
+        ("w8_scale", C.c_void_p), ("w8_amax", C.c_void_p),
+    ]
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = C.CDLL(build())
+        L.oracle_fp8_decode.restype = C.c_float
+        L.oracle_fp8_decode.argtypes = [C.c_uint8, C.c_int]
+        L.oracle_fp8_encode.restype = C.c_uint8
+        L.oracle_fp8_encode.argtypes = [C.c_float, C.c_int]
+        L.oracle_f32_to_f16.restype = C.c_uint16
+        L.oracle_f32_to_f16.argtypes = [C.c_float]
+        L.oracle_f16_to_f32.restype = C.c_float
+        L.oracle_f16_to_f32.argtypes = [C.c_uint16]
+        L.oracle_bf16_to_f32.restype = C.c_float
+        L.oracle_bf16_to_f32.argtypes = [C.c_uint16]
+        L.oracle_scale_from_amax.restype = C.c_float
+        L.oracle_scale_from_amax.argtypes = [C.c_float, C.c_int]
+        L.oracle_fp8_max.restype = C.c_double
+        L.oracle_fp8_max.argtypes = [C.c_int]
+        L.oracle_cast_scaled.restype = C.c_int
+        L.oracle_cast_scaled.argtypes = [C.c_void_p, C.c_int, C.c_int64, C.c_int,
+                                         C.c_void_p, C.c_void_p, C.c_void_p]
+        L.oracle_adamw_step.restype = C.c_int
+        L.oracle_adamw_step.argtypes = [C.POINTER(Param), C.c_int, C.c_float,
+                                        C.c_float, C.c_float, C.c_float,
+                                        C.c_float, C.c_int64, C.c_float]
+        L.oracle_state_bytes.restype = C.c_int
+        L.oracle_state_bytes.argtypes = [C.c_int]
+        for nm in ("oracle_fp8_encode_array", "oracle_fp8_decode_array"):
+            getattr(L, nm).restype = None
+            getattr(L, nm).argtypes = [C.c_void_p, C.c_int64, C.c_int, C.c_void_p]
+        for nm in ("oracle_f32_to_f16_array", "oracle_f16_to_f32_array"):
+            getattr(L, nm).restype = None
+            getattr(L, nm).argtypes = [C.c_void_p, C.c_int64, C.c_void_p]
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+# ------------------------------------------------------------------ codecs
+
+def fp8_decode(codes: np.ndarray, fmt: int) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float32)
+    lib().oracle_fp8_decode_array(_ptr(c), c.size, fmt, _ptr(out))
+    return out
+
+
+def fp8_encode(x: np.ndarray, fmt: int) -> np.ndarray:
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.uint8)
+    lib().oracle_fp8_encode_array(_ptr(a), a.size, fmt, _ptr(out))
+    return out
+
+
+def f32_to_f16(x: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.uint16)
+    lib().oracle_f32_to_f16_array(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def f16_to_f32(h: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(a.shape, dtype=np.float32)
+    lib().oracle_f16_to_f32_array(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def scale_from_amax(amax: float, fmt: int) -> float:
+    return lib().oracle_scale_from_amax(amax, fmt)
+
+
+def fp8_max(fmt: int) -> float:
+    return lib().oracle_fp8_max(fmt)
+
+
+def state_bytes(level: int) -> int:
+    return lib().oracle_state_bytes(level)
+
+
+# -------------------------------------------------------------------- cast
+
+def cast_scaled(src: np.ndarray, dtype: int, fmt: int):
+    """Returns (codes uint8, amax float32 scalar, scale float32 scalar)."""
+    want = np.float32 if dtype == F32 else np.uint16
+    s = np.ascontiguousarray(src, dtype=want).ravel()
+    codes = np.empty(s.size, dtype=np.uint8)
+    amax = np.zeros(1, dtype=np.float32)
+    scale = np.zeros(1, dtype=np.float32)
+    rc = lib().oracle_cast_scaled(_ptr(s), dtype, s.size, fmt, _ptr(codes),
+                                  _ptr(amax), _ptr(scale))
+    if rc != 0:
+        raise ValueError(f"oracle_cast_scaled rejected its arguments ({rc})")
+    return codes, amax[0], scale[0]
+
+
+# -------------------------------------------------------------------- step
+
+class StepState:
+    """One tensor's optimizer state, as numpy arrays the oracle updates in place.
+
+    g: uint8 gradient codes; g_scale: float; g_fmt: E4M3/E5M2;
+    m: uint8 E4M3 codes; m_scale: float32[1]; v, w: uint16 FP16 bits;
+    O3 only: w8 uint8, w8_scale float32[1], w8_amax float32[1].
+    """
+
+    def __init__(self, g, g_scale, m, m_scale, v, w, g_fmt=E4M3, o3=False):
+        self.g = np.ascontiguousarray(g, dtype=np.uint8).ravel()
+        self.g_scale = float(np.float32(g_scale))
+        self.g_fmt = g_fmt
+        self.m = np.ascontiguousarray(m, dtype=np.uint8).ravel().copy()
+        self.m_scale = np.array([m_scale], dtype=np.float32)
+        self.v = np.ascontiguousarray(v, dtype=np.uint16).ravel().copy()
+        self.w = np.ascontiguousarray(w, dtype=np.uint16).ravel().copy()
+        n = self.g.size
+        assert self.m.size == n and self.v.size == n and self.w.size == n
+        if o3:
+            self.w8 = np.zeros(n, dtype=np.uint8)
+            self.w8_scale = np.ones(1, dtype=np.float32)
+            self.w8_amax = np.zeros(1, dtype=np.float32)
+        else:
+            self.w8 = self.w8_scale = self.w8_amax = None
+
+    @property
+    def numel(self):
+        return self.g.size
+
+    def copy(self):
+        c = StepState.__new__(StepState)
+        for k, v in self.__dict__.items():
+            setattr(c, k, v.copy() if isinstance(v, np.ndarray) else v)
+        return c
+
+    def _param(self) -> Param:
+        p = Param()
+        p.numel = self.g.size
+        p.g = _ptr(self.g)
+        p.g_scale = self.g_scale
+        p.g_fmt = self.g_fmt
+        p.m = _ptr(self.m)
+        p.m_scale = _ptr(self.m_scale)
+        p.v = _ptr(self.v)
+        p.w = _ptr(self.w)
+        if self.w8 is not None:
+            p.w8 = _ptr(self.w8)
+            p.w8_scale = _ptr(self.w8_scale)
+            p.w8_amax = _ptr(self.w8_amax)
+        return p
+
+
+def adamw_step(states: Sequence[StepState], lr, beta1, beta2, eps, wd, step,
+               inv_loss_scale) -> int:
+    """One oracle AdamW step over the list; returns found_inf (0 or 1)."""
+    arr = (Param * max(1, len(states)))()
+    for i, s in enumerate(states):
+        arr[i] = s._param()
+    rc = lib().oracle_adamw_step(arr, len(states), lr, beta1, beta2, eps, wd,
+                                 step, inv_loss_scale)
+    if rc < 0:
+        raise ValueError(f"oracle_adamw_step rejected its arguments ({rc})")
+    return rc

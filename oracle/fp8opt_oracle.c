@@ -1,0 +1,387 @@
+/*
+ * fp8opt oracle: a plain, slow, scalar CPU implementation of the scaled FP8
+ * cast and of the FP8-state AdamW step (MS-AMP levels O2 and O3).
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the bench's
+ * CPU-baseline leg may load or call this file.  It shares no code with the
+ * CUDA library: its own codecs, its own loops, its own scalar set-up.
+ *
+ * Sources.  MS-AMP documentation, "Optimization Level" page: O1 keeps weight
+ * gradients in FP8; O2 keeps the Adam/AdamW first moment in FP8 and the second
+ * moment in FP16 with FP16 weights; O3 adds an FP16 master weight and an FP8
+ * regular weight (the level table).  MS-AMP README, "Usage": the GradScaler
+ * loop (scale, backward, step) and "Recognized optimizers are torch.optim.Adam
+ * and torch.optim.AdamW".  TransformerEngine issue #131: the two FP8 formats
+ * E4M3 and E5M2.  The pages give neither bit layouts nor a scaling rule nor an
+ * update order; the readings used here are:
+ *   - E4M3 / E5M2 are the OCP 8-bit floating-point formats (E4M3: bias 7, no
+ *     infinity, NaN = S.1111.111, max 448; E5M2: bias 15, IEEE-like, max
+ *     57344).  Encoding rounds to nearest, ties to even, and saturates finite
+ *     overflow to +-max.  A NaN input gives code 0x7F; an infinite input gives
+ *     0x7F in E4M3 and the signed infinity code in E5M2.
+ *   - The per-tensor scale is fp8_max / amax, computed just in time from the
+ *     tensor being encoded, as one fp32 IEEE division; it is 1.0 when amax is
+ *     zero or not finite, or when the quotient is not finite.
+ *   - amax orders NaN above +inf above every finite |x|; a NaN amax is
+ *     returned as the quiet NaN 0x7FC00000.
+ *   - The AdamW update follows torch.optim.AdamW (decoupled weight decay, eps
+ *     added after the bias-corrected square root), in fp32 with every product
+ *     and sum rounded on its own (no fused multiply-add), in the order written
+ *     in oracle_adamw_step below.  GradScaler order: dequantize, then unscale.
+ *   - found_inf is set when any unscaled gradient element is not finite; then
+ *     no state element changes.
+ *   - The first moment is re-encoded from the fp32 value of this step, with a
+ *     scale taken from this step's amax; the O3 weight copy is encoded from the
+ *     FP16-rounded master.
+ *
+ * Floating point: compiled with -ffp-contract=off and no fast-math, so every
+ * float expression below is evaluated as written in IEEE binary32 with
+ * round-to-nearest-even (C float arithmetic with FLT_EVAL_METHOD 0).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+enum { OR_E4M3 = 0, OR_E5M2 = 1 };
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2 };
+
+/* ---------------------------------------------------------------- formats */
+
+typedef struct {
+    int mbits;       /* explicit mantissa bits */
+    int bias;        /* exponent bias */
+    double maxval;   /* largest finite magnitude */
+    int has_inf;     /* all-ones exponent with zero mantissa is infinity */
+} or_format;
+
+/* E4M3, E5M2 (OCP 8-bit formats), and IEEE binary16 for the FP16 state. */
+static const or_format OR_FMT[2] = {
+    {3, 7, 448.0, 0},
+    {2, 15, 57344.0, 1},
+};
+static const or_format OR_HALF = {10, 15, 65504.0, 1};
+
+static float or_bits_f32(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+
+/* Largest finite magnitude of an FP8 format (448 or 57344). */
+double oracle_fp8_max(int fmt) { return OR_FMT[fmt].maxval; }
+
+/* Value of an FP8 code by the format definition: (-1)^s * 2^(E-bias) *
+ * (1 + M/2^mbits) for a nonzero exponent field, (-1)^s * 2^(1-bias) *
+ * M/2^mbits for a zero one; E4M3's S.1111.111 is NaN, E5M2's all-ones
+ * exponent is infinity (M = 0) or NaN. */
+float oracle_fp8_decode(uint8_t c, int fmt)
+{
+    const or_format *f = &OR_FMT[fmt];
+    int ebits = 7 - f->mbits;
+    int s = c >> 7;
+    int e = (c >> f->mbits) & ((1 << ebits) - 1);
+    int m = c & ((1 << f->mbits) - 1);
+    int eall = (1 << ebits) - 1;
+    double v;
+    if (!f->has_inf && e == eall && m == (1 << f->mbits) - 1)
+        return or_bits_f32(0x7FC00000u);
+    if (f->has_inf && e == eall) {
+        if (m != 0) return or_bits_f32(0x7FC00000u);
+        v = INFINITY;
+    } else if (e == 0) {
+        v = ldexp((double)m, 1 - f->bias - f->mbits);
+    } else {
+        v = ldexp(1.0 + ldexp((double)m, -f->mbits), e - f->bias);
+    }
+    return (float)(s ? -v : v);   /* exact: at most 4 significant bits */
+}
+
+/* Round |a| (finite, >= 0) to the nearest value of format f with an
+ * unbounded exponent range above, ties to even.  The spacing of f's values in
+ * the binade of a is 2^(lead - mbits), lead = max(floor(log2 a), 1 - bias);
+ * a / spacing is exact in double and rint() rounds it half-to-even. */
+static double or_round_rne(double a, const or_format *f)
+{
+    int emin = 1 - f->bias;
+    int lead = emin;
+    if (a > 0.0) {
+        int e;
+        frexp(a, &e);           /* a = fr * 2^e, fr in [0.5, 1) */
+        lead = e - 1;
+        if (lead < emin) lead = emin;
+    }
+    double q = ldexp(1.0, lead - f->mbits);
+    return rint(a / q) * q;
+}
+
+/* Bit fields of a representable magnitude r of format f (no sign). */
+static uint32_t or_fields(double r, const or_format *f)
+{
+    if (r == 0.0) return 0;
+    int emin = 1 - f->bias;
+    int e;
+    frexp(r, &e);
+    int lead = e - 1;
+    if (lead < emin)   /* subnormal: exponent field 0, M = r / 2^(emin-mbits) */
+        return (uint32_t)(r / ldexp(1.0, emin - f->mbits));
+    uint32_t M = (uint32_t)((r / ldexp(1.0, lead) - 1.0) * (double)(1 << f->mbits));
+    return ((uint32_t)(lead + f->bias) << f->mbits) | M;
+}
+
+/* FP8 code of x: round to nearest even, saturate finite overflow to +-max. */
+uint8_t oracle_fp8_encode(float x, int fmt)
+{
+    const or_format *f = &OR_FMT[fmt];
+    if (isnan(x)) return 0x7F;
+    int neg = signbit(x) != 0;
+    if (isinf(x)) return f->has_inf ? (neg ? 0xFC : 0x7C) : 0x7F;
+    double r = or_round_rne(fabs((double)x), f);
+    if (r > f->maxval) r = f->maxval;
+    uint32_t code = or_fields(r, f);
+    return (uint8_t)(neg ? (code | 0x80u) : code);
+}
+
+/* IEEE binary16 bits of x: round to nearest even; overflow gives infinity
+ * (a value that rounds above 65504 is out of range); NaN gives 0x7E00. */
+uint16_t oracle_f32_to_f16(float x)
+{
+    if (isnan(x)) return 0x7E00;
+    int neg = signbit(x) != 0;
+    uint32_t bits;
+    if (isinf(x)) {
+        bits = 0x7C00;
+    } else {
+        double r = or_round_rne(fabs((double)x), &OR_HALF);
+        bits = (r > OR_HALF.maxval) ? 0x7C00u : or_fields(r, &OR_HALF);
+    }
+    return (uint16_t)(neg ? (bits | 0x8000u) : bits);
+}
+
+/* Value of IEEE binary16 bits. */
+float oracle_f16_to_f32(uint16_t h)
+{
+    int s = h >> 15, e = (h >> 10) & 0x1F, m = h & 0x3FF;
+    double v;
+    if (e == 0x1F) {
+        if (m) return or_bits_f32(0x7FC00000u);
+        v = INFINITY;
+    } else if (e == 0) {
+        v = ldexp((double)m, -24);
+    } else {
+        v = ldexp(1.0 + ldexp((double)m, -10), e - 15);
+    }
+    return (float)(s ? -v : v);
+}
+
+/* bfloat16 is the upper half of a binary32 pattern. */
+float oracle_bf16_to_f32(uint16_t h) { return or_bits_f32((uint32_t)h << 16); }
+
+/* ------------------------------------------------------------ amax, scale */
+
+/* Running amax with NaN above +inf above every finite magnitude. */
+typedef struct { int nan; int inf; float fin; } or_amax;
+
+static void or_amax_add(or_amax *a, float x)
+{
+    if (isnan(x)) a->nan = 1;
+    else if (isinf(x)) a->inf = 1;
+    else if (fabsf(x) > a->fin) a->fin = fabsf(x);
+}
+
+static float or_amax_value(const or_amax *a)
+{
+    if (a->nan) return or_bits_f32(0x7FC00000u);
+    if (a->inf) return INFINITY;
+    return a->fin;
+}
+
+/* Just-in-time per-tensor scale fp8_max / amax, one fp32 division; 1.0 when
+ * amax is zero or not finite, or when the quotient is not finite. */
+float oracle_scale_from_amax(float amax, int fmt)
+{
+    if (!(amax > 0.0f) || !isfinite(amax)) return 1.0f;
+    float q = (float)OR_FMT[fmt].maxval / amax;
+    if (!isfinite(q)) return 1.0f;
+    return q;
+}
+
+static float or_load(const void *src, int dtype, int64_t i)
+{
+    switch (dtype) {
+    case OR_F32: return ((const float *)src)[i];
+    case OR_BF16: return oracle_bf16_to_f32(((const uint16_t *)src)[i]);
+    default: return oracle_f16_to_f32(((const uint16_t *)src)[i]);
+    }
+}
+
+/* ------------------------------------------------------------------- cast */
+
+/* Scaled FP8 cast of one tensor (weight gradients from wider types to FP8,
+ * MS-AMP O1): amax over the tensor, scale = fp8_max / amax, then each element
+ * is multiplied by the scale in fp32 and encoded.  Returns 0, or -1 on a bad
+ * argument. */
+int oracle_cast_scaled(const void *src, int dtype, int64_t numel, int fmt,
+                       uint8_t *codes, float *amax_out, float *scale_out)
+{
+    if (numel < 0 || fmt < 0 || fmt > 1 || dtype < 0 || dtype > 2) return -1;
+    or_amax a = {0, 0, 0.0f};
+    for (int64_t i = 0; i < numel; ++i) or_amax_add(&a, or_load(src, dtype, i));
+    float amax = or_amax_value(&a);
+    float scale = oracle_scale_from_amax(amax, fmt);
+    for (int64_t i = 0; i < numel; ++i) {
+        float x = or_load(src, dtype, i);
+        if (!isfinite(x)) { codes[i] = oracle_fp8_encode(x, fmt); continue; }
+        float t = x * scale;
+        codes[i] = oracle_fp8_encode(t, fmt);
+    }
+    *amax_out = amax;
+    *scale_out = scale;
+    return 0;
+}
+
+/* ------------------------------------------------------------------- step */
+
+typedef struct {
+    int64_t numel;
+    const uint8_t *g;      /* gradient codes */
+    float g_scale;         /* scale the gradient codes were encoded with */
+    int g_fmt;             /* OR_E4M3 or OR_E5M2 */
+    uint8_t *m;            /* first moment, E4M3 codes (in/out) */
+    float *m_scale;        /* its scale (in/out) */
+    uint16_t *v;           /* second moment, FP16 bits (in/out) */
+    uint16_t *w;           /* O2: FP16 weight; O3: FP16 master (in/out) */
+    uint8_t *w8;           /* O3 only: E4M3 weight copy (out), else NULL */
+    float *w8_scale;       /* O3 only: its scale (out) */
+    float *w8_amax;        /* O3 only: amax of the FP16 master (out) */
+} oracle_param;
+
+/* Per-call scalars, computed on the host in double and rounded to float. */
+typedef struct {
+    float bc1, bc2, sbc2, omb1, omb2, decay;
+} or_scalars;
+
+static or_scalars or_make_scalars(float lr, float beta1, float beta2,
+                                  float wd, int64_t step)
+{
+    or_scalars s;
+    double bc1 = 1.0 - pow((double)beta1, (double)step);
+    double bc2 = 1.0 - pow((double)beta2, (double)step);
+    s.bc1 = (float)bc1;
+    s.bc2 = (float)bc2;
+    s.sbc2 = (float)sqrt(bc2);
+    s.omb1 = 1.0f - beta1;
+    s.omb2 = 1.0f - beta2;
+    s.decay = 1.0f - lr * wd;
+    return s;
+}
+
+/* Unscaled gradient: dequantize (code value times 1/g_scale), then multiply by
+ * the GradScaler's inverse loss scale. */
+static float or_grad(const oracle_param *p, float ginv, float ils, int64_t i)
+{
+    float g = oracle_fp8_decode(p->g[i], p->g_fmt) * ginv;
+    return g * ils;
+}
+
+/* New first moment in fp32: beta1 * m_prev + (1 - beta1) * g. */
+static float or_m_new(const oracle_param *p, float minv, float g, float beta1,
+                      const or_scalars *s, int64_t i)
+{
+    float mp = oracle_fp8_decode(p->m[i], OR_E4M3) * minv;
+    float a = beta1 * mp;
+    float b = s->omb1 * g;
+    return a + b;
+}
+
+/* One multi-tensor AdamW step with FP8 first moment and FP16 second moment.
+ * Returns 1 when found_inf (nothing written), 0 after an update, -1 on a bad
+ * argument. */
+int oracle_adamw_step(const oracle_param *p, int n, float lr, float beta1,
+                      float beta2, float eps, float wd, int64_t step,
+                      float inv_loss_scale)
+{
+    if (n < 0 || step < 1) return -1;
+    or_scalars s = or_make_scalars(lr, beta1, beta2, wd, step);
+
+    /* GradScaler check over every tensor before any state changes. */
+    for (int t = 0; t < n; ++t) {
+        float ginv = 1.0f / p[t].g_scale;
+        for (int64_t i = 0; i < p[t].numel; ++i)
+            if (!isfinite(or_grad(&p[t], ginv, inv_loss_scale, i))) return 1;
+    }
+
+    for (int t = 0; t < n; ++t) {
+        const oracle_param *q = &p[t];
+        float ginv = 1.0f / q->g_scale;
+        float minv = 1.0f / *q->m_scale;
+
+        /* amax of this step's fp32 first moment -> its new scale. */
+        or_amax am = {0, 0, 0.0f};
+        for (int64_t i = 0; i < q->numel; ++i) {
+            float g = or_grad(q, ginv, inv_loss_scale, i);
+            or_amax_add(&am, or_m_new(q, minv, g, beta1, &s, i));
+        }
+        float m_scale_new = oracle_scale_from_amax(or_amax_value(&am), OR_E4M3);
+
+        or_amax aw = {0, 0, 0.0f};
+        for (int64_t i = 0; i < q->numel; ++i) {
+            float g = or_grad(q, ginv, inv_loss_scale, i);
+            float m = or_m_new(q, minv, g, beta1, &s, i);
+            float vp = oracle_f16_to_f32(q->v[i]);
+            float wp = oracle_f16_to_f32(q->w[i]);
+            float gg = g * g;
+            float v = beta2 * vp + s.omb2 * gg;
+            float denom = sqrtf(v) / s.sbc2 + eps;
+            float upd = (m / s.bc1) / denom;
+            float w = wp * s.decay - lr * upd;
+            q->m[i] = oracle_fp8_encode(m * m_scale_new, OR_E4M3);
+            q->v[i] = oracle_f32_to_f16(v);
+            q->w[i] = oracle_f32_to_f16(w);
+            if (q->w8) or_amax_add(&aw, oracle_f16_to_f32(q->w[i]));
+        }
+        *q->m_scale = m_scale_new;
+
+        /* O3: FP8 weight copy encoded from the FP16 master. */
+        if (q->w8) {
+            float amax_w = or_amax_value(&aw);
+            float w8_scale = oracle_scale_from_amax(amax_w, OR_E4M3);
+            for (int64_t i = 0; i < q->numel; ++i)
+                q->w8[i] = oracle_fp8_encode(oracle_f16_to_f32(q->w[i]) * w8_scale,
+                                             OR_E4M3);
+            *q->w8_scale = w8_scale;
+            *q->w8_amax = amax_w;
+        }
+    }
+    return 0;
+}
+
+/* Optimizer-state bytes per parameter for a level of the MS-AMP table:
+ * first moment + second moment.  FP32+FP32 for FP16 AMP and O1 (level 0, 1),
+ * FP8+FP16 for O2 and O3 (level 2, 3); -1 for another level. */
+int oracle_state_bytes(int level)
+{
+    switch (level) {
+    case 0: case 1: return (int)(sizeof(float) + sizeof(float));
+    case 2: case 3: return (int)(sizeof(uint8_t) + sizeof(uint16_t));
+    default: return -1;
+    }
+}
+
+/* ------------------------------------------------------ array entry points */
+
+/* Element-wise forms of the codecs above, for tests over many values. */
+void oracle_fp8_encode_array(const float *x, int64_t n, int fmt, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_fp8_encode(x[i], fmt);
+}
+
+void oracle_fp8_decode_array(const uint8_t *c, int64_t n, int fmt, float *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_fp8_decode(c[i], fmt);
+}
+
+void oracle_f32_to_f16_array(const float *x, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_f16(x[i]);
+}
+
+void oracle_f16_to_f32_array(const uint16_t *h, int64_t n, float *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f16_to_f32(h[i]);
+}

@@ -1,0 +1,234 @@
+"""Pins of the oracle's FP8-state AdamW step.
+
+* torch.optim.AdamW in float64 (a library routine) run from the dequantized
+  state: the oracle's stored FP16 v / w are within one FP16 ulp of it and its
+  E4M3 first moment within one code, across settings where eps, weight decay
+  and the bias corrections each move the result.
+* the closed form of the first bias-corrected step, and the beta1 = beta2 = 0
+  special case (a sign-like normalised step at every step).
+* the GradScaler check against torch's own non-finite-check-and-unscale.
+* the O3 weight copy, the empty tensor, and the 62.5% state footprint.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+E4M3, E5M2 = 0, 1
+F32 = 0
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def tdec(codes, fmt=E4M3):
+    dt = torch.float8_e4m3fn if fmt == E4M3 else torch.float8_e5m2
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(dt).double()
+
+
+def f16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.float16)).double()
+
+
+def f16_bits(x64):
+    return x64.numpy().astype(np.float16).view(np.uint16)
+
+
+def make_states(orc, sizes, rng, g_sigma=1e-2, m_sigma=1e-3, v_mag=1e-6,
+                o3=False, g_fmt=E4M3, fresh=False):
+    states = []
+    for n in sizes:
+        g, _, gs = orc.cast_scaled(
+            (rng.standard_normal(n) * g_sigma).astype(np.float32), F32, g_fmt)
+        if fresh:
+            m, ms = np.zeros(n, np.uint8), np.float32(1.0)
+            v = np.zeros(n, np.uint16)
+        else:
+            m, _, ms = orc.cast_scaled(
+                (rng.standard_normal(n) * m_sigma).astype(np.float32), F32, E4M3)
+            v = (np.abs(rng.standard_normal(n)) * v_mag).astype(np.float16).view(np.uint16)
+        w = (rng.standard_normal(n) * 0.02).astype(np.float16).view(np.uint16)
+        states.append(orc.StepState(g, gs, m, ms, v, w, g_fmt=g_fmt, o3=o3))
+    return states
+
+
+def torch_adamw_f64(st, lr, b1, b2, eps, wd, step, ils):
+    """One torch.optim.AdamW step in float64 from the dequantized state."""
+    p = torch.nn.Parameter(f16(st.w).clone())
+    p.grad = tdec(st.g, st.g_fmt) / float(st.g_scale) * ils
+    opt = torch.optim.AdamW([p], lr=lr, betas=(b1, b2), eps=eps,
+                            weight_decay=wd, foreach=False)
+    opt.state[p] = {
+        "step": torch.tensor(float(step - 1)),
+        "exp_avg": tdec(st.m) / float(st.m_scale[0]),
+        "exp_avg_sq": f16(st.v).clone(),
+    }
+    opt.step()
+    s = opt.state[p]
+    return p.detach(), s["exp_avg"], s["exp_avg_sq"]
+
+
+def within_one_f16_ulp(bits, x64, min_exact):
+    rne = f16_bits(x64).astype(np.int32)
+    got = bits.astype(np.int32)
+    d = np.abs(got - rne)
+    # same-sign fp16 patterns are ordered, so a bit difference of 1 is one ulp
+    same_sign = (got >> 15) == (rne >> 15)
+    ok = (d <= 1) & (same_sign | (x64.abs().numpy() < 6e-8))
+    assert ok.all(), (np.flatnonzero(~ok)[:5], got[~ok][:5], rne[~ok][:5])
+    assert (d == 0).mean() >= min_exact
+
+
+SETTINGS = [
+    # lr, beta1, beta2, eps, wd, step, inv_loss_scale
+    (1e-2, 0.9, 0.99, 1e-3, 0.1, 3, 1.0),       # eps comparable to sqrt(v)
+    (1e-3, 0.9, 0.999, 1e-8, 0.01, 1, 0.5),     # first step
+    (5e-3, 0.8, 0.95, 1e-6, 0.0, 10, 2.0 ** -10),
+    (1e-2, 0.0, 0.5, 1e-4, 0.5, 2, 1.0),
+]
+
+
+@pytest.mark.parametrize("setting", SETTINGS)
+@pytest.mark.parametrize("o3", [False, True])
+def test_step_matches_torch_adamw_float64(orc, setting, o3):
+    lr, b1, b2, eps, wd, step, ils = setting
+    rng = np.random.default_rng(hash((setting, o3)) % 2**32)
+    states = make_states(orc, [37, 64, 1000], rng, g_sigma=1e-2 / ils, o3=o3)
+    before = [s.copy() for s in states]
+    assert orc.adamw_step(states, lr, b1, b2, eps, wd, step, ils) == 0
+    for s0, s1 in zip(before, states):
+        w64, m64, v64 = torch_adamw_f64(s0, lr, b1, b2, eps, wd, step, ils)
+        within_one_f16_ulp(s1.v, v64, 0.99)
+        within_one_f16_ulp(s1.w, w64, 0.99)
+        # E4M3 first moment: scale from this step's amax, code within 1
+        amax64 = m64.abs().max().item()
+        assert abs(float(s1.m_scale[0]) - 448.0 / amax64) <= 4e-7 * 448.0 / amax64
+        ref = torch.from_numpy((m64.numpy() * float(s1.m_scale[0])).astype(np.float32))
+        ref_codes = ref.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        dcode = np.abs(s1.m.astype(np.int32) - ref_codes.astype(np.int32))
+        dcode = np.where((s1.m ^ ref_codes) & 0x80, 999, dcode)
+        ok = (dcode <= 1) | (np.abs(m64.numpy()) * float(s1.m_scale[0]) < 2.0 ** -9)
+        assert ok.all()
+        if o3:
+            master = s1.w.view(np.float16).astype(np.float32)
+            assert s1.w8_amax[0] == np.abs(master).max()
+            assert s1.w8_scale[0] == np.float32(448.0) / s1.w8_amax[0]
+            ref8 = (torch.from_numpy(master) * torch.tensor(s1.w8_scale[0])).to(
+                torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(s1.w8, ref8)
+
+
+def test_first_step_closed_form(orc):
+    """m = v = 0, t = 1: m_hat = g and v_hat = g^2, so
+    w1 = w0 (1 - lr wd) - lr g / (|g| + eps) ~= w0 (1 - lr wd) - lr sign(g)."""
+    rng = np.random.default_rng(3)
+    lr, b1, b2, eps, wd = 1e-3, 0.9, 0.999, 1e-8, 0.01
+    states = make_states(orc, [4096], rng, g_sigma=1e-3, fresh=True)
+    s0 = states[0].copy()
+    assert orc.adamw_step(states, lr, b1, b2, eps, wd, 1, 1.0) == 0
+    g = (tdec(s0.g) / s0.g_scale).numpy()
+    w0 = f16(s0.w).numpy()
+    closed = w0 * (1 - lr * wd) - lr * g / (np.abs(g) + eps)
+    within_one_f16_ulp(states[0].w, torch.from_numpy(closed), 0.99)
+    big = np.abs(g) > 1e3 * eps                 # eps << |g|
+    assert big.mean() > 0.9
+    sign_step = w0 * (1 - lr * wd) - lr * np.sign(g)
+    got = f16(states[0].w).numpy()
+    ulp = np.spacing(np.abs(sign_step).astype(np.float16)).astype(np.float64)
+    assert np.all(np.abs(got - sign_step)[big] <= (ulp + 2e-3 * lr)[big])
+    # stored moments: v = (1 - beta2) g^2, m = (1 - beta1) g
+    within_one_f16_ulp(states[0].v, torch.from_numpy((1 - b2) * g * g), 0.99)
+    m_back = tdec(states[0].m).numpy() / states[0].m_scale[0]
+    assert np.allclose(m_back, (1 - b1) * g, rtol=2 ** -4, atol=1e-12)
+
+
+def test_zero_betas_give_normalised_step_every_step(orc):
+    """beta1 = beta2 = 0, wd = 0: both bias corrections are 1, m = g and
+    v = g^2, so each step moves w by lr g / (|g| + eps)."""
+    rng = np.random.default_rng(4)
+    lr, eps = 1e-2, 1e-6
+    states = make_states(orc, [333], rng, g_sigma=1e-3)
+    for t in range(1, 6):
+        new = make_states(orc, [333], rng, g_sigma=1e-3)[0]
+        states[0].g, states[0].g_scale = new.g, new.g_scale
+        s0 = states[0].copy()
+        assert orc.adamw_step(states, lr, 0.0, 0.0, eps, 0.0, t, 1.0) == 0
+        g = (tdec(s0.g) / s0.g_scale).numpy()
+        expect = f16(s0.w).numpy() - lr * g / (np.abs(g) + eps)
+        within_one_f16_ulp(states[0].w, torch.from_numpy(expect), 0.99)
+        within_one_f16_ulp(states[0].v, torch.from_numpy(g * g), 0.99)
+
+
+@pytest.mark.parametrize("case", ["nan_code", "overflow_after_unscale",
+                                  "e5m2_inf", "clean"])
+def test_found_inf_matches_torch_gradscaler_check(orc, case):
+    rng = np.random.default_rng(5)
+    g_fmt = E5M2 if case == "e5m2_inf" else E4M3
+    states = make_states(orc, [50, 70], rng, g_fmt=g_fmt)
+    ils = 1.0
+    if case == "nan_code":
+        states[1].g[13] = 0xFF
+    elif case == "e5m2_inf":
+        states[0].g[7] = 0x7C
+    elif case == "overflow_after_unscale":
+        states[0].g_scale = float(np.float32(1e-36))
+        ils = 1e10
+    before = [s.copy() for s in states]
+    found = orc.adamw_step(states, 1e-3, 0.9, 0.999, 1e-8, 0.01, 2, ils)
+    grads = [(tdec(s.g, s.g_fmt).float() * (np.float32(1.0) / np.float32(s.g_scale)))
+             for s in before]
+    flag = torch.zeros(1)
+    torch._amp_foreach_non_finite_check_and_unscale_(
+        grads, flag, torch.tensor(ils, dtype=torch.float32))
+    assert found == int(flag.item())
+    assert found == (0 if case == "clean" else 1)
+    if found:
+        for a, b in zip(before, states):
+            for k in ("m", "m_scale", "v", "w"):
+                assert np.array_equal(getattr(a, k), getattr(b, k))
+
+
+def test_empty_and_zero_tensors(orc):
+    rng = np.random.default_rng(6)
+    states = make_states(orc, [0, 16, 5], rng, fresh=True)
+    states[2].g[:] = 0
+    states[2].g_scale = 1.0
+    w_before = states[2].w.copy()
+    assert orc.adamw_step(states, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0) == 0
+    assert states[0].m_scale[0] == 1.0          # empty: amax 0 -> scale 1
+    assert states[2].m_scale[0] == 1.0          # zero moment -> scale 1
+    assert not states[2].m.any() and not states[2].v.any()
+    assert np.array_equal(states[2].w, w_before)   # wd 0, zero update
+
+
+def test_bad_arguments(orc):
+    rng = np.random.default_rng(8)
+    states = make_states(orc, [4], rng)
+    with pytest.raises(ValueError):
+        orc.adamw_step(states, 1e-3, 0.9, 0.999, 1e-8, 0.0, 0, 1.0)
+
+
+def read_levels():
+    rows, saving = {}, None
+    for line in open(os.path.join(GOLDEN, "optimization_levels.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = line.split()
+        if f[0] == "saving_O2_percent":
+            saving = float(f[1])
+        else:
+            rows[f[0]] = f[1:]
+    return rows, saving
+
+
+def test_state_footprint_is_the_published_saving(orc):
+    rows, saving = read_levels()
+    width = {"FP8": 1, "FP16": 2, "FP32": 4}
+    for lvl, name in ((0, "FP16_AMP"), (1, "MSAMP_O1"), (2, "MSAMP_O2"),
+                      (3, "MSAMP_O3")):
+        a, b = rows[name][5].split("+")
+        assert orc.state_bytes(lvl) == width[a] + width[b]
+    # the oracle's own state arrays: uint8 first moment, uint16 second moment
+    st = make_states(orc, [10], np.random.default_rng(0))[0]
+    assert st.m.itemsize + st.v.itemsize == orc.state_bytes(2) == 3
+    assert 100.0 * (1 - orc.state_bytes(2) / orc.state_bytes(0)) == saving
