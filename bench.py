@@ -1,0 +1,396 @@
+#!/usr/bin/env python
+"""Benchmark of the FP8 mixed-precision optimizer hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic gradients:
+``fp8_cast_scaled`` of the BF16 gradient list to E4M3 (per-tensor
+just-in-time scale), then ``fp8_adamw_step`` (E4M3 first moment, FP16 second
+moment, FP16 weights, GradScaler inf/NaN check).  Default workload: the
+6.7B-parameter long-tail list (32 layers, d 4096, ffn 16384, vocab 50304, plus
+200 tiny tensors and one all-zero tensor; 589 tensors, 6,658,707,493 params).
+
+Prints one JSON line.  ``value`` is whole-job Gparams/s with inputs resident
+in HBM (CUDA events on the launching stream); ``e2e`` is the same metric when
+every step also copies its gradients from pinned host memory and reads
+found_inf back; ``roofline`` covers the dominant kernel (the fused AdamW
+update), timed live with the library's per-kernel events; ``cpu_baseline`` is
+the scalar C oracle on a bounded sample of the same workload.
+
+``--impl reference`` times the oracle (the plain CPU implementation) instead.
+Under torchrun each rank steps its own copy of the workload (independent
+problems, weak scaling, no data-path collective); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("FP8-state AdamW step Gparams/s and HBM GB/s (% of GB300 peak); "
+          "FP8 cast GB/s")
+UNIT = "Gparams/s"
+# algorithmic HBM bytes per parameter of one step (BF16 gradients in):
+#   cast: amax read 2 + encode read 2 / write 1 = 5
+#   O2 step: pass 1 reads g, m = 2; update reads g, m, v, w = 6, writes 5
+#   O3 adds the weight copy: master read 2, codes write 1 = 3
+CAST_BYTES = 5
+STEP_BYTES = {"O2": 13, "O3": 16}
+UPDATE_BYTES = 11          # the dominant kernel, per parameter
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="o2_6p7b_tail",
+                   choices=["o2_6p7b_tail", "o3_1p3b", "o2_350m", "tiny"])
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_desc(wl):
+    return {
+        "workload": wl.name,
+        "tensors": len(wl.shapes),
+        "params": wl.n_params,
+        "level": wl.level,
+        "grad_dtype": str(wl.grad_dtype).replace("torch.", ""),
+        "grad_fmt": wl.grad_fmt,
+        "step": "fp8_cast_scaled (grads -> E4M3) + fp8_adamw_step",
+        "bytes_per_param": CAST_BYTES + STEP_BYTES[wl.level],
+        "l2": "inputs larger than L2 (no flush needed)" if wl.n_params > 1e8
+              else "inputs smaller than L2",
+    }
+
+
+# ------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def _once(self):
+        try:
+            out = subprocess.run(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev)], capture_output=True, text=True, timeout=20)
+            return out.stdout.strip().splitlines()
+        except Exception:
+            return []
+
+    def start(self):
+        self.lines += self._once()
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=10)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines += out.strip().splitlines()
+        self.lines += self._once()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ oracle leg
+
+def oracle_sample(wl, budget_s: float):
+    """Tensors of ``wl`` forming a bounded sample: small ones first (the tail,
+    norms, biases), then whole matrices while the estimated oracle time (about
+    5 M params/s for cast + step) stays within budget_s."""
+    order = sorted(range(len(wl.shapes)), key=lambda i: wl.numels[i])
+    limit = max(1, int(budget_s * 5e6))
+    chosen, total = [], 0
+    for i in order:
+        if total + wl.numels[i] > limit and chosen:
+            continue
+        chosen.append(i)
+        total += wl.numels[i]
+    return sorted(chosen), total
+
+
+def oracle_step_time(wl, idx, step):
+    """Wall time of one oracle cast + step over tensors idx (single thread)."""
+    import numpy as np
+    import torch
+    import oracle
+    fmt = oracle.FMT[wl.grad_fmt]
+    states = []
+    grads = []
+    for i in idx:
+        g = wl.grad(i, step).contiguous()
+        grads.append(g)
+        w = wl.weight(i).contiguous().view(torch.int16).numpy().view(np.uint16)
+        n = wl.numels[i]
+        states.append(oracle.StepState(np.zeros(n, np.uint8), 1.0,
+                                       np.zeros(n, np.uint8), 1.0,
+                                       np.zeros(n, np.uint16), w, g_fmt=fmt,
+                                       o3=wl.level == "O3"))
+    dt = {torch.float32: oracle.F32, torch.bfloat16: oracle.BF16,
+          torch.float16: oracle.F16}[wl.grad_dtype]
+    srcs = [g.numpy() if g.dtype == torch.float32 else
+            g.view(torch.int16).numpy().view(np.uint16) for g in grads]
+    t0 = time.perf_counter()
+    for s, src in zip(states, srcs):
+        c, _, sc = oracle.cast_scaled(src, dt, fmt)
+        s.g, s.g_scale = c, float(sc)
+    oracle.adamw_step(states, wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, step,
+                      wl.inv_loss_scale)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, budget_s: float):
+    idx, total = oracle_sample(wl, budget_s)
+    secs = oracle_step_time(wl, idx, 1)
+    return {"value": total / secs / 1e9, "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"1 cast+step over {len(idx)} of {len(wl.shapes)} tensors "
+                      f"({total} params, {secs:.1f} s, single thread)"}
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    per_step = max(1.0, 90.0 / max(1, args.steps + args.warmup))
+    idx, total = oracle_sample(wl, per_step)
+    for w in range(args.warmup):
+        oracle_step_time(wl, idx, w + 1)
+    times = [oracle_step_time(wl, idx, args.warmup + k + 1) for k in range(args.steps)]
+    secs = sum(times)
+    value = total * args.steps / secs / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_desc(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step: cast+step over {len(idx)} of "
+                                   f"{len(wl.shapes)} tensors ({total} params)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def build_state(wl, device):
+    import torch
+    import bit_optimizer_gb300 as bo
+    numels = wl.numels
+    params = bo.arena_views(numels, torch.float16, device)
+    for i, p in enumerate(params):
+        p.copy_(wl.weight(i, device))
+    grads, flat = bo.arena_views(numels, wl.grad_dtype, device, return_base=True)
+    for i, g in enumerate(grads):
+        g.copy_(wl.grad(i, 1, device))
+    torch.cuda.synchronize()
+    opt = bo.Fp8AdamW(params, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
+                      weight_decay=wl.wd, level=wl.level, grad_fmt=wl.grad_fmt)
+    return params, grads, flat, opt
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+    import bit_optimizer_gb300 as bo
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    params, grads, flat, opt = build_state(wl, device)
+    stream = torch.cuda.current_stream()
+    flag = torch.zeros(1, dtype=torch.int32, device=device)
+    ils = wl.inv_loss_scale
+
+    for _ in range(args.warmup):
+        opt.step(grads, ils, found_inf_dev=flag, sync=False)
+    barrier()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    bo.timing_enable(True)
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        opt.step(grads, ils, found_inf_dev=flag, sync=False)
+    t1.record(stream)
+    barrier()
+    bo.timing_enable(False)
+    sampler.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    if int(flag.item()) != 0:
+        raise RuntimeError("found_inf set on a finite workload")
+    kern = {k: bo.timing_read(k) for k in bo.KERNELS}
+    launches = sum(n for n, _ in kern.values())
+
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    n_params = wl.n_params
+    value = world * n_params / (ms * 1e-3) / 1e9
+    bytes_step = (CAST_BYTES + STEP_BYTES[wl.level]) * n_params
+    peak, peak_kind = measured_peak()
+    upd_n, upd_ms = kern["step_update"]
+    upd_avg_ms = upd_ms / max(upd_n, 1)
+    achieved = UPDATE_BYTES * n_params / (upd_avg_ms * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        # Host buffers: every step copies its gradients from pinned host
+        # memory, runs the cast and the step, and reads found_inf back.
+        # The gradient arena is one flat buffer, so one copy moves a step's
+        # gradients (alignment padding included).
+        host = torch.empty(flat.shape, dtype=flat.dtype, pin_memory=True)
+        host.copy_(flat)
+        h2d = host.numel() * host.element_size()
+        for _ in range(2):
+            flat.copy_(host, non_blocking=True)
+            opt.step(grads, ils, sync=True)
+        barrier()
+        k = max(1, args.e2e_steps)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k):
+            flat.copy_(host, non_blocking=True)
+            if opt.step(grads, ils, sync=True) != 0:
+                raise RuntimeError("found_inf set on a finite workload")
+        e1.record(stream)
+        barrier()
+        ems = e0.elapsed_time(e1) / k
+        if world > 1:
+            t = torch.tensor([ems], dtype=torch.float64, device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * n_params / (ems * 1e-3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4,
+               "ms_per_step": ems, "steps": k}
+        del host
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic", "config": workload_desc(wl),
+            "hbm_gbs": world * bytes_step / (ms * 1e-3) / 1e9,
+            "hbm_frac_of_peak": bytes_step / (ms * 1e-3) / 1e9 / peak,
+            "roofline": {"bound": "hbm", "kernel": "step_update",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_source": f"{peak_kind} hbm_gbs",
+                         "bytes_per_launch": UPDATE_BYTES * n_params,
+                         "avg_launch_ms": upd_avg_ms},
+            "kernels_ms_per_launch": {k: (v[1] / v[0] if v[0] else None)
+                                      for k, v in kern.items()},
+            "gpu_launches": launches,
+            "clocks": sampler.summary(),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    import dataclasses
+    import synth
+    wl = synth.WORKLOADS[args.workload]()
+    # a timed step must be a full update: a workload that seeds an inf (the
+    # GradScaler skip case) is timed with that element cleared
+    wl = dataclasses.replace(wl, inf_site=None)
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

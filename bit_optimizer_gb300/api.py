@@ -1,0 +1,319 @@
+"""PyTorch-facing binding of libfp8opt.
+
+PyTorch supplies device memory and streams only; every step of the cast and
+the optimizer runs in the library's CUDA kernels, reached through the C ABI.
+
+* ``fp8_cast_scaled`` / ``CastPlan``: per-tensor just-in-time scaled FP8 cast
+  of a tensor list (MS-AMP O1 gradients in FP8).
+* ``fp8_adamw_step`` / ``AdamWPlan``: one multi-tensor AdamW step with E4M3
+  first moment and FP16 second moment (MS-AMP O2), FP16 master plus E4M3
+  weight copy for O3, and the GradScaler inf/NaN skip.
+* ``Fp8AdamW``: an optimizer object that owns the low-bit state in flat,
+  256-byte-aligned arenas and runs cast + step for a list of FP16 weights,
+  with ``state_dict`` / ``load_state_dict`` for checkpoint and resume.
+
+A "plan" marshals its tensor list into the C records once; calling it again
+passes the same records, so a repeated call costs one ctypes call and, inside
+the library, no table upload.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+from typing import Dict, List, Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import BF16, E4M3, E5M2, F16, F32, CastItem, Param, check, load
+
+FMTS = {"e4m3": E4M3, "e5m2": E5M2, E4M3: E4M3, E5M2: E5M2}
+_DT = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
+
+__all__ = ["fp8_cast_scaled", "fp8_adamw_step", "CastPlan", "AdamWPlan",
+           "Fp8AdamW", "arena_views", "FMTS"]
+
+
+def _fmt(f) -> int:
+    try:
+        return FMTS[f]
+    except KeyError:
+        raise ValueError(f"unknown FP8 format {f!r}") from None
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> Optional[int]:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream or None
+
+
+def _cuda(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _slot_ptr(t: torch.Tensor, i: int, name: str) -> int:
+    """Address of element i of a float32 vector (one scale/amax per tensor)."""
+    _cuda(t, name)
+    if t.dtype != torch.float32 or t.numel() <= i:
+        raise ValueError(f"{name} must be float32 with one element per tensor")
+    return t.data_ptr() + 4 * i
+
+
+def arena_views(numels: Sequence[int], dtype: torch.dtype, device,
+                align_bytes: int = 256, fill=None, return_base=False):
+    """One flat allocation cut into per-tensor views, each starting on an
+    ``align_bytes`` boundary (the vector path wants 16-byte starts).  With
+    ``return_base`` also returns the flat buffer."""
+    isz = torch.empty((), dtype=dtype).element_size()
+    step = max(1, align_bytes // isz)
+    offs, total = [], 0
+    for n in numels:
+        offs.append(total)
+        total += (n + step - 1) // step * step
+    buf = (torch.empty(max(total, 1), dtype=dtype, device=device)
+           if fill is None else
+           torch.full((max(total, 1),), fill, dtype=dtype, device=device))
+    views = [buf[o:o + n] for o, n in zip(offs, numels)]
+    return (views, buf) if return_base else views
+
+
+# ------------------------------------------------------------------- cast
+
+class CastPlan:
+    """A marshalled ``fp8_cast_scaled`` over fixed buffers.
+
+    srcs: contiguous CUDA tensors (float32, bfloat16 or float16);
+    codes: uint8 CUDA tensors with the same numels; amax, scale: float32 CUDA
+    vectors with one entry per tensor.
+    """
+
+    def __init__(self, srcs, codes, amax, scale, fmt="e4m3"):
+        n = len(srcs)
+        if len(codes) != n:
+            raise ValueError("srcs and codes differ in length")
+        self.fmt = _fmt(fmt)
+        self.n = n
+        self._keep = (list(srcs), list(codes), amax, scale)
+        self._items = (CastItem * max(n, 1))()
+        for i, (s, c) in enumerate(zip(srcs, codes)):
+            _cuda(s, "src")
+            _cuda(c, "codes")
+            if s.dtype not in _DT:
+                raise TypeError(f"src {i}: unsupported dtype {s.dtype}")
+            if c.dtype != torch.uint8 or c.numel() != s.numel():
+                raise ValueError(f"codes {i} must be uint8 with the src numel")
+            it = self._items[i]
+            it.src, it.numel, it.dtype = s.data_ptr(), s.numel(), _DT[s.dtype]
+            it.codes = c.data_ptr()
+            it.amax = _slot_ptr(amax, i, "amax")
+            it.scale = _slot_ptr(scale, i, "scale")
+
+    def __call__(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+        check(load().fp8_cast_scaled(self._items, self.n, self.fmt,
+                                     _stream_ptr(stream)))
+
+
+def fp8_cast_scaled(srcs: Sequence[torch.Tensor], fmt="e4m3", codes=None,
+                    amax=None, scale=None, stream=None):
+    """Scaled FP8 cast of each tensor: returns (codes list, amax, scale).
+
+    amax[i] = max |srcs[i]|; scale[i] = fp8_max / amax[i] (1.0 for a zero or
+    non-finite amax); codes[i] = RNE-saturating FP8 encode of srcs[i] * scale.
+    """
+    srcs = list(srcs)
+    dev = srcs[0].device if srcs else torch.device("cuda")
+    if codes is None:
+        codes = [torch.empty(s.numel(), dtype=torch.uint8, device=dev) for s in srcs]
+    if amax is None:
+        amax = torch.empty(max(len(srcs), 1), dtype=torch.float32, device=dev)
+    if scale is None:
+        scale = torch.empty(max(len(srcs), 1), dtype=torch.float32, device=dev)
+    CastPlan(srcs, codes, amax, scale, fmt)(stream)
+    return codes, amax, scale
+
+
+# ------------------------------------------------------------------- step
+
+class AdamWPlan:
+    """A marshalled ``fp8_adamw_step`` over fixed state buffers.
+
+    g: uint8 gradient codes per tensor; g_scale: float32 vector (n);
+    m: uint8 E4M3 first moments; m_scale: float32 vector (n); v: float16
+    second moments; w: float16 weights (O2) or masters (O3).  O3 when w8 (uint8
+    per tensor), w8_scale and w8_amax (float32 vectors) are given.
+    """
+
+    def __init__(self, g, g_scale, m, m_scale, v, w, w8=None, w8_scale=None,
+                 w8_amax=None, g_fmt="e4m3"):
+        n = len(g)
+        if not (len(m) == len(v) == len(w) == n):
+            raise ValueError("g, m, v and w differ in length")
+        o3 = w8 is not None
+        if o3 and (w8_scale is None or w8_amax is None or len(w8) != n):
+            raise ValueError("O3 needs w8, w8_scale and w8_amax")
+        self.n = n
+        self.o3 = o3
+        self._keep = (list(g), g_scale, list(m), m_scale, list(v), list(w),
+                      None if w8 is None else list(w8), w8_scale, w8_amax)
+        fmts = g_fmt if isinstance(g_fmt, (list, tuple)) else [g_fmt] * n
+        self._params = (Param * max(n, 1))()
+        for i in range(n):
+            ne = w[i].numel()
+            for name, t, dt in (("g", g[i], torch.uint8), ("m", m[i], torch.uint8),
+                                ("v", v[i], torch.float16),
+                                ("w", w[i], torch.float16)):
+                _cuda(t, name)
+                if t.dtype != dt or t.numel() != ne:
+                    raise ValueError(f"{name}[{i}] must be {dt} with numel {ne}")
+            p = self._params[i]
+            p.numel = ne
+            p.g, p.g_fmt = g[i].data_ptr(), _fmt(fmts[i])
+            p.g_scale = _slot_ptr(g_scale, i, "g_scale")
+            p.m, p.m_scale = m[i].data_ptr(), _slot_ptr(m_scale, i, "m_scale")
+            p.v, p.w = v[i].data_ptr(), w[i].data_ptr()
+            if o3:
+                _cuda(w8[i], "w8")
+                if w8[i].dtype != torch.uint8 or w8[i].numel() != ne:
+                    raise ValueError(f"w8[{i}] must be uint8 with numel {ne}")
+                p.w8 = w8[i].data_ptr()
+                p.w8_scale = _slot_ptr(w8_scale, i, "w8_scale")
+                p.w8_amax = _slot_ptr(w8_amax, i, "w8_amax")
+        self._found = C.c_int(0)
+
+    def __call__(self, lr, beta1, beta2, eps, wd, step, inv_loss_scale=1.0,
+                 found_inf_dev: Optional[torch.Tensor] = None, sync=True,
+                 stream=None) -> Optional[int]:
+        """Runs one step.  sync=True returns found_inf (0/1) after waiting
+        for the stream; sync=False returns None without waiting (found_inf is
+        then only in found_inf_dev, a uint32/int32 CUDA tensor, if given)."""
+        fdev = None
+        if found_inf_dev is not None:
+            _cuda(found_inf_dev, "found_inf_dev")
+            fdev = found_inf_dev.data_ptr()
+        fptr = C.byref(self._found) if sync else None
+        check(load().fp8_adamw_step(self._params, self.n, lr, beta1, beta2, eps,
+                                    wd, int(step), inv_loss_scale, fptr, fdev,
+                                    _stream_ptr(stream)))
+        return self._found.value if sync else None
+
+
+def fp8_adamw_step(g, g_scale, m, m_scale, v, w, lr, beta1, beta2, eps, wd,
+                   step, inv_loss_scale=1.0, w8=None, w8_scale=None,
+                   w8_amax=None, g_fmt="e4m3", found_inf_dev=None, sync=True,
+                   stream=None):
+    """One FP8-state AdamW step over a tensor list; returns found_inf."""
+    plan = AdamWPlan(g, g_scale, m, m_scale, v, w, w8, w8_scale, w8_amax, g_fmt)
+    return plan(lr, beta1, beta2, eps, wd, step, inv_loss_scale, found_inf_dev,
+                sync, stream)
+
+
+# -------------------------------------------------------------- optimizer
+
+class Fp8AdamW:
+    """AdamW over a list of FP16 weights with MS-AMP low-bit state.
+
+    level "O2": FP16 weights updated in place; E4M3 first moment, FP16 second
+    moment.  level "O3": the FP16 tensors are master weights, and after each
+    step ``w8`` / ``w8_scale`` hold their E4M3 copies for forward/backward.
+
+    ``step(grads, inv_loss_scale)`` casts the gradients to FP8 (per-tensor
+    just-in-time scale) and runs the update; it returns found_inf and, like a
+    GradScaler step, leaves every state tensor and the step count unchanged
+    when found_inf is 1.
+    """
+
+    def __init__(self, params: Sequence[torch.Tensor], lr=1e-3,
+                 betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01, level="O2",
+                 grad_fmt="e4m3"):
+        if level not in ("O2", "O3"):
+            raise ValueError("level must be 'O2' or 'O3'")
+        self.params = list(params)
+        for i, p in enumerate(self.params):
+            _cuda(p, f"params[{i}]")
+            if p.dtype != torch.float16:
+                raise TypeError("params must be float16")
+        self.lr, (self.beta1, self.beta2) = lr, betas
+        self.eps, self.wd = eps, weight_decay
+        self.level, self.grad_fmt = level, grad_fmt
+        self.step_count = 0
+        n = len(self.params)
+        dev = self.params[0].device if n else torch.device("cuda")
+        numels = [p.numel() for p in self.params]
+        self.g_codes = arena_views(numels, torch.uint8, dev)
+        self.m = arena_views(numels, torch.uint8, dev, fill=0)
+        self.v = arena_views(numels, torch.float16, dev, fill=0)
+        self.g_amax = torch.zeros(max(n, 1), dtype=torch.float32, device=dev)
+        self.g_scale = torch.ones(max(n, 1), dtype=torch.float32, device=dev)
+        self.m_scale = torch.ones(max(n, 1), dtype=torch.float32, device=dev)
+        w = [p.view(-1) for p in self.params]
+        if level == "O3":
+            self.w8 = arena_views(numels, torch.uint8, dev, fill=0)
+            self.w8_scale = torch.ones(max(n, 1), dtype=torch.float32, device=dev)
+            self.w8_amax = torch.zeros(max(n, 1), dtype=torch.float32, device=dev)
+        else:
+            self.w8 = self.w8_scale = self.w8_amax = None
+        self._plan = AdamWPlan(self.g_codes, self.g_scale, self.m, self.m_scale,
+                               self.v, w, self.w8, self.w8_scale, self.w8_amax,
+                               grad_fmt)
+        self._cast_key = None
+        self._cast = None
+
+    def _cast_plan(self, grads: Sequence[torch.Tensor]) -> CastPlan:
+        key = tuple((g.data_ptr(), g.numel(), g.dtype) for g in grads)
+        if key != self._cast_key:
+            flat = [g.view(-1) for g in grads]
+            self._cast = CastPlan(flat, self.g_codes, self.g_amax, self.g_scale,
+                                  self.grad_fmt)
+            self._cast_key = key
+        return self._cast
+
+    def step(self, grads: Sequence[torch.Tensor], inv_loss_scale=1.0,
+             found_inf_dev=None, sync=True, stream=None):
+        """Cast ``grads`` to FP8 and apply one AdamW step.  Returns found_inf
+        (sync=True) or None (sync=False; the step count then advances
+        unconditionally and the caller reads found_inf_dev)."""
+        if len(grads) != len(self.params):
+            raise ValueError("one gradient per parameter")
+        self._cast_plan(grads)(stream)
+        t = self.step_count + 1
+        found = self._plan(self.lr, self.beta1, self.beta2, self.eps, self.wd, t,
+                           inv_loss_scale, found_inf_dev, sync, stream)
+        if not sync or found == 0:
+            self.step_count = t
+        return found
+
+    def state_dict(self) -> Dict[str, object]:
+        d = {"step": self.step_count, "level": self.level,
+             "grad_fmt": self.grad_fmt,
+             "hparams": (self.lr, self.beta1, self.beta2, self.eps, self.wd),
+             "m": [t.clone() for t in self.m], "v": [t.clone() for t in self.v],
+             "m_scale": self.m_scale.clone()}
+        if self.level == "O3":
+            d["w8"] = [t.clone() for t in self.w8]
+            d["w8_scale"] = self.w8_scale.clone()
+            d["w8_amax"] = self.w8_amax.clone()
+        return d
+
+    def load_state_dict(self, d: Dict[str, object]) -> None:
+        if d["level"] != self.level or len(d["m"]) != len(self.m):
+            raise ValueError("state dict does not match this optimizer")
+        self.step_count = int(d["step"])
+        self.lr, self.beta1, self.beta2, self.eps, self.wd = d["hparams"]
+        for dst, src in zip(self.m, d["m"]):
+            dst.copy_(src)
+        for dst, src in zip(self.v, d["v"]):
+            dst.copy_(src)
+        self.m_scale.copy_(d["m_scale"])
+        if self.level == "O3":
+            for dst, src in zip(self.w8, d["w8"]):
+                dst.copy_(src)
+            self.w8_scale.copy_(d["w8_scale"])
+            self.w8_amax.copy_(d["w8_amax"])
+
+    @staticmethod
+    def state_bytes_per_param(level="O2") -> int:
+        """Optimizer-state bytes per parameter: 1 (E4M3 m) + 2 (FP16 v)."""
+        return 1 + 2

@@ -1,0 +1,274 @@
+// Scaled FP8 cast of a tensor list (MS-AMP O1: weight gradients kept in FP8).
+//
+// Two persistent kernels over the chunk table:
+//   cast_amax_kernel    per-tensor max |x| (on the fp32 bit patterns, so NaN
+//                       orders above +inf above every finite value), reduced
+//                       with warp max-reductions, a shared-memory CTA step,
+//                       and one 64-bit atomicMax per (chunk, tensor).
+//   cast_encode_kernel  scale = fp8_max / amax in each CTA's chunk prologue,
+//                       then code = RNE-saturating encode of x * scale.  It
+//                       walks the chunk table backwards, so the chunks the
+//                       amax pass read last are still in L2 when it starts.
+// Bytes per element: BF16/FP16 in: 2 (amax) + 2 + 1 (encode); FP32: 4 + 4 + 1.
+#include "fp8opt_internal.cuh"
+
+namespace fp8opt {
+
+namespace {
+
+constexpr int kAmaxGroups = 4;   // 8-element groups per thread per tile
+constexpr int kEncGroups = 2;
+
+// ---------------------------------------------------------------- amax pass
+
+// Max of |x| bit patterns over the four words of a uint4 of 16-bit values,
+// accumulated per 16-bit lane.
+__device__ __forceinline__ uint32_t vmax16x8(uint32_t acc, uint4 a) {
+  acc = __vmaxu2(acc, a.x & 0x7FFF7FFFu);
+  acc = __vmaxu2(acc, a.y & 0x7FFF7FFFu);
+  acc = __vmaxu2(acc, a.z & 0x7FFF7FFFu);
+  return __vmaxu2(acc, a.w & 0x7FFF7FFFu);
+}
+
+__device__ __forceinline__ uint32_t vmax32x4(uint32_t acc, uint4 a) {
+  acc = max(acc, a.x & 0x7FFFFFFFu);
+  acc = max(acc, a.y & 0x7FFFFFFFu);
+  acc = max(acc, a.z & 0x7FFFFFFFu);
+  return max(acc, a.w & 0x7FFFFFFFu);
+}
+
+// This thread's share of max |x| over [begin, end), as an fp32 bit pattern
+// (not yet NaN-canonical).  For 16-bit types the running maximum is kept per
+// 16-bit lane of a 32-bit word and widened at the end; the order of
+// non-negative bit patterns is the order of their values in all three types.
+template <int DT>
+__device__ uint32_t thread_amax(const void* src, int64_t begin, int64_t end,
+                                bool vec) {
+  constexpr int64_t kTile = (int64_t)kThreads * kGroup * kAmaxGroups;
+  const int tid = threadIdx.x;
+  uint32_t acc = 0;
+  for (int64_t base = begin; base < end; base += kTile) {
+    if (vec && base + kTile <= end) {
+      if (DT == kF32) {
+        const float* f = static_cast<const float*>(src);
+        uint4 a[kAmaxGroups][2];
+#pragma unroll
+        for (int k = 0; k < kAmaxGroups; ++k) {
+          const int64_t i0 = base + k * (kThreads * kGroup) + tid * kGroup;
+          a[k][0] = ld_keep4(f + i0);
+          a[k][1] = ld_keep4(f + i0 + 4);
+        }
+#pragma unroll
+        for (int k = 0; k < kAmaxGroups; ++k)
+          acc = vmax32x4(vmax32x4(acc, a[k][0]), a[k][1]);
+      } else {
+        const uint16_t* h = static_cast<const uint16_t*>(src);
+        uint4 a[kAmaxGroups];
+#pragma unroll
+        for (int k = 0; k < kAmaxGroups; ++k)
+          a[k] = ld_keep4(h + base + k * (kThreads * kGroup) + tid * kGroup);
+#pragma unroll
+        for (int k = 0; k < kAmaxGroups; ++k) acc = vmax16x8(acc, a[k]);
+      }
+    } else {
+#pragma unroll 1
+      for (int k = 0; k < kAmaxGroups; ++k) {
+        const int64_t i0 = base + k * (kThreads * kGroup) + tid * kGroup;
+        for (int j = 0; j < kGroup; ++j) {
+          const int64_t i = i0 + j;
+          if (i >= end) break;
+          if (DT == kF32) {
+            acc = max(acc, __float_as_uint(static_cast<const float*>(src)[i]) &
+                               0x7FFFFFFFu);
+          } else {
+            const uint32_t b = static_cast<const uint16_t*>(src)[i] & 0x7FFFu;
+            acc = __vmaxu2(acc, b);
+          }
+        }
+      }
+    }
+  }
+  if (DT == kF32) return acc;
+  const uint32_t h = max(acc & 0xFFFFu, acc >> 16);
+  if (DT == kBF16) return h << 16;
+  if (h > 0x7C00u) return 0x7FC00000u;                 // FP16 NaN
+  return __float_as_uint(h_to_f((uint16_t)h));          // exact widening
+}
+
+__global__ void __launch_bounds__(kThreads)
+cast_amax_kernel(const CastDesc* __restrict__ descs,
+                 const Chunk* __restrict__ chunks, uint32_t nchunks,
+                 unsigned long long* __restrict__ slots, uint32_t epoch) {
+  __shared__ uint32_t red[kThreads / 32];
+  for (uint32_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+    const Chunk ch = chunks[c];
+    const CastDesc d = descs[ch.tensor];
+    const int64_t begin = (int64_t)ch.index * kChunkElems;
+    const int64_t end = min(begin + kChunkElems, d.numel);
+    const bool vec = d.vec_ok != 0;
+    uint32_t mx;
+    if (d.dtype == kF32)
+      mx = thread_amax<kF32>(d.src, begin, end, vec);
+    else if (d.dtype == kBF16)
+      mx = thread_amax<kBF16>(d.src, begin, end, vec);
+    else
+      mx = thread_amax<kF16>(d.src, begin, end, vec);
+    mx = block_max_u32(mx, red);
+    if (threadIdx.x == 0 && mx != 0)
+      atomicMax(&slots[ch.tensor], slot_tag(epoch, canon_amax_bits(mx)));
+  }
+}
+
+// -------------------------------------------------------------- encode pass
+
+template <int DT>
+__device__ __forceinline__ void load8(const void* src, int64_t i0,
+                                      float (&x)[8]) {
+  if (DT == kF32) {
+    const float* f = static_cast<const float*>(src) + i0;
+    const uint4 a = ld_once4(f), b = ld_once4(f + 4);
+    x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+    x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+    x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+    x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
+  } else {
+    const uint4 a = ld_once4(static_cast<const uint16_t*>(src) + i0);
+    if (DT == kF16) {
+      h8_to_f(a, x);
+    } else {
+      const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[2 * j] = __uint_as_float(w[j] << 16);
+        x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+    }
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ float load1(const void* src, int64_t i) {
+  if (DT == kF32) return static_cast<const float*>(src)[i];
+  const uint16_t b = static_cast<const uint16_t*>(src)[i];
+  if (DT == kF16) return h_to_f(b);
+  return __uint_as_float((uint32_t)b << 16);
+}
+
+// Encode this thread's share of [begin, end).  CHECKED when the tensor holds a
+// non-finite element (its amax is not finite): those take the explicit
+// NaN / infinity codes; otherwise every product is finite.
+template <int DT, int FMT, bool CHECKED>
+__device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
+                              int64_t end, bool vec, float scale) {
+  constexpr int64_t kTile = (int64_t)kThreads * kGroup * kEncGroups;
+  const int tid = threadIdx.x;
+  for (int64_t base = begin; base < end; base += kTile) {
+    if (vec && base + kTile <= end) {
+      float x[kEncGroups][8];
+#pragma unroll
+      for (int k = 0; k < kEncGroups; ++k)
+        load8<DT>(src, base + k * (kThreads * kGroup) + tid * kGroup, x[k]);
+#pragma unroll
+      for (int k = 0; k < kEncGroups; ++k) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[k][j] = __fmul_rn(x[k][j], scale);
+        const int64_t i0 = base + k * (kThreads * kGroup) + tid * kGroup;
+        *reinterpret_cast<uint2*>(codes + i0) = enc8<FMT, CHECKED>(x[k]);
+      }
+    } else {
+#pragma unroll 1
+      for (int k = 0; k < kEncGroups; ++k) {
+        const int64_t i0 = base + k * (kThreads * kGroup) + tid * kGroup;
+        if (vec && i0 + kGroup <= end) {
+          float x[8];
+          load8<DT>(src, i0, x);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) x[j] = __fmul_rn(x[j], scale);
+          *reinterpret_cast<uint2*>(codes + i0) = enc8<FMT, CHECKED>(x);
+        } else {
+          for (int j = 0; j < kGroup; ++j) {
+            const int64_t i = i0 + j;
+            if (i >= end) break;
+            const float t = __fmul_rn(load1<DT>(src, i), scale);
+            codes[i] = (uint8_t)(CHECKED ? enc1_checked<FMT>(t)
+                                         : (enc2<FMT>(t, 0.0f) & 0xFFu));
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int DT, int FMT>
+__device__ __forceinline__ void encode_dispatch(const CastDesc& d,
+                                                int64_t begin, int64_t end,
+                                                float scale, bool checked) {
+  const bool vec = d.vec_ok != 0;
+  if (checked)
+    thread_encode<DT, FMT, true>(d.src, d.codes, begin, end, vec, scale);
+  else
+    thread_encode<DT, FMT, false>(d.src, d.codes, begin, end, vec, scale);
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+cast_encode_kernel(const CastDesc* __restrict__ descs,
+                   const Chunk* __restrict__ chunks, uint32_t nchunks,
+                   const unsigned long long* __restrict__ slots,
+                   uint32_t epoch) {
+  for (uint32_t r = blockIdx.x; r < nchunks; r += gridDim.x) {
+    const Chunk ch = chunks[nchunks - 1 - r];
+    const CastDesc d = descs[ch.tensor];
+    const uint32_t ab = slot_value(slots[ch.tensor], epoch);
+    const float scale = scale_from_amax_bits(ab, fp8_max_of<FMT>());
+    if (ch.index == 0 && threadIdx.x == 0) {
+      *d.amax_out = __uint_as_float(ab);
+      *d.scale_out = scale;
+    }
+    const int64_t begin = (int64_t)ch.index * kChunkElems;
+    const int64_t end = min(begin + kChunkElems, d.numel);
+    const bool checked = ab >= 0x7F800000u;
+    if (d.dtype == kF32)
+      encode_dispatch<kF32, FMT>(d, begin, end, scale, checked);
+    else if (d.dtype == kBF16)
+      encode_dispatch<kBF16, FMT>(d, begin, end, scale, checked);
+    else
+      encode_dispatch<kF16, FMT>(d, begin, end, scale, checked);
+  }
+}
+
+}  // namespace
+
+// Launches both passes on `stream`; grid is the persistent CTA count.
+cudaError_t launch_cast(const CastDesc* descs, const Chunk* chunks,
+                        uint32_t nchunks, unsigned long long* slots,
+                        uint32_t epoch, int fmt, int grid_amax,
+                        int grid_encode, cudaStream_t stream, LaunchMark mark) {
+  if (nchunks == 0) return cudaSuccess;
+  const uint32_t ga = grid_min((uint32_t)grid_amax, nchunks);
+  const uint32_t ge = grid_min((uint32_t)grid_encode, nchunks);
+  if (mark) mark(kCastAmaxK, 0, stream);
+  cast_amax_kernel<<<ga, kThreads, 0, stream>>>(descs, chunks, nchunks, slots,
+                                                epoch);
+  if (mark) mark(kCastAmaxK, 1, stream);
+  if (mark) mark(kCastEncodeK, 0, stream);
+  if (fmt == kE4M3)
+    cast_encode_kernel<kE4M3><<<ge, kThreads, 0, stream>>>(descs, chunks,
+                                                           nchunks, slots, epoch);
+  else
+    cast_encode_kernel<kE5M2><<<ge, kThreads, 0, stream>>>(descs, chunks,
+                                                           nchunks, slots, epoch);
+  if (mark) mark(kCastEncodeK, 1, stream);
+  return cudaGetLastError();
+}
+
+// Resident CTAs per SM of each cast kernel (for persistent grid sizing).
+cudaError_t cast_occupancy(int* amax_per_sm, int* encode_per_sm) {
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      amax_per_sm, cast_amax_kernel, kThreads, 0);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      encode_per_sm, cast_encode_kernel<kE4M3>, kThreads, 0);
+}
+
+}  // namespace fp8opt

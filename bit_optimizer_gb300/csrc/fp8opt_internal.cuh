@@ -1,0 +1,243 @@
+// Internal definitions shared by the libfp8opt kernels and the host layer.
+//
+// Work decomposition (multi-tensor chunk table): every tensor of a call is cut
+// into chunks of kChunkElems elements (the last chunk of a tensor may be
+// shorter; an empty tensor gets one empty chunk so that its per-tensor outputs
+// are still written).  The host builds the chunk table once per tensor list
+// and caches it on the device.  Each kernel is a persistent grid (a multiple
+// of the SM count) whose CTAs stride over the chunk table; a CTA handles one
+// chunk at a time in tiles of kTileElems elements: thread t takes the 8-element
+// groups starting at tile + k * (kThreads * 8) + t * 8 for k = 0, 1, so every
+// load and store instruction of a warp touches one contiguous span.
+//
+// Per-tensor reductions (amax) and the found_inf flag live in 64-bit slots
+// tagged with a per-call epoch in the high word: a slot is current only when
+// its tag equals this call's epoch, and atomicMax on (epoch << 32 | bits)
+// both starts a new call's maximum and ignores stale values, so the slots need
+// no clearing between calls.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp8opt {
+
+constexpr int kThreads = 256;                    // threads per CTA
+constexpr int kGroup = 8;                        // elements per vector group
+constexpr int kTileElems = kThreads * kGroup * 2;  // 4096 elements per tile
+constexpr int64_t kChunkElems = 32768;           // elements per chunk
+
+constexpr int kE4M3 = 0;
+constexpr int kE5M2 = 1;
+constexpr int kF32 = 0;
+constexpr int kBF16 = 1;
+constexpr int kF16 = 2;
+
+struct Chunk {
+  uint32_t tensor;  // index into the tensor table
+  uint32_t index;   // chunk number within the tensor
+};
+
+struct CastDesc {
+  const void* src;
+  uint8_t* codes;
+  float* amax_out;
+  float* scale_out;
+  int64_t numel;
+  int32_t dtype;
+  int32_t vec_ok;   // all buffers aligned for the vector path
+};
+
+struct StepDesc {
+  const uint8_t* g;
+  uint8_t* m;
+  uint16_t* v;
+  uint16_t* w;
+  uint8_t* w8;
+  const float* g_scale;
+  float* m_scale;
+  float* w8_scale;
+  float* w8_amax;
+  int64_t numel;
+  int32_t g_fmt;
+  int32_t vec_ok;
+};
+
+// Kernels, for the optional per-launch event timing.
+enum KernelId { kCastAmaxK = 0, kCastEncodeK, kStepAmaxK, kStepUpdateK,
+                kStepW8K, kNumKernels };
+
+// Called before (end = 0) and after (end = 1) each kernel launch when timing
+// is on; nullptr otherwise.
+typedef void (*LaunchMark)(int kernel, int end, cudaStream_t stream);
+
+// Per-call scalars of the AdamW step (computed on the host).
+struct StepScalars {
+  float lr, beta1, beta2, eps, omb1, omb2, bc1, sbc2, decay, ils;
+};
+
+// Scratch of one step call: per-tensor slots and the old first-moment scales.
+struct StepScratch {
+  unsigned long long* amax_m;   // [n] amax of this step's fp32 first moment
+  unsigned long long* amax_w;   // [n] amax of the FP16 master (O3)
+  unsigned long long* found;    // [1] found_inf
+  float* old_m_scale;           // [n] m_scale before this step
+};
+
+// ------------------------------------------------------------------ helpers
+
+inline uint32_t grid_min(uint32_t a, uint32_t b) { return a < b ? a : b; }
+
+__device__ __forceinline__ uint32_t canon_amax_bits(uint32_t b) {
+  return b > 0x7F800000u ? 0x7FC00000u : b;   // any NaN -> one quiet NaN
+}
+
+__device__ __forceinline__ uint32_t slot_value(unsigned long long s,
+                                               uint32_t epoch) {
+  return (uint32_t)(s >> 32) == epoch ? (uint32_t)s : 0u;
+}
+
+__device__ __forceinline__ unsigned long long slot_tag(uint32_t epoch,
+                                                       uint32_t bits) {
+  return ((unsigned long long)epoch << 32) | bits;
+}
+
+// fp8_max / amax with the guards: 1.0 when amax is zero or not finite, or
+// when the IEEE quotient is not finite.
+__device__ __forceinline__ float scale_from_amax_bits(uint32_t bits,
+                                                      float fp8_max) {
+  float amax = __uint_as_float(bits);
+  if (!(amax > 0.0f) || bits >= 0x7F800000u) return 1.0f;
+  float q = __fdiv_rn(fp8_max, amax);
+  return (__float_as_uint(q) & 0x7FFFFFFFu) >= 0x7F800000u ? 1.0f : q;
+}
+
+template <int FMT>
+__device__ __forceinline__ float fp8_max_of() {
+  return FMT == kE4M3 ? 448.0f : 57344.0f;
+}
+
+// Two FP8 codes (low byte first) -> two floats, exactly (through FP16).
+template <int FMT>
+__device__ __forceinline__ float2 dec2(uint32_t two) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+      (__nv_fp8x2_storage_t)two, FMT == kE4M3 ? __NV_E4M3 : __NV_E5M2);
+  return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
+// Two floats -> two FP8 codes (x in the low byte), nearest-even, finite
+// overflow saturated.  Only for finite inputs.
+template <int FMT>
+__device__ __forceinline__ uint32_t enc2(float a, float b) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(
+      make_float2(a, b), __NV_SATFINITE, FMT == kE4M3 ? __NV_E4M3 : __NV_E5M2);
+}
+
+// One float -> code, with the non-finite cases selected explicitly (the
+// saturating conversion would map an infinity to the maximum).
+template <int FMT>
+__device__ __forceinline__ uint32_t enc1_checked(float x) {
+  uint32_t b = __float_as_uint(x);
+  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 0x7Fu;
+  if ((b & 0x7FFFFFFFu) == 0x7F800000u)
+    return FMT == kE4M3 ? 0x7Fu : ((b >> 31) ? 0xFCu : 0x7Cu);
+  return (uint32_t)__nv_cvt_float_to_fp8(
+      x, __NV_SATFINITE, FMT == kE4M3 ? __NV_E4M3 : __NV_E5M2);
+}
+
+// Eight floats -> eight codes packed in a uint2 (element 0 in the low byte).
+template <int FMT, bool CHECKED>
+__device__ __forceinline__ uint2 enc8(const float (&x)[8]) {
+  uint32_t p[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (CHECKED)
+      p[j] = enc1_checked<FMT>(x[2 * j]) | (enc1_checked<FMT>(x[2 * j + 1]) << 8);
+    else
+      p[j] = enc2<FMT>(x[2 * j], x[2 * j + 1]);
+  }
+  return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+}
+
+// Any of the four bytes of w a non-finite code?  E4M3: low seven bits all
+// ones; E5M2: exponent field all ones.
+template <int FMT>
+__device__ __forceinline__ uint32_t nonfinite_code_bytes(uint32_t w) {
+  if (FMT == kE4M3) return ((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+  return ((w & 0x7C7C7C7Cu) + 0x04040404u) & 0x80808080u;
+}
+
+// Eight codes in a uint2 -> eight floats.
+template <int FMT>
+__device__ __forceinline__ void dec8(uint2 c, float (&x)[8]) {
+  float2 a = dec2<FMT>(c.x & 0xFFFFu), b = dec2<FMT>(c.x >> 16);
+  float2 d = dec2<FMT>(c.y & 0xFFFFu), e = dec2<FMT>(c.y >> 16);
+  x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+  x[4] = d.x; x[5] = d.y; x[6] = e.x; x[7] = e.y;
+}
+
+// Eight FP16 in a uint4 -> eight floats, and back (nearest-even).
+__device__ __forceinline__ void h8_to_f(uint4 h, float (&x)[8]) {
+  const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+    x[2 * j] = f.x;
+    x[2 * j + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ uint4 f_to_h8(const float (&x)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    __half2 h = __floats2half2_rn(x[2 * j], x[2 * j + 1]);
+    w[j] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ uint16_t f_to_h(float x) {
+  __half h = __float2half_rn(x);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+__device__ __forceinline__ float h_to_f(uint16_t b) {
+  return __half2float(*reinterpret_cast<const __half*>(&b));
+}
+
+// Loads.  ld_keep: read-only data that a later pass reads again (normal
+// caching, through the non-coherent path).  ld_once: data read for the last
+// time in this call, including buffers this kernel overwrites in place
+// (cache-streaming, evict-first; coherent path).
+__device__ __forceinline__ uint2 ld_keep2(const void* p) {
+  return __ldg(reinterpret_cast<const uint2*>(p));
+}
+__device__ __forceinline__ uint4 ld_keep4(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ uint2 ld_once2(const void* p) {
+  return __ldcs(reinterpret_cast<const uint2*>(p));
+}
+__device__ __forceinline__ uint4 ld_once4(const void* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+
+// Max over the CTA of a per-thread uint32; the result is valid in thread 0.
+// Every thread of the CTA must call it.
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* smem) {
+  v = __reduce_max_sync(0xFFFFFFFFu, v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();                 // smem may still be read by a prior call
+  if (lane == 0) smem[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    v = lane < (kThreads / 32) ? smem[lane] : 0u;
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+  }
+  return v;
+}
+
+}  // namespace fp8opt

@@ -1,0 +1,183 @@
+/*
+ * libfp8opt: the scaled FP8 cast and the FP8-state AdamW step of the MS-AMP
+ * mixed-precision scheme, as hand-written CUDA kernels for one GB300 (sm_103a).
+ *
+ * Where the operations come from:
+ *   - MS-AMP documentation, "Optimization Level" page, O1 paragraph and level
+ *     table: weight gradients are kept in FP8 (the cast below).
+ *   - Same page, O2 paragraph and table row: the Adam/AdamW first moment is
+ *     kept in FP8 and the second moment in FP16, with FP16 weights.
+ *   - Same page, O3 paragraph and table row: an FP16 master weight plus an
+ *     FP8 regular weight used for forward/backward.
+ *   - MS-AMP README, "Usage": the GradScaler loop (scaler.scale(loss).backward(),
+ *     scaler.step(optimizer)) and the recognised optimizers (torch.optim.Adam,
+ *     torch.optim.AdamW).
+ *   - TransformerEngine issue #131 ("FP8 questions"): the two FP8 formats
+ *     E4M3 and E5M2, each used in its own place, never cast into one another.
+ *
+ * Formats: E4M3 and E5M2 are the OCP 8-bit floating-point formats (E4M3:
+ * bias 7, max 448, no infinity, NaN = 0x7F/0xFF; E5M2: bias 15, max 57344,
+ * +-inf = 0x7C/0xFC).  FP16 buffers hold IEEE binary16 bit patterns, BF16
+ * buffers bfloat16 bit patterns.  Every encode rounds to nearest, ties to even,
+ * and saturates finite overflow to +-max; a NaN encodes as 0x7F, an infinity
+ * as 0x7F in E4M3 and as the signed infinity code in E5M2.
+ *
+ * Memory: every pointer in an item or parameter record is a DEVICE pointer
+ * owned by the caller; the library never frees or keeps them beyond the call's
+ * stream work.  The library owns a per-(device, stream) workspace (tensor
+ * tables, chunk tables, amax slots, the found_inf word) that it allocates on
+ * first use and grows when a longer list arrives; fp8opt_release() frees all
+ * of it.  The workspace also caches the tensor tables of the last list seen on
+ * each stream, so repeating a call with the same list uploads nothing.
+ *
+ * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ * work of a call is ordered on that stream; the calls return before the GPU
+ * finishes unless the caller asks for found_inf on the host.  Calls on one
+ * stream must come from one host thread at a time; calls on different streams
+ * use different workspaces and may run concurrently.
+ *
+ * Errors: every entry point returns FP8OPT_OK (0) or a negative status.  On an
+ * argument error nothing is launched and no output is touched.  On a CUDA
+ * error the CUDA error text is kept for fp8opt_last_error().
+ */
+#ifndef FP8OPT_H
+#define FP8OPT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported symbols (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define FP8OPT_API __attribute__((visibility("default")))
+#else
+#define FP8OPT_API
+#endif
+
+/* FP8 formats. */
+#define FP8OPT_E4M3 0
+#define FP8OPT_E5M2 1
+
+/* Element types accepted by the cast. */
+#define FP8OPT_F32  0
+#define FP8OPT_BF16 1
+#define FP8OPT_F16  2
+
+/* Status codes. */
+#define FP8OPT_OK               0
+#define FP8OPT_ERR_ARG         (-1)  /* null pointer, n < 0, numel < 0, step < 1,
+                                        incomplete O3 record */
+#define FP8OPT_ERR_UNSUPPORTED (-2)  /* unknown format or element type */
+#define FP8OPT_ERR_CUDA        (-4)  /* a CUDA call failed; see fp8opt_last_error */
+
+/* One tensor of a scaled cast. */
+typedef struct {
+    const void *src;   /* numel elements of type `dtype`, contiguous */
+    int64_t numel;     /* >= 0; 0 is allowed (amax 0, scale 1) */
+    int32_t dtype;     /* FP8OPT_F32, FP8OPT_BF16 or FP8OPT_F16 */
+    int32_t reserved;  /* must be 0 */
+    uint8_t *codes;    /* out: numel FP8 codes */
+    float *amax;       /* out: one fp32, max |x| (NaN above inf above finite;
+                          a NaN amax is written as 0x7FC00000) */
+    float *scale;      /* out: one fp32, fp8_max / amax, or 1.0 when amax is 0
+                          or not finite or the quotient is not finite */
+} fp8opt_cast_item;
+
+/*
+ * fp8_cast_scaled: per-tensor just-in-time scaled cast of a tensor list to FP8
+ * (MS-AMP O1: weight gradients from a wider type to FP8).
+ *
+ * For each item: amax = max |x|; scale = fp8_max / amax (one IEEE fp32
+ * division; fp8_max 448 for E4M3, 57344 for E5M2); code[i] = encode(x[i] *
+ * scale) with one fp32 round-to-nearest product.  One launch covers the whole
+ * list (two passes over the data: amax, then encode).
+ *
+ * items: host array of n records; n >= 0; fmt: FP8OPT_E4M3 or FP8OPT_E5M2;
+ * stream: cudaStream_t.  Source buffers may be unaligned (a scalar path takes
+ * them); the output buffers may not overlap the inputs.
+ */
+FP8OPT_API int fp8_cast_scaled(const fp8opt_cast_item *items, int n, int fmt, void *stream);
+
+/* One tensor of the AdamW step.  O2 when w8 == NULL; O3 when w8, w8_scale and
+ * w8_amax are all set. */
+typedef struct {
+    int64_t numel;         /* >= 0 */
+    const uint8_t *g;      /* numel gradient codes (format g_fmt), as written by
+                              fp8_cast_scaled; may hold loss-scaled values */
+    const float *g_scale;  /* one fp32: the scale the codes were encoded with */
+    int32_t g_fmt;         /* FP8OPT_E4M3 or FP8OPT_E5M2 */
+    int32_t reserved;      /* must be 0 */
+    uint8_t *m;            /* in/out: first moment, numel E4M3 codes */
+    float *m_scale;        /* in/out: one fp32, its scale (1.0 for m = 0) */
+    uint16_t *v;           /* in/out: second moment, numel FP16 */
+    uint16_t *w;           /* in/out: O2 weight, or O3 master weight, FP16 */
+    uint8_t *w8;           /* O3 out: numel E4M3 codes of the master, else NULL */
+    float *w8_scale;       /* O3 out: one fp32, its scale, else NULL */
+    float *w8_amax;        /* O3 out: one fp32, max |master|, else NULL */
+} fp8opt_param;
+
+/*
+ * fp8_adamw_step: one multi-tensor AdamW step with FP8 first moment and FP16
+ * second moment (MS-AMP O2), with FP16 master and FP8 weight copy for O3
+ * records, and the GradScaler inf/NaN skip.
+ *
+ * Per element, in fp32 with each product and sum rounded on its own:
+ *   g = decode(g_code) * (1 / g_scale);  g = g * inv_loss_scale
+ *   m = beta1 * decode(m_code) * (1 / m_scale_old) + (1 - beta1) * g
+ *   v = beta2 * v_old + (1 - beta2) * (g * g)
+ *   w = w_old * (1 - lr * wd) - lr * ((m / bc1) / (sqrt(v) / sqrt(bc2) + eps))
+ * with bc1 = 1 - beta1^step and bc2 = 1 - beta2^step evaluated in double and
+ * rounded to fp32 (sqrt(bc2) from the double).  The first moment is stored as
+ * E4M3 with the new scale 448 / amax(m) of this step; v and w are stored as
+ * FP16 (round to nearest even, overflow to inf).  For O3 records, the FP16
+ * master's amax gives w8_scale = 448 / w8_amax and w8 = encode(master *
+ * w8_scale).
+ *
+ * found_inf: if any unscaled g of any record is not finite, nothing is
+ * written (no code, no state, no scale) and found_inf is 1; the caller then
+ * lowers its loss scale and does not advance `step`, like a GradScaler.
+ *
+ * params: host array of n records; step >= 1.  found_inf: host int, may be
+ * NULL; when set the call waits for the stream and writes 0 or 1.
+ * found_inf_dev: device uint32, may be NULL; when set the kernels write 0 or 1
+ * there without a host round trip.  stream: cudaStream_t.  A record's buffers
+ * must not overlap another record's.  Returns a status; found_inf is a result,
+ * not an error.
+ */
+FP8OPT_API int fp8_adamw_step(const fp8opt_param *params, int n, float lr, float beta1,
+                   float beta2, float eps, float wd, int64_t step,
+                   float inv_loss_scale, int *found_inf,
+                   uint32_t *found_inf_dev, void *stream);
+
+/* Text of a status code (static storage). */
+FP8OPT_API const char *fp8opt_strerror(int status);
+
+/* Detail of the last failing call on this host thread (static or thread-local
+ * storage, valid until the next call on the thread). */
+FP8OPT_API const char *fp8opt_last_error(void);
+
+/* Per-kernel timing (off by default).  While it is on, every kernel the
+ * library launches is bracketed by two CUDA events recorded on the call's
+ * stream, so a caller can measure each kernel's device time inside its own
+ * timed region.  fp8opt_timing_enable(1) clears the record and starts
+ * recording; fp8opt_timing_enable(0) stops.  fp8opt_timing_read waits for the
+ * recorded events and returns, for one kernel name ("cast_amax",
+ * "cast_encode", "step_amax", "step_update", "step_w8"), the launches
+ * recorded since enabling and their summed duration in milliseconds.  Returns
+ * FP8OPT_ERR_ARG for an unknown name or NULL outputs. */
+FP8OPT_API int fp8opt_timing_enable(int on);
+FP8OPT_API int fp8opt_timing_read(const char *kernel, int *launches,
+                                  double *total_ms);
+
+/* Frees every workspace the library holds, on every device.  The caller must
+ * make sure no call's work is still running. */
+FP8OPT_API void fp8opt_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8OPT_H */

@@ -1,0 +1,120 @@
+"""The C-ABI library: it builds, loads without a GPU, exports every entry
+point include/*.h declares, its records have the layout the header gives, and
+argument errors come back as status codes before any CUDA call."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INCLUDE = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_optimizer_gb300 import build
+    build.build()
+    from bit_optimizer_gb300 import _lib
+    return _lib
+
+
+def declared_entry_points():
+    names = []
+    for f in sorted(os.listdir(INCLUDE)):
+        if f.endswith(".h"):
+            text = open(os.path.join(INCLUDE, f)).read()
+            names += re.findall(r"^FP8OPT_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, re.M)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_entry_points()
+    assert {"fp8_cast_scaled", "fp8_adamw_step"} <= set(names)
+    L = lib.load()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(lib.EXPORTS)
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert set(names) <= exported
+
+
+def test_record_layout_matches_header(lib, tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(r'''
+#include <stddef.h>
+#include <stdio.h>
+#include "fp8opt.h"
+#define F(T, m) printf(#T "." #m " %zu\n", offsetof(T, m))
+int main(void) {
+  printf("cast %zu\nparam %zu\n", sizeof(fp8opt_cast_item), sizeof(fp8opt_param));
+  F(fp8opt_cast_item, src); F(fp8opt_cast_item, numel); F(fp8opt_cast_item, dtype);
+  F(fp8opt_cast_item, codes); F(fp8opt_cast_item, amax); F(fp8opt_cast_item, scale);
+  F(fp8opt_param, numel); F(fp8opt_param, g); F(fp8opt_param, g_scale);
+  F(fp8opt_param, g_fmt); F(fp8opt_param, m); F(fp8opt_param, m_scale);
+  F(fp8opt_param, v); F(fp8opt_param, w); F(fp8opt_param, w8);
+  F(fp8opt_param, w8_scale); F(fp8opt_param, w8_amax);
+  return 0;
+}''')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", INCLUDE, str(src), "-o", str(exe)],
+                   check=True)
+    got = dict(l.rsplit(" ", 1) for l in
+               subprocess.run([str(exe)], capture_output=True, text=True,
+                              check=True).stdout.splitlines())
+    assert int(got["cast"]) == C.sizeof(lib.CastItem)
+    assert int(got["param"]) == C.sizeof(lib.Param)
+    for key, val in got.items():
+        if "." in key:
+            t, m = key.split(".")
+            cls = lib.CastItem if t == "fp8opt_cast_item" else lib.Param
+            assert getattr(cls, m).offset == int(val), key
+
+
+def test_argument_errors_need_no_gpu(lib):
+    L = lib.load()
+    item = (lib.CastItem * 1)()
+    assert L.fp8_cast_scaled(item, -1, 0, None) == lib.ERR_ARG
+    assert L.fp8_cast_scaled(None, 1, 0, None) == lib.ERR_ARG
+    assert L.fp8_cast_scaled(item, 1, 7, None) == lib.ERR_UNSUPPORTED
+    item[0].dtype = 9
+    assert L.fp8_cast_scaled(item, 1, 0, None) == lib.ERR_UNSUPPORTED
+    item[0].dtype = 1
+    item[0].numel = 10          # NULL src/codes/amax/scale
+    assert L.fp8_cast_scaled(item, 1, 0, None) == lib.ERR_ARG
+    assert "item 0" in L.fp8opt_last_error().decode()
+    assert L.fp8_cast_scaled(item, 0, 0, None) == lib.OK   # empty list
+
+    p = (lib.Param * 1)()
+    f = C.c_int(7)
+    args = (1e-3, 0.9, 0.999, 1e-8, 0.0)
+    assert L.fp8_adamw_step(p, 1, *args, 0, 1.0, C.byref(f), None, None) == lib.ERR_ARG
+    assert L.fp8_adamw_step(p, -1, *args, 1, 1.0, C.byref(f), None, None) == lib.ERR_ARG
+    p[0].g_fmt = 3
+    assert L.fp8_adamw_step(p, 1, *args, 1, 1.0, None, None, None) == lib.ERR_UNSUPPORTED
+    p[0].g_fmt = 0
+    dummy = C.c_float(1.0)
+    p[0].g_scale = p[0].m_scale = C.addressof(dummy)   # pointers never read
+    p[0].w8 = 0x1000                                    # incomplete O3 record
+    assert L.fp8_adamw_step(p, 1, *args, 1, 1.0, None, None, None) == lib.ERR_ARG
+    assert "O3" in L.fp8opt_last_error().decode()
+    assert L.fp8_adamw_step(p, 0, *args, 1, 1.0, C.byref(f), None, None) == lib.OK
+    assert f.value == 0
+
+
+def test_strerror_texts(lib):
+    assert lib.strerror(0) == "success"
+    assert lib.strerror(-1) == "invalid argument"
+    assert lib.strerror(-4) == "CUDA error"
+    assert lib.strerror(-99) == "unknown status"
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    import bit_optimizer_gb300 as bo
+    with pytest.raises(TypeError):
+        bo.CastPlan([torch.zeros(4)], [torch.zeros(4, dtype=torch.uint8)],
+                    torch.zeros(1), torch.zeros(1))
