@@ -60,7 +60,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     if not os.path.exists(path):
         raise ImportError(
             f"libfp8opt is not built ({path} is missing); run "
-            "`python -m bit_optimizer_gb300.build` or __graft_entry__.build()")
+            "`python bit_optimizer_gb300/build.py` or __graft_entry__.build()")
     L = C.CDLL(path)
     L.fp8_cast_scaled.restype = C.c_int
     L.fp8_cast_scaled.argtypes = [C.POINTER(CastItem), C.c_int, C.c_int,

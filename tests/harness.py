@@ -136,3 +136,117 @@ class GpuState:
             self.w[i].copy_(from_np_u16(s.w, self.w[i].device))
         self.g_scale[:len(states)].copy_(torch.tensor([s.g_scale for s in states]))
         self.m_scale[:len(states)].copy_(torch.tensor([s.m_scale[0] for s in states]))
+
+
+class DeviceList:
+    """A whole workload resident on the device, in 256-byte-aligned arenas, run
+    through the same plans ``bench.py`` times (CastPlan + AdamWPlan).  The
+    oracle follows a sample of whole tensors: before each step their device
+    state is overwritten with the oracle's, so every compared output is one
+    step of the library from the oracle's inputs."""
+
+    def __init__(self, wl, device="cuda"):
+        import bit_optimizer_gb300 as bo
+        self.wl = wl
+        self.device = device
+        self.o3 = wl.level == "O3"
+        self.fmt = oracle.FMT[wl.grad_fmt]
+        n = len(wl.shapes)
+        numels = wl.numels
+        f32 = dict(dtype=torch.float32, device=device)
+        self.w = bo.arena_views(numels, torch.float16, device)
+        for i, w in enumerate(self.w):
+            w.copy_(wl.weight(i, device))
+        self.src = bo.arena_views(numels, wl.grad_dtype, device)
+        self.g = bo.arena_views(numels, torch.uint8, device)
+        self.m = bo.arena_views(numels, torch.uint8, device, fill=0)
+        self.v = bo.arena_views(numels, torch.float16, device, fill=0)
+        self.g_amax = torch.zeros(n, **f32)
+        self.g_scale = torch.ones(n, **f32)
+        self.m_scale = torch.ones(n, **f32)
+        if self.o3:
+            self.w8 = bo.arena_views(numels, torch.uint8, device, fill=0)
+            self.w8_scale = torch.ones(n, **f32)
+            self.w8_amax = torch.zeros(n, **f32)
+        else:
+            self.w8 = self.w8_scale = self.w8_amax = None
+        self.cast = bo.CastPlan(self.src, self.g, self.g_amax, self.g_scale,
+                                wl.grad_fmt)
+        self.plan = bo.AdamWPlan(self.g, self.g_scale, self.m, self.m_scale,
+                                 self.v, self.w, self.w8, self.w8_scale,
+                                 self.w8_amax, wl.grad_fmt)
+        self.found_dev = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def gen_grads(self, step, wl=None):
+        wl = wl or self.wl
+        for i, s in enumerate(self.src):
+            s.copy_(wl.grad(i, step, self.device))
+
+    def fresh_oracle(self, i):
+        n = self.wl.numels[i]
+        return oracle.StepState(np.zeros(n, np.uint8), 1.0, np.zeros(n, np.uint8),
+                                1.0, np.zeros(n, np.uint16), to_np_u16(self.w[i]),
+                                g_fmt=self.fmt, o3=self.o3)
+
+    def cast_and_check(self, sample, states):
+        """GPU cast of every tensor; the oracle casts the sampled ones from
+        the same values and its codes become their step inputs."""
+        self.cast()
+        torch.cuda.synchronize()
+        amax = self.g_amax.cpu().numpy()
+        scale = self.g_scale.cpu().numpy()
+        for i in sample:
+            a, dt = host_src(self.src[i])
+            codes, am, sc = oracle.cast_scaled(a, dt, self.fmt)
+            check_f32_exact(amax[i:i + 1], [am], f"grad amax[{i}]")
+            check_f32_exact(scale[i:i + 1], [sc], f"grad scale[{i}]")
+            check_codes(to_np_u8(self.g[i]), codes, self.fmt, name=f"grad[{i}]")
+            states[i].g = codes
+            states[i].g_scale = float(sc)
+
+    def put(self, i, st):
+        self.g[i].copy_(torch.from_numpy(st.g))
+        self.g_scale[i] = st.g_scale
+        self.m[i].copy_(torch.from_numpy(st.m))
+        self.m_scale[i] = float(st.m_scale[0])
+        self.v[i].copy_(from_np_u16(st.v, self.device))
+        self.w[i].copy_(from_np_u16(st.w, self.device))
+
+    def step(self, t, ils=None):
+        wl = self.wl
+        return self.plan(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, t,
+                         wl.inv_loss_scale if ils is None else ils,
+                         found_inf_dev=self.found_dev)
+
+    def compare(self, i, st):
+        check_f32_exact(self.m_scale[i:i + 1].cpu().numpy(), st.m_scale, f"m_scale[{i}]")
+        check_codes(to_np_u8(self.m[i]), st.m, name=f"m[{i}]")
+        check_f16(to_np_u16(self.v[i]), st.v, name=f"v[{i}]")
+        w = to_np_u16(self.w[i])
+        check_f16(w, st.w, name=f"w[{i}]")
+        if self.o3:
+            check_master(w, st.w, name=f"master[{i}]")
+            check_codes(to_np_u8(self.w8[i]), st.w8, name=f"w8[{i}]")
+            check_f32_exact(self.w8_scale[i:i + 1].cpu().numpy(), st.w8_scale,
+                            f"w8_scale[{i}]")
+            check_f32_exact(self.w8_amax[i:i + 1].cpu().numpy(), st.w8_amax,
+                            f"w8_amax[{i}]")
+
+    def invariants(self):
+        """Properties of a finished step that hold for every tensor at any
+        size: the just-in-time scale puts each nonzero first moment's largest
+        element on the E4M3 maximum, no moment is NaN, v is non-negative, and
+        the weights are finite."""
+        for i in range(len(self.m)):
+            if self.m[i].numel() == 0:
+                continue
+            mag = self.m[i] & 0x7F
+            top = int(mag.max().item())
+            assert top in (0, 0x7E), f"tensor {i}: largest |m| code {top:#x}"
+            assert not bool((mag == 0x7F).any().item()), f"tensor {i}: NaN m"
+            v = self.v[i]
+            assert not bool((v < 0).any().item()), f"tensor {i}: negative v"
+            assert bool(torch.isfinite(self.w[i]).all().item()), f"tensor {i}: w"
+            if self.o3:
+                top8 = int((self.w8[i] & 0x7F).max().item())
+                assert top8 in (0, 0x7E), f"tensor {i}: largest |w8| code {top8:#x}"

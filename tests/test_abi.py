@@ -14,8 +14,8 @@ INCLUDE = os.path.join(ROOT, "include")
 
 @pytest.fixture(scope="module")
 def lib():
-    from bit_optimizer_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     from bit_optimizer_gb300 import _lib
     return _lib
 

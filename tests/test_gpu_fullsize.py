@@ -1,0 +1,121 @@
+"""Parity at the workloads' full sizes, in the launch configuration the
+bench times.  Every tensor is resident and stepped by the library; the
+oracle follows a sample of whole tensors (all the small ones and the
+position embedding, and for the cast every tensor), and properties that hold
+at any size are checked on every tensor."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from harness import DeviceList, host_src, oracle_step
+from parity import check_codes, check_f32_exact, to_np_u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bo():
+    import bit_optimizer_gb300 as bo
+    return bo
+
+
+def sample_of(wl, limit):
+    """The position embedding (a multi-chunk tensor with a ragged last tile)
+    and whole tensors, smallest first, up to `limit` parameters."""
+    order = sorted(range(len(wl.shapes)), key=lambda i: wl.numels[i])
+    out, total = [1], wl.numels[1]
+    for i in order:
+        if i == 1:
+            continue
+        if total + wl.numels[i] <= limit:
+            out.append(i)
+            total += wl.numels[i]
+    return sorted(out)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_cast_gpt2_124m_every_tensor(bo, fmt):
+    wl = synth.gpt2_cast()
+    assert wl.n_params == 124_439_808
+    dev = [wl.grad(i, 1, "cuda") for i in range(len(wl.shapes))]
+    codes, amax, scale = bo.fp8_cast_scaled(dev, fmt)
+    torch.cuda.synchronize()
+    amax, scale = amax.cpu().numpy(), scale.cpu().numpy()
+    f = oracle.FMT[fmt]
+    for i, g in enumerate(dev):
+        a, dt = host_src(g)
+        rc, ra, rs = oracle.cast_scaled(a, dt, f)
+        check_f32_exact(amax[i:i + 1], [ra], f"amax[{i}]")
+        check_f32_exact(scale[i:i + 1], [rs], f"scale[{i}]")
+        check_codes(to_np_u8(codes[i]), rc, f, name=f"codes[{i}]")
+
+
+def lockstep_full(wl, steps, sample, first=1):
+    dl = DeviceList(wl)
+    states = {i: dl.fresh_oracle(i) for i in sample}
+    for t in range(first, first + steps):
+        dl.gen_grads(t)
+        dl.cast_and_check(sample, states)
+        for i in sample:
+            dl.put(i, states[i])
+        f_ref = oracle_step([states[i] for i in sample], wl, t)
+        assert dl.step(t) == f_ref == 0
+        for i in sample:
+            dl.compare(i, states[i])
+    return dl, states
+
+
+def test_o2_350m_full_inf_skip_and_step(bo):
+    wl = synth.o2_350m()
+    clean = dataclasses.replace(wl, inf_site=None)
+    sample = sample_of(wl, 3_000_000)
+    assert wl.inf_site[0] in sample
+    dl, states = lockstep_full(clean, wl.warmup_steps, sample)
+    t = wl.warmup_steps + 1
+    # the measured step's gradients hold one +inf: nothing may change
+    dl.gen_grads(t, wl)
+    dl.cast_and_check(sample, states)
+    for i in sample:
+        dl.put(i, states[i])
+    sums = [(x.sum(dtype=torch.int64).item(), x.numel()) for x in dl.m]
+    vsum = [x.view(torch.int16).sum(dtype=torch.int64).item() for x in dl.v]
+    wsum = [x.view(torch.int16).sum(dtype=torch.int64).item() for x in dl.w]
+    mscale = dl.m_scale.clone()
+    assert oracle_step([states[i] for i in sample], wl, t) == 1
+    assert dl.step(t) == 1 and dl.found_dev.item() == 1
+    assert sums == [(x.sum(dtype=torch.int64).item(), x.numel()) for x in dl.m]
+    assert vsum == [x.view(torch.int16).sum(dtype=torch.int64).item() for x in dl.v]
+    assert wsum == [x.view(torch.int16).sum(dtype=torch.int64).item() for x in dl.w]
+    assert torch.equal(mscale, dl.m_scale)
+    # the same step with the inf cleared
+    dl.gen_grads(t, clean)
+    dl.cast_and_check(sample, states)
+    for i in sample:
+        dl.put(i, states[i])
+    assert oracle_step([states[i] for i in sample], wl, t) == 0
+    assert dl.step(t) == 0
+    for i in sample:
+        dl.compare(i, states[i])
+    dl.invariants()
+
+
+def test_o3_1p3b_full(bo):
+    wl = synth.o3_1p3b()
+    sample = sample_of(wl, 6_000_000)
+    dl, _ = lockstep_full(wl, wl.warmup_steps + 1, sample)
+    dl.invariants()
+
+
+def test_o2_6p7b_tail_full_10_steps(bo):
+    wl = synth.o2_6p7b_tail()
+    assert len(wl.shapes) == 589
+    sample = sample_of(wl, 12_000_000)       # every tail tensor, norms, biases, wpe
+    assert len(wl.shapes) - 1 in sample and 1 in sample
+    dl, _ = lockstep_full(wl, wl.steps, sample)
+    dl.invariants()
+    zero = len(wl.shapes) - 1
+    assert dl.m_scale[zero].item() == 1.0 and not bool(dl.m[zero].any().item())
