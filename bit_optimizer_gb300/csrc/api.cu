@@ -74,14 +74,17 @@ struct DeviceInfo {
   int step_amax = 0, step_update = 0, step_w8 = 0;
 };
 
-// Per-(device, stream) state.  Slot region layout (uint64 words):
-// [0, n) per-tensor amax A, [n, 2n) per-tensor amax B, [2n] found_inf;
-// then n floats of saved scales.
+// Per-(device, stream) state.  The slot region holds only epoch-tagged
+// uint64 words: [0, n) per-tensor amax A, [n, 2n) per-tensor amax B, [2n]
+// found_inf (a call with another n lays them out differently, which is safe
+// because every word carries an older epoch).  Untagged scratch (the saved
+// first-moment scales) lives in its own buffer, so it can never be read as a
+// tag.
 struct Workspace {
   int device = 0;
   uint32_t epoch = 0;
   DevBuf slots;
-  size_t slot_tensors = 0;   // n the slot region is laid out for
+  DevBuf saved_scales;       // n floats: m_scale before the step
   // cast tables
   std::vector<fp8opt_cast_item> cast_key;
   DevBuf cast_descs, cast_chunks;
@@ -94,6 +97,7 @@ struct Workspace {
 
   void release() {
     slots.release();
+    saved_scales.release();
     cast_descs.release();
     cast_chunks.release();
     step_descs.release();
@@ -101,7 +105,6 @@ struct Workspace {
     cast_key.clear();
     step_key.clear();
     have_cast = have_step = false;
-    slot_tensors = 0;
   }
 };
 
@@ -143,17 +146,12 @@ Workspace* workspace(int dev, cudaStream_t s) {
 // Slots for n tensors, zeroed when (re)allocated or when the epoch wraps.
 cudaError_t prepare_slots(Workspace* ws, size_t n, cudaStream_t stream,
                           uint32_t* epoch_out) {
-  const size_t bytes = (2 * n + 1) * sizeof(unsigned long long) + n * sizeof(float);
+  const size_t bytes = (2 * n + 1) * sizeof(unsigned long long);
   bool fresh = false;
   if (bytes > ws->slots.cap) {
     cudaError_t e = ws->slots.reserve(bytes);
     if (e != cudaSuccess) return e;
     fresh = true;
-  }
-  if (n != ws->slot_tensors) {
-    // the slot layout moved: old tags may sit at other tensors' indices, but
-    // they carry older epochs, so they read as zero; nothing to clear
-    ws->slot_tensors = n;
   }
   ws->epoch += 1;
   if (ws->epoch == 0) {   // 2^32 calls: tags would repeat
@@ -347,9 +345,12 @@ extern "C" int fp8_adamw_step(const fp8opt_param* params, int n, float lr,
         (p.numel > 0 && (p.g == nullptr || p.m == nullptr || p.v == nullptr ||
                          p.w == nullptr)))
       return fail(FP8OPT_ERR_ARG, at + ": bad numel, reserved field or NULL pointer");
-    const int o3 = (p.w8 != nullptr) + (p.w8_scale != nullptr) + (p.w8_amax != nullptr);
-    if (o3 != 0 && o3 != 3)
+    const bool o3 = p.w8_scale != nullptr || p.w8_amax != nullptr;
+    if (o3 && (p.w8_scale == nullptr || p.w8_amax == nullptr ||
+               (p.numel > 0 && p.w8 == nullptr)))
       return fail(FP8OPT_ERR_ARG, at + ": O3 needs w8, w8_scale and w8_amax together");
+    if (!o3 && p.w8 != nullptr)
+      return fail(FP8OPT_ERR_ARG, at + ": w8 given without w8_scale and w8_amax");
   }
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   if (n == 0) {
@@ -361,18 +362,18 @@ extern "C" int fp8_adamw_step(const fp8opt_param* params, int n, float lr,
     return FP8OPT_OK;
   }
 
-  // Per-call scalars: bias corrections in double, rounded to fp32.
+  // Per-call scalars: the bias corrections 1 - beta^t in double, entering
+  // only through lr / bc1 and 1 / sqrt(bc2), each rounded to fp32 once.
   StepScalars s;
   const double bc1 = 1.0 - std::pow((double)beta1, (double)step);
   const double bc2 = 1.0 - std::pow((double)beta2, (double)step);
-  s.lr = lr;
   s.beta1 = beta1;
   s.beta2 = beta2;
   s.eps = eps;
   s.omb1 = 1.0f - beta1;
   s.omb2 = 1.0f - beta2;
-  s.bc1 = (float)bc1;
-  s.sbc2 = (float)std::sqrt(bc2);
+  s.step_size = (float)((double)lr / bc1);
+  s.inv_sbc2 = (float)(1.0 / std::sqrt(bc2));
   s.decay = 1.0f - lr * wd;
   s.ils = inv_loss_scale;
 
@@ -405,11 +406,12 @@ extern "C" int fp8_adamw_step(const fp8opt_param* params, int n, float lr,
       d.w8_amax = p.w8_amax;
       d.numel = p.numel;
       d.g_fmt = p.g_fmt;
+      d.o3 = p.w8_scale != nullptr;
       d.vec_ok = aligned(p.g, 8) && aligned(p.m, 8) && aligned(p.v, 16) &&
                  aligned(p.w, 16) && (p.w8 == nullptr || aligned(p.w8, 8));
       for (uint32_t c = 0, nc = chunks_of(p.numel); c < nc; ++c) {
         chunks.push_back(Chunk{(uint32_t)i, c});
-        if (p.w8 != nullptr) chunks_o3.push_back(Chunk{(uint32_t)i, c});
+        if (d.o3) chunks_o3.push_back(Chunk{(uint32_t)i, c});
       }
     }
     const uint32_t nmain = (uint32_t)chunks.size();
@@ -430,12 +432,14 @@ extern "C" int fp8_adamw_step(const fp8opt_param* params, int n, float lr,
   uint32_t epoch = 0;
   if ((e = prepare_slots(ws, (size_t)n, stream, &epoch)) != cudaSuccess)
     return cuda_fail(e, "fp8_adamw_step: workspace");
+  if ((e = ws->saved_scales.reserve((size_t)n * sizeof(float))) != cudaSuccess)
+    return cuda_fail(e, "fp8_adamw_step: workspace");
   unsigned long long* slots = static_cast<unsigned long long*>(ws->slots.ptr);
   StepScratch sc;
   sc.amax_m = slots;
   sc.amax_w = slots + n;
   sc.found = slots + 2 * (size_t)n;
-  sc.old_m_scale = reinterpret_cast<float*>(slots + 2 * (size_t)n + 1);
+  sc.old_m_scale = static_cast<float*>(ws->saved_scales.ptr);
   const Chunk* chunks = static_cast<const Chunk*>(ws->step_chunks.ptr);
   e = launch_step(static_cast<const StepDesc*>(ws->step_descs.ptr), chunks,
                   ws->step_nchunks, chunks + ws->step_nchunks, ws->step_nchunks_o3,

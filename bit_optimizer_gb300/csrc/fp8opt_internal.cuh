@@ -62,7 +62,8 @@ struct StepDesc {
   float* w8_amax;
   int64_t numel;
   int32_t g_fmt;
-  int32_t vec_ok;
+  int16_t vec_ok;
+  int16_t o3;       // emits the E4M3 weight copy (w8 is NULL if numel is 0)
 };
 
 // Kernels, for the optional per-launch event timing.
@@ -73,9 +74,11 @@ enum KernelId { kCastAmaxK = 0, kCastEncodeK, kStepAmaxK, kStepUpdateK,
 // is on; nullptr otherwise.
 typedef void (*LaunchMark)(int kernel, int end, cudaStream_t stream);
 
-// Per-call scalars of the AdamW step (computed on the host).
+// Per-call scalars of the AdamW step (computed on the host): the bias
+// corrections enter only through step_size = lr / (1 - beta1^t) and
+// inv_sbc2 = 1 / sqrt(1 - beta2^t), each evaluated in double and rounded once.
 struct StepScalars {
-  float lr, beta1, beta2, eps, omb1, omb2, bc1, sbc2, decay, ils;
+  float beta1, beta2, eps, omb1, omb2, step_size, inv_sbc2, decay, ils;
 };
 
 // Scratch of one step call: per-tensor slots and the old first-moment scales.
@@ -207,6 +210,33 @@ __device__ __forceinline__ uint16_t f_to_h(float x) {
 __device__ __forceinline__ float h_to_f(uint16_t b) {
   return __half2float(*reinterpret_cast<const __half*>(&b));
 }
+
+// Paired fp32 arithmetic (one instruction for two lanes of a float2).  Each
+// lane is rounded exactly like the scalar operation (round to nearest even,
+// denormals kept).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// a * b + c with one rounding per lane.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
 
 // Loads.  ld_keep: read-only data that a later pass reads again (normal
 // caching, through the non-coherent path).  ld_once: data read for the last

@@ -18,85 +18,126 @@
 // The update walks the chunk table backwards and the O3 pass forwards, so
 // each pass starts on the chunks the previous one left in L2.
 //
-// Every product and sum is rounded on its own (the file is compiled without
-// multiply-add contraction), in the order of the definition, so the first
-// moment, and with it its amax and scale, is bit-identical to a scalar fp32
-// evaluation of the same expression.
+// Arithmetic per element, in fp32 (each operation rounded once; fma rounds
+// the product and the sum once together):
+//   g = dec(g_code) * k                       k = inv_loss_scale / g_scale
+//   m = fma(beta1, dec(m_code) * minv, (1 - beta1) * g)   minv = 1 / m_scale
+//   v = fma(beta2, v_old, (1 - beta2) * (g * g))
+//   u = m / fma(sqrt(v), inv_sbc2, eps)
+//   w = fma(-step_size, u, w_old * decay)
+// Elements are processed in pairs with the paired fp32 instructions, which
+// round each lane like the scalar ones, so the first moment, its amax and its
+// scale are bit-identical to a scalar fp32 evaluation of the same lines.
 #include "fp8opt_internal.cuh"
 
 namespace fp8opt {
 
 namespace {
 
-constexpr int kAmaxGroups = 2;   // 8-element groups per thread per tile
-constexpr int kUpdGroups = 2;
-
-// Unscaled gradients of eight codes: decode, times 1/g_scale, times the
-// inverse loss scale.
-template <int GF>
-__device__ __forceinline__ void grad8(uint2 gc, float ginv, float ils,
-                                      float (&g)[8]) {
-  dec8<GF>(gc, g);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) g[j] = __fmul_rn(__fmul_rn(g[j], ginv), ils);
-}
-
-__device__ __forceinline__ float m_new(float mdec, float minv, float g,
-                                       const StepScalars& s) {
-  const float mp = __fmul_rn(mdec, minv);
-  return __fadd_rn(__fmul_rn(s.beta1, mp), __fmul_rn(s.omb1, g));
-}
+// Tunables (compile-time): 8-element groups each thread keeps in flight per
+// tile in the amax and update passes, and the update kernel's resident CTAs
+// per SM (which caps its registers a thread).
+#ifndef FP8OPT_STEP_AMAX_GROUPS
+#define FP8OPT_STEP_AMAX_GROUPS 2
+#endif
+#ifndef FP8OPT_UPD_GROUPS
+#define FP8OPT_UPD_GROUPS 2
+#endif
+#ifndef FP8OPT_UPD_MIN_BLOCKS
+#define FP8OPT_UPD_MIN_BLOCKS 3
+#endif
+constexpr int kAmaxGroups = FP8OPT_STEP_AMAX_GROUPS;
+constexpr int kUpdGroups = FP8OPT_UPD_GROUPS;
+constexpr int kW8Groups = 2;
 
 __device__ __forceinline__ uint32_t nonfinite(float x) {
   return (__float_as_uint(x) & 0x7FFFFFFFu) >= 0x7F800000u;
 }
 
+__device__ __forceinline__ uint32_t abs_bits(float x) {
+  return __float_as_uint(x) & 0x7FFFFFFFu;
+}
+
+// The scalar forms of the lines above (tails and unaligned tensors).
+__device__ __forceinline__ float m_new1(float mdec, float minv, float g,
+                                        const StepScalars& s) {
+  return __fmaf_rn(s.beta1, __fmul_rn(mdec, minv), __fmul_rn(s.omb1, g));
+}
+
+__device__ __forceinline__ void adamw1(float g, float m, float vp, float wp,
+                                       const StepScalars& s, float& v,
+                                       float& w) {
+  v = __fmaf_rn(s.beta2, vp, __fmul_rn(s.omb2, __fmul_rn(g, g)));
+  const float den = __fmaf_rn(__fsqrt_rn(v), s.inv_sbc2, s.eps);
+  const float u = __fdiv_rn(m, den);
+  w = __fmaf_rn(-s.step_size, u, __fmul_rn(wp, s.decay));
+}
+
+// Two FP16 (one 32-bit word) <-> float2.
+__device__ __forceinline__ float2 h2_to_f2(uint32_t h) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+__device__ __forceinline__ uint32_t f2_to_h2(float2 f) {
+  __half2 h = __float22half2_rn(f);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Code pair j (0..3) of eight codes held in a uint2.
+__device__ __forceinline__ uint32_t code_pair(uint2 c, int j) {
+  const uint32_t w = j < 2 ? c.x : c.y;
+  return (j & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+__device__ __forceinline__ uint32_t half_pair(uint4 h, int j) {
+  return j == 0 ? h.x : j == 1 ? h.y : j == 2 ? h.z : h.w;
+}
+
 // ------------------------------------------------------------ pass 1: amax
 
-// SAFE: every finite gradient code unscales to a finite value (checked once
+// SAFE: every finite gradient code unscales to a finite value (decided once
 // per chunk from the largest code), so found_inf only needs the codes.
 template <int GF, bool SAFE>
 __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
-                                 float ginv, float minv, const StepScalars& s,
+                                 float k, float minv, const StepScalars& s,
                                  uint32_t& mx, uint32_t& bad) {
   constexpr int64_t kTile = (int64_t)kThreads * kGroup * kAmaxGroups;
   const int tid = threadIdx.x;
   const bool vec = d.vec_ok != 0;
+  const float2 k2 = splat2(k), minv2 = splat2(minv), b1 = splat2(s.beta1),
+               omb1 = splat2(s.omb1);
   for (int64_t base = begin; base < end; base += kTile) {
     if (vec && base + kTile <= end) {
       uint2 gc[kAmaxGroups], mc[kAmaxGroups];
 #pragma unroll
-      for (int k = 0; k < kAmaxGroups; ++k) {
-        const int64_t i0 = base + k * (kThreads * kGroup) + tid * kGroup;
-        gc[k] = ld_keep2(d.g + i0);
-        mc[k] = ld_keep2(d.m + i0);
+      for (int q = 0; q < kAmaxGroups; ++q) {
+        const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
+        gc[q] = ld_keep2(d.g + i0);
+        mc[q] = ld_keep2(d.m + i0);
       }
 #pragma unroll
-      for (int k = 0; k < kAmaxGroups; ++k) {
-        float g[8], md[8];
-        grad8<GF>(gc[k], ginv, s.ils, g);
-        dec8<kE4M3>(mc[k], md);
-        if (SAFE) {
-          bad |= nonfinite_code_bytes<GF>(gc[k].x) | nonfinite_code_bytes<GF>(gc[k].y);
-        }
+      for (int q = 0; q < kAmaxGroups; ++q) {
+        if (SAFE)
+          bad |= nonfinite_code_bytes<GF>(gc[q].x) | nonfinite_code_bytes<GF>(gc[q].y);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (!SAFE) bad |= nonfinite(g[j]);
-          mx = max(mx, __float_as_uint(m_new(md[j], minv, g[j], s)) & 0x7FFFFFFFu);
+        for (int j = 0; j < 4; ++j) {
+          const float2 g = mul2(dec2<GF>(code_pair(gc[q], j)), k2);
+          if (!SAFE) bad |= nonfinite(g.x) | nonfinite(g.y);
+          const float2 m = fma2(b1, mul2(dec2<kE4M3>(code_pair(mc[q], j)), minv2),
+                                mul2(omb1, g));
+          mx = max(mx, max(abs_bits(m.x), abs_bits(m.y)));
         }
       }
     } else {
 #pragma unroll 1
-      for (int k = 0; k < kAmaxGroups; ++k) {
-        const int64_t i0 = base + k * (kThreads * kGroup) + tid * kGroup;
+      for (int q = 0; q < kAmaxGroups; ++q) {
+        const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
         for (int j = 0; j < kGroup; ++j) {
           const int64_t i = i0 + j;
           if (i >= end) break;
-          const float gd = dec2<GF>(d.g[i]).x;
-          const float g = __fmul_rn(__fmul_rn(gd, ginv), s.ils);
+          const float g = __fmul_rn(dec2<GF>(d.g[i]).x, k);
           bad |= nonfinite(g);
-          const float md = dec2<kE4M3>(d.m[i]).x;
-          mx = max(mx, __float_as_uint(m_new(md, minv, g, s)) & 0x7FFFFFFFu);
+          mx = max(mx, abs_bits(m_new1(dec2<kE4M3>(d.m[i]).x, minv, g, s)));
         }
       }
     }
@@ -106,16 +147,15 @@ __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
 template <int GF>
 __device__ __forceinline__ void step_amax_dispatch(const StepDesc& d,
                                                    int64_t begin, int64_t end,
-                                                   float ginv, float minv,
+                                                   float k, float minv,
                                                    const StepScalars& s,
                                                    uint32_t& mx, uint32_t& bad) {
-  // The largest finite code unscales to the largest |g|; rounding is
-  // monotonic, so if that is finite every finite code gives a finite g.
-  const float gmax = __fmul_rn(__fmul_rn(fp8_max_of<GF>(), ginv), fabsf(s.ils));
-  if (!nonfinite(__fmul_rn(fp8_max_of<GF>(), ginv)) && !nonfinite(gmax))
-    thread_step_amax<GF, true>(d, begin, end, ginv, minv, s, mx, bad);
+  // The largest finite code gives the largest |g|; rounding is monotonic, so
+  // if that product is finite every finite code gives a finite g.
+  if (!nonfinite(__fmul_rn(fp8_max_of<GF>(), k)))
+    thread_step_amax<GF, true>(d, begin, end, k, minv, s, mx, bad);
   else
-    thread_step_amax<GF, false>(d, begin, end, ginv, minv, s, mx, bad);
+    thread_step_amax<GF, false>(d, begin, end, k, minv, s, mx, bad);
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -128,14 +168,14 @@ step_amax_kernel(const StepDesc* __restrict__ descs,
     const StepDesc d = descs[ch.tensor];
     const float gs = *d.g_scale, ms = *d.m_scale;
     if (ch.index == 0 && threadIdx.x == 0) sc.old_m_scale[ch.tensor] = ms;
-    const float ginv = __frcp_rn(gs), minv = __frcp_rn(ms);
+    const float k = __fdiv_rn(s.ils, gs), minv = __frcp_rn(ms);
     const int64_t begin = (int64_t)ch.index * kChunkElems;
     const int64_t end = min(begin + kChunkElems, d.numel);
     uint32_t mx = 0, bad = 0;
     if (d.g_fmt == kE4M3)
-      step_amax_dispatch<kE4M3>(d, begin, end, ginv, minv, s, mx, bad);
+      step_amax_dispatch<kE4M3>(d, begin, end, k, minv, s, mx, bad);
     else
-      step_amax_dispatch<kE5M2>(d, begin, end, ginv, minv, s, mx, bad);
+      step_amax_dispatch<kE5M2>(d, begin, end, k, minv, s, mx, bad);
     mx = block_max_u32(mx, red);
     const int any_bad = __syncthreads_or(bad != 0);
     if (threadIdx.x == 0) {
@@ -147,75 +187,78 @@ step_amax_kernel(const StepDesc* __restrict__ descs,
 
 // ---------------------------------------------------------- pass 2: update
 
-// The update of one element; returns the new fp32 m, v and w.
-__device__ __forceinline__ void adamw1(float g, float mdec, float minv,
-                                       float vp, float wp, const StepScalars& s,
-                                       float& m, float& v, float& w) {
-  m = m_new(mdec, minv, g, s);
-  v = __fadd_rn(__fmul_rn(s.beta2, vp), __fmul_rn(s.omb2, __fmul_rn(g, g)));
-  const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.sbc2), s.eps);
-  const float upd = __fdiv_rn(__fdiv_rn(m, s.bc1), denom);
-  w = __fsub_rn(__fmul_rn(wp, s.decay), __fmul_rn(s.lr, upd));
-}
-
 // MCHECK: the first moment holds a non-finite value (its amax is not
 // finite), so its codes take the explicit NaN code.  O3: also reduce the
 // FP16 master's max |bits| per 16-bit lane into hmax.
 template <int GF, bool O3, bool MCHECK>
 __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
-                              float ginv, float minv, float msc,
+                              float k, float minv, float msc,
                               const StepScalars& s, uint32_t& hmax) {
   constexpr int64_t kTile = (int64_t)kThreads * kGroup * kUpdGroups;
   const int tid = threadIdx.x;
   const bool vec = d.vec_ok != 0;
+  const float2 k2 = splat2(k), minv2 = splat2(minv), b1 = splat2(s.beta1),
+               omb1 = splat2(s.omb1), b2 = splat2(s.beta2),
+               omb2 = splat2(s.omb2), isbc2 = splat2(s.inv_sbc2),
+               eps2 = splat2(s.eps), nstep = splat2(-s.step_size),
+               decay = splat2(s.decay), msc2 = splat2(msc);
   for (int64_t base = begin; base < end; base += kTile) {
     if (vec && base + kTile <= end) {
       uint2 gc[kUpdGroups], mc[kUpdGroups];
       uint4 vh[kUpdGroups], wh[kUpdGroups];
 #pragma unroll
-      for (int k = 0; k < kUpdGroups; ++k) {
-        const int64_t i0 = base + k * (kThreads * kGroup) + tid * kGroup;
-        gc[k] = ld_once2(d.g + i0);
-        mc[k] = ld_once2(d.m + i0);
-        vh[k] = ld_once4(d.v + i0);
-        wh[k] = ld_once4(d.w + i0);
+      for (int q = 0; q < kUpdGroups; ++q) {
+        const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
+        gc[q] = ld_once2(d.g + i0);
+        mc[q] = ld_once2(d.m + i0);
+        vh[q] = ld_once4(d.v + i0);
+        wh[q] = ld_once4(d.w + i0);
       }
 #pragma unroll
-      for (int k = 0; k < kUpdGroups; ++k) {
-        const int64_t i0 = base + k * (kThreads * kGroup) + tid * kGroup;
-        float g[8], md[8], vp[8], wp[8], m[8], v[8], w[8];
-        grad8<GF>(gc[k], ginv, s.ils, g);
-        dec8<kE4M3>(mc[k], md);
-        h8_to_f(vh[k], vp);
-        h8_to_f(wh[k], wp);
+      for (int q = 0; q < kUpdGroups; ++q) {
+        const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
+        uint32_t mo[4], vo[4], wo[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          adamw1(g[j], md[j], minv, vp[j], wp[j], s, m[j], v[j], w[j]);
-          m[j] = __fmul_rn(m[j], msc);
+        for (int j = 0; j < 4; ++j) {
+          const float2 g = mul2(dec2<GF>(code_pair(gc[q], j)), k2);
+          const float2 m = fma2(b1, mul2(dec2<kE4M3>(code_pair(mc[q], j)), minv2),
+                                mul2(omb1, g));
+          const float2 v = fma2(b2, h2_to_f2(half_pair(vh[q], j)),
+                                mul2(omb2, mul2(g, g)));
+          float2 sq;
+          sq.x = __fsqrt_rn(v.x);
+          sq.y = __fsqrt_rn(v.y);
+          const float2 den = fma2(sq, isbc2, eps2);
+          float2 u;
+          u.x = __fdiv_rn(m.x, den.x);
+          u.y = __fdiv_rn(m.y, den.y);
+          const float2 w = fma2(nstep, u, mul2(h2_to_f2(half_pair(wh[q], j)), decay));
+          const float2 mt = mul2(m, msc2);
+          mo[j] = MCHECK ? (enc1_checked<kE4M3>(mt.x) | (enc1_checked<kE4M3>(mt.y) << 8))
+                         : enc2<kE4M3>(mt.x, mt.y);
+          vo[j] = f2_to_h2(v);
+          wo[j] = f2_to_h2(w);
         }
-        *reinterpret_cast<uint2*>(d.m + i0) = enc8<kE4M3, MCHECK>(m);
-        *reinterpret_cast<uint4*>(d.v + i0) = f_to_h8(v);
-        const uint4 wn = f_to_h8(w);
-        *reinterpret_cast<uint4*>(d.w + i0) = wn;
+        *reinterpret_cast<uint2*>(d.m + i0) =
+            make_uint2(mo[0] | (mo[1] << 16), mo[2] | (mo[3] << 16));
+        *reinterpret_cast<uint4*>(d.v + i0) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+        *reinterpret_cast<uint4*>(d.w + i0) = make_uint4(wo[0], wo[1], wo[2], wo[3]);
         if (O3) {
-          hmax = __vmaxu2(hmax, wn.x & 0x7FFF7FFFu);
-          hmax = __vmaxu2(hmax, wn.y & 0x7FFF7FFFu);
-          hmax = __vmaxu2(hmax, wn.z & 0x7FFF7FFFu);
-          hmax = __vmaxu2(hmax, wn.w & 0x7FFF7FFFu);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) hmax = __vmaxu2(hmax, wo[j] & 0x7FFF7FFFu);
         }
       }
     } else {
 #pragma unroll 1
-      for (int k = 0; k < kUpdGroups; ++k) {
-        const int64_t i0 = base + k * (kThreads * kGroup) + tid * kGroup;
+      for (int q = 0; q < kUpdGroups; ++q) {
+        const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
         for (int j = 0; j < kGroup; ++j) {
           const int64_t i = i0 + j;
           if (i >= end) break;
-          const float gd = dec2<GF>(d.g[i]).x;
-          const float g = __fmul_rn(__fmul_rn(gd, ginv), s.ils);
-          const float md = dec2<kE4M3>(d.m[i]).x;
-          float m, v, w;
-          adamw1(g, md, minv, h_to_f(d.v[i]), h_to_f(d.w[i]), s, m, v, w);
+          const float g = __fmul_rn(dec2<GF>(d.g[i]).x, k);
+          const float m = m_new1(dec2<kE4M3>(d.m[i]).x, minv, g, s);
+          float v, w;
+          adamw1(g, m, h_to_f(d.v[i]), h_to_f(d.w[i]), s, v, w);
           const float mt = __fmul_rn(m, msc);
           d.m[i] = (uint8_t)(MCHECK ? enc1_checked<kE4M3>(mt)
                                     : (enc2<kE4M3>(mt, 0.0f) & 0xFFu));
@@ -232,27 +275,27 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
 template <int GF, bool O3>
 __device__ __forceinline__ void update_dispatch2(const StepDesc& d,
                                                  int64_t begin, int64_t end,
-                                                 float ginv, float minv,
-                                                 float msc, bool mcheck,
+                                                 float k, float minv, float msc,
+                                                 bool mcheck,
                                                  const StepScalars& s,
                                                  uint32_t& hmax) {
   if (mcheck)
-    thread_update<GF, O3, true>(d, begin, end, ginv, minv, msc, s, hmax);
+    thread_update<GF, O3, true>(d, begin, end, k, minv, msc, s, hmax);
   else
-    thread_update<GF, O3, false>(d, begin, end, ginv, minv, msc, s, hmax);
+    thread_update<GF, O3, false>(d, begin, end, k, minv, msc, s, hmax);
 }
 
 template <int GF>
 __device__ __forceinline__ void update_dispatch(const StepDesc& d,
                                                 int64_t begin, int64_t end,
-                                                float ginv, float minv,
-                                                float msc, bool mcheck,
+                                                float k, float minv, float msc,
+                                                bool mcheck,
                                                 const StepScalars& s,
                                                 uint32_t& hmax) {
-  if (d.w8 != nullptr)
-    update_dispatch2<GF, true>(d, begin, end, ginv, minv, msc, mcheck, s, hmax);
+  if (d.o3)
+    update_dispatch2<GF, true>(d, begin, end, k, minv, msc, mcheck, s, hmax);
   else
-    update_dispatch2<GF, false>(d, begin, end, ginv, minv, msc, mcheck, s, hmax);
+    update_dispatch2<GF, false>(d, begin, end, k, minv, msc, mcheck, s, hmax);
 }
 
 __device__ __forceinline__ bool found_set(const StepScratch& sc, uint32_t epoch) {
@@ -260,7 +303,9 @@ __device__ __forceinline__ bool found_set(const StepScratch& sc, uint32_t epoch)
          slot_tag(epoch, 1u);
 }
 
-__global__ void __launch_bounds__(kThreads)
+// Several resident CTAs per SM keep enough warps to hide the latency of the
+// square root and division sequences.
+__global__ void __launch_bounds__(kThreads, FP8OPT_UPD_MIN_BLOCKS)
 step_update_kernel(const StepDesc* __restrict__ descs,
                    const Chunk* __restrict__ chunks, uint32_t nchunks,
                    StepScratch sc, StepScalars s, uint32_t epoch,
@@ -273,7 +318,7 @@ step_update_kernel(const StepDesc* __restrict__ descs,
   for (uint32_t r = blockIdx.x; r < nchunks; r += gridDim.x) {
     const Chunk ch = chunks[nchunks - 1 - r];
     const StepDesc d = descs[ch.tensor];
-    const float ginv = __frcp_rn(*d.g_scale);
+    const float k = __fdiv_rn(s.ils, *d.g_scale);
     const float minv = __frcp_rn(sc.old_m_scale[ch.tensor]);
     const uint32_t am = slot_value(sc.amax_m[ch.tensor], epoch);
     const float msc = scale_from_amax_bits(am, 448.0f);
@@ -283,10 +328,10 @@ step_update_kernel(const StepDesc* __restrict__ descs,
     const bool mcheck = am >= 0x7F800000u;
     uint32_t hmax = 0;
     if (d.g_fmt == kE4M3)
-      update_dispatch<kE4M3>(d, begin, end, ginv, minv, msc, mcheck, s, hmax);
+      update_dispatch<kE4M3>(d, begin, end, k, minv, msc, mcheck, s, hmax);
     else
-      update_dispatch<kE5M2>(d, begin, end, ginv, minv, msc, mcheck, s, hmax);
-    if (d.w8 != nullptr) {   // uniform over the CTA
+      update_dispatch<kE5M2>(d, begin, end, k, minv, msc, mcheck, s, hmax);
+    if (d.o3) {   // uniform over the CTA
       uint32_t h = max(hmax & 0xFFFFu, hmax >> 16);
       h = block_max_u32(h, red);
       if (threadIdx.x == 0 && h != 0) {
@@ -303,28 +348,33 @@ step_update_kernel(const StepDesc* __restrict__ descs,
 template <bool CHECKED>
 __device__ void thread_w8(const StepDesc& d, int64_t begin, int64_t end,
                           float scale) {
-  constexpr int64_t kTile = (int64_t)kThreads * kGroup * kUpdGroups;
+  constexpr int64_t kTile = (int64_t)kThreads * kGroup * kW8Groups;
   const int tid = threadIdx.x;
   const bool vec = d.vec_ok != 0;
+  const float2 sc2 = splat2(scale);
   for (int64_t base = begin; base < end; base += kTile) {
     if (vec && base + kTile <= end) {
-      uint4 wh[kUpdGroups];
+      uint4 wh[kW8Groups];
 #pragma unroll
-      for (int k = 0; k < kUpdGroups; ++k)
-        wh[k] = ld_once4(d.w + base + k * (kThreads * kGroup) + tid * kGroup);
+      for (int q = 0; q < kW8Groups; ++q)
+        wh[q] = ld_once4(d.w + base + q * (kThreads * kGroup) + tid * kGroup);
 #pragma unroll
-      for (int k = 0; k < kUpdGroups; ++k) {
-        float x[8];
-        h8_to_f(wh[k], x);
+      for (int q = 0; q < kW8Groups; ++q) {
+        uint32_t o[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) x[j] = __fmul_rn(x[j], scale);
-        const int64_t i0 = base + k * (kThreads * kGroup) + tid * kGroup;
-        *reinterpret_cast<uint2*>(d.w8 + i0) = enc8<kE4M3, CHECKED>(x);
+        for (int j = 0; j < 4; ++j) {
+          const float2 t = mul2(h2_to_f2(half_pair(wh[q], j)), sc2);
+          o[j] = CHECKED ? (enc1_checked<kE4M3>(t.x) | (enc1_checked<kE4M3>(t.y) << 8))
+                         : enc2<kE4M3>(t.x, t.y);
+        }
+        const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
+        *reinterpret_cast<uint2*>(d.w8 + i0) =
+            make_uint2(o[0] | (o[1] << 16), o[2] | (o[3] << 16));
       }
     } else {
 #pragma unroll 1
-      for (int k = 0; k < kUpdGroups; ++k) {
-        const int64_t i0 = base + k * (kThreads * kGroup) + tid * kGroup;
+      for (int q = 0; q < kW8Groups; ++q) {
+        const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
         for (int j = 0; j < kGroup; ++j) {
           const int64_t i = i0 + j;
           if (i >= end) break;

@@ -69,7 +69,8 @@ extern "C" {
 /* Status codes. */
 #define FP8OPT_OK               0
 #define FP8OPT_ERR_ARG         (-1)  /* null pointer, n < 0, numel < 0, step < 1,
-                                        incomplete O3 record */
+                                        nonzero reserved field, incomplete O3
+                                        record */
 #define FP8OPT_ERR_UNSUPPORTED (-2)  /* unknown format or element type */
 #define FP8OPT_ERR_CUDA        (-4)  /* a CUDA call failed; see fp8opt_last_error */
 
@@ -101,8 +102,9 @@ typedef struct {
  */
 FP8OPT_API int fp8_cast_scaled(const fp8opt_cast_item *items, int n, int fmt, void *stream);
 
-/* One tensor of the AdamW step.  O2 when w8 == NULL; O3 when w8, w8_scale and
- * w8_amax are all set. */
+/* One tensor of the AdamW step.  O2 when w8, w8_scale and w8_amax are all
+ * NULL; O3 when w8_scale and w8_amax are set, with w8 set too unless numel is
+ * 0 (an empty tensor's buffer may have a NULL address). */
 typedef struct {
     int64_t numel;         /* >= 0 */
     const uint8_t *g;      /* numel gradient codes (format g_fmt), as written by
@@ -124,13 +126,17 @@ typedef struct {
  * second moment (MS-AMP O2), with FP16 master and FP8 weight copy for O3
  * records, and the GradScaler inf/NaN skip.
  *
- * Per element, in fp32 with each product and sum rounded on its own:
- *   g = decode(g_code) * (1 / g_scale);  g = g * inv_loss_scale
- *   m = beta1 * decode(m_code) * (1 / m_scale_old) + (1 - beta1) * g
- *   v = beta2 * v_old + (1 - beta2) * (g * g)
- *   w = w_old * (1 - lr * wd) - lr * ((m / bc1) / (sqrt(v) / sqrt(bc2) + eps))
- * with bc1 = 1 - beta1^step and bc2 = 1 - beta2^step evaluated in double and
- * rounded to fp32 (sqrt(bc2) from the double).  The first moment is stored as
+ * Per element, in fp32, each operation rounded once (fma: product and sum
+ * rounded once together), in this order:
+ *   g = decode(g_code) * k,               k = inv_loss_scale / g_scale
+ *   m = fma(beta1, decode(m_code) * (1 / m_scale_old), (1 - beta1) * g)
+ *   v = fma(beta2, v_old, (1 - beta2) * (g * g))
+ *   u = m / fma(sqrt(v), inv_sbc2, eps)
+ *   w = fma(-step_size, u, w_old * (1 - lr * wd))
+ * with step_size = lr / (1 - beta1^step) and inv_sbc2 = 1 / sqrt(1 -
+ * beta2^step) evaluated in double and rounded to fp32 once: torch.optim.AdamW's
+ * update (decoupled decay, eps after the bias-corrected root) with the bias
+ * corrections folded into two scalars.  The first moment is stored as
  * E4M3 with the new scale 448 / amax(m) of this step; v and w are stored as
  * FP16 (round to nearest even, overflow to inf).  For O3 records, the FP16
  * master's amax gives w8_scale = 448 / w8_amax and w8 = encode(master *

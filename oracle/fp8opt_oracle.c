@@ -24,10 +24,15 @@
  *     zero or not finite, or when the quotient is not finite.
  *   - amax orders NaN above +inf above every finite |x|; a NaN amax is
  *     returned as the quiet NaN 0x7FC00000.
- *   - The AdamW update follows torch.optim.AdamW (decoupled weight decay, eps
- *     added after the bias-corrected square root), in fp32 with every product
- *     and sum rounded on its own (no fused multiply-add), in the order written
- *     in oracle_adamw_step below.  GradScaler order: dequantize, then unscale.
+ *   - The AdamW update is torch.optim.AdamW's (decoupled weight decay applied
+ *     as w * (1 - lr * wd), eps added after the bias-corrected square root),
+ *     evaluated in fp32 in the order written in oracle_adamw_step below.  The
+ *     bias corrections enter as two per-call scalars computed in double and
+ *     rounded once: step_size = lr / (1 - beta1^t) and inv_sbc2 =
+ *     1 / sqrt(1 - beta2^t).  Dequantization and the GradScaler unscale are
+ *     one per-tensor factor k = inv_loss_scale / g_scale.  Where the order
+ *     below writes fmaf, the product and sum are rounded once (IEEE fused
+ *     multiply-add); every other product and sum is rounded on its own.
  *   - found_inf is set when any unscaled gradient element is not finite; then
  *     no state element changes.
  *   - The first moment is re-encoded from the fp32 value of this step, with a
@@ -251,9 +256,11 @@ typedef struct {
     float *w8_amax;        /* O3 only: amax of the FP16 master (out) */
 } oracle_param;
 
-/* Per-call scalars, computed on the host in double and rounded to float. */
+/* Per-call scalars.  The bias corrections 1 - beta^t are evaluated in double
+ * and enter only through step_size = lr / bc1 and inv_sbc2 = 1 / sqrt(bc2),
+ * each rounded to float once. */
 typedef struct {
-    float bc1, bc2, sbc2, omb1, omb2, decay;
+    float step_size, inv_sbc2, omb1, omb2, decay;
 } or_scalars;
 
 static or_scalars or_make_scalars(float lr, float beta1, float beta2,
@@ -262,31 +269,34 @@ static or_scalars or_make_scalars(float lr, float beta1, float beta2,
     or_scalars s;
     double bc1 = 1.0 - pow((double)beta1, (double)step);
     double bc2 = 1.0 - pow((double)beta2, (double)step);
-    s.bc1 = (float)bc1;
-    s.bc2 = (float)bc2;
-    s.sbc2 = (float)sqrt(bc2);
+    s.step_size = (float)((double)lr / bc1);
+    s.inv_sbc2 = (float)(1.0 / sqrt(bc2));
     s.omb1 = 1.0f - beta1;
     s.omb2 = 1.0f - beta2;
     s.decay = 1.0f - lr * wd;
     return s;
 }
 
-/* Unscaled gradient: dequantize (code value times 1/g_scale), then multiply by
- * the GradScaler's inverse loss scale. */
-static float or_grad(const oracle_param *p, float ginv, float ils, int64_t i)
+/* The per-tensor factor that dequantizes a gradient code and undoes the loss
+ * scale at once: k = inv_loss_scale / g_scale. */
+static float or_grad_factor(const oracle_param *p, float inv_loss_scale)
 {
-    float g = oracle_fp8_decode(p->g[i], p->g_fmt) * ginv;
-    return g * ils;
+    return inv_loss_scale / p->g_scale;
 }
 
-/* New first moment in fp32: beta1 * m_prev + (1 - beta1) * g. */
+/* Unscaled gradient: the code's value times k. */
+static float or_grad(const oracle_param *p, float k, int64_t i)
+{
+    return oracle_fp8_decode(p->g[i], p->g_fmt) * k;
+}
+
+/* New first moment in fp32: beta1 * m_prev + (1 - beta1) * g, with the
+ * previous moment dequantized as code value times 1 / m_scale. */
 static float or_m_new(const oracle_param *p, float minv, float g, float beta1,
                       const or_scalars *s, int64_t i)
 {
     float mp = oracle_fp8_decode(p->m[i], OR_E4M3) * minv;
-    float a = beta1 * mp;
-    float b = s->omb1 * g;
-    return a + b;
+    return fmaf(beta1, mp, s->omb1 * g);
 }
 
 /* One multi-tensor AdamW step with FP8 first moment and FP16 second moment.
@@ -301,35 +311,34 @@ int oracle_adamw_step(const oracle_param *p, int n, float lr, float beta1,
 
     /* GradScaler check over every tensor before any state changes. */
     for (int t = 0; t < n; ++t) {
-        float ginv = 1.0f / p[t].g_scale;
+        float k = or_grad_factor(&p[t], inv_loss_scale);
         for (int64_t i = 0; i < p[t].numel; ++i)
-            if (!isfinite(or_grad(&p[t], ginv, inv_loss_scale, i))) return 1;
+            if (!isfinite(or_grad(&p[t], k, i))) return 1;
     }
 
     for (int t = 0; t < n; ++t) {
         const oracle_param *q = &p[t];
-        float ginv = 1.0f / q->g_scale;
+        float k = or_grad_factor(q, inv_loss_scale);
         float minv = 1.0f / *q->m_scale;
 
         /* amax of this step's fp32 first moment -> its new scale. */
         or_amax am = {0, 0, 0.0f};
         for (int64_t i = 0; i < q->numel; ++i) {
-            float g = or_grad(q, ginv, inv_loss_scale, i);
+            float g = or_grad(q, k, i);
             or_amax_add(&am, or_m_new(q, minv, g, beta1, &s, i));
         }
         float m_scale_new = oracle_scale_from_amax(or_amax_value(&am), OR_E4M3);
 
         or_amax aw = {0, 0, 0.0f};
         for (int64_t i = 0; i < q->numel; ++i) {
-            float g = or_grad(q, ginv, inv_loss_scale, i);
+            float g = or_grad(q, k, i);
             float m = or_m_new(q, minv, g, beta1, &s, i);
             float vp = oracle_f16_to_f32(q->v[i]);
             float wp = oracle_f16_to_f32(q->w[i]);
-            float gg = g * g;
-            float v = beta2 * vp + s.omb2 * gg;
-            float denom = sqrtf(v) / s.sbc2 + eps;
-            float upd = (m / s.bc1) / denom;
-            float w = wp * s.decay - lr * upd;
+            float v = fmaf(beta2, vp, s.omb2 * (g * g));
+            float denom = fmaf(sqrtf(v), s.inv_sbc2, eps);
+            float upd = m / denom;
+            float w = fmaf(-s.step_size, upd, wp * s.decay);
             q->m[i] = oracle_fp8_encode(m * m_scale_new, OR_E4M3);
             q->v[i] = oracle_f32_to_f16(v);
             q->w[i] = oracle_f32_to_f16(w);

@@ -98,9 +98,14 @@ def test_argument_errors_need_no_gpu(lib):
     p[0].g_fmt = 0
     dummy = C.c_float(1.0)
     p[0].g_scale = p[0].m_scale = C.addressof(dummy)   # pointers never read
-    p[0].w8 = 0x1000                                    # incomplete O3 record
+    p[0].w8 = 0x1000                                    # w8 without its scales
     assert L.fp8_adamw_step(p, 1, *args, 1, 1.0, None, None, None) == lib.ERR_ARG
-    assert "O3" in L.fp8opt_last_error().decode()
+    assert "w8" in L.fp8opt_last_error().decode()
+    p[0].w8, p[0].w8_scale, p[0].numel = None, C.addressof(dummy), 4
+    p[0].g = p[0].m = p[0].v = p[0].w = 0x1000          # never dereferenced
+    assert L.fp8_adamw_step(p, 1, *args, 1, 1.0, None, None, None) == lib.ERR_ARG
+    assert "O3" in L.fp8opt_last_error().decode()       # incomplete O3 record
+    p[0].numel = 0
     assert L.fp8_adamw_step(p, 0, *args, 1, 1.0, C.byref(f), None, None) == lib.OK
     assert f.value == 0
 

@@ -258,3 +258,16 @@ def test_timing_records_each_kernel(bo):
     for k in bo.KERNELS:
         n, ms = bo.timing_read(k)
         assert n == 2 and ms > 0.0, k
+
+
+def test_workspace_reuse_across_list_lengths(bo):
+    """A short step list, then a longer cast and step on the same stream: the
+    longer calls' per-tensor slots must not see the shorter call's scratch."""
+    small = synth.tiny()
+    s_states = fresh_states(small.weights(), o3=False)
+    codes, _, scale = oracle_cast(small.grads(1), E4M3)
+    set_grads(s_states, codes, scale)
+    GpuState([s.copy() for s in s_states]).step(small, 1)
+    wl = synth.o2_6p7b_tail(n_layer=1, d=64, ffn=256, vocab=300, ctx=32, n_tail=20)
+    states = fresh_states(wl.weights(), o3=False)
+    lockstep(bo, wl, states, 1, 2)
