@@ -253,6 +253,11 @@ int current_device_and_info(int* dev, DeviceInfo** info) {
 }
 
 }  // namespace
+
+// Records the detail fp8opt_last_error() returns, for entry points defined
+// in other translation units.
+int record_error(int status, const char* what) { return fail(status, what); }
+
 }  // namespace fp8opt
 
 using namespace fp8opt;
@@ -463,6 +468,7 @@ extern "C" const char* fp8opt_strerror(int status) {
     case FP8OPT_ERR_ARG: return "invalid argument";
     case FP8OPT_ERR_UNSUPPORTED: return "unsupported format or element type";
     case FP8OPT_ERR_CUDA: return "CUDA error";
+    case FP8OPT_ERR_LIMIT: return "size above a fixed maximum";
     default: return "unknown status";
   }
 }

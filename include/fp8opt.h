@@ -73,6 +73,8 @@ extern "C" {
                                         record */
 #define FP8OPT_ERR_UNSUPPORTED (-2)  /* unknown format or element type */
 #define FP8OPT_ERR_CUDA        (-4)  /* a CUDA call failed; see fp8opt_last_error */
+#define FP8OPT_ERR_LIMIT       (-5)  /* a size above a fixed maximum (the
+                                        no-allocation entry point's limits) */
 
 /* One tensor of a scaled cast. */
 typedef struct {
@@ -157,6 +159,35 @@ FP8OPT_API int fp8_adamw_step(const fp8opt_param *params, int n, float lr, float
                    float beta2, float eps, float wd, int64_t step,
                    float inv_loss_scale, int *found_inf,
                    uint32_t *found_inf_dev, void *stream);
+
+/* Limits of fp8_cast_scaled_noalloc: tensors per call, and chunks of 32768
+ * elements per call (an empty tensor counts as one chunk). */
+#define FP8OPT_NOALLOC_MAX_TENSORS 1024
+#define FP8OPT_NOALLOC_MAX_CHUNKS  65536
+
+/*
+ * fp8_cast_scaled_noalloc: fp8_cast_scaled for callers that must not allocate
+ * device memory.  No counterpart in the MS-AMP pages: it exists for callers
+ * such as code running under CUDA graph capture, runtimes whose pool allocator
+ * owns all device memory, or services that must not stall on or fail from an
+ * allocation mid-step.  fp8_cast_scaled allocates its workspace on first use;
+ * this entry point instead keeps its tensor table, chunk table and amax slots
+ * in one fixed array compiled into the library (about 0.6 MB per device,
+ * present on every device that loads the library, until the process exits),
+ * and calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Same arguments, same results and same errors as fp8_cast_scaled, plus
+ * FP8OPT_ERR_LIMIT (nothing launched) when n exceeds
+ * FP8OPT_NOALLOC_MAX_TENSORS or the list needs more than
+ * FP8OPT_NOALLOC_MAX_CHUNKS chunks.  The first call on each device sets the
+ * entry point up for that device (it looks up the array's device address);
+ * make that first call before any stream capture.  All calls on a device share
+ * the one array, which keeps the previous call's contents; each call clears
+ * what it needs zeroed, but calls whose GPU work overlaps (on different
+ * streams, or from different host threads) race on the array: order them.
+ */
+FP8OPT_API int fp8_cast_scaled_noalloc(const fp8opt_cast_item *items, int n,
+                                       int fmt, void *stream);
 
 /* Text of a status code (static storage). */
 FP8OPT_API const char *fp8opt_strerror(int status);
