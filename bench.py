@@ -57,6 +57,10 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--n-layer", type=int, default=None,
+                   help="override the workload's layer count (profiling cases)")
+    p.add_argument("--vocab", type=int, default=None,
+                   help="override the workload's vocabulary (profiling cases)")
     return p.parse_args()
 
 
@@ -249,6 +253,37 @@ def build_state(wl, device):
     return params, grads, flat, opt
 
 
+KERNEL_SOURCES = ("bit_optimizer_gb300/csrc/step_kernels.cu",
+                  "bit_optimizer_gb300/csrc/fp8opt_internal.cuh")
+TRAFFIC_SUMMARY = "profiles/step_update_o2_1layer.md"
+
+
+def kernel_source_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def update_traffic_per_param():
+    """DRAM bytes per parameter of one step_update launch from the committed
+    ncu summary, or None when the kernel source changed since the capture."""
+    try:
+        text = open(os.path.join(ROOT, TRAFFIC_SUMMARY)).read()
+    except OSError:
+        return None
+    fields = dict(line.split(":", 1) for line in text.splitlines()
+                  if line.startswith(("traffic_bytes_per_param:", "source_digest:")))
+    if fields.get("source_digest", "").strip() != kernel_source_digest():
+        return None
+    try:
+        return float(fields["traffic_bytes_per_param"])
+    except (KeyError, ValueError):
+        return None
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -314,6 +349,7 @@ def run_ours(args, wl):
     upd_n, upd_ms = kern["step_update"]
     upd_avg_ms = upd_ms / max(upd_n, 1)
     achieved = UPDATE_BYTES * n_params / (upd_avg_ms * 1e-3) / 1e9
+    tpp = update_traffic_per_param()
 
     e2e = None
     if not args.no_e2e:
@@ -362,7 +398,8 @@ def run_ours(args, wl):
             "hbm_frac_of_peak": bytes_step / (ms * 1e-3) / 1e9 / peak,
             "roofline": {"bound": "hbm", "kernel": "step_update",
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak,
+                         "traffic": (None if tpp is None else tpp * n_params),
                          "peak_source": f"{peak_kind} hbm_gbs",
                          "bytes_per_launch": UPDATE_BYTES * n_params,
                          "avg_launch_ms": upd_avg_ms},
@@ -382,7 +419,9 @@ def main():
     args = parse()
     import dataclasses
     import synth
-    wl = synth.WORKLOADS[args.workload]()
+    over = {k: v for k, v in (("n_layer", args.n_layer), ("vocab", args.vocab))
+            if v is not None}
+    wl = synth.WORKLOADS[args.workload](**over)
     # a timed step must be a full update: a workload that seeds an inf (the
     # GradScaler skip case) is timed with that element cleared
     wl = dataclasses.replace(wl, inf_site=None)
