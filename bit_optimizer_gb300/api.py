@@ -31,7 +31,7 @@ FMTS = {"e4m3": E4M3, "e5m2": E5M2, E4M3: E4M3, E5M2: E5M2}
 _DT = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
 
 __all__ = ["fp8_cast_scaled", "fp8_adamw_step", "CastPlan", "AdamWPlan",
-           "Fp8AdamW", "arena_views", "FMTS"]
+           "CastStepPlan", "Fp8AdamW", "arena_views", "FMTS"]
 
 
 def _fmt(f) -> int:
@@ -210,6 +210,34 @@ def fp8_adamw_step(g, g_scale, m, m_scale, v, w, lr, beta1, beta2, eps, wd,
                 sync, stream)
 
 
+class CastStepPlan:
+    """A marshalled ``fp8_cast_adamw_step``: the cast of ``cast`` and the step
+    of ``step`` in one call (one pass fewer over memory).  The cast plan's
+    codes and scales must be the step plan's ``g`` and ``g_scale``, with the
+    same format; the library checks this and raises otherwise."""
+
+    def __init__(self, cast: CastPlan, step: AdamWPlan):
+        if cast.n != step.n:
+            raise ValueError("cast and step plans differ in length")
+        self.cast = cast
+        self.step_plan = step
+        self._found = C.c_int(0)
+
+    def __call__(self, lr, beta1, beta2, eps, wd, step, inv_loss_scale=1.0,
+                 found_inf_dev: Optional[torch.Tensor] = None, sync=True,
+                 stream=None) -> Optional[int]:
+        fdev = None
+        if found_inf_dev is not None:
+            _cuda(found_inf_dev, "found_inf_dev")
+            fdev = found_inf_dev.data_ptr()
+        fptr = C.byref(self._found) if sync else None
+        check(load().fp8_cast_adamw_step(
+            self.cast._items, self.step_plan._params, self.cast.n, self.cast.fmt,
+            lr, beta1, beta2, eps, wd, int(step), inv_loss_scale, fptr, fdev,
+            _stream_ptr(stream)))
+        return self._found.value if sync else None
+
+
 # -------------------------------------------------------------- optimizer
 
 class Fp8AdamW:
@@ -227,7 +255,7 @@ class Fp8AdamW:
 
     def __init__(self, params: Sequence[torch.Tensor], lr=1e-3,
                  betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01, level="O2",
-                 grad_fmt="e4m3"):
+                 grad_fmt="e4m3", fused=True):
         if level not in ("O2", "O3"):
             raise ValueError("level must be 'O2' or 'O3'")
         self.params = list(params)
@@ -238,6 +266,7 @@ class Fp8AdamW:
         self.lr, (self.beta1, self.beta2) = lr, betas
         self.eps, self.wd = eps, weight_decay
         self.level, self.grad_fmt = level, grad_fmt
+        self.fused = fused        # one fp8_cast_adamw_step call per step
         self.step_count = 0
         n = len(self.params)
         dev = self.params[0].device if n else torch.device("cuda")
@@ -260,6 +289,7 @@ class Fp8AdamW:
                                grad_fmt)
         self._cast_key = None
         self._cast = None
+        self._cast_step = None
 
     def _cast_plan(self, grads: Sequence[torch.Tensor]) -> CastPlan:
         key = tuple((g.data_ptr(), g.numel(), g.dtype) for g in grads)
@@ -267,6 +297,7 @@ class Fp8AdamW:
             flat = [g.view(-1) for g in grads]
             self._cast = CastPlan(flat, self.g_codes, self.g_amax, self.g_scale,
                                   self.grad_fmt)
+            self._cast_step = CastStepPlan(self._cast, self._plan)
             self._cast_key = key
         return self._cast
 
@@ -277,10 +308,16 @@ class Fp8AdamW:
         unconditionally and the caller reads found_inf_dev)."""
         if len(grads) != len(self.params):
             raise ValueError("one gradient per parameter")
-        self._cast_plan(grads)(stream)
+        cast = self._cast_plan(grads)
         t = self.step_count + 1
-        found = self._plan(self.lr, self.beta1, self.beta2, self.eps, self.wd, t,
-                           inv_loss_scale, found_inf_dev, sync, stream)
+        if self.fused:
+            found = self._cast_step(self.lr, self.beta1, self.beta2, self.eps,
+                                    self.wd, t, inv_loss_scale, found_inf_dev,
+                                    sync, stream)
+        else:
+            cast(stream)
+            found = self._plan(self.lr, self.beta1, self.beta2, self.eps, self.wd,
+                               t, inv_loss_scale, found_inf_dev, sync, stream)
         if not sync or found == 0:
             self.step_count = t
         return found

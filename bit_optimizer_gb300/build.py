@@ -18,7 +18,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libfp8opt.so")
-SOURCES = ["api.cu", "cast_kernels.cu", "step_kernels.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "cast_kernels.cu", "step_kernels.cu", "fused_kernels.cu",
+           "noalloc.cu"]
 DEPS = ["fp8opt_internal.cuh", os.path.join("..", "..", "include", "fp8opt.h")]
 
 NVCC = os.environ.get("NVCC", "nvcc")

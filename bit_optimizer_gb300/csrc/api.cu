@@ -27,6 +27,15 @@ cudaError_t launch_step(const StepDesc* descs, const Chunk* chunks,
                         uint32_t* found_dev, int grid_amax, int grid_update,
                         int grid_w8, cudaStream_t stream, LaunchMark mark);
 cudaError_t step_occupancy(int* amax_per_sm, int* update_per_sm, int* w8_per_sm);
+cudaError_t launch_cast_step(const CastDesc* cdescs, const StepDesc* sdescs,
+                             const Chunk* chunks, uint32_t nchunks,
+                             const Chunk* chunks_o3, uint32_t nchunks_o3,
+                             unsigned long long* gslots, const StepScratch& sc,
+                             const StepScalars& s, uint32_t epoch, int fmt,
+                             uint32_t* found_dev, int grid_amax, int grid_fused,
+                             int grid_update, int grid_w8, cudaStream_t stream,
+                             LaunchMark mark);
+cudaError_t cast_step_occupancy(int* per_sm);
 
 namespace {
 
@@ -72,6 +81,7 @@ struct DeviceInfo {
   int sms = 0;
   int cast_amax = 0, cast_encode = 0;          // persistent grid sizes
   int step_amax = 0, step_update = 0, step_w8 = 0;
+  int cast_step = 0;
 };
 
 // Per-(device, stream) state.  The slot region holds only epoch-tagged
@@ -129,6 +139,8 @@ cudaError_t device_info(int dev, DeviceInfo** out) {
   info.step_amax = info.sms * (a > 0 ? a : 1);
   info.step_update = info.sms * (b > 0 ? b : 1);
   info.step_w8 = info.sms * (c > 0 ? c : 1);
+  if ((e = cast_step_occupancy(&a)) != cudaSuccess) return e;
+  info.cast_step = info.sms * (a > 0 ? a : 1);
   *out = &(g_dev[dev] = info);
   return cudaSuccess;
 }
@@ -143,10 +155,11 @@ Workspace* workspace(int dev, cudaStream_t s) {
   return w;
 }
 
-// Slots for n tensors, zeroed when (re)allocated or when the epoch wraps.
-cudaError_t prepare_slots(Workspace* ws, size_t n, cudaStream_t stream,
+// `words` tagged slots for this call, zeroed when (re)allocated or when the
+// epoch wraps; returns the call's epoch.
+cudaError_t prepare_slots(Workspace* ws, size_t words, cudaStream_t stream,
                           uint32_t* epoch_out) {
-  const size_t bytes = (2 * n + 1) * sizeof(unsigned long long);
+  const size_t bytes = words * sizeof(unsigned long long);
   bool fresh = false;
   if (bytes > ws->slots.cap) {
     cudaError_t e = ws->slots.reserve(bytes);
@@ -169,7 +182,8 @@ cudaError_t prepare_slots(Workspace* ws, size_t n, cudaStream_t stream,
 // ------------------------------------------------------- per-kernel timing
 
 const char* const kKernelNames[kNumKernels] = {
-    "cast_amax", "cast_encode", "step_amax", "step_update", "step_w8"};
+    "cast_amax", "cast_encode", "step_amax", "step_update", "step_w8",
+    "cast_step_amax"};
 
 struct Timing {
   bool on = false;
@@ -262,87 +276,36 @@ int record_error(int status, const char* what) { return fail(status, what); }
 
 using namespace fp8opt;
 
-extern "C" int fp8_cast_scaled(const fp8opt_cast_item* items, int n, int fmt,
-                               void* stream_ptr) {
+namespace fp8opt {
+namespace {
+
+int check_cast_args(const char* fn, const fp8opt_cast_item* items, int n,
+                    int fmt) {
   if (n < 0 || (n > 0 && items == nullptr))
-    return fail(FP8OPT_ERR_ARG, "fp8_cast_scaled: n < 0 or items is NULL");
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": n < 0 or items is NULL");
   if (fmt != FP8OPT_E4M3 && fmt != FP8OPT_E5M2)
-    return fail(FP8OPT_ERR_UNSUPPORTED, "fp8_cast_scaled: unknown format");
+    return fail(FP8OPT_ERR_UNSUPPORTED, std::string(fn) + ": unknown format");
   for (int i = 0; i < n; ++i) {
     const fp8opt_cast_item& it = items[i];
+    const std::string at = std::string(fn) + ": item " + std::to_string(i);
     if (it.dtype != FP8OPT_F32 && it.dtype != FP8OPT_BF16 && it.dtype != FP8OPT_F16)
-      return fail(FP8OPT_ERR_UNSUPPORTED,
-                  "fp8_cast_scaled: item " + std::to_string(i) + ": unknown dtype");
+      return fail(FP8OPT_ERR_UNSUPPORTED, at + ": unknown dtype");
     if (it.numel < 0 || it.reserved != 0 || it.amax == nullptr ||
         it.scale == nullptr ||
         (it.numel > 0 && (it.src == nullptr || it.codes == nullptr)))
-      return fail(FP8OPT_ERR_ARG, "fp8_cast_scaled: item " + std::to_string(i) +
-                                      ": bad numel, reserved field or NULL pointer");
+      return fail(FP8OPT_ERR_ARG, at + ": bad numel, reserved field or NULL pointer");
   }
-  if (n == 0) return FP8OPT_OK;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-
-  std::lock_guard<std::mutex> lock(g_mu);
-  int dev = 0;
-  DeviceInfo* info = nullptr;
-  int st = current_device_and_info(&dev, &info);
-  if (st != FP8OPT_OK) return st;
-  Workspace* ws = workspace(dev, stream);
-  cudaError_t e;
-
-  if (!ws->have_cast || !same_list(ws->cast_key, items, n)) {
-    std::vector<CastDesc> descs((size_t)n);
-    std::vector<Chunk> chunks;
-    size_t total = 0;
-    for (int i = 0; i < n; ++i) total += chunks_of(items[i].numel);
-    if (total > 0xFFFFFFFFull)
-      return fail(FP8OPT_ERR_ARG, "fp8_cast_scaled: list too long");
-    chunks.reserve(total);
-    for (int i = 0; i < n; ++i) {
-      const fp8opt_cast_item& it = items[i];
-      CastDesc& d = descs[(size_t)i];
-      d.src = it.src;
-      d.codes = it.codes;
-      d.amax_out = it.amax;
-      d.scale_out = it.scale;
-      d.numel = it.numel;
-      d.dtype = it.dtype;
-      d.vec_ok = aligned(it.src, 16) && aligned(it.codes, 8);
-      for (uint32_t c = 0, nc = chunks_of(it.numel); c < nc; ++c)
-        chunks.push_back(Chunk{(uint32_t)i, c});
-    }
-    ws->have_cast = false;
-    if ((e = upload(ws->cast_descs, descs.data(), descs.size() * sizeof(CastDesc),
-                    stream)) != cudaSuccess ||
-        (e = upload(ws->cast_chunks, chunks.data(), chunks.size() * sizeof(Chunk),
-                    stream)) != cudaSuccess)
-      return cuda_fail(e, "fp8_cast_scaled: table upload");
-    ws->cast_key.assign(items, items + n);
-    ws->cast_nchunks = (uint32_t)chunks.size();
-    ws->have_cast = true;
-  }
-
-  uint32_t epoch = 0;
-  if ((e = prepare_slots(ws, (size_t)n, stream, &epoch)) != cudaSuccess)
-    return cuda_fail(e, "fp8_cast_scaled: workspace");
-  e = launch_cast(static_cast<const CastDesc*>(ws->cast_descs.ptr),
-                  static_cast<const Chunk*>(ws->cast_chunks.ptr), ws->cast_nchunks,
-                  static_cast<unsigned long long*>(ws->slots.ptr), epoch, fmt,
-                  info->cast_amax, info->cast_encode, stream, launch_mark());
-  if (e != cudaSuccess) return cuda_fail(e, "fp8_cast_scaled: launch");
   return FP8OPT_OK;
 }
 
-extern "C" int fp8_adamw_step(const fp8opt_param* params, int n, float lr,
-                              float beta1, float beta2, float eps, float wd,
-                              int64_t step, float inv_loss_scale, int* found_inf,
-                              uint32_t* found_inf_dev, void* stream_ptr) {
+int check_step_args(const char* fn, const fp8opt_param* params, int n,
+                    int64_t step) {
   if (n < 0 || (n > 0 && params == nullptr))
-    return fail(FP8OPT_ERR_ARG, "fp8_adamw_step: n < 0 or params is NULL");
-  if (step < 1) return fail(FP8OPT_ERR_ARG, "fp8_adamw_step: step < 1");
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": n < 0 or params is NULL");
+  if (step < 1) return fail(FP8OPT_ERR_ARG, std::string(fn) + ": step < 1");
   for (int i = 0; i < n; ++i) {
     const fp8opt_param& p = params[i];
-    const std::string at = "fp8_adamw_step: param " + std::to_string(i);
+    const std::string at = std::string(fn) + ": param " + std::to_string(i);
     if (p.g_fmt != FP8OPT_E4M3 && p.g_fmt != FP8OPT_E5M2)
       return fail(FP8OPT_ERR_UNSUPPORTED, at + ": unknown gradient format");
     if (p.numel < 0 || p.reserved != 0 || p.g_scale == nullptr ||
@@ -357,18 +320,13 @@ extern "C" int fp8_adamw_step(const fp8opt_param* params, int n, float lr,
     if (!o3 && p.w8 != nullptr)
       return fail(FP8OPT_ERR_ARG, at + ": w8 given without w8_scale and w8_amax");
   }
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  if (n == 0) {
-    if (found_inf != nullptr) *found_inf = 0;
-    if (found_inf_dev != nullptr) {
-      cudaError_t e = cudaMemsetAsync(found_inf_dev, 0, sizeof(uint32_t), stream);
-      if (e != cudaSuccess) return cuda_fail(e, "fp8_adamw_step: found_inf_dev");
-    }
-    return FP8OPT_OK;
-  }
+  return FP8OPT_OK;
+}
 
-  // Per-call scalars: the bias corrections 1 - beta^t in double, entering
-  // only through lr / bc1 and 1 / sqrt(bc2), each rounded to fp32 once.
+// Per-call scalars: the bias corrections 1 - beta^t in double, entering only
+// through lr / bc1 and 1 / sqrt(bc2), each rounded to fp32 once.
+StepScalars make_scalars(float lr, float beta1, float beta2, float eps, float wd,
+                         int64_t step, float inv_loss_scale) {
   StepScalars s;
   const double bc1 = 1.0 - std::pow((double)beta1, (double)step);
   const double bc2 = 1.0 - std::pow((double)beta2, (double)step);
@@ -381,64 +339,170 @@ extern "C" int fp8_adamw_step(const fp8opt_param* params, int n, float lr,
   s.inv_sbc2 = (float)(1.0 / std::sqrt(bc2));
   s.decay = 1.0f - lr * wd;
   s.ils = inv_loss_scale;
+  return s;
+}
+
+// The workspace's cast tables for this item list (uploaded when the list
+// differs from the cached one).
+int ensure_cast_tables(const char* fn, Workspace* ws,
+                       const fp8opt_cast_item* items, int n,
+                       cudaStream_t stream) {
+  if (ws->have_cast && same_list(ws->cast_key, items, n)) return FP8OPT_OK;
+  std::vector<CastDesc> descs((size_t)n);
+  std::vector<Chunk> chunks;
+  size_t total = 0;
+  for (int i = 0; i < n; ++i) total += chunks_of(items[i].numel);
+  if (total > 0xFFFFFFFFull)
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": list too long");
+  chunks.reserve(total);
+  for (int i = 0; i < n; ++i) {
+    const fp8opt_cast_item& it = items[i];
+    CastDesc& d = descs[(size_t)i];
+    d.src = it.src;
+    d.codes = it.codes;
+    d.amax_out = it.amax;
+    d.scale_out = it.scale;
+    d.numel = it.numel;
+    d.dtype = it.dtype;
+    d.vec_ok = aligned(it.src, 16) && aligned(it.codes, 8);
+    for (uint32_t c = 0, nc = chunks_of(it.numel); c < nc; ++c)
+      chunks.push_back(Chunk{(uint32_t)i, c});
+  }
+  ws->have_cast = false;
+  cudaError_t e;
+  if ((e = upload(ws->cast_descs, descs.data(), descs.size() * sizeof(CastDesc),
+                  stream)) != cudaSuccess ||
+      (e = upload(ws->cast_chunks, chunks.data(), chunks.size() * sizeof(Chunk),
+                  stream)) != cudaSuccess)
+    return cuda_fail(e, (std::string(fn) + ": table upload").c_str());
+  ws->cast_key.assign(items, items + n);
+  ws->cast_nchunks = (uint32_t)chunks.size();
+  ws->have_cast = true;
+  return FP8OPT_OK;
+}
+
+// The workspace's step tables: the main chunk list, then the O3 chunks.
+int ensure_step_tables(const char* fn, Workspace* ws, const fp8opt_param* params,
+                       int n, cudaStream_t stream) {
+  if (ws->have_step && same_list(ws->step_key, params, n)) return FP8OPT_OK;
+  std::vector<StepDesc> descs((size_t)n);
+  std::vector<Chunk> chunks, chunks_o3;
+  size_t total = 0;
+  for (int i = 0; i < n; ++i) total += 2 * (size_t)chunks_of(params[i].numel);
+  if (total > 0xFFFFFFFFull)
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": list too long");
+  for (int i = 0; i < n; ++i) {
+    const fp8opt_param& p = params[i];
+    StepDesc& d = descs[(size_t)i];
+    d.g = p.g;
+    d.m = p.m;
+    d.v = p.v;
+    d.w = p.w;
+    d.w8 = p.w8;
+    d.g_scale = p.g_scale;
+    d.m_scale = p.m_scale;
+    d.w8_scale = p.w8_scale;
+    d.w8_amax = p.w8_amax;
+    d.numel = p.numel;
+    d.g_fmt = p.g_fmt;
+    d.o3 = p.w8_scale != nullptr;
+    d.vec_ok = aligned(p.g, 8) && aligned(p.m, 8) && aligned(p.v, 16) &&
+               aligned(p.w, 16) && (p.w8 == nullptr || aligned(p.w8, 8));
+    for (uint32_t c = 0, nc = chunks_of(p.numel); c < nc; ++c) {
+      chunks.push_back(Chunk{(uint32_t)i, c});
+      if (d.o3) chunks_o3.push_back(Chunk{(uint32_t)i, c});
+    }
+  }
+  const uint32_t nmain = (uint32_t)chunks.size();
+  const uint32_t no3 = (uint32_t)chunks_o3.size();
+  chunks.insert(chunks.end(), chunks_o3.begin(), chunks_o3.end());
+  ws->have_step = false;
+  cudaError_t e;
+  if ((e = upload(ws->step_descs, descs.data(), descs.size() * sizeof(StepDesc),
+                  stream)) != cudaSuccess ||
+      (e = upload(ws->step_chunks, chunks.data(), chunks.size() * sizeof(Chunk),
+                  stream)) != cudaSuccess)
+    return cuda_fail(e, (std::string(fn) + ": table upload").c_str());
+  ws->step_key.assign(params, params + n);
+  ws->step_nchunks = nmain;
+  ws->step_nchunks_o3 = no3;
+  ws->have_step = true;
+  return FP8OPT_OK;
+}
+
+// The empty-list result of a step call.
+int empty_step(const char* fn, int* found_inf, uint32_t* found_inf_dev,
+               cudaStream_t stream) {
+  if (found_inf != nullptr) *found_inf = 0;
+  if (found_inf_dev != nullptr) {
+    cudaError_t e = cudaMemsetAsync(found_inf_dev, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": found_inf_dev").c_str());
+  }
+  return FP8OPT_OK;
+}
+
+// Waits for the stream and reads this call's found_inf word.
+int read_found(const char* fn, const unsigned long long* found, uint32_t epoch,
+               cudaStream_t stream, int* out) {
+  unsigned long long tag = 0;
+  cudaError_t e = cudaMemcpyAsync(&tag, found, sizeof(tag), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": found_inf read").c_str());
+  *out = tag == (((unsigned long long)epoch << 32) | 1ull) ? 1 : 0;
+  return FP8OPT_OK;
+}
+
+}  // namespace
+}  // namespace fp8opt
+
+extern "C" int fp8_cast_scaled(const fp8opt_cast_item* items, int n, int fmt,
+                               void* stream_ptr) {
+  const char* fn = "fp8_cast_scaled";
+  int st = check_cast_args(fn, items, n, fmt);
+  if (st != FP8OPT_OK || n == 0) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0;
   DeviceInfo* info = nullptr;
-  int st = current_device_and_info(&dev, &info);
-  if (st != FP8OPT_OK) return st;
+  if ((st = current_device_and_info(&dev, &info)) != FP8OPT_OK) return st;
   Workspace* ws = workspace(dev, stream);
-  cudaError_t e;
-
-  if (!ws->have_step || !same_list(ws->step_key, params, n)) {
-    std::vector<StepDesc> descs((size_t)n);
-    std::vector<Chunk> chunks, chunks_o3;
-    size_t total = 0;
-    for (int i = 0; i < n; ++i) total += 2 * (size_t)chunks_of(params[i].numel);
-    if (total > 0xFFFFFFFFull)
-      return fail(FP8OPT_ERR_ARG, "fp8_adamw_step: list too long");
-    for (int i = 0; i < n; ++i) {
-      const fp8opt_param& p = params[i];
-      StepDesc& d = descs[(size_t)i];
-      d.g = p.g;
-      d.m = p.m;
-      d.v = p.v;
-      d.w = p.w;
-      d.w8 = p.w8;
-      d.g_scale = p.g_scale;
-      d.m_scale = p.m_scale;
-      d.w8_scale = p.w8_scale;
-      d.w8_amax = p.w8_amax;
-      d.numel = p.numel;
-      d.g_fmt = p.g_fmt;
-      d.o3 = p.w8_scale != nullptr;
-      d.vec_ok = aligned(p.g, 8) && aligned(p.m, 8) && aligned(p.v, 16) &&
-                 aligned(p.w, 16) && (p.w8 == nullptr || aligned(p.w8, 8));
-      for (uint32_t c = 0, nc = chunks_of(p.numel); c < nc; ++c) {
-        chunks.push_back(Chunk{(uint32_t)i, c});
-        if (d.o3) chunks_o3.push_back(Chunk{(uint32_t)i, c});
-      }
-    }
-    const uint32_t nmain = (uint32_t)chunks.size();
-    const uint32_t no3 = (uint32_t)chunks_o3.size();
-    chunks.insert(chunks.end(), chunks_o3.begin(), chunks_o3.end());
-    ws->have_step = false;
-    if ((e = upload(ws->step_descs, descs.data(), descs.size() * sizeof(StepDesc),
-                    stream)) != cudaSuccess ||
-        (e = upload(ws->step_chunks, chunks.data(), chunks.size() * sizeof(Chunk),
-                    stream)) != cudaSuccess)
-      return cuda_fail(e, "fp8_adamw_step: table upload");
-    ws->step_key.assign(params, params + n);
-    ws->step_nchunks = nmain;
-    ws->step_nchunks_o3 = no3;
-    ws->have_step = true;
-  }
+  if ((st = ensure_cast_tables(fn, ws, items, n, stream)) != FP8OPT_OK) return st;
 
   uint32_t epoch = 0;
-  if ((e = prepare_slots(ws, (size_t)n, stream, &epoch)) != cudaSuccess)
-    return cuda_fail(e, "fp8_adamw_step: workspace");
-  if ((e = ws->saved_scales.reserve((size_t)n * sizeof(float))) != cudaSuccess)
-    return cuda_fail(e, "fp8_adamw_step: workspace");
+  cudaError_t e = prepare_slots(ws, (size_t)n, stream, &epoch);   // [0, n) amax
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_cast_scaled: workspace");
+  e = launch_cast(static_cast<const CastDesc*>(ws->cast_descs.ptr),
+                  static_cast<const Chunk*>(ws->cast_chunks.ptr), ws->cast_nchunks,
+                  static_cast<unsigned long long*>(ws->slots.ptr), epoch, fmt,
+                  info->cast_amax, info->cast_encode, stream, launch_mark());
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_cast_scaled: launch");
+  return FP8OPT_OK;
+}
+
+extern "C" int fp8_adamw_step(const fp8opt_param* params, int n, float lr,
+                              float beta1, float beta2, float eps, float wd,
+                              int64_t step, float inv_loss_scale, int* found_inf,
+                              uint32_t* found_inf_dev, void* stream_ptr) {
+  const char* fn = "fp8_adamw_step";
+  int st = check_step_args(fn, params, n, step);
+  if (st != FP8OPT_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (n == 0) return empty_step(fn, found_inf, found_inf_dev, stream);
+  const StepScalars s = make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale);
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  DeviceInfo* info = nullptr;
+  if ((st = current_device_and_info(&dev, &info)) != FP8OPT_OK) return st;
+  Workspace* ws = workspace(dev, stream);
+  if ((st = ensure_step_tables(fn, ws, params, n, stream)) != FP8OPT_OK) return st;
+
+  uint32_t epoch = 0;
+  // slots: [0, n) amax of m, [n, 2n) amax of the master, [2n] found_inf
+  cudaError_t e = prepare_slots(ws, 2 * (size_t)n + 1, stream, &epoch);
+  if (e == cudaSuccess) e = ws->saved_scales.reserve((size_t)n * sizeof(float));
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_adamw_step: workspace");
   unsigned long long* slots = static_cast<unsigned long long*>(ws->slots.ptr);
   StepScratch sc;
   sc.amax_m = slots;
@@ -451,14 +515,61 @@ extern "C" int fp8_adamw_step(const fp8opt_param* params, int n, float lr,
                   sc, s, epoch, found_inf_dev, info->step_amax, info->step_update,
                   info->step_w8, stream, launch_mark());
   if (e != cudaSuccess) return cuda_fail(e, "fp8_adamw_step: launch");
+  if (found_inf != nullptr) return read_found(fn, sc.found, epoch, stream, found_inf);
+  return FP8OPT_OK;
+}
 
-  if (found_inf != nullptr) {
-    unsigned long long tag = 0;
-    e = cudaMemcpyAsync(&tag, sc.found, sizeof(tag), cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return cuda_fail(e, "fp8_adamw_step: found_inf read");
-    *found_inf = tag == (((unsigned long long)epoch << 32) | 1ull) ? 1 : 0;
+extern "C" int fp8_cast_adamw_step(const fp8opt_cast_item* grads,
+                                   const fp8opt_param* params, int n, int fmt,
+                                   float lr, float beta1, float beta2, float eps,
+                                   float wd, int64_t step, float inv_loss_scale,
+                                   int* found_inf, uint32_t* found_inf_dev,
+                                   void* stream_ptr) {
+  const char* fn = "fp8_cast_adamw_step";
+  int st = check_cast_args(fn, grads, n, fmt);
+  if (st == FP8OPT_OK) st = check_step_args(fn, params, n, step);
+  if (st != FP8OPT_OK) return st;
+  for (int i = 0; i < n; ++i) {
+    const fp8opt_param& p = params[i];
+    if (p.g != grads[i].codes || p.g_scale != grads[i].scale ||
+        p.numel != grads[i].numel || p.g_fmt != fmt)
+      return fail(FP8OPT_ERR_ARG, std::string(fn) + ": param " + std::to_string(i) +
+                                      " does not take item " + std::to_string(i) +
+                                      "'s codes, scale, numel and format");
   }
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (n == 0) return empty_step(fn, found_inf, found_inf_dev, stream);
+  const StepScalars s = make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale);
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  DeviceInfo* info = nullptr;
+  if ((st = current_device_and_info(&dev, &info)) != FP8OPT_OK) return st;
+  Workspace* ws = workspace(dev, stream);
+  if ((st = ensure_cast_tables(fn, ws, grads, n, stream)) != FP8OPT_OK) return st;
+  if ((st = ensure_step_tables(fn, ws, params, n, stream)) != FP8OPT_OK) return st;
+
+  // slots: [0, n) gradient amax, [n, 2n) amax of m, [2n, 3n) amax of the
+  // master, [3n] found_inf
+  uint32_t epoch = 0;
+  cudaError_t e = prepare_slots(ws, 3 * (size_t)n + 1, stream, &epoch);
+  if (e == cudaSuccess) e = ws->saved_scales.reserve((size_t)n * sizeof(float));
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_cast_adamw_step: workspace");
+  unsigned long long* slots = static_cast<unsigned long long*>(ws->slots.ptr);
+  StepScratch sc;
+  sc.amax_m = slots + n;
+  sc.amax_w = slots + 2 * (size_t)n;
+  sc.found = slots + 3 * (size_t)n;
+  sc.old_m_scale = static_cast<float*>(ws->saved_scales.ptr);
+  const Chunk* chunks = static_cast<const Chunk*>(ws->step_chunks.ptr);
+  e = launch_cast_step(static_cast<const CastDesc*>(ws->cast_descs.ptr),
+                       static_cast<const StepDesc*>(ws->step_descs.ptr), chunks,
+                       ws->step_nchunks, chunks + ws->step_nchunks,
+                       ws->step_nchunks_o3, slots, sc, s, epoch, fmt,
+                       found_inf_dev, info->cast_amax, info->cast_step,
+                       info->step_update, info->step_w8, stream, launch_mark());
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_cast_adamw_step: launch");
+  if (found_inf != nullptr) return read_found(fn, sc.found, epoch, stream, found_inf);
   return FP8OPT_OK;
 }
 

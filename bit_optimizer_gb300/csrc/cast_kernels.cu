@@ -121,39 +121,6 @@ cast_amax_kernel(const CastDesc* __restrict__ descs,
 
 // -------------------------------------------------------------- encode pass
 
-template <int DT>
-__device__ __forceinline__ void load8(const void* src, int64_t i0,
-                                      float (&x)[8]) {
-  if (DT == kF32) {
-    const float* f = static_cast<const float*>(src) + i0;
-    const uint4 a = ld_once4(f), b = ld_once4(f + 4);
-    x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
-    x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
-    x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
-    x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
-  } else {
-    const uint4 a = ld_once4(static_cast<const uint16_t*>(src) + i0);
-    if (DT == kF16) {
-      h8_to_f(a, x);
-    } else {
-      const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        x[2 * j] = __uint_as_float(w[j] << 16);
-        x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-      }
-    }
-  }
-}
-
-template <int DT>
-__device__ __forceinline__ float load1(const void* src, int64_t i) {
-  if (DT == kF32) return static_cast<const float*>(src)[i];
-  const uint16_t b = static_cast<const uint16_t*>(src)[i];
-  if (DT == kF16) return h_to_f(b);
-  return __uint_as_float((uint32_t)b << 16);
-}
-
 // Encode this thread's share of [begin, end).  CHECKED when the tensor holds a
 // non-finite element (its amax is not finite): those take the explicit
 // NaN / infinity codes; otherwise every product is finite.
@@ -259,6 +226,19 @@ cudaError_t launch_cast(const CastDesc* descs, const Chunk* chunks,
     cast_encode_kernel<kE5M2><<<ge, kThreads, 0, stream>>>(descs, chunks,
                                                            nchunks, slots, epoch);
   if (mark) mark(kCastEncodeK, 1, stream);
+  return cudaGetLastError();
+}
+
+// The amax pass alone (the fused cast + step path runs its own encode pass).
+cudaError_t launch_cast_amax(const CastDesc* descs, const Chunk* chunks,
+                             uint32_t nchunks, unsigned long long* slots,
+                             uint32_t epoch, int grid_amax, cudaStream_t stream,
+                             LaunchMark mark) {
+  if (nchunks == 0) return cudaSuccess;
+  if (mark) mark(kCastAmaxK, 0, stream);
+  cast_amax_kernel<<<grid_min((uint32_t)grid_amax, nchunks), kThreads, 0,
+                     stream>>>(descs, chunks, nchunks, slots, epoch);
+  if (mark) mark(kCastAmaxK, 1, stream);
   return cudaGetLastError();
 }
 

@@ -68,7 +68,7 @@ struct StepDesc {
 
 // Kernels, for the optional per-launch event timing.
 enum KernelId { kCastAmaxK = 0, kCastEncodeK, kStepAmaxK, kStepUpdateK,
-                kStepW8K, kNumKernels };
+                kStepW8K, kCastStepAmaxK, kNumKernels };
 
 // Called before (end = 0) and after (end = 1) each kernel launch when timing
 // is on; nullptr otherwise.
@@ -253,6 +253,71 @@ __device__ __forceinline__ uint2 ld_once2(const void* p) {
 }
 __device__ __forceinline__ uint4 ld_once4(const void* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+
+// ------------------------------------------- shared by several kernels
+
+__device__ __forceinline__ uint32_t nonfinite(float x) {
+  return (__float_as_uint(x) & 0x7FFFFFFFu) >= 0x7F800000u;
+}
+
+__device__ __forceinline__ uint32_t abs_bits(float x) {
+  return __float_as_uint(x) & 0x7FFFFFFFu;
+}
+
+// Two FP16 (one 32-bit word) <-> float2.
+__device__ __forceinline__ float2 h2_to_f2(uint32_t h) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+__device__ __forceinline__ uint32_t f2_to_h2(float2 f) {
+  __half2 h = __float22half2_rn(f);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Code pair j (0..3) of eight codes held in a uint2.
+__device__ __forceinline__ uint32_t code_pair(uint2 c, int j) {
+  const uint32_t w = j < 2 ? c.x : c.y;
+  return (j & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+__device__ __forceinline__ uint32_t half_pair(uint4 h, int j) {
+  return j == 0 ? h.x : j == 1 ? h.y : j == 2 ? h.z : h.w;
+}
+
+// Eight source elements of type DT from element i0 (vector path, last use),
+// and one element (scalar path), widened exactly to fp32.
+template <int DT>
+__device__ __forceinline__ void load8(const void* src, int64_t i0,
+                                      float (&x)[8]) {
+  if (DT == kF32) {
+    const float* f = static_cast<const float*>(src) + i0;
+    const uint4 a = ld_once4(f), b = ld_once4(f + 4);
+    x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+    x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+    x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+    x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
+  } else {
+    const uint4 a = ld_once4(static_cast<const uint16_t*>(src) + i0);
+    if (DT == kF16) {
+      h8_to_f(a, x);
+    } else {
+      const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[2 * j] = __uint_as_float(w[j] << 16);
+        x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+    }
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ float load1(const void* src, int64_t i) {
+  if (DT == kF32) return static_cast<const float*>(src)[i];
+  const uint16_t b = static_cast<const uint16_t*>(src)[i];
+  if (DT == kF16) return h_to_f(b);
+  return __uint_as_float((uint32_t)b << 16);
 }
 
 // Max over the CTA of a per-thread uint32; the result is valid in thread 0.

@@ -50,14 +50,6 @@ constexpr int kAmaxGroups = FP8OPT_STEP_AMAX_GROUPS;
 constexpr int kUpdGroups = FP8OPT_UPD_GROUPS;
 constexpr int kW8Groups = 2;
 
-__device__ __forceinline__ uint32_t nonfinite(float x) {
-  return (__float_as_uint(x) & 0x7FFFFFFFu) >= 0x7F800000u;
-}
-
-__device__ __forceinline__ uint32_t abs_bits(float x) {
-  return __float_as_uint(x) & 0x7FFFFFFFu;
-}
-
 // The scalar forms of the lines above (tails and unaligned tensors).
 __device__ __forceinline__ float m_new1(float mdec, float minv, float g,
                                         const StepScalars& s) {
@@ -71,26 +63,6 @@ __device__ __forceinline__ void adamw1(float g, float m, float vp, float wp,
   const float den = __fmaf_rn(__fsqrt_rn(v), s.inv_sbc2, s.eps);
   const float u = __fdiv_rn(m, den);
   w = __fmaf_rn(-s.step_size, u, __fmul_rn(wp, s.decay));
-}
-
-// Two FP16 (one 32-bit word) <-> float2.
-__device__ __forceinline__ float2 h2_to_f2(uint32_t h) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&h));
-}
-
-__device__ __forceinline__ uint32_t f2_to_h2(float2 f) {
-  __half2 h = __float22half2_rn(f);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Code pair j (0..3) of eight codes held in a uint2.
-__device__ __forceinline__ uint32_t code_pair(uint2 c, int j) {
-  const uint32_t w = j < 2 ? c.x : c.y;
-  return (j & 1) ? (w >> 16) : (w & 0xFFFFu);
-}
-
-__device__ __forceinline__ uint32_t half_pair(uint4 h, int j) {
-  return j == 0 ? h.x : j == 1 ? h.y : j == 2 ? h.z : h.w;
 }
 
 // ------------------------------------------------------------ pass 1: amax
@@ -412,6 +384,27 @@ step_w8_kernel(const StepDesc* __restrict__ descs,
 
 }  // namespace
 
+// The update pass, then (for O3 chunks) the weight-copy pass.
+cudaError_t launch_step_update(const StepDesc* descs, const Chunk* chunks,
+                               uint32_t nchunks, const Chunk* chunks_o3,
+                               uint32_t nchunks_o3, const StepScratch& sc,
+                               const StepScalars& s, uint32_t epoch,
+                               uint32_t* found_dev, int grid_update, int grid_w8,
+                               cudaStream_t stream, LaunchMark mark) {
+  if (mark) mark(kStepUpdateK, 0, stream);
+  step_update_kernel<<<grid_min((uint32_t)grid_update, nchunks), kThreads,
+                       0, stream>>>(descs, chunks, nchunks, sc, s, epoch,
+                                    found_dev);
+  if (mark) mark(kStepUpdateK, 1, stream);
+  if (nchunks_o3 != 0) {
+    if (mark) mark(kStepW8K, 0, stream);
+    step_w8_kernel<<<grid_min((uint32_t)grid_w8, nchunks_o3), kThreads, 0,
+                     stream>>>(descs, chunks_o3, nchunks_o3, sc, epoch);
+    if (mark) mark(kStepW8K, 1, stream);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_step(const StepDesc* descs, const Chunk* chunks,
                         uint32_t nchunks, const Chunk* chunks_o3,
                         uint32_t nchunks_o3, const StepScratch& sc,
@@ -426,18 +419,10 @@ cudaError_t launch_step(const StepDesc* descs, const Chunk* chunks,
   step_amax_kernel<<<grid_min((uint32_t)grid_amax, nchunks), kThreads, 0,
                      stream>>>(descs, chunks, nchunks, sc, s, epoch);
   if (mark) mark(kStepAmaxK, 1, stream);
-  if (mark) mark(kStepUpdateK, 0, stream);
-  step_update_kernel<<<grid_min((uint32_t)grid_update, nchunks), kThreads,
-                       0, stream>>>(descs, chunks, nchunks, sc, s, epoch,
-                                    found_dev);
-  if (mark) mark(kStepUpdateK, 1, stream);
-  if (nchunks_o3 != 0) {
-    if (mark) mark(kStepW8K, 0, stream);
-    step_w8_kernel<<<grid_min((uint32_t)grid_w8, nchunks_o3), kThreads, 0,
-                     stream>>>(descs, chunks_o3, nchunks_o3, sc, epoch);
-    if (mark) mark(kStepW8K, 1, stream);
-  }
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_step_update(descs, chunks, nchunks, chunks_o3, nchunks_o3, sc, s,
+                            epoch, found_dev, grid_update, grid_w8, stream, mark);
 }
 
 cudaError_t step_occupancy(int* amax_per_sm, int* update_per_sm,

@@ -189,6 +189,28 @@ FP8OPT_API int fp8_adamw_step(const fp8opt_param *params, int n, float lr, float
 FP8OPT_API int fp8_cast_scaled_noalloc(const fp8opt_cast_item *items, int n,
                                        int fmt, void *stream);
 
+/*
+ * fp8_cast_adamw_step: fp8_cast_scaled(grads, n, fmt) followed by
+ * fp8_adamw_step(params, n, ...) on the codes it wrote, in one call and with
+ * one pass fewer over memory: the encode pass of the cast also computes the
+ * step's first pass (found_inf and the amax of the new first moment) from the
+ * codes it has just produced.  Results, found_inf semantics and errors are
+ * those of the two calls made in turn (MS-AMP O1 gradient cast, then the
+ * O2/O3 step with the GradScaler skip).
+ *
+ * params[i] must take grads[i]'s output: params[i].g == grads[i].codes,
+ * params[i].g_scale == grads[i].scale, the same numel, and g_fmt == fmt;
+ * otherwise FP8OPT_ERR_ARG and nothing is launched.  Other arguments as for
+ * the two calls.  With BF16 gradients an O2 step moves 17 bytes per parameter
+ * instead of 18.
+ */
+FP8OPT_API int fp8_cast_adamw_step(const fp8opt_cast_item *grads,
+                                   const fp8opt_param *params, int n, int fmt,
+                                   float lr, float beta1, float beta2, float eps,
+                                   float wd, int64_t step, float inv_loss_scale,
+                                   int *found_inf, uint32_t *found_inf_dev,
+                                   void *stream);
+
 /* Text of a status code (static storage). */
 FP8OPT_API const char *fp8opt_strerror(int status);
 
@@ -202,7 +224,8 @@ FP8OPT_API const char *fp8opt_last_error(void);
  * timed region.  fp8opt_timing_enable(1) clears the record and starts
  * recording; fp8opt_timing_enable(0) stops.  fp8opt_timing_read waits for the
  * recorded events and returns, for one kernel name ("cast_amax",
- * "cast_encode", "step_amax", "step_update", "step_w8"), the launches
+ * "cast_encode", "step_amax", "step_update", "step_w8", "cast_step_amax"),
+ * the launches
  * recorded since enabling and their summed duration in milliseconds.  Returns
  * FP8OPT_ERR_ARG for an unknown name or NULL outputs. */
 FP8OPT_API int fp8opt_timing_enable(int on);

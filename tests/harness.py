@@ -218,6 +218,32 @@ class DeviceList:
                          wl.inv_loss_scale if ils is None else ils,
                          found_inf_dev=self.found_dev)
 
+    def cast_step(self, t, ils=None):
+        """The cast of every tensor and the step in one fp8_cast_adamw_step
+        call (the bench's configuration)."""
+        import bit_optimizer_gb300 as bo
+        wl = self.wl
+        if not hasattr(self, "fused"):
+            self.fused = bo.CastStepPlan(self.cast, self.plan)
+        return self.fused(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, t,
+                          wl.inv_loss_scale if ils is None else ils,
+                          found_inf_dev=self.found_dev)
+
+    def check_cast(self, sample, states):
+        """After a fused call: the sampled tensors' codes, amax and scale
+        against the oracle's cast of the same values, which become the
+        oracle's step inputs."""
+        amax = self.g_amax.cpu().numpy()
+        scale = self.g_scale.cpu().numpy()
+        for i in sample:
+            a, dt = host_src(self.src[i])
+            codes, am, sc = oracle.cast_scaled(a, dt, self.fmt)
+            check_f32_exact(amax[i:i + 1], [am], f"grad amax[{i}]")
+            check_f32_exact(scale[i:i + 1], [sc], f"grad scale[{i}]")
+            check_codes(to_np_u8(self.g[i]), codes, self.fmt, name=f"grad[{i}]")
+            states[i].g = codes
+            states[i].g_scale = float(sc)
+
     def compare(self, i, st):
         check_f32_exact(self.m_scale[i:i + 1].cpu().numpy(), st.m_scale, f"m_scale[{i}]")
         check_codes(to_np_u8(self.m[i]), st.m, name=f"m[{i}]")

@@ -110,6 +110,27 @@ def test_argument_errors_need_no_gpu(lib):
     assert f.value == 0
 
 
+def test_fused_call_checks_that_the_step_takes_the_cast_outputs(lib):
+    L = lib.load()
+    item = (lib.CastItem * 1)()
+    p = (lib.Param * 1)()
+    dummy = C.c_float(1.0)
+    item[0].dtype, item[0].numel = 1, 4
+    item[0].src = item[0].codes = 0x1000
+    item[0].amax = item[0].scale = C.addressof(dummy)
+    p[0].numel = 4
+    p[0].g, p[0].g_scale = 0x1000, C.addressof(dummy)
+    p[0].m = p[0].v = p[0].w = 0x2000
+    p[0].m_scale = C.addressof(dummy)
+    args = (1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0, None, None, None)
+    p[0].g = 0x3000                                   # not the cast's codes
+    assert L.fp8_cast_adamw_step(item, p, 1, 0, *args) == lib.ERR_ARG
+    assert "does not take item 0" in L.fp8opt_last_error().decode()
+    p[0].g, p[0].g_fmt = 0x1000, 1                    # other format
+    assert L.fp8_cast_adamw_step(item, p, 1, 0, *args) == lib.ERR_ARG
+    assert L.fp8_cast_adamw_step(item, p, 0, 0, *args) == lib.OK
+
+
 def test_strerror_texts(lib):
     assert lib.strerror(0) == "success"
     assert lib.strerror(-1) == "invalid argument"

@@ -54,16 +54,26 @@ def test_cast_gpt2_124m_every_tensor(bo, fmt):
         check_codes(to_np_u8(codes[i]), rc, f, name=f"codes[{i}]")
 
 
-def lockstep_full(wl, steps, sample, first=1):
+def lockstep_full(wl, steps, sample, first=1, fused=False):
+    """Every tensor stepped by the library; the sampled ones start each step
+    from the oracle's state.  fused: one fp8_cast_adamw_step call per step
+    (the bench's configuration), else fp8_cast_scaled then fp8_adamw_step."""
     dl = DeviceList(wl)
     states = {i: dl.fresh_oracle(i) for i in sample}
     for t in range(first, first + steps):
         dl.gen_grads(t)
-        dl.cast_and_check(sample, states)
-        for i in sample:
-            dl.put(i, states[i])
+        if fused:
+            for i in sample:
+                dl.put(i, states[i])
+            f = dl.cast_step(t)
+            dl.check_cast(sample, states)
+        else:
+            dl.cast_and_check(sample, states)
+            for i in sample:
+                dl.put(i, states[i])
+            f = dl.step(t)
         f_ref = oracle_step([states[i] for i in sample], wl, t)
-        assert dl.step(t) == f_ref == 0
+        assert f == f_ref == 0
         for i in sample:
             dl.compare(i, states[i])
     return dl, states
@@ -103,10 +113,11 @@ def test_o2_350m_full_inf_skip_and_step(bo):
     dl.invariants()
 
 
-def test_o3_1p3b_full(bo):
+@pytest.mark.parametrize("fused", [False, True])
+def test_o3_1p3b_full(bo, fused):
     wl = synth.o3_1p3b()
     sample = sample_of(wl, 6_000_000)
-    dl, _ = lockstep_full(wl, wl.warmup_steps + 1, sample)
+    dl, _ = lockstep_full(wl, wl.warmup_steps + 1, sample, fused=fused)
     dl.invariants()
 
 
@@ -115,7 +126,7 @@ def test_o2_6p7b_tail_full_10_steps(bo):
     assert len(wl.shapes) == 589
     sample = sample_of(wl, 12_000_000)       # every tail tensor, norms, biases, wpe
     assert len(wl.shapes) - 1 in sample and 1 in sample
-    dl, _ = lockstep_full(wl, wl.steps, sample)
+    dl, _ = lockstep_full(wl, wl.steps, sample, fused=True)
     dl.invariants()
     zero = len(wl.shapes) - 1
     assert dl.m_scale[zero].item() == 1.0 and not bool(dl.m[zero].any().item())

@@ -247,17 +247,23 @@ def test_checkpoint_resume_is_bit_identical(bo):
     assert torch.equal(a.m_scale, b.m_scale) and torch.equal(a.w8_scale, b.w8_scale)
 
 
-def test_timing_records_each_kernel(bo):
+@pytest.mark.parametrize("fused", [True, False])
+def test_timing_records_each_kernel(bo, fused):
     wl = synth.tiny()
     params = [w.cuda() for w in wl.weights()]
-    opt = bo.Fp8AdamW(params, level="O3")
+    opt = bo.Fp8AdamW(params, level="O3", fused=fused)
     bo.timing_enable(True)
     for t in (1, 2):
         opt.step([g.cuda() for g in wl.grads(t)])
     bo.timing_enable(False)
+    ran = ({"cast_amax", "cast_step_amax", "step_update", "step_w8"} if fused else
+           {"cast_amax", "cast_encode", "step_amax", "step_update", "step_w8"})
     for k in bo.KERNELS:
         n, ms = bo.timing_read(k)
-        assert n == 2 and ms > 0.0, k
+        if k in ran:
+            assert n == 2 and ms > 0.0, k
+        else:
+            assert n == 0, k
 
 
 def test_workspace_reuse_across_list_lengths(bo):
@@ -271,3 +277,109 @@ def test_workspace_reuse_across_list_lengths(bo):
     wl = synth.o2_6p7b_tail(n_layer=1, d=64, ffn=256, vocab=300, ctx=32, n_tail=20)
     states = fresh_states(wl.weights(), o3=False)
     lockstep(bo, wl, states, 1, 2)
+
+
+# ----------------------------------------------------------- fused call
+
+def lockstep_fused(bo, wl, states, t0, t1, fmt=E4M3, misalign=(), clean=None):
+    """Steps t0..t1 through fp8_cast_adamw_step: each step the GPU starts
+    from the oracle's state and casts the same gradients itself."""
+    gpu = None
+    found = []
+    for t in range(t0, t1 + 1):
+        grads = (clean or wl).grads(t)
+        codes, amax, scale = oracle_cast(grads, fmt)
+        set_grads(states, codes, scale)
+        if gpu is None:
+            gpu = GpuState([s.copy() for s in states], misalign=misalign)
+        else:
+            gpu.load_state(states)
+        before = [s.copy() for s in states]
+        src = [g.cuda() for g in grads]
+        g_amax = torch.empty(max(len(src), 1), device="cuda")
+        fused = bo.CastStepPlan(bo.CastPlan(src, gpu.g, g_amax, gpu.g_scale, fmt),
+                                gpu.plan)
+        f_ref = oracle_step(states, wl, t)
+        f = fused(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, t, wl.inv_loss_scale,
+                  found_inf_dev=gpu.found_dev)
+        assert f == f_ref == int(gpu.found_dev.item())
+        n = len(grads)
+        check_f32_exact(g_amax.cpu().numpy()[:n], amax, "grad amax")
+        check_f32_exact(gpu.g_scale.cpu().numpy()[:n], scale, "grad scale")
+        for i, (c, r) in enumerate(zip(gpu.g, codes)):
+            check_codes(to_np_u8(c), r, fmt, name=f"grad codes[{i}]")
+        if f == 0:
+            gpu.compare(states)
+        else:
+            for i, s in enumerate(before):
+                assert np.array_equal(to_np_u8(gpu.m[i]), s.m)
+                assert np.array_equal(to_np_u16(gpu.v[i]), s.v)
+                assert np.array_equal(to_np_u16(gpu.w[i]), s.w)
+        found.append(f)
+    return gpu, found
+
+
+def test_fused_tiny_10_steps(bo):
+    wl = synth.tiny()
+    states = fresh_states(wl.weights(), o3=False)
+    _, found = lockstep_fused(bo, wl, states, 1, wl.steps)
+    assert found == [0] * wl.steps
+
+
+def test_fused_350m_reduced_inf_skip_then_step(bo):
+    wl = reduced_350m()
+    states = fresh_states(wl.weights(), o3=False)
+    warm_up(wl, states, wl.warmup_steps)
+    t = wl.warmup_steps + 1
+    _, found = lockstep_fused(bo, wl, states, t, t)          # +inf: skipped
+    assert found == [1]
+    clean = dataclasses.replace(wl, inf_site=None)
+    _, found = lockstep_fused(bo, wl, states, t, t, clean=clean)
+    assert found == [0]
+
+
+def test_fused_o3_and_long_tail_reduced(bo):
+    wl = synth.o3_1p3b(n_layer=2, d=128, ffn=512, vocab=1000, ctx=64)
+    states = fresh_states(wl.weights(), o3=True)
+    warm_up(wl, states, wl.warmup_steps)
+    lockstep_fused(bo, wl, states, wl.warmup_steps + 1, wl.warmup_steps + 2)
+    wl = synth.o2_6p7b_tail(n_layer=1, d=128, ffn=512, vocab=1000, ctx=64)
+    states = fresh_states(wl.weights(), o3=False)
+    lockstep_fused(bo, wl, states, 1, 3)
+
+
+def test_fused_e5m2_unaligned_and_odd(bo):
+    wl = dataclasses.replace(synth.tiny(), grad_fmt="e5m2")
+    states = fresh_states(wl.weights(), o3=False, g_fmt=E5M2)
+    lockstep_fused(bo, wl, states, 1, 3, fmt=E5M2, misalign={0, 2})
+    sizes = [0, 1, 3, 17, 4097]
+    g = torch.Generator().manual_seed(21)
+    weights = [(torch.randn(n, generator=g) * 0.02).half() for n in sizes]
+    odd = dataclasses.replace(synth.tiny(), names=[f"t{i}" for i in range(5)],
+                              shapes=[(n,) for n in sizes])
+    states = fresh_states(weights, o3=True)
+    lockstep_fused(bo, odd, states, 1, 2)
+
+
+def test_fused_equals_the_two_calls(bo):
+    """The fused entry and fp8_cast_scaled + fp8_adamw_step, from the same
+    state and gradients, give byte-identical results."""
+    wl = synth.o2_6p7b_tail(n_layer=1, d=256, ffn=1024, vocab=2000, ctx=64, n_tail=50)
+    weights = [w.cuda() for w in wl.weights()]
+    grads = [g.cuda() for g in wl.grads(1)]
+    outs = []
+    for fused in (True, False):
+        params = [w.clone() for w in weights]
+        opt = bo.Fp8AdamW(params, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
+                          weight_decay=wl.wd, level="O3", fused=fused)
+        for t in (1, 2):
+            assert opt.step([g * t for g in grads]) == 0
+        outs.append((params, opt))
+    (pa, a), (pb, b) = outs
+    for x, y in zip(pa, pb):
+        assert torch.equal(x, y)
+    for name in ("g_codes", "m", "v", "w8"):
+        for x, y in zip(getattr(a, name), getattr(b, name)):
+            assert torch.equal(x, y), name
+    for name in ("g_amax", "g_scale", "m_scale", "w8_scale", "w8_amax"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
