@@ -19,6 +19,12 @@ namespace {
 constexpr int kAmaxGroups = 4;   // 8-element groups per thread per tile
 constexpr int kEncGroups = 2;
 
+// Tiles ahead of the current one the encode pass prefetches into L2 (0:
+// none).  Measured: no gain for this pass or for the read-only amax pass.
+#ifndef FP8OPT_ENC_PREFETCH
+#define FP8OPT_ENC_PREFETCH 0
+#endif
+
 // ---------------------------------------------------------------- amax pass
 
 // Max of |x| bit patterns over the four words of a uint4 of 16-bit values,
@@ -128,8 +134,16 @@ template <int DT, int FMT, bool CHECKED>
 __device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
                               int64_t end, bool vec, float scale) {
   constexpr int64_t kTile = (int64_t)kThreads * kGroup * kEncGroups;
+  constexpr uint32_t kSrcBytes = DT == kF32 ? 4 : 2;
   const int tid = threadIdx.x;
+  const bool pf = FP8OPT_ENC_PREFETCH > 0 && tid == 0 && vec && aligned16(src);
   for (int64_t base = begin; base < end; base += kTile) {
+    if (pf) {
+      const int64_t ahead = base + FP8OPT_ENC_PREFETCH * kTile;
+      if (ahead + kTile <= end)
+        prefetch_l2(static_cast<const char*>(src) + ahead * kSrcBytes,
+                    (uint32_t)(kSrcBytes * kTile));
+    }
     if (vec && base + kTile <= end) {
       float x[kEncGroups][8];
 #pragma unroll

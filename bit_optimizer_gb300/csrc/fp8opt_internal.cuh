@@ -320,6 +320,17 @@ __device__ __forceinline__ float load1(const void* src, int64_t i) {
   return __uint_as_float((uint32_t)b << 16);
 }
 
+// Asynchronous bulk prefetch of [p, p + bytes) into L2 (no shared memory, no
+// completion to wait for).  p and bytes must be multiples of 16.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+               :: "l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
 // Max over the CTA of a per-thread uint32; the result is valid in thread 0.
 // Every thread of the CTA must call it.
 __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* smem) {

@@ -38,6 +38,11 @@ namespace {
 
 constexpr int kFusedGroups = 2;   // 8-element groups per thread per tile
 
+// Tiles ahead of the current one prefetched into L2 (0: none).
+#ifndef FP8OPT_FUSED_PREFETCH
+#define FP8OPT_FUSED_PREFETCH 1
+#endif
+
 // Encode eight values (CHECKED: explicit codes for non-finite inputs).
 template <int FMT, bool CHECKED>
 __device__ __forceinline__ uint32_t enc_pair(float2 t) {
@@ -57,7 +62,18 @@ __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
   const bool vec = cd.vec_ok != 0 && sd.vec_ok != 0;
   const float2 sc2 = splat2(scale), k2 = splat2(k), minv2 = splat2(minv),
                b1 = splat2(s.beta1), omb1 = splat2(s.omb1);
+  constexpr uint32_t kSrcBytes = DT == kF32 ? 4 : 2;
+  const bool pf = FP8OPT_FUSED_PREFETCH > 0 && tid == 0 && vec &&
+                  aligned16(cd.src) && aligned16(sd.m);
   for (int64_t base = begin; base < end; base += kTile) {
+    if (pf) {
+      const int64_t ahead = base + FP8OPT_FUSED_PREFETCH * kTile;
+      if (ahead + kTile <= end) {
+        prefetch_l2(static_cast<const char*>(cd.src) + ahead * kSrcBytes,
+                    (uint32_t)(kSrcBytes * kTile));
+        prefetch_l2(sd.m + ahead, (uint32_t)kTile);
+      }
+    }
     if (vec && base + kTile <= end) {
       float x[kFusedGroups][8];
       uint2 mc[kFusedGroups];

@@ -46,6 +46,16 @@ namespace {
 #ifndef FP8OPT_UPD_MIN_BLOCKS
 #define FP8OPT_UPD_MIN_BLOCKS 3
 #endif
+// Tiles ahead of the current one that the update and amax passes prefetch
+// into L2 (0: none).  Measured on the 6.7B list: the update pass is 7 %
+// slower with a prefetch one or two tiles ahead, and the amax pass gains
+// nothing, so both are off.
+#ifndef FP8OPT_UPD_PREFETCH
+#define FP8OPT_UPD_PREFETCH 0
+#endif
+#ifndef FP8OPT_STEP_AMAX_PREFETCH
+#define FP8OPT_STEP_AMAX_PREFETCH 0
+#endif
 constexpr int kAmaxGroups = FP8OPT_STEP_AMAX_GROUPS;
 constexpr int kUpdGroups = FP8OPT_UPD_GROUPS;
 constexpr int kW8Groups = 2;
@@ -78,7 +88,16 @@ __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
   const bool vec = d.vec_ok != 0;
   const float2 k2 = splat2(k), minv2 = splat2(minv), b1 = splat2(s.beta1),
                omb1 = splat2(s.omb1);
+  const bool pf = FP8OPT_STEP_AMAX_PREFETCH > 0 && tid == 0 && vec &&
+                  aligned16(d.g) && aligned16(d.m);
   for (int64_t base = begin; base < end; base += kTile) {
+    if (pf) {
+      const int64_t ahead = base + FP8OPT_STEP_AMAX_PREFETCH * kTile;
+      if (ahead + kTile <= end) {
+        prefetch_l2(d.g + ahead, (uint32_t)kTile);
+        prefetch_l2(d.m + ahead, (uint32_t)kTile);
+      }
+    }
     if (vec && base + kTile <= end) {
       uint2 gc[kAmaxGroups], mc[kAmaxGroups];
 #pragma unroll
@@ -174,7 +193,22 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
                omb2 = splat2(s.omb2), isbc2 = splat2(s.inv_sbc2),
                eps2 = splat2(s.eps), nstep = splat2(-s.step_size),
                decay = splat2(s.decay), msc2 = splat2(msc);
+  // One thread asks L2 for the tile FP8OPT_UPD_PREFETCH tiles ahead (whole
+  // tiles of 16-byte-aligned tensors only), so the loads below find their
+  // lines on chip while the DRAM reads for later tiles are already running.
+  const bool pf = FP8OPT_UPD_PREFETCH > 0 && tid == 0 && vec &&
+                  aligned16(d.g) && aligned16(d.m) && aligned16(d.v) &&
+                  aligned16(d.w);
   for (int64_t base = begin; base < end; base += kTile) {
+    if (pf) {
+      const int64_t ahead = base + FP8OPT_UPD_PREFETCH * kTile;
+      if (ahead + kTile <= end) {
+        prefetch_l2(d.g + ahead, (uint32_t)kTile);
+        prefetch_l2(d.m + ahead, (uint32_t)kTile);
+        prefetch_l2(d.v + ahead, (uint32_t)(2 * kTile));
+        prefetch_l2(d.w + ahead, (uint32_t)(2 * kTile));
+      }
+    }
     if (vec && base + kTile <= end) {
       uint2 gc[kUpdGroups], mc[kUpdGroups];
       uint4 vh[kUpdGroups], wh[kUpdGroups];
