@@ -58,6 +58,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--no-other-configs", action="store_true",
+                   help="skip the cast (124M), O2 350M, O3 1.3B and tiny lines")
     p.add_argument("--n-layer", type=int, default=None,
                    help="override the workload's layer count (profiling cases)")
     p.add_argument("--vocab", type=int, default=None,
@@ -294,6 +296,66 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
+def _events_ms(fn, reps):
+    """Average device milliseconds of fn() over reps calls (CUDA events on
+    the current stream, synchronised on both sides)."""
+    import torch
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def other_configs(device, peak):
+    """The remaining workloads, each timed on its own after the headline:
+    the scaled cast of the 124M GPT-2 list (BF16 -> E4M3 and -> E5M2, 5 B per
+    element), the O2 step on the 350M list (the inf cleared), the O3 step on
+    the 1.3B list (20 B per param with the cast), and the launch-bound tiny
+    list."""
+    import dataclasses
+    import torch
+    import synth
+    import bit_optimizer_gb300 as bo
+    out = {}
+    wl = synth.gpt2_cast()
+    srcs = bo.arena_views(wl.numels, torch.bfloat16, device)
+    for i, x in enumerate(srcs):
+        x.copy_(wl.grad(i, 1, device))
+    codes = bo.arena_views(wl.numels, torch.uint8, device)
+    amax = torch.empty(len(srcs), device=device)
+    scale = torch.empty(len(srcs), device=device)
+    for fmt in ("e4m3", "e5m2"):
+        plan = bo.CastPlan(srcs, codes, amax, scale, fmt)
+        for _ in range(3):
+            plan()
+        ms = _events_ms(plan, 20)
+        gbs = 5 * wl.n_params / (ms * 1e-3) / 1e9
+        out[f"cast_gpt2_124m_{fmt}"] = {"ms": ms, "GB/s": gbs, "frac": gbs / peak,
+                                        "bytes_per_elem": 5}
+    del srcs, codes
+    for name, mk, reps in (("o2_350m", synth.o2_350m, 20),
+                           ("o3_1p3b", synth.o3_1p3b, 10), ("tiny", synth.tiny, 200)):
+        w = dataclasses.replace(mk(), inf_site=None)
+        params, grads, _, opt = build_state(w, device)
+        flag = torch.zeros(1, dtype=torch.int32, device=device)
+        fn = lambda: opt.step(grads, w.inv_loss_scale, found_inf_dev=flag, sync=False)
+        for _ in range(3):
+            fn()
+        ms = _events_ms(fn, reps)
+        gbs = STEP_BYTES[w.level] * w.n_params / (ms * 1e-3) / 1e9
+        out[name] = {"ms_per_step": ms, "Gparams/s": w.n_params / (ms * 1e-3) / 1e9,
+                     "GB/s": gbs, "frac": gbs / peak, "level": w.level,
+                     "params": w.n_params}
+        del params, grads, opt
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -388,6 +450,11 @@ def run_ours(args, wl):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, args.cpu_seconds)
+    others = None
+    if rank == 0 and world == 1 and not args.no_other_configs:
+        del params, grads, flat, opt
+        torch.cuda.empty_cache()
+        others = other_configs(device, peak)
 
     if rank == 0:
         line = {
@@ -410,6 +477,7 @@ def run_ours(args, wl):
             "clocks": sampler.summary(),
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "other_configs": others,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -178,9 +178,69 @@ step_amax_kernel(const StepDesc* __restrict__ descs,
 
 // ---------------------------------------------------------- pass 2: update
 
-// MCHECK: the first moment holds a non-finite value (its amax is not
-// finite), so its codes take the explicit NaN code.  O3: also reduce the
-// FP16 master's max |bits| per 16-bit lane into hmax.
+// Per-chunk constants of the update, as paired lanes.
+struct UpdConsts {
+  float2 k2, minv2, b1, omb1, b2, omb2, isbc2, eps2, nstep, decay, msc2;
+};
+
+__device__ __forceinline__ UpdConsts upd_consts(float k, float minv, float msc,
+                                                const StepScalars& s) {
+  UpdConsts c;
+  c.k2 = splat2(k);
+  c.minv2 = splat2(minv);
+  c.b1 = splat2(s.beta1);
+  c.omb1 = splat2(s.omb1);
+  c.b2 = splat2(s.beta2);
+  c.omb2 = splat2(s.omb2);
+  c.isbc2 = splat2(s.inv_sbc2);
+  c.eps2 = splat2(s.eps);
+  c.nstep = splat2(-s.step_size);
+  c.decay = splat2(s.decay);
+  c.msc2 = splat2(msc);
+  return c;
+}
+
+// The update of eight elements: gradient codes gc, moment codes mc, FP16 v
+// and w in; new moment codes, v and w out.  MCHECK: the first moment holds a
+// non-finite value (its amax is not finite), so its codes take the explicit
+// NaN code.  O3: also reduce the FP16 master's max |bits| per 16-bit lane
+// into hmax.
+template <int GF, bool O3, bool MCHECK>
+__device__ __forceinline__ void update8(uint2 gc, uint2 mc, uint4 vh, uint4 wh,
+                                        const UpdConsts& c, uint2& mo2,
+                                        uint4& vo4, uint4& wo4, uint32_t& hmax) {
+  uint32_t mo[4], vo[4], wo[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 g = mul2(dec2<GF>(code_pair(gc, j)), c.k2);
+    const float2 m = fma2(c.b1, mul2(dec2<kE4M3>(code_pair(mc, j)), c.minv2),
+                          mul2(c.omb1, g));
+    const float2 v = fma2(c.b2, h2_to_f2(half_pair(vh, j)),
+                          mul2(c.omb2, mul2(g, g)));
+    float2 sq;
+    sq.x = __fsqrt_rn(v.x);
+    sq.y = __fsqrt_rn(v.y);
+    const float2 den = fma2(sq, c.isbc2, c.eps2);
+    float2 u;
+    u.x = __fdiv_rn(m.x, den.x);
+    u.y = __fdiv_rn(m.y, den.y);
+    const float2 w = fma2(c.nstep, u, mul2(h2_to_f2(half_pair(wh, j)), c.decay));
+    const float2 mt = mul2(m, c.msc2);
+    mo[j] = MCHECK ? (enc1_checked<kE4M3>(mt.x) | (enc1_checked<kE4M3>(mt.y) << 8))
+                   : enc2<kE4M3>(mt.x, mt.y);
+    vo[j] = f2_to_h2(v);
+    wo[j] = f2_to_h2(w);
+  }
+  mo2 = make_uint2(mo[0] | (mo[1] << 16), mo[2] | (mo[3] << 16));
+  vo4 = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+  wo4 = make_uint4(wo[0], wo[1], wo[2], wo[3]);
+  if (O3) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) hmax = __vmaxu2(hmax, wo[j] & 0x7FFF7FFFu);
+  }
+}
+
+// The update of this thread's share of [begin, end) from global memory.
 template <int GF, bool O3, bool MCHECK>
 __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
                               float k, float minv, float msc,
@@ -188,11 +248,7 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
   constexpr int64_t kTile = (int64_t)kThreads * kGroup * kUpdGroups;
   const int tid = threadIdx.x;
   const bool vec = d.vec_ok != 0;
-  const float2 k2 = splat2(k), minv2 = splat2(minv), b1 = splat2(s.beta1),
-               omb1 = splat2(s.omb1), b2 = splat2(s.beta2),
-               omb2 = splat2(s.omb2), isbc2 = splat2(s.inv_sbc2),
-               eps2 = splat2(s.eps), nstep = splat2(-s.step_size),
-               decay = splat2(s.decay), msc2 = splat2(msc);
+  const UpdConsts c = upd_consts(k, minv, msc, s);
   // One thread asks L2 for the tile FP8OPT_UPD_PREFETCH tiles ahead (whole
   // tiles of 16-byte-aligned tensors only), so the loads below find their
   // lines on chip while the DRAM reads for later tiles are already running.
@@ -223,36 +279,12 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
 #pragma unroll
       for (int q = 0; q < kUpdGroups; ++q) {
         const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
-        uint32_t mo[4], vo[4], wo[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 g = mul2(dec2<GF>(code_pair(gc[q], j)), k2);
-          const float2 m = fma2(b1, mul2(dec2<kE4M3>(code_pair(mc[q], j)), minv2),
-                                mul2(omb1, g));
-          const float2 v = fma2(b2, h2_to_f2(half_pair(vh[q], j)),
-                                mul2(omb2, mul2(g, g)));
-          float2 sq;
-          sq.x = __fsqrt_rn(v.x);
-          sq.y = __fsqrt_rn(v.y);
-          const float2 den = fma2(sq, isbc2, eps2);
-          float2 u;
-          u.x = __fdiv_rn(m.x, den.x);
-          u.y = __fdiv_rn(m.y, den.y);
-          const float2 w = fma2(nstep, u, mul2(h2_to_f2(half_pair(wh[q], j)), decay));
-          const float2 mt = mul2(m, msc2);
-          mo[j] = MCHECK ? (enc1_checked<kE4M3>(mt.x) | (enc1_checked<kE4M3>(mt.y) << 8))
-                         : enc2<kE4M3>(mt.x, mt.y);
-          vo[j] = f2_to_h2(v);
-          wo[j] = f2_to_h2(w);
-        }
-        *reinterpret_cast<uint2*>(d.m + i0) =
-            make_uint2(mo[0] | (mo[1] << 16), mo[2] | (mo[3] << 16));
-        *reinterpret_cast<uint4*>(d.v + i0) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
-        *reinterpret_cast<uint4*>(d.w + i0) = make_uint4(wo[0], wo[1], wo[2], wo[3]);
-        if (O3) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) hmax = __vmaxu2(hmax, wo[j] & 0x7FFF7FFFu);
-        }
+        uint2 mo;
+        uint4 vo, wo;
+        update8<GF, O3, MCHECK>(gc[q], mc[q], vh[q], wh[q], c, mo, vo, wo, hmax);
+        *reinterpret_cast<uint2*>(d.m + i0) = mo;
+        *reinterpret_cast<uint4*>(d.v + i0) = vo;
+        *reinterpret_cast<uint4*>(d.w + i0) = wo;
       }
     } else {
 #pragma unroll 1
