@@ -48,6 +48,7 @@ class Param(C.Structure):
         ("g_fmt", C.c_int), ("m", C.c_void_p), ("m_scale", C.c_void_p),
         ("v", C.c_void_p), ("w", C.c_void_p), ("w8", C.c_void_p),
         ("w8_scale", C.c_void_p), ("w8_amax", C.c_void_p),
+        ("v_bound", C.c_void_p),
     ]
 
 
@@ -76,6 +77,12 @@ def lib():
         L.oracle_adamw_step.argtypes = [C.POINTER(Param), C.c_int, C.c_float,
                                         C.c_float, C.c_float, C.c_float,
                                         C.c_float, C.c_int64, C.c_float]
+        L.oracle_adam_step.restype = C.c_int
+        L.oracle_adam_step.argtypes = [C.POINTER(Param), C.c_int, C.c_int,
+                                       C.c_float, C.c_float, C.c_float,
+                                       C.c_float, C.c_float, C.c_int64, C.c_float]
+        L.oracle_v_scale_from_bound.restype = C.c_float
+        L.oracle_v_scale_from_bound.argtypes = [C.c_float]
         L.oracle_state_bytes.restype = C.c_int
         L.oracle_state_bytes.argtypes = [C.c_int]
         for nm in ("oracle_fp8_encode_array", "oracle_fp8_decode_array"):
@@ -159,9 +166,12 @@ class StepState:
     g: uint8 gradient codes; g_scale: float; g_fmt: E4M3/E5M2;
     m: uint8 E4M3 codes; m_scale: float32[1]; v, w: uint16 FP16 bits;
     O3 only: w8 uint8, w8_scale float32[1], w8_amax float32[1].
+    Scaled second moment only: v_bound float32[1] (v then holds FP16 of
+    v * 2^14 / v_bound).
     """
 
-    def __init__(self, g, g_scale, m, m_scale, v, w, g_fmt=E4M3, o3=False):
+    def __init__(self, g, g_scale, m, m_scale, v, w, g_fmt=E4M3, o3=False,
+                 scaled_v=False, v_bound=0.0):
         self.g = np.ascontiguousarray(g, dtype=np.uint8).ravel()
         self.g_scale = float(np.float32(g_scale))
         self.g_fmt = g_fmt
@@ -177,6 +187,8 @@ class StepState:
             self.w8_amax = np.zeros(1, dtype=np.float32)
         else:
             self.w8 = self.w8_scale = self.w8_amax = None
+        self.v_bound = (np.array([v_bound], dtype=np.float32) if scaled_v
+                        else None)
 
     @property
     def numel(self):
@@ -202,17 +214,24 @@ class StepState:
             p.w8 = _ptr(self.w8)
             p.w8_scale = _ptr(self.w8_scale)
             p.w8_amax = _ptr(self.w8_amax)
+        if self.v_bound is not None:
+            p.v_bound = _ptr(self.v_bound)
         return p
 
 
+def v_scale_from_bound(b: float) -> float:
+    return lib().oracle_v_scale_from_bound(b)
+
+
 def adamw_step(states: Sequence[StepState], lr, beta1, beta2, eps, wd, step,
-               inv_loss_scale) -> int:
-    """One oracle AdamW step over the list; returns found_inf (0 or 1)."""
+               inv_loss_scale, l2=False) -> int:
+    """One oracle step over the list (AdamW, or Adam with L2 decay when l2);
+    returns found_inf (0 or 1)."""
     arr = (Param * max(1, len(states)))()
     for i, s in enumerate(states):
         arr[i] = s._param()
-    rc = lib().oracle_adamw_step(arr, len(states), lr, beta1, beta2, eps, wd,
-                                 step, inv_loss_scale)
+    rc = lib().oracle_adam_step(arr, len(states), 1 if l2 else 0, lr, beta1,
+                                beta2, eps, wd, step, inv_loss_scale)
     if rc < 0:
         raise ValueError(f"oracle_adamw_step rejected its arguments ({rc})")
     return rc

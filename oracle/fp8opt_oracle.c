@@ -38,6 +38,14 @@
  *   - The first moment is re-encoded from the fp32 value of this step, with a
  *     scale taken from this step's amax; the O3 weight copy is encoded from the
  *     FP16-rounded master.
+ *   - Optional per-tensor scaled second moment (the O2 paragraph's "FP16"
+ *     state, kept clear of FP16 underflow): a per-tensor bound B on max v
+ *     follows B_new = fma(beta2, B_old, (1 - beta2) * gmax^2), gmax = max |g|
+ *     of this step; v is stored as FP16 of v * 2^14 / B_new and read back as
+ *     FP16 value * B_old * 2^-14.  B = 0 means v = 0.
+ *   - Optional Adam with L2 weight decay (torch.optim.Adam, the other
+ *     recognised optimizer): g = fma(wd, w, g) before the moments, and the
+ *     weight itself is not decayed.
  *
  * Floating point: compiled with -ffp-contract=off and no fast-math, so every
  * float expression below is evaluated as written in IEEE binary32 with
@@ -254,7 +262,20 @@ typedef struct {
     uint8_t *w8;           /* O3 only: E4M3 weight copy (out), else NULL */
     float *w8_scale;       /* O3 only: its scale (out) */
     float *w8_amax;        /* O3 only: amax of the FP16 master (out) */
+    float *v_bound;        /* scaled second moment only (in/out), else NULL */
 } oracle_param;
+
+/* Largest value a scaled second moment is stored at (as FP16 of v * scale). */
+#define OR_V_TARGET 16384.0f
+
+/* Scale of a scaled second moment from its bound: 2^14 / B, one fp32
+ * division; 1.0 when B is zero or not finite, or the quotient is not finite. */
+float oracle_v_scale_from_bound(float b)
+{
+    if (!(b > 0.0f) || !isfinite(b)) return 1.0f;
+    float q = OR_V_TARGET / b;
+    return isfinite(q) ? q : 1.0f;
+}
 
 /* Per-call scalars.  The bias corrections 1 - beta^t are evaluated in double
  * and enter only through step_size = lr / bc1 and inv_sbc2 = 1 / sqrt(bc2),
@@ -264,7 +285,7 @@ typedef struct {
 } or_scalars;
 
 static or_scalars or_make_scalars(float lr, float beta1, float beta2,
-                                  float wd, int64_t step)
+                                  float wd, int64_t step, int l2)
 {
     or_scalars s;
     double bc1 = 1.0 - pow((double)beta1, (double)step);
@@ -273,7 +294,7 @@ static or_scalars or_make_scalars(float lr, float beta1, float beta2,
     s.inv_sbc2 = (float)(1.0 / sqrt(bc2));
     s.omb1 = 1.0f - beta1;
     s.omb2 = 1.0f - beta2;
-    s.decay = 1.0f - lr * wd;
+    s.decay = l2 ? 1.0f : 1.0f - lr * wd;
     return s;
 }
 
@@ -299,17 +320,25 @@ static float or_m_new(const oracle_param *p, float minv, float g, float beta1,
     return fmaf(beta1, mp, s->omb1 * g);
 }
 
-/* One multi-tensor AdamW step with FP8 first moment and FP16 second moment.
- * Returns 1 when found_inf (nothing written), 0 after an update, -1 on a bad
- * argument. */
-int oracle_adamw_step(const oracle_param *p, int n, float lr, float beta1,
-                      float beta2, float eps, float wd, int64_t step,
-                      float inv_loss_scale)
+/* Gradient after the optional L2 decay term: fma(wd, w, g). */
+static float or_grad_l2(const oracle_param *p, float g, int l2, float wd,
+                        int64_t i)
+{
+    return l2 ? fmaf(wd, oracle_f16_to_f32(p->w[i]), g) : g;
+}
+
+/* One multi-tensor Adam step with FP8 first moment and FP16 second moment:
+ * l2 = 0 is AdamW (decoupled decay), l2 = 1 is Adam with L2 decay.  Returns 1
+ * when found_inf (nothing written), 0 after an update, -1 on a bad argument. */
+int oracle_adam_step(const oracle_param *p, int n, int l2, float lr, float beta1,
+                     float beta2, float eps, float wd, int64_t step,
+                     float inv_loss_scale)
 {
     if (n < 0 || step < 1) return -1;
-    or_scalars s = or_make_scalars(lr, beta1, beta2, wd, step);
+    or_scalars s = or_make_scalars(lr, beta1, beta2, wd, step, l2);
 
-    /* GradScaler check over every tensor before any state changes. */
+    /* GradScaler check over every tensor before any state changes (on the
+     * unscaled gradients, before any decay term). */
     for (int t = 0; t < n; ++t) {
         float k = or_grad_factor(&p[t], inv_loss_scale);
         for (int64_t i = 0; i < p[t].numel; ++i)
@@ -320,31 +349,43 @@ int oracle_adamw_step(const oracle_param *p, int n, float lr, float beta1,
         const oracle_param *q = &p[t];
         float k = or_grad_factor(q, inv_loss_scale);
         float minv = 1.0f / *q->m_scale;
+        int scaled_v = q->v_bound != NULL;
 
-        /* amax of this step's fp32 first moment -> its new scale. */
-        or_amax am = {0, 0, 0.0f};
+        /* amax of this step's fp32 first moment -> its new scale; for a
+         * scaled second moment also max |g|. */
+        or_amax am = {0, 0, 0.0f}, ag = {0, 0, 0.0f};
         for (int64_t i = 0; i < q->numel; ++i) {
-            float g = or_grad(q, k, i);
+            float g = or_grad_l2(q, or_grad(q, k, i), l2, wd, i);
             or_amax_add(&am, or_m_new(q, minv, g, beta1, &s, i));
+            if (scaled_v) or_amax_add(&ag, g);
         }
         float m_scale_new = oracle_scale_from_amax(or_amax_value(&am), OR_E4M3);
+        float vinv = 1.0f, b_new = 0.0f, v_scale_new = 1.0f;
+        if (scaled_v) {
+            float gmax = or_amax_value(&ag);
+            vinv = *q->v_bound * 0x1p-14f;
+            b_new = fmaf(beta2, *q->v_bound, s.omb2 * (gmax * gmax));
+            v_scale_new = oracle_v_scale_from_bound(b_new);
+        }
 
         or_amax aw = {0, 0, 0.0f};
         for (int64_t i = 0; i < q->numel; ++i) {
-            float g = or_grad(q, k, i);
+            float g = or_grad_l2(q, or_grad(q, k, i), l2, wd, i);
             float m = or_m_new(q, minv, g, beta1, &s, i);
             float vp = oracle_f16_to_f32(q->v[i]);
+            if (scaled_v) vp = vp * vinv;
             float wp = oracle_f16_to_f32(q->w[i]);
             float v = fmaf(beta2, vp, s.omb2 * (g * g));
             float denom = fmaf(sqrtf(v), s.inv_sbc2, eps);
             float upd = m / denom;
             float w = fmaf(-s.step_size, upd, wp * s.decay);
             q->m[i] = oracle_fp8_encode(m * m_scale_new, OR_E4M3);
-            q->v[i] = oracle_f32_to_f16(v);
+            q->v[i] = oracle_f32_to_f16(scaled_v ? v * v_scale_new : v);
             q->w[i] = oracle_f32_to_f16(w);
             if (q->w8) or_amax_add(&aw, oracle_f16_to_f32(q->w[i]));
         }
         *q->m_scale = m_scale_new;
+        if (scaled_v) *q->v_bound = b_new;
 
         /* O3: FP8 weight copy encoded from the FP16 master. */
         if (q->w8) {
@@ -358,6 +399,15 @@ int oracle_adamw_step(const oracle_param *p, int n, float lr, float beta1,
         }
     }
     return 0;
+}
+
+/* AdamW: oracle_adam_step with decoupled weight decay. */
+int oracle_adamw_step(const oracle_param *p, int n, float lr, float beta1,
+                      float beta2, float eps, float wd, int64_t step,
+                      float inv_loss_scale)
+{
+    return oracle_adam_step(p, n, 0, lr, beta1, beta2, eps, wd, step,
+                            inv_loss_scale);
 }
 
 /* Optimizer-state bytes per parameter for a level of the MS-AMP table:

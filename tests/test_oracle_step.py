@@ -232,3 +232,152 @@ def test_state_footprint_is_the_published_saving(orc):
     st = make_states(orc, [10], np.random.default_rng(0))[0]
     assert st.m.itemsize + st.v.itemsize == orc.state_bytes(2) == 3
     assert 100.0 * (1 - orc.state_bytes(2) / orc.state_bytes(0)) == saving
+
+
+# ------------------------------------------- scaled second moment, Adam L2
+
+def make_states_v(orc, sizes, rng, g_sigma, scaled_v, o3=False):
+    """Fresh state (m = v = 0), gradients N(0, g_sigma) cast to E4M3."""
+    out = []
+    for n in sizes:
+        g, _, gs = orc.cast_scaled(
+            (rng.standard_normal(n) * g_sigma).astype(np.float32), F32, E4M3)
+        w = (rng.standard_normal(n) * 0.02).astype(np.float16).view(np.uint16)
+        out.append(orc.StepState(g, gs, np.zeros(n, np.uint8), 1.0,
+                                 np.zeros(n, np.uint16), w, o3=o3,
+                                 scaled_v=scaled_v))
+    return out
+
+
+def stored_v(st):
+    """The second moment a state holds, as float64."""
+    v = f16(st.v)
+    if st.v_bound is not None:
+        v = v * (float(st.v_bound[0]) * 2.0 ** -14)
+    return v
+
+
+def torch_step_f64(st, lr, b1, b2, eps, wd, step, ils, l2):
+    """One torch.optim.AdamW (or torch.optim.Adam with L2 weight decay) step
+    in float64 from the state's dequantized values."""
+    p = torch.nn.Parameter(f16(st.w).clone())
+    p.grad = tdec(st.g, st.g_fmt) / float(st.g_scale) * ils
+    cls = torch.optim.Adam if l2 else torch.optim.AdamW
+    opt = cls([p], lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd,
+              foreach=False)
+    opt.state[p] = {"step": torch.tensor(float(step - 1)),
+                    "exp_avg": tdec(st.m) / float(st.m_scale[0]),
+                    "exp_avg_sq": stored_v(st).clone()}
+    opt.step()
+    return p.detach(), opt.state[p]["exp_avg_sq"]
+
+
+def run_against_torch(orc, states, steps, lr, b1, b2, eps, wd, l2, rng,
+                      g_sigma):
+    """Steps 1..steps; each step compares the oracle with torch in float64
+    from the same dequantized state; returns the worst relative v error and
+    the fraction of weights within one FP16 ulp."""
+    worst_v, w_ok = 0.0, []
+    for t in range(1, steps + 1):
+        for s in states:
+            g, _, gs = orc.cast_scaled(
+                (rng.standard_normal(s.numel) * g_sigma).astype(np.float32), F32, E4M3)
+            s.g, s.g_scale = g, float(gs)
+        before = [s.copy() for s in states]
+        assert orc.adamw_step(states, lr, b1, b2, eps, wd, t, 1.0, l2=l2) == 0
+        for s0, s1 in zip(before, states):
+            w64, v64 = torch_step_f64(s0, lr, b1, b2, eps, wd, t, 1.0, l2)
+            got = stored_v(s1).numpy()
+            ref = v64.numpy()
+            big = ref > ref.max() * 2.0 ** -20
+            worst_v = max(worst_v, float(np.max(np.abs(got - ref)[big] / ref[big])))
+            rne = f16_bits(w64).astype(np.int32)
+            w_ok.append(np.abs(s1.w.astype(np.int32) - rne) <= 1)
+    return worst_v, float(np.mean(np.concatenate(w_ok)))
+
+
+def free_run_weight_change(orc, scaled_v, g_sigma, steps=3):
+    """The oracle and torch.optim.AdamW (float64 state throughout) run side by
+    side on the same dequantized gradients; returns the median relative
+    difference of their total weight change."""
+    lr, betas, eps, wd = 1e-3, (0.9, 0.999), 1e-8, 0.0
+    states = make_states_v(orc, [3000], np.random.default_rng(1), g_sigma, scaled_v)
+    st = states[0]
+    w0 = f16(st.w).clone()
+    p = torch.nn.Parameter(w0.clone())
+    opt = torch.optim.AdamW([p], lr=lr, betas=betas, eps=eps, weight_decay=wd,
+                            foreach=False)
+    rng = np.random.default_rng(2)
+    for t in range(1, steps + 1):
+        g, _, gs = orc.cast_scaled((rng.standard_normal(3000) * g_sigma)
+                                   .astype(np.float32), F32, E4M3)
+        st.g, st.g_scale = g, float(gs)
+        p.grad = tdec(g) / float(gs)
+        opt.step()
+        assert orc.adamw_step(states, lr, *betas, eps, wd, t, 1.0) == 0
+    dw_torch = (p.detach() - w0).numpy()
+    dw_oracle = (f16(st.w) - w0).numpy()
+    keep = np.abs(dw_torch) > 1e-4
+    return float(np.median(np.abs(dw_oracle - dw_torch)[keep] / np.abs(dw_torch)[keep]))
+
+
+def test_scaled_v_follows_torch_where_plain_fp16_underflows(orc):
+    """Gradients near 1e-5: (1 - beta2) g^2 ~ 1e-13 is below FP16's smallest
+    subnormal, so a plain FP16 second moment stores 0 and every later step
+    sees only its own (1 - beta2) g^2, off by the whole history; the scaled
+    second moment keeps the trajectory torch's AdamW takes (to the precision
+    of the E4M3 first moment and the FP16 weights)."""
+    assert free_run_weight_change(orc, False, 1e-5) > 0.3      # the hazard
+    assert free_run_weight_change(orc, True, 1e-5) < 0.02
+    # with gradients FP16 can hold, both follow torch
+    assert free_run_weight_change(orc, False, 1e-1) < 0.02
+    assert free_run_weight_change(orc, True, 1e-1) < 0.02
+
+
+@pytest.mark.parametrize("l2", [False, True])
+@pytest.mark.parametrize("o3", [False, True])
+def test_scaled_v_and_l2_match_torch_over_steps(orc, l2, o3):
+    states = make_states_v(orc, [37, 1000, 2048], np.random.default_rng(3), 1e-2,
+                           True, o3=o3)
+    worst, ok = run_against_torch(orc, states, 5, lr=3e-3, b1=0.9, b2=0.99,
+                                  eps=1e-6, wd=0.1, l2=l2,
+                                  rng=np.random.default_rng(4), g_sigma=1e-2)
+    assert worst <= 2.0 ** -10
+    assert ok >= 0.99
+
+
+def test_l2_mode_plain_v_matches_torch_adam(orc):
+    """Adam with L2 decay on the plain FP16 second moment (gradients large
+    enough for FP16): torch.optim.Adam with weight_decay."""
+    states = make_states_v(orc, [500, 64], np.random.default_rng(5), 1e-2, False)
+    worst, ok = run_against_torch(orc, states, 4, lr=1e-2, b1=0.8, b2=0.95,
+                                  eps=1e-4, wd=0.3, l2=True,
+                                  rng=np.random.default_rng(6), g_sigma=1e-2)
+    assert ok >= 0.99
+
+
+def test_v_bound_holds_and_stays_below_fp16_overflow(orc):
+    rng = np.random.default_rng(7)
+    states = make_states_v(orc, [4096], rng, 1e-3, True)
+    st = states[0]
+    for t in range(1, 11):
+        sigma = 10.0 ** rng.uniform(-6, -1)           # gradients jump around
+        g, _, gs = orc.cast_scaled((rng.standard_normal(4096) * sigma)
+                                   .astype(np.float32), F32, E4M3)
+        st.g, st.g_scale = g, float(gs)
+        assert orc.adamw_step(states, 1e-3, 0.9, 0.999, 1e-8, 0.0, t, 1.0) == 0
+        codes = f16(st.v).numpy()
+        assert codes.max() <= 16384 * (1 + 2.0 ** -9)   # far below 65504
+        assert stored_v(st).max().item() <= st.v_bound[0] * (1 + 2.0 ** -9)
+        assert codes.max() >= 16384 / 4096           # the bound is not loose
+
+
+def test_found_inf_leaves_v_bound_unchanged(orc):
+    states = make_states_v(orc, [100], np.random.default_rng(8), 1e-3, True)
+    assert orc.adamw_step(states, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0) == 0
+    b = states[0].v_bound.copy()
+    states[0].g[3] = 0x7F
+    before = states[0].copy()
+    assert orc.adamw_step(states, 1e-3, 0.9, 0.999, 1e-8, 0.0, 2, 1.0) == 1
+    assert np.array_equal(states[0].v_bound, b)
+    assert np.array_equal(states[0].v, before.v)
