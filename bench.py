@@ -240,7 +240,7 @@ def run_reference(args, wl):
 
 # ---------------------------------------------------------------- GPU leg
 
-def build_state(wl, device):
+def build_state(wl, device, **opt_kw):
     import torch
     import bit_optimizer_gb300 as bo
     numels = wl.numels
@@ -252,7 +252,8 @@ def build_state(wl, device):
         g.copy_(wl.grad(i, 1, device))
     torch.cuda.synchronize()
     opt = bo.Fp8AdamW(params, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
-                      weight_decay=wl.wd, level=wl.level, grad_fmt=wl.grad_fmt)
+                      weight_decay=wl.wd, level=wl.level, grad_fmt=wl.grad_fmt,
+                      **opt_kw)
     return params, grads, flat, opt
 
 
@@ -315,8 +316,9 @@ def other_configs(device, peak):
     """The remaining workloads, each timed on its own after the headline:
     the scaled cast of the 124M GPT-2 list (BF16 -> E4M3 and -> E5M2, 5 B per
     element), the O2 step on the 350M list (the inf cleared), the O3 step on
-    the 1.3B list (20 B per param with the cast), and the launch-bound tiny
-    list."""
+    the 1.3B list (20 B per param with the cast), the same with the scaled
+    second moment, Adam with L2 decay on the 350M list, and the launch-bound
+    tiny list."""
     import dataclasses
     import torch
     import synth
@@ -338,19 +340,29 @@ def other_configs(device, peak):
         out[f"cast_gpt2_124m_{fmt}"] = {"ms": ms, "GB/s": gbs, "frac": gbs / peak,
                                         "bytes_per_elem": 5}
     del srcs, codes
-    for name, mk, reps in (("o2_350m", synth.o2_350m, 20),
-                           ("o3_1p3b", synth.o3_1p3b, 10), ("tiny", synth.tiny, 200)):
+    # (name, workload, reps, optimizer options, algorithmic bytes per param)
+    runs = (
+        ("o2_350m", synth.o2_350m, 20, {}, STEP_BYTES["O2"]),
+        ("o3_1p3b", synth.o3_1p3b, 10, {}, STEP_BYTES["O3"]),
+        ("o3_1p3b_scaled_v", synth.o3_1p3b, 10, {"scaled_v": True},
+         STEP_BYTES["O3"]),
+        # Adam with L2 decay runs as two calls and its first pass reads w:
+        # cast 5 + first pass 4 + update 11
+        ("o2_350m_adam_l2", synth.o2_350m, 20, {"l2": True}, 20),
+        ("tiny", synth.tiny, 200, {}, STEP_BYTES["O2"]),
+    )
+    for name, mk, reps, kw, bpp in runs:
         w = dataclasses.replace(mk(), inf_site=None)
-        params, grads, _, opt = build_state(w, device)
+        params, grads, _, opt = build_state(w, device, **kw)
         flag = torch.zeros(1, dtype=torch.int32, device=device)
         fn = lambda: opt.step(grads, w.inv_loss_scale, found_inf_dev=flag, sync=False)
         for _ in range(3):
             fn()
         ms = _events_ms(fn, reps)
-        gbs = STEP_BYTES[w.level] * w.n_params / (ms * 1e-3) / 1e9
+        gbs = bpp * w.n_params / (ms * 1e-3) / 1e9
         out[name] = {"ms_per_step": ms, "Gparams/s": w.n_params / (ms * 1e-3) / 1e9,
                      "GB/s": gbs, "frac": gbs / peak, "level": w.level,
-                     "params": w.n_params}
+                     "params": w.n_params, "bytes_per_param": bpp, **kw}
         del params, grads, opt
         torch.cuda.empty_cache()
     return out

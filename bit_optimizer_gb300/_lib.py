@@ -18,7 +18,8 @@ F32, BF16, F16 = 0, 1, 2
 OK, ERR_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_LIMIT = 0, -1, -2, -4, -5
 
 # Every entry point the header declares.
-EXPORTS = ("fp8_cast_scaled", "fp8_adamw_step", "fp8_cast_adamw_step",
+EXPORTS = ("fp8_cast_scaled", "fp8_adamw_step", "fp8_adam_step",
+           "fp8_cast_adamw_step",
            "fp8_cast_scaled_noalloc", "fp8opt_strerror",
            "fp8opt_last_error", "fp8opt_timing_enable", "fp8opt_timing_read",
            "fp8opt_release")
@@ -42,6 +43,7 @@ class Param(C.Structure):
         ("g_fmt", C.c_int32), ("reserved", C.c_int32), ("m", C.c_void_p),
         ("m_scale", C.c_void_p), ("v", C.c_void_p), ("w", C.c_void_p),
         ("w8", C.c_void_p), ("w8_scale", C.c_void_p), ("w8_amax", C.c_void_p),
+        ("v_bound", C.c_void_p),
     ]
 
 
@@ -67,6 +69,11 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     L.fp8_cast_scaled.restype = C.c_int
     L.fp8_cast_scaled.argtypes = [C.POINTER(CastItem), C.c_int, C.c_int,
                                   C.c_void_p]
+    L.fp8_adam_step.restype = C.c_int
+    L.fp8_adam_step.argtypes = [
+        C.POINTER(Param), C.c_int, C.c_float, C.c_float, C.c_float, C.c_float,
+        C.c_float, C.c_int64, C.c_float, C.POINTER(C.c_int), C.c_void_p,
+        C.c_void_p]
     L.fp8_cast_adamw_step.restype = C.c_int
     L.fp8_cast_adamw_step.argtypes = [
         C.POINTER(CastItem), C.POINTER(Param), C.c_int, C.c_int, C.c_float,

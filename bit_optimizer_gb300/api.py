@@ -143,11 +143,13 @@ class AdamWPlan:
     g: uint8 gradient codes per tensor; g_scale: float32 vector (n);
     m: uint8 E4M3 first moments; m_scale: float32 vector (n); v: float16
     second moments; w: float16 weights (O2) or masters (O3).  O3 when w8 (uint8
-    per tensor), w8_scale and w8_amax (float32 vectors) are given.
+    per tensor), w8_scale and w8_amax (float32 vectors) are given.  A scaled
+    second moment when v_bound (float32 vector, one bound per tensor, 0 with
+    v = 0 at the start) is given.
     """
 
     def __init__(self, g, g_scale, m, m_scale, v, w, w8=None, w8_scale=None,
-                 w8_amax=None, g_fmt="e4m3"):
+                 w8_amax=None, g_fmt="e4m3", v_bound=None):
         n = len(g)
         if not (len(m) == len(v) == len(w) == n):
             raise ValueError("g, m, v and w differ in length")
@@ -157,7 +159,8 @@ class AdamWPlan:
         self.n = n
         self.o3 = o3
         self._keep = (list(g), g_scale, list(m), m_scale, list(v), list(w),
-                      None if w8 is None else list(w8), w8_scale, w8_amax)
+                      None if w8 is None else list(w8), w8_scale, w8_amax,
+                      v_bound)
         fmts = g_fmt if isinstance(g_fmt, (list, tuple)) else [g_fmt] * n
         self._params = (Param * max(n, 1))()
         for i in range(n):
@@ -181,22 +184,25 @@ class AdamWPlan:
                 p.w8 = w8[i].data_ptr()
                 p.w8_scale = _slot_ptr(w8_scale, i, "w8_scale")
                 p.w8_amax = _slot_ptr(w8_amax, i, "w8_amax")
+            if v_bound is not None:
+                p.v_bound = _slot_ptr(v_bound, i, "v_bound")
         self._found = C.c_int(0)
 
     def __call__(self, lr, beta1, beta2, eps, wd, step, inv_loss_scale=1.0,
                  found_inf_dev: Optional[torch.Tensor] = None, sync=True,
-                 stream=None) -> Optional[int]:
-        """Runs one step.  sync=True returns found_inf (0/1) after waiting
-        for the stream; sync=False returns None without waiting (found_inf is
-        then only in found_inf_dev, a uint32/int32 CUDA tensor, if given)."""
+                 stream=None, l2=False) -> Optional[int]:
+        """Runs one step: AdamW, or Adam with L2 decay when l2.  sync=True
+        returns found_inf (0/1) after waiting for the stream; sync=False
+        returns None without waiting (found_inf is then only in
+        found_inf_dev, a uint32/int32 CUDA tensor, if given)."""
         fdev = None
         if found_inf_dev is not None:
             _cuda(found_inf_dev, "found_inf_dev")
             fdev = found_inf_dev.data_ptr()
         fptr = C.byref(self._found) if sync else None
-        check(load().fp8_adamw_step(self._params, self.n, lr, beta1, beta2, eps,
-                                    wd, int(step), inv_loss_scale, fptr, fdev,
-                                    _stream_ptr(stream)))
+        fn = load().fp8_adam_step if l2 else load().fp8_adamw_step
+        check(fn(self._params, self.n, lr, beta1, beta2, eps, wd, int(step),
+                 inv_loss_scale, fptr, fdev, _stream_ptr(stream)))
         return self._found.value if sync else None
 
 
@@ -246,6 +252,10 @@ class Fp8AdamW:
     level "O2": FP16 weights updated in place; E4M3 first moment, FP16 second
     moment.  level "O3": the FP16 tensors are master weights, and after each
     step ``w8`` / ``w8_scale`` hold their E4M3 copies for forward/backward.
+    ``scaled_v``: the FP16 second moment is kept relative to a per-tensor
+    bound (``v_bound``), so small gradients do not underflow it.  ``l2``:
+    Adam with L2 weight decay (torch.optim.Adam) instead of AdamW; it runs as
+    two calls (the fused call is AdamW only).
 
     ``step(grads, inv_loss_scale)`` casts the gradients to FP8 (per-tensor
     just-in-time scale) and runs the update; it returns found_inf and, like a
@@ -255,7 +265,7 @@ class Fp8AdamW:
 
     def __init__(self, params: Sequence[torch.Tensor], lr=1e-3,
                  betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01, level="O2",
-                 grad_fmt="e4m3", fused=True):
+                 grad_fmt="e4m3", fused=True, scaled_v=False, l2=False):
         if level not in ("O2", "O3"):
             raise ValueError("level must be 'O2' or 'O3'")
         self.params = list(params)
@@ -266,7 +276,8 @@ class Fp8AdamW:
         self.lr, (self.beta1, self.beta2) = lr, betas
         self.eps, self.wd = eps, weight_decay
         self.level, self.grad_fmt = level, grad_fmt
-        self.fused = fused        # one fp8_cast_adamw_step call per step
+        self.l2 = l2
+        self.fused = fused and not l2   # one fp8_cast_adamw_step call per step
         self.step_count = 0
         n = len(self.params)
         dev = self.params[0].device if n else torch.device("cuda")
@@ -284,9 +295,11 @@ class Fp8AdamW:
             self.w8_amax = torch.zeros(max(n, 1), dtype=torch.float32, device=dev)
         else:
             self.w8 = self.w8_scale = self.w8_amax = None
+        self.v_bound = (torch.zeros(max(n, 1), dtype=torch.float32, device=dev)
+                        if scaled_v else None)
         self._plan = AdamWPlan(self.g_codes, self.g_scale, self.m, self.m_scale,
                                self.v, w, self.w8, self.w8_scale, self.w8_amax,
-                               grad_fmt)
+                               grad_fmt, self.v_bound)
         self._cast_key = None
         self._cast = None
         self._cast_step = None
@@ -317,7 +330,8 @@ class Fp8AdamW:
         else:
             cast(stream)
             found = self._plan(self.lr, self.beta1, self.beta2, self.eps, self.wd,
-                               t, inv_loss_scale, found_inf_dev, sync, stream)
+                               t, inv_loss_scale, found_inf_dev, sync, stream,
+                               l2=self.l2)
         if not sync or found == 0:
             self.step_count = t
         return found
@@ -327,7 +341,8 @@ class Fp8AdamW:
              "grad_fmt": self.grad_fmt,
              "hparams": (self.lr, self.beta1, self.beta2, self.eps, self.wd),
              "m": [t.clone() for t in self.m], "v": [t.clone() for t in self.v],
-             "m_scale": self.m_scale.clone()}
+             "m_scale": self.m_scale.clone(), "l2": self.l2,
+             "v_bound": None if self.v_bound is None else self.v_bound.clone()}
         if self.level == "O3":
             d["w8"] = [t.clone() for t in self.w8]
             d["w8_scale"] = self.w8_scale.clone()
@@ -344,6 +359,10 @@ class Fp8AdamW:
         for dst, src in zip(self.v, d["v"]):
             dst.copy_(src)
         self.m_scale.copy_(d["m_scale"])
+        if (d.get("v_bound") is None) != (self.v_bound is None):
+            raise ValueError("state dict and optimizer differ in scaled_v")
+        if self.v_bound is not None:
+            self.v_bound.copy_(d["v_bound"])
         if self.level == "O3":
             for dst, src in zip(self.w8, d["w8"]):
                 dst.copy_(src)

@@ -25,7 +25,8 @@ cudaError_t launch_step(const StepDesc* descs, const Chunk* chunks,
                         uint32_t nchunks_o3, const StepScratch& sc,
                         const StepScalars& s, uint32_t epoch,
                         uint32_t* found_dev, int grid_amax, int grid_update,
-                        int grid_w8, cudaStream_t stream, LaunchMark mark);
+                        int grid_w8, bool any_vs, cudaStream_t stream,
+                        LaunchMark mark);
 cudaError_t step_occupancy(int* amax_per_sm, int* update_per_sm, int* w8_per_sm);
 cudaError_t launch_cast_step(const CastDesc* cdescs, const StepDesc* sdescs,
                              const Chunk* chunks, uint32_t nchunks,
@@ -33,8 +34,8 @@ cudaError_t launch_cast_step(const CastDesc* cdescs, const StepDesc* sdescs,
                              unsigned long long* gslots, const StepScratch& sc,
                              const StepScalars& s, uint32_t epoch, int fmt,
                              uint32_t* found_dev, int grid_amax, int grid_fused,
-                             int grid_update, int grid_w8, cudaStream_t stream,
-                             LaunchMark mark);
+                             int grid_update, int grid_w8, bool any_vs,
+                             cudaStream_t stream, LaunchMark mark);
 cudaError_t cast_step_occupancy(int* per_sm);
 
 namespace {
@@ -103,6 +104,7 @@ struct Workspace {
   std::vector<fp8opt_param> step_key;
   DevBuf step_descs, step_chunks;
   uint32_t step_nchunks = 0, step_nchunks_o3 = 0;
+  bool step_any_vs = false;   // some record has a scaled second moment
   bool have_cast = false, have_step = false;
 
   void release() {
@@ -326,7 +328,7 @@ int check_step_args(const char* fn, const fp8opt_param* params, int n,
 // Per-call scalars: the bias corrections 1 - beta^t in double, entering only
 // through lr / bc1 and 1 / sqrt(bc2), each rounded to fp32 once.
 StepScalars make_scalars(float lr, float beta1, float beta2, float eps, float wd,
-                         int64_t step, float inv_loss_scale) {
+                         int64_t step, float inv_loss_scale, bool l2) {
   StepScalars s;
   const double bc1 = 1.0 - std::pow((double)beta1, (double)step);
   const double bc2 = 1.0 - std::pow((double)beta2, (double)step);
@@ -337,8 +339,10 @@ StepScalars make_scalars(float lr, float beta1, float beta2, float eps, float wd
   s.omb2 = 1.0f - beta2;
   s.step_size = (float)((double)lr / bc1);
   s.inv_sbc2 = (float)(1.0 / std::sqrt(bc2));
-  s.decay = 1.0f - lr * wd;
+  s.decay = l2 ? 1.0f : 1.0f - lr * wd;
   s.ils = inv_loss_scale;
+  s.wd = wd;
+  s.l2 = l2 ? 1 : 0;
   return s;
 }
 
@@ -403,6 +407,7 @@ int ensure_step_tables(const char* fn, Workspace* ws, const fp8opt_param* params
     d.m_scale = p.m_scale;
     d.w8_scale = p.w8_scale;
     d.w8_amax = p.w8_amax;
+    d.v_bound = p.v_bound;
     d.numel = p.numel;
     d.g_fmt = p.g_fmt;
     d.o3 = p.w8_scale != nullptr;
@@ -426,6 +431,8 @@ int ensure_step_tables(const char* fn, Workspace* ws, const fp8opt_param* params
   ws->step_key.assign(params, params + n);
   ws->step_nchunks = nmain;
   ws->step_nchunks_o3 = no3;
+  ws->step_any_vs = false;
+  for (int i = 0; i < n; ++i) ws->step_any_vs |= params[i].v_bound != nullptr;
   ws->have_step = true;
   return FP8OPT_OK;
 }
@@ -480,16 +487,20 @@ extern "C" int fp8_cast_scaled(const fp8opt_cast_item* items, int n, int fmt,
   return FP8OPT_OK;
 }
 
-extern "C" int fp8_adamw_step(const fp8opt_param* params, int n, float lr,
-                              float beta1, float beta2, float eps, float wd,
-                              int64_t step, float inv_loss_scale, int* found_inf,
-                              uint32_t* found_inf_dev, void* stream_ptr) {
-  const char* fn = "fp8_adamw_step";
+namespace fp8opt {
+namespace {
+
+// The two step entry points: AdamW (l2 false) and Adam with L2 decay.
+int adam_step(const char* fn, bool l2, const fp8opt_param* params, int n,
+              float lr, float beta1, float beta2, float eps, float wd,
+              int64_t step, float inv_loss_scale, int* found_inf,
+              uint32_t* found_inf_dev, void* stream_ptr) {
   int st = check_step_args(fn, params, n, step);
   if (st != FP8OPT_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   if (n == 0) return empty_step(fn, found_inf, found_inf_dev, stream);
-  const StepScalars s = make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale);
+  const StepScalars s =
+      make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale, l2);
 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0;
@@ -499,24 +510,46 @@ extern "C" int fp8_adamw_step(const fp8opt_param* params, int n, float lr,
   if ((st = ensure_step_tables(fn, ws, params, n, stream)) != FP8OPT_OK) return st;
 
   uint32_t epoch = 0;
-  // slots: [0, n) amax of m, [n, 2n) amax of the master, [2n] found_inf
-  cudaError_t e = prepare_slots(ws, 2 * (size_t)n + 1, stream, &epoch);
-  if (e == cudaSuccess) e = ws->saved_scales.reserve((size_t)n * sizeof(float));
-  if (e != cudaSuccess) return cuda_fail(e, "fp8_adamw_step: workspace");
+  // slots: [0, n) amax of m, [n, 2n) amax of the master, [2n, 3n) max |g|,
+  // [3n] found_inf; saved: [0, n) m_scale, [n, 2n) v_bound
+  cudaError_t e = prepare_slots(ws, 3 * (size_t)n + 1, stream, &epoch);
+  if (e == cudaSuccess) e = ws->saved_scales.reserve(2 * (size_t)n * sizeof(float));
+  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": workspace").c_str());
   unsigned long long* slots = static_cast<unsigned long long*>(ws->slots.ptr);
   StepScratch sc;
   sc.amax_m = slots;
   sc.amax_w = slots + n;
-  sc.found = slots + 2 * (size_t)n;
+  sc.amax_g = slots + 2 * (size_t)n;
+  sc.found = slots + 3 * (size_t)n;
   sc.old_m_scale = static_cast<float*>(ws->saved_scales.ptr);
+  sc.old_v_bound = sc.old_m_scale + n;
   const Chunk* chunks = static_cast<const Chunk*>(ws->step_chunks.ptr);
   e = launch_step(static_cast<const StepDesc*>(ws->step_descs.ptr), chunks,
                   ws->step_nchunks, chunks + ws->step_nchunks, ws->step_nchunks_o3,
                   sc, s, epoch, found_inf_dev, info->step_amax, info->step_update,
-                  info->step_w8, stream, launch_mark());
-  if (e != cudaSuccess) return cuda_fail(e, "fp8_adamw_step: launch");
+                  info->step_w8, ws->step_any_vs, stream, launch_mark());
+  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
   if (found_inf != nullptr) return read_found(fn, sc.found, epoch, stream, found_inf);
   return FP8OPT_OK;
+}
+
+}  // namespace
+}  // namespace fp8opt
+
+extern "C" int fp8_adamw_step(const fp8opt_param* params, int n, float lr,
+                              float beta1, float beta2, float eps, float wd,
+                              int64_t step, float inv_loss_scale, int* found_inf,
+                              uint32_t* found_inf_dev, void* stream_ptr) {
+  return adam_step("fp8_adamw_step", false, params, n, lr, beta1, beta2, eps, wd,
+                   step, inv_loss_scale, found_inf, found_inf_dev, stream_ptr);
+}
+
+extern "C" int fp8_adam_step(const fp8opt_param* params, int n, float lr,
+                             float beta1, float beta2, float eps, float wd,
+                             int64_t step, float inv_loss_scale, int* found_inf,
+                             uint32_t* found_inf_dev, void* stream_ptr) {
+  return adam_step("fp8_adam_step", true, params, n, lr, beta1, beta2, eps, wd,
+                   step, inv_loss_scale, found_inf, found_inf_dev, stream_ptr);
 }
 
 extern "C" int fp8_cast_adamw_step(const fp8opt_cast_item* grads,
@@ -539,7 +572,8 @@ extern "C" int fp8_cast_adamw_step(const fp8opt_cast_item* grads,
   }
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   if (n == 0) return empty_step(fn, found_inf, found_inf_dev, stream);
-  const StepScalars s = make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale);
+  const StepScalars s =
+      make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale, false);
 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0;
@@ -550,24 +584,27 @@ extern "C" int fp8_cast_adamw_step(const fp8opt_cast_item* grads,
   if ((st = ensure_step_tables(fn, ws, params, n, stream)) != FP8OPT_OK) return st;
 
   // slots: [0, n) gradient amax, [n, 2n) amax of m, [2n, 3n) amax of the
-  // master, [3n] found_inf
+  // master, [3n, 4n) max |g|, [4n] found_inf; saved: m_scale, v_bound
   uint32_t epoch = 0;
-  cudaError_t e = prepare_slots(ws, 3 * (size_t)n + 1, stream, &epoch);
-  if (e == cudaSuccess) e = ws->saved_scales.reserve((size_t)n * sizeof(float));
+  cudaError_t e = prepare_slots(ws, 4 * (size_t)n + 1, stream, &epoch);
+  if (e == cudaSuccess) e = ws->saved_scales.reserve(2 * (size_t)n * sizeof(float));
   if (e != cudaSuccess) return cuda_fail(e, "fp8_cast_adamw_step: workspace");
   unsigned long long* slots = static_cast<unsigned long long*>(ws->slots.ptr);
   StepScratch sc;
   sc.amax_m = slots + n;
   sc.amax_w = slots + 2 * (size_t)n;
-  sc.found = slots + 3 * (size_t)n;
+  sc.amax_g = slots + 3 * (size_t)n;
+  sc.found = slots + 4 * (size_t)n;
   sc.old_m_scale = static_cast<float*>(ws->saved_scales.ptr);
+  sc.old_v_bound = sc.old_m_scale + n;
   const Chunk* chunks = static_cast<const Chunk*>(ws->step_chunks.ptr);
   e = launch_cast_step(static_cast<const CastDesc*>(ws->cast_descs.ptr),
                        static_cast<const StepDesc*>(ws->step_descs.ptr), chunks,
                        ws->step_nchunks, chunks + ws->step_nchunks,
                        ws->step_nchunks_o3, slots, sc, s, epoch, fmt,
                        found_inf_dev, info->cast_amax, info->cast_step,
-                       info->step_update, info->step_w8, stream, launch_mark());
+                       info->step_update, info->step_w8, ws->step_any_vs, stream,
+                       launch_mark());
   if (e != cudaSuccess) return cuda_fail(e, "fp8_cast_adamw_step: launch");
   if (found_inf != nullptr) return read_found(fn, sc.found, epoch, stream, found_inf);
   return FP8OPT_OK;

@@ -60,6 +60,7 @@ struct StepDesc {
   float* m_scale;
   float* w8_scale;
   float* w8_amax;
+  float* v_bound;   // scaled second moment: its bound (in/out), else NULL
   int64_t numel;
   int32_t g_fmt;
   int16_t vec_ok;
@@ -79,14 +80,21 @@ typedef void (*LaunchMark)(int kernel, int end, cudaStream_t stream);
 // inv_sbc2 = 1 / sqrt(1 - beta2^t), each evaluated in double and rounded once.
 struct StepScalars {
   float beta1, beta2, eps, omb1, omb2, step_size, inv_sbc2, decay, ils;
+  float wd;       // the L2 coefficient (used when l2)
+  int32_t l2;     // Adam with L2 decay: g = fma(wd, w, g); decay is then 1
 };
+
+// A scaled second moment is stored as FP16 of v * kVTarget / bound.
+constexpr float kVTarget = 16384.0f;
 
 // Scratch of one step call: per-tensor slots and the old first-moment scales.
 struct StepScratch {
   unsigned long long* amax_m;   // [n] amax of this step's fp32 first moment
   unsigned long long* amax_w;   // [n] amax of the FP16 master (O3)
+  unsigned long long* amax_g;   // [n] max |g| (scaled second moment)
   unsigned long long* found;    // [1] found_inf
   float* old_m_scale;           // [n] m_scale before this step
+  float* old_v_bound;           // [n] v_bound before this step
 };
 
 // ------------------------------------------------------------------ helpers
@@ -114,6 +122,14 @@ __device__ __forceinline__ float scale_from_amax_bits(uint32_t bits,
   float amax = __uint_as_float(bits);
   if (!(amax > 0.0f) || bits >= 0x7F800000u) return 1.0f;
   float q = __fdiv_rn(fp8_max, amax);
+  return (__float_as_uint(q) & 0x7FFFFFFFu) >= 0x7F800000u ? 1.0f : q;
+}
+
+// Scale of a scaled second moment from its bound: kVTarget / bound, with
+// the same guards as scale_from_amax_bits.
+__device__ __forceinline__ float v_scale_from_bound(float b) {
+  if (!(b > 0.0f) || (__float_as_uint(b) & 0x7FFFFFFFu) >= 0x7F800000u) return 1.0f;
+  const float q = __fdiv_rn(kVTarget, b);
   return (__float_as_uint(q) & 0x7FFFFFFFu) >= 0x7F800000u ? 1.0f : q;
 }
 

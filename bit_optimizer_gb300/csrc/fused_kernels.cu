@@ -32,7 +32,8 @@ cudaError_t launch_step_update(const StepDesc* descs, const Chunk* chunks,
                                uint32_t nchunks_o3, const StepScratch& sc,
                                const StepScalars& s, uint32_t epoch,
                                uint32_t* found_dev, int grid_update, int grid_w8,
-                               cudaStream_t stream, LaunchMark mark);
+                               bool any_vs, cudaStream_t stream,
+                               LaunchMark mark);
 
 namespace {
 
@@ -51,12 +52,13 @@ __device__ __forceinline__ uint32_t enc_pair(float2 t) {
 }
 
 // This thread's share of [begin, end): encode, store the codes, and fold the
-// step's first pass into mx (max |m| bits) and bad (non-finite gradient).
-template <int DT, int FMT, bool CHECKED, bool SAFE>
+// step's first pass into mx (max |m| bits), gx (max |g| bits, when GX: for a
+// scaled second moment) and bad (non-finite gradient).
+template <int DT, int FMT, bool CHECKED, bool SAFE, bool GX>
 __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
                                  int64_t begin, int64_t end, float scale,
                                  float k, float minv, const StepScalars& s,
-                                 uint32_t& mx, uint32_t& bad) {
+                                 uint32_t& mx, uint32_t& gx, uint32_t& bad) {
   constexpr int64_t kTile = (int64_t)kThreads * kGroup * kFusedGroups;
   const int tid = threadIdx.x;
   const bool vec = cd.vec_ok != 0 && sd.vec_ok != 0;
@@ -98,6 +100,7 @@ __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
         for (int j = 0; j < 4; ++j) {
           const float2 g = mul2(dec2<FMT>(c[j]), k2);
           if (!SAFE) bad |= nonfinite(g.x) | nonfinite(g.y);
+          if (GX) gx = max(gx, max(abs_bits(g.x), abs_bits(g.y)));
           const float2 m = fma2(b1, mul2(dec2<kE4M3>(code_pair(mc[q], j)), minv2),
                                 mul2(omb1, g));
           mx = max(mx, max(abs_bits(m.x), abs_bits(m.y)));
@@ -116,6 +119,7 @@ __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
           cd.codes[i] = (uint8_t)code;
           const float g = __fmul_rn(dec2<FMT>(code).x, k);
           bad |= nonfinite(g);
+          if (GX) gx = max(gx, abs_bits(g));
           const float mp = __fmul_rn(dec2<kE4M3>(sd.m[i]).x, minv);
           mx = max(mx, abs_bits(__fmaf_rn(s.beta1, mp, __fmul_rn(s.omb1, g))));
         }
@@ -124,32 +128,51 @@ __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
   }
 }
 
-template <int DT, int FMT>
+template <int DT, int FMT, bool GX>
+__device__ __forceinline__ void cast_step_dispatch2(const CastDesc& cd,
+                                                    const StepDesc& sd,
+                                                    int64_t begin, int64_t end,
+                                                    float scale, float k,
+                                                    float minv, bool checked,
+                                                    const StepScalars& s,
+                                                    uint32_t& mx, uint32_t& gx,
+                                                    uint32_t& bad) {
+  // As in the unfused step: when the largest finite code unscales to a finite
+  // value, every finite code does, and found_inf needs only the codes.
+  const bool safe = !nonfinite(__fmul_rn(fp8_max_of<FMT>(), k));
+  if (checked) {
+    if (safe)
+      thread_cast_step<DT, FMT, true, true, GX>(cd, sd, begin, end, scale, k, minv, s, mx, gx, bad);
+    else
+      thread_cast_step<DT, FMT, true, false, GX>(cd, sd, begin, end, scale, k, minv, s, mx, gx, bad);
+  } else {
+    if (safe)
+      thread_cast_step<DT, FMT, false, true, GX>(cd, sd, begin, end, scale, k, minv, s, mx, gx, bad);
+    else
+      thread_cast_step<DT, FMT, false, false, GX>(cd, sd, begin, end, scale, k, minv, s, mx, gx, bad);
+  }
+}
+
+template <int DT, int FMT, bool ANY_VS>
 __device__ __forceinline__ void cast_step_dispatch(const CastDesc& cd,
                                                    const StepDesc& sd,
                                                    int64_t begin, int64_t end,
                                                    float scale, float k,
                                                    float minv, bool checked,
                                                    const StepScalars& s,
-                                                   uint32_t& mx, uint32_t& bad) {
-  // As in the unfused step: when the largest finite code unscales to a finite
-  // value, every finite code does, and found_inf needs only the codes.
-  const bool safe = !nonfinite(__fmul_rn(fp8_max_of<FMT>(), k));
-  if (checked) {
-    if (safe)
-      thread_cast_step<DT, FMT, true, true>(cd, sd, begin, end, scale, k, minv, s, mx, bad);
-    else
-      thread_cast_step<DT, FMT, true, false>(cd, sd, begin, end, scale, k, minv, s, mx, bad);
-  } else {
-    if (safe)
-      thread_cast_step<DT, FMT, false, true>(cd, sd, begin, end, scale, k, minv, s, mx, bad);
-    else
-      thread_cast_step<DT, FMT, false, false>(cd, sd, begin, end, scale, k, minv, s, mx, bad);
-  }
+                                                   uint32_t& mx, uint32_t& gx,
+                                                   uint32_t& bad) {
+  if (ANY_VS && sd.v_bound != nullptr)
+    cast_step_dispatch2<DT, FMT, true>(cd, sd, begin, end, scale, k, minv, checked,
+                                       s, mx, gx, bad);
+  else
+    cast_step_dispatch2<DT, FMT, false>(cd, sd, begin, end, scale, k, minv, checked,
+                                        s, mx, gx, bad);
 }
 
-// At most 64 registers a thread: 4 resident CTAs per SM.
-template <int FMT>
+// At most 64 registers a thread: 4 resident CTAs per SM.  ANY_VS: some
+// tensor of the call has a scaled second moment.
+template <int FMT, bool ANY_VS>
 __global__ void __launch_bounds__(kThreads, 4)
 cast_step_amax_kernel(const CastDesc* __restrict__ cdescs,
                       const StepDesc* __restrict__ sdescs,
@@ -169,19 +192,25 @@ cast_step_amax_kernel(const CastDesc* __restrict__ cdescs,
       *cd.amax_out = __uint_as_float(ab);
       *cd.scale_out = scale;
       sc.old_m_scale[ch.tensor] = ms;
+      if (sd.v_bound != nullptr) sc.old_v_bound[ch.tensor] = *sd.v_bound;
     }
     const float k = __fdiv_rn(s.ils, scale), minv = __frcp_rn(ms);
     const int64_t begin = (int64_t)ch.index * kChunkElems;
     const int64_t end = min(begin + kChunkElems, cd.numel);
     const bool checked = ab >= 0x7F800000u;
-    uint32_t mx = 0, bad = 0;
+    uint32_t mx = 0, gx = 0, bad = 0;
     if (cd.dtype == kF32)
-      cast_step_dispatch<kF32, FMT>(cd, sd, begin, end, scale, k, minv, checked, s, mx, bad);
+      cast_step_dispatch<kF32, FMT, ANY_VS>(cd, sd, begin, end, scale, k, minv, checked, s, mx, gx, bad);
     else if (cd.dtype == kBF16)
-      cast_step_dispatch<kBF16, FMT>(cd, sd, begin, end, scale, k, minv, checked, s, mx, bad);
+      cast_step_dispatch<kBF16, FMT, ANY_VS>(cd, sd, begin, end, scale, k, minv, checked, s, mx, gx, bad);
     else
-      cast_step_dispatch<kF16, FMT>(cd, sd, begin, end, scale, k, minv, checked, s, mx, bad);
+      cast_step_dispatch<kF16, FMT, ANY_VS>(cd, sd, begin, end, scale, k, minv, checked, s, mx, gx, bad);
     mx = block_max_u32(mx, red);
+    if (ANY_VS && sd.v_bound != nullptr) {   // uniform over the CTA
+      gx = block_max_u32(gx, red);
+      if (threadIdx.x == 0 && gx != 0)
+        atomicMax(&sc.amax_g[ch.tensor], slot_tag(epoch, canon_amax_bits(gx)));
+    }
     const int any_bad = __syncthreads_or(bad != 0);
     if (threadIdx.x == 0) {
       if (mx != 0) atomicMax(&sc.amax_m[ch.tensor], slot_tag(epoch, canon_amax_bits(mx)));
@@ -198,8 +227,8 @@ cudaError_t launch_cast_step(const CastDesc* cdescs, const StepDesc* sdescs,
                              unsigned long long* gslots, const StepScratch& sc,
                              const StepScalars& s, uint32_t epoch, int fmt,
                              uint32_t* found_dev, int grid_amax, int grid_fused,
-                             int grid_update, int grid_w8, cudaStream_t stream,
-                             LaunchMark mark) {
+                             int grid_update, int grid_w8, bool any_vs,
+                             cudaStream_t stream, LaunchMark mark) {
   if (nchunks == 0) {
     if (found_dev) return cudaMemsetAsync(found_dev, 0, sizeof(uint32_t), stream);
     return cudaSuccess;
@@ -209,22 +238,28 @@ cudaError_t launch_cast_step(const CastDesc* cdescs, const StepDesc* sdescs,
   if (e != cudaSuccess) return e;
   const uint32_t g = grid_min((uint32_t)grid_fused, nchunks);
   if (mark) mark(kCastStepAmaxK, 0, stream);
-  if (fmt == kE4M3)
-    cast_step_amax_kernel<kE4M3><<<g, kThreads, 0, stream>>>(
+  if (fmt == kE4M3 && any_vs)
+    cast_step_amax_kernel<kE4M3, true><<<g, kThreads, 0, stream>>>(
+        cdescs, sdescs, chunks, nchunks, gslots, sc, s, epoch);
+  else if (fmt == kE4M3)
+    cast_step_amax_kernel<kE4M3, false><<<g, kThreads, 0, stream>>>(
+        cdescs, sdescs, chunks, nchunks, gslots, sc, s, epoch);
+  else if (any_vs)
+    cast_step_amax_kernel<kE5M2, true><<<g, kThreads, 0, stream>>>(
         cdescs, sdescs, chunks, nchunks, gslots, sc, s, epoch);
   else
-    cast_step_amax_kernel<kE5M2><<<g, kThreads, 0, stream>>>(
+    cast_step_amax_kernel<kE5M2, false><<<g, kThreads, 0, stream>>>(
         cdescs, sdescs, chunks, nchunks, gslots, sc, s, epoch);
   if (mark) mark(kCastStepAmaxK, 1, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_step_update(sdescs, chunks, nchunks, chunks_o3, nchunks_o3, sc,
-                            s, epoch, found_dev, grid_update, grid_w8, stream,
-                            mark);
+                            s, epoch, found_dev, grid_update, grid_w8, any_vs,
+                            stream, mark);
 }
 
 cudaError_t cast_step_occupancy(int* per_sm) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      per_sm, cast_step_amax_kernel<kE4M3>, kThreads, 0);
+      per_sm, cast_step_amax_kernel<kE4M3, false>, kThreads, 0);
 }
 
 }  // namespace fp8opt

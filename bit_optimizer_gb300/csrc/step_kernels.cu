@@ -21,10 +21,15 @@
 // Arithmetic per element, in fp32 (each operation rounded once; fma rounds
 // the product and the sum once together):
 //   g = dec(g_code) * k                       k = inv_loss_scale / g_scale
+//   [Adam with L2 decay: g = fma(wd, w_old, g)]
 //   m = fma(beta1, dec(m_code) * minv, (1 - beta1) * g)   minv = 1 / m_scale
 //   v = fma(beta2, v_old, (1 - beta2) * (g * g))
 //   u = m / fma(sqrt(v), inv_sbc2, eps)
-//   w = fma(-step_size, u, w_old * decay)
+//   w = fma(-step_size, u, w_old * decay)     decay = 1 - lr * wd, or 1 (L2)
+// A scaled second moment (v_bound set) keeps a per-tensor bound B on max v:
+// B_new = fma(beta2, B_old, (1 - beta2) * gmax * gmax) with gmax = max |g|
+// from the first pass; v_old = FP16 * (B_old * 2^-14) and v is stored as FP16
+// of v * (2^14 / B_new).
 // Elements are processed in pairs with the paired fp32 instructions, which
 // round each lane like the scalar ones, so the first moment, its amax and its
 // scale are bit-identical to a scalar fp32 evaluation of the same lines.
@@ -79,15 +84,18 @@ __device__ __forceinline__ void adamw1(float g, float m, float vp, float wp,
 
 // SAFE: every finite gradient code unscales to a finite value (decided once
 // per chunk from the largest code), so found_inf only needs the codes.
-template <int GF, bool SAFE>
+// L2: the gradient takes the decay term fma(wd, w, g) (so w is read too).
+// Besides the amax of the first moment (mx) this also reduces max |g| (gx),
+// the input of a scaled second moment's bound.
+template <int GF, bool SAFE, bool L2>
 __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
                                  float k, float minv, const StepScalars& s,
-                                 uint32_t& mx, uint32_t& bad) {
+                                 uint32_t& mx, uint32_t& gx, uint32_t& bad) {
   constexpr int64_t kTile = (int64_t)kThreads * kGroup * kAmaxGroups;
   const int tid = threadIdx.x;
   const bool vec = d.vec_ok != 0;
   const float2 k2 = splat2(k), minv2 = splat2(minv), b1 = splat2(s.beta1),
-               omb1 = splat2(s.omb1);
+               omb1 = splat2(s.omb1), wd2 = splat2(s.wd);
   const bool pf = FP8OPT_STEP_AMAX_PREFETCH > 0 && tid == 0 && vec &&
                   aligned16(d.g) && aligned16(d.m);
   for (int64_t base = begin; base < end; base += kTile) {
@@ -100,11 +108,13 @@ __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
     }
     if (vec && base + kTile <= end) {
       uint2 gc[kAmaxGroups], mc[kAmaxGroups];
+      uint4 wh[kAmaxGroups];
 #pragma unroll
       for (int q = 0; q < kAmaxGroups; ++q) {
         const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
         gc[q] = ld_keep2(d.g + i0);
         mc[q] = ld_keep2(d.m + i0);
+        if (L2) wh[q] = ld_keep4(d.w + i0);
       }
 #pragma unroll
       for (int q = 0; q < kAmaxGroups; ++q) {
@@ -112,8 +122,10 @@ __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
           bad |= nonfinite_code_bytes<GF>(gc[q].x) | nonfinite_code_bytes<GF>(gc[q].y);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float2 g = mul2(dec2<GF>(code_pair(gc[q], j)), k2);
+          float2 g = mul2(dec2<GF>(code_pair(gc[q], j)), k2);
           if (!SAFE) bad |= nonfinite(g.x) | nonfinite(g.y);
+          if (L2) g = fma2(wd2, h2_to_f2(half_pair(wh[q], j)), g);
+          gx = max(gx, max(abs_bits(g.x), abs_bits(g.y)));
           const float2 m = fma2(b1, mul2(dec2<kE4M3>(code_pair(mc[q], j)), minv2),
                                 mul2(omb1, g));
           mx = max(mx, max(abs_bits(m.x), abs_bits(m.y)));
@@ -126,8 +138,10 @@ __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
         for (int j = 0; j < kGroup; ++j) {
           const int64_t i = i0 + j;
           if (i >= end) break;
-          const float g = __fmul_rn(dec2<GF>(d.g[i]).x, k);
+          float g = __fmul_rn(dec2<GF>(d.g[i]).x, k);
           bad |= nonfinite(g);
+          if (L2) g = __fmaf_rn(s.wd, h_to_f(d.w[i]), g);
+          gx = max(gx, abs_bits(g));
           mx = max(mx, abs_bits(m_new1(dec2<kE4M3>(d.m[i]).x, minv, g, s)));
         }
       }
@@ -135,20 +149,22 @@ __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
   }
 }
 
-template <int GF>
+template <int GF, bool L2>
 __device__ __forceinline__ void step_amax_dispatch(const StepDesc& d,
                                                    int64_t begin, int64_t end,
                                                    float k, float minv,
                                                    const StepScalars& s,
-                                                   uint32_t& mx, uint32_t& bad) {
+                                                   uint32_t& mx, uint32_t& gx,
+                                                   uint32_t& bad) {
   // The largest finite code gives the largest |g|; rounding is monotonic, so
   // if that product is finite every finite code gives a finite g.
   if (!nonfinite(__fmul_rn(fp8_max_of<GF>(), k)))
-    thread_step_amax<GF, true>(d, begin, end, k, minv, s, mx, bad);
+    thread_step_amax<GF, true, L2>(d, begin, end, k, minv, s, mx, gx, bad);
   else
-    thread_step_amax<GF, false>(d, begin, end, k, minv, s, mx, bad);
+    thread_step_amax<GF, false, L2>(d, begin, end, k, minv, s, mx, gx, bad);
 }
 
+template <bool L2>
 __global__ void __launch_bounds__(kThreads)
 step_amax_kernel(const StepDesc* __restrict__ descs,
                  const Chunk* __restrict__ chunks, uint32_t nchunks,
@@ -158,16 +174,24 @@ step_amax_kernel(const StepDesc* __restrict__ descs,
     const Chunk ch = chunks[c];
     const StepDesc d = descs[ch.tensor];
     const float gs = *d.g_scale, ms = *d.m_scale;
-    if (ch.index == 0 && threadIdx.x == 0) sc.old_m_scale[ch.tensor] = ms;
+    if (ch.index == 0 && threadIdx.x == 0) {
+      sc.old_m_scale[ch.tensor] = ms;
+      if (d.v_bound != nullptr) sc.old_v_bound[ch.tensor] = *d.v_bound;
+    }
     const float k = __fdiv_rn(s.ils, gs), minv = __frcp_rn(ms);
     const int64_t begin = (int64_t)ch.index * kChunkElems;
     const int64_t end = min(begin + kChunkElems, d.numel);
-    uint32_t mx = 0, bad = 0;
+    uint32_t mx = 0, gx = 0, bad = 0;
     if (d.g_fmt == kE4M3)
-      step_amax_dispatch<kE4M3>(d, begin, end, k, minv, s, mx, bad);
+      step_amax_dispatch<kE4M3, L2>(d, begin, end, k, minv, s, mx, gx, bad);
     else
-      step_amax_dispatch<kE5M2>(d, begin, end, k, minv, s, mx, bad);
+      step_amax_dispatch<kE5M2, L2>(d, begin, end, k, minv, s, mx, gx, bad);
     mx = block_max_u32(mx, red);
+    if (d.v_bound != nullptr) {   // uniform over the CTA
+      gx = block_max_u32(gx, red);
+      if (threadIdx.x == 0 && gx != 0)
+        atomicMax(&sc.amax_g[ch.tensor], slot_tag(epoch, canon_amax_bits(gx)));
+    }
     const int any_bad = __syncthreads_or(bad != 0);
     if (threadIdx.x == 0) {
       if (mx != 0) atomicMax(&sc.amax_m[ch.tensor], slot_tag(epoch, canon_amax_bits(mx)));
@@ -180,10 +204,12 @@ step_amax_kernel(const StepDesc* __restrict__ descs,
 
 // Per-chunk constants of the update, as paired lanes.
 struct UpdConsts {
-  float2 k2, minv2, b1, omb1, b2, omb2, isbc2, eps2, nstep, decay, msc2;
+  float2 k2, minv2, b1, omb1, b2, omb2, isbc2, eps2, nstep, decay, msc2, wd2,
+      vinv2, vsc2;
 };
 
 __device__ __forceinline__ UpdConsts upd_consts(float k, float minv, float msc,
+                                                float vinv, float vsc,
                                                 const StepScalars& s) {
   UpdConsts c;
   c.k2 = splat2(k);
@@ -197,6 +223,9 @@ __device__ __forceinline__ UpdConsts upd_consts(float k, float minv, float msc,
   c.nstep = splat2(-s.step_size);
   c.decay = splat2(s.decay);
   c.msc2 = splat2(msc);
+  c.wd2 = splat2(s.wd);
+  c.vinv2 = splat2(vinv);
+  c.vsc2 = splat2(vsc);
   return c;
 }
 
@@ -204,19 +233,22 @@ __device__ __forceinline__ UpdConsts upd_consts(float k, float minv, float msc,
 // and w in; new moment codes, v and w out.  MCHECK: the first moment holds a
 // non-finite value (its amax is not finite), so its codes take the explicit
 // NaN code.  O3: also reduce the FP16 master's max |bits| per 16-bit lane
-// into hmax.
-template <int GF, bool O3, bool MCHECK>
+// into hmax.  VS: the second moment is scaled (read as FP16 * vinv, stored as
+// FP16 of v * vsc).  L2: the gradient takes the decay term fma(wd, w, g).
+template <int GF, bool O3, bool MCHECK, bool VS, bool L2>
 __device__ __forceinline__ void update8(uint2 gc, uint2 mc, uint4 vh, uint4 wh,
                                         const UpdConsts& c, uint2& mo2,
                                         uint4& vo4, uint4& wo4, uint32_t& hmax) {
   uint32_t mo[4], vo[4], wo[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float2 g = mul2(dec2<GF>(code_pair(gc, j)), c.k2);
+    float2 g = mul2(dec2<GF>(code_pair(gc, j)), c.k2);
+    if (L2) g = fma2(c.wd2, h2_to_f2(half_pair(wh, j)), g);
     const float2 m = fma2(c.b1, mul2(dec2<kE4M3>(code_pair(mc, j)), c.minv2),
                           mul2(c.omb1, g));
-    const float2 v = fma2(c.b2, h2_to_f2(half_pair(vh, j)),
-                          mul2(c.omb2, mul2(g, g)));
+    float2 vp = h2_to_f2(half_pair(vh, j));
+    if (VS) vp = mul2(vp, c.vinv2);
+    const float2 v = fma2(c.b2, vp, mul2(c.omb2, mul2(g, g)));
     float2 sq;
     sq.x = __fsqrt_rn(v.x);
     sq.y = __fsqrt_rn(v.y);
@@ -228,7 +260,7 @@ __device__ __forceinline__ void update8(uint2 gc, uint2 mc, uint4 vh, uint4 wh,
     const float2 mt = mul2(m, c.msc2);
     mo[j] = MCHECK ? (enc1_checked<kE4M3>(mt.x) | (enc1_checked<kE4M3>(mt.y) << 8))
                    : enc2<kE4M3>(mt.x, mt.y);
-    vo[j] = f2_to_h2(v);
+    vo[j] = f2_to_h2(VS ? mul2(v, c.vsc2) : v);
     wo[j] = f2_to_h2(w);
   }
   mo2 = make_uint2(mo[0] | (mo[1] << 16), mo[2] | (mo[3] << 16));
@@ -241,14 +273,15 @@ __device__ __forceinline__ void update8(uint2 gc, uint2 mc, uint4 vh, uint4 wh,
 }
 
 // The update of this thread's share of [begin, end) from global memory.
-template <int GF, bool O3, bool MCHECK>
+template <int GF, bool O3, bool MCHECK, bool VS, bool L2>
 __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
-                              float k, float minv, float msc,
-                              const StepScalars& s, uint32_t& hmax) {
+                              float k, float minv, float msc, float vinv,
+                              float vsc, const StepScalars& s, uint32_t& hmax) {
   constexpr int64_t kTile = (int64_t)kThreads * kGroup * kUpdGroups;
   const int tid = threadIdx.x;
   const bool vec = d.vec_ok != 0;
-  const UpdConsts c = upd_consts(k, minv, msc, s);
+  // built here, so an instantiation keeps only the constants it uses
+  const UpdConsts c = upd_consts(k, minv, msc, vinv, vsc, s);
   // One thread asks L2 for the tile FP8OPT_UPD_PREFETCH tiles ahead (whole
   // tiles of 16-byte-aligned tensors only), so the loads below find their
   // lines on chip while the DRAM reads for later tiles are already running.
@@ -281,7 +314,8 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
         const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
         uint2 mo;
         uint4 vo, wo;
-        update8<GF, O3, MCHECK>(gc[q], mc[q], vh[q], wh[q], c, mo, vo, wo, hmax);
+        update8<GF, O3, MCHECK, VS, L2>(gc[q], mc[q], vh[q], wh[q], c, mo, vo, wo,
+                                        hmax);
         *reinterpret_cast<uint2*>(d.m + i0) = mo;
         *reinterpret_cast<uint4*>(d.v + i0) = vo;
         *reinterpret_cast<uint4*>(d.w + i0) = wo;
@@ -293,14 +327,18 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
         for (int j = 0; j < kGroup; ++j) {
           const int64_t i = i0 + j;
           if (i >= end) break;
-          const float g = __fmul_rn(dec2<GF>(d.g[i]).x, k);
+          const float wp = h_to_f(d.w[i]);
+          float g = __fmul_rn(dec2<GF>(d.g[i]).x, k);
+          if (L2) g = __fmaf_rn(s.wd, wp, g);
           const float m = m_new1(dec2<kE4M3>(d.m[i]).x, minv, g, s);
+          float vp = h_to_f(d.v[i]);
+          if (VS) vp = __fmul_rn(vp, vinv);
           float v, w;
-          adamw1(g, m, h_to_f(d.v[i]), h_to_f(d.w[i]), s, v, w);
+          adamw1(g, m, vp, wp, s, v, w);
           const float mt = __fmul_rn(m, msc);
           d.m[i] = (uint8_t)(MCHECK ? enc1_checked<kE4M3>(mt)
                                     : (enc2<kE4M3>(mt, 0.0f) & 0xFFu));
-          d.v[i] = f_to_h(v);
+          d.v[i] = f_to_h(VS ? __fmul_rn(v, vsc) : v);
           const uint16_t wn = f_to_h(w);
           d.w[i] = wn;
           if (O3) hmax = __vmaxu2(hmax, wn & 0x7FFFu);
@@ -310,30 +348,51 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
   }
 }
 
-template <int GF, bool O3>
+template <int GF, bool O3, bool MCHECK, bool ANY_VS, bool L2>
+__device__ __forceinline__ void update_dispatch3(const StepDesc& d,
+                                                 int64_t begin, int64_t end,
+                                                 float k, float minv, float msc,
+                                                 float vinv, float vsc,
+                                                 const StepScalars& s,
+                                                 uint32_t& hmax) {
+  if (ANY_VS && d.v_bound != nullptr)
+    thread_update<GF, O3, MCHECK, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv,
+                                              vsc, s, hmax);
+  else
+    thread_update<GF, O3, MCHECK, false, L2>(d, begin, end, k, minv, msc, vinv,
+                                             vsc, s, hmax);
+}
+
+template <int GF, bool O3, bool ANY_VS, bool L2>
 __device__ __forceinline__ void update_dispatch2(const StepDesc& d,
                                                  int64_t begin, int64_t end,
                                                  float k, float minv, float msc,
+                                                 float vinv, float vsc,
                                                  bool mcheck,
                                                  const StepScalars& s,
                                                  uint32_t& hmax) {
   if (mcheck)
-    thread_update<GF, O3, true>(d, begin, end, k, minv, msc, s, hmax);
+    update_dispatch3<GF, O3, true, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv,
+                                               vsc, s, hmax);
   else
-    thread_update<GF, O3, false>(d, begin, end, k, minv, msc, s, hmax);
+    update_dispatch3<GF, O3, false, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv,
+                                                vsc, s, hmax);
 }
 
-template <int GF>
+template <int GF, bool ANY_VS, bool L2>
 __device__ __forceinline__ void update_dispatch(const StepDesc& d,
                                                 int64_t begin, int64_t end,
                                                 float k, float minv, float msc,
+                                                float vinv, float vsc,
                                                 bool mcheck,
                                                 const StepScalars& s,
                                                 uint32_t& hmax) {
   if (d.o3)
-    update_dispatch2<GF, true>(d, begin, end, k, minv, msc, mcheck, s, hmax);
+    update_dispatch2<GF, true, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv, vsc,
+                                           mcheck, s, hmax);
   else
-    update_dispatch2<GF, false>(d, begin, end, k, minv, msc, mcheck, s, hmax);
+    update_dispatch2<GF, false, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv, vsc,
+                                            mcheck, s, hmax);
 }
 
 __device__ __forceinline__ bool found_set(const StepScratch& sc, uint32_t epoch) {
@@ -342,7 +401,10 @@ __device__ __forceinline__ bool found_set(const StepScratch& sc, uint32_t epoch)
 }
 
 // Several resident CTAs per SM keep enough warps to hide the latency of the
-// square root and division sequences.
+// square root and division sequences.  ANY_VS: some tensor of the call has a
+// scaled second moment; L2: Adam with L2 decay.  Separate instantiations keep
+// the plain AdamW kernel free of the other variants' registers.
+template <bool ANY_VS, bool L2>
 __global__ void __launch_bounds__(kThreads, FP8OPT_UPD_MIN_BLOCKS)
 step_update_kernel(const StepDesc* __restrict__ descs,
                    const Chunk* __restrict__ chunks, uint32_t nchunks,
@@ -360,15 +422,29 @@ step_update_kernel(const StepDesc* __restrict__ descs,
     const float minv = __frcp_rn(sc.old_m_scale[ch.tensor]);
     const uint32_t am = slot_value(sc.amax_m[ch.tensor], epoch);
     const float msc = scale_from_amax_bits(am, 448.0f);
+    float vinv = 1.0f, vsc = 1.0f;
+    if (ANY_VS && d.v_bound != nullptr) {
+      // bound of this step: fma(beta2, old bound, (1 - beta2) * gmax^2)
+      const float b_old = sc.old_v_bound[ch.tensor];
+      const float gmax = __uint_as_float(slot_value(sc.amax_g[ch.tensor], epoch));
+      const float b_new = __fmaf_rn(s.beta2, b_old,
+                                    __fmul_rn(s.omb2, __fmul_rn(gmax, gmax)));
+      vinv = __fmul_rn(b_old, 0x1p-14f);
+      vsc = v_scale_from_bound(b_new);
+      if (ch.index == 0 && threadIdx.x == 0) *d.v_bound = b_new;
+    }
     if (ch.index == 0 && threadIdx.x == 0) *d.m_scale = msc;
     const int64_t begin = (int64_t)ch.index * kChunkElems;
     const int64_t end = min(begin + kChunkElems, d.numel);
     const bool mcheck = am >= 0x7F800000u;
+    const UpdConsts c = upd_consts(k, minv, msc, vinv, vsc, s);
     uint32_t hmax = 0;
     if (d.g_fmt == kE4M3)
-      update_dispatch<kE4M3>(d, begin, end, k, minv, msc, mcheck, s, hmax);
+      update_dispatch<kE4M3, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv, vsc,
+                                         mcheck, s, hmax);
     else
-      update_dispatch<kE5M2>(d, begin, end, k, minv, msc, mcheck, s, hmax);
+      update_dispatch<kE5M2, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv, vsc,
+                                         mcheck, s, hmax);
     if (d.o3) {   // uniform over the CTA
       uint32_t h = max(hmax & 0xFFFFu, hmax >> 16);
       h = block_max_u32(h, red);
@@ -450,17 +526,29 @@ step_w8_kernel(const StepDesc* __restrict__ descs,
 
 }  // namespace
 
-// The update pass, then (for O3 chunks) the weight-copy pass.
+// The update pass, then (for O3 chunks) the weight-copy pass.  any_vs: some
+// record has a scaled second moment.
 cudaError_t launch_step_update(const StepDesc* descs, const Chunk* chunks,
                                uint32_t nchunks, const Chunk* chunks_o3,
                                uint32_t nchunks_o3, const StepScratch& sc,
                                const StepScalars& s, uint32_t epoch,
                                uint32_t* found_dev, int grid_update, int grid_w8,
-                               cudaStream_t stream, LaunchMark mark) {
+                               bool any_vs, cudaStream_t stream,
+                               LaunchMark mark) {
   if (mark) mark(kStepUpdateK, 0, stream);
-  step_update_kernel<<<grid_min((uint32_t)grid_update, nchunks), kThreads,
-                       0, stream>>>(descs, chunks, nchunks, sc, s, epoch,
-                                    found_dev);
+  const uint32_t g = grid_min((uint32_t)grid_update, nchunks);
+  if (any_vs && s.l2)
+    step_update_kernel<true, true><<<g, kThreads, 0, stream>>>(
+        descs, chunks, nchunks, sc, s, epoch, found_dev);
+  else if (any_vs)
+    step_update_kernel<true, false><<<g, kThreads, 0, stream>>>(
+        descs, chunks, nchunks, sc, s, epoch, found_dev);
+  else if (s.l2)
+    step_update_kernel<false, true><<<g, kThreads, 0, stream>>>(
+        descs, chunks, nchunks, sc, s, epoch, found_dev);
+  else
+    step_update_kernel<false, false><<<g, kThreads, 0, stream>>>(
+        descs, chunks, nchunks, sc, s, epoch, found_dev);
   if (mark) mark(kStepUpdateK, 1, stream);
   if (nchunks_o3 != 0) {
     if (mark) mark(kStepW8K, 0, stream);
@@ -476,28 +564,35 @@ cudaError_t launch_step(const StepDesc* descs, const Chunk* chunks,
                         uint32_t nchunks_o3, const StepScratch& sc,
                         const StepScalars& s, uint32_t epoch,
                         uint32_t* found_dev, int grid_amax, int grid_update,
-                        int grid_w8, cudaStream_t stream, LaunchMark mark) {
+                        int grid_w8, bool any_vs, cudaStream_t stream,
+                        LaunchMark mark) {
   if (nchunks == 0) {
     if (found_dev) return cudaMemsetAsync(found_dev, 0, sizeof(uint32_t), stream);
     return cudaSuccess;
   }
   if (mark) mark(kStepAmaxK, 0, stream);
-  step_amax_kernel<<<grid_min((uint32_t)grid_amax, nchunks), kThreads, 0,
-                     stream>>>(descs, chunks, nchunks, sc, s, epoch);
+  const uint32_t ga = grid_min((uint32_t)grid_amax, nchunks);
+  if (s.l2)
+    step_amax_kernel<true><<<ga, kThreads, 0, stream>>>(descs, chunks, nchunks,
+                                                        sc, s, epoch);
+  else
+    step_amax_kernel<false><<<ga, kThreads, 0, stream>>>(descs, chunks, nchunks,
+                                                         sc, s, epoch);
   if (mark) mark(kStepAmaxK, 1, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_step_update(descs, chunks, nchunks, chunks_o3, nchunks_o3, sc, s,
-                            epoch, found_dev, grid_update, grid_w8, stream, mark);
+                            epoch, found_dev, grid_update, grid_w8, any_vs,
+                            stream, mark);
 }
 
 cudaError_t step_occupancy(int* amax_per_sm, int* update_per_sm,
                            int* w8_per_sm) {
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      amax_per_sm, step_amax_kernel, kThreads, 0);
+      amax_per_sm, step_amax_kernel<false>, kThreads, 0);
   if (e != cudaSuccess) return e;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      update_per_sm, step_update_kernel, kThreads, 0);
+      update_per_sm, step_update_kernel<false, false>, kThreads, 0);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(w8_per_sm,
                                                        step_w8_kernel, kThreads, 0);

@@ -121,6 +121,9 @@ typedef struct {
     uint8_t *w8;           /* O3 out: numel E4M3 codes of the master, else NULL */
     float *w8_scale;       /* O3 out: one fp32, its scale, else NULL */
     float *w8_amax;        /* O3 out: one fp32, max |master|, else NULL */
+    float *v_bound;        /* in/out: one fp32 for a scaled second moment
+                              (v then holds FP16 of v * 2^14 / v_bound; start
+                              at 0 with v = 0), or NULL for plain FP16 v */
 } fp8opt_param;
 
 /*
@@ -143,6 +146,15 @@ typedef struct {
  * FP16 (round to nearest even, overflow to inf).  For O3 records, the FP16
  * master's amax gives w8_scale = 448 / w8_amax and w8 = encode(master *
  * w8_scale).
+ *
+ * Scaled second moment (v_bound set): plain FP16 cannot hold the (1 -
+ * beta2) g^2 of small gradients (about 1e-13 at g ~ 1e-5; FP16's smallest
+ * subnormal is 6e-8), so v is kept relative to a per-tensor bound B on max v:
+ * B_new = fma(beta2, B_old, (1 - beta2) * gmax * gmax) with gmax = max |g| of
+ * this step; v_old = FP16 * (B_old * 2^-14), and v is stored as FP16 of v *
+ * (2^14 / B_new) (1.0 when B_new is 0 or not finite), so the stored values
+ * stay below about 2^14 * (1 + 2^-10).  The bound is written only when the
+ * step is taken.
  *
  * found_inf: if any unscaled g of any record is not finite, nothing is
  * written (no code, no state, no scale) and found_inf is 1; the caller then
@@ -188,6 +200,19 @@ FP8OPT_API int fp8_adamw_step(const fp8opt_param *params, int n, float lr, float
  */
 FP8OPT_API int fp8_cast_scaled_noalloc(const fp8opt_cast_item *items, int n,
                                        int fmt, void *stream);
+
+/*
+ * fp8_adam_step: as fp8_adamw_step, but Adam with L2 weight decay (the
+ * README's other recognised optimizer, torch.optim.Adam with weight_decay):
+ * each unscaled gradient becomes g = fma(wd, w_old, g) before the moments
+ * (found_inf is still decided on the unscaled g), and the weight is not
+ * decayed (w = fma(-step_size, u, w_old)).  Its first pass also reads w:
+ * 2 bytes more per parameter.  Same arguments, results and errors otherwise.
+ */
+FP8OPT_API int fp8_adam_step(const fp8opt_param *params, int n, float lr,
+                             float beta1, float beta2, float eps, float wd,
+                             int64_t step, float inv_loss_scale, int *found_inf,
+                             uint32_t *found_inf_dev, void *stream);
 
 /*
  * fp8_cast_adamw_step: fp8_cast_scaled(grads, n, fmt) followed by

@@ -37,13 +37,15 @@ def oracle_cast(grads: Sequence[torch.Tensor], fmt: int):
     return codes, np.array(amax, np.float32), np.array(scale, np.float32)
 
 
-def fresh_states(weights: Sequence[torch.Tensor], o3: bool, g_fmt=oracle.E4M3):
+def fresh_states(weights: Sequence[torch.Tensor], o3: bool, g_fmt=oracle.E4M3,
+                 scaled_v=False):
     out = []
     for w in weights:
         n = w.numel()
         out.append(oracle.StepState(
             np.zeros(n, np.uint8), 1.0, np.zeros(n, np.uint8), 1.0,
-            np.zeros(n, np.uint16), to_np_u16(w.cpu()), g_fmt=g_fmt, o3=o3))
+            np.zeros(n, np.uint16), to_np_u16(w.cpu()), g_fmt=g_fmt, o3=o3,
+            scaled_v=scaled_v))
     return out
 
 
@@ -53,9 +55,10 @@ def set_grads(states, codes, scales):
         s.g_scale = float(np.float32(sc))
 
 
-def oracle_step(states, wl, step, ils=None):
+def oracle_step(states, wl, step, ils=None, l2=False):
     return oracle.adamw_step(states, wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd,
-                             step, wl.inv_loss_scale if ils is None else ils)
+                             step, wl.inv_loss_scale if ils is None else ils,
+                             l2=l2)
 
 
 class GpuState:
@@ -92,16 +95,19 @@ class GpuState:
             self.w8_amax = torch.tensor([s.w8_amax[0] for s in states], **f32)
         else:
             self.w8 = self.w8_scale = self.w8_amax = None
+        self.scaled_v = n > 0 and states[0].v_bound is not None
+        self.v_bound = (torch.tensor([s.v_bound[0] for s in states], **f32)
+                        if self.scaled_v else None)
         fmts = [s.g_fmt for s in states]
         self.plan = bo.AdamWPlan(self.g, self.g_scale, self.m, self.m_scale,
                                  self.v, self.w, self.w8, self.w8_scale,
-                                 self.w8_amax, g_fmt=fmts)
+                                 self.w8_amax, g_fmt=fmts, v_bound=self.v_bound)
         self.found_dev = torch.full((1,), 7, dtype=torch.int32, device=device)
 
-    def step(self, wl, step, ils=None):
+    def step(self, wl, step, ils=None, l2=False):
         found = self.plan(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, step,
                           wl.inv_loss_scale if ils is None else ils,
-                          found_inf_dev=self.found_dev)
+                          found_inf_dev=self.found_dev, l2=l2)
         assert int(self.found_dev.item()) == found
         return found
 
@@ -109,6 +115,9 @@ class GpuState:
         """Compare every output against oracle states; returns exact rates."""
         m_scale = self.m_scale.cpu().numpy()[:len(ref_states)]
         check_f32_exact(m_scale, [s.m_scale[0] for s in ref_states], "m_scale")
+        if self.scaled_v:
+            check_f32_exact(self.v_bound.cpu().numpy()[:len(ref_states)],
+                            [s.v_bound[0] for s in ref_states], "v_bound")
         rates = {"m": [], "v": [], "w": [], "w8": []}
         for i, s in enumerate(ref_states):
             rates["m"].append(check_codes(to_np_u8(self.m[i]), s.m, name=f"m[{i}]"))
@@ -136,6 +145,9 @@ class GpuState:
             self.w[i].copy_(from_np_u16(s.w, self.w[i].device))
         self.g_scale[:len(states)].copy_(torch.tensor([s.g_scale for s in states]))
         self.m_scale[:len(states)].copy_(torch.tensor([s.m_scale[0] for s in states]))
+        if self.scaled_v:
+            self.v_bound[:len(states)].copy_(
+                torch.tensor([s.v_bound[0] for s in states]))
 
 
 class DeviceList:
@@ -145,10 +157,11 @@ class DeviceList:
     state is overwritten with the oracle's, so every compared output is one
     step of the library from the oracle's inputs."""
 
-    def __init__(self, wl, device="cuda"):
+    def __init__(self, wl, device="cuda", scaled_v=False):
         import bit_optimizer_gb300 as bo
         self.wl = wl
         self.device = device
+        self.scaled_v = scaled_v
         self.o3 = wl.level == "O3"
         self.fmt = oracle.FMT[wl.grad_fmt]
         n = len(wl.shapes)
@@ -170,11 +183,12 @@ class DeviceList:
             self.w8_amax = torch.zeros(n, **f32)
         else:
             self.w8 = self.w8_scale = self.w8_amax = None
+        self.v_bound = torch.zeros(n, **f32) if scaled_v else None
         self.cast = bo.CastPlan(self.src, self.g, self.g_amax, self.g_scale,
                                 wl.grad_fmt)
         self.plan = bo.AdamWPlan(self.g, self.g_scale, self.m, self.m_scale,
                                  self.v, self.w, self.w8, self.w8_scale,
-                                 self.w8_amax, wl.grad_fmt)
+                                 self.w8_amax, wl.grad_fmt, self.v_bound)
         self.found_dev = torch.zeros(1, dtype=torch.int32, device=device)
 
     def gen_grads(self, step, wl=None):
@@ -186,7 +200,7 @@ class DeviceList:
         n = self.wl.numels[i]
         return oracle.StepState(np.zeros(n, np.uint8), 1.0, np.zeros(n, np.uint8),
                                 1.0, np.zeros(n, np.uint16), to_np_u16(self.w[i]),
-                                g_fmt=self.fmt, o3=self.o3)
+                                g_fmt=self.fmt, o3=self.o3, scaled_v=self.scaled_v)
 
     def cast_and_check(self, sample, states):
         """GPU cast of every tensor; the oracle casts the sampled ones from
@@ -211,6 +225,8 @@ class DeviceList:
         self.m_scale[i] = float(st.m_scale[0])
         self.v[i].copy_(from_np_u16(st.v, self.device))
         self.w[i].copy_(from_np_u16(st.w, self.device))
+        if self.scaled_v:
+            self.v_bound[i] = float(st.v_bound[0])
 
     def step(self, t, ils=None):
         wl = self.wl
@@ -246,6 +262,9 @@ class DeviceList:
 
     def compare(self, i, st):
         check_f32_exact(self.m_scale[i:i + 1].cpu().numpy(), st.m_scale, f"m_scale[{i}]")
+        if self.scaled_v:
+            check_f32_exact(self.v_bound[i:i + 1].cpu().numpy(), st.v_bound,
+                            f"v_bound[{i}]")
         check_codes(to_np_u8(self.m[i]), st.m, name=f"m[{i}]")
         check_f16(to_np_u16(self.v[i]), st.v, name=f"v[{i}]")
         w = to_np_u16(self.w[i])

@@ -54,11 +54,11 @@ def test_cast_gpt2_124m_every_tensor(bo, fmt):
         check_codes(to_np_u8(codes[i]), rc, f, name=f"codes[{i}]")
 
 
-def lockstep_full(wl, steps, sample, first=1, fused=False):
+def lockstep_full(wl, steps, sample, first=1, fused=False, scaled_v=False):
     """Every tensor stepped by the library; the sampled ones start each step
     from the oracle's state.  fused: one fp8_cast_adamw_step call per step
     (the bench's configuration), else fp8_cast_scaled then fp8_adamw_step."""
-    dl = DeviceList(wl)
+    dl = DeviceList(wl, scaled_v=scaled_v)
     states = {i: dl.fresh_oracle(i) for i in sample}
     for t in range(first, first + steps):
         dl.gen_grads(t)
@@ -130,3 +130,13 @@ def test_o2_6p7b_tail_full_10_steps(bo):
     dl.invariants()
     zero = len(wl.shapes) - 1
     assert dl.m_scale[zero].item() == 1.0 and not bool(dl.m[zero].any().item())
+
+
+def test_o2_6p7b_tail_full_scaled_v(bo):
+    """The long-tail list with the scaled second moment, through the fused
+    call, 3 steps."""
+    wl = synth.o2_6p7b_tail()
+    sample = sample_of(wl, 12_000_000)
+    dl, _ = lockstep_full(wl, 3, sample, fused=True, scaled_v=True)
+    dl.invariants()
+    assert float(dl.v_bound.max().item()) > 0

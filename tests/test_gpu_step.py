@@ -43,7 +43,7 @@ def warm_up(wl, states, steps, fmt=E4M3):
         assert oracle_step(states, wl, t) == 0
 
 
-def lockstep(bo, wl, states, t0, t1, fmt=E4M3, misalign=()):
+def lockstep(bo, wl, states, t0, t1, fmt=E4M3, misalign=(), l2=False):
     """Steps t0..t1: each step the GPU starts from the oracle's state."""
     gpu = None
     for t in range(t0, t1 + 1):
@@ -53,8 +53,8 @@ def lockstep(bo, wl, states, t0, t1, fmt=E4M3, misalign=()):
             gpu = GpuState([s.copy() for s in states], misalign=misalign)
         else:
             gpu.load_state(states)
-        f_ref = oracle_step(states, wl, t)
-        assert gpu.step(wl, t) == f_ref == 0
+        f_ref = oracle_step(states, wl, t, l2=l2)
+        assert gpu.step(wl, t, l2=l2) == f_ref == 0
         rates = gpu.compare(states)
     return gpu, rates
 
@@ -383,3 +383,73 @@ def test_fused_equals_the_two_calls(bo):
             assert torch.equal(x, y), name
     for name in ("g_amax", "g_scale", "m_scale", "w8_scale", "w8_amax"):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+# ------------------------------------- scaled second moment, Adam with L2
+
+@pytest.mark.parametrize("l2", [False, True])
+def test_scaled_v_long_tail_reduced(bo, l2):
+    """The long-tail list at reduced size has gradients down to sigma ~ 1e-5,
+    where a plain FP16 second moment underflows."""
+    wl = synth.o2_6p7b_tail(n_layer=1, d=128, ffn=512, vocab=1000, ctx=64, n_tail=60)
+    states = fresh_states(wl.weights(), o3=False, scaled_v=True)
+    gpu, _ = lockstep(bo, wl, states, 1, 4, l2=l2)
+    assert (gpu.v_bound.cpu().numpy()[:len(states) - 1] > 0).all()
+
+
+@pytest.mark.parametrize("l2", [False, True])
+def test_plain_v_adam_l2_o3_reduced(bo, l2):
+    wl = synth.o3_1p3b(n_layer=1, d=128, ffn=512, vocab=500, ctx=64)
+    states = fresh_states(wl.weights(), o3=True)
+    lockstep(bo, wl, states, 1, 3, l2=l2, misalign={2})
+
+
+def test_scaled_v_o3_unaligned_and_fused(bo):
+    wl = synth.o3_1p3b(n_layer=1, d=128, ffn=512, vocab=500, ctx=64)
+    states = fresh_states(wl.weights(), o3=True, scaled_v=True)
+    lockstep(bo, wl, states, 1, 2, misalign={0, 4})
+    wl = synth.o2_6p7b_tail(n_layer=1, d=128, ffn=512, vocab=1000, ctx=64, n_tail=40)
+    states = fresh_states(wl.weights(), o3=False, scaled_v=True)
+    lockstep_fused(bo, wl, states, 1, 3)
+
+
+def test_found_inf_keeps_v_bound(bo):
+    wl = synth.tiny()
+    states = fresh_states(wl.weights(), o3=False, scaled_v=True)
+    codes, _, scale = oracle_cast(wl.grads(1), E4M3)
+    set_grads(states, codes, scale)
+    oracle_step(states, wl, 1)
+    codes, _, scale = oracle_cast(wl.grads(2), E4M3)
+    set_grads(states, codes, scale)
+    states[1].g[7] = 0x7F
+    gpu = GpuState([s.copy() for s in states])
+    before = gpu.v_bound.clone()
+    assert oracle_step(states, wl, 2) == 1
+    assert gpu.step(wl, 2) == 1
+    assert torch.equal(gpu.v_bound, before)
+
+
+def test_optimizer_options_checkpoint(bo):
+    """Fp8AdamW with scaled_v and with l2: state_dict round trip, and the
+    two configurations differ from plain AdamW where they should."""
+    wl = synth.tiny()
+    weights = [w.cuda() for w in wl.weights()]
+    outs = {}
+    for name, kw in (("plain", {}), ("scaled", {"scaled_v": True}),
+                     ("l2", {"l2": True})):
+        params = [w.clone() for w in weights]
+        opt = bo.Fp8AdamW(params, lr=wl.lr, weight_decay=0.1, **kw)
+        for t in (1, 2):
+            opt.step([g.cuda() * 1e-3 for g in wl.grads(t)])
+        sd = opt.state_dict()
+        b_params = [p.clone() for p in params]
+        b = bo.Fp8AdamW(b_params, lr=wl.lr, weight_decay=0.1, **kw)
+        b.load_state_dict(sd)
+        g3 = [g.cuda() * 1e-3 for g in wl.grads(3)]
+        opt.step(g3)
+        b.step(g3)
+        for x, y in zip(params, b_params):
+            assert torch.equal(x, y)
+        outs[name] = params
+    assert not torch.equal(outs["plain"][0], outs["scaled"][0])
+    assert not torch.equal(outs["plain"][0], outs["l2"][0])
