@@ -73,6 +73,11 @@ def lib():
         L.oracle_cast_scaled.restype = C.c_int
         L.oracle_cast_scaled.argtypes = [C.c_void_p, C.c_int, C.c_int64, C.c_int,
                                          C.c_void_p, C.c_void_p, C.c_void_p]
+        L.oracle_reduce_scaled.restype = C.c_int
+        L.oracle_reduce_scaled.argtypes = [C.c_void_p, C.c_int64, C.c_int64,
+                                           C.c_void_p, C.c_int, C.c_int, C.c_int,
+                                           C.c_float, C.c_void_p, C.c_void_p,
+                                           C.c_void_p]
         L.oracle_adamw_step.restype = C.c_int
         L.oracle_adamw_step.argtypes = [C.POINTER(Param), C.c_int, C.c_float,
                                         C.c_float, C.c_float, C.c_float,
@@ -155,6 +160,31 @@ def cast_scaled(src: np.ndarray, dtype: int, fmt: int):
                                   _ptr(amax), _ptr(scale))
     if rc != 0:
         raise ValueError(f"oracle_cast_scaled rejected its arguments ({rc})")
+    return codes, amax[0], scale[0]
+
+
+# ---------------------------------------------------------- FP8 reduction
+
+def reduce_scaled(shards: np.ndarray, scales, in_fmt: int, out_fmt: int,
+                  post: float = 1.0, numel: int = None):
+    """Local reduction of k FP8 shards: ``shards`` is a [k, stride] uint8
+    array (each row one shard's codes; the first ``numel`` columns are used,
+    all of them by default), ``scales`` the k encode scales.  Returns (codes
+    uint8[numel], amax float32 scalar, scale float32 scalar)."""
+    sh = np.ascontiguousarray(shards, dtype=np.uint8)
+    assert sh.ndim == 2
+    k, stride = sh.shape
+    n = stride if numel is None else int(numel)
+    sc = np.ascontiguousarray(scales, dtype=np.float32).ravel()
+    assert sc.size == k
+    codes = np.empty(n, dtype=np.uint8)
+    amax = np.zeros(1, dtype=np.float32)
+    scale = np.zeros(1, dtype=np.float32)
+    rc = lib().oracle_reduce_scaled(_ptr(sh), n, stride, _ptr(sc), k, in_fmt,
+                                    out_fmt, post, _ptr(codes), _ptr(amax),
+                                    _ptr(scale))
+    if rc != 0:
+        raise ValueError(f"oracle_reduce_scaled rejected its arguments ({rc})")
     return codes, amax[0], scale[0]
 
 

@@ -1,6 +1,7 @@
 /*
  * fp8opt oracle: a plain, slow, scalar CPU implementation of the scaled FP8
- * cast and of the FP8-state AdamW step (MS-AMP levels O2 and O3).
+ * cast, of the local reduction of FP8 shards, and of the FP8-state AdamW step
+ * (MS-AMP levels O1, O2 and O3).
  *
  * TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the bench's
  * CPU-baseline leg may load or call this file.  It shares no code with the
@@ -46,6 +47,12 @@
  *   - Optional Adam with L2 weight decay (torch.optim.Adam, the other
  *     recognised optimizer): g = fma(wd, w, g) before the moments, and the
  *     weight itself is not decayed.
+ *   - The local reduction of an FP8 all-reduce (the O1 paragraph's FP8
+ *     AllReduce communication of weight gradients): k shards of one tensor,
+ *     shard j encoded with its own scale s_j, are dequantized as code value
+ *     times (1 / s_j), summed in fp32 in shard order, multiplied by a
+ *     caller-given factor (1 for a sum, 1 / k for a mean), and cast back to
+ *     FP8 with a just-in-time scale like any other tensor.
  *
  * Floating point: compiled with -ffp-contract=off and no fast-math, so every
  * float expression below is evaluated as written in IEEE binary32 with
@@ -53,6 +60,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 enum { OR_E4M3 = 0, OR_E5M2 = 1 };
@@ -408,6 +416,40 @@ int oracle_adamw_step(const oracle_param *p, int n, float lr, float beta1,
 {
     return oracle_adam_step(p, n, 0, lr, beta1, beta2, eps, wd, step,
                             inv_loss_scale);
+}
+
+/* --------------------------------------------------------- FP8 reduction */
+
+/* Local reduction of k FP8 shards of one tensor.  Shard j is the numel codes
+ * at src + j * stride (format in_fmt, encoded with scale scales[j]).  Each
+ * element's reduced value is
+ *     y = (((x_0 + x_1) + x_2) + ... + x_{k-1}) * post,
+ *     x_j = decode(code_j) * (1 / s_j),
+ * every product and sum rounded to fp32 on its own; then y is cast to out_fmt
+ * exactly as oracle_cast_scaled casts an fp32 tensor.  Returns 0, or -1 on a
+ * bad argument. */
+int oracle_reduce_scaled(const uint8_t *src, int64_t numel, int64_t stride,
+                         const float *scales, int k, int in_fmt, int out_fmt,
+                         float post, uint8_t *codes, float *amax_out,
+                         float *scale_out)
+{
+    if (numel < 0 || k < 1 || k > 64 || stride < numel || in_fmt < 0 ||
+        in_fmt > 1 || out_fmt < 0 || out_fmt > 1)
+        return -1;
+    float r[64];
+    for (int j = 0; j < k; ++j) r[j] = 1.0f / scales[j];
+    float *y = malloc((size_t)(numel > 0 ? numel : 1) * sizeof(float));
+    if (y == NULL) return -1;
+    for (int64_t i = 0; i < numel; ++i) {
+        float acc = oracle_fp8_decode(src[i], in_fmt) * r[0];
+        for (int j = 1; j < k; ++j)
+            acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) * r[j];
+        y[i] = acc * post;
+    }
+    int rc = oracle_cast_scaled(y, OR_F32, numel, out_fmt, codes, amax_out,
+                                scale_out);
+    free(y);
+    return rc;
 }
 
 /* Optimizer-state bytes per parameter for a level of the MS-AMP table:
