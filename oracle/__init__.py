@@ -86,6 +86,16 @@ def lib():
         L.oracle_adam_step.argtypes = [C.POINTER(Param), C.c_int, C.c_int,
                                        C.c_float, C.c_float, C.c_float,
                                        C.c_float, C.c_float, C.c_int64, C.c_float]
+        L.oracle_grad_norm.restype = C.c_int
+        L.oracle_grad_norm.argtypes = [C.POINTER(Param), C.c_int, C.c_float,
+                                       C.POINTER(C.c_double)]
+        L.oracle_clip_coef.restype = C.c_float
+        L.oracle_clip_coef.argtypes = [C.c_double, C.c_float]
+        L.oracle_adam_step_clipped.restype = C.c_int
+        L.oracle_adam_step_clipped.argtypes = [
+            C.POINTER(Param), C.c_int, C.c_int, C.c_float, C.c_float, C.c_float,
+            C.c_float, C.c_float, C.c_int64, C.c_float, C.c_float,
+            C.POINTER(C.c_double)]
         L.oracle_v_scale_from_bound.restype = C.c_float
         L.oracle_v_scale_from_bound.argtypes = [C.c_float]
         L.oracle_state_bytes.restype = C.c_int
@@ -265,3 +275,39 @@ def adamw_step(states: Sequence[StepState], lr, beta1, beta2, eps, wd, step,
     if rc < 0:
         raise ValueError(f"oracle_adamw_step rejected its arguments ({rc})")
     return rc
+
+
+def _params(states):
+    arr = (Param * max(1, len(states)))()
+    for i, s in enumerate(states):
+        arr[i] = s._param()
+    return arr
+
+
+def grad_norm(states: Sequence[StepState], inv_loss_scale):
+    """(found_inf, norm): the global L2 norm of the unscaled gradient codes of
+    the list (+inf when found_inf)."""
+    norm = C.c_double(0.0)
+    rc = lib().oracle_grad_norm(_params(states), len(states), inv_loss_scale,
+                                C.byref(norm))
+    if rc < 0:
+        raise ValueError(f"oracle_grad_norm rejected its arguments ({rc})")
+    return rc, norm.value
+
+
+def clip_coef(norm: float, max_norm: float) -> float:
+    return lib().oracle_clip_coef(norm, max_norm)
+
+
+def adam_step_clipped(states: Sequence[StepState], lr, beta1, beta2, eps, wd,
+                      step, inv_loss_scale, max_norm, l2=False):
+    """One oracle step with global gradient-norm clipping; returns
+    (found_inf, norm)."""
+    norm = C.c_double(0.0)
+    rc = lib().oracle_adam_step_clipped(_params(states), len(states),
+                                        1 if l2 else 0, lr, beta1, beta2, eps,
+                                        wd, step, inv_loss_scale, max_norm,
+                                        C.byref(norm))
+    if rc < 0:
+        raise ValueError(f"oracle_adam_step_clipped rejected its arguments ({rc})")
+    return rc, norm.value

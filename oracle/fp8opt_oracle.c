@@ -47,6 +47,12 @@
  *   - Optional Adam with L2 weight decay (torch.optim.Adam, the other
  *     recognised optimizer): g = fma(wd, w, g) before the moments, and the
  *     weight itself is not decayed.
+ *   - The global gradient norm for clipping (the run script's --clip-grad):
+ *     the L2 norm of the unscaled gradient, taken from the codes with each
+ *     tensor's sum of squares exact and the tensors combined in double in
+ *     order; clipping multiplies each tensor's dequantization factor by
+ *     max_norm / (norm + 1e-6) (torch's clip_grad_norm_ coefficient) when
+ *     that is below 1.
  *   - The local reduction of an FP8 all-reduce (the O1 paragraph's FP8
  *     AllReduce communication of weight gradients): k shards of one tensor,
  *     shard j encoded with its own scale s_j, are dequantized as code value
@@ -335,12 +341,27 @@ static float or_grad_l2(const oracle_param *p, float g, int l2, float wd,
     return l2 ? fmaf(wd, oracle_f16_to_f32(p->w[i]), g) : g;
 }
 
+/* The step below with an optional gradient-clipping coefficient: clip != 1
+ * multiplies each tensor's factor k (after the found_inf check, which uses the
+ * unclipped k). */
+static int or_adam_step(const oracle_param *p, int n, int l2, float lr,
+                        float beta1, float beta2, float eps, float wd,
+                        int64_t step, float inv_loss_scale, float clip);
+
 /* One multi-tensor Adam step with FP8 first moment and FP16 second moment:
  * l2 = 0 is AdamW (decoupled decay), l2 = 1 is Adam with L2 decay.  Returns 1
  * when found_inf (nothing written), 0 after an update, -1 on a bad argument. */
 int oracle_adam_step(const oracle_param *p, int n, int l2, float lr, float beta1,
                      float beta2, float eps, float wd, int64_t step,
                      float inv_loss_scale)
+{
+    return or_adam_step(p, n, l2, lr, beta1, beta2, eps, wd, step,
+                        inv_loss_scale, 1.0f);
+}
+
+static int or_adam_step(const oracle_param *p, int n, int l2, float lr,
+                        float beta1, float beta2, float eps, float wd,
+                        int64_t step, float inv_loss_scale, float clip)
 {
     if (n < 0 || step < 1) return -1;
     or_scalars s = or_make_scalars(lr, beta1, beta2, wd, step, l2);
@@ -356,6 +377,7 @@ int oracle_adam_step(const oracle_param *p, int n, int l2, float lr, float beta1
     for (int t = 0; t < n; ++t) {
         const oracle_param *q = &p[t];
         float k = or_grad_factor(q, inv_loss_scale);
+        if (clip != 1.0f) k = k * clip;
         float minv = 1.0f / *q->m_scale;
         int scaled_v = q->v_bound != NULL;
 
@@ -450,6 +472,68 @@ int oracle_reduce_scaled(const uint8_t *src, int64_t numel, int64_t stride,
                                 scale_out);
     free(y);
     return rc;
+}
+
+/* ------------------------------------------------ gradient norm, clipping */
+
+/* Global L2 norm of the unscaled gradient of a step call, the quantity a
+ * training loop clips (torch.nn.utils.clip_grad_norm_ in the run script's
+ * --clip-grad).  Element i of tensor t is g = decode(code) * k_t, k_t the
+ * step's factor inv_loss_scale / g_scale.  The norm is
+ *     sqrt( sum over t, in tensor order, of k_t^2 * S_t ),
+ *     S_t = sum over i of decode(code_i)^2, taken exactly,
+ * where each k_t^2 * S_t is rounded to double once (k_t^2 is exact in double
+ * and S_t is rounded to double first), each sum in tensor order is rounded to
+ * double, and the root is the correctly rounded double root.  Decoded codes
+ * are integer multiples of 2^-16, so S_t is an integer count of 2^-32 held
+ * here in 128 bits.  Returns 1 with *norm = +inf when found_inf (some g not
+ * finite, the step's test), else 0; -1 on a bad argument. */
+int oracle_grad_norm(const oracle_param *p, int n, float inv_loss_scale,
+                     double *norm)
+{
+    if (n < 0) return -1;
+    double total = 0.0;
+    for (int t = 0; t < n; ++t) {
+        float k = or_grad_factor(&p[t], inv_loss_scale);
+        unsigned __int128 sum = 0;
+        for (int64_t i = 0; i < p[t].numel; ++i) {
+            if (!isfinite(or_grad(&p[t], k, i))) { *norm = INFINITY; return 1; }
+            double d = fabs((double)oracle_fp8_decode(p[t].g[i], p[t].g_fmt));
+            uint64_t q = (uint64_t)ldexp(d, 16);           /* exact integer */
+            sum += (unsigned __int128)q * q;
+        }
+        double kk = (double)k * (double)k;
+        total = total + kk * ldexp((double)sum, -32);
+    }
+    *norm = sqrt(total);
+    return 0;
+}
+
+/* Clip coefficient of a global norm: max_norm / (norm + 1e-6) in double,
+ * rounded to float, when that is below 1; 1 (no clipping) otherwise or when
+ * max_norm <= 0. */
+float oracle_clip_coef(double norm, float max_norm)
+{
+    if (!(max_norm > 0.0f)) return 1.0f;
+    double c = (double)max_norm / (norm + 1e-6);
+    return c < 1.0 ? (float)c : 1.0f;
+}
+
+/* The Adam / AdamW step with global gradient-norm clipping: the norm of the
+ * unscaled gradient (oracle_grad_norm) gives the coefficient c
+ * (oracle_clip_coef), and every tensor's factor becomes k_t * c, rounded to
+ * float, when c < 1.  found_inf is decided on the unclipped gradient.  *norm
+ * receives the norm (+inf when found_inf).  Returns as oracle_adam_step. */
+int oracle_adam_step_clipped(const oracle_param *p, int n, int l2, float lr,
+                             float beta1, float beta2, float eps, float wd,
+                             int64_t step, float inv_loss_scale,
+                             float max_norm, double *norm)
+{
+    if (n < 0 || step < 1) return -1;
+    int found = oracle_grad_norm(p, n, inv_loss_scale, norm);
+    if (found != 0) return found;
+    return or_adam_step(p, n, l2, lr, beta1, beta2, eps, wd, step,
+                        inv_loss_scale, oracle_clip_coef(*norm, max_norm));
 }
 
 /* Optimizer-state bytes per parameter for a level of the MS-AMP table:
