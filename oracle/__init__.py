@@ -89,6 +89,9 @@ def lib():
         L.oracle_grad_norm.restype = C.c_int
         L.oracle_grad_norm.argtypes = [C.POINTER(Param), C.c_int, C.c_float,
                                        C.POINTER(C.c_double)]
+        L.oracle_grad_norm_terms.restype = C.c_int
+        L.oracle_grad_norm_terms.argtypes = [C.POINTER(Param), C.c_int, C.c_float,
+                                             C.c_void_p]
         L.oracle_clip_coef.restype = C.c_float
         L.oracle_clip_coef.argtypes = [C.c_double, C.c_float]
         L.oracle_adam_step_clipped.restype = C.c_int
@@ -96,6 +99,10 @@ def lib():
             C.POINTER(Param), C.c_int, C.c_int, C.c_float, C.c_float, C.c_float,
             C.c_float, C.c_float, C.c_int64, C.c_float, C.c_float,
             C.POINTER(C.c_double)]
+        L.oracle_adam_step_coef.restype = C.c_int
+        L.oracle_adam_step_coef.argtypes = [
+            C.POINTER(Param), C.c_int, C.c_int, C.c_float, C.c_float, C.c_float,
+            C.c_float, C.c_float, C.c_int64, C.c_float, C.c_float]
         L.oracle_v_scale_from_bound.restype = C.c_float
         L.oracle_v_scale_from_bound.argtypes = [C.c_float]
         L.oracle_state_bytes.restype = C.c_int
@@ -284,6 +291,38 @@ def _params(states):
     return arr
 
 
+def grad_norm_codes(codes: Sequence[np.ndarray], g_scales, g_fmts,
+                    inv_loss_scale):
+    """grad_norm over gradient codes alone (no optimizer state):
+    (found_inf, norm)."""
+    n = len(codes)
+    arr = (Param * max(1, n))()
+    keep = []
+    for i, c in enumerate(codes):
+        c = np.ascontiguousarray(c, dtype=np.uint8).ravel()
+        keep.append(c)
+        arr[i].numel = c.size
+        arr[i].g = _ptr(c)
+        arr[i].g_scale = float(np.float32(g_scales[i]))
+        arr[i].g_fmt = g_fmts[i] if isinstance(g_fmts, (list, tuple)) else g_fmts
+    norm = C.c_double(0.0)
+    rc = lib().oracle_grad_norm(arr, n, inv_loss_scale, C.byref(norm))
+    if rc < 0:
+        raise ValueError(f"oracle_grad_norm rejected its arguments ({rc})")
+    return rc, norm.value
+
+
+def adam_step_coef(states: Sequence[StepState], lr, beta1, beta2, eps, wd, step,
+                   inv_loss_scale, clip, l2=False) -> int:
+    """One oracle step with a given clip coefficient; returns found_inf."""
+    rc = lib().oracle_adam_step_coef(_params(states), len(states),
+                                     1 if l2 else 0, lr, beta1, beta2, eps, wd,
+                                     step, inv_loss_scale, clip)
+    if rc < 0:
+        raise ValueError(f"oracle_adam_step_coef rejected its arguments ({rc})")
+    return rc
+
+
 def grad_norm(states: Sequence[StepState], inv_loss_scale):
     """(found_inf, norm): the global L2 norm of the unscaled gradient codes of
     the list (+inf when found_inf)."""
@@ -293,6 +332,16 @@ def grad_norm(states: Sequence[StepState], inv_loss_scale):
     if rc < 0:
         raise ValueError(f"oracle_grad_norm rejected its arguments ({rc})")
     return rc, norm.value
+
+
+def grad_norm_terms(states: Sequence[StepState], inv_loss_scale):
+    """(found_inf, terms): the per-tensor terms k_t^2 * S_t of the norm."""
+    terms = np.zeros(max(1, len(states)), dtype=np.float64)
+    rc = lib().oracle_grad_norm_terms(_params(states), len(states),
+                                      inv_loss_scale, _ptr(terms))
+    if rc < 0:
+        raise ValueError(f"oracle_grad_norm_terms rejected its arguments ({rc})")
+    return rc, terms[:len(states)]
 
 
 def clip_coef(norm: float, max_norm: float) -> float:

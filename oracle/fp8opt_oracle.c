@@ -476,6 +476,31 @@ int oracle_reduce_scaled(const uint8_t *src, int64_t numel, int64_t stride,
 
 /* ------------------------------------------------ gradient norm, clipping */
 
+/* The per-tensor terms of the norm below: terms[t] = k_t^2 * S_t rounded
+ * to double once (k_t^2 is exact in double; S_t, the exact sum of squared
+ * code values, is rounded to double first).  Returns 1 when found_inf (some
+ * unscaled g not finite; the terms are then not meaningful), else 0; -1 on
+ * a bad argument. */
+int oracle_grad_norm_terms(const oracle_param *p, int n, float inv_loss_scale,
+                           double *terms)
+{
+    if (n < 0) return -1;
+    int found = 0;
+    for (int t = 0; t < n; ++t) {
+        float k = or_grad_factor(&p[t], inv_loss_scale);
+        unsigned __int128 sum = 0;
+        for (int64_t i = 0; i < p[t].numel; ++i) {
+            if (!isfinite(or_grad(&p[t], k, i))) { found = 1; continue; }
+            double d = fabs((double)oracle_fp8_decode(p[t].g[i], p[t].g_fmt));
+            uint64_t q = (uint64_t)ldexp(d, 16);           /* exact integer */
+            sum += (unsigned __int128)q * q;
+        }
+        double kk = (double)k * (double)k;
+        terms[t] = kk * ldexp((double)sum, -32);
+    }
+    return found;
+}
+
 /* Global L2 norm of the unscaled gradient of a step call, the quantity a
  * training loop clips (torch.nn.utils.clip_grad_norm_ in the run script's
  * --clip-grad).  Element i of tensor t is g = decode(code) * k_t, k_t the
@@ -492,19 +517,13 @@ int oracle_grad_norm(const oracle_param *p, int n, float inv_loss_scale,
                      double *norm)
 {
     if (n < 0) return -1;
+    double *terms = malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    if (terms == NULL) return -1;
+    int found = oracle_grad_norm_terms(p, n, inv_loss_scale, terms);
     double total = 0.0;
-    for (int t = 0; t < n; ++t) {
-        float k = or_grad_factor(&p[t], inv_loss_scale);
-        unsigned __int128 sum = 0;
-        for (int64_t i = 0; i < p[t].numel; ++i) {
-            if (!isfinite(or_grad(&p[t], k, i))) { *norm = INFINITY; return 1; }
-            double d = fabs((double)oracle_fp8_decode(p[t].g[i], p[t].g_fmt));
-            uint64_t q = (uint64_t)ldexp(d, 16);           /* exact integer */
-            sum += (unsigned __int128)q * q;
-        }
-        double kk = (double)k * (double)k;
-        total = total + kk * ldexp((double)sum, -32);
-    }
+    for (int t = 0; t < n; ++t) total = total + terms[t];
+    free(terms);
+    if (found != 0) { *norm = INFINITY; return found; }
     *norm = sqrt(total);
     return 0;
 }
@@ -534,6 +553,16 @@ int oracle_adam_step_clipped(const oracle_param *p, int n, int l2, float lr,
     if (found != 0) return found;
     return or_adam_step(p, n, l2, lr, beta1, beta2, eps, wd, step,
                         inv_loss_scale, oracle_clip_coef(*norm, max_norm));
+}
+
+/* The step with a given clip coefficient (oracle_adam_step_clipped after
+ * the norm): every tensor's factor becomes k_t * clip when clip != 1. */
+int oracle_adam_step_coef(const oracle_param *p, int n, int l2, float lr,
+                          float beta1, float beta2, float eps, float wd,
+                          int64_t step, float inv_loss_scale, float clip)
+{
+    return or_adam_step(p, n, l2, lr, beta1, beta2, eps, wd, step,
+                        inv_loss_scale, clip);
 }
 
 /* Optimizer-state bytes per parameter for a level of the MS-AMP table:

@@ -162,3 +162,42 @@ def test_clipped_step_with_found_inf_writes_nothing(orc):
     for a, b in zip(states, before):
         for f in ("m", "v", "w", "m_scale"):
             assert np.array_equal(getattr(a, f), getattr(b, f)), f
+
+
+def test_step_with_a_given_coefficient_is_the_clipped_step(orc):
+    rng = np.random.default_rng(11)
+    args = (1e-3, 0.9, 0.999, 1e-8, 0.01, 2, 1.0)
+    states = make_states(orc, [100, 3000], rng)
+    a = [s.copy() for s in states]
+    b = [s.copy() for s in states]
+    c = [s.copy() for s in states]
+    found, norm = orc.adam_step_clipped(a, *args, 0.01)
+    assert found == 0
+    assert orc.adam_step_coef(b, *args, orc.clip_coef(norm, 0.01)) == 0
+    assert orc.grad_norm_codes([s.g for s in states], [s.g_scale for s in states],
+                               E4M3, 1.0) == (0, norm)
+    assert orc.adam_step_coef(c, *args, 1.0) == 0
+    plain = [s.copy() for s in states]
+    orc.adamw_step(plain, *args)
+    for x, y, z, p in zip(a, b, c, plain):
+        for f in ("m", "v", "w", "m_scale"):
+            assert np.array_equal(getattr(x, f), getattr(y, f)), f
+            assert np.array_equal(getattr(z, f), getattr(p, f)), f
+
+
+def test_per_tensor_terms(orc):
+    """Each term is the tensor's squared norm (torch float64), and the norm
+    is the root of the terms summed in tensor order."""
+    rng = np.random.default_rng(12)
+    states = make_states(orc, [1, 500, 7000], rng)
+    found, terms = orc.grad_norm_terms(states, 0.5)
+    assert found == 0
+    for s, t in zip(states, terms):
+        ref = torch_norm([s], 0.5) ** 2
+        assert abs(t - ref) <= 1e-13 * ref
+    total = 0.0
+    for t in terms:
+        total += t
+    assert orc.grad_norm(states, 0.5) == (0, math.sqrt(total))
+    states[1].g[3] = 0x7F
+    assert orc.grad_norm_terms(states, 0.5)[0] == 1
