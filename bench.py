@@ -64,6 +64,12 @@ def parse():
                    help="override the workload's layer count (profiling cases)")
     p.add_argument("--vocab", type=int, default=None,
                    help="override the workload's vocabulary (profiling cases)")
+    p.add_argument("--max-grad-norm", type=float, default=None,
+                   help="clip the headline step to this global gradient norm "
+                        "(the unfused path with the norm pass; profiling case)")
+    p.add_argument("--reduce-only", type=int, default=None, metavar="K",
+                   help="time only the local FP8 reduction of K shards of the "
+                        "124M list and print its line (profiling case)")
     return p.parse_args()
 
 
@@ -312,12 +318,51 @@ def _events_ms(fn, reps):
     return a.elapsed_time(b) / reps
 
 
+def reduce_configs(device, peak, ranks=(2, 8)):
+    """The local FP8 reduction on the 124M GPT-2 list: k shards per tensor
+    (each rank's BF16 gradient cast to E4M3 by the library, rows of a
+    [k, numel] buffer with 16-byte row stride), reduced to their mean in E4M3;
+    2k + 1 bytes per element."""
+    import torch
+    import synth
+    import bit_optimizer_gb300 as bo
+    out = {}
+    for k in ranks:
+        wl = synth.fp8_reduce(ranks=k)
+        n_t = len(wl.shapes)
+        shards = [torch.empty((k, (n + 15) // 16 * 16), dtype=torch.uint8,
+                              device=device)[:, :n] for n in wl.numels]
+        scales = torch.empty((n_t, k), device=device)
+        amax = torch.empty(n_t, device=device)
+        for r in range(k):
+            grads = [wl.rank_grad(i, 1, r, device) for i in range(n_t)]
+            rs = torch.empty(n_t, device=device)
+            bo.CastPlan(grads, [sh[r] for sh in shards], amax, rs, "e4m3")()
+            scales[:, r] = rs
+            del grads
+        codes = bo.arena_views(wl.numels, torch.uint8, device)
+        scale = torch.empty(n_t, device=device)
+        plan = bo.ReducePlan(shards, scales, codes, amax, scale, "e4m3", "e4m3",
+                             1.0 / k)
+        for _ in range(3):
+            plan()
+        ms = _events_ms(plan, 20)
+        bpe = 2 * k + 1
+        gbs = bpe * wl.n_params / (ms * 1e-3) / 1e9
+        out[f"reduce_gpt2_124m_k{k}"] = {"ms": ms, "GB/s": gbs, "frac": gbs / peak,
+                                         "bytes_per_elem": bpe, "shards": k}
+        del shards, codes
+        torch.cuda.empty_cache()
+    return out
+
+
 def other_configs(device, peak):
     """The remaining workloads, each timed on its own after the headline:
     the scaled cast of the 124M GPT-2 list (BF16 -> E4M3 and -> E5M2, 5 B per
-    element), the O2 step on the 350M list (the inf cleared), the O3 step on
+    element), the local FP8 reduction of 2 and 8 shards of that list, the O2 step on the 350M list (the inf cleared), the O3 step on
     the 1.3B list (20 B per param with the cast), the same with the scaled
-    second moment, Adam with L2 decay on the 350M list, and the launch-bound
+    second moment, Adam with L2 decay on the 350M list, the 350M step clipped
+    to a global gradient norm (and the norm pass alone), and the launch-bound
     tiny list."""
     import dataclasses
     import torch
@@ -340,6 +385,7 @@ def other_configs(device, peak):
         out[f"cast_gpt2_124m_{fmt}"] = {"ms": ms, "GB/s": gbs, "frac": gbs / peak,
                                         "bytes_per_elem": 5}
     del srcs, codes
+    out.update(reduce_configs(device, peak))
     # (name, workload, reps, optimizer options, algorithmic bytes per param)
     runs = (
         ("o2_350m", synth.o2_350m, 20, {}, STEP_BYTES["O2"]),
@@ -349,6 +395,8 @@ def other_configs(device, peak):
         # Adam with L2 decay runs as two calls and its first pass reads w:
         # cast 5 + first pass 4 + update 11
         ("o2_350m_adam_l2", synth.o2_350m, 20, {"l2": True}, 20),
+        # clipping to a global norm: cast 5 + norm 1 + first pass 2 + update 11
+        ("o2_350m_clip", synth.o2_350m, 20, {"max_grad_norm": 1.0}, 19),
         ("tiny", synth.tiny, 200, {}, STEP_BYTES["O2"]),
     )
     for name, mk, reps, kw, bpp in runs:
@@ -363,6 +411,17 @@ def other_configs(device, peak):
         out[name] = {"ms_per_step": ms, "Gparams/s": w.n_params / (ms * 1e-3) / 1e9,
                      "GB/s": gbs, "frac": gbs / peak, "level": w.level,
                      "params": w.n_params, "bytes_per_param": bpp, **kw}
+        if "max_grad_norm" in kw:
+            # the norm alone: one byte per parameter (plus its finalisation)
+            nd = torch.zeros(1, device=device)
+            fn = lambda: opt._plan.grad_norm(w.inv_loss_scale, norm_dev=nd,
+                                             sync=False)
+            for _ in range(3):
+                fn()
+            ms = _events_ms(fn, reps)
+            gbs = w.n_params / (ms * 1e-3) / 1e9
+            out["grad_norm_350m"] = {"ms": ms, "GB/s": gbs, "frac": gbs / peak,
+                                     "bytes_per_param": 1}
         del params, grads, opt
         torch.cuda.empty_cache()
     return out
@@ -384,7 +443,9 @@ def run_ours(args, wl):
             dist.barrier()
         torch.cuda.synchronize()
 
-    params, grads, flat, opt = build_state(wl, device)
+    clip_kw = ({} if args.max_grad_norm is None
+               else {"max_grad_norm": args.max_grad_norm})
+    params, grads, flat, opt = build_state(wl, device, **clip_kw)
     stream = torch.cuda.current_stream()
     flag = torch.zeros(1, dtype=torch.int32, device=device)
     ils = wl.inv_loss_scale
@@ -419,7 +480,9 @@ def run_ours(args, wl):
 
     n_params = wl.n_params
     value = world * n_params / (ms * 1e-3) / 1e9
-    bytes_step = STEP_BYTES[wl.level] * n_params
+    # with clipping: the unfused path (cast 5, norm 1, first pass 2, update 11)
+    bytes_step = (STEP_BYTES[wl.level] if not clip_kw
+                  else STEP_BYTES[wl.level] + 2) * n_params
     peak, peak_kind = measured_peak()
     upd_n, upd_ms = kern["step_update"]
     upd_avg_ms = upd_ms / max(upd_n, 1)
@@ -491,6 +554,10 @@ def run_ours(args, wl):
             "cpu_baseline": cpu,
             "other_configs": others,
         }
+        if clip_kw:
+            line["config"]["step"] = ("fp8_cast_scaled, then fp8_adam_step_clipped "
+                                      f"(global norm {args.max_grad_norm})")
+            line["config"]["bytes_per_param"] = STEP_BYTES[wl.level] + 2
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -498,6 +565,12 @@ def run_ours(args, wl):
 
 def main():
     args = parse()
+    if args.reduce_only is not None:
+        import torch
+        peak, _ = measured_peak()
+        print(json.dumps(reduce_configs(torch.device("cuda", 0), peak,
+                                        ranks=(args.reduce_only,))), flush=True)
+        return
     import dataclasses
     import synth
     over = {k: v for k, v in (("n_layer", args.n_layer), ("vocab", args.vocab))

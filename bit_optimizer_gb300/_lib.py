@@ -19,12 +19,16 @@ OK, ERR_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_LIMIT = 0, -1, -2, -4, -5
 
 # Every entry point the header declares.
 EXPORTS = ("fp8_cast_scaled", "fp8_adamw_step", "fp8_adam_step",
-           "fp8_cast_adamw_step",
+           "fp8_cast_adamw_step", "fp8_reduce_scaled", "fp8_grad_norm",
+           "fp8_adam_step_clipped", "fp8_grad_norm_terms", "fp8_clip_coef",
+           "fp8_adam_step_begin", "fp8_adam_step_finish",
            "fp8_cast_scaled_noalloc", "fp8opt_strerror",
            "fp8opt_last_error", "fp8opt_timing_enable", "fp8opt_timing_read",
            "fp8opt_release")
 KERNELS = ("cast_amax", "cast_encode", "step_amax", "step_update", "step_w8",
-           "cast_step_amax")
+           "cast_step_amax", "reduce_amax", "reduce_encode", "grad_norm",
+           "grad_norm_terms", "clip_coef", "found")
+MAX_SHARDS = 64
 
 
 class CastItem(C.Structure):
@@ -44,6 +48,15 @@ class Param(C.Structure):
         ("m_scale", C.c_void_p), ("v", C.c_void_p), ("w", C.c_void_p),
         ("w8", C.c_void_p), ("w8_scale", C.c_void_p), ("w8_amax", C.c_void_p),
         ("v_bound", C.c_void_p),
+    ]
+
+
+class ReduceItem(C.Structure):
+    """fp8opt_reduce_item."""
+    _fields_ = [
+        ("src", C.c_void_p), ("numel", C.c_int64), ("stride", C.c_int64),
+        ("src_scale", C.c_void_p), ("codes", C.c_void_p), ("amax", C.c_void_p),
+        ("scale", C.c_void_p),
     ]
 
 
@@ -79,6 +92,33 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         C.POINTER(CastItem), C.POINTER(Param), C.c_int, C.c_int, C.c_float,
         C.c_float, C.c_float, C.c_float, C.c_float, C.c_int64, C.c_float,
         C.POINTER(C.c_int), C.c_void_p, C.c_void_p]
+    L.fp8_reduce_scaled.restype = C.c_int
+    L.fp8_reduce_scaled.argtypes = [C.POINTER(ReduceItem), C.c_int, C.c_int,
+                                    C.c_int, C.c_int, C.c_float, C.c_void_p]
+    L.fp8_grad_norm.restype = C.c_int
+    L.fp8_grad_norm.argtypes = [C.POINTER(Param), C.c_int, C.c_float,
+                                C.POINTER(C.c_double), C.c_void_p,
+                                C.POINTER(C.c_int), C.c_void_p]
+    L.fp8_adam_step_clipped.restype = C.c_int
+    L.fp8_adam_step_clipped.argtypes = [
+        C.POINTER(Param), C.c_int, C.c_float, C.c_float, C.c_float, C.c_float,
+        C.c_float, C.c_int64, C.c_float, C.c_int, C.c_float,
+        C.POINTER(C.c_double), C.c_void_p, C.POINTER(C.c_int), C.c_void_p,
+        C.c_void_p]
+    L.fp8_grad_norm_terms.restype = C.c_int
+    L.fp8_grad_norm_terms.argtypes = [C.POINTER(Param), C.c_int, C.c_float,
+                                      C.c_void_p, C.c_void_p, C.c_void_p]
+    L.fp8_clip_coef.restype = C.c_int
+    L.fp8_clip_coef.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_float,
+                                C.c_void_p, C.c_void_p, C.c_void_p]
+    step_head = [C.POINTER(Param), C.c_int, C.c_float, C.c_float, C.c_float,
+                 C.c_float, C.c_float, C.c_int64, C.c_float, C.c_int]
+    L.fp8_adam_step_begin.restype = C.c_int
+    L.fp8_adam_step_begin.argtypes = step_head + [C.c_void_p, C.c_void_p,
+                                                  C.c_void_p]
+    L.fp8_adam_step_finish.restype = C.c_int
+    L.fp8_adam_step_finish.argtypes = step_head + [C.c_void_p, C.c_void_p,
+                                                   C.c_void_p, C.c_void_p]
     L.fp8_cast_scaled_noalloc.restype = C.c_int
     L.fp8_cast_scaled_noalloc.argtypes = [C.POINTER(CastItem), C.c_int, C.c_int,
                                           C.c_void_p]

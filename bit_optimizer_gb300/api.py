@@ -8,6 +8,9 @@ the optimizer runs in the library's CUDA kernels, reached through the C ABI.
 * ``fp8_adamw_step`` / ``AdamWPlan``: one multi-tensor AdamW step with E4M3
   first moment and FP16 second moment (MS-AMP O2), FP16 master plus E4M3
   weight copy for O3, and the GradScaler inf/NaN skip.
+* ``fp8_reduce_scaled`` / ``ReducePlan``: local reduction of k FP8 shards per
+  tensor (the arithmetic half of an FP8 all-reduce), re-encoded with a
+  just-in-time scale.
 * ``Fp8AdamW``: an optimizer object that owns the low-bit state in flat,
   256-byte-aligned arenas and runs cast + step for a list of FP16 weights,
   with ``state_dict`` / ``load_state_dict`` for checkpoint and resume.
@@ -25,13 +28,15 @@ from typing import Dict, List, Optional, Sequence
 import torch
 
 from . import _lib
-from ._lib import BF16, E4M3, E5M2, F16, F32, CastItem, Param, check, load
+from ._lib import (BF16, E4M3, E5M2, F16, F32, CastItem, Param, ReduceItem,
+                   check, load)
 
 FMTS = {"e4m3": E4M3, "e5m2": E5M2, E4M3: E4M3, E5M2: E5M2}
 _DT = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
 
-__all__ = ["fp8_cast_scaled", "fp8_adamw_step", "CastPlan", "AdamWPlan",
-           "CastStepPlan", "Fp8AdamW", "arena_views", "FMTS"]
+__all__ = ["fp8_cast_scaled", "fp8_adamw_step", "fp8_reduce_scaled",
+           "clip_coef", "CastPlan", "AdamWPlan", "CastStepPlan", "ReducePlan",
+           "Fp8AdamW", "arena_views", "FMTS"]
 
 
 def _fmt(f) -> int:
@@ -78,6 +83,15 @@ def arena_views(numels: Sequence[int], dtype: torch.dtype, device,
            torch.full((max(total, 1),), fill, dtype=dtype, device=device))
     views = [buf[o:o + n] for o, n in zip(offs, numels)]
     return (views, buf) if return_base else views
+
+
+def _ptr_or_none(t: Optional[torch.Tensor], name: str, dtype) -> Optional[int]:
+    if t is None:
+        return None
+    _cuda(t, name)
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    return t.data_ptr()
 
 
 # ------------------------------------------------------------------- cast
@@ -135,6 +149,84 @@ def fp8_cast_scaled(srcs: Sequence[torch.Tensor], fmt="e4m3", codes=None,
     return codes, amax, scale
 
 
+# ------------------------------------------------------------- reduction
+
+class ReducePlan:
+    """A marshalled ``fp8_reduce_scaled`` over fixed buffers.
+
+    shards: per tensor a uint8 CUDA tensor of shape [k, numel] whose rows are
+    the k shards (unit stride within a row; the row stride may exceed numel,
+    e.g. a slice of a padded receive buffer); scales: per tensor the k shard
+    scales, as a float32 CUDA tensor [n, k] (row i for tensor i) or a list of
+    k-element float32 CUDA vectors; codes: uint8 CUDA tensors of numel (one
+    may be row 0 of its shards for an in-place reduction); amax, scale:
+    float32 CUDA vectors with one entry per tensor.  post multiplies the sum
+    (1 / k for a mean).
+    """
+
+    def __init__(self, shards, scales, codes, amax, scale, in_fmt="e4m3",
+                 out_fmt="e4m3", post=1.0):
+        n = len(shards)
+        if len(codes) != n or len(scales) != n:
+            raise ValueError("shards, scales and codes differ in length")
+        ks = {int(t.shape[0]) for t in shards} if n else {1}
+        if len(ks) != 1:
+            raise ValueError("every tensor needs the same number of shards")
+        self.k = ks.pop()
+        self.in_fmt, self.out_fmt = _fmt(in_fmt), _fmt(out_fmt)
+        self.post = float(post)
+        self.n = n
+        self._keep = (list(shards), scales, list(codes), amax, scale)
+        self._items = (ReduceItem * max(n, 1))()
+        for i in range(n):
+            sh, c, sc = shards[i], codes[i], scales[i]
+            if not isinstance(sh, torch.Tensor) or not sh.is_cuda:
+                raise TypeError("shards must be CUDA tensors")
+            if sh.dtype != torch.uint8 or sh.dim() != 2 or sh.stride(1) != 1:
+                raise ValueError(f"shards[{i}] must be uint8 [k, numel] with unit row stride")
+            _cuda(c, "codes")
+            ne = int(sh.shape[1])
+            if c.dtype != torch.uint8 or c.numel() != ne:
+                raise ValueError(f"codes[{i}] must be uint8 with numel {ne}")
+            _cuda(sc, "scales")
+            if sc.dtype != torch.float32 or sc.numel() != self.k:
+                raise ValueError(f"scales[{i}] must be float32 with k elements")
+            it = self._items[i]
+            it.src, it.numel = sh.data_ptr(), ne
+            it.stride = sh.stride(0) if self.k > 1 else ne
+            it.src_scale = sc.data_ptr()
+            it.codes = c.data_ptr()
+            it.amax = _slot_ptr(amax, i, "amax")
+            it.scale = _slot_ptr(scale, i, "scale")
+
+    def __call__(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+        check(load().fp8_reduce_scaled(self._items, self.n, self.k, self.in_fmt,
+                                       self.out_fmt, self.post,
+                                       _stream_ptr(stream)))
+
+
+def fp8_reduce_scaled(shards: Sequence[torch.Tensor], scales, in_fmt="e4m3",
+                      out_fmt="e4m3", post=1.0, codes=None, amax=None,
+                      scale=None, stream=None):
+    """Reduce k FP8 shards per tensor: returns (codes list, amax, scale).
+
+    y = post * sum_j decode(shards[i][j]) / scales[i][j] (fp32, shard order);
+    amax[i] = max |y|; scale[i] = fp8_max(out_fmt) / amax[i]; codes[i] =
+    encode(y * scale[i]).
+    """
+    shards = list(shards)
+    dev = shards[0].device if shards else torch.device("cuda")
+    if codes is None:
+        codes = [torch.empty(int(s.shape[1]), dtype=torch.uint8, device=dev)
+                 for s in shards]
+    if amax is None:
+        amax = torch.empty(max(len(shards), 1), dtype=torch.float32, device=dev)
+    if scale is None:
+        scale = torch.empty(max(len(shards), 1), dtype=torch.float32, device=dev)
+    ReducePlan(shards, scales, codes, amax, scale, in_fmt, out_fmt, post)(stream)
+    return codes, amax, scale
+
+
 # ------------------------------------------------------------------- step
 
 class AdamWPlan:
@@ -187,23 +279,84 @@ class AdamWPlan:
             if v_bound is not None:
                 p.v_bound = _slot_ptr(v_bound, i, "v_bound")
         self._found = C.c_int(0)
+        self._norm = C.c_double(0.0)
+        self.last_grad_norm: Optional[float] = None
 
     def __call__(self, lr, beta1, beta2, eps, wd, step, inv_loss_scale=1.0,
                  found_inf_dev: Optional[torch.Tensor] = None, sync=True,
-                 stream=None, l2=False) -> Optional[int]:
+                 stream=None, l2=False, max_grad_norm=None,
+                 grad_norm_dev: Optional[torch.Tensor] = None) -> Optional[int]:
         """Runs one step: AdamW, or Adam with L2 decay when l2.  sync=True
         returns found_inf (0/1) after waiting for the stream; sync=False
         returns None without waiting (found_inf is then only in
-        found_inf_dev, a uint32/int32 CUDA tensor, if given)."""
+        found_inf_dev, a uint32/int32 CUDA tensor, if given).
+        max_grad_norm: clip the unscaled gradient to this global L2 norm
+        (0 reports the norm without clipping); the norm is then left in
+        ``last_grad_norm`` (sync=True) and in grad_norm_dev (float32 CUDA
+        scalar), if given."""
         fdev = None
         if found_inf_dev is not None:
             _cuda(found_inf_dev, "found_inf_dev")
             fdev = found_inf_dev.data_ptr()
         fptr = C.byref(self._found) if sync else None
-        fn = load().fp8_adam_step if l2 else load().fp8_adamw_step
-        check(fn(self._params, self.n, lr, beta1, beta2, eps, wd, int(step),
-                 inv_loss_scale, fptr, fdev, _stream_ptr(stream)))
+        if max_grad_norm is None:
+            fn = load().fp8_adam_step if l2 else load().fp8_adamw_step
+            check(fn(self._params, self.n, lr, beta1, beta2, eps, wd, int(step),
+                     inv_loss_scale, fptr, fdev, _stream_ptr(stream)))
+        else:
+            ndev = None
+            if grad_norm_dev is not None:
+                ndev = _slot_ptr(grad_norm_dev, 0, "grad_norm_dev")
+            nptr = C.byref(self._norm) if sync else None
+            check(load().fp8_adam_step_clipped(
+                self._params, self.n, lr, beta1, beta2, eps, wd, int(step),
+                inv_loss_scale, 1 if l2 else 0, float(max_grad_norm), nptr, ndev,
+                fptr, fdev, _stream_ptr(stream)))
+            self.last_grad_norm = self._norm.value if sync else None
         return self._found.value if sync else None
+
+    def grad_norm(self, inv_loss_scale=1.0, norm_dev=None, sync=True,
+                  stream=None):
+        """The global L2 norm of the unscaled gradient codes (no step):
+        returns (found_inf, norm) with sync=True, else None (the norm is then
+        only in norm_dev, a float32 CUDA scalar, if given)."""
+        ndev = None if norm_dev is None else _slot_ptr(norm_dev, 0, "norm_dev")
+        nptr = C.byref(self._norm) if sync else None
+        fptr = C.byref(self._found) if sync else None
+        check(load().fp8_grad_norm(self._params, self.n, inv_loss_scale, nptr,
+                                   ndev, fptr, _stream_ptr(stream)))
+        return (self._found.value, self._norm.value) if sync else None
+
+    # The step split at the exchange between ranks (fp8_grad_norm_terms,
+    # fp8_adam_step_begin, fp8_adam_step_finish).  hp = (lr, beta1, beta2,
+    # eps, wd, step, inv_loss_scale, l2); clip, found_in: float32 / int32 CUDA
+    # scalars or None; terms: float64 CUDA, one per record; found: int32 CUDA
+    # scalar out, or None.  None of these waits for the stream.
+
+    def norm_terms(self, inv_loss_scale, terms: torch.Tensor,
+                   found: Optional[torch.Tensor] = None, stream=None) -> None:
+        if terms.numel() < self.n:
+            raise ValueError("terms needs one float64 per record")
+        check(load().fp8_grad_norm_terms(
+            self._params, self.n, inv_loss_scale,
+            _ptr_or_none(terms, "terms", torch.float64),
+            _ptr_or_none(found, "found", torch.int32), _stream_ptr(stream)))
+
+    def begin(self, hp, clip=None, found=None, stream=None) -> None:
+        lr, b1, b2, eps, wd, step, ils, l2 = hp
+        check(load().fp8_adam_step_begin(
+            self._params, self.n, lr, b1, b2, eps, wd, int(step), ils, int(l2),
+            _ptr_or_none(clip, "clip", torch.float32),
+            _ptr_or_none(found, "found", torch.int32), _stream_ptr(stream)))
+
+    def finish(self, hp, clip=None, found_in=None, found=None,
+               stream=None) -> None:
+        lr, b1, b2, eps, wd, step, ils, l2 = hp
+        check(load().fp8_adam_step_finish(
+            self._params, self.n, lr, b1, b2, eps, wd, int(step), ils, int(l2),
+            _ptr_or_none(clip, "clip", torch.float32),
+            _ptr_or_none(found_in, "found_in", torch.int32),
+            _ptr_or_none(found, "found", torch.int32), _stream_ptr(stream)))
 
 
 def fp8_adamw_step(g, g_scale, m, m_scale, v, w, lr, beta1, beta2, eps, wd,
@@ -255,7 +408,10 @@ class Fp8AdamW:
     ``scaled_v``: the FP16 second moment is kept relative to a per-tensor
     bound (``v_bound``), so small gradients do not underflow it.  ``l2``:
     Adam with L2 weight decay (torch.optim.Adam) instead of AdamW; it runs as
-    two calls (the fused call is AdamW only).
+    two calls (the fused call is AdamW only).  ``max_grad_norm``: clip the
+    unscaled gradient to this global L2 norm (torch's clip_grad_norm_; 0
+    only measures it); also two calls, and ``last_grad_norm`` holds the norm
+    after a synchronous step.
 
     ``step(grads, inv_loss_scale)`` casts the gradients to FP8 (per-tensor
     just-in-time scale) and runs the update; it returns found_inf and, like a
@@ -265,7 +421,8 @@ class Fp8AdamW:
 
     def __init__(self, params: Sequence[torch.Tensor], lr=1e-3,
                  betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01, level="O2",
-                 grad_fmt="e4m3", fused=True, scaled_v=False, l2=False):
+                 grad_fmt="e4m3", fused=True, scaled_v=False, l2=False,
+                 max_grad_norm=None):
         if level not in ("O2", "O3"):
             raise ValueError("level must be 'O2' or 'O3'")
         self.params = list(params)
@@ -277,7 +434,10 @@ class Fp8AdamW:
         self.eps, self.wd = eps, weight_decay
         self.level, self.grad_fmt = level, grad_fmt
         self.l2 = l2
-        self.fused = fused and not l2   # one fp8_cast_adamw_step call per step
+        self.max_grad_norm = max_grad_norm
+        # one fp8_cast_adamw_step call per step (AdamW without clipping)
+        self.fused = fused and not l2 and max_grad_norm is None
+        self.last_grad_norm: Optional[float] = None
         self.step_count = 0
         n = len(self.params)
         dev = self.params[0].device if n else torch.device("cuda")
@@ -331,7 +491,8 @@ class Fp8AdamW:
             cast(stream)
             found = self._plan(self.lr, self.beta1, self.beta2, self.eps, self.wd,
                                t, inv_loss_scale, found_inf_dev, sync, stream,
-                               l2=self.l2)
+                               l2=self.l2, max_grad_norm=self.max_grad_norm)
+            self.last_grad_norm = self._plan.last_grad_norm
         if not sync or found == 0:
             self.step_count = t
         return found
@@ -342,6 +503,7 @@ class Fp8AdamW:
              "hparams": (self.lr, self.beta1, self.beta2, self.eps, self.wd),
              "m": [t.clone() for t in self.m], "v": [t.clone() for t in self.v],
              "m_scale": self.m_scale.clone(), "l2": self.l2,
+             "max_grad_norm": self.max_grad_norm,
              "v_bound": None if self.v_bound is None else self.v_bound.clone()}
         if self.level == "O3":
             d["w8"] = [t.clone() for t in self.w8]
@@ -373,3 +535,17 @@ class Fp8AdamW:
     def state_bytes_per_param(level="O2") -> int:
         """Optimizer-state bytes per parameter: 1 (E4M3 m) + 2 (FP16 v)."""
         return 1 + 2
+
+
+def clip_coef(terms: torch.Tensor, max_grad_norm: float, clip: torch.Tensor,
+              norm: Optional[torch.Tensor] = None,
+              found: Optional[torch.Tensor] = None, stream=None) -> None:
+    """fp8_clip_coef: the global norm (float64 CUDA scalar, optional) and the
+    clip coefficient (float32 CUDA scalar) from the terms of every record
+    (float64 CUDA, in record order); found (int32 CUDA scalar, optional)
+    nonzero makes the norm +inf."""
+    check(load().fp8_clip_coef(
+        _ptr_or_none(terms, "terms", torch.float64), terms.numel(),
+        _ptr_or_none(found, "found", torch.int32), float(max_grad_norm),
+        _ptr_or_none(norm, "norm", torch.float64),
+        _ptr_or_none(clip, "clip", torch.float32), _stream_ptr(stream)))

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libfp8opt.so")
 SOURCES = ["api.cu", "cast_kernels.cu", "step_kernels.cu", "fused_kernels.cu",
-           "noalloc.cu"]
+           "noalloc.cu", "reduce_kernels.cu", "norm_kernels.cu"]
 DEPS = ["fp8opt_internal.cuh", os.path.join("..", "..", "include", "fp8opt.h")]
 
 NVCC = os.environ.get("NVCC", "nvcc")

@@ -37,6 +37,38 @@ cudaError_t launch_cast_step(const CastDesc* cdescs, const StepDesc* sdescs,
                              int grid_update, int grid_w8, bool any_vs,
                              cudaStream_t stream, LaunchMark mark);
 cudaError_t cast_step_occupancy(int* per_sm);
+cudaError_t launch_reduce(const ReduceDesc* descs, const Chunk* chunks,
+                          uint32_t nchunks, unsigned long long* slots,
+                          uint32_t epoch, int k, int in_fmt, int out_fmt,
+                          float post, int grid_amax, int grid_encode,
+                          cudaStream_t stream, LaunchMark mark);
+cudaError_t reduce_occupancy(int* amax_per_sm, int* encode_per_sm);
+cudaError_t launch_grad_norm_terms(const StepDesc* descs, const Chunk* chunks,
+                                   uint32_t nchunks, int n, float ils,
+                                   unsigned long long* sums,
+                                   unsigned long long* found, uint32_t epoch,
+                                   double* terms, uint32_t* found_out, int grid,
+                                   cudaStream_t stream, LaunchMark mark);
+cudaError_t launch_clip_coef(const double* terms, int n,
+                             const unsigned long long* found_slot, uint32_t epoch,
+                             const uint32_t* found_flag, float max_norm,
+                             double* norm_out, float* clip_out, float* user_norm,
+                             cudaStream_t stream, LaunchMark mark);
+cudaError_t launch_found(unsigned long long* slot, uint32_t epoch,
+                         const uint32_t* in, uint32_t* out, cudaStream_t stream,
+                         LaunchMark mark);
+cudaError_t launch_step_amax(const StepDesc* descs, const Chunk* chunks,
+                             uint32_t nchunks, const StepScratch& sc,
+                             const StepScalars& s, uint32_t epoch, int grid_amax,
+                             cudaStream_t stream, LaunchMark mark);
+cudaError_t launch_step_update(const StepDesc* descs, const Chunk* chunks,
+                               uint32_t nchunks, const Chunk* chunks_o3,
+                               uint32_t nchunks_o3, const StepScratch& sc,
+                               const StepScalars& s, uint32_t epoch,
+                               uint32_t* found_dev, int grid_update, int grid_w8,
+                               bool any_vs, cudaStream_t stream,
+                               LaunchMark mark);
+cudaError_t grad_norm_occupancy(int* per_sm);
 
 namespace {
 
@@ -83,6 +115,8 @@ struct DeviceInfo {
   int cast_amax = 0, cast_encode = 0;          // persistent grid sizes
   int step_amax = 0, step_update = 0, step_w8 = 0;
   int cast_step = 0;
+  int reduce_amax = 0, reduce_encode = 0;
+  int grad_norm = 0;
 };
 
 // Per-(device, stream) state.  The slot region holds only epoch-tagged
@@ -96,6 +130,7 @@ struct Workspace {
   uint32_t epoch = 0;
   DevBuf slots;
   DevBuf saved_scales;       // n floats: m_scale before the step
+  DevBuf norm_buf;           // gradient norm: 2n sum words, norm, clip
   // cast tables
   std::vector<fp8opt_cast_item> cast_key;
   DevBuf cast_descs, cast_chunks;
@@ -105,18 +140,27 @@ struct Workspace {
   DevBuf step_descs, step_chunks;
   uint32_t step_nchunks = 0, step_nchunks_o3 = 0;
   bool step_any_vs = false;   // some record has a scaled second moment
-  bool have_cast = false, have_step = false;
+  uint32_t begin_epoch = 0;   // epoch of an fp8_adam_step_begin awaiting its finish
+  // reduction tables
+  std::vector<fp8opt_reduce_item> reduce_key;
+  DevBuf reduce_descs, reduce_chunks;
+  uint32_t reduce_nchunks = 0;
+  bool have_cast = false, have_step = false, have_reduce = false;
 
   void release() {
     slots.release();
     saved_scales.release();
+    norm_buf.release();
     cast_descs.release();
     cast_chunks.release();
     step_descs.release();
     step_chunks.release();
+    reduce_descs.release();
+    reduce_chunks.release();
     cast_key.clear();
     step_key.clear();
-    have_cast = have_step = false;
+    reduce_key.clear();
+    have_cast = have_step = have_reduce = false;
   }
 };
 
@@ -143,6 +187,11 @@ cudaError_t device_info(int dev, DeviceInfo** out) {
   info.step_w8 = info.sms * (c > 0 ? c : 1);
   if ((e = cast_step_occupancy(&a)) != cudaSuccess) return e;
   info.cast_step = info.sms * (a > 0 ? a : 1);
+  if ((e = reduce_occupancy(&a, &b)) != cudaSuccess) return e;
+  info.reduce_amax = info.sms * (a > 0 ? a : 1);
+  info.reduce_encode = info.sms * (b > 0 ? b : 1);
+  if ((e = grad_norm_occupancy(&a)) != cudaSuccess) return e;
+  info.grad_norm = info.sms * (a > 0 ? a : 1);
   *out = &(g_dev[dev] = info);
   return cudaSuccess;
 }
@@ -185,7 +234,8 @@ cudaError_t prepare_slots(Workspace* ws, size_t words, cudaStream_t stream,
 
 const char* const kKernelNames[kNumKernels] = {
     "cast_amax", "cast_encode", "step_amax", "step_update", "step_w8",
-    "cast_step_amax"};
+    "cast_step_amax", "reduce_amax", "reduce_encode", "grad_norm",
+    "grad_norm_terms", "clip_coef", "found"};
 
 struct Timing {
   bool on = false;
@@ -343,6 +393,7 @@ StepScalars make_scalars(float lr, float beta1, float beta2, float eps, float wd
   s.ils = inv_loss_scale;
   s.wd = wd;
   s.l2 = l2 ? 1 : 0;
+  s.clip = nullptr;
   return s;
 }
 
@@ -437,6 +488,69 @@ int ensure_step_tables(const char* fn, Workspace* ws, const fp8opt_param* params
   return FP8OPT_OK;
 }
 
+int check_reduce_args(const char* fn, const fp8opt_reduce_item* items, int n,
+                      int k, int in_fmt, int out_fmt) {
+  if (n < 0 || (n > 0 && items == nullptr))
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": n < 0 or items is NULL");
+  if (k < 1 || k > FP8OPT_MAX_SHARDS)
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": k outside [1, FP8OPT_MAX_SHARDS]");
+  if ((in_fmt != FP8OPT_E4M3 && in_fmt != FP8OPT_E5M2) ||
+      (out_fmt != FP8OPT_E4M3 && out_fmt != FP8OPT_E5M2))
+    return fail(FP8OPT_ERR_UNSUPPORTED, std::string(fn) + ": unknown format");
+  for (int i = 0; i < n; ++i) {
+    const fp8opt_reduce_item& it = items[i];
+    const std::string at = std::string(fn) + ": item " + std::to_string(i);
+    if (it.numel < 0 || it.stride < it.numel || it.amax == nullptr ||
+        it.scale == nullptr ||
+        (it.numel > 0 && (it.src == nullptr || it.src_scale == nullptr ||
+                          it.codes == nullptr)))
+      return fail(FP8OPT_ERR_ARG, at + ": bad numel or stride, or NULL pointer");
+    if (it.numel > 0 && it.stride > (INT64_MAX - it.numel) / k)
+      return fail(FP8OPT_ERR_ARG, at + ": k * stride overflows");
+  }
+  return FP8OPT_OK;
+}
+
+// The workspace's reduction tables for this item list.
+int ensure_reduce_tables(const char* fn, Workspace* ws,
+                         const fp8opt_reduce_item* items, int n,
+                         cudaStream_t stream) {
+  if (ws->have_reduce && same_list(ws->reduce_key, items, n)) return FP8OPT_OK;
+  std::vector<ReduceDesc> descs((size_t)n);
+  std::vector<Chunk> chunks;
+  size_t total = 0;
+  for (int i = 0; i < n; ++i) total += chunks_of(items[i].numel);
+  if (total > 0xFFFFFFFFull)
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": list too long");
+  chunks.reserve(total);
+  for (int i = 0; i < n; ++i) {
+    const fp8opt_reduce_item& it = items[i];
+    ReduceDesc& d = descs[(size_t)i];
+    d.src = it.src;
+    d.src_scale = it.src_scale;
+    d.codes = it.codes;
+    d.amax_out = it.amax;
+    d.scale_out = it.scale;
+    d.numel = it.numel;
+    d.stride = it.stride;
+    d.vec_ok = aligned(it.src, 16) && aligned(it.codes, 16) && it.stride % 16 == 0;
+    d.pad = 0;
+    for (uint32_t c = 0, nc = chunks_of(it.numel); c < nc; ++c)
+      chunks.push_back(Chunk{(uint32_t)i, c});
+  }
+  ws->have_reduce = false;
+  cudaError_t e;
+  if ((e = upload(ws->reduce_descs, descs.data(), descs.size() * sizeof(ReduceDesc),
+                  stream)) != cudaSuccess ||
+      (e = upload(ws->reduce_chunks, chunks.data(), chunks.size() * sizeof(Chunk),
+                  stream)) != cudaSuccess)
+    return cuda_fail(e, (std::string(fn) + ": table upload").c_str());
+  ws->reduce_key.assign(items, items + n);
+  ws->reduce_nchunks = (uint32_t)chunks.size();
+  ws->have_reduce = true;
+  return FP8OPT_OK;
+}
+
 // The empty-list result of a step call.
 int empty_step(const char* fn, int* found_inf, uint32_t* found_inf_dev,
                cudaStream_t stream) {
@@ -487,54 +601,329 @@ extern "C" int fp8_cast_scaled(const fp8opt_cast_item* items, int n, int fmt,
   return FP8OPT_OK;
 }
 
-namespace fp8opt {
-namespace {
-
-// The two step entry points: AdamW (l2 false) and Adam with L2 decay.
-int adam_step(const char* fn, bool l2, const fp8opt_param* params, int n,
-              float lr, float beta1, float beta2, float eps, float wd,
-              int64_t step, float inv_loss_scale, int* found_inf,
-              uint32_t* found_inf_dev, void* stream_ptr) {
-  int st = check_step_args(fn, params, n, step);
-  if (st != FP8OPT_OK) return st;
+extern "C" int fp8_reduce_scaled(const fp8opt_reduce_item* items, int n, int k,
+                                 int in_fmt, int out_fmt, float post,
+                                 void* stream_ptr) {
+  const char* fn = "fp8_reduce_scaled";
+  int st = check_reduce_args(fn, items, n, k, in_fmt, out_fmt);
+  if (st != FP8OPT_OK || n == 0) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  if (n == 0) return empty_step(fn, found_inf, found_inf_dev, stream);
-  const StepScalars s =
-      make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale, l2);
 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0;
   DeviceInfo* info = nullptr;
   if ((st = current_device_and_info(&dev, &info)) != FP8OPT_OK) return st;
   Workspace* ws = workspace(dev, stream);
-  if ((st = ensure_step_tables(fn, ws, params, n, stream)) != FP8OPT_OK) return st;
+  if ((st = ensure_reduce_tables(fn, ws, items, n, stream)) != FP8OPT_OK) return st;
 
   uint32_t epoch = 0;
+  cudaError_t e = prepare_slots(ws, (size_t)n, stream, &epoch);   // [0, n) amax
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_reduce_scaled: workspace");
+  e = launch_reduce(static_cast<const ReduceDesc*>(ws->reduce_descs.ptr),
+                    static_cast<const Chunk*>(ws->reduce_chunks.ptr),
+                    ws->reduce_nchunks,
+                    static_cast<unsigned long long*>(ws->slots.ptr), epoch, k,
+                    in_fmt, out_fmt, post, info->reduce_amax, info->reduce_encode,
+                    stream, launch_mark());
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_reduce_scaled: launch");
+  return FP8OPT_OK;
+}
+
+namespace fp8opt {
+namespace {
+
+// The gradient-norm request of a call: the norm pass runs when `on`; the
+// step (if any) clips to max_norm when max_norm > 0.
+struct NormReq {
+  bool on = false;
+  float max_norm = 0.0f;
+  double* norm = nullptr;      // host out, or NULL
+  float* norm_dev = nullptr;   // device out, or NULL
+};
+
+// Waits for the stream and reads this call's found_inf word and norm.
+int read_results(const char* fn, const unsigned long long* found, uint32_t epoch,
+                 const double* norm_dev, cudaStream_t stream, int* found_out,
+                 double* norm_out) {
+  unsigned long long tag = 0;
+  double norm = 0.0;
+  cudaError_t e = cudaSuccess;
+  if (found_out != nullptr)
+    e = cudaMemcpyAsync(&tag, found, sizeof(tag), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess && norm_out != nullptr)
+    e = cudaMemcpyAsync(&norm, norm_dev, sizeof(norm), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": result read").c_str());
+  if (found_out != nullptr)
+    *found_out = tag == (((unsigned long long)epoch << 32) | 1ull) ? 1 : 0;
+  if (norm_out != nullptr) *norm_out = norm;
+  return FP8OPT_OK;
+}
+
+// One step call's device state: tables, slots and scratch on the stream's
+// workspace, with this call's epoch.
+struct StepCall {
+  cudaStream_t stream = nullptr;
+  DeviceInfo* info = nullptr;
+  Workspace* ws = nullptr;
+  uint32_t epoch = 0;
+  StepScratch sc;
+  const StepDesc* descs = nullptr;
+  const Chunk* chunks = nullptr;
+  unsigned long long* sums = nullptr;   // norm: 2n words
+  double* terms = nullptr;              // norm: n terms
+  double* norm = nullptr;               // norm: the norm
+  float* clip = nullptr;                // norm: the clip coefficient
+};
+
+// Tables and scratch for n records; fresh = false keeps the current epoch
+// (the finish of a begun step).  Must run under g_mu.
+int setup_step(const char* fn, const fp8opt_param* params, int n,
+               void* stream_ptr, bool with_norm, bool fresh, StepCall* c) {
+  c->stream = static_cast<cudaStream_t>(stream_ptr);
+  int dev = 0;
+  int st = current_device_and_info(&dev, &c->info);
+  if (st != FP8OPT_OK) return st;
+  Workspace* ws = c->ws = workspace(dev, c->stream);
+  if ((st = ensure_step_tables(fn, ws, params, n, c->stream)) != FP8OPT_OK) return st;
   // slots: [0, n) amax of m, [n, 2n) amax of the master, [2n, 3n) max |g|,
-  // [3n] found_inf; saved: [0, n) m_scale, [n, 2n) v_bound
-  cudaError_t e = prepare_slots(ws, 3 * (size_t)n + 1, stream, &epoch);
+  // [3n] found_inf; saved: [0, n) m_scale, [n, 2n) v_bound; norm: [0, 2n)
+  // 128-bit sums, n terms, the norm (double) and the clip coefficient (float)
+  cudaError_t e = cudaSuccess;
+  if (fresh) e = prepare_slots(ws, 3 * (size_t)n + 1, c->stream, &c->epoch);
+  else c->epoch = ws->epoch;
   if (e == cudaSuccess) e = ws->saved_scales.reserve(2 * (size_t)n * sizeof(float));
+  const size_t sum_bytes = 2 * (size_t)n * sizeof(unsigned long long);
+  const size_t norm_bytes = sum_bytes + (size_t)n * sizeof(double) + 16;
+  if (e == cudaSuccess && with_norm) e = ws->norm_buf.reserve(norm_bytes);
+  if (e == cudaSuccess && with_norm)
+    e = cudaMemsetAsync(ws->norm_buf.ptr, 0, sum_bytes, c->stream);
   if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": workspace").c_str());
   unsigned long long* slots = static_cast<unsigned long long*>(ws->slots.ptr);
-  StepScratch sc;
-  sc.amax_m = slots;
-  sc.amax_w = slots + n;
-  sc.amax_g = slots + 2 * (size_t)n;
-  sc.found = slots + 3 * (size_t)n;
-  sc.old_m_scale = static_cast<float*>(ws->saved_scales.ptr);
-  sc.old_v_bound = sc.old_m_scale + n;
-  const Chunk* chunks = static_cast<const Chunk*>(ws->step_chunks.ptr);
-  e = launch_step(static_cast<const StepDesc*>(ws->step_descs.ptr), chunks,
-                  ws->step_nchunks, chunks + ws->step_nchunks, ws->step_nchunks_o3,
-                  sc, s, epoch, found_inf_dev, info->step_amax, info->step_update,
-                  info->step_w8, ws->step_any_vs, stream, launch_mark());
-  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
-  if (found_inf != nullptr) return read_found(fn, sc.found, epoch, stream, found_inf);
+  c->sc.amax_m = slots;
+  c->sc.amax_w = slots + n;
+  c->sc.amax_g = slots + 2 * (size_t)n;
+  c->sc.found = slots + 3 * (size_t)n;
+  c->sc.old_m_scale = static_cast<float*>(ws->saved_scales.ptr);
+  c->sc.old_v_bound = c->sc.old_m_scale + n;
+  c->descs = static_cast<const StepDesc*>(ws->step_descs.ptr);
+  c->chunks = static_cast<const Chunk*>(ws->step_chunks.ptr);
+  if (with_norm) {
+    char* nb = static_cast<char*>(ws->norm_buf.ptr);
+    c->sums = reinterpret_cast<unsigned long long*>(nb);
+    c->terms = reinterpret_cast<double*>(nb + sum_bytes);
+    c->norm = c->terms + n;
+    c->clip = reinterpret_cast<float*>(c->norm + 1);
+  }
+  return FP8OPT_OK;
+}
+
+// The step entry points: AdamW (l2 false) or Adam with L2 decay, optionally
+// with the gradient-norm pass (and clipping); run_step false runs the norm
+// pass alone.
+int adam_step(const char* fn, bool l2, const fp8opt_param* params, int n,
+              float lr, float beta1, float beta2, float eps, float wd,
+              int64_t step, float inv_loss_scale, int* found_inf,
+              uint32_t* found_inf_dev, void* stream_ptr,
+              const NormReq& nr = NormReq(), bool run_step = true) {
+  int st = check_step_args(fn, params, n, step);
+  if (st != FP8OPT_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (n == 0) {
+    if (nr.norm != nullptr) *nr.norm = 0.0;
+    if (nr.norm_dev != nullptr) {
+      cudaError_t e = cudaMemsetAsync(nr.norm_dev, 0, sizeof(float), stream);
+      if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": norm_dev").c_str());
+    }
+    return empty_step(fn, found_inf, found_inf_dev, stream);
+  }
+  StepScalars s =
+      make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale, l2);
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  StepCall c;
+  if ((st = setup_step(fn, params, n, stream_ptr, nr.on, true, &c)) != FP8OPT_OK)
+    return st;
+  Workspace* ws = c.ws;
+  cudaError_t e = cudaSuccess;
+  if (nr.on) {
+    e = launch_grad_norm_terms(c.descs, c.chunks, ws->step_nchunks, n,
+                               inv_loss_scale, c.sums, c.sc.found, c.epoch,
+                               c.terms, nullptr, c.info->grad_norm, stream,
+                               launch_mark());
+    if (e == cudaSuccess)
+      e = launch_clip_coef(c.terms, n, c.sc.found, c.epoch, nullptr,
+                           run_step ? nr.max_norm : 0.0f, c.norm, c.clip,
+                           nr.norm_dev, stream, launch_mark());
+    if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
+    if (nr.max_norm > 0.0f) s.clip = c.clip;
+  }
+  if (run_step) {
+    e = launch_step(c.descs, c.chunks, ws->step_nchunks,
+                    c.chunks + ws->step_nchunks, ws->step_nchunks_o3, c.sc, s,
+                    c.epoch, found_inf_dev, c.info->step_amax,
+                    c.info->step_update, c.info->step_w8, ws->step_any_vs,
+                    stream, launch_mark());
+    if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
+  }
+  if (found_inf != nullptr || nr.norm != nullptr)
+    return read_results(fn, c.sc.found, c.epoch, c.norm, stream, found_inf, nr.norm);
   return FP8OPT_OK;
 }
 
 }  // namespace
 }  // namespace fp8opt
+
+extern "C" int fp8_grad_norm(const fp8opt_param* params, int n,
+                             float inv_loss_scale, double* norm, float* norm_dev,
+                             int* found_inf, void* stream_ptr) {
+  NormReq nr;
+  nr.on = true;
+  nr.norm = norm;
+  nr.norm_dev = norm_dev;
+  return adam_step("fp8_grad_norm", false, params, n, 0.0f, 0.0f, 0.0f, 0.0f,
+                   0.0f, 1, inv_loss_scale, found_inf, nullptr, stream_ptr, nr,
+                   false);
+}
+
+extern "C" int fp8_adam_step_clipped(const fp8opt_param* params, int n, float lr,
+                                     float beta1, float beta2, float eps,
+                                     float wd, int64_t step, float inv_loss_scale,
+                                     int l2, float max_grad_norm,
+                                     double* grad_norm, float* grad_norm_dev,
+                                     int* found_inf, uint32_t* found_inf_dev,
+                                     void* stream_ptr) {
+  if (l2 != 0 && l2 != 1)
+    return fail(FP8OPT_ERR_ARG, "fp8_adam_step_clipped: l2 must be 0 or 1");
+  if (std::isnan(max_grad_norm))
+    return fail(FP8OPT_ERR_ARG, "fp8_adam_step_clipped: max_grad_norm is NaN");
+  NormReq nr;
+  nr.on = true;
+  nr.max_norm = max_grad_norm;
+  nr.norm = grad_norm;
+  nr.norm_dev = grad_norm_dev;
+  return adam_step("fp8_adam_step_clipped", l2 != 0, params, n, lr, beta1, beta2,
+                   eps, wd, step, inv_loss_scale, found_inf, found_inf_dev,
+                   stream_ptr, nr, true);
+}
+
+extern "C" int fp8_grad_norm_terms(const fp8opt_param* params, int n,
+                                   float inv_loss_scale, double* terms_dev,
+                                   uint32_t* found_dev, void* stream_ptr) {
+  const char* fn = "fp8_grad_norm_terms";
+  int st = check_step_args(fn, params, n, 1);
+  if (st != FP8OPT_OK) return st;
+  if (n > 0 && terms_dev == nullptr)
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": terms_dev is NULL");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (n == 0) return empty_step(fn, nullptr, found_dev, stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  StepCall c;
+  if ((st = setup_step(fn, params, n, stream_ptr, true, true, &c)) != FP8OPT_OK)
+    return st;
+  cudaError_t e = launch_grad_norm_terms(
+      c.descs, c.chunks, c.ws->step_nchunks, n, inv_loss_scale, c.sums,
+      c.sc.found, c.epoch, terms_dev, found_dev, c.info->grad_norm, stream,
+      launch_mark());
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_grad_norm_terms: launch");
+  return FP8OPT_OK;
+}
+
+extern "C" int fp8_clip_coef(const double* terms_dev, int n,
+                             const uint32_t* found_dev, float max_grad_norm,
+                             double* norm_dev, float* clip_dev,
+                             void* stream_ptr) {
+  if (n < 0 || (n > 0 && terms_dev == nullptr) || clip_dev == nullptr ||
+      std::isnan(max_grad_norm))
+    return fail(FP8OPT_ERR_ARG,
+                "fp8_clip_coef: n < 0, NULL terms or clip, or a NaN max_grad_norm");
+  std::lock_guard<std::mutex> lock(g_mu);
+  cudaError_t e = launch_clip_coef(terms_dev, n, nullptr, 0, found_dev,
+                                   max_grad_norm, norm_dev, clip_dev, nullptr,
+                                   static_cast<cudaStream_t>(stream_ptr),
+                                   launch_mark());
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_clip_coef: launch");
+  return FP8OPT_OK;
+}
+
+namespace fp8opt {
+namespace {
+
+int check_phase_args(const char* fn, int l2) {
+  if (l2 != 0 && l2 != 1) return fail(FP8OPT_ERR_ARG, std::string(fn) + ": l2 must be 0 or 1");
+  return FP8OPT_OK;
+}
+
+}  // namespace
+}  // namespace fp8opt
+
+extern "C" int fp8_adam_step_begin(const fp8opt_param* params, int n, float lr,
+                                   float beta1, float beta2, float eps, float wd,
+                                   int64_t step, float inv_loss_scale, int l2,
+                                   const float* clip_dev, uint32_t* found_dev,
+                                   void* stream_ptr) {
+  const char* fn = "fp8_adam_step_begin";
+  int st = check_phase_args(fn, l2);
+  if (st == FP8OPT_OK) st = check_step_args(fn, params, n, step);
+  if (st != FP8OPT_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (n == 0) return empty_step(fn, nullptr, found_dev, stream);
+  StepScalars s = make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale,
+                               l2 != 0);
+  s.clip = clip_dev;
+  std::lock_guard<std::mutex> lock(g_mu);
+  StepCall c;
+  if ((st = setup_step(fn, params, n, stream_ptr, false, true, &c)) != FP8OPT_OK)
+    return st;
+  cudaError_t e = launch_step_amax(c.descs, c.chunks, c.ws->step_nchunks, c.sc, s,
+                                   c.epoch, c.info->step_amax, stream,
+                                   launch_mark());
+  if (e == cudaSuccess && found_dev != nullptr)
+    e = launch_found(c.sc.found, c.epoch, nullptr, found_dev, stream, launch_mark());
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_adam_step_begin: launch");
+  c.ws->begin_epoch = c.epoch;
+  return FP8OPT_OK;
+}
+
+extern "C" int fp8_adam_step_finish(const fp8opt_param* params, int n, float lr,
+                                    float beta1, float beta2, float eps,
+                                    float wd, int64_t step, float inv_loss_scale,
+                                    int l2, const float* clip_dev,
+                                    const uint32_t* found_in_dev,
+                                    uint32_t* found_dev, void* stream_ptr) {
+  const char* fn = "fp8_adam_step_finish";
+  int st = check_phase_args(fn, l2);
+  if (st == FP8OPT_OK) st = check_step_args(fn, params, n, step);
+  if (st != FP8OPT_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (n == 0) return empty_step(fn, nullptr, found_dev, stream);
+  StepScalars s = make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale,
+                               l2 != 0);
+  s.clip = clip_dev;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  DeviceInfo* info = nullptr;
+  if ((st = current_device_and_info(&dev, &info)) != FP8OPT_OK) return st;
+  Workspace* ws = workspace(dev, stream);
+  if (!ws->have_step || !same_list(ws->step_key, params, n) ||
+      ws->begin_epoch == 0 || ws->begin_epoch != ws->epoch)
+    return fail(FP8OPT_ERR_ARG, std::string(fn) +
+                                    ": no fp8_adam_step_begin of this list is "
+                                    "pending on this stream");
+  StepCall c;
+  if ((st = setup_step(fn, params, n, stream_ptr, false, false, &c)) != FP8OPT_OK)
+    return st;
+  ws->begin_epoch = 0;
+  cudaError_t e = launch_found(c.sc.found, c.epoch, found_in_dev, nullptr, stream,
+                               launch_mark());
+  if (e == cudaSuccess)
+    e = launch_step_update(c.descs, c.chunks, ws->step_nchunks,
+                           c.chunks + ws->step_nchunks, ws->step_nchunks_o3, c.sc,
+                           s, c.epoch, found_dev, info->step_update, info->step_w8,
+                           ws->step_any_vs, stream, launch_mark());
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_adam_step_finish: launch");
+  return FP8OPT_OK;
+}
 
 extern "C" int fp8_adamw_step(const fp8opt_param* params, int n, float lr,
                               float beta1, float beta2, float eps, float wd,

@@ -67,9 +67,28 @@ struct StepDesc {
   int16_t o3;       // emits the E4M3 weight copy (w8 is NULL if numel is 0)
 };
 
+// One tensor of a local FP8 reduction: k shards of numel codes, shard j at
+// src + j * stride, encoded with scale src_scale[j].
+struct ReduceDesc {
+  const uint8_t* src;
+  const float* src_scale;
+  uint8_t* codes;
+  float* amax_out;
+  float* scale_out;
+  int64_t numel;
+  int64_t stride;
+  int32_t vec_ok;   // src, stride and codes aligned for 16-byte accesses
+  int32_t pad;
+};
+
+// Most shards one reduction call takes.
+constexpr int kMaxShards = 64;
+
 // Kernels, for the optional per-launch event timing.
 enum KernelId { kCastAmaxK = 0, kCastEncodeK, kStepAmaxK, kStepUpdateK,
-                kStepW8K, kCastStepAmaxK, kNumKernels };
+                kStepW8K, kCastStepAmaxK, kReduceAmaxK, kReduceEncodeK,
+                kGradNormK, kGradNormTermsK, kClipCoefK, kFoundK,
+                kNumKernels };
 
 // Called before (end = 0) and after (end = 1) each kernel launch when timing
 // is on; nullptr otherwise.
@@ -82,6 +101,7 @@ struct StepScalars {
   float beta1, beta2, eps, omb1, omb2, step_size, inv_sbc2, decay, ils;
   float wd;       // the L2 coefficient (used when l2)
   int32_t l2;     // Adam with L2 decay: g = fma(wd, w, g); decay is then 1
+  const float* clip;  // device clip coefficient (k becomes k * clip), or NULL
 };
 
 // A scaled second moment is stored as FP16 of v * kVTarget / bound.

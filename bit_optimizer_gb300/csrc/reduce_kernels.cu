@@ -1,0 +1,311 @@
+// Local reduction of FP8 shards: the arithmetic half of an FP8 all-reduce
+// (MS-AMP O1 keeps weight gradients and their AllReduce communication in FP8).
+//
+// k shards of one tensor, shard j encoded with its own scale s_j, are summed
+// per element as y = post * (((x_0 + x_1) + x_2) + ...), x_j = decode(c_j) *
+// (1 / s_j), in fp32 with every product and sum rounded on its own, and y is
+// cast back to FP8 with a just-in-time per-tensor scale.  Two persistent
+// kernels over the chunk table, like the cast:
+//   reduce_amax_kernel    y per element, per-tensor max |y| (NaN above +inf
+//                         above every finite value) into the tagged slots.
+//   reduce_encode_kernel  scale = fp8_max / amax in each chunk's prologue, y
+//                         again, code = encode(y * scale).  It walks the
+//                         chunk table backwards so the chunks the first pass
+//                         read last are still in L2.
+// Bytes per element: k (first pass) + k + 1 (encode).
+//
+// Vector path: thread t of a CTA takes the 16-code groups at tile + g *
+// (kThreads * 16) + t * 16 (g = 0, 1): one 16-byte load per shard and group,
+// issued for kShardBatch shards at a time before their sums, so a warp's
+// every access is one contiguous 512-byte span and a thread keeps four loads
+// in flight.  A
+// tensor whose sum has a non-finite element (amax not finite) is encoded on
+// the scalar path, which selects the NaN / infinity codes explicitly.
+#include "fp8opt_internal.cuh"
+
+namespace fp8opt {
+
+namespace {
+
+constexpr int kRGroup = 16;    // codes per vector group (one 16-byte access)
+constexpr int kRGroups = 2;    // groups per thread per tile
+constexpr int kShardBatch = 2; // shards whose loads are issued before their sums
+constexpr int64_t kRTile = (int64_t)kThreads * kRGroup * kRGroups;  // 8192
+
+// Resident CTAs per SM both kernels are compiled for (caps their registers).
+#ifndef FP8OPT_REDUCE_MIN_BLOCKS
+#define FP8OPT_REDUCE_MIN_BLOCKS 3
+#endif
+
+// acc (+)= decode(16 codes) * r.  The product and the sum are the scalar
+// round-to-nearest intrinsics, which are never merged into a fused
+// multiply-add: the sum must round twice, as written.
+__device__ __forceinline__ float2 mul_add2(float2 acc, float2 x, float r) {
+  return make_float2(__fadd_rn(acc.x, __fmul_rn(x.x, r)),
+                     __fadd_rn(acc.y, __fmul_rn(x.y, r)));
+}
+
+template <int IN, bool FIRST>
+__device__ __forceinline__ void accum16(uint4 c, float r, float2 (&acc)[8]) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 a = dec2<IN>(w[q] & 0xFFFFu), b = dec2<IN>(w[q] >> 16);
+    if (FIRST) {
+      acc[2 * q] = make_float2(__fmul_rn(a.x, r), __fmul_rn(a.y, r));
+      acc[2 * q + 1] = make_float2(__fmul_rn(b.x, r), __fmul_rn(b.y, r));
+    } else {
+      acc[2 * q] = mul_add2(acc[2 * q], a, r);
+      acc[2 * q + 1] = mul_add2(acc[2 * q + 1], b, r);
+    }
+  }
+}
+
+// y for this thread's kRGroups full 16-code groups at i0[g]: the shard-order
+// sum times post.  LAST: the codes are read for the last time (encode pass).
+template <int IN, bool LAST>
+__device__ __forceinline__ void reduce_groups(const uint8_t* src, int64_t stride,
+                                              int k, const float* r_s,
+                                              float post, const int64_t (&i0)[kRGroups],
+                                              float2 (&y)[kRGroups][8]) {
+#pragma unroll 1
+  for (int j0 = 0; j0 < k; j0 += kShardBatch) {
+    uint4 c[kShardBatch][kRGroups];
+#pragma unroll
+    for (int b = 0; b < kShardBatch; ++b) {
+      if (j0 + b < k) {
+        const uint8_t* p = src + (int64_t)(j0 + b) * stride;
+#pragma unroll
+        for (int g = 0; g < kRGroups; ++g)
+          c[b][g] = LAST ? ld_once4(p + i0[g]) : ld_keep4(p + i0[g]);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kShardBatch; ++b) {
+      if (j0 + b < k) {
+        const float r = r_s[j0 + b];
+#pragma unroll
+        for (int g = 0; g < kRGroups; ++g) {
+          if (j0 + b == 0)
+            accum16<IN, true>(c[b][g], r, y[g]);
+          else
+            accum16<IN, false>(c[b][g], r, y[g]);
+        }
+      }
+    }
+  }
+  const float2 pp = splat2(post);
+#pragma unroll
+  for (int g = 0; g < kRGroups; ++g)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) y[g][q] = mul2(y[g][q], pp);
+}
+
+// y of one element (scalar path: unaligned buffers and ragged tails).
+template <int IN>
+__device__ __forceinline__ float reduce_one(const uint8_t* src, int64_t stride,
+                                            int k, const float* r_s, float post,
+                                            int64_t i) {
+  float acc = __fmul_rn(dec2<IN>(src[i]).x, r_s[0]);
+  for (int j = 1; j < k; ++j)
+    acc = __fadd_rn(acc, __fmul_rn(dec2<IN>(src[(int64_t)j * stride + i]).x, r_s[j]));
+  return __fmul_rn(acc, post);
+}
+
+// r_s[j] = 1 / s_j for this chunk's tensor (one IEEE division per shard).
+__device__ __forceinline__ void load_reciprocals(const ReduceDesc& d, int k,
+                                                 float* r_s) {
+  __syncthreads();   // the previous chunk may still be reading r_s
+  if (threadIdx.x < k && d.numel > 0)
+    r_s[threadIdx.x] = __fdiv_rn(1.0f, d.src_scale[threadIdx.x]);
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- amax pass
+
+template <int IN>
+__device__ uint32_t thread_reduce_amax(const ReduceDesc& d, int k,
+                                       const float* r_s, float post,
+                                       int64_t begin, int64_t end) {
+  const int tid = threadIdx.x;
+  const bool vec = d.vec_ok != 0;
+  uint32_t mx = 0;
+#pragma unroll 1
+  for (int64_t base = begin; base < end; base += kRTile) {
+    if (vec && base + kRTile <= end) {
+      int64_t i0[kRGroups];
+#pragma unroll
+      for (int g = 0; g < kRGroups; ++g)
+        i0[g] = base + g * (kThreads * kRGroup) + tid * kRGroup;
+      float2 y[kRGroups][8];
+      reduce_groups<IN, false>(d.src, d.stride, k, r_s, post, i0, y);
+#pragma unroll
+      for (int g = 0; g < kRGroups; ++g)
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          mx = max(mx, max(abs_bits(y[g][q].x), abs_bits(y[g][q].y)));
+    } else {
+#pragma unroll 1
+      for (int g = 0; g < kRGroups; ++g) {
+        const int64_t i0 = base + g * (kThreads * kRGroup) + tid * kRGroup;
+        for (int e = 0; e < kRGroup; ++e) {
+          const int64_t i = i0 + e;
+          if (i >= end) break;
+          mx = max(mx, abs_bits(reduce_one<IN>(d.src, d.stride, k, r_s, post, i)));
+        }
+      }
+    }
+  }
+  return mx;
+}
+
+template <int IN>
+__global__ void __launch_bounds__(kThreads, FP8OPT_REDUCE_MIN_BLOCKS)
+reduce_amax_kernel(const ReduceDesc* __restrict__ descs,
+                   const Chunk* __restrict__ chunks, uint32_t nchunks, int k,
+                   float post, unsigned long long* __restrict__ slots,
+                   uint32_t epoch) {
+  __shared__ uint32_t red[kThreads / 32];
+  __shared__ float r_s[kMaxShards];
+  for (uint32_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+    const Chunk ch = chunks[c];
+    const ReduceDesc d = descs[ch.tensor];
+    load_reciprocals(d, k, r_s);
+    const int64_t begin = (int64_t)ch.index * kChunkElems;
+    const int64_t end = min(begin + kChunkElems, d.numel);
+    uint32_t mx = thread_reduce_amax<IN>(d, k, r_s, post, begin, end);
+    mx = block_max_u32(mx, red);
+    if (threadIdx.x == 0 && mx != 0)
+      atomicMax(&slots[ch.tensor], slot_tag(epoch, canon_amax_bits(mx)));
+  }
+}
+
+// -------------------------------------------------------------- encode pass
+
+// Sixteen finite y -> sixteen codes of format OUT in a uint4.
+template <int OUT>
+__device__ __forceinline__ uint4 encode16(const float2 (&y)[8], float scale) {
+  const float2 ss = splat2(scale);
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 a = mul2(y[2 * q], ss), b = mul2(y[2 * q + 1], ss);
+    w[q] = enc2<OUT>(a.x, a.y) | (enc2<OUT>(b.x, b.y) << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int IN, int OUT, bool CHECKED>
+__device__ void thread_reduce_encode(const ReduceDesc& d, int k,
+                                     const float* r_s, float post, float scale,
+                                     int64_t begin, int64_t end) {
+  const int tid = threadIdx.x;
+  const bool vec = d.vec_ok != 0 && !CHECKED;
+#pragma unroll 1
+  for (int64_t base = begin; base < end; base += kRTile) {
+    if (vec && base + kRTile <= end) {
+      int64_t i0[kRGroups];
+#pragma unroll
+      for (int g = 0; g < kRGroups; ++g)
+        i0[g] = base + g * (kThreads * kRGroup) + tid * kRGroup;
+      float2 y[kRGroups][8];
+      reduce_groups<IN, true>(d.src, d.stride, k, r_s, post, i0, y);
+#pragma unroll
+      for (int g = 0; g < kRGroups; ++g)
+        *reinterpret_cast<uint4*>(d.codes + i0[g]) = encode16<OUT>(y[g], scale);
+    } else {
+#pragma unroll 1
+      for (int g = 0; g < kRGroups; ++g) {
+        const int64_t i0 = base + g * (kThreads * kRGroup) + tid * kRGroup;
+        for (int e = 0; e < kRGroup; ++e) {
+          const int64_t i = i0 + e;
+          if (i >= end) break;
+          const float t =
+              __fmul_rn(reduce_one<IN>(d.src, d.stride, k, r_s, post, i), scale);
+          d.codes[i] = (uint8_t)(CHECKED ? enc1_checked<OUT>(t)
+                                         : (enc2<OUT>(t, 0.0f) & 0xFFu));
+        }
+      }
+    }
+  }
+}
+
+template <int IN, int OUT>
+__global__ void __launch_bounds__(kThreads, FP8OPT_REDUCE_MIN_BLOCKS)
+reduce_encode_kernel(const ReduceDesc* __restrict__ descs,
+                     const Chunk* __restrict__ chunks, uint32_t nchunks, int k,
+                     float post, const unsigned long long* __restrict__ slots,
+                     uint32_t epoch) {
+  __shared__ float r_s[kMaxShards];
+  for (uint32_t r = blockIdx.x; r < nchunks; r += gridDim.x) {
+    const Chunk ch = chunks[nchunks - 1 - r];
+    const ReduceDesc d = descs[ch.tensor];
+    load_reciprocals(d, k, r_s);
+    const uint32_t ab = slot_value(slots[ch.tensor], epoch);
+    const float scale = scale_from_amax_bits(ab, fp8_max_of<OUT>());
+    if (ch.index == 0 && threadIdx.x == 0) {
+      *d.amax_out = __uint_as_float(ab);
+      *d.scale_out = scale;
+    }
+    const int64_t begin = (int64_t)ch.index * kChunkElems;
+    const int64_t end = min(begin + kChunkElems, d.numel);
+    if (ab >= 0x7F800000u)
+      thread_reduce_encode<IN, OUT, true>(d, k, r_s, post, scale, begin, end);
+    else
+      thread_reduce_encode<IN, OUT, false>(d, k, r_s, post, scale, begin, end);
+  }
+}
+
+template <int IN>
+void launch_encode(uint32_t grid, const ReduceDesc* descs, const Chunk* chunks,
+                   uint32_t nchunks, int k, float post,
+                   const unsigned long long* slots, uint32_t epoch, int out_fmt,
+                   cudaStream_t stream) {
+  if (out_fmt == kE4M3)
+    reduce_encode_kernel<IN, kE4M3><<<grid, kThreads, 0, stream>>>(
+        descs, chunks, nchunks, k, post, slots, epoch);
+  else
+    reduce_encode_kernel<IN, kE5M2><<<grid, kThreads, 0, stream>>>(
+        descs, chunks, nchunks, k, post, slots, epoch);
+}
+
+}  // namespace
+
+// Launches both passes on `stream`; 1 <= k <= kMaxShards.
+cudaError_t launch_reduce(const ReduceDesc* descs, const Chunk* chunks,
+                          uint32_t nchunks, unsigned long long* slots,
+                          uint32_t epoch, int k, int in_fmt, int out_fmt,
+                          float post, int grid_amax, int grid_encode,
+                          cudaStream_t stream, LaunchMark mark) {
+  if (nchunks == 0) return cudaSuccess;
+  const uint32_t ga = grid_min((uint32_t)grid_amax, nchunks);
+  const uint32_t ge = grid_min((uint32_t)grid_encode, nchunks);
+  if (mark) mark(kReduceAmaxK, 0, stream);
+  if (in_fmt == kE4M3)
+    reduce_amax_kernel<kE4M3><<<ga, kThreads, 0, stream>>>(descs, chunks, nchunks,
+                                                           k, post, slots, epoch);
+  else
+    reduce_amax_kernel<kE5M2><<<ga, kThreads, 0, stream>>>(descs, chunks, nchunks,
+                                                           k, post, slots, epoch);
+  if (mark) mark(kReduceAmaxK, 1, stream);
+  if (mark) mark(kReduceEncodeK, 0, stream);
+  if (in_fmt == kE4M3)
+    launch_encode<kE4M3>(ge, descs, chunks, nchunks, k, post, slots, epoch,
+                         out_fmt, stream);
+  else
+    launch_encode<kE5M2>(ge, descs, chunks, nchunks, k, post, slots, epoch,
+                         out_fmt, stream);
+  if (mark) mark(kReduceEncodeK, 1, stream);
+  return cudaGetLastError();
+}
+
+// Resident CTAs per SM of the two reduction kernels.
+cudaError_t reduce_occupancy(int* amax_per_sm, int* encode_per_sm) {
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      amax_per_sm, reduce_amax_kernel<kE4M3>, kThreads, 0);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      encode_per_sm, reduce_encode_kernel<kE4M3, kE4M3>, kThreads, 0);
+}
+
+}  // namespace fp8opt

@@ -21,6 +21,8 @@
 // Arithmetic per element, in fp32 (each operation rounded once; fma rounds
 // the product and the sum once together):
 //   g = dec(g_code) * k                       k = inv_loss_scale / g_scale
+//                                             (times the clip coefficient
+//                                             when the call clips)
 //   [Adam with L2 decay: g = fma(wd, w_old, g)]
 //   m = fma(beta1, dec(m_code) * minv, (1 - beta1) * g)   minv = 1 / m_scale
 //   v = fma(beta2, v_old, (1 - beta2) * (g * g))
@@ -178,7 +180,9 @@ step_amax_kernel(const StepDesc* __restrict__ descs,
       sc.old_m_scale[ch.tensor] = ms;
       if (d.v_bound != nullptr) sc.old_v_bound[ch.tensor] = *d.v_bound;
     }
-    const float k = __fdiv_rn(s.ils, gs), minv = __frcp_rn(ms);
+    float k = __fdiv_rn(s.ils, gs);
+    if (s.clip != nullptr) k = __fmul_rn(k, *s.clip);
+    const float minv = __frcp_rn(ms);
     const int64_t begin = (int64_t)ch.index * kChunkElems;
     const int64_t end = min(begin + kChunkElems, d.numel);
     uint32_t mx = 0, gx = 0, bad = 0;
@@ -418,7 +422,8 @@ step_update_kernel(const StepDesc* __restrict__ descs,
   for (uint32_t r = blockIdx.x; r < nchunks; r += gridDim.x) {
     const Chunk ch = chunks[nchunks - 1 - r];
     const StepDesc d = descs[ch.tensor];
-    const float k = __fdiv_rn(s.ils, *d.g_scale);
+    float k = __fdiv_rn(s.ils, *d.g_scale);
+    if (s.clip != nullptr) k = __fmul_rn(k, *s.clip);
     const float minv = __frcp_rn(sc.old_m_scale[ch.tensor]);
     const uint32_t am = slot_value(sc.amax_m[ch.tensor], epoch);
     const float msc = scale_from_amax_bits(am, 448.0f);
@@ -559,6 +564,24 @@ cudaError_t launch_step_update(const StepDesc* descs, const Chunk* chunks,
   return cudaGetLastError();
 }
 
+// The first pass alone (found_inf, the amax of the new first moment, max |g|).
+cudaError_t launch_step_amax(const StepDesc* descs, const Chunk* chunks,
+                             uint32_t nchunks, const StepScratch& sc,
+                             const StepScalars& s, uint32_t epoch, int grid_amax,
+                             cudaStream_t stream, LaunchMark mark) {
+  if (nchunks == 0) return cudaSuccess;
+  if (mark) mark(kStepAmaxK, 0, stream);
+  const uint32_t ga = grid_min((uint32_t)grid_amax, nchunks);
+  if (s.l2)
+    step_amax_kernel<true><<<ga, kThreads, 0, stream>>>(descs, chunks, nchunks,
+                                                        sc, s, epoch);
+  else
+    step_amax_kernel<false><<<ga, kThreads, 0, stream>>>(descs, chunks, nchunks,
+                                                         sc, s, epoch);
+  if (mark) mark(kStepAmaxK, 1, stream);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_step(const StepDesc* descs, const Chunk* chunks,
                         uint32_t nchunks, const Chunk* chunks_o3,
                         uint32_t nchunks_o3, const StepScratch& sc,
@@ -570,16 +593,8 @@ cudaError_t launch_step(const StepDesc* descs, const Chunk* chunks,
     if (found_dev) return cudaMemsetAsync(found_dev, 0, sizeof(uint32_t), stream);
     return cudaSuccess;
   }
-  if (mark) mark(kStepAmaxK, 0, stream);
-  const uint32_t ga = grid_min((uint32_t)grid_amax, nchunks);
-  if (s.l2)
-    step_amax_kernel<true><<<ga, kThreads, 0, stream>>>(descs, chunks, nchunks,
-                                                        sc, s, epoch);
-  else
-    step_amax_kernel<false><<<ga, kThreads, 0, stream>>>(descs, chunks, nchunks,
-                                                         sc, s, epoch);
-  if (mark) mark(kStepAmaxK, 1, stream);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_step_amax(descs, chunks, nchunks, sc, s, epoch,
+                                   grid_amax, stream, mark);
   if (e != cudaSuccess) return e;
   return launch_step_update(descs, chunks, nchunks, chunks_o3, nchunks_o3, sc, s,
                             epoch, found_dev, grid_update, grid_w8, any_vs,

@@ -236,6 +236,154 @@ FP8OPT_API int fp8_cast_adamw_step(const fp8opt_cast_item *grads,
                                    int *found_inf, uint32_t *found_inf_dev,
                                    void *stream);
 
+/*
+ * fp8_grad_norm: the global L2 norm of the unscaled gradient of a step call
+ * (the quantity torch.nn.utils.clip_grad_norm_ clips; the run script's
+ * --clip-grad), without a step.  Element i of record t is g = decode(g code)
+ * * k_t with k_t = inv_loss_scale / g_scale, the step's own factor.  The norm
+ * is sqrt(sum over t, in record order, of fl64(k_t^2 * fl64(S_t))), where
+ * S_t = sum of decode(code)^2 over record t is taken exactly (every code value
+ * is a multiple of 2^-16, so S_t is an integer count of 2^-32; the library
+ * sums it in 128-bit integers), each sum over records is rounded to double,
+ * and the root is correctly rounded.  The result does not depend on the
+ * kernel schedule.  If some g is not finite (found_inf, the step's test) the
+ * norm is +inf.
+ *
+ * Reads only the records' g, g_scale, g_fmt and numel (one byte per element);
+ * the other fields must still be valid (same checks as fp8_adamw_step).
+ * norm: host double, may be NULL (when set, the call waits for the stream);
+ * norm_dev: device fp32, may be NULL; found_inf: host int, may be NULL.
+ */
+FP8OPT_API int fp8_grad_norm(const fp8opt_param *params, int n,
+                             float inv_loss_scale, double *norm, float *norm_dev,
+                             int *found_inf, void *stream);
+
+/*
+ * fp8_adam_step_clipped: fp8_adamw_step (l2 = 0) or fp8_adam_step (l2 = 1)
+ * with the unscaled gradient clipped to a global L2 norm of max_grad_norm, as
+ * torch.nn.utils.clip_grad_norm_ does between GradScaler.unscale_ and the
+ * optimizer step.  The norm is fp8_grad_norm's; the clip coefficient is
+ * c = max_grad_norm / (norm + 1e-6) in double, rounded to fp32, applied when
+ * it is below 1 by multiplying every record's factor: k_t' = fl32(k_t * c).
+ * found_inf is decided on the unclipped gradient, as the norm's +inf.  With
+ * max_grad_norm <= 0 nothing is clipped (the step equals the unclipped one and
+ * the norm is still reported).  One extra pass over the gradient codes (1 byte
+ * per element) precedes the step.
+ *
+ * grad_norm: host double, may be NULL; grad_norm_dev: device fp32, may be
+ * NULL.  Other arguments, results and errors as fp8_adamw_step; also
+ * FP8OPT_ERR_ARG for l2 not 0 or 1, or a NaN max_grad_norm.
+ */
+FP8OPT_API int fp8_adam_step_clipped(const fp8opt_param *params, int n, float lr,
+                                     float beta1, float beta2, float eps,
+                                     float wd, int64_t step,
+                                     float inv_loss_scale, int l2,
+                                     float max_grad_norm, double *grad_norm,
+                                     float *grad_norm_dev, int *found_inf,
+                                     uint32_t *found_inf_dev, void *stream);
+
+/*
+ * Sharded steps.  When each of several ranks (one per GPU) owns the optimizer
+ * state of a disjoint set of whole tensors (ZeRO-1 style), a step needs one
+ * exchange between ranks: found_inf must be combined (every rank skips if any
+ * rank saw a non-finite gradient) and, with clipping, the global norm taken
+ * over all ranks' tensors.  The calls below split the step at that exchange;
+ * the caller runs the collective (e.g. NCCL) between them.  On one rank they
+ * give exactly fp8_adamw_step / fp8_adam_step / fp8_adam_step_clipped.
+ *
+ * fp8_grad_norm_terms: for each of the n records, term_t = fl64(k_t^2 *
+ * fl64(S_t)) with S_t the exact sum of squared code values (fp8_grad_norm's
+ * definition), written to terms_dev[t] (device doubles); found_dev (device
+ * uint32, may be NULL) receives this rank's found_inf.  A rank places its
+ * terms at its records' positions of a vector of all records, zero elsewhere;
+ * summing those vectors over ranks (any order: each position has one nonzero
+ * addend) reproduces every term exactly.
+ *
+ * fp8_clip_coef: from the n terms of all records (in record order), norm =
+ * sqrt(sum of terms in order) (+inf if *found_dev is nonzero; found_dev may be
+ * NULL), written to norm_dev (device double, may be NULL), and the clip
+ * coefficient (fp8_adam_step_clipped's) to clip_dev (device fp32): 1 when
+ * max_grad_norm <= 0 or the norm is within it.
+ *
+ * fp8_adam_step_begin: the step's first pass over this rank's records
+ * (found_inf, and the amax of each new first moment); found_dev (device
+ * uint32, may be NULL) receives this rank's found_inf.  clip_dev: a device
+ * fp32 clip coefficient (from fp8_clip_coef) or NULL for none.
+ *
+ * fp8_adam_step_finish: the rest of the step (update and O3 weight copy) of
+ * the same records, skipped when this rank's found_inf or *found_in_dev (the
+ * value combined over ranks; may be NULL) is nonzero; found_dev (may be NULL)
+ * receives the combined flag.  It must follow fp8_adam_step_begin on the same
+ * stream with the same records and the same hyperparameters, with no other
+ * step, cast or norm call on that stream in between; otherwise FP8OPT_ERR_ARG
+ * and nothing is launched.
+ *
+ * Arguments otherwise as fp8_adamw_step; l2: 0 AdamW, 1 Adam with L2 decay.
+ * None of these calls waits for the stream.
+ */
+FP8OPT_API int fp8_grad_norm_terms(const fp8opt_param *params, int n,
+                                   float inv_loss_scale, double *terms_dev,
+                                   uint32_t *found_dev, void *stream);
+FP8OPT_API int fp8_clip_coef(const double *terms_dev, int n,
+                             const uint32_t *found_dev, float max_grad_norm,
+                             double *norm_dev, float *clip_dev, void *stream);
+FP8OPT_API int fp8_adam_step_begin(const fp8opt_param *params, int n, float lr,
+                                   float beta1, float beta2, float eps, float wd,
+                                   int64_t step, float inv_loss_scale, int l2,
+                                   const float *clip_dev, uint32_t *found_dev,
+                                   void *stream);
+FP8OPT_API int fp8_adam_step_finish(const fp8opt_param *params, int n, float lr,
+                                    float beta1, float beta2, float eps,
+                                    float wd, int64_t step,
+                                    float inv_loss_scale, int l2,
+                                    const float *clip_dev,
+                                    const uint32_t *found_in_dev,
+                                    uint32_t *found_dev, void *stream);
+
+/* Most shards one fp8_reduce_scaled call takes. */
+#define FP8OPT_MAX_SHARDS 64
+
+/* One tensor of a local FP8 reduction: k shards of numel codes each. */
+typedef struct {
+    const uint8_t *src;       /* k shards: shard j is the numel codes at
+                                 src + j * stride (the call's in_fmt) */
+    int64_t numel;            /* >= 0; 0 is allowed (amax 0, scale 1) */
+    int64_t stride;           /* codes from one shard to the next, >= numel */
+    const float *src_scale;   /* k fp32: shard j was encoded with scale
+                                 src_scale[j], so its values are code * (1 /
+                                 src_scale[j]); may be NULL when numel is 0 */
+    uint8_t *codes;           /* out: numel codes of the result (out_fmt); may
+                                 be the address of one of the shards (an
+                                 in-place reduction), may not overlap them
+                                 otherwise */
+    float *amax;              /* out: one fp32, max |y| (as the cast's amax) */
+    float *scale;             /* out: one fp32, fp8_max(out_fmt) / amax, with
+                                 the cast's guards */
+} fp8opt_reduce_item;
+
+/*
+ * fp8_reduce_scaled: local reduction of k FP8 shards per tensor, the
+ * arithmetic half of an FP8 all-reduce (MS-AMP O1: weight gradients and their
+ * AllReduce communication in FP8), e.g. the receive side of a reduce-scatter
+ * or the k-way sum of gradient shards gathered on one GPU.
+ *
+ * Per element, in fp32 with every product and sum rounded on its own:
+ *   y = (((x_0 + x_1) + x_2) + ... + x_{k-1}) * post,
+ *   x_j = decode(code_j) * r_j,   r_j = 1 / src_scale[j] (one division)
+ * then, per tensor, the cast of y exactly as fp8_cast_scaled casts an fp32
+ * tensor: amax = max |y|, scale = fp8_max / amax, code = encode(y * scale).
+ * post = 1 gives the sum, 1 / k the mean.  A NaN or infinite x_j, or an
+ * overflowing sum, gives a non-finite y that takes the cast's non-finite codes.
+ *
+ * items: host array of n records; 1 <= k <= FP8OPT_MAX_SHARDS; in_fmt and
+ * out_fmt: FP8OPT_E4M3 or FP8OPT_E5M2.  16-byte-aligned src and codes with a
+ * stride that is a multiple of 16 take the vector path; other buffers a
+ * scalar path.  Bytes per element: 2k + 1 (two passes over the shards).
+ */
+FP8OPT_API int fp8_reduce_scaled(const fp8opt_reduce_item *items, int n, int k,
+                                 int in_fmt, int out_fmt, float post,
+                                 void *stream);
+
 /* Text of a status code (static storage). */
 FP8OPT_API const char *fp8opt_strerror(int status);
 
@@ -249,8 +397,9 @@ FP8OPT_API const char *fp8opt_last_error(void);
  * timed region.  fp8opt_timing_enable(1) clears the record and starts
  * recording; fp8opt_timing_enable(0) stops.  fp8opt_timing_read waits for the
  * recorded events and returns, for one kernel name ("cast_amax",
- * "cast_encode", "step_amax", "step_update", "step_w8", "cast_step_amax"),
- * the launches
+ * "cast_encode", "step_amax", "step_update", "step_w8", "cast_step_amax",
+ * "reduce_amax", "reduce_encode", "grad_norm", "grad_norm_terms", "clip_coef",
+ * "found"), the launches
  * recorded since enabling and their summed duration in milliseconds.  Returns
  * FP8OPT_ERR_ARG for an unknown name or NULL outputs. */
 FP8OPT_API int fp8opt_timing_enable(int on);

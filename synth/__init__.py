@@ -23,6 +23,10 @@ Workloads (transformer-shaped lists, GPT-2/GPT-3 naming):
 * ``o3_1p3b``     24 layers, d 2048, ffn 8192, vocab 50304 (292 tensors);
                   grads N(0, sigma), sigma log-uniform [1e-5, 1e-2]; FP16
                   master weights N(0, 0.02); O3 (emits an E4M3 weight copy).
+* ``fp8_reduce``  the ``gpt2_cast`` list with ``ranks`` = 8 data-parallel
+                  gradient copies per tensor (``rank_grad``), each a BF16
+                  N(0, sigma_t * f_r) draw, f_r log-uniform in [1/2, 2]: the
+                  shards an FP8 all-reduce sums once each is cast to FP8.
 * ``o2_6p7b_tail`` 32 layers, d 4096, ffn 16384, vocab 50304 (388 tensors),
                   plus 200 tiny tensors with sizes log-uniform in [1, 4096]
                   and one all-zero-gradient tensor of 4096 elements (589
@@ -42,7 +46,8 @@ from typing import List, Optional, Sequence, Tuple
 import torch
 
 __all__ = [
-    "Workload", "gpt_shapes", "tiny", "gpt2_cast", "o2_350m", "o3_1p3b",
+    "Workload", "gpt_shapes", "tiny", "gpt2_cast", "fp8_reduce", "o2_350m",
+    "o3_1p3b",
     "o2_6p7b_tail", "WORKLOADS", "tensor_seed",
 ]
 
@@ -55,7 +60,8 @@ def _mix64(x: int) -> int:
     return x ^ (x >> 31)
 
 
-_ROLES = {"grad": 1, "weight": 2, "sigma": 3, "tail": 4, "m": 5, "v": 6}
+_ROLES = {"grad": 1, "weight": 2, "sigma": 3, "tail": 4, "m": 5, "v": 6,
+          "rank": 7}
 
 
 def tensor_seed(seed: int, index: int, role: str, step: int = 0) -> int:
@@ -116,6 +122,7 @@ class Workload:
     inv_loss_scale: float = 1.0
     steps: int = 1
     warmup_steps: int = 0
+    ranks: int = 1                        # data-parallel gradient copies
 
     @property
     def numels(self) -> List[int]:
@@ -156,6 +163,19 @@ class Workload:
     def grads(self, step: int, device="cpu") -> List[torch.Tensor]:
         return [self.grad(i, step, device) for i in range(len(self.shapes))]
 
+    def rank_grad(self, i: int, step: int, rank: int, device="cpu") -> torch.Tensor:
+        """Pre-cast gradient of tensor ``i`` on data-parallel rank ``rank``:
+        an independent draw per rank from the tensor's distribution, with the
+        rank's std the tensor's times a factor log-uniform in [1/2, 2]."""
+        n = self.numels[i]
+        if i in self.zero_grad_tensors:
+            return torch.zeros(n, dtype=self.grad_dtype, device=device)
+        g = _gen(device, tensor_seed(self.seed, i, "rank", step * 4096 + rank))
+        f = math.exp(random.Random(tensor_seed(self.seed, i, "rank", rank))
+                     .uniform(-math.log(2.0), math.log(2.0)))
+        x = torch.randn(n, generator=g, device=device, dtype=torch.float32)
+        return x.mul_(self.sigma(i) * f * self.grad_mult).to(self.grad_dtype)
+
     def weight(self, i: int, device="cpu") -> torch.Tensor:
         """Initial FP16 weight (O2) or FP16 master weight (O3), flat."""
         g = _gen(device, tensor_seed(self.seed, i, "weight"))
@@ -189,6 +209,14 @@ def gpt2_cast(n_layer=12, d=768, ffn=3072, vocab=50257, ctx=1024,
     nm, sh = zip(*gpt_shapes(n_layer, d, ffn, vocab, ctx))
     return Workload("gpt2_cast", list(nm), list(sh), seed=seed,
                     grad_dtype=torch.bfloat16, sigma_range=(1e-6, 1e-1))
+
+
+def fp8_reduce(ranks=8, n_layer=12, d=768, ffn=3072, vocab=50257, ctx=1024,
+               seed=6) -> Workload:
+    nm, sh = zip(*gpt_shapes(n_layer, d, ffn, vocab, ctx))
+    return Workload("fp8_reduce", list(nm), list(sh), seed=seed,
+                    grad_dtype=torch.bfloat16, sigma_range=(1e-6, 1e-1),
+                    ranks=ranks)
 
 
 def o2_350m(n_layer=24, d=1024, ffn=4096, vocab=50304, ctx=2048,
@@ -226,6 +254,7 @@ def o2_6p7b_tail(n_layer=32, d=4096, ffn=16384, vocab=50304, ctx=2048,
 
 
 WORKLOADS = {
-    "tiny": tiny, "gpt2_cast": gpt2_cast, "o2_350m": o2_350m,
+    "tiny": tiny, "gpt2_cast": gpt2_cast, "fp8_reduce": fp8_reduce,
+    "o2_350m": o2_350m,
     "o3_1p3b": o3_1p3b, "o2_6p7b_tail": o2_6p7b_tail,
 }

@@ -50,13 +50,18 @@ def test_record_layout_matches_header(lib, tmp_path):
 #include "fp8opt.h"
 #define F(T, m) printf(#T "." #m " %zu\n", offsetof(T, m))
 int main(void) {
-  printf("cast %zu\nparam %zu\n", sizeof(fp8opt_cast_item), sizeof(fp8opt_param));
+  printf("cast %zu\nparam %zu\nreduce %zu\n", sizeof(fp8opt_cast_item),
+         sizeof(fp8opt_param), sizeof(fp8opt_reduce_item));
   F(fp8opt_cast_item, src); F(fp8opt_cast_item, numel); F(fp8opt_cast_item, dtype);
   F(fp8opt_cast_item, codes); F(fp8opt_cast_item, amax); F(fp8opt_cast_item, scale);
   F(fp8opt_param, numel); F(fp8opt_param, g); F(fp8opt_param, g_scale);
   F(fp8opt_param, g_fmt); F(fp8opt_param, m); F(fp8opt_param, m_scale);
   F(fp8opt_param, v); F(fp8opt_param, w); F(fp8opt_param, w8);
-  F(fp8opt_param, w8_scale); F(fp8opt_param, w8_amax);
+  F(fp8opt_param, w8_scale); F(fp8opt_param, w8_amax); F(fp8opt_param, v_bound);
+  F(fp8opt_reduce_item, src); F(fp8opt_reduce_item, numel);
+  F(fp8opt_reduce_item, stride); F(fp8opt_reduce_item, src_scale);
+  F(fp8opt_reduce_item, codes); F(fp8opt_reduce_item, amax);
+  F(fp8opt_reduce_item, scale);
   return 0;
 }''')
     exe = tmp_path / "layout"
@@ -67,10 +72,13 @@ int main(void) {
                               check=True).stdout.splitlines())
     assert int(got["cast"]) == C.sizeof(lib.CastItem)
     assert int(got["param"]) == C.sizeof(lib.Param)
+    assert int(got["reduce"]) == C.sizeof(lib.ReduceItem)
+    classes = {"fp8opt_cast_item": lib.CastItem, "fp8opt_param": lib.Param,
+               "fp8opt_reduce_item": lib.ReduceItem}
     for key, val in got.items():
         if "." in key:
             t, m = key.split(".")
-            cls = lib.CastItem if t == "fp8opt_cast_item" else lib.Param
+            cls = classes[t]
             assert getattr(cls, m).offset == int(val), key
 
 
@@ -129,6 +137,47 @@ def test_fused_call_checks_that_the_step_takes_the_cast_outputs(lib):
     p[0].g, p[0].g_fmt = 0x1000, 1                    # other format
     assert L.fp8_cast_adamw_step(item, p, 1, 0, *args) == lib.ERR_ARG
     assert L.fp8_cast_adamw_step(item, p, 0, 0, *args) == lib.OK
+
+
+def test_reduce_argument_errors_need_no_gpu(lib):
+    L = lib.load()
+    it = (lib.ReduceItem * 1)()
+    dummy = C.c_float(1.0)
+    assert L.fp8_reduce_scaled(it, -1, 2, 0, 0, 1.0, None) == lib.ERR_ARG
+    assert L.fp8_reduce_scaled(it, 1, 0, 0, 0, 1.0, None) == lib.ERR_ARG
+    assert L.fp8_reduce_scaled(it, 1, lib.MAX_SHARDS + 1, 0, 0, 1.0, None) == lib.ERR_ARG
+    assert L.fp8_reduce_scaled(it, 1, 2, 0, 3, 1.0, None) == lib.ERR_UNSUPPORTED
+    assert L.fp8_reduce_scaled(it, 1, 2, 2, 0, 1.0, None) == lib.ERR_UNSUPPORTED
+    it[0].numel, it[0].stride = 100, 100            # NULL buffers
+    it[0].amax = it[0].scale = C.addressof(dummy)
+    assert L.fp8_reduce_scaled(it, 1, 2, 0, 0, 1.0, None) == lib.ERR_ARG
+    it[0].src = it[0].codes = it[0].src_scale = 0x1000   # never dereferenced
+    it[0].stride = 99                                # stride below numel
+    assert L.fp8_reduce_scaled(it, 1, 2, 0, 0, 1.0, None) == lib.ERR_ARG
+    assert "item 0" in L.fp8opt_last_error().decode()
+    it[0].stride = 2 ** 62                           # k * stride overflows
+    assert L.fp8_reduce_scaled(it, 1, 4, 0, 0, 1.0, None) == lib.ERR_ARG
+    assert L.fp8_reduce_scaled(it, 0, 2, 0, 0, 1.0, None) == lib.OK
+
+
+def test_norm_and_clip_argument_errors_need_no_gpu(lib):
+    L = lib.load()
+    p = (lib.Param * 1)()
+    norm, found = C.c_double(-1.0), C.c_int(7)
+    args = (1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+    assert L.fp8_grad_norm(p, -1, 1.0, None, None, None, None) == lib.ERR_ARG
+    assert L.fp8_grad_norm(p, 0, 1.0, C.byref(norm), None, C.byref(found), None) == lib.OK
+    assert norm.value == 0.0 and found.value == 0
+    assert L.fp8_adam_step_clipped(p, 0, *args, 2, 1.0, None, None, None, None,
+                                   None) == lib.ERR_ARG          # l2 not 0 or 1
+    assert L.fp8_adam_step_clipped(p, 0, *args, 0, float("nan"), None, None,
+                                   None, None, None) == lib.ERR_ARG
+    p[0].g_fmt = 3
+    assert L.fp8_adam_step_clipped(p, 1, *args, 0, 1.0, None, None, None, None,
+                                   None) == lib.ERR_UNSUPPORTED
+    p[0].g_fmt = 0
+    assert L.fp8_adam_step_clipped(p, 0, *args, 1, 1.0, C.byref(norm), None,
+                                   C.byref(found), None, None) == lib.OK
 
 
 def test_strerror_texts(lib):

@@ -1,0 +1,176 @@
+"""GPU parity of the gradient norm (fp8_grad_norm) and of the clipped step
+(fp8_adam_step_clipped) against the oracle, through the C ABI: the norm is
+bit-exact as a double, and the clipped step's state meets the step's
+tolerances."""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from harness import GpuState, fresh_states, oracle_cast, set_grads
+from parity import check_f32_exact, to_np_u16, to_np_u8
+
+pytestmark = pytest.mark.gpu
+E4M3, E5M2 = oracle.E4M3, oracle.E5M2
+
+
+@pytest.fixture(scope="module")
+def bo():
+    import bit_optimizer_gb300 as bo
+    return bo
+
+
+def states_for(wl, step, fmt=E4M3, o3=False, scaled_v=False):
+    states = fresh_states(wl.weights(), o3=o3, g_fmt=fmt, scaled_v=scaled_v)
+    codes, _, scale = oracle_cast(wl.grads(step), fmt)
+    set_grads(states, codes, scale)
+    return states
+
+
+def gpu_norm(gpu, ils):
+    nd = torch.full((1,), -1.0, device="cuda")
+    found, norm = gpu.plan.grad_norm(ils, norm_dev=nd)
+    assert nd.item() == np.float32(norm) or (math.isinf(norm) and math.isinf(nd.item()))
+    return found, norm
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("ils", [1.0, 2.0 ** -16, 0.37])
+def test_grad_norm_bit_exact(bo, fmt, ils):
+    wl = synth.o2_6p7b_tail(n_layer=1, d=128, ffn=512, vocab=3000, ctx=64,
+                            n_tail=40)
+    wl = dataclasses.replace(wl, grad_mult=1.0 / ils)
+    states = states_for(wl, 1, fmt)
+    gpu = GpuState([s.copy() for s in states], misalign={1, 7})
+    found, norm = gpu_norm(gpu, ils)
+    rf, rn = oracle.grad_norm(states, ils)
+    assert found == rf == 0
+    assert norm == rn, (norm, rn)
+
+
+def test_grad_norm_exactness_case(bo):
+    """One E5M2 maximum and 4096 minimum subnormals: only an exact sum keeps
+    the small squares (the oracle's exactness pin, on the GPU)."""
+    g = np.concatenate([[0x7B], np.full(4096, 0x01), np.full(40000, 0x81)]).astype(np.uint8)
+    n = g.size
+    st = oracle.StepState(g, 1.0, np.zeros(n, np.uint8), 1.0, np.zeros(n, np.uint16),
+                          np.zeros(n, np.uint16), g_fmt=E5M2)
+    gpu = GpuState([st.copy()])
+    found, norm = gpu_norm(gpu, 1.0)
+    assert (found, norm) == oracle.grad_norm([st], 1.0)
+    assert norm == math.sqrt(57344.0 ** 2 + 44096 * 2.0 ** -32)
+
+
+@pytest.mark.parametrize("case", ["nan_code", "e5m2_inf", "overflow"])
+def test_grad_norm_found_inf(bo, case):
+    wl = synth.tiny()
+    fmt = E5M2 if case == "e5m2_inf" else E4M3
+    states = states_for(wl, 1, fmt)
+    ils = 1.0
+    if case == "nan_code":
+        states[2].g[1234] = 0xFF
+    elif case == "e5m2_inf":
+        states[0].g[5] = 0x7C
+    else:
+        states[1].g_scale = 1.0
+        ils = 1e37
+    gpu = GpuState([s.copy() for s in states])
+    assert gpu_norm(gpu, ils) == (1, math.inf) == oracle.grad_norm(states, ils)
+
+
+def clipped_lockstep(bo, wl, states, steps, max_norm, l2=False, fmt=E4M3,
+                     misalign=()):
+    gpu = None
+    norms = []
+    for t in range(1, steps + 1):
+        codes, _, scale = oracle_cast(wl.grads(t), fmt)
+        set_grads(states, codes, scale)
+        if gpu is None:
+            gpu = GpuState([s.copy() for s in states], misalign=misalign)
+        else:
+            gpu.load_state(states)
+        f_ref, n_ref = oracle.adam_step_clipped(
+            states, wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, t,
+            wl.inv_loss_scale, max_norm, l2=l2)
+        nd = torch.zeros(1, device="cuda")
+        found = gpu.plan(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, t,
+                         wl.inv_loss_scale, found_inf_dev=gpu.found_dev, l2=l2,
+                         max_grad_norm=max_norm, grad_norm_dev=nd)
+        assert found == f_ref == 0
+        assert gpu.plan.last_grad_norm == n_ref
+        assert nd.item() == np.float32(n_ref)
+        gpu.compare(states)
+        norms.append(n_ref)
+    return norms
+
+
+@pytest.mark.parametrize("l2", [False, True])
+def test_clipped_steps_o2_long_tail(bo, l2):
+    wl = synth.o2_6p7b_tail(n_layer=1, d=128, ffn=512, vocab=3000, ctx=64,
+                            n_tail=30)
+    states = fresh_states(wl.weights(), o3=False)
+    # the gradient norm of this list is far above 0.05: every step clips
+    norms = clipped_lockstep(bo, wl, states, 3, 0.05, l2=l2)
+    assert min(norms) > 0.05
+
+
+def test_clipped_steps_o3_scaled_v_unaligned(bo):
+    wl = synth.o3_1p3b(n_layer=1, d=64, ffn=256, vocab=300, ctx=32)
+    states = fresh_states(wl.weights(), o3=True, scaled_v=True)
+    clipped_lockstep(bo, wl, states, 2, 0.01, misalign={0, 3})
+
+
+def test_clip_threshold_above_the_norm_equals_the_plain_step(bo):
+    wl = synth.tiny()
+    states = states_for(wl, 1)
+    a = GpuState([s.copy() for s in states])
+    b = GpuState([s.copy() for s in states])
+    assert a.plan(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, 1,
+                  max_grad_norm=1e9) == 0
+    assert b.plan(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, 1) == 0
+    for i in range(len(states)):
+        assert torch.equal(a.m[i], b.m[i]) and torch.equal(a.v[i], b.v[i])
+        assert torch.equal(a.w[i], b.w[i])
+    assert torch.equal(a.m_scale, b.m_scale)
+
+
+def test_clipped_step_with_found_inf_writes_nothing(bo):
+    wl = synth.tiny()
+    states = states_for(wl, 1)
+    states[0].g[10] = 0x7F
+    gpu = GpuState([s.copy() for s in states])
+    found = gpu.plan(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, 1,
+                     found_inf_dev=gpu.found_dev, max_grad_norm=0.1)
+    assert found == 1 and gpu.found_dev.item() == 1
+    assert gpu.plan.last_grad_norm == math.inf
+    for i, s in enumerate(states):
+        assert np.array_equal(to_np_u8(gpu.m[i]), s.m)
+        assert np.array_equal(to_np_u16(gpu.v[i]), s.v)
+        assert np.array_equal(to_np_u16(gpu.w[i]), s.w)
+
+
+def test_optimizer_with_clipping_against_the_oracle(bo):
+    """Fp8AdamW(max_grad_norm): the library's cast, then the clipped step; the
+    oracle follows from the same gradient values."""
+    wl = synth.tiny()
+    params = [w.cuda() for w in wl.weights()]
+    opt = bo.Fp8AdamW(params, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
+                      weight_decay=wl.wd, max_grad_norm=0.02)
+    assert not opt.fused
+    states = fresh_states(wl.weights(), o3=False)
+    for t in range(1, 4):
+        grads = wl.grads(t)
+        assert opt.step([g.cuda() for g in grads]) == 0
+        codes, _, scale = oracle_cast(grads, E4M3)
+        set_grads(states, codes, scale)
+        f, n = oracle.adam_step_clipped(states, wl.lr, wl.beta1, wl.beta2,
+                                        wl.eps, wl.wd, t, 1.0, 0.02)
+        assert f == 0 and opt.last_grad_norm == n
+        check_f32_exact(opt.m_scale.cpu().numpy()[:3], [s.m_scale[0] for s in states])
+        for i, s in enumerate(states):
+            assert np.array_equal(to_np_u16(params[i].view(-1)), s.w) or \
+                np.abs(to_np_u16(params[i].view(-1)).astype(int) - s.w.astype(int)).max() <= 1

@@ -12,7 +12,8 @@ import torch
 import oracle
 import synth
 from harness import DeviceList, host_src, oracle_step
-from parity import check_codes, check_f32_exact, to_np_u8
+from parity import (check_codes, check_f16, check_f32_exact, check_master,
+                    to_np_u16, to_np_u8)
 
 pytestmark = pytest.mark.gpu
 
@@ -140,3 +141,89 @@ def test_o2_6p7b_tail_full_scaled_v(bo):
     dl, _ = lockstep_full(wl, 3, sample, fused=True, scaled_v=True)
     dl.invariants()
     assert float(dl.v_bound.max().item()) > 0
+
+
+def test_reduce_gpt2_124m_8_shards_every_tensor(bo):
+    """The 124M list with 8 shards per tensor (1 GB of codes), every output
+    compared with the oracle.  Each shard is a rank's gradient put into E4M3
+    codes by torch's float8 type at scale 448 / max |g| (torch's amax)."""
+    wl = synth.fp8_reduce()
+    assert wl.n_params == 124_439_808 and wl.ranks == 8
+    k = wl.ranks
+    shards, scales = [], torch.empty((len(wl.shapes), k))
+    for i in range(len(wl.shapes)):
+        rows = torch.empty((k, wl.numels[i]), dtype=torch.uint8, device="cuda")
+        for r in range(k):
+            g = wl.rank_grad(i, 1, r, "cuda").float()
+            s = torch.tensor(448.0, device="cuda") / g.abs().max()
+            rows[r] = (g * s).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+            scales[i, r] = s.item()
+        shards.append(rows)
+    codes, amax, scale = bo.fp8_reduce_scaled(shards, scales.cuda(), "e4m3",
+                                              "e4m3", 1.0 / k)
+    torch.cuda.synchronize()
+    amax, scale = amax.cpu().numpy(), scale.cpu().numpy()
+    for i in range(len(wl.shapes)):
+        rc, ra, rs = oracle.reduce_scaled(to_np_u8(shards[i]).reshape(k, -1),
+                                          scales[i].numpy(), oracle.E4M3,
+                                          oracle.E4M3, 1.0 / k)
+        check_f32_exact(amax[i:i + 1], [ra], f"amax[{i}]")
+        check_f32_exact(scale[i:i + 1], [rs], f"scale[{i}]")
+        check_codes(to_np_u8(codes[i]), rc, oracle.E4M3, name=f"codes[{i}]")
+
+
+def test_grad_norm_and_clipped_step_o3_1p3b(bo):
+    """The 1.3B list (1.3 G gradient codes): the library's norm over every
+    tensor equals the oracle's bit for bit, and one clipped O3 step of the
+    whole list matches the oracle's step, at the oracle's coefficient, on a
+    sample of whole tensors.  Gradient codes are put into E4M3 by torch's
+    float8 type at scale 448 / max |g| (torch's amax)."""
+    wl = synth.o3_1p3b()
+    n = len(wl.shapes)
+    numels = wl.numels
+    g = bo.arena_views(numels, torch.uint8, "cuda")
+    g_scale = torch.empty(n, device="cuda")
+    for i in range(n):
+        x = wl.grad(i, 1, "cuda").float()
+        s = torch.tensor(448.0, device="cuda") / x.abs().max()
+        g[i].copy_((x * s).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8))
+        g_scale[i] = s
+    del x
+    w = bo.arena_views(numels, torch.float16, "cuda")
+    for i in range(n):
+        w[i].copy_(wl.weight(i, "cuda"))
+    m = bo.arena_views(numels, torch.uint8, "cuda", fill=0)
+    v = bo.arena_views(numels, torch.float16, "cuda", fill=0)
+    m_scale = torch.ones(n, device="cuda")
+    w8 = bo.arena_views(numels, torch.uint8, "cuda", fill=0)
+    w8_scale = torch.ones(n, device="cuda")
+    w8_amax = torch.zeros(n, device="cuda")
+    plan = bo.AdamWPlan(g, g_scale, m, m_scale, v, w, w8, w8_scale, w8_amax)
+    host_g = [to_np_u8(t) for t in g]
+    scales = g_scale.cpu().numpy()
+    found, norm = oracle.grad_norm_codes(host_g, scales, oracle.E4M3, 1.0)
+    assert found == 0
+    assert plan.grad_norm(1.0) == (0, norm)
+    max_norm = norm / 3.0
+    sample = sample_of(wl, 30_000_000)
+    states = []
+    for i in sample:
+        ne = numels[i]
+        states.append(oracle.StepState(host_g[i], scales[i], np.zeros(ne, np.uint8),
+                                       1.0, np.zeros(ne, np.uint16),
+                                       to_np_u16(w[i]), o3=True))
+    assert plan(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, 1, 1.0,
+                max_grad_norm=max_norm) == 0
+    assert plan.last_grad_norm == norm
+    coef = oracle.clip_coef(norm, max_norm)
+    assert coef < 1.0
+    assert oracle.adam_step_coef(states, wl.lr, wl.beta1, wl.beta2, wl.eps,
+                                 wl.wd, 1, 1.0, coef) == 0
+    ms, w8s = m_scale.cpu().numpy(), w8_scale.cpu().numpy()
+    for i, st in zip(sample, states):
+        check_f32_exact(ms[i:i + 1], st.m_scale, f"m_scale[{i}]")
+        check_f32_exact(w8s[i:i + 1], st.w8_scale, f"w8_scale[{i}]")
+        check_codes(to_np_u8(m[i]), st.m, name=f"m[{i}]")
+        check_f16(to_np_u16(v[i]), st.v, name=f"v[{i}]")
+        check_master(to_np_u16(w[i]), st.w, name=f"master[{i}]")
+        check_codes(to_np_u8(w8[i]), st.w8, name=f"w8[{i}]")
