@@ -10,8 +10,9 @@ FP16 second moment, FP16 weights, GradScaler inf/NaN check) in one call.  Defaul
 
 Prints one JSON line.  ``value`` is whole-job Gparams/s with inputs resident
 in HBM (CUDA events on the launching stream); ``e2e`` is the same metric when
-every step also copies its gradients from pinned host memory and reads
-found_inf back; ``roofline`` covers the dominant kernel (the fused AdamW
+every step also copies its gradients from pinned host memory (double-buffered:
+the next step's copy overlaps this step's kernels) and reads found_inf back;
+``roofline`` covers the dominant kernel (the fused AdamW
 update), timed live with the library's per-kernel events; ``cpu_baseline`` is
 the scalar C oracle on a bounded sample of the same workload.
 
@@ -66,7 +67,10 @@ def parse():
                    help="override the workload's vocabulary (profiling cases)")
     p.add_argument("--max-grad-norm", type=float, default=None,
                    help="clip the headline step to this global gradient norm "
-                        "(the unfused path with the norm pass; profiling case)")
+                        "(fp8_cast_adam_step_clipped; profiling case)")
+    p.add_argument("--unfused", action="store_true",
+                   help="run the headline as two calls (the cast, then the "
+                        "step; profiling case)")
     p.add_argument("--reduce-only", type=int, default=None, metavar="K",
                    help="time only the local FP8 reduction of K shards of the "
                         "124M list and print its line (profiling case)")
@@ -395,8 +399,9 @@ def other_configs(device, peak):
         # Adam with L2 decay runs as two calls and its first pass reads w:
         # cast 5 + first pass 4 + update 11
         ("o2_350m_adam_l2", synth.o2_350m, 20, {"l2": True}, 20),
-        # clipping to a global norm: cast 5 + norm 1 + first pass 2 + update 11
-        ("o2_350m_clip", synth.o2_350m, 20, {"max_grad_norm": 1.0}, 19),
+        # clipping to a global norm, one call: gradient amax 2, encode with
+        # the exact squares 3, first pass 2, update 11
+        ("o2_350m_clip", synth.o2_350m, 20, {"max_grad_norm": 1.0}, 18),
         ("tiny", synth.tiny, 200, {}, STEP_BYTES["O2"]),
     )
     for name, mk, reps, kw, bpp in runs:
@@ -445,7 +450,8 @@ def run_ours(args, wl):
 
     clip_kw = ({} if args.max_grad_norm is None
                else {"max_grad_norm": args.max_grad_norm})
-    params, grads, flat, opt = build_state(wl, device, **clip_kw)
+    params, grads, flat, opt = build_state(wl, device, fused=not args.unfused,
+                                           **clip_kw)
     stream = torch.cuda.current_stream()
     flag = torch.zeros(1, dtype=torch.int32, device=device)
     ils = wl.inv_loss_scale
@@ -480,9 +486,11 @@ def run_ours(args, wl):
 
     n_params = wl.n_params
     value = world * n_params / (ms * 1e-3) / 1e9
-    # with clipping: the unfused path (cast 5, norm 1, first pass 2, update 11)
-    bytes_step = (STEP_BYTES[wl.level] if not clip_kw
-                  else STEP_BYTES[wl.level] + 2) * n_params
+    # with clipping (fp8_cast_adam_step_clipped): amax 2, encode 3, first
+    # pass 2, update 11 (O3: + 3); as two calls the cast (5) and the step's
+    # first pass (2) are separate, plus 1 for a norm pass
+    extra = (1 if clip_kw else 0) if not args.unfused else (2 if clip_kw else 1)
+    bytes_step = (STEP_BYTES[wl.level] + extra) * n_params
     peak, peak_kind = measured_peak()
     upd_n, upd_ms = kern["step_update"]
     upd_avg_ms = upd_ms / max(upd_n, 1)
@@ -492,27 +500,63 @@ def run_ours(args, wl):
     e2e = None
     if not args.no_e2e:
         # Host buffers: every step copies its gradients from pinned host
-        # memory, runs the cast and the step, and reads found_inf back.
-        # The gradient arena is one flat buffer, so one copy moves a step's
-        # gradients (alignment padding included).
+        # memory (one copy of the flat arena, alignment padding included),
+        # runs the cast and the step through the public plans, and reads
+        # found_inf back to the host.  Two device gradient arenas alternate:
+        # step t+1's copy (on its own stream) overlaps step t's kernels, and
+        # waits only until the step that last read its arena has finished.
         host = torch.empty(flat.shape, dtype=flat.dtype, pin_memory=True)
         host.copy_(flat)
         h2d = host.numel() * host.element_size()
-        for _ in range(2):
-            flat.copy_(host, non_blocking=True)
-            opt.step(grads, ils, sync=True)
+        grads2, flat2 = bo.arena_views(wl.numels, wl.grad_dtype, device,
+                                       return_base=True)
+        bufs = [(grads, flat), (grads2, flat2)]
+        streams = [torch.cuda.Stream(device), torch.cuda.Stream(device)]
+        copy_stream = torch.cuda.Stream(device)
+        fused = [bo.CastStepPlan(bo.CastPlan(g, opt.g_codes, opt.g_amax,
+                                             opt.g_scale, opt.grad_fmt), opt._plan)
+                 for g, _ in bufs]
+        hp = (opt.lr, opt.beta1, opt.beta2, opt.eps, opt.wd)
+        clip = {"max_grad_norm": opt.max_grad_norm} if clip_kw else {}
+
+        def run(k):
+            """k steps; returns their milliseconds between CUDA events: the
+            first copy's start on the copy stream and the last step's end."""
+            copied = [torch.cuda.Event(), torch.cuda.Event()]
+            done = [torch.cuda.Event(), torch.cuda.Event()]
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(copy_stream):
+                e0.record(copy_stream)
+                bufs[0][1].copy_(host, non_blocking=True)
+                copied[0].record(copy_stream)
+            for t in range(k):
+                b, nb = t % 2, (t + 1) % 2
+                if t + 1 < k:                 # the next step's gradients
+                    with torch.cuda.stream(copy_stream):
+                        if t >= 1:
+                            copy_stream.wait_event(done[nb])
+                        bufs[nb][1].copy_(host, non_blocking=True)
+                        copied[nb].record(copy_stream)
+                s = streams[b]
+                s.wait_event(copied[b])
+                if t >= 1:
+                    s.wait_event(done[nb])    # the previous step (shared state)
+                opt.step_count += 1
+                found = fused[b](*hp, opt.step_count, ils, sync=True, stream=s,
+                                 l2=opt.l2, **clip)
+                done[b].record(s)
+                if found != 0:
+                    raise RuntimeError("found_inf set on a finite workload")
+            e1.record(streams[(k - 1) % 2])
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1)
+
+        run(2)
         barrier()
         k = max(1, args.e2e_steps)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(k):
-            flat.copy_(host, non_blocking=True)
-            if opt.step(grads, ils, sync=True) != 0:
-                raise RuntimeError("found_inf set on a finite workload")
-        e1.record(stream)
+        ems = run(k) / k
         barrier()
-        ems = e0.elapsed_time(e1) / k
         if world > 1:
             t = torch.tensor([ems], dtype=torch.float64, device=device)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -554,10 +598,13 @@ def run_ours(args, wl):
             "cpu_baseline": cpu,
             "other_configs": others,
         }
-        if clip_kw:
-            line["config"]["step"] = ("fp8_cast_scaled, then fp8_adam_step_clipped "
-                                      f"(global norm {args.max_grad_norm})")
-            line["config"]["bytes_per_param"] = STEP_BYTES[wl.level] + 2
+        if clip_kw or args.unfused:
+            line["config"]["step"] = (
+                ("fp8_cast_scaled, then " if args.unfused else "") +
+                ("fp8_adam_step_clipped" if args.unfused else
+                 "fp8_cast_adam_step_clipped" if clip_kw else "fp8_adamw_step") +
+                (f" (global norm {args.max_grad_norm})" if clip_kw else ""))
+            line["config"]["bytes_per_param"] = bytes_step // n_params
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

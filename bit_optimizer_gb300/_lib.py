@@ -22,6 +22,7 @@ EXPORTS = ("fp8_cast_scaled", "fp8_adamw_step", "fp8_adam_step",
            "fp8_cast_adamw_step", "fp8_reduce_scaled", "fp8_grad_norm",
            "fp8_adam_step_clipped", "fp8_grad_norm_terms", "fp8_clip_coef",
            "fp8_adam_step_begin", "fp8_adam_step_finish",
+           "fp8_cast_adam_step_clipped",
            "fp8_cast_scaled_noalloc", "fp8opt_strerror",
            "fp8opt_last_error", "fp8opt_timing_enable", "fp8opt_timing_read",
            "fp8opt_release")
@@ -119,6 +120,12 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     L.fp8_adam_step_finish.restype = C.c_int
     L.fp8_adam_step_finish.argtypes = step_head + [C.c_void_p, C.c_void_p,
                                                    C.c_void_p, C.c_void_p]
+    L.fp8_cast_adam_step_clipped.restype = C.c_int
+    L.fp8_cast_adam_step_clipped.argtypes = [
+        C.POINTER(CastItem), C.POINTER(Param), C.c_int, C.c_int, C.c_float,
+        C.c_float, C.c_float, C.c_float, C.c_float, C.c_int64, C.c_float, C.c_int,
+        C.c_float, C.POINTER(C.c_double), C.c_void_p, C.POINTER(C.c_int),
+        C.c_void_p, C.c_void_p]
     L.fp8_cast_scaled_noalloc.restype = C.c_int
     L.fp8_cast_scaled_noalloc.argtypes = [C.POINTER(CastItem), C.c_int, C.c_int,
                                           C.c_void_p]

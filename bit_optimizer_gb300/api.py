@@ -312,7 +312,7 @@ class AdamWPlan:
                 self._params, self.n, lr, beta1, beta2, eps, wd, int(step),
                 inv_loss_scale, 1 if l2 else 0, float(max_grad_norm), nptr, ndev,
                 fptr, fdev, _stream_ptr(stream)))
-            self.last_grad_norm = self._norm.value if sync else None
+            self.last_grad_norm = self._norm.value if nptr is not None else None
         return self._found.value if sync else None
 
     def grad_norm(self, inv_loss_scale=1.0, norm_dev=None, sync=True,
@@ -381,19 +381,39 @@ class CastStepPlan:
         self.cast = cast
         self.step_plan = step
         self._found = C.c_int(0)
+        self._norm = C.c_double(0.0)
+        self.last_grad_norm: Optional[float] = None
 
     def __call__(self, lr, beta1, beta2, eps, wd, step, inv_loss_scale=1.0,
                  found_inf_dev: Optional[torch.Tensor] = None, sync=True,
-                 stream=None) -> Optional[int]:
+                 stream=None, l2=False, max_grad_norm=None,
+                 grad_norm_dev: Optional[torch.Tensor] = None) -> Optional[int]:
+        """AdamW through fp8_cast_adamw_step; with l2 or max_grad_norm (0
+        reports the norm without clipping), Adam / AdamW with the gradient
+        norm through fp8_cast_adam_step_clipped, the norm then left in
+        ``last_grad_norm`` (sync=True) and grad_norm_dev, if given."""
         fdev = None
         if found_inf_dev is not None:
             _cuda(found_inf_dev, "found_inf_dev")
             fdev = found_inf_dev.data_ptr()
         fptr = C.byref(self._found) if sync else None
-        check(load().fp8_cast_adamw_step(
-            self.cast._items, self.step_plan._params, self.cast.n, self.cast.fmt,
-            lr, beta1, beta2, eps, wd, int(step), inv_loss_scale, fptr, fdev,
-            _stream_ptr(stream)))
+        if not l2 and max_grad_norm is None:
+            check(load().fp8_cast_adamw_step(
+                self.cast._items, self.step_plan._params, self.cast.n,
+                self.cast.fmt, lr, beta1, beta2, eps, wd, int(step),
+                inv_loss_scale, fptr, fdev, _stream_ptr(stream)))
+        else:
+            ndev = (None if grad_norm_dev is None
+                    else _slot_ptr(grad_norm_dev, 0, "grad_norm_dev"))
+            nptr = (C.byref(self._norm)
+                    if sync and max_grad_norm is not None else None)
+            check(load().fp8_cast_adam_step_clipped(
+                self.cast._items, self.step_plan._params, self.cast.n,
+                self.cast.fmt, lr, beta1, beta2, eps, wd, int(step),
+                inv_loss_scale, 1 if l2 else 0,
+                0.0 if max_grad_norm is None else float(max_grad_norm), nptr,
+                ndev, fptr, fdev, _stream_ptr(stream)))
+            self.last_grad_norm = self._norm.value if nptr is not None else None
         return self._found.value if sync else None
 
 
@@ -407,11 +427,11 @@ class Fp8AdamW:
     step ``w8`` / ``w8_scale`` hold their E4M3 copies for forward/backward.
     ``scaled_v``: the FP16 second moment is kept relative to a per-tensor
     bound (``v_bound``), so small gradients do not underflow it.  ``l2``:
-    Adam with L2 weight decay (torch.optim.Adam) instead of AdamW; it runs as
-    two calls (the fused call is AdamW only).  ``max_grad_norm``: clip the
-    unscaled gradient to this global L2 norm (torch's clip_grad_norm_; 0
-    only measures it); also two calls, and ``last_grad_norm`` holds the norm
-    after a synchronous step.
+    Adam with L2 weight decay (torch.optim.Adam) instead of AdamW.
+    ``max_grad_norm``: clip the unscaled gradient to this global L2 norm
+    (torch's clip_grad_norm_; 0 only measures it); ``last_grad_norm`` holds
+    the norm after a synchronous step.  With ``fused`` (the default) a step
+    is one library call; otherwise the cast and the step are two.
 
     ``step(grads, inv_loss_scale)`` casts the gradients to FP8 (per-tensor
     just-in-time scale) and runs the update; it returns found_inf and, like a
@@ -435,8 +455,9 @@ class Fp8AdamW:
         self.level, self.grad_fmt = level, grad_fmt
         self.l2 = l2
         self.max_grad_norm = max_grad_norm
-        # one fp8_cast_adamw_step call per step (AdamW without clipping)
-        self.fused = fused and not l2 and max_grad_norm is None
+        # one call per step: fp8_cast_adamw_step, or fp8_cast_adam_step_clipped
+        # with l2 or clipping
+        self.fused = fused
         self.last_grad_norm: Optional[float] = None
         self.step_count = 0
         n = len(self.params)
@@ -486,7 +507,9 @@ class Fp8AdamW:
         if self.fused:
             found = self._cast_step(self.lr, self.beta1, self.beta2, self.eps,
                                     self.wd, t, inv_loss_scale, found_inf_dev,
-                                    sync, stream)
+                                    sync, stream, l2=self.l2,
+                                    max_grad_norm=self.max_grad_norm)
+            self.last_grad_norm = self._cast_step.last_grad_norm
         else:
             cast(stream)
             found = self._plan(self.lr, self.beta1, self.beta2, self.eps, self.wd,

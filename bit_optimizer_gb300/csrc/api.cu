@@ -28,6 +28,21 @@ cudaError_t launch_step(const StepDesc* descs, const Chunk* chunks,
                         int grid_w8, bool any_vs, cudaStream_t stream,
                         LaunchMark mark);
 cudaError_t step_occupancy(int* amax_per_sm, int* update_per_sm, int* w8_per_sm);
+cudaError_t launch_cast_amax(const CastDesc* descs, const Chunk* chunks,
+                             uint32_t nchunks, unsigned long long* slots,
+                             uint32_t epoch, int grid_amax, cudaStream_t stream,
+                             LaunchMark mark);
+cudaError_t launch_cast_encode_sq(const CastDesc* descs, const Chunk* chunks,
+                                  uint32_t nchunks, const unsigned long long* slots,
+                                  uint32_t epoch, int fmt, int grid_encode,
+                                  unsigned long long* sums,
+                                  unsigned long long* found, float ils,
+                                  cudaStream_t stream, LaunchMark mark);
+cudaError_t cast_encode_sq_occupancy(int* per_sm);
+cudaError_t launch_cast_encode(const CastDesc* descs, const Chunk* chunks,
+                               uint32_t nchunks, const unsigned long long* slots,
+                               uint32_t epoch, int fmt, int grid_encode,
+                               cudaStream_t stream, LaunchMark mark);
 cudaError_t launch_cast_step(const CastDesc* cdescs, const StepDesc* sdescs,
                              const Chunk* chunks, uint32_t nchunks,
                              const Chunk* chunks_o3, uint32_t nchunks_o3,
@@ -117,6 +132,7 @@ struct DeviceInfo {
   int cast_step = 0;
   int reduce_amax = 0, reduce_encode = 0;
   int grad_norm = 0;
+  int cast_encode_sq = 0;
 };
 
 // Per-(device, stream) state.  The slot region holds only epoch-tagged
@@ -192,6 +208,8 @@ cudaError_t device_info(int dev, DeviceInfo** out) {
   info.reduce_encode = info.sms * (b > 0 ? b : 1);
   if ((e = grad_norm_occupancy(&a)) != cudaSuccess) return e;
   info.grad_norm = info.sms * (a > 0 ? a : 1);
+  if ((e = cast_encode_sq_occupancy(&a)) != cudaSuccess) return e;
+  info.cast_encode_sq = info.sms * (a > 0 ? a : 1);
   *out = &(g_dev[dev] = info);
   return cudaSuccess;
 }
@@ -548,6 +566,20 @@ int ensure_reduce_tables(const char* fn, Workspace* ws,
   ws->reduce_key.assign(items, items + n);
   ws->reduce_nchunks = (uint32_t)chunks.size();
   ws->have_reduce = true;
+  return FP8OPT_OK;
+}
+
+// A fused cast + step call: params[i] must take grads[i]'s output.
+int check_takes_cast(const char* fn, const fp8opt_cast_item* grads,
+                     const fp8opt_param* params, int n, int fmt) {
+  for (int i = 0; i < n; ++i) {
+    const fp8opt_param& p = params[i];
+    if (p.g != grads[i].codes || p.g_scale != grads[i].scale ||
+        p.numel != grads[i].numel || p.g_fmt != fmt)
+      return fail(FP8OPT_ERR_ARG, std::string(fn) + ": param " + std::to_string(i) +
+                                      " does not take item " + std::to_string(i) +
+                                      "'s codes, scale, numel and format");
+  }
   return FP8OPT_OK;
 }
 
@@ -950,15 +982,8 @@ extern "C" int fp8_cast_adamw_step(const fp8opt_cast_item* grads,
   const char* fn = "fp8_cast_adamw_step";
   int st = check_cast_args(fn, grads, n, fmt);
   if (st == FP8OPT_OK) st = check_step_args(fn, params, n, step);
+  if (st == FP8OPT_OK) st = check_takes_cast(fn, grads, params, n, fmt);
   if (st != FP8OPT_OK) return st;
-  for (int i = 0; i < n; ++i) {
-    const fp8opt_param& p = params[i];
-    if (p.g != grads[i].codes || p.g_scale != grads[i].scale ||
-        p.numel != grads[i].numel || p.g_fmt != fmt)
-      return fail(FP8OPT_ERR_ARG, std::string(fn) + ": param " + std::to_string(i) +
-                                      " does not take item " + std::to_string(i) +
-                                      "'s codes, scale, numel and format");
-  }
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   if (n == 0) return empty_step(fn, found_inf, found_inf_dev, stream);
   const StepScalars s =
@@ -996,6 +1021,99 @@ extern "C" int fp8_cast_adamw_step(const fp8opt_cast_item* grads,
                        launch_mark());
   if (e != cudaSuccess) return cuda_fail(e, "fp8_cast_adamw_step: launch");
   if (found_inf != nullptr) return read_found(fn, sc.found, epoch, stream, found_inf);
+  return FP8OPT_OK;
+}
+
+extern "C" int fp8_cast_adam_step_clipped(
+    const fp8opt_cast_item* grads, const fp8opt_param* params, int n, int fmt,
+    float lr, float beta1, float beta2, float eps, float wd, int64_t step,
+    float inv_loss_scale, int l2, float max_grad_norm, double* grad_norm,
+    float* grad_norm_dev, int* found_inf, uint32_t* found_inf_dev,
+    void* stream_ptr) {
+  const char* fn = "fp8_cast_adam_step_clipped";
+  if (l2 != 0 && l2 != 1) return fail(FP8OPT_ERR_ARG, std::string(fn) + ": l2 must be 0 or 1");
+  if (std::isnan(max_grad_norm))
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": max_grad_norm is NaN");
+  int st = check_cast_args(fn, grads, n, fmt);
+  if (st == FP8OPT_OK) st = check_step_args(fn, params, n, step);
+  if (st == FP8OPT_OK) st = check_takes_cast(fn, grads, params, n, fmt);
+  if (st != FP8OPT_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (n == 0) {
+    if (grad_norm != nullptr) *grad_norm = 0.0;
+    if (grad_norm_dev != nullptr) {
+      cudaError_t e = cudaMemsetAsync(grad_norm_dev, 0, sizeof(float), stream);
+      if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": norm_dev").c_str());
+    }
+    return empty_step(fn, found_inf, found_inf_dev, stream);
+  }
+  StepScalars s = make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale,
+                               l2 != 0);
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  DeviceInfo* info = nullptr;
+  if ((st = current_device_and_info(&dev, &info)) != FP8OPT_OK) return st;
+  Workspace* ws = workspace(dev, stream);
+  if ((st = ensure_cast_tables(fn, ws, grads, n, stream)) != FP8OPT_OK) return st;
+  if ((st = ensure_step_tables(fn, ws, params, n, stream)) != FP8OPT_OK) return st;
+
+  // slots: [0, n) gradient amax, then the step's [n, 4n + 1) (amax of m, of
+  // the master, max |g|, found_inf); norm: sums, terms, norm, clip
+  uint32_t epoch = 0;
+  cudaError_t e = prepare_slots(ws, 4 * (size_t)n + 1, stream, &epoch);
+  if (e == cudaSuccess) e = ws->saved_scales.reserve(2 * (size_t)n * sizeof(float));
+  const size_t sum_bytes = 2 * (size_t)n * sizeof(unsigned long long);
+  if (e == cudaSuccess)
+    e = ws->norm_buf.reserve(sum_bytes + (size_t)n * sizeof(double) + 16);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws->norm_buf.ptr, 0, sum_bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": workspace").c_str());
+  unsigned long long* slots = static_cast<unsigned long long*>(ws->slots.ptr);
+  StepScratch sc;
+  sc.amax_m = slots + n;
+  sc.amax_w = slots + 2 * (size_t)n;
+  sc.amax_g = slots + 3 * (size_t)n;
+  sc.found = slots + 4 * (size_t)n;
+  sc.old_m_scale = static_cast<float*>(ws->saved_scales.ptr);
+  sc.old_v_bound = sc.old_m_scale + n;
+  char* nb = static_cast<char*>(ws->norm_buf.ptr);
+  unsigned long long* sums = reinterpret_cast<unsigned long long*>(nb);
+  double* terms = reinterpret_cast<double*>(nb + sum_bytes);
+  double* norm = terms + n;
+  float* clip = reinterpret_cast<float*>(norm + 1);
+  const CastDesc* cdescs = static_cast<const CastDesc*>(ws->cast_descs.ptr);
+  const StepDesc* sdescs = static_cast<const StepDesc*>(ws->step_descs.ptr);
+  const Chunk* cchunks = static_cast<const Chunk*>(ws->cast_chunks.ptr);
+  const Chunk* schunks = static_cast<const Chunk*>(ws->step_chunks.ptr);
+  LaunchMark mark = launch_mark();
+  // the norm only when it clips or is asked for (Adam with L2 decay alone
+  // takes the plain encode pass)
+  const bool want_norm = max_grad_norm > 0.0f || grad_norm != nullptr ||
+                         grad_norm_dev != nullptr;
+  e = launch_cast_amax(cdescs, cchunks, ws->cast_nchunks, slots, epoch,
+                       info->cast_amax, stream, mark);
+  if (e == cudaSuccess && want_norm)
+    e = launch_cast_encode_sq(cdescs, cchunks, ws->cast_nchunks, slots, epoch, fmt,
+                              info->cast_encode_sq, sums, sc.found,
+                              inv_loss_scale, stream, mark);
+  if (e == cudaSuccess && !want_norm)
+    e = launch_cast_encode(cdescs, cchunks, ws->cast_nchunks, slots, epoch, fmt,
+                           info->cast_encode, stream, mark);
+  if (e == cudaSuccess && want_norm)
+    e = launch_grad_norm_terms(sdescs, schunks, 0, n, inv_loss_scale, sums,
+                               sc.found, epoch, terms, nullptr, 0, stream, mark);
+  if (e == cudaSuccess && want_norm)
+    e = launch_clip_coef(terms, n, sc.found, epoch, nullptr, max_grad_norm, norm,
+                         clip, grad_norm_dev, stream, mark);
+  if (max_grad_norm > 0.0f) s.clip = clip;
+  if (e == cudaSuccess)
+    e = launch_step(sdescs, schunks, ws->step_nchunks, schunks + ws->step_nchunks,
+                    ws->step_nchunks_o3, sc, s, epoch, found_inf_dev,
+                    info->step_amax, info->step_update, info->step_w8,
+                    ws->step_any_vs, stream, mark);
+  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
+  if (found_inf != nullptr || grad_norm != nullptr)
+    return read_results(fn, sc.found, epoch, norm, stream, found_inf, grad_norm);
   return FP8OPT_OK;
 }
 

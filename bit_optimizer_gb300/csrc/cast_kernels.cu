@@ -127,12 +127,23 @@ cast_amax_kernel(const CastDesc* __restrict__ descs,
 
 // -------------------------------------------------------------- encode pass
 
+// Where an encode pass also sums the exact squares of the codes it writes
+// (the gradient norm of a clipped step): the tensors' 128-bit slots, the
+// found_inf slot, and the step's inverse loss scale.
+struct SqOut {
+  unsigned long long* sums;
+  unsigned long long* found;
+  float ils;
+};
+
 // Encode this thread's share of [begin, end).  CHECKED when the tensor holds a
 // non-finite element (its amax is not finite): those take the explicit
-// NaN / infinity codes; otherwise every product is finite.
-template <int DT, int FMT, bool CHECKED>
+// NaN / infinity codes; otherwise every product is finite.  SQ: also add the
+// codes written to acc.
+template <int DT, int FMT, bool CHECKED, bool SQ>
 __device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
-                              int64_t end, bool vec, float scale) {
+                              int64_t end, bool vec, float scale,
+                              SqAcc<FMT>& acc) {
   constexpr int64_t kTile = (int64_t)kThreads * kGroup * kEncGroups;
   constexpr uint32_t kSrcBytes = DT == kF32 ? 4 : 2;
   const int tid = threadIdx.x;
@@ -154,7 +165,12 @@ __device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
 #pragma unroll
         for (int j = 0; j < 8; ++j) x[k][j] = __fmul_rn(x[k][j], scale);
         const int64_t i0 = base + k * (kThreads * kGroup) + tid * kGroup;
-        *reinterpret_cast<uint2*>(codes + i0) = enc8<FMT, CHECKED>(x[k]);
+        const uint2 c = enc8<FMT, CHECKED>(x[k]);
+        *reinterpret_cast<uint2*>(codes + i0) = c;
+        if (SQ) {
+          acc.add_word(c.x);
+          acc.add_word(c.y);
+        }
       }
     } else {
 #pragma unroll 1
@@ -165,14 +181,21 @@ __device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
           load8<DT>(src, i0, x);
 #pragma unroll
           for (int j = 0; j < 8; ++j) x[j] = __fmul_rn(x[j], scale);
-          *reinterpret_cast<uint2*>(codes + i0) = enc8<FMT, CHECKED>(x);
+          const uint2 c = enc8<FMT, CHECKED>(x);
+          *reinterpret_cast<uint2*>(codes + i0) = c;
+          if (SQ) {
+            acc.add_word(c.x);
+            acc.add_word(c.y);
+          }
         } else {
           for (int j = 0; j < kGroup; ++j) {
             const int64_t i = i0 + j;
             if (i >= end) break;
             const float t = __fmul_rn(load1<DT>(src, i), scale);
-            codes[i] = (uint8_t)(CHECKED ? enc1_checked<FMT>(t)
-                                         : (enc2<FMT>(t, 0.0f) & 0xFFu));
+            const uint32_t c = CHECKED ? enc1_checked<FMT>(t)
+                                       : (enc2<FMT>(t, 0.0f) & 0xFFu);
+            codes[i] = (uint8_t)c;
+            if (SQ) acc.add_word(c);
           }
         }
       }
@@ -180,23 +203,27 @@ __device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
   }
 }
 
-template <int DT, int FMT>
+template <int DT, int FMT, bool SQ>
 __device__ __forceinline__ void encode_dispatch(const CastDesc& d,
                                                 int64_t begin, int64_t end,
-                                                float scale, bool checked) {
+                                                float scale, bool checked,
+                                                SqAcc<FMT>& acc) {
   const bool vec = d.vec_ok != 0;
   if (checked)
-    thread_encode<DT, FMT, true>(d.src, d.codes, begin, end, vec, scale);
+    thread_encode<DT, FMT, true, SQ>(d.src, d.codes, begin, end, vec, scale, acc);
   else
-    thread_encode<DT, FMT, false>(d.src, d.codes, begin, end, vec, scale);
+    thread_encode<DT, FMT, false, SQ>(d.src, d.codes, begin, end, vec, scale, acc);
 }
 
-template <int FMT>
-__global__ void __launch_bounds__(kThreads)
-cast_encode_kernel(const CastDesc* __restrict__ descs,
-                   const Chunk* __restrict__ chunks, uint32_t nchunks,
-                   const unsigned long long* __restrict__ slots,
-                   uint32_t epoch) {
+// One chunk-strided encode pass (SQ: with the exact squares of the codes).
+template <int FMT, bool SQ>
+__device__ __forceinline__ void encode_pass(const CastDesc* __restrict__ descs,
+                                            const Chunk* __restrict__ chunks,
+                                            uint32_t nchunks,
+                                            const unsigned long long* __restrict__ slots,
+                                            uint32_t epoch, const SqOut& sq,
+                                            unsigned long long* red64,
+                                            uint32_t* red32) {
   for (uint32_t r = blockIdx.x; r < nchunks; r += gridDim.x) {
     const Chunk ch = chunks[nchunks - 1 - r];
     const CastDesc d = descs[ch.tensor];
@@ -209,13 +236,41 @@ cast_encode_kernel(const CastDesc* __restrict__ descs,
     const int64_t begin = (int64_t)ch.index * kChunkElems;
     const int64_t end = min(begin + kChunkElems, d.numel);
     const bool checked = ab >= 0x7F800000u;
+    SqAcc<FMT> acc;
     if (d.dtype == kF32)
-      encode_dispatch<kF32, FMT>(d, begin, end, scale, checked);
+      encode_dispatch<kF32, FMT, SQ>(d, begin, end, scale, checked, acc);
     else if (d.dtype == kBF16)
-      encode_dispatch<kBF16, FMT>(d, begin, end, scale, checked);
+      encode_dispatch<kBF16, FMT, SQ>(d, begin, end, scale, checked, acc);
     else
-      encode_dispatch<kF16, FMT>(d, begin, end, scale, checked);
+      encode_dispatch<kF16, FMT, SQ>(d, begin, end, scale, checked, acc);
+    if (SQ)
+      sq_commit<FMT>(acc, ch.tensor, end > begin, __fdiv_rn(sq.ils, scale),
+                     sq.sums, sq.found, epoch, red64, red32);
   }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+cast_encode_kernel(const CastDesc* __restrict__ descs,
+                   const Chunk* __restrict__ chunks, uint32_t nchunks,
+                   const unsigned long long* __restrict__ slots,
+                   uint32_t epoch) {
+  const SqOut none = {nullptr, nullptr, 0.0f};
+  encode_pass<FMT, false>(descs, chunks, nchunks, slots, epoch, none, nullptr,
+                          nullptr);
+}
+
+// The encode pass with the exact squares (its sums and the found_inf test
+// need more registers; four CTAs per SM keep it free of spills).
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 4)
+cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
+                      const Chunk* __restrict__ chunks, uint32_t nchunks,
+                      const unsigned long long* __restrict__ slots,
+                      uint32_t epoch, SqOut sq) {
+  __shared__ unsigned long long red64[2 * (kThreads / 32)];
+  __shared__ uint32_t red32[kThreads / 32];
+  encode_pass<FMT, true>(descs, chunks, nchunks, slots, epoch, sq, red64, red32);
 }
 
 }  // namespace
@@ -243,6 +298,47 @@ cudaError_t launch_cast(const CastDesc* descs, const Chunk* chunks,
   return cudaGetLastError();
 }
 
+// The encode pass alone (after launch_cast_amax).
+cudaError_t launch_cast_encode(const CastDesc* descs, const Chunk* chunks,
+                               uint32_t nchunks, const unsigned long long* slots,
+                               uint32_t epoch, int fmt, int grid_encode,
+                               cudaStream_t stream, LaunchMark mark) {
+  if (nchunks == 0) return cudaSuccess;
+  const uint32_t ge = grid_min((uint32_t)grid_encode, nchunks);
+  if (mark) mark(kCastEncodeK, 0, stream);
+  if (fmt == kE4M3)
+    cast_encode_kernel<kE4M3><<<ge, kThreads, 0, stream>>>(descs, chunks,
+                                                           nchunks, slots, epoch);
+  else
+    cast_encode_kernel<kE5M2><<<ge, kThreads, 0, stream>>>(descs, chunks,
+                                                           nchunks, slots, epoch);
+  if (mark) mark(kCastEncodeK, 1, stream);
+  return cudaGetLastError();
+}
+
+// The encode pass alone (after launch_cast_amax), also summing the exact
+// squares of the codes it writes into sums (2n zeroed words) and setting the
+// found_inf slot `found` as a step with factor inv_loss_scale / scale would.
+cudaError_t launch_cast_encode_sq(const CastDesc* descs, const Chunk* chunks,
+                                  uint32_t nchunks, const unsigned long long* slots,
+                                  uint32_t epoch, int fmt, int grid_encode,
+                                  unsigned long long* sums,
+                                  unsigned long long* found, float ils,
+                                  cudaStream_t stream, LaunchMark mark) {
+  if (nchunks == 0) return cudaSuccess;
+  const uint32_t ge = grid_min((uint32_t)grid_encode, nchunks);
+  const SqOut sq = {sums, found, ils};
+  if (mark) mark(kCastEncodeK, 0, stream);
+  if (fmt == kE4M3)
+    cast_encode_sq_kernel<kE4M3><<<ge, kThreads, 0, stream>>>(
+        descs, chunks, nchunks, slots, epoch, sq);
+  else
+    cast_encode_sq_kernel<kE5M2><<<ge, kThreads, 0, stream>>>(
+        descs, chunks, nchunks, slots, epoch, sq);
+  if (mark) mark(kCastEncodeK, 1, stream);
+  return cudaGetLastError();
+}
+
 // The amax pass alone (the fused cast + step path runs its own encode pass).
 cudaError_t launch_cast_amax(const CastDesc* descs, const Chunk* chunks,
                              uint32_t nchunks, unsigned long long* slots,
@@ -263,6 +359,11 @@ cudaError_t cast_occupancy(int* amax_per_sm, int* encode_per_sm) {
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       encode_per_sm, cast_encode_kernel<kE4M3>, kThreads, 0);
+}
+
+cudaError_t cast_encode_sq_occupancy(int* per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      per_sm, cast_encode_sq_kernel<kE4M3>, kThreads, 0);
 }
 
 }  // namespace fp8opt

@@ -382,4 +382,145 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* smem) {
   return v;
 }
 
+// ------------------------------------- exact sums of squared FP8 code values
+//
+// Every E4M3 or E5M2 code's value is a multiple of 2^-16, so its square is an
+// integer count of 2^-32 and a tensor's sum of squares can be taken exactly:
+//   E4M3: r = |value| * 2^9 is an integer below 2^18 (taken exactly from the
+//         decoded float with one fused multiply-add against 2^23), r^2 below
+//         2^36 in units of 2^-18, summed in 64 bits per thread;
+//   E5M2: r = |value| * 2^16 below 2^32 from the code's fields, r^2 below
+//         2^64 in units of 2^-32, summed in 128 bits per thread.
+// Integer sums are exact and order-free, so a norm built on them does not
+// depend on the kernel schedule.  A thread's share of one chunk (at most
+// kChunkElems / kThreads codes) keeps the E4M3 sum below 2^43.
+
+struct U128 {
+  unsigned long long lo, hi;
+};
+
+__device__ __forceinline__ U128 add128(U128 a, U128 b) {
+  U128 r;
+  r.lo = a.lo + b.lo;
+  r.hi = a.hi + b.hi + (r.lo < a.lo ? 1ull : 0ull);
+  return r;
+}
+
+__device__ __forceinline__ U128 add64(U128 a, unsigned long long b) {
+  U128 r;
+  r.lo = a.lo + b;
+  r.hi = a.hi + (r.lo < a.lo ? 1ull : 0ull);
+  return r;
+}
+
+// Sum over the CTA; the result is valid in thread 0.  Every thread calls it.
+// smem: 2 * kThreads / 32 words.
+__device__ __forceinline__ U128 block_sum128(U128 v, unsigned long long* smem) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    U128 w;
+    w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
+    w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
+    v = add128(v, w);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) {
+    smem[2 * warp] = v.lo;
+    smem[2 * warp + 1] = v.hi;
+  }
+  __syncthreads();
+  U128 s = {0ull, 0ull};
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kThreads / 32; ++i) s = add128(s, U128{smem[2 * i], smem[2 * i + 1]});
+  return s;
+}
+
+// acc += r^2 over the four E4M3 codes of a word (sign bits cleared): the
+// decoded values are exact floats below 2^9, and v * 512 + 2^23 is an exact
+// float whose low 23 bits are the integer r.
+__device__ __forceinline__ void sq_e4m3(uint32_t w, unsigned long long& acc) {
+  const float2 a = dec2<kE4M3>(w & 0xFFFFu), b = dec2<kE4M3>(w >> 16);
+  const float2 ta = fma2(a, splat2(512.0f), splat2(8388608.0f));
+  const float2 tb = fma2(b, splat2(512.0f), splat2(8388608.0f));
+  const uint32_t r0 = __float_as_uint(ta.x) & 0x7FFFFFu;
+  const uint32_t r1 = __float_as_uint(ta.y) & 0x7FFFFFu;
+  const uint32_t r2 = __float_as_uint(tb.x) & 0x7FFFFFu;
+  const uint32_t r3 = __float_as_uint(tb.y) & 0x7FFFFFu;
+  acc += (unsigned long long)r0 * r0;
+  acc += (unsigned long long)r1 * r1;
+  acc += (unsigned long long)r2 * r2;
+  acc += (unsigned long long)r3 * r3;
+}
+
+// acc += r^2 over the four E5M2 codes of a word (sign bits cleared), with
+// r = (4 + m) << (e - 1) for exponent field e >= 1 and r = m for e = 0
+// (non-finite codes count 0; they set found_inf instead).
+__device__ __forceinline__ U128 sq_e5m2(uint32_t w, U128 acc) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t mag = (w >> (8 * j)) & 0x7Fu;
+    const uint32_t e = mag >> 2, m = mag & 3u;
+    const uint32_t r = e == 0 ? m : (e == 31 ? 0u : ((4u | m) << (e - 1)));
+    acc = add64(acc, (unsigned long long)r * r);
+  }
+  return acc;
+}
+
+// A thread's exact sum of squared code values (format FMT) and the largest
+// code magnitude it saw.  A non-finite code has the largest magnitudes of its
+// format (E4M3 0x7F, E5M2 0x7C and above), so the maximum also tells whether
+// one was seen.
+template <int FMT>
+struct SqAcc {
+  unsigned long long s4 = 0;   // E4M3: units of 2^-18
+  U128 s5 = {0ull, 0ull};      // E5M2: units of 2^-32
+  uint32_t vmax = 0;           // per-byte max of the magnitudes
+
+  __device__ __forceinline__ void add_word(uint32_t w) {
+    w &= 0x7F7F7F7Fu;
+    vmax = __vmaxu4(vmax, w);
+    if (FMT == kE4M3)
+      sq_e4m3(w, s4);
+    else
+      s5 = sq_e5m2(w, s5);
+  }
+  // the sum in units of 2^-32
+  __device__ __forceinline__ U128 sum() const {
+    if (FMT == kE4M3) return U128{s4 << 14, s4 >> 50};
+    return s5;
+  }
+  __device__ __forceinline__ uint32_t cmax() const {
+    return max(max(vmax & 0xFFu, (vmax >> 8) & 0xFFu),
+               max((vmax >> 16) & 0xFFu, vmax >> 24));
+  }
+};
+
+// End of a chunk of tensor t: the CTA's exact sum goes to the tensor's
+// 128-bit slot (sums[2t], sums[2t + 1]; the low word's carry to the high
+// word), and found_inf is set when a code is non-finite or the largest
+// |value| times k is not finite (the step's test on this chunk; the product
+// is monotone in |value|).  Every thread calls it.
+template <int FMT>
+__device__ __forceinline__ void sq_commit(const SqAcc<FMT>& a, uint32_t t,
+                                          bool nonempty, float k,
+                                          unsigned long long* sums,
+                                          unsigned long long* found,
+                                          uint32_t epoch,
+                                          unsigned long long* red64,
+                                          uint32_t* red32) {
+  const U128 s = block_sum128(a.sum(), red64);
+  const uint32_t cmax = block_max_u32(a.cmax(), red32);
+  if (threadIdx.x == 0 && nonempty) {
+    if (s.lo | s.hi) {
+      const unsigned long long old = atomicAdd(&sums[2 * t], s.lo);
+      const unsigned long long carry = old + s.lo < old ? 1ull : 0ull;
+      if (s.hi + carry) atomicAdd(&sums[2 * t + 1], s.hi + carry);
+    }
+    const bool bad = FMT == kE4M3 ? cmax == 0x7Fu : cmax >= 0x7Cu;
+    if (bad || nonfinite(__fmul_rn(dec2<FMT>(cmax).x, k)))
+      atomicMax(found, slot_tag(epoch, 1u));
+  }
+}
+
 }  // namespace fp8opt

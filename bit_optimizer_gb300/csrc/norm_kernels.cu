@@ -2,21 +2,10 @@
 // coefficient that follows from it (torch.nn.utils.clip_grad_norm_, the run
 // script's --clip-grad).
 //
-// grad_norm_kernel: a persistent grid over the step's chunk table.  Every
-// code's value is a multiple of 2^-16, so its square is an integer count of
-// 2^-32 and the sum of squares of a tensor can be taken exactly:
-//   E4M3: r = |value| * 2^9 is an integer below 2^18 (taken exactly from the
-//         decoded float with one fused multiply-add against 2^23), r^2 below
-//         2^36 in units of 2^-18, summed in 64 bits per thread;
-//   E5M2: r = |value| * 2^16 below 2^32 from the code's fields, r^2 below
-//         2^64 in units of 2^-32, summed in 128 bits per thread.
-// Each CTA reduces its chunk to one 128-bit sum (units of 2^-32) and adds it
-// to the tensor's slot with two 64-bit atomics (the low word's carry goes to
-// the high word).  Integer sums are exact and order-free, so the result does
-// not depend on the schedule.  The kernel also decides found_inf exactly as
-// the step's first pass does: a non-finite code, or the largest |value| of
-// the chunk times k not finite (the product is monotone in |value|), both
-// read from the largest code magnitude of the chunk.
+// grad_norm_kernel: a persistent grid over the step's chunk table; each
+// chunk's exact sum of squared code values (SqAcc, fp8opt_internal.cuh) goes
+// to its tensor's 128-bit slot, and found_inf is decided exactly as the
+// step's first pass does (sq_commit).
 //
 // grad_norm_terms_kernel: one thread per record, term_t = fl64(k_t^2 *
 // fl64(S_t) * 2^-32) (k_t^2 is exact in double).
@@ -35,90 +24,11 @@ namespace {
 constexpr int kNormGroups = 4;   // 8-code groups per thread per tile
 constexpr int64_t kNormTile = (int64_t)kThreads * kGroup * kNormGroups;
 
-struct U128 {
-  unsigned long long lo, hi;
-};
-
-__device__ __forceinline__ U128 add128(U128 a, U128 b) {
-  U128 r;
-  r.lo = a.lo + b.lo;
-  r.hi = a.hi + b.hi + (r.lo < a.lo ? 1ull : 0ull);
-  return r;
-}
-
-__device__ __forceinline__ U128 add64(U128 a, unsigned long long b) {
-  U128 r;
-  r.lo = a.lo + b;
-  r.hi = a.hi + (r.lo < a.lo ? 1ull : 0ull);
-  return r;
-}
-
-// Sum over the CTA; the result is valid in thread 0.  Every thread calls it.
-__device__ U128 block_sum128(U128 v, unsigned long long* smem) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    U128 w;
-    w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
-    w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
-    v = add128(v, w);
-  }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) {
-    smem[2 * warp] = v.lo;
-    smem[2 * warp + 1] = v.hi;
-  }
-  __syncthreads();
-  U128 s = {0ull, 0ull};
-  if (threadIdx.x == 0)
-    for (int i = 0; i < kThreads / 32; ++i) s = add128(s, U128{smem[2 * i], smem[2 * i + 1]});
-  return s;
-}
-
-// acc += r * r in one 32 x 32 -> 64-bit multiply-add.
-__device__ __forceinline__ void mad_sq(unsigned long long& acc, uint32_t r) {
-  asm("mad.wide.u32 %0, %1, %1, %0;" : "+l"(acc) : "r"(r));
-}
-
-// acc += r^2 over the four codes of a word (sign bits already cleared).
-// E4M3: the decoded values are exact floats below 2^9; v * 512 + 2^23 is an
-// exact float whose low 23 bits are the integer r.
-__device__ __forceinline__ void sq_e4m3(uint32_t w, unsigned long long& acc) {
-  const float2 a = dec2<kE4M3>(w & 0xFFFFu), b = dec2<kE4M3>(w >> 16);
-  const float2 ta = fma2(a, splat2(512.0f), splat2(8388608.0f));
-  const float2 tb = fma2(b, splat2(512.0f), splat2(8388608.0f));
-  mad_sq(acc, __float_as_uint(ta.x) & 0x7FFFFFu);
-  mad_sq(acc, __float_as_uint(ta.y) & 0x7FFFFFu);
-  mad_sq(acc, __float_as_uint(tb.x) & 0x7FFFFFu);
-  mad_sq(acc, __float_as_uint(tb.y) & 0x7FFFFFu);
-}
-
-// E5M2: r = |value| * 2^16 from the code's exponent e and mantissa m:
-// (4 + m) << (e - 1) for e >= 1, m for e = 0 (non-finite codes give 0; they
-// set found_inf instead).
-__device__ __forceinline__ U128 sq_e5m2(uint32_t w, U128 acc) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t mag = (w >> (8 * j)) & 0x7Fu;
-    const uint32_t e = mag >> 2, m = mag & 3u;
-    const uint32_t r = e == 0 ? m : (e == 31 ? 0u : ((4u | m) << (e - 1)));
-    acc = add64(acc, (unsigned long long)r * r);
-  }
-  return acc;
-}
-
-// This thread's share of [begin, end): the exact sum of squares in units of
-// 2^-32 and the largest code magnitude.  A non-finite code has the largest
-// magnitudes of its format (E4M3 0x7F, E5M2 0x7C and above), so the maximum
-// also tells whether one was seen; its square is not meaningful, but the
-// norm is then +inf anyway.
+// This thread's share of [begin, end) into acc.
 template <int GF>
 __device__ void thread_norm(const uint8_t* g, int64_t begin, int64_t end,
-                            bool vec, U128& sum, uint32_t& cmax) {
+                            bool vec, SqAcc<GF>& acc) {
   const int tid = threadIdx.x;
-  unsigned long long s4 = 0;   // E4M3: units of 2^-18
-  U128 s5 = {0ull, 0ull};      // E5M2: units of 2^-32
-  uint32_t vmax = 0;           // per-byte max of the code magnitudes
 #pragma unroll 1
   for (int64_t base = begin; base < end; base += kNormTile) {
     if (vec && base + kNormTile <= end) {
@@ -128,14 +38,8 @@ __device__ void thread_norm(const uint8_t* g, int64_t begin, int64_t end,
         c[q] = ld_once2(g + base + q * (kThreads * kGroup) + tid * kGroup);
 #pragma unroll
       for (int q = 0; q < kNormGroups; ++q) {
-        const uint32_t x = c[q].x & 0x7F7F7F7Fu, y = c[q].y & 0x7F7F7F7Fu;
-        vmax = __vmaxu4(vmax, __vmaxu4(x, y));
-        if (GF == kE4M3) {
-          sq_e4m3(x, s4);
-          sq_e4m3(y, s4);
-        } else {
-          s5 = sq_e5m2(y, sq_e5m2(x, s5));
-        }
+        acc.add_word(c[q].x);
+        acc.add_word(c[q].y);
       }
     } else {
 #pragma unroll 1
@@ -144,60 +48,43 @@ __device__ void thread_norm(const uint8_t* g, int64_t begin, int64_t end,
         for (int e = 0; e < kGroup; ++e) {
           const int64_t i = i0 + e;
           if (i >= end) break;
-          const uint32_t x = g[i] & 0x7Fu;
-          vmax = __vmaxu4(vmax, x);
-          if (GF == kE4M3)
-            sq_e4m3(x, s4);
-          else
-            s5 = sq_e5m2(x, s5);
+          acc.add_word(g[i]);
         }
       }
     }
   }
-  if (GF == kE4M3) {
-    sum.lo = s4 << 14;           // s4 < 2^43 here, so no bits are lost
-    sum.hi = s4 >> 50;
-  } else {
-    sum = s5;
-  }
-  cmax = max(max(vmax & 0xFFu, (vmax >> 8) & 0xFFu),
-             max((vmax >> 16) & 0xFFu, vmax >> 24));
 }
 
-__global__ void __launch_bounds__(kThreads, 4)
+template <int GF>
+__device__ __forceinline__ void norm_chunk(const StepDesc& d, const Chunk& ch,
+                                           int64_t begin, int64_t end, float ils,
+                                           unsigned long long* sums,
+                                           unsigned long long* found,
+                                           uint32_t epoch,
+                                           unsigned long long* red64,
+                                           uint32_t* red32) {
+  SqAcc<GF> acc;
+  thread_norm<GF>(d.g, begin, end, d.vec_ok != 0, acc);
+  const float k = __fdiv_rn(ils, *d.g_scale);
+  sq_commit<GF>(acc, ch.tensor, end > begin, k, sums, found, epoch, red64, red32);
+}
+
+__global__ void __launch_bounds__(kThreads, 5)
 grad_norm_kernel(const StepDesc* __restrict__ descs,
                  const Chunk* __restrict__ chunks, uint32_t nchunks, float ils,
                  unsigned long long* __restrict__ sums,
                  unsigned long long* __restrict__ found, uint32_t epoch) {
-  __shared__ unsigned long long red[2 * (kThreads / 32)];
-  __shared__ uint32_t redm[kThreads / 32];
+  __shared__ unsigned long long red64[2 * (kThreads / 32)];
+  __shared__ uint32_t red32[kThreads / 32];
   for (uint32_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
     const Chunk ch = chunks[c];
     const StepDesc d = descs[ch.tensor];
     const int64_t begin = (int64_t)ch.index * kChunkElems;
     const int64_t end = min(begin + kChunkElems, d.numel);
-    const bool vec = d.vec_ok != 0;
-    U128 s = {0ull, 0ull};
-    uint32_t cmax = 0;
     if (d.g_fmt == kE4M3)
-      thread_norm<kE4M3>(d.g, begin, end, vec, s, cmax);
+      norm_chunk<kE4M3>(d, ch, begin, end, ils, sums, found, epoch, red64, red32);
     else
-      thread_norm<kE5M2>(d.g, begin, end, vec, s, cmax);
-    s = block_sum128(s, red);
-    cmax = block_max_u32(cmax, redm);
-    if (threadIdx.x == 0 && end > begin) {
-      const bool any_bad = d.g_fmt == kE4M3 ? cmax == 0x7Fu : cmax >= 0x7Cu;
-      if (s.lo | s.hi) {
-        const unsigned long long old = atomicAdd(&sums[2 * ch.tensor], s.lo);
-        const unsigned long long carry = old + s.lo < old ? 1ull : 0ull;
-        if (s.hi + carry) atomicAdd(&sums[2 * ch.tensor + 1], s.hi + carry);
-      }
-      // the step's test: decode(code) * k not finite for some code
-      const float k = __fdiv_rn(ils, *d.g_scale);
-      const float vmax = d.g_fmt == kE4M3 ? dec2<kE4M3>(cmax).x : dec2<kE5M2>(cmax).x;
-      if (any_bad || nonfinite(__fmul_rn(vmax, k)))
-        atomicMax(found, slot_tag(epoch, 1u));
-    }
+      norm_chunk<kE5M2>(d, ch, begin, end, ils, sums, found, epoch, red64, red32);
   }
 }
 

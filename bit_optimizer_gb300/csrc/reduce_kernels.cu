@@ -27,15 +27,38 @@ namespace fp8opt {
 
 namespace {
 
-constexpr int kRGroup = 16;    // codes per vector group (one 16-byte access)
-constexpr int kRGroups = 2;    // groups per thread per tile
-constexpr int kShardBatch = 2; // shards whose loads are issued before their sums
-constexpr int64_t kRTile = (int64_t)kThreads * kRGroup * kRGroups;  // 8192
-
-// Resident CTAs per SM both kernels are compiled for (caps their registers).
+// Tunables: 16-code groups per thread per tile, shards whose loads are issued
+// before their sums, resident CTAs per SM both kernels are compiled for (caps
+// their registers), and tiles ahead of the current one that one thread per
+// CTA prefetches into L2 (0: none).
+#ifndef FP8OPT_REDUCE_GROUPS
+#define FP8OPT_REDUCE_GROUPS 2
+#endif
+#ifndef FP8OPT_REDUCE_BATCH
+#define FP8OPT_REDUCE_BATCH 2
+#endif
 #ifndef FP8OPT_REDUCE_MIN_BLOCKS
 #define FP8OPT_REDUCE_MIN_BLOCKS 3
 #endif
+#ifndef FP8OPT_REDUCE_PREFETCH
+#define FP8OPT_REDUCE_PREFETCH 1
+#endif
+
+constexpr int kRGroup = 16;    // codes per vector group (one 16-byte access)
+constexpr int kRGroups = FP8OPT_REDUCE_GROUPS;
+constexpr int kShardBatch = FP8OPT_REDUCE_BATCH;
+constexpr int64_t kRTile = (int64_t)kThreads * kRGroup * kRGroups;
+
+// L2 prefetch of the tile FP8OPT_REDUCE_PREFETCH tiles after `base`, every
+// shard (thread 0 only; vector path, so the rows are 16-byte aligned).
+__device__ __forceinline__ void prefetch_tiles(const uint8_t* src, int64_t stride,
+                                               int k, int64_t base, int64_t end) {
+  if (FP8OPT_REDUCE_PREFETCH == 0 || threadIdx.x != 0) return;
+  const int64_t ahead = base + FP8OPT_REDUCE_PREFETCH * kRTile;
+  if (ahead + kRTile > end) return;
+  for (int j = 0; j < k; ++j)
+    prefetch_l2(src + (int64_t)j * stride + ahead, (uint32_t)kRTile);
+}
 
 // acc (+)= decode(16 codes) * r.  The product and the sum are the scalar
 // round-to-nearest intrinsics, which are never merged into a fused
@@ -133,6 +156,7 @@ __device__ uint32_t thread_reduce_amax(const ReduceDesc& d, int k,
 #pragma unroll 1
   for (int64_t base = begin; base < end; base += kRTile) {
     if (vec && base + kRTile <= end) {
+      prefetch_tiles(d.src, d.stride, k, base, end);
       int64_t i0[kRGroups];
 #pragma unroll
       for (int g = 0; g < kRGroups; ++g)
@@ -204,6 +228,7 @@ __device__ void thread_reduce_encode(const ReduceDesc& d, int k,
 #pragma unroll 1
   for (int64_t base = begin; base < end; base += kRTile) {
     if (vec && base + kRTile <= end) {
+      prefetch_tiles(d.src, d.stride, k, base, end);
       int64_t i0[kRGroups];
 #pragma unroll
       for (int g = 0; g < kRGroups; ++g)

@@ -180,6 +180,23 @@ def test_norm_and_clip_argument_errors_need_no_gpu(lib):
                                    C.byref(found), None, None) == lib.OK
 
 
+def test_fused_clip_argument_errors_need_no_gpu(lib):
+    L = lib.load()
+    item = (lib.CastItem * 1)()
+    p = (lib.Param * 1)()
+    args = (1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+    tail = (None, None, None, None, None)
+    assert L.fp8_cast_adam_step_clipped(item, p, 0, 0, *args, 2, 1.0, *tail) == lib.ERR_ARG
+    assert L.fp8_cast_adam_step_clipped(item, p, 0, 0, *args, 0, float("nan"),
+                                        *tail) == lib.ERR_ARG
+    assert L.fp8_cast_adam_step_clipped(item, p, 0, 7, *args, 0, 1.0, *tail) == \
+        lib.ERR_UNSUPPORTED
+    norm, found = C.c_double(-1.0), C.c_int(7)
+    assert L.fp8_cast_adam_step_clipped(item, p, 0, 0, *args, 1, 1.0, C.byref(norm),
+                                        None, C.byref(found), None, None) == lib.OK
+    assert norm.value == 0.0 and found.value == 0
+
+
 def test_strerror_texts(lib):
     assert lib.strerror(0) == "success"
     assert lib.strerror(-1) == "invalid argument"

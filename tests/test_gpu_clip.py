@@ -160,7 +160,7 @@ def test_optimizer_with_clipping_against_the_oracle(bo):
     params = [w.cuda() for w in wl.weights()]
     opt = bo.Fp8AdamW(params, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
                       weight_decay=wl.wd, max_grad_norm=0.02)
-    assert not opt.fused
+    assert opt.fused           # one fp8_cast_adam_step_clipped call per step
     states = fresh_states(wl.weights(), o3=False)
     for t in range(1, 4):
         grads = wl.grads(t)
@@ -174,3 +174,97 @@ def test_optimizer_with_clipping_against_the_oracle(bo):
         for i, s in enumerate(states):
             assert np.array_equal(to_np_u16(params[i].view(-1)), s.w) or \
                 np.abs(to_np_u16(params[i].view(-1)).astype(int) - s.w.astype(int)).max() <= 1
+
+
+# ------------------------------------- the cast and the clipped step fused
+
+def fused_clipped_lockstep(bo, wl, steps, max_norm, l2=False, o3=False,
+                           scaled_v=False, fmt="e4m3", misalign=()):
+    """fp8_cast_adam_step_clipped over the whole list against the oracle's
+    cast, then its clipped step, from the same gradient values."""
+    f = oracle.FMT[fmt]
+    states = fresh_states(wl.weights(), o3=o3, g_fmt=f, scaled_v=scaled_v)
+    gpu = GpuState([s.copy() for s in states], misalign=misalign)
+    n = len(states)
+    srcs = [torch.zeros(x, dtype=wl.grad_dtype, device="cuda") for x in wl.numels]
+    amax = torch.zeros(n, device="cuda")
+    cast = bo.CastPlan(srcs, gpu.g, amax, gpu.g_scale, fmt)
+    fused = bo.CastStepPlan(cast, gpu.plan)
+    norms = []
+    for t in range(1, steps + 1):
+        grads = wl.grads(t)
+        for d, h in zip(srcs, grads):
+            d.copy_(h)
+        codes, _, scale = oracle_cast(grads, f)
+        set_grads(states, codes, scale)
+        gpu.load_state(states)
+        f_ref, n_ref = oracle.adam_step_clipped(
+            states, wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, t,
+            wl.inv_loss_scale, max_norm, l2=l2)
+        nd = torch.zeros(1, device="cuda")
+        found = fused(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, t,
+                      wl.inv_loss_scale, found_inf_dev=gpu.found_dev, l2=l2,
+                      max_grad_norm=max_norm, grad_norm_dev=nd)
+        assert found == f_ref
+        assert fused.last_grad_norm == n_ref
+        if f_ref == 0:
+            assert nd.item() == np.float32(n_ref)
+            for i, c in enumerate(codes):
+                assert np.array_equal(to_np_u8(gpu.g[i]), c)
+            gpu.compare(states)
+        norms.append(n_ref)
+    return gpu, states, norms
+
+
+@pytest.mark.parametrize("l2", [False, True])
+def test_fused_clipped_long_tail(bo, l2):
+    wl = synth.o2_6p7b_tail(n_layer=1, d=128, ffn=512, vocab=3000, ctx=64,
+                            n_tail=30)
+    _, _, norms = fused_clipped_lockstep(bo, wl, 3, 0.05, l2=l2)
+    assert min(norms) > 0.05
+
+
+def test_fused_clipped_o3_scaled_v_e5m2_unaligned(bo):
+    wl = synth.o3_1p3b(n_layer=1, d=64, ffn=256, vocab=300, ctx=32)
+    fused_clipped_lockstep(bo, wl, 2, 0.01, o3=True, scaled_v=True, fmt="e5m2",
+                           misalign={0, 3})
+
+
+def test_fused_clipped_threshold_above_norm_and_zero(bo):
+    wl = synth.tiny()
+    fused_clipped_lockstep(bo, wl, 2, 1e9)      # never clips
+    fused_clipped_lockstep(bo, wl, 2, 0.0)      # measures only
+
+
+def test_fused_clipped_inf_in_a_gradient_skips(bo):
+    wl = dataclasses.replace(synth.o2_350m(n_layer=1, d=64, ffn=256, vocab=300,
+                                           ctx=32), inf_site=(3, 17))
+    gpu, states, norms = fused_clipped_lockstep(bo, wl, 1, 0.1)
+    assert norms == [math.inf]
+    for i, s in enumerate(states):
+        assert np.array_equal(to_np_u8(gpu.m[i]), s.m)
+        assert np.array_equal(to_np_u16(gpu.w[i]), s.w)
+
+
+def test_fused_clipped_equals_the_two_calls(bo):
+    """fp8_cast_adam_step_clipped against fp8_cast_scaled followed by
+    fp8_adam_step_clipped on the same buffers: identical bytes."""
+    wl = synth.o2_6p7b_tail(n_layer=1, d=64, ffn=256, vocab=1000, ctx=32,
+                            n_tail=20)
+    outs = []
+    for fused in (True, False):
+        params = [w.cuda() for w in wl.weights()]
+        opt = bo.Fp8AdamW(params, lr=wl.lr, weight_decay=0.1, fused=fused,
+                          max_grad_norm=0.03)
+        norms = []
+        for t in (1, 2, 3):
+            assert opt.step([g.cuda() for g in wl.grads(t)]) == 0
+            norms.append(opt.last_grad_norm)
+        outs.append((params, opt, norms))
+    (pa, oa, na), (pb, ob, nb) = outs
+    assert na == nb
+    for x, y in zip(pa, pb):
+        assert torch.equal(x, y)
+    for x, y in zip(oa.m + oa.v, ob.m + ob.v):
+        assert torch.equal(x, y)
+    assert torch.equal(oa.m_scale, ob.m_scale)

@@ -177,3 +177,70 @@ def test_partition_is_balanced_and_contiguous():
                 m = max(sum(w[x:y]) for x, y in zip(bounds, bounds[1:]))
                 opt = m if opt is None else min(opt, m)
             assert best == opt
+
+
+class FailingEngine:
+    """Wraps an engine; its step's begin raises on one step (a rank that
+    dies between the first pass and the exchange)."""
+
+    def __init__(self, inner, fail_step):
+        self.inner, self.fail_step, self.calls = inner, fail_step, 0
+
+    def __getattr__(self, name):
+        return getattr(self.inner, name)
+
+    def make_step(self, *args):
+        step = self.inner.make_step(*args)
+        outer = self
+
+        class Step:
+            def __getattr__(self, name):
+                return getattr(step, name)
+
+            def begin(self, *a, **k):
+                outer.calls += 1
+                if outer.calls == outer.fail_step:
+                    raise RuntimeError("injected rank failure")
+                return step.begin(*a, **k)
+        return Step()
+
+
+def failing_worker(rank, world, port, out_dir):
+    sys.path[:0] = [ROOT, HERE]
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    import datetime
+    import torch.distributed as dist
+    from bit_optimizer_gb300.sharded import ShardedFp8AdamW, TorchDistComm
+    from oracle_engine import OracleEngine
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=20))
+    wl = workload()
+    engine = FailingEngine(OracleEngine(), 2) if rank == 1 else OracleEngine()
+    opt = ShardedFp8AdamW(wl.weights(), TorchDistComm(), engine=engine,
+                          device="cpu")
+    outcome = "ok"
+    try:
+        for t in (1, 2, 3):
+            opt.step(local_grads(wl, t, rank))
+    except Exception as e:   # noqa: BLE001  (recorded for the parent)
+        outcome = f"{type(e).__name__}: {e}"[:200]
+    with open(os.path.join(out_dir, f"rank{rank}.txt"), "w") as f:
+        f.write(f"{outcome}\n{opt.step_count}\n")
+
+
+def test_a_failing_rank_stops_the_others_at_the_exchange(tmp_path):
+    """Rank 1 raises in its second step before the exchange; rank 0 gets an
+    error from that step's collective (it does not hang) and neither rank
+    counts the step."""
+    import time
+    import torch.multiprocessing as mp
+    ctx = mp.spawn(failing_worker, args=(2, free_port(), str(tmp_path)),
+                   nprocs=2, join=False)
+    t0 = time.time()
+    while not ctx.join(timeout=5):
+        assert time.time() - t0 < 120, "ranks still running after 120 s"
+    out = [open(tmp_path / f"rank{r}.txt").read().split("\n") for r in range(2)]
+    assert out[1][0].startswith("RuntimeError: injected rank failure")
+    assert out[0][0] != "ok"          # the collective reported the lost peer
+    assert out[0][1] == "1" and out[1][1] == "1"
