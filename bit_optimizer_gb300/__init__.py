@@ -5,8 +5,8 @@ Importing the package loads the in-tree shared library and fails if it has
 not been built: there is no fallback path.
 """
 from ._lib import (BF16, E4M3, E5M2, EXPORTS, F16, F32, KERNELS, Fp8OptError,
-                   LIB_PATH, load, release, strerror, timing_enable,
-                   timing_read)
+                   LIB_PATH, load, release, release_stream, strerror,
+                   timing_enable, timing_read)
 from .api import (AdamWPlan, CastPlan, CastStepPlan, Fp8AdamW, ReducePlan,
                   arena_views, fp8_adamw_step, fp8_cast_scaled,
                   fp8_reduce_scaled)
@@ -16,5 +16,6 @@ load()
 __all__ = ["fp8_cast_scaled", "fp8_adamw_step", "fp8_reduce_scaled",
            "CastPlan", "AdamWPlan", "CastStepPlan", "ReducePlan",
            "Fp8AdamW", "arena_views", "E4M3", "E5M2", "F32", "BF16", "F16",
-           "Fp8OptError", "strerror", "release", "load", "LIB_PATH", "EXPORTS",
+           "Fp8OptError", "strerror", "release", "release_stream", "load",
+           "LIB_PATH", "EXPORTS",
            "KERNELS", "timing_enable", "timing_read"]

@@ -22,10 +22,10 @@ EXPORTS = ("fp8_cast_scaled", "fp8_adamw_step", "fp8_adam_step",
            "fp8_cast_adamw_step", "fp8_reduce_scaled", "fp8_grad_norm",
            "fp8_adam_step_clipped", "fp8_grad_norm_terms", "fp8_clip_coef",
            "fp8_adam_step_begin", "fp8_adam_step_finish",
-           "fp8_cast_adam_step_clipped",
+           "fp8_cast_adam_step_clipped", "fp8_reduce_scaled_norm",
            "fp8_cast_scaled_noalloc", "fp8opt_strerror",
            "fp8opt_last_error", "fp8opt_timing_enable", "fp8opt_timing_read",
-           "fp8opt_release")
+           "fp8opt_release", "fp8opt_release_stream")
 KERNELS = ("cast_amax", "cast_encode", "step_amax", "step_update", "step_w8",
            "cast_step_amax", "reduce_amax", "reduce_encode", "grad_norm",
            "grad_norm_terms", "clip_coef", "found")
@@ -126,6 +126,10 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         C.c_float, C.c_float, C.c_float, C.c_float, C.c_int64, C.c_float, C.c_int,
         C.c_float, C.POINTER(C.c_double), C.c_void_p, C.POINTER(C.c_int),
         C.c_void_p, C.c_void_p]
+    L.fp8_reduce_scaled_norm.restype = C.c_int
+    L.fp8_reduce_scaled_norm.argtypes = [C.POINTER(ReduceItem), C.c_int, C.c_int,
+                                         C.c_int, C.c_int, C.c_float, C.c_float,
+                                         C.c_void_p, C.c_void_p, C.c_void_p]
     L.fp8_cast_scaled_noalloc.restype = C.c_int
     L.fp8_cast_scaled_noalloc.argtypes = [C.POINTER(CastItem), C.c_int, C.c_int,
                                           C.c_void_p]
@@ -145,6 +149,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
                                      C.POINTER(C.c_double)]
     L.fp8opt_release.restype = None
     L.fp8opt_release.argtypes = []
+    L.fp8opt_release_stream.restype = None
+    L.fp8opt_release_stream.argtypes = [C.c_void_p]
     _lib = L
     return L
 
@@ -175,3 +181,10 @@ def timing_read(kernel: str):
 
 def release() -> None:
     load().fp8opt_release()
+
+
+def release_stream(stream) -> None:
+    """Frees the workspace of one stream (a torch.cuda.Stream or a raw
+    cudaStream_t), e.g. after the CUDA graphs captured on it are destroyed."""
+    ptr = getattr(stream, "cuda_stream", stream)
+    load().fp8opt_release_stream(ptr or None)

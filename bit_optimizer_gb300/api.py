@@ -182,7 +182,8 @@ class ReducePlan:
             sh, c, sc = shards[i], codes[i], scales[i]
             if not isinstance(sh, torch.Tensor) or not sh.is_cuda:
                 raise TypeError("shards must be CUDA tensors")
-            if sh.dtype != torch.uint8 or sh.dim() != 2 or sh.stride(1) != 1:
+            if sh.dtype != torch.uint8 or sh.dim() != 2 or (
+                    sh.shape[1] > 1 and sh.stride(1) != 1):
                 raise ValueError(f"shards[{i}] must be uint8 [k, numel] with unit row stride")
             _cuda(c, "codes")
             ne = int(sh.shape[1])
@@ -193,16 +194,32 @@ class ReducePlan:
                 raise ValueError(f"scales[{i}] must be float32 with k elements")
             it = self._items[i]
             it.src, it.numel = sh.data_ptr(), ne
-            it.stride = sh.stride(0) if self.k > 1 else ne
+            # (the library rejects a row stride below numel; an empty tensor's
+            # stride does not matter)
+            it.stride = (sh.stride(0) if ne else 0) if self.k > 1 else ne
             it.src_scale = sc.data_ptr()
             it.codes = c.data_ptr()
             it.amax = _slot_ptr(amax, i, "amax")
             it.scale = _slot_ptr(scale, i, "scale")
 
-    def __call__(self, stream: Optional[torch.cuda.Stream] = None) -> None:
-        check(load().fp8_reduce_scaled(self._items, self.n, self.k, self.in_fmt,
-                                       self.out_fmt, self.post,
-                                       _stream_ptr(stream)))
+    def __call__(self, stream: Optional[torch.cuda.Stream] = None,
+                 norm_terms: Optional[torch.Tensor] = None,
+                 found: Optional[torch.Tensor] = None,
+                 inv_loss_scale: float = 1.0) -> None:
+        """One reduction.  With norm_terms (float64 CUDA, one per tensor):
+        also the norm terms of the outputs and, in found (int32 CUDA scalar,
+        optional), their found_inf (fp8_reduce_scaled_norm)."""
+        if norm_terms is None:
+            check(load().fp8_reduce_scaled(self._items, self.n, self.k,
+                                           self.in_fmt, self.out_fmt, self.post,
+                                           _stream_ptr(stream)))
+            return
+        if norm_terms.numel() < self.n:
+            raise ValueError("norm_terms needs one float64 per tensor")
+        check(load().fp8_reduce_scaled_norm(
+            self._items, self.n, self.k, self.in_fmt, self.out_fmt, self.post,
+            inv_loss_scale, _ptr_or_none(norm_terms, "norm_terms", torch.float64),
+            _ptr_or_none(found, "found", torch.int32), _stream_ptr(stream)))
 
 
 def fp8_reduce_scaled(shards: Sequence[torch.Tensor], scales, in_fmt="e4m3",

@@ -56,8 +56,10 @@ cudaError_t launch_reduce(const ReduceDesc* descs, const Chunk* chunks,
                           uint32_t nchunks, unsigned long long* slots,
                           uint32_t epoch, int k, int in_fmt, int out_fmt,
                           float post, int grid_amax, int grid_encode,
-                          cudaStream_t stream, LaunchMark mark);
+                          const ReduceNorm* norm, cudaStream_t stream,
+                          LaunchMark mark);
 cudaError_t reduce_occupancy(int* amax_per_sm, int* encode_per_sm);
+cudaError_t reduce_encode_sq_occupancy(int* per_sm);
 cudaError_t launch_grad_norm_terms(const StepDesc* descs, const Chunk* chunks,
                                    uint32_t nchunks, int n, float ils,
                                    unsigned long long* sums,
@@ -100,12 +102,15 @@ int cuda_fail(cudaError_t e, const char* where) {
                   cudaGetErrorString(e));
 }
 
-// A device buffer that only grows.
+// A device buffer that only grows, and not at all once frozen (a captured
+// CUDA graph holds its address).
 struct DevBuf {
   void* ptr = nullptr;
   size_t cap = 0;
+  bool frozen = false;
   cudaError_t reserve(size_t bytes) {
     if (bytes <= cap) return cudaSuccess;
+    if (frozen) return cudaErrorNotPermitted;
     if (ptr != nullptr) {
       cudaError_t e = cudaFree(ptr);
       if (e != cudaSuccess) return e;
@@ -132,7 +137,7 @@ struct DeviceInfo {
   int cast_step = 0;
   int reduce_amax = 0, reduce_encode = 0;
   int grad_norm = 0;
-  int cast_encode_sq = 0;
+  int cast_encode_sq = 0, reduce_encode_sq = 0;
 };
 
 // Per-(device, stream) state.  The slot region holds only epoch-tagged
@@ -162,6 +167,16 @@ struct Workspace {
   DevBuf reduce_descs, reduce_chunks;
   uint32_t reduce_nchunks = 0;
   bool have_cast = false, have_step = false, have_reduce = false;
+  // A CUDA graph captured on this stream refers to these buffers and tables:
+  // from then on they neither move nor change to another list.
+  bool frozen = false;
+
+  void freeze() {
+    frozen = true;
+    for (DevBuf* b : {&slots, &saved_scales, &norm_buf, &cast_descs, &cast_chunks,
+                      &step_descs, &step_chunks, &reduce_descs, &reduce_chunks})
+      b->frozen = true;
+  }
 
   void release() {
     slots.release();
@@ -210,6 +225,8 @@ cudaError_t device_info(int dev, DeviceInfo** out) {
   info.grad_norm = info.sms * (a > 0 ? a : 1);
   if ((e = cast_encode_sq_occupancy(&a)) != cudaSuccess) return e;
   info.cast_encode_sq = info.sms * (a > 0 ? a : 1);
+  if ((e = reduce_encode_sq_occupancy(&a)) != cudaSuccess) return e;
+  info.reduce_encode_sq = info.sms * (a > 0 ? a : 1);
   *out = &(g_dev[dev] = info);
   return cudaSuccess;
 }
@@ -224,12 +241,25 @@ Workspace* workspace(int dev, cudaStream_t s) {
   return w;
 }
 
+// Whether work on `stream` is being captured into a CUDA graph.
+bool capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  return cudaStreamIsCapturing(stream, &st) == cudaSuccess &&
+         st != cudaStreamCaptureStatusNone;
+}
+
 // `words` tagged slots for this call, zeroed when (re)allocated or when the
-// epoch wraps; returns the call's epoch.
+// epoch wraps; returns the call's epoch.  Under stream capture the epoch is
+// fixed into the graph, so the slots are zeroed as part of the captured
+// work: every replay then starts from clean slots (and a capture may not
+// grow the workspace: run the same list once before capturing).
 cudaError_t prepare_slots(Workspace* ws, size_t words, cudaStream_t stream,
                           uint32_t* epoch_out) {
   const size_t bytes = words * sizeof(unsigned long long);
-  bool fresh = false;
+  const bool graph = capturing(stream);
+  if (graph && bytes > ws->slots.cap) return cudaErrorStreamCaptureUnsupported;
+  if (graph) ws->freeze();
+  bool fresh = graph;
   if (bytes > ws->slots.cap) {
     cudaError_t e = ws->slots.reserve(bytes);
     if (e != cudaSuccess) return e;
@@ -241,7 +271,8 @@ cudaError_t prepare_slots(Workspace* ws, size_t words, cudaStream_t stream,
     ws->epoch = 1;
   }
   if (fresh) {
-    cudaError_t e = cudaMemsetAsync(ws->slots.ptr, 0, ws->slots.cap, stream);
+    cudaError_t e = cudaMemsetAsync(ws->slots.ptr, 0, graph ? bytes : ws->slots.cap,
+                                    stream);
     if (e != cudaSuccess) return e;
   }
   *epoch_out = ws->epoch;
@@ -278,6 +309,7 @@ cudaEvent_t timing_event() {
 }
 
 void timing_mark(int kernel, int end, cudaStream_t stream) {
+  if (capturing(stream)) return;   // graph replays are not timed per kernel
   cudaEvent_t e = timing_event();
   cudaEventRecord(e, stream);
   if (!end) {
@@ -348,6 +380,17 @@ using namespace fp8opt;
 
 namespace fp8opt {
 namespace {
+
+// A new tensor list is refused under stream capture (the table upload
+// would record a copy from host memory the library frees after the call)
+// and on a stream whose workspace a captured graph holds.
+int refuse_capture(const char* fn) {
+  return fail(FP8OPT_ERR_ARG, std::string(fn) +
+                                  ": a new tensor list under stream capture, or "
+                                  "on a stream a captured CUDA graph uses; run "
+                                  "the list once on this stream before capturing, "
+                                  "and other lists on other streams");
+}
 
 int check_cast_args(const char* fn, const fp8opt_cast_item* items, int n,
                     int fmt) {
@@ -421,6 +464,7 @@ int ensure_cast_tables(const char* fn, Workspace* ws,
                        const fp8opt_cast_item* items, int n,
                        cudaStream_t stream) {
   if (ws->have_cast && same_list(ws->cast_key, items, n)) return FP8OPT_OK;
+  if (capturing(stream) || ws->frozen) return refuse_capture(fn);
   std::vector<CastDesc> descs((size_t)n);
   std::vector<Chunk> chunks;
   size_t total = 0;
@@ -458,6 +502,7 @@ int ensure_cast_tables(const char* fn, Workspace* ws,
 int ensure_step_tables(const char* fn, Workspace* ws, const fp8opt_param* params,
                        int n, cudaStream_t stream) {
   if (ws->have_step && same_list(ws->step_key, params, n)) return FP8OPT_OK;
+  if (capturing(stream) || ws->frozen) return refuse_capture(fn);
   std::vector<StepDesc> descs((size_t)n);
   std::vector<Chunk> chunks, chunks_o3;
   size_t total = 0;
@@ -534,6 +579,7 @@ int ensure_reduce_tables(const char* fn, Workspace* ws,
                          const fp8opt_reduce_item* items, int n,
                          cudaStream_t stream) {
   if (ws->have_reduce && same_list(ws->reduce_key, items, n)) return FP8OPT_OK;
+  if (capturing(stream) || ws->frozen) return refuse_capture(fn);
   std::vector<ReduceDesc> descs((size_t)n);
   std::vector<Chunk> chunks;
   size_t total = 0;
@@ -633,13 +679,21 @@ extern "C" int fp8_cast_scaled(const fp8opt_cast_item* items, int n, int fmt,
   return FP8OPT_OK;
 }
 
-extern "C" int fp8_reduce_scaled(const fp8opt_reduce_item* items, int n, int k,
-                                 int in_fmt, int out_fmt, float post,
-                                 void* stream_ptr) {
-  const char* fn = "fp8_reduce_scaled";
+namespace fp8opt {
+namespace {
+
+// The reduction entry points; terms_dev set: also the norm terms of the
+// outputs (with found_dev, may be NULL).
+int reduce_call(const char* fn, const fp8opt_reduce_item* items, int n, int k,
+                int in_fmt, int out_fmt, float post, bool with_norm, float ils,
+                double* terms_dev, uint32_t* found_dev, void* stream_ptr) {
   int st = check_reduce_args(fn, items, n, k, in_fmt, out_fmt);
-  if (st != FP8OPT_OK || n == 0) return st;
+  if (st != FP8OPT_OK) return st;
+  if (with_norm && n > 0 && terms_dev == nullptr)
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": terms_dev is NULL");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (n == 0)
+    return with_norm ? empty_step(fn, nullptr, found_dev, stream) : FP8OPT_OK;
 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0;
@@ -648,17 +702,43 @@ extern "C" int fp8_reduce_scaled(const fp8opt_reduce_item* items, int n, int k,
   Workspace* ws = workspace(dev, stream);
   if ((st = ensure_reduce_tables(fn, ws, items, n, stream)) != FP8OPT_OK) return st;
 
+  // slots: [0, n) amax, [n] found_inf; norm: 2n words of exact sums
   uint32_t epoch = 0;
-  cudaError_t e = prepare_slots(ws, (size_t)n, stream, &epoch);   // [0, n) amax
-  if (e != cudaSuccess) return cuda_fail(e, "fp8_reduce_scaled: workspace");
+  cudaError_t e = prepare_slots(ws, (size_t)n + 1, stream, &epoch);
+  const size_t sum_bytes = 2 * (size_t)n * sizeof(unsigned long long);
+  if (e == cudaSuccess && with_norm) e = ws->norm_buf.reserve(sum_bytes);
+  if (e == cudaSuccess && with_norm)
+    e = cudaMemsetAsync(ws->norm_buf.ptr, 0, sum_bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": workspace").c_str());
+  unsigned long long* slots = static_cast<unsigned long long*>(ws->slots.ptr);
+  ReduceNorm norm = {static_cast<unsigned long long*>(ws->norm_buf.ptr),
+                     slots + n, ils, n, terms_dev, found_dev};
   e = launch_reduce(static_cast<const ReduceDesc*>(ws->reduce_descs.ptr),
                     static_cast<const Chunk*>(ws->reduce_chunks.ptr),
-                    ws->reduce_nchunks,
-                    static_cast<unsigned long long*>(ws->slots.ptr), epoch, k,
-                    in_fmt, out_fmt, post, info->reduce_amax, info->reduce_encode,
-                    stream, launch_mark());
-  if (e != cudaSuccess) return cuda_fail(e, "fp8_reduce_scaled: launch");
+                    ws->reduce_nchunks, slots, epoch, k, in_fmt, out_fmt, post,
+                    info->reduce_amax,
+                    with_norm ? info->reduce_encode_sq : info->reduce_encode,
+                    with_norm ? &norm : nullptr, stream, launch_mark());
+  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
   return FP8OPT_OK;
+}
+
+}  // namespace
+}  // namespace fp8opt
+
+extern "C" int fp8_reduce_scaled(const fp8opt_reduce_item* items, int n, int k,
+                                 int in_fmt, int out_fmt, float post,
+                                 void* stream_ptr) {
+  return reduce_call("fp8_reduce_scaled", items, n, k, in_fmt, out_fmt, post,
+                     false, 1.0f, nullptr, nullptr, stream_ptr);
+}
+
+extern "C" int fp8_reduce_scaled_norm(const fp8opt_reduce_item* items, int n,
+                                      int k, int in_fmt, int out_fmt, float post,
+                                      float inv_loss_scale, double* terms_dev,
+                                      uint32_t* found_dev, void* stream_ptr) {
+  return reduce_call("fp8_reduce_scaled_norm", items, n, k, in_fmt, out_fmt, post,
+                     true, inv_loss_scale, terms_dev, found_dev, stream_ptr);
 }
 
 namespace fp8opt {
@@ -1158,6 +1238,17 @@ extern "C" int fp8opt_timing_read(const char* kernel, int* launches,
   *launches = g_timing.launches[k];
   *total_ms = g_timing.ms[k];
   return FP8OPT_OK;
+}
+
+extern "C" void fp8opt_release_stream(void* stream_ptr) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return;
+  auto it = g_ws.find(std::make_pair(dev, static_cast<cudaStream_t>(stream_ptr)));
+  if (it == g_ws.end()) return;
+  it->second->release();
+  delete it->second;
+  g_ws.erase(it);
 }
 
 extern "C" void fp8opt_release(void) {

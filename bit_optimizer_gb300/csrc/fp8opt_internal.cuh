@@ -84,6 +84,18 @@ struct ReduceDesc {
 // Most shards one reduction call takes.
 constexpr int kMaxShards = 64;
 
+// The gradient norm of a reduction's outputs: 2n zeroed words of exact sums,
+// the call's found_inf slot, the inverse loss scale, n terms out and the
+// found flag out (may be NULL).
+struct ReduceNorm {
+  unsigned long long* sums;
+  unsigned long long* found;
+  float ils;
+  int n;
+  double* terms;
+  uint32_t* found_out;
+};
+
 // Kernels, for the optional per-launch event timing.
 enum KernelId { kCastAmaxK = 0, kCastEncodeK, kStepAmaxK, kStepUpdateK,
                 kStepW8K, kCastStepAmaxK, kReduceAmaxK, kReduceEncodeK,
@@ -521,6 +533,27 @@ __device__ __forceinline__ void sq_commit(const SqAcc<FMT>& a, uint32_t t,
     if (bad || nonfinite(__fmul_rn(dec2<FMT>(cmax).x, k)))
       atomicMax(found, slot_tag(epoch, 1u));
   }
+}
+
+// Correctly rounded conversion of a 128-bit unsigned integer to double: the
+// top 64 bits after normalisation, with every lower bit folded into the
+// lowest one (a sticky bit, eleven places below the rounding position), then
+// an exact power-of-two scaling.
+__device__ __forceinline__ double u128_to_double(U128 v) {
+  if (v.hi == 0) return __ull2double_rn(v.lo);
+  const int lz = __clzll((long long)v.hi);
+  const unsigned long long top = lz ? (v.hi << lz) | (v.lo >> (64 - lz)) : v.hi;
+  const unsigned long long rest = v.lo << lz;
+  const double d = __ull2double_rn(top | (rest != 0 ? 1ull : 0ull));
+  return __dmul_rn(d, __longlong_as_double((long long)(1023 + 64 - lz) << 52));
+}
+
+// A record's norm term from its exact sum S (units of 2^-32) and factor k:
+// fl64(k^2 * fl64(S * 2^-32)), where k^2 and the power-of-two scaling are
+// exact in double.
+__device__ __forceinline__ double norm_term(U128 s, float k) {
+  const double kd = (double)k;
+  return __dmul_rn(__dmul_rn(kd, kd), __dmul_rn(u128_to_double(s), 0x1p-32));
 }
 
 }  // namespace fp8opt

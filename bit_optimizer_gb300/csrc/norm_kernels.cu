@@ -88,19 +88,6 @@ grad_norm_kernel(const StepDesc* __restrict__ descs,
   }
 }
 
-// Correctly rounded conversion of a 128-bit unsigned integer to double: the
-// top 64 bits after normalisation, with every lower bit folded into the
-// lowest one (a sticky bit, eleven places below the rounding position), then
-// an exact power-of-two scaling.
-__device__ double u128_to_double(U128 v) {
-  if (v.hi == 0) return __ull2double_rn(v.lo);
-  const int lz = __clzll((long long)v.hi);
-  const unsigned long long top = lz ? (v.hi << lz) | (v.lo >> (64 - lz)) : v.hi;
-  const unsigned long long rest = v.lo << lz;
-  const double d = __ull2double_rn(top | (rest != 0 ? 1ull : 0ull));
-  return __dmul_rn(d, __longlong_as_double((long long)(1023 + 64 - lz) << 52));
-}
-
 // Per-record terms fl64(k^2 * fl64(S) * 2^-32) (k^2 is exact in double), one
 // thread per record; block 0 also exports this call's found_inf.
 __global__ void __launch_bounds__(kThreads)
@@ -112,8 +99,8 @@ grad_norm_terms_kernel(const StepDesc* __restrict__ descs, int n, float ils,
   const int t = blockIdx.x * kThreads + threadIdx.x;
   if (t < n) {
     const U128 s = {sums[2 * t], sums[2 * t + 1]};
-    const double k = (double)__fdiv_rn(ils, *descs[t].g_scale);
-    terms[t] = __dmul_rn(__dmul_rn(k, k), __dmul_rn(u128_to_double(s), 0x1p-32));
+    const float k = __fdiv_rn(ils, *descs[t].g_scale);
+    terms[t] = norm_term(s, k);
   }
   if (found_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
     *found_out = slot_value(*found, epoch) != 0 ? 1u : 0u;

@@ -219,10 +219,11 @@ __device__ __forceinline__ uint4 encode16(const float2 (&y)[8], float scale) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <int IN, int OUT, bool CHECKED>
+template <int IN, int OUT, bool CHECKED, bool SQ>
 __device__ void thread_reduce_encode(const ReduceDesc& d, int k,
                                      const float* r_s, float post, float scale,
-                                     int64_t begin, int64_t end) {
+                                     int64_t begin, int64_t end,
+                                     SqAcc<OUT>& acc) {
   const int tid = threadIdx.x;
   const bool vec = d.vec_ok != 0 && !CHECKED;
 #pragma unroll 1
@@ -236,8 +237,16 @@ __device__ void thread_reduce_encode(const ReduceDesc& d, int k,
       float2 y[kRGroups][8];
       reduce_groups<IN, true>(d.src, d.stride, k, r_s, post, i0, y);
 #pragma unroll
-      for (int g = 0; g < kRGroups; ++g)
-        *reinterpret_cast<uint4*>(d.codes + i0[g]) = encode16<OUT>(y[g], scale);
+      for (int g = 0; g < kRGroups; ++g) {
+        const uint4 c = encode16<OUT>(y[g], scale);
+        *reinterpret_cast<uint4*>(d.codes + i0[g]) = c;
+        if (SQ) {
+          acc.add_word(c.x);
+          acc.add_word(c.y);
+          acc.add_word(c.z);
+          acc.add_word(c.w);
+        }
+      }
     } else {
 #pragma unroll 1
       for (int g = 0; g < kRGroups; ++g) {
@@ -247,21 +256,33 @@ __device__ void thread_reduce_encode(const ReduceDesc& d, int k,
           if (i >= end) break;
           const float t =
               __fmul_rn(reduce_one<IN>(d.src, d.stride, k, r_s, post, i), scale);
-          d.codes[i] = (uint8_t)(CHECKED ? enc1_checked<OUT>(t)
-                                         : (enc2<OUT>(t, 0.0f) & 0xFFu));
+          const uint32_t c = CHECKED ? enc1_checked<OUT>(t)
+                                     : (enc2<OUT>(t, 0.0f) & 0xFFu);
+          d.codes[i] = (uint8_t)c;
+          if (SQ) acc.add_word(c);
         }
       }
     }
   }
 }
 
-template <int IN, int OUT>
-__global__ void __launch_bounds__(kThreads, FP8OPT_REDUCE_MIN_BLOCKS)
-reduce_encode_kernel(const ReduceDesc* __restrict__ descs,
-                     const Chunk* __restrict__ chunks, uint32_t nchunks, int k,
-                     float post, const unsigned long long* __restrict__ slots,
-                     uint32_t epoch) {
-  __shared__ float r_s[kMaxShards];
+// Where an encode pass also sums the exact squares of the codes it writes
+// (the gradient norm of the reduced tensors): the 128-bit slots, the
+// found_inf slot and the inverse loss scale.
+struct RedSq {
+  unsigned long long* sums;
+  unsigned long long* found;
+  float ils;
+};
+
+template <int IN, int OUT, bool SQ>
+__device__ __forceinline__ void encode_pass(const ReduceDesc* __restrict__ descs,
+                                            const Chunk* __restrict__ chunks,
+                                            uint32_t nchunks, int k, float post,
+                                            const unsigned long long* __restrict__ slots,
+                                            uint32_t epoch, const RedSq& sq,
+                                            float* r_s, unsigned long long* red64,
+                                            uint32_t* red32) {
   for (uint32_t r = blockIdx.x; r < nchunks; r += gridDim.x) {
     const Chunk ch = chunks[nchunks - 1 - r];
     const ReduceDesc d = descs[ch.tensor];
@@ -274,34 +295,94 @@ reduce_encode_kernel(const ReduceDesc* __restrict__ descs,
     }
     const int64_t begin = (int64_t)ch.index * kChunkElems;
     const int64_t end = min(begin + kChunkElems, d.numel);
+    SqAcc<OUT> acc;
     if (ab >= 0x7F800000u)
-      thread_reduce_encode<IN, OUT, true>(d, k, r_s, post, scale, begin, end);
+      thread_reduce_encode<IN, OUT, true, SQ>(d, k, r_s, post, scale, begin, end, acc);
     else
-      thread_reduce_encode<IN, OUT, false>(d, k, r_s, post, scale, begin, end);
+      thread_reduce_encode<IN, OUT, false, SQ>(d, k, r_s, post, scale, begin, end, acc);
+    if (SQ)
+      sq_commit<OUT>(acc, ch.tensor, end > begin, __fdiv_rn(sq.ils, scale),
+                     sq.sums, sq.found, epoch, red64, red32);
   }
+}
+
+template <int IN, int OUT>
+__global__ void __launch_bounds__(kThreads, FP8OPT_REDUCE_MIN_BLOCKS)
+reduce_encode_kernel(const ReduceDesc* __restrict__ descs,
+                     const Chunk* __restrict__ chunks, uint32_t nchunks, int k,
+                     float post, const unsigned long long* __restrict__ slots,
+                     uint32_t epoch) {
+  __shared__ float r_s[kMaxShards];
+  const RedSq none = {nullptr, nullptr, 0.0f};
+  encode_pass<IN, OUT, false>(descs, chunks, nchunks, k, post, slots, epoch,
+                              none, r_s, nullptr, nullptr);
+}
+
+// (the exact squares need more registers than the plain pass: two CTAs per
+// SM keep it free of spills)
+template <int IN, int OUT>
+__global__ void __launch_bounds__(kThreads, 2)
+reduce_encode_sq_kernel(const ReduceDesc* __restrict__ descs,
+                        const Chunk* __restrict__ chunks, uint32_t nchunks, int k,
+                        float post, const unsigned long long* __restrict__ slots,
+                        uint32_t epoch, RedSq sq) {
+  __shared__ float r_s[kMaxShards];
+  __shared__ unsigned long long red64[2 * (kThreads / 32)];
+  __shared__ uint32_t red32[kThreads / 32];
+  encode_pass<IN, OUT, true>(descs, chunks, nchunks, k, post, slots, epoch, sq,
+                             r_s, red64, red32);
+}
+
+// Per-item norm terms of the reduced tensors (k = ils / the output scale);
+// block 0 also exports found_inf.
+__global__ void __launch_bounds__(kThreads)
+reduce_terms_kernel(const ReduceDesc* __restrict__ descs, int n, float ils,
+                    const unsigned long long* __restrict__ sums,
+                    const unsigned long long* __restrict__ found, uint32_t epoch,
+                    double* __restrict__ terms, uint32_t* __restrict__ found_out) {
+  const int t = blockIdx.x * kThreads + threadIdx.x;
+  if (t < n) {
+    const U128 s = {sums[2 * t], sums[2 * t + 1]};
+    terms[t] = norm_term(s, __fdiv_rn(ils, *descs[t].scale_out));
+  }
+  if (found_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
+    *found_out = slot_value(*found, epoch) != 0 ? 1u : 0u;
 }
 
 template <int IN>
 void launch_encode(uint32_t grid, const ReduceDesc* descs, const Chunk* chunks,
                    uint32_t nchunks, int k, float post,
                    const unsigned long long* slots, uint32_t epoch, int out_fmt,
-                   cudaStream_t stream) {
-  if (out_fmt == kE4M3)
-    reduce_encode_kernel<IN, kE4M3><<<grid, kThreads, 0, stream>>>(
-        descs, chunks, nchunks, k, post, slots, epoch);
-  else
-    reduce_encode_kernel<IN, kE5M2><<<grid, kThreads, 0, stream>>>(
-        descs, chunks, nchunks, k, post, slots, epoch);
+                   const RedSq* sq, cudaStream_t stream) {
+  if (sq == nullptr) {
+    if (out_fmt == kE4M3)
+      reduce_encode_kernel<IN, kE4M3><<<grid, kThreads, 0, stream>>>(
+          descs, chunks, nchunks, k, post, slots, epoch);
+    else
+      reduce_encode_kernel<IN, kE5M2><<<grid, kThreads, 0, stream>>>(
+          descs, chunks, nchunks, k, post, slots, epoch);
+  } else {
+    if (out_fmt == kE4M3)
+      reduce_encode_sq_kernel<IN, kE4M3><<<grid, kThreads, 0, stream>>>(
+          descs, chunks, nchunks, k, post, slots, epoch, *sq);
+    else
+      reduce_encode_sq_kernel<IN, kE5M2><<<grid, kThreads, 0, stream>>>(
+          descs, chunks, nchunks, k, post, slots, epoch, *sq);
+  }
 }
 
 }  // namespace
 
-// Launches both passes on `stream`; 1 <= k <= kMaxShards.
+// Launches both passes on `stream`; 1 <= k <= kMaxShards.  With norm set,
+// the encode pass also sums the exact squares of the codes it writes into
+// norm->sums (2n zeroed words; found_inf into norm->found), and a last kernel
+// writes each item's norm term and the found flag.
 cudaError_t launch_reduce(const ReduceDesc* descs, const Chunk* chunks,
                           uint32_t nchunks, unsigned long long* slots,
                           uint32_t epoch, int k, int in_fmt, int out_fmt,
                           float post, int grid_amax, int grid_encode,
-                          cudaStream_t stream, LaunchMark mark) {
+                          const ReduceNorm* norm, cudaStream_t stream,
+                          LaunchMark mark) {
   if (nchunks == 0) return cudaSuccess;
   const uint32_t ga = grid_min((uint32_t)grid_amax, nchunks);
   const uint32_t ge = grid_min((uint32_t)grid_encode, nchunks);
@@ -314,14 +395,29 @@ cudaError_t launch_reduce(const ReduceDesc* descs, const Chunk* chunks,
                                                            k, post, slots, epoch);
   if (mark) mark(kReduceAmaxK, 1, stream);
   if (mark) mark(kReduceEncodeK, 0, stream);
+  RedSq sq;
+  if (norm != nullptr) sq = RedSq{norm->sums, norm->found, norm->ils};
+  const RedSq* sqp = norm != nullptr ? &sq : nullptr;
   if (in_fmt == kE4M3)
     launch_encode<kE4M3>(ge, descs, chunks, nchunks, k, post, slots, epoch,
-                         out_fmt, stream);
+                         out_fmt, sqp, stream);
   else
     launch_encode<kE5M2>(ge, descs, chunks, nchunks, k, post, slots, epoch,
-                         out_fmt, stream);
+                         out_fmt, sqp, stream);
   if (mark) mark(kReduceEncodeK, 1, stream);
+  if (norm != nullptr && norm->n > 0) {
+    if (mark) mark(kGradNormTermsK, 0, stream);
+    reduce_terms_kernel<<<(norm->n + kThreads - 1) / kThreads, kThreads, 0, stream>>>(
+        descs, norm->n, norm->ils, norm->sums, norm->found, epoch, norm->terms,
+        norm->found_out);
+    if (mark) mark(kGradNormTermsK, 1, stream);
+  }
   return cudaGetLastError();
+}
+
+cudaError_t reduce_encode_sq_occupancy(int* per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      per_sm, reduce_encode_sq_kernel<kE4M3, kE4M3>, kThreads, 0);
 }
 
 // Resident CTAs per SM of the two reduction kernels.

@@ -6,8 +6,10 @@ Level" page, O3 paragraph).  Here every rank owns the optimizer state (E4M3
 first moment, FP16 second moment, FP16 master) of a contiguous range of whole
 tensors, balanced by size; a step on each rank is
 
-  1. (clipping only) the gradient-norm pass over its own tensors, giving
-     per-tensor terms and its found_inf;
+  1. the FP8 cast of its local gradients, an all-to-all that brings every
+     tensor's codes from all ranks to its owner, and the FP8 mean of those
+     shards (with clipping, that reduction also gives the owned tensors' norm
+     terms and found_inf);
   2. the step's first pass over its own tensors (``begin``), giving found_inf;
   3. one exchange: found_inf MAX over ranks (and, with clipping, the per-tensor
      norm terms, each held by exactly one rank, summed so every rank holds all
@@ -286,14 +288,17 @@ class ShardedFp8AdamW:
         if n_own:
             self._scale_t[:n_own].copy_(
                 self._recv_scale[:world * n_own].view(world, n_own).t())
-        # 3. the mean of the ranks' shards, re-encoded
-        self._reduce()
-        # 4. found_inf (and the global norm) over ranks, then the step
+        # 3. the mean of the ranks' shards, re-encoded (with clipping, the
+        #    encode pass also gives the owned tensors' norm terms)
         clip = None
         if self.max_grad_norm is not None:
             self._terms.zero_()
-            self._step.norm_terms(inv_loss_scale, self._terms[lo:max(hi, lo + 1)],
-                                  self._found)
+            self._reduce(norm_terms=self._terms[lo:max(hi, lo + 1)],
+                         found=self._found, inv_loss_scale=inv_loss_scale)
+        else:
+            self._reduce()
+        # 4. found_inf (and the global norm) over ranks, then the step
+        if self.max_grad_norm is not None:
             comm.all_reduce_sum(self._terms)
             comm.all_reduce_max(self._found)
             self.engine.clip_coef(self._terms[:self.n], self.max_grad_norm,

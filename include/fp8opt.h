@@ -36,6 +36,24 @@
  * stream must come from one host thread at a time; calls on different streams
  * use different workspaces and may run concurrently.
  *
+ * CUDA graphs: a call may be captured into a CUDA graph (stream capture) once
+ * the same tensor list has run on that stream, so that its tables and
+ * workspace exist; a list not yet seen on the stream is refused under capture
+ * (FP8OPT_ERR_ARG).  The graph then refers to that stream's workspace, which
+ * is frozen: later calls on the stream must use the lists already there (a
+ * new list is refused with FP8OPT_ERR_ARG, a larger workspace fails with
+ * FP8OPT_ERR_CUDA, "operation not permitted"), so other lists belong on other
+ * streams; fp8opt_release_stream() or fp8opt_release() frees it (after the
+ * graph is destroyed).  A
+ * captured call
+ * zeroes its per-tensor slots as part of the captured work, so every replay
+ * is a fresh call on the buffers' current contents.  Host outputs (found_inf,
+ * the host norm) wait for the stream and cannot be captured: pass NULL and use
+ * the device outputs.  What a capture fixes: the records, and the step's
+ * scalars (lr, the bias corrections of `step`, inv_loss_scale, the clip
+ * threshold); the cast and the reduction have none, so their replays are
+ * exactly new calls.
+ *
  * Errors: every entry point returns FP8OPT_OK (0) or a negative status.  On an
  * argument error nothing is launched and no output is touched.  On a CUDA
  * error the CUDA error text is kept for fp8opt_last_error().
@@ -405,6 +423,21 @@ FP8OPT_API int fp8_cast_adam_step_clipped(const fp8opt_cast_item *grads,
                                           int *found_inf, uint32_t *found_inf_dev,
                                           void *stream);
 
+/*
+ * fp8_reduce_scaled_norm: fp8_reduce_scaled, whose encode pass also sums the
+ * exact squares of the codes it writes, so that the reduced gradients' norm
+ * terms come without a pass of their own: terms_dev[t] (device doubles, one
+ * per item) = fp8_grad_norm_terms' term of item t's output codes with the
+ * factor k_t = inv_loss_scale / (item t's output scale), and found_dev
+ * (device uint32, may be NULL) = whether some code value times k_t is not
+ * finite.  For the sharded step's exchange (see fp8_grad_norm_terms); same
+ * arguments and errors as fp8_reduce_scaled otherwise.
+ */
+FP8OPT_API int fp8_reduce_scaled_norm(const fp8opt_reduce_item *items, int n,
+                                      int k, int in_fmt, int out_fmt, float post,
+                                      float inv_loss_scale, double *terms_dev,
+                                      uint32_t *found_dev, void *stream);
+
 /* Text of a status code (static storage). */
 FP8OPT_API const char *fp8opt_strerror(int status);
 
@@ -430,6 +463,12 @@ FP8OPT_API int fp8opt_timing_read(const char *kernel, int *launches,
 /* Frees every workspace the library holds, on every device.  The caller must
  * make sure no call's work is still running. */
 FP8OPT_API void fp8opt_release(void);
+
+/* Frees the workspace of one stream (on the current device), e.g. after the
+ * CUDA graphs captured on it are destroyed, so that the stream takes any
+ * tensor list again.  The caller must make sure no work that uses it is
+ * still running. */
+FP8OPT_API void fp8opt_release_stream(void *stream);
 
 #ifdef __cplusplus
 }

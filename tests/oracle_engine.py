@@ -36,13 +36,23 @@ class OracleEngine:
                     post):
         fi, fo = oracle.FMT[in_fmt], oracle.FMT[out_fmt]
 
-        def run():
+        def run(stream=None, norm_terms=None, found=None, inv_loss_scale=1.0):
             for i, sh in enumerate(shards):
                 cc, am, sc = oracle.reduce_scaled(sh.contiguous().numpy(),
                                                   scales[i].numpy(), fi, fo, post)
                 codes[i].copy_(torch.from_numpy(cc))
                 amax[i] = float(am)
                 scale[i] = float(sc)
+            if norm_terms is not None:
+                states = [oracle.StepState(c.numpy(), float(scale[i]),
+                                           np.zeros(c.numel(), np.uint8), 1.0,
+                                           np.zeros(c.numel(), np.uint16),
+                                           np.zeros(c.numel(), np.uint16), g_fmt=fo)
+                          for i, c in enumerate(codes)]
+                f, tt = oracle.grad_norm_terms(states, inv_loss_scale)
+                norm_terms[:len(codes)] = torch.from_numpy(tt.copy())
+                if found is not None:
+                    found[0] = f
         return run
 
     def make_step(self, g, g_scale, m, m_scale, v, w, w8, w8_scale, w8_amax,

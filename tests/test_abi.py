@@ -158,6 +158,11 @@ def test_reduce_argument_errors_need_no_gpu(lib):
     it[0].stride = 2 ** 62                           # k * stride overflows
     assert L.fp8_reduce_scaled(it, 1, 4, 0, 0, 1.0, None) == lib.ERR_ARG
     assert L.fp8_reduce_scaled(it, 0, 2, 0, 0, 1.0, None) == lib.OK
+    it[0].stride = 100
+    assert L.fp8_reduce_scaled_norm(it, 1, 2, 0, 0, 1.0, 1.0, None, None,
+                                    None) == lib.ERR_ARG   # NULL terms
+    assert L.fp8_reduce_scaled_norm(it, 0, 2, 0, 0, 1.0, 1.0, None, None,
+                                    None) == lib.OK
 
 
 def test_norm_and_clip_argument_errors_need_no_gpu(lib):
