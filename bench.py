@@ -71,6 +71,11 @@ def parse():
     p.add_argument("--unfused", action="store_true",
                    help="run the headline as two calls (the cast, then the "
                         "step; profiling case)")
+    p.add_argument("--sharded", action="store_true",
+                   help="under torchrun: the ZeRO-1 sharded data-parallel step "
+                        "(each rank casts its own gradients of every tensor, "
+                        "FP8 all-to-all, FP8 mean, owners step their tensors, "
+                        "weights broadcast) instead of independent replicas")
     p.add_argument("--reduce-only", type=int, default=None, metavar="K",
                    help="time only the local FP8 reduction of K shards of the "
                         "124M list and print its line (profiling case)")
@@ -610,6 +615,71 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+def run_sharded(args, wl):
+    """The data-parallel step of one model over the ranks of a torchrun job
+    (NCCL): every rank holds its own BF16 gradients of every tensor; one step
+    casts them, sends each tensor's codes to its owner, reduces the ranks'
+    shards to their mean, steps the owned tensors and broadcasts the new
+    weights.  value = the model's parameters stepped per second (the model is
+    fixed: strong scaling)."""
+    import torch
+    import torch.distributed as dist
+    import bit_optimizer_gb300 as bo
+    from bit_optimizer_gb300.sharded import ShardedFp8AdamW, TorchDistComm
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist.init_process_group("nccl", device_id=device)
+    weights = [wl.weight(i, device) for i in range(len(wl.shapes))]
+    opt = ShardedFp8AdamW(weights, TorchDistComm(), lr=wl.lr,
+                          betas=(wl.beta1, wl.beta2), eps=wl.eps,
+                          weight_decay=wl.wd, level=wl.level,
+                          grad_fmt=wl.grad_fmt, max_grad_norm=args.max_grad_norm)
+    del weights
+    grads, _ = bo.arena_views(wl.numels, wl.grad_dtype, device, return_base=True)
+    for i, g in enumerate(grads):
+        g.copy_(wl.rank_grad(i, 1, rank, device))
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        if opt.step(grads, wl.inv_loss_scale) != 0:
+            raise RuntimeError("found_inf set on a finite workload")
+    dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        opt.step(grads, wl.inv_loss_scale)
+    t1.record()
+    dist.barrier()
+    torch.cuda.synchronize()
+    sampler.stop()
+    t = torch.tensor([t0.elapsed_time(t1) / args.steps], dtype=torch.float64,
+                     device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    if rank == 0:
+        desc = workload_desc(wl)
+        desc["step"] = ("sharded data-parallel step: FP8 cast of each rank's "
+                        "gradients, FP8 all-to-all, FP8 mean, owners' step, "
+                        "weight broadcast (NCCL)")
+        lo, hi = opt.own
+        line = {
+            "metric": METRIC, "value": wl.n_params / (ms * 1e-3) / 1e9,
+            "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": desc,
+            "partition_rank0": [lo, hi, sum(wl.numels[lo:hi])],
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    dist.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.reduce_only is not None:
@@ -628,6 +698,8 @@ def main():
     wl = dataclasses.replace(wl, inf_site=None)
     if args.impl == "reference":
         run_reference(args, wl)
+    elif args.sharded:
+        run_sharded(args, wl)
     else:
         run_ours(args, wl)
 
