@@ -45,7 +45,7 @@ namespace {
 // tile in the amax and update passes, and the update kernel's resident CTAs
 // per SM (which caps its registers a thread).
 #ifndef FP8OPT_STEP_AMAX_GROUPS
-#define FP8OPT_STEP_AMAX_GROUPS 2
+#define FP8OPT_STEP_AMAX_GROUPS 4
 #endif
 #ifndef FP8OPT_UPD_GROUPS
 #define FP8OPT_UPD_GROUPS 2
@@ -55,8 +55,9 @@ namespace {
 #endif
 // Tiles ahead of the current one that the update and amax passes prefetch
 // into L2 (0: none).  Measured on the 6.7B list: the update pass is 7 %
-// slower with a prefetch one or two tiles ahead, and the amax pass gains
-// nothing, so both are off.
+// slower with a prefetch one or two tiles ahead, and the amax pass 4 - 5 %
+// slower, so both are off.  The amax pass with four groups in flight: 2.21
+// ms against 2.25 with two.
 #ifndef FP8OPT_UPD_PREFETCH
 #define FP8OPT_UPD_PREFETCH 0
 #endif
@@ -87,9 +88,9 @@ __device__ __forceinline__ void adamw1(float g, float m, float vp, float wp,
 // SAFE: every finite gradient code unscales to a finite value (decided once
 // per chunk from the largest code), so found_inf only needs the codes.
 // L2: the gradient takes the decay term fma(wd, w, g) (so w is read too).
-// Besides the amax of the first moment (mx) this also reduces max |g| (gx),
-// the input of a scaled second moment's bound.
-template <int GF, bool SAFE, bool L2>
+// Besides the amax of the first moment (mx) this also reduces max |g| (gx)
+// when GX: the input of a scaled second moment's bound.
+template <int GF, bool SAFE, bool L2, bool GX>
 __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
                                  float k, float minv, const StepScalars& s,
                                  uint32_t& mx, uint32_t& gx, uint32_t& bad) {
@@ -127,7 +128,7 @@ __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
           float2 g = mul2(dec2<GF>(code_pair(gc[q], j)), k2);
           if (!SAFE) bad |= nonfinite(g.x) | nonfinite(g.y);
           if (L2) g = fma2(wd2, h2_to_f2(half_pair(wh[q], j)), g);
-          gx = max(gx, max(abs_bits(g.x), abs_bits(g.y)));
+          if (GX) gx = max(gx, max(abs_bits(g.x), abs_bits(g.y)));
           const float2 m = fma2(b1, mul2(dec2<kE4M3>(code_pair(mc[q], j)), minv2),
                                 mul2(omb1, g));
           mx = max(mx, max(abs_bits(m.x), abs_bits(m.y)));
@@ -143,7 +144,7 @@ __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
           float g = __fmul_rn(dec2<GF>(d.g[i]).x, k);
           bad |= nonfinite(g);
           if (L2) g = __fmaf_rn(s.wd, h_to_f(d.w[i]), g);
-          gx = max(gx, abs_bits(g));
+          if (GX) gx = max(gx, abs_bits(g));
           mx = max(mx, abs_bits(m_new1(dec2<kE4M3>(d.m[i]).x, minv, g, s)));
         }
       }
@@ -160,10 +161,18 @@ __device__ __forceinline__ void step_amax_dispatch(const StepDesc& d,
                                                    uint32_t& bad) {
   // The largest finite code gives the largest |g|; rounding is monotonic, so
   // if that product is finite every finite code gives a finite g.
-  if (!nonfinite(__fmul_rn(fp8_max_of<GF>(), k)))
-    thread_step_amax<GF, true, L2>(d, begin, end, k, minv, s, mx, gx, bad);
-  else
-    thread_step_amax<GF, false, L2>(d, begin, end, k, minv, s, mx, gx, bad);
+  const bool safe = !nonfinite(__fmul_rn(fp8_max_of<GF>(), k));
+  if (d.v_bound != nullptr) {
+    if (safe)
+      thread_step_amax<GF, true, L2, true>(d, begin, end, k, minv, s, mx, gx, bad);
+    else
+      thread_step_amax<GF, false, L2, true>(d, begin, end, k, minv, s, mx, gx, bad);
+  } else {
+    if (safe)
+      thread_step_amax<GF, true, L2, false>(d, begin, end, k, minv, s, mx, gx, bad);
+    else
+      thread_step_amax<GF, false, L2, false>(d, begin, end, k, minv, s, mx, gx, bad);
+  }
 }
 
 template <bool L2>
