@@ -136,8 +136,8 @@ def run_whole(bo, cfg, world):
     return dict(w=w, m=m, v=v, w8=w8, w8s=w8s, found=found, norms=norms)
 
 
-@pytest.mark.parametrize("world", [1, 2])
-@pytest.mark.parametrize("case", sorted(CASES))
+@pytest.mark.parametrize("case,world", [(c, w) for c in sorted(CASES) for w in (1, 2)]
+                         + [("o3_clip", 3), ("o2_l2_scaled_v_clip", 3)])
 def test_sharded_equals_whole_and_oracle(bo, case, world):
     cfg = CASES[case]
     whole = run_whole(bo, cfg, world)

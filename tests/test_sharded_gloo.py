@@ -121,16 +121,17 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("case", sorted(CASES))
-def test_two_cpu_ranks_match_the_whole_pipeline(case, tmp_path):
+@pytest.mark.parametrize("case,world", [(c, 2) for c in sorted(CASES)] +
+                         [("o3_clip", 3)])
+def test_cpu_ranks_match_the_whole_pipeline(case, world, tmp_path):
     import torch.multiprocessing as mp
     cfg = CASES[case]
-    mp.spawn(worker, args=(2, free_port(), cfg, str(tmp_path)), nprocs=2,
+    mp.spawn(worker, args=(world, free_port(), cfg, str(tmp_path)), nprocs=world,
              join=True)
-    res = [dict(np.load(tmp_path / f"rank{r}.npz")) for r in range(2)]
-    states, found, norms = reference(cfg)
+    res = [dict(np.load(tmp_path / f"rank{r}.npz")) for r in range(world)]
+    states, found, norms = reference(cfg, world)
     wl = workload()
-    for r in range(2):
+    for r in range(world):
         assert list(res[r]["found"]) == found
         assert np.array_equal(res[r]["norms"], np.array(norms, np.float64))
         for i, st in enumerate(states):
@@ -144,10 +145,10 @@ def test_two_cpu_ranks_match_the_whole_pipeline(case, tmp_path):
                 assert np.array_equal(res[r][f"v{i}"].view(np.uint16), st.v), (r, i)
                 if cfg["level"] == "O3":
                     assert np.array_equal(res[r][f"w{i}"].view(np.uint16), st.w)
-    # each tensor owned by exactly one rank, and both ranks own some
-    owned = [k for r in range(2) for k in res[r] if k.startswith("m")]
+    # each tensor owned by exactly one rank, and every rank owns some
+    owned = [k for r in range(world) for k in res[r] if k.startswith("m")]
     assert sorted(owned) == sorted(f"m{i}" for i in range(len(wl.shapes)))
-    assert all(any(k.startswith("m") for k in res[r]) for r in range(2))
+    assert all(any(k.startswith("m") for k in res[r]) for r in range(world))
     if cfg["inf_at"] is not None:
         assert found[cfg["inf_at"][0] - 1] == 1 and sum(found) == 1
 
