@@ -227,3 +227,24 @@ def test_grad_norm_and_clipped_step_o3_1p3b(bo):
         check_f16(to_np_u16(v[i]), st.v, name=f"v[{i}]")
         check_master(to_np_u16(w[i]), st.w, name=f"master[{i}]")
         check_codes(to_np_u8(w8[i]), st.w8, name=f"w8[{i}]")
+
+
+def test_cast_tensor_above_two_giga_elements(bo):
+    """One BF16 tensor of 2^31 + 12345 elements (past 32-bit indexing):
+    amax and scale bit-exact against the oracle over the whole tensor, and
+    the codes of a strided sample plus the last 40,000 elements."""
+    n = (1 << 31) + 12345
+    g = torch.Generator(device="cuda")
+    g.manual_seed(synth.tensor_seed(7, 0, "grad"))
+    x = (torch.randn(n, generator=g, device="cuda") * 1e-3).to(torch.bfloat16)
+    x[n - 7] = 0.25                       # the largest element, in the tail
+    codes, amax, scale = bo.fp8_cast_scaled([x], "e4m3")
+    torch.cuda.synchronize()
+    host = x.view(torch.int16).cpu().numpy().view(np.uint16)
+    rc, ra, rs = oracle.cast_scaled(host, oracle.BF16, oracle.E4M3)
+    check_f32_exact(amax.cpu().numpy()[:1], [ra], "amax")
+    check_f32_exact(scale.cpu().numpy()[:1], [rs], "scale")
+    got = codes[0]
+    idx = np.concatenate([np.arange(0, n, 9973), np.arange(n - 40000, n)])
+    assert np.array_equal(got[torch.from_numpy(idx).cuda()].cpu().numpy(), rc[idx])
+    assert int(got[n - 7].item()) == 0x7E
