@@ -103,6 +103,8 @@ def lib():
         L.oracle_adam_step_coef.argtypes = [
             C.POINTER(Param), C.c_int, C.c_int, C.c_float, C.c_float, C.c_float,
             C.c_float, C.c_float, C.c_int64, C.c_float, C.c_float]
+        L.oracle_bias_power.restype = C.c_double
+        L.oracle_bias_power.argtypes = [C.c_double, C.c_int64]
         L.oracle_v_scale_from_bound.restype = C.c_float
         L.oracle_v_scale_from_bound.argtypes = [C.c_float]
         L.oracle_state_bytes.restype = C.c_int
@@ -264,6 +266,12 @@ class StepState:
         if self.v_bound is not None:
             p.v_bound = _ptr(self.v_bound)
         return p
+
+
+def bias_power(b: float, t: int) -> float:
+    """beta^t as the step's bias corrections take it (binary exponentiation
+    in double)."""
+    return lib().oracle_bias_power(b, t)
 
 
 def v_scale_from_bound(b: float) -> float:

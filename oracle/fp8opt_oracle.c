@@ -30,7 +30,8 @@
  *     evaluated in fp32 in the order written in oracle_adamw_step below.  The
  *     bias corrections enter as two per-call scalars computed in double and
  *     rounded once: step_size = lr / (1 - beta1^t) and inv_sbc2 =
- *     1 / sqrt(1 - beta2^t).  Dequantization and the GradScaler unscale are
+ *     1 / sqrt(1 - beta2^t), with beta^t by binary exponentiation in double
+ *     (oracle_bias_power).  Dequantization and the GradScaler unscale are
  *     one per-tensor factor k = inv_loss_scale / g_scale.  Where the order
  *     below writes fmaf, the product and sum are rounded once (IEEE fused
  *     multiply-add); every other product and sum is rounded on its own.
@@ -291,6 +292,21 @@ float oracle_v_scale_from_bound(float b)
     return isfinite(q) ? q : 1.0f;
 }
 
+/* beta^t in double by binary exponentiation: from the lowest bit of t up,
+ * r = r * b when the bit is set, then b = b * b, each product rounded to
+ * double.  (libm's pow is not specified to the bit, and platforms differ;
+ * this form gives the same bits wherever double products round to nearest.) */
+double oracle_bias_power(double b, int64_t t)
+{
+    double r = 1.0;
+    while (t > 0) {
+        if (t & 1) r = r * b;
+        b = b * b;
+        t >>= 1;
+    }
+    return r;
+}
+
 /* Per-call scalars.  The bias corrections 1 - beta^t are evaluated in double
  * and enter only through step_size = lr / bc1 and inv_sbc2 = 1 / sqrt(bc2),
  * each rounded to float once. */
@@ -302,8 +318,8 @@ static or_scalars or_make_scalars(float lr, float beta1, float beta2,
                                   float wd, int64_t step, int l2)
 {
     or_scalars s;
-    double bc1 = 1.0 - pow((double)beta1, (double)step);
-    double bc2 = 1.0 - pow((double)beta2, (double)step);
+    double bc1 = 1.0 - oracle_bias_power((double)beta1, step);
+    double bc2 = 1.0 - oracle_bias_power((double)beta2, step);
     s.step_size = (float)((double)lr / bc1);
     s.inv_sbc2 = (float)(1.0 / sqrt(bc2));
     s.omb1 = 1.0f - beta1;

@@ -381,3 +381,21 @@ def test_found_inf_leaves_v_bound_unchanged(orc):
     assert orc.adamw_step(states, 1e-3, 0.9, 0.999, 1e-8, 0.0, 2, 1.0) == 1
     assert np.array_equal(states[0].v_bound, b)
     assert np.array_equal(states[0].v, before.v)
+
+
+def test_bias_power_is_beta_to_the_t(orc):
+    """beta^t by binary exponentiation: exact where every product is exact
+    (powers of two), otherwise within t * 2^-52 relative of the exact power
+    (a rational computed with Python integers)."""
+    from fractions import Fraction
+    for b in (0.5, 0.25, 2.0 ** -10):
+        for t in (1, 2, 3, 10, 77, 1000):
+            assert orc.bias_power(b, t) == b ** t
+    for b in (0.9, 0.999, 0.95, 0.8):
+        for t in (1, 2, 5, 100, 1000, 12345):
+            exact = Fraction(b) ** t
+            if exact < Fraction(1, 2 ** 1000):       # past double's normal range
+                continue
+            got = Fraction(orc.bias_power(b, t))
+            assert abs(got - exact) <= exact * Fraction(t, 2 ** 52)
+    assert orc.bias_power(0.9, 0) == 1.0
