@@ -436,13 +436,26 @@ int check_step_args(const char* fn, const fp8opt_param* params, int n,
   return FP8OPT_OK;
 }
 
+// beta^t in double by binary exponentiation (each product rounded to
+// double): the same bits on every platform, and the same as a device kernel
+// computing it with the same products.
+double bias_power(double b, int64_t t) {
+  double r = 1.0;
+  while (t > 0) {
+    if (t & 1) r = r * b;
+    b = b * b;
+    t >>= 1;
+  }
+  return r;
+}
+
 // Per-call scalars: the bias corrections 1 - beta^t in double, entering only
 // through lr / bc1 and 1 / sqrt(bc2), each rounded to fp32 once.
 StepScalars make_scalars(float lr, float beta1, float beta2, float eps, float wd,
                          int64_t step, float inv_loss_scale, bool l2) {
   StepScalars s;
-  const double bc1 = 1.0 - std::pow((double)beta1, (double)step);
-  const double bc2 = 1.0 - std::pow((double)beta2, (double)step);
+  const double bc1 = 1.0 - bias_power((double)beta1, step);
+  const double bc2 = 1.0 - bias_power((double)beta2, step);
   s.beta1 = beta1;
   s.beta2 = beta2;
   s.eps = eps;
