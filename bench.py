@@ -173,70 +173,199 @@ class ClockSampler:
 
 # ------------------------------------------------------------ oracle leg
 
-def oracle_sample(wl, budget_s: float):
-    """Tensors of ``wl`` forming a bounded sample: small ones first (the tail,
-    norms, biases), then whole matrices while the estimated oracle time (about
-    5 M params/s for cast + step) stays within budget_s."""
+def oracle_sample(wl, budget_s: float, parts: int = 1):
+    """A bounded sample of ``wl`` as (tensor, elements) entries: small tensors
+    first (the tail, norms, biases), then whole matrices, while the estimated
+    oracle time (about 5 M params/s for cast + step) stays within budget_s.
+    For a sample split over ``parts`` processes no entry is larger than one
+    process's share: what budget is left then takes the leading share of the
+    next larger tensors, each entry a tensor of its own."""
     order = sorted(range(len(wl.shapes)), key=lambda i: wl.numels[i])
     limit = max(1, int(budget_s * 5e6))
+    cap = max(1, limit // parts)
     chosen, total = [], 0
     for i in order:
-        if total + wl.numels[i] > limit and chosen:
+        n = wl.numels[i]
+        if (total + n > limit or n > cap) and chosen:
             continue
-        chosen.append(i)
-        total += wl.numels[i]
+        chosen.append((i, n))
+        total += n
+    if parts > 1:
+        taken = {i for i, _ in chosen}
+        for i in order:
+            if total + cap > limit:
+                break
+            if i not in taken and wl.numels[i] > cap:
+                chosen.append((i, cap))
+                total += cap
     return sorted(chosen), total
 
 
-def oracle_step_time(wl, idx, step):
-    """Wall time of one oracle cast + step over tensors idx (single thread)."""
+def _oracle_states(wl, entries):
+    """Fresh oracle optimizer state (m = v = 0, the workload's weights) for
+    the sample's entries."""
     import numpy as np
     import torch
     import oracle
     fmt = oracle.FMT[wl.grad_fmt]
     states = []
-    grads = []
-    for i in idx:
-        g = wl.grad(i, step).contiguous()
-        grads.append(g)
-        w = wl.weight(i).contiguous().view(torch.int16).numpy().view(np.uint16)
-        n = wl.numels[i]
+    for i, n in entries:
+        w = wl.weight(i).reshape(-1)[:n].contiguous()
+        w = w.view(torch.int16).numpy().view(np.uint16)
         states.append(oracle.StepState(np.zeros(n, np.uint8), 1.0,
                                        np.zeros(n, np.uint8), 1.0,
                                        np.zeros(n, np.uint16), w, g_fmt=fmt,
                                        o3=wl.level == "O3"))
+    return states
+
+
+def _oracle_grads(wl, entries, step):
+    """The gradients of the sample's entries at ``step`` as the oracle's raw
+    arrays."""
+    import numpy as np
+    import torch
+    out = []
+    for i, n in entries:
+        g = wl.grad(i, step).reshape(-1)[:n].contiguous()
+        out.append(g.numpy() if g.dtype == torch.float32 else
+                   g.view(torch.int16).numpy().view(np.uint16))
+    return out
+
+
+def _oracle_cast_step(wl, states, srcs, step):
+    """One oracle cast + AdamW step of the given tensors (timed work)."""
+    import torch
+    import oracle
+    fmt = oracle.FMT[wl.grad_fmt]
     dt = {torch.float32: oracle.F32, torch.bfloat16: oracle.BF16,
           torch.float16: oracle.F16}[wl.grad_dtype]
-    srcs = [g.numpy() if g.dtype == torch.float32 else
-            g.view(torch.int16).numpy().view(np.uint16) for g in grads]
-    t0 = time.perf_counter()
-    for s, src in zip(states, srcs):
+    for st, src in zip(states, srcs):
         c, _, sc = oracle.cast_scaled(src, dt, fmt)
-        s.g, s.g_scale = c, float(sc)
+        st.g, st.g_scale = c, float(sc)
     oracle.adamw_step(states, wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, step,
                       wl.inv_loss_scale)
+
+
+def oracle_step_time(wl, entries, step):
+    """Wall time of one oracle cast + step over the entries (single thread)."""
+    states = _oracle_states(wl, entries)
+    srcs = _oracle_grads(wl, entries, step)
+    t0 = time.perf_counter()
+    _oracle_cast_step(wl, states, srcs, step)
     return time.perf_counter() - t0
 
 
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _split_by_size(entries, parts: int):
+    """The entries dealt to ``parts`` lists, largest first onto the lightest."""
+    lists = [[] for _ in range(parts)]
+    load = [0] * parts
+    for e in sorted(entries, key=lambda e: -e[1]):
+        r = load.index(min(load))
+        lists[r].append(e)
+        load[r] += e[1]
+    return [sorted(x) for x in lists if x]
+
+
+def _oracle_worker(wl, entries, steps, barrier, out):
+    """One process of the parallel oracle: its own entries and state, kept
+    across steps.  The gradients of step 1 are made once, before the first
+    common start, and serve every step (the oracle's work per element does
+    not depend on their values)."""
+    import torch
+    torch.set_num_threads(1)
+    states = _oracle_states(wl, entries)
+    srcs = _oracle_grads(wl, entries, 1)
+    for k in range(steps):
+        barrier.wait()
+        t0 = time.perf_counter()
+        _oracle_cast_step(wl, states, srcs, k + 1)
+        out.put((k, t0, time.perf_counter()))
+    barrier.wait()
+
+
+def oracle_parallel_times(wl, entries, steps: int, procs: int):
+    """Wall time of each of ``steps`` oracle cast + steps over the entries,
+    split over ``procs`` spawned processes that start each step together: the
+    step ends when the last process does.  Tensors are independent apart from
+    found_inf, which no timed workload sets, so the results equal one
+    process's."""
+    import multiprocessing as mp
+    import queue
+    ctx = mp.get_context("spawn")
+    parts = _split_by_size(entries, procs)
+    barrier = ctx.Barrier(len(parts))
+    out = ctx.Queue()
+    ps = [ctx.Process(target=_oracle_worker, args=(wl, part, steps, barrier, out),
+                      daemon=True) for part in parts]
+    for p in ps:
+        p.start()
+    t0 = [math.inf] * steps
+    t1 = [0.0] * steps
+    try:
+        got = 0
+        while got < steps * len(parts):
+            try:
+                k, a, b = out.get(timeout=1.0)
+            except queue.Empty:
+                dead = [p.exitcode for p in ps if p.exitcode not in (None, 0)]
+                if dead:
+                    raise RuntimeError(f"oracle process exited with {dead[0]}")
+                continue
+            t0[k] = min(t0[k], a)
+            t1[k] = max(t1[k], b)
+            got += 1
+    finally:
+        for p in ps:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.terminate()
+    return [b - a for a, b in zip(t0, t1)], len(parts)
+
+
+def _describe(wl, entries, total):
+    whole = sum(1 for i, n in entries if n == wl.numels[i])
+    return (f"{len(entries)} tensors of {len(wl.shapes)}: {whole} whole, "
+            f"{len(entries) - whole} leading slices ({total} params)")
+
+
 def cpu_baseline(wl, budget_s: float):
-    idx, total = oracle_sample(wl, budget_s)
-    secs = oracle_step_time(wl, idx, 1)
-    return {"value": total / secs / 1e9, "unit": UNIT, "cores": 1,
+    """The oracle on the host cores: one process on a sample of about
+    budget_s / 2 of single-thread work, then every core on a sample that
+    many times larger."""
+    e1, total1 = oracle_sample(wl, budget_s / 2)
+    secs1 = oracle_step_time(wl, e1, 1)
+    cores = host_cores()
+    entries, total = oracle_sample(wl, budget_s / 2 * cores, cores)
+    times, used = oracle_parallel_times(wl, entries, 1, cores)
+    secs = times[0]
+    return {"value": total / secs / 1e9, "unit": UNIT, "cores": used,
             "kind": "oracle",
-            "sample": f"1 cast+step over {len(idx)} of {len(wl.shapes)} tensors "
-                      f"({total} params, {secs:.1f} s, single thread)"}
+            "sample": f"1 cast+step over {_describe(wl, entries, total)}, "
+                      f"{secs:.1f} s, split by tensor over {used} processes",
+            "single_thread": {"value": total1 / secs1 / 1e9, "unit": UNIT,
+                              "cores": 1,
+                              "sample": f"1 cast+step over "
+                                        f"{_describe(wl, e1, total1)}, "
+                                        f"{secs1:.1f} s"}}
 
 
 def run_reference(args, wl):
     rank, world, _ = dist_env()
     if rank != 0:
         return
+    cores = host_cores()
     per_step = max(1.0, 90.0 / max(1, args.steps + args.warmup))
-    idx, total = oracle_sample(wl, per_step)
-    for w in range(args.warmup):
-        oracle_step_time(wl, idx, w + 1)
-    times = [oracle_step_time(wl, idx, args.warmup + k + 1) for k in range(args.steps)]
-    secs = sum(times)
+    entries, total = oracle_sample(wl, per_step * cores, cores)
+    times, used = oracle_parallel_times(wl, entries, args.warmup + args.steps,
+                                        cores)
+    secs = sum(times[args.warmup:])
     value = total * args.steps / secs / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
@@ -244,9 +373,12 @@ def run_reference(args, wl):
         "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": workload_desc(wl),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"each step: cast+step over {len(idx)} of "
-                                   f"{len(wl.shapes)} tensors ({total} params)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used,
+                         "kind": "oracle",
+                         "sample": f"each step: cast+step over "
+                                   f"{_describe(wl, entries, total)}, split by "
+                                   f"tensor over {used} processes, the step-1 "
+                                   f"gradients in every step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
