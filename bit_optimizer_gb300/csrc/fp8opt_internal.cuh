@@ -379,8 +379,9 @@ __device__ __forceinline__ bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
-// Max over the CTA of a per-thread uint32; the result is valid in thread 0.
-// Every thread of the CTA must call it.
+// Max over the CTA (NT threads) of a per-thread uint32; the result is valid
+// in thread 0.  Every thread of the CTA must call it.
+template <int NT = kThreads>
 __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* smem) {
   v = __reduce_max_sync(0xFFFFFFFFu, v);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -388,7 +389,7 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* smem) {
   if (lane == 0) smem[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    v = lane < (kThreads / 32) ? smem[lane] : 0u;
+    v = lane < (NT / 32) ? smem[lane] : 0u;
     v = __reduce_max_sync(0xFFFFFFFFu, v);
   }
   return v;

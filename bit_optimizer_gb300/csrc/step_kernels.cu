@@ -42,16 +42,22 @@ namespace fp8opt {
 namespace {
 
 // Tunables (compile-time): 8-element groups each thread keeps in flight per
-// tile in the amax and update passes, and the update kernel's resident CTAs
-// per SM (which caps its registers a thread).
+// tile in the amax and update passes, and the update kernel's CTA size and
+// resident CTAs per SM (which cap its registers a thread).  The update kernel
+// is latency-bound, so what counts is the warps an SM holds: at 72 registers
+// an SM holds 28 warps as seven CTAs of 128 threads but 24 as three of 256
+// (76 registers).  Measured on the 6.7B list: 11.56 ms against 12.16 ms.
 #ifndef FP8OPT_STEP_AMAX_GROUPS
 #define FP8OPT_STEP_AMAX_GROUPS 4
 #endif
 #ifndef FP8OPT_UPD_GROUPS
 #define FP8OPT_UPD_GROUPS 2
 #endif
+#ifndef FP8OPT_UPD_THREADS
+#define FP8OPT_UPD_THREADS 128
+#endif
 #ifndef FP8OPT_UPD_MIN_BLOCKS
-#define FP8OPT_UPD_MIN_BLOCKS 3
+#define FP8OPT_UPD_MIN_BLOCKS 7
 #endif
 // Tiles ahead of the current one that the update and amax passes prefetch
 // into L2 (0: none).  Measured on the 6.7B list: the update pass is 7 %
@@ -66,6 +72,7 @@ namespace {
 #endif
 constexpr int kAmaxGroups = FP8OPT_STEP_AMAX_GROUPS;
 constexpr int kUpdGroups = FP8OPT_UPD_GROUPS;
+constexpr int kUpdThreads = FP8OPT_UPD_THREADS;
 constexpr int kW8Groups = 2;
 
 // The scalar forms of the lines above (tails and unaligned tensors).
@@ -290,7 +297,7 @@ template <int GF, bool O3, bool MCHECK, bool VS, bool L2>
 __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
                               float k, float minv, float msc, float vinv,
                               float vsc, const StepScalars& s, uint32_t& hmax) {
-  constexpr int64_t kTile = (int64_t)kThreads * kGroup * kUpdGroups;
+  constexpr int64_t kTile = (int64_t)kUpdThreads * kGroup * kUpdGroups;
   const int tid = threadIdx.x;
   const bool vec = d.vec_ok != 0;
   // built here, so an instantiation keeps only the constants it uses
@@ -316,7 +323,7 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
       uint4 vh[kUpdGroups], wh[kUpdGroups];
 #pragma unroll
       for (int q = 0; q < kUpdGroups; ++q) {
-        const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
+        const int64_t i0 = base + q * (kUpdThreads * kGroup) + tid * kGroup;
         gc[q] = ld_once2(d.g + i0);
         mc[q] = ld_once2(d.m + i0);
         vh[q] = ld_once4(d.v + i0);
@@ -324,7 +331,7 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
       }
 #pragma unroll
       for (int q = 0; q < kUpdGroups; ++q) {
-        const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
+        const int64_t i0 = base + q * (kUpdThreads * kGroup) + tid * kGroup;
         uint2 mo;
         uint4 vo, wo;
         update8<GF, O3, MCHECK, VS, L2>(gc[q], mc[q], vh[q], wh[q], c, mo, vo, wo,
@@ -336,7 +343,7 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
     } else {
 #pragma unroll 1
       for (int q = 0; q < kUpdGroups; ++q) {
-        const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
+        const int64_t i0 = base + q * (kUpdThreads * kGroup) + tid * kGroup;
         for (int j = 0; j < kGroup; ++j) {
           const int64_t i = i0 + j;
           if (i >= end) break;
@@ -418,12 +425,12 @@ __device__ __forceinline__ bool found_set(const StepScratch& sc, uint32_t epoch)
 // scaled second moment; L2: Adam with L2 decay.  Separate instantiations keep
 // the plain AdamW kernel free of the other variants' registers.
 template <bool ANY_VS, bool L2>
-__global__ void __launch_bounds__(kThreads, FP8OPT_UPD_MIN_BLOCKS)
+__global__ void __launch_bounds__(kUpdThreads, FP8OPT_UPD_MIN_BLOCKS)
 step_update_kernel(const StepDesc* __restrict__ descs,
                    const Chunk* __restrict__ chunks, uint32_t nchunks,
                    StepScratch sc, StepScalars s, uint32_t epoch,
                    uint32_t* found_dev) {
-  __shared__ uint32_t red[kThreads / 32];
+  __shared__ uint32_t red[kUpdThreads / 32];
   const bool found = found_set(sc, epoch);
   if (found_dev != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
     *found_dev = found ? 1u : 0u;
@@ -461,7 +468,7 @@ step_update_kernel(const StepDesc* __restrict__ descs,
                                          mcheck, s, hmax);
     if (d.o3) {   // uniform over the CTA
       uint32_t h = max(hmax & 0xFFFFu, hmax >> 16);
-      h = block_max_u32(h, red);
+      h = block_max_u32<kUpdThreads>(h, red);
       if (threadIdx.x == 0 && h != 0) {
         const uint32_t fb = h > 0x7C00u ? 0x7FC00000u
                                         : __float_as_uint(h_to_f((uint16_t)h));
@@ -552,16 +559,16 @@ cudaError_t launch_step_update(const StepDesc* descs, const Chunk* chunks,
   if (mark) mark(kStepUpdateK, 0, stream);
   const uint32_t g = grid_min((uint32_t)grid_update, nchunks);
   if (any_vs && s.l2)
-    step_update_kernel<true, true><<<g, kThreads, 0, stream>>>(
+    step_update_kernel<true, true><<<g, kUpdThreads, 0, stream>>>(
         descs, chunks, nchunks, sc, s, epoch, found_dev);
   else if (any_vs)
-    step_update_kernel<true, false><<<g, kThreads, 0, stream>>>(
+    step_update_kernel<true, false><<<g, kUpdThreads, 0, stream>>>(
         descs, chunks, nchunks, sc, s, epoch, found_dev);
   else if (s.l2)
-    step_update_kernel<false, true><<<g, kThreads, 0, stream>>>(
+    step_update_kernel<false, true><<<g, kUpdThreads, 0, stream>>>(
         descs, chunks, nchunks, sc, s, epoch, found_dev);
   else
-    step_update_kernel<false, false><<<g, kThreads, 0, stream>>>(
+    step_update_kernel<false, false><<<g, kUpdThreads, 0, stream>>>(
         descs, chunks, nchunks, sc, s, epoch, found_dev);
   if (mark) mark(kStepUpdateK, 1, stream);
   if (nchunks_o3 != 0) {
@@ -616,7 +623,7 @@ cudaError_t step_occupancy(int* amax_per_sm, int* update_per_sm,
       amax_per_sm, step_amax_kernel<false>, kThreads, 0);
   if (e != cudaSuccess) return e;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      update_per_sm, step_update_kernel<false, false>, kThreads, 0);
+      update_per_sm, step_update_kernel<false, false>, kUpdThreads, 0);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(w8_per_sm,
                                                        step_w8_kernel, kThreads, 0);
