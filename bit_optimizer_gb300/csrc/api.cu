@@ -58,7 +58,8 @@ cudaError_t launch_reduce(const ReduceDesc* descs, const Chunk* chunks,
                           float post, int grid_amax, int grid_encode,
                           const ReduceNorm* norm, cudaStream_t stream,
                           LaunchMark mark);
-cudaError_t reduce_occupancy(int* amax_per_sm, int* encode_per_sm);
+cudaError_t reduce_occupancy(int* amax_per_sm, int* amax_small_per_sm,
+                             int* encode_per_sm, int* encode_small_per_sm);
 cudaError_t reduce_encode_sq_occupancy(int* per_sm);
 cudaError_t launch_grad_norm_terms(const StepDesc* descs, const Chunk* chunks,
                                    uint32_t nchunks, int n, float ils,
@@ -135,7 +136,8 @@ struct DeviceInfo {
   int cast_amax = 0, cast_encode = 0;          // persistent grid sizes
   int step_amax = 0, step_update = 0, step_w8 = 0;
   int cast_step = 0;
-  int reduce_amax = 0, reduce_encode = 0;
+  int reduce_amax = 0, reduce_amax_small = 0;
+  int reduce_encode = 0, reduce_encode_small = 0;
   int grad_norm = 0;
   int cast_encode_sq = 0, reduce_encode_sq = 0;
 };
@@ -218,8 +220,11 @@ cudaError_t device_info(int dev, DeviceInfo** out) {
   info.step_w8 = info.sms * (c > 0 ? c : 1);
   if ((e = cast_step_occupancy(&a)) != cudaSuccess) return e;
   info.cast_step = info.sms * (a > 0 ? a : 1);
-  if ((e = reduce_occupancy(&a, &b)) != cudaSuccess) return e;
+  int d = 0;
+  if ((e = reduce_occupancy(&a, &c, &b, &d)) != cudaSuccess) return e;
   info.reduce_amax = info.sms * (a > 0 ? a : 1);
+  info.reduce_amax_small = info.sms * (c > 0 ? c : 1);
+  info.reduce_encode_small = info.sms * (d > 0 ? d : 1);
   info.reduce_encode = info.sms * (b > 0 ? b : 1);
   if ((e = grad_norm_occupancy(&a)) != cudaSuccess) return e;
   info.grad_norm = info.sms * (a > 0 ? a : 1);
@@ -729,8 +734,10 @@ int reduce_call(const char* fn, const fp8opt_reduce_item* items, int n, int k,
   e = launch_reduce(static_cast<const ReduceDesc*>(ws->reduce_descs.ptr),
                     static_cast<const Chunk*>(ws->reduce_chunks.ptr),
                     ws->reduce_nchunks, slots, epoch, k, in_fmt, out_fmt, post,
-                    info->reduce_amax,
-                    with_norm ? info->reduce_encode_sq : info->reduce_encode,
+                    k <= 2 ? info->reduce_amax_small : info->reduce_amax,
+                    with_norm ? info->reduce_encode_sq
+                    : k <= 2  ? info->reduce_encode_small
+                              : info->reduce_encode,
                     with_norm ? &norm : nullptr, stream, launch_mark());
   if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
   return FP8OPT_OK;

@@ -12,7 +12,9 @@
 //                         again, code = encode(y * scale).  It walks the
 //                         chunk table backwards so the chunks the first pass
 //                         read last are still in L2.
-// Bytes per element: k (first pass) + k + 1 (encode).
+// Bytes per element: k (first pass) + k + 1 (encode).  With one or two
+// shards both passes run in forms specialised on k (reduce_amax_small_kernel,
+// reduce_encode_small_kernel).
 //
 // Vector path: thread t of a CTA takes the 16-code groups at tile + g *
 // (kThreads * 16) + t * 16 (g = 0, 1): one 16-byte load per shard and group,
@@ -42,6 +44,16 @@ namespace {
 #endif
 #ifndef FP8OPT_REDUCE_PREFETCH
 #define FP8OPT_REDUCE_PREFETCH 1
+#endif
+// The first pass for one or two shards: 16-code groups per thread per tile
+// and resident CTAs per SM.  Measured on the 124M list with two shards (the
+// whole reduction): 0.111 ms with two groups and 4 CTAs/SM, 0.113 with four
+// groups (3 or 4 CTAs/SM), 0.119 on the general kernel.
+#ifndef FP8OPT_RSMALL_GROUPS
+#define FP8OPT_RSMALL_GROUPS 2
+#endif
+#ifndef FP8OPT_RSMALL_MIN_BLOCKS
+#define FP8OPT_RSMALL_MIN_BLOCKS 4
 #endif
 
 constexpr int kRGroup = 16;    // codes per vector group (one 16-byte access)
@@ -204,6 +216,96 @@ reduce_amax_kernel(const ReduceDesc* __restrict__ descs,
   }
 }
 
+constexpr int kSGroups = FP8OPT_RSMALL_GROUPS;
+constexpr int64_t kSTile = (int64_t)kThreads * kRGroup * kSGroups;
+
+// The first pass for K = 1 or 2 shards.  Every shard's loads for all the
+// tile's groups are issued first. Each group's sum is then reduced to its max
+// at once, not kept for the encode.  A thread thus keeps K * kSGroups 16-byte
+// loads in flight in few registers, and four CTAs fit on an SM.  The sum is
+// the same expression as in reduce_groups, so y and its max are identical.
+template <int IN, int K>
+__global__ void __launch_bounds__(kThreads, FP8OPT_RSMALL_MIN_BLOCKS)
+reduce_amax_small_kernel(const ReduceDesc* __restrict__ descs,
+                         const Chunk* __restrict__ chunks, uint32_t nchunks,
+                         float post, unsigned long long* __restrict__ slots,
+                         uint32_t epoch) {
+  __shared__ uint32_t red[kThreads / 32];
+  __shared__ float r_s[kMaxShards];
+  const int tid = threadIdx.x;
+  const float2 pp = splat2(post);
+  for (uint32_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+    const Chunk ch = chunks[c];
+    const ReduceDesc d = descs[ch.tensor];
+    load_reciprocals(d, K, r_s);
+    float r[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) r[j] = r_s[j];
+    const int64_t begin = (int64_t)ch.index * kChunkElems;
+    const int64_t end = min(begin + kChunkElems, d.numel);
+    const bool vec = d.vec_ok != 0;
+    uint32_t mx = 0;
+#pragma unroll 1
+    for (int64_t base = begin; base < end; base += kSTile) {
+      if (vec && base + kSTile <= end) {
+        if (FP8OPT_REDUCE_PREFETCH > 0 && tid == 0) {
+          const int64_t ahead = base + FP8OPT_REDUCE_PREFETCH * kSTile;
+          if (ahead + kSTile <= end)
+            for (int j = 0; j < K; ++j)
+              prefetch_l2(d.src + (int64_t)j * d.stride + ahead, (uint32_t)kSTile);
+        }
+        uint4 cv[K][kSGroups];
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+#pragma unroll
+          for (int g = 0; g < kSGroups; ++g)
+            cv[j][g] = ld_keep4(d.src + (int64_t)j * d.stride + base +
+                                g * (kThreads * kRGroup) + tid * kRGroup);
+#pragma unroll
+        for (int g = 0; g < kSGroups; ++g) {
+          float2 y[8];
+          accum16<IN, true>(cv[0][g], r[0], y);
+#pragma unroll
+          for (int j = 1; j < K; ++j) accum16<IN, false>(cv[j][g], r[j], y);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float2 t = mul2(y[q], pp);
+            mx = max(mx, max(abs_bits(t.x), abs_bits(t.y)));
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int g = 0; g < kSGroups; ++g) {
+          const int64_t i0 = base + g * (kThreads * kRGroup) + tid * kRGroup;
+          for (int e = 0; e < kRGroup; ++e) {
+            const int64_t i = i0 + e;
+            if (i >= end) break;
+            mx = max(mx, abs_bits(reduce_one<IN>(d.src, d.stride, K, r_s, post, i)));
+          }
+        }
+      }
+    }
+    mx = block_max_u32(mx, red);
+    if (threadIdx.x == 0 && mx != 0)
+      atomicMax(&slots[ch.tensor], slot_tag(epoch, canon_amax_bits(mx)));
+  }
+}
+
+template <int IN>
+void launch_amax(uint32_t grid, const ReduceDesc* descs, const Chunk* chunks,
+                 uint32_t nchunks, int k, float post, unsigned long long* slots,
+                 uint32_t epoch, cudaStream_t stream) {
+  if (k == 1)
+    reduce_amax_small_kernel<IN, 1><<<grid, kThreads, 0, stream>>>(
+        descs, chunks, nchunks, post, slots, epoch);
+  else if (k == 2)
+    reduce_amax_small_kernel<IN, 2><<<grid, kThreads, 0, stream>>>(
+        descs, chunks, nchunks, post, slots, epoch);
+  else
+    reduce_amax_kernel<IN><<<grid, kThreads, 0, stream>>>(descs, chunks, nchunks,
+                                                          k, post, slots, epoch);
+}
+
 // -------------------------------------------------------------- encode pass
 
 // Sixteen finite y -> sixteen codes of format OUT in a uint4.
@@ -266,6 +368,62 @@ __device__ void thread_reduce_encode(const ReduceDesc& d, int k,
   }
 }
 
+// The encode pass's vector path for K = 1 or 2 shards (finite amax): like
+// reduce_amax_small_kernel, all loads of the tile first, then each group is
+// summed, encoded and stored at once.
+template <int IN, int OUT, int K>
+__device__ void thread_reduce_encode_small(const ReduceDesc& d, const float* r_s,
+                                           float post, float scale,
+                                           int64_t begin, int64_t end) {
+  const int tid = threadIdx.x;
+  const bool vec = d.vec_ok != 0;
+  const float2 pp = splat2(post);
+  float r[K];
+#pragma unroll
+  for (int j = 0; j < K; ++j) r[j] = r_s[j];
+#pragma unroll 1
+  for (int64_t base = begin; base < end; base += kSTile) {
+    if (vec && base + kSTile <= end) {
+      if (FP8OPT_REDUCE_PREFETCH > 0 && tid == 0) {
+        const int64_t ahead = base + FP8OPT_REDUCE_PREFETCH * kSTile;
+        if (ahead + kSTile <= end)
+          for (int j = 0; j < K; ++j)
+            prefetch_l2(d.src + (int64_t)j * d.stride + ahead, (uint32_t)kSTile);
+      }
+      uint4 cv[K][kSGroups];
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+#pragma unroll
+        for (int g = 0; g < kSGroups; ++g)
+          cv[j][g] = ld_once4(d.src + (int64_t)j * d.stride + base +
+                              g * (kThreads * kRGroup) + tid * kRGroup);
+#pragma unroll
+      for (int g = 0; g < kSGroups; ++g) {
+        float2 y[8];
+        accum16<IN, true>(cv[0][g], r[0], y);
+#pragma unroll
+        for (int j = 1; j < K; ++j) accum16<IN, false>(cv[j][g], r[j], y);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) y[q] = mul2(y[q], pp);
+        *reinterpret_cast<uint4*>(d.codes + base + g * (kThreads * kRGroup) +
+                                  tid * kRGroup) = encode16<OUT>(y, scale);
+      }
+    } else {
+#pragma unroll 1
+      for (int g = 0; g < kSGroups; ++g) {
+        const int64_t i0 = base + g * (kThreads * kRGroup) + tid * kRGroup;
+        for (int e = 0; e < kRGroup; ++e) {
+          const int64_t i = i0 + e;
+          if (i >= end) break;
+          const float t =
+              __fmul_rn(reduce_one<IN>(d.src, d.stride, K, r_s, post, i), scale);
+          d.codes[i] = (uint8_t)(enc2<OUT>(t, 0.0f) & 0xFFu);
+        }
+      }
+    }
+  }
+}
+
 // Where an encode pass also sums the exact squares of the codes it writes
 // (the gradient norm of the reduced tensors): the 128-bit slots, the
 // found_inf slot and the inverse loss scale.
@@ -275,7 +433,9 @@ struct RedSq {
   float ils;
 };
 
-template <int IN, int OUT, bool SQ>
+// KS: 0, or the number of shards (1 or 2) the vector path is specialised on
+// (plain encode only).
+template <int IN, int OUT, bool SQ, int KS>
 __device__ __forceinline__ void encode_pass(const ReduceDesc* __restrict__ descs,
                                             const Chunk* __restrict__ chunks,
                                             uint32_t nchunks, int k, float post,
@@ -298,6 +458,9 @@ __device__ __forceinline__ void encode_pass(const ReduceDesc* __restrict__ descs
     SqAcc<OUT> acc;
     if (ab >= 0x7F800000u)
       thread_reduce_encode<IN, OUT, true, SQ>(d, k, r_s, post, scale, begin, end, acc);
+    else if (KS > 0)
+      thread_reduce_encode_small<IN, OUT, (KS > 0 ? KS : 1)>(d, r_s, post, scale,
+                                                            begin, end);
     else
       thread_reduce_encode<IN, OUT, false, SQ>(d, k, r_s, post, scale, begin, end, acc);
     if (SQ)
@@ -314,8 +477,20 @@ reduce_encode_kernel(const ReduceDesc* __restrict__ descs,
                      uint32_t epoch) {
   __shared__ float r_s[kMaxShards];
   const RedSq none = {nullptr, nullptr, 0.0f};
-  encode_pass<IN, OUT, false>(descs, chunks, nchunks, k, post, slots, epoch,
-                              none, r_s, nullptr, nullptr);
+  encode_pass<IN, OUT, false, 0>(descs, chunks, nchunks, k, post, slots, epoch,
+                                 none, r_s, nullptr, nullptr);
+}
+
+template <int IN, int OUT, int K>
+__global__ void __launch_bounds__(kThreads, FP8OPT_RSMALL_MIN_BLOCKS)
+reduce_encode_small_kernel(const ReduceDesc* __restrict__ descs,
+                           const Chunk* __restrict__ chunks, uint32_t nchunks,
+                           float post, const unsigned long long* __restrict__ slots,
+                           uint32_t epoch) {
+  __shared__ float r_s[kMaxShards];
+  const RedSq none = {nullptr, nullptr, 0.0f};
+  encode_pass<IN, OUT, false, K>(descs, chunks, nchunks, K, post, slots, epoch,
+                                 none, r_s, nullptr, nullptr);
 }
 
 // (the exact squares need more registers than the plain pass: two CTAs per
@@ -329,8 +504,8 @@ reduce_encode_sq_kernel(const ReduceDesc* __restrict__ descs,
   __shared__ float r_s[kMaxShards];
   __shared__ unsigned long long red64[2 * (kThreads / 32)];
   __shared__ uint32_t red32[kThreads / 32];
-  encode_pass<IN, OUT, true>(descs, chunks, nchunks, k, post, slots, epoch, sq,
-                             r_s, red64, red32);
+  encode_pass<IN, OUT, true, 0>(descs, chunks, nchunks, k, post, slots, epoch, sq,
+                                r_s, red64, red32);
 }
 
 // Per-item norm terms of the reduced tensors (k = ils / the output scale);
@@ -354,7 +529,23 @@ void launch_encode(uint32_t grid, const ReduceDesc* descs, const Chunk* chunks,
                    uint32_t nchunks, int k, float post,
                    const unsigned long long* slots, uint32_t epoch, int out_fmt,
                    const RedSq* sq, cudaStream_t stream) {
-  if (sq == nullptr) {
+  if (sq == nullptr && k <= 2) {
+    if (out_fmt == kE4M3) {
+      if (k == 1)
+        reduce_encode_small_kernel<IN, kE4M3, 1><<<grid, kThreads, 0, stream>>>(
+            descs, chunks, nchunks, post, slots, epoch);
+      else
+        reduce_encode_small_kernel<IN, kE4M3, 2><<<grid, kThreads, 0, stream>>>(
+            descs, chunks, nchunks, post, slots, epoch);
+    } else {
+      if (k == 1)
+        reduce_encode_small_kernel<IN, kE5M2, 1><<<grid, kThreads, 0, stream>>>(
+            descs, chunks, nchunks, post, slots, epoch);
+      else
+        reduce_encode_small_kernel<IN, kE5M2, 2><<<grid, kThreads, 0, stream>>>(
+            descs, chunks, nchunks, post, slots, epoch);
+    }
+  } else if (sq == nullptr) {
     if (out_fmt == kE4M3)
       reduce_encode_kernel<IN, kE4M3><<<grid, kThreads, 0, stream>>>(
           descs, chunks, nchunks, k, post, slots, epoch);
@@ -373,7 +564,9 @@ void launch_encode(uint32_t grid, const ReduceDesc* descs, const Chunk* chunks,
 
 }  // namespace
 
-// Launches both passes on `stream`; 1 <= k <= kMaxShards.  With norm set,
+// Launches both passes on `stream`; 1 <= k <= kMaxShards.  With k <= 2 the
+// grids are sized for the small-k kernels (the first pass, and the encode
+// pass when no norm is asked for).  With norm set,
 // the encode pass also sums the exact squares of the codes it writes into
 // norm->sums (2n zeroed words; found_inf into norm->found), and a last kernel
 // writes each item's norm term and the found flag.
@@ -388,11 +581,9 @@ cudaError_t launch_reduce(const ReduceDesc* descs, const Chunk* chunks,
   const uint32_t ge = grid_min((uint32_t)grid_encode, nchunks);
   if (mark) mark(kReduceAmaxK, 0, stream);
   if (in_fmt == kE4M3)
-    reduce_amax_kernel<kE4M3><<<ga, kThreads, 0, stream>>>(descs, chunks, nchunks,
-                                                           k, post, slots, epoch);
+    launch_amax<kE4M3>(ga, descs, chunks, nchunks, k, post, slots, epoch, stream);
   else
-    reduce_amax_kernel<kE5M2><<<ga, kThreads, 0, stream>>>(descs, chunks, nchunks,
-                                                           k, post, slots, epoch);
+    launch_amax<kE5M2>(ga, descs, chunks, nchunks, k, post, slots, epoch, stream);
   if (mark) mark(kReduceAmaxK, 1, stream);
   if (mark) mark(kReduceEncodeK, 0, stream);
   RedSq sq;
@@ -420,10 +611,18 @@ cudaError_t reduce_encode_sq_occupancy(int* per_sm) {
       per_sm, reduce_encode_sq_kernel<kE4M3, kE4M3>, kThreads, 0);
 }
 
-// Resident CTAs per SM of the two reduction kernels.
-cudaError_t reduce_occupancy(int* amax_per_sm, int* encode_per_sm) {
+// Resident CTAs per SM of the reduction kernels: the first and the encode
+// pass, each in its general and its small-k form.
+cudaError_t reduce_occupancy(int* amax_per_sm, int* amax_small_per_sm,
+                             int* encode_per_sm, int* encode_small_per_sm) {
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       amax_per_sm, reduce_amax_kernel<kE4M3>, kThreads, 0);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      amax_small_per_sm, reduce_amax_small_kernel<kE4M3, 2>, kThreads, 0);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      encode_small_per_sm, reduce_encode_small_kernel<kE4M3, kE4M3, 2>, kThreads, 0);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       encode_per_sm, reduce_encode_kernel<kE4M3, kE4M3>, kThreads, 0);
