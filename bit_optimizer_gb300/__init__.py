@@ -8,13 +8,13 @@ from ._lib import (BF16, E4M3, E5M2, EXPORTS, F16, F32, KERNELS, Fp8OptError,
                    LIB_PATH, load, release, release_stream, strerror,
                    timing_enable, timing_read)
 from .api import (AdamWPlan, CastPlan, CastStepPlan, Fp8AdamW, ReducePlan,
-                  arena_views, fp8_adamw_step, fp8_cast_scaled,
+                  StepState, arena_views, fp8_adamw_step, fp8_cast_scaled,
                   fp8_reduce_scaled)
 
 load()
 
 __all__ = ["fp8_cast_scaled", "fp8_adamw_step", "fp8_reduce_scaled",
-           "CastPlan", "AdamWPlan", "CastStepPlan", "ReducePlan",
+           "CastPlan", "AdamWPlan", "CastStepPlan", "ReducePlan", "StepState",
            "Fp8AdamW", "arena_views", "E4M3", "E5M2", "F32", "BF16", "F16",
            "Fp8OptError", "strerror", "release", "release_stream", "load",
            "LIB_PATH", "EXPORTS",

@@ -246,6 +246,30 @@ def fp8_reduce_scaled(shards: Sequence[torch.Tensor], scales, in_fmt="e4m3",
 
 # ------------------------------------------------------------------- step
 
+class StepState:
+    """fp8opt_step_state in device memory: lr, inv_loss_scale and the step
+    count read by the *_dev step calls at run (or graph replay) time.
+    ``lr`` and ``inv_loss_scale`` are float32 CUDA scalars, ``step`` an int64
+    CUDA scalar (steps taken so far), all views of one 16-byte buffer.  Write
+    them with tensor operations (``state.lr.fill_(x)``,
+    ``state.inv_loss_scale.copy_(t)``), inside or outside a captured graph."""
+
+    def __init__(self, lr=1e-3, inv_loss_scale=1.0, step=0, device=None):
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        self.buf = torch.zeros(2, dtype=torch.int64, device=dev)
+        f = self.buf.view(torch.float32)
+        self.lr = f[0]
+        self.inv_loss_scale = f[1]
+        self.step = self.buf[1]
+        self.lr.fill_(float(lr))
+        self.inv_loss_scale.fill_(float(inv_loss_scale))
+        self.step.fill_(int(step))
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+
 class AdamWPlan:
     """A marshalled ``fp8_adamw_step`` over fixed state buffers.
 
@@ -331,6 +355,21 @@ class AdamWPlan:
                 fptr, fdev, _stream_ptr(stream)))
             self.last_grad_norm = self._norm.value if nptr is not None else None
         return self._found.value if sync else None
+
+    def step_dev(self, state: StepState, beta1, beta2, eps, wd, l2=False,
+                 found_inf_dev: Optional[torch.Tensor] = None,
+                 stream=None) -> None:
+        """One step with lr, inv_loss_scale and the step count read from
+        ``state`` on the device (fp8_adam_step_dev): capturable into a CUDA
+        graph that serves every step.  Never waits for the stream; found_inf
+        goes to found_inf_dev, if given, and the step count advances on the
+        device unless the step was skipped."""
+        fdev = None
+        if found_inf_dev is not None:
+            fdev = _cuda(found_inf_dev, "found_inf_dev").data_ptr()
+        check(load().fp8_adam_step_dev(self._params, self.n, beta1, beta2, eps,
+                                       wd, 1 if l2 else 0, state.ptr, fdev,
+                                       _stream_ptr(stream)))
 
     def grad_norm(self, inv_loss_scale=1.0, norm_dev=None, sync=True,
                   stream=None):
@@ -434,6 +473,20 @@ class CastStepPlan:
         return self._found.value if sync else None
 
 
+    def step_dev(self, state: StepState, beta1, beta2, eps, wd,
+                 found_inf_dev: Optional[torch.Tensor] = None,
+                 stream=None) -> None:
+        """The cast and an AdamW step with lr, inv_loss_scale and the step
+        count read from ``state`` on the device (fp8_cast_adamw_step_dev);
+        capturable, never waits (see AdamWPlan.step_dev)."""
+        fdev = None
+        if found_inf_dev is not None:
+            fdev = _cuda(found_inf_dev, "found_inf_dev").data_ptr()
+        check(load().fp8_cast_adamw_step_dev(
+            self.cast._items, self.step_plan._params, self.cast.n, self.cast.fmt,
+            beta1, beta2, eps, wd, state.ptr, fdev, _stream_ptr(stream)))
+
+
 # -------------------------------------------------------------- optimizer
 
 class Fp8AdamW:
@@ -454,14 +507,23 @@ class Fp8AdamW:
     just-in-time scale) and runs the update; it returns found_inf and, like a
     GradScaler step, leaves every state tensor and the step count unchanged
     when found_inf is 1.
+
+    ``capturable``: lr, inv_loss_scale and the step count live on the device
+    (``self.state``, a StepState), so ``step`` can be captured into a CUDA
+    graph once and replayed every step.  ``step`` then never waits: it returns
+    None, takes inv_loss_scale from ``self.state`` (write it there) and
+    reports found_inf only through found_inf_dev.  Set the learning rate with
+    ``set_lr``.  Not with max_grad_norm.
     """
 
     def __init__(self, params: Sequence[torch.Tensor], lr=1e-3,
                  betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01, level="O2",
                  grad_fmt="e4m3", fused=True, scaled_v=False, l2=False,
-                 max_grad_norm=None):
+                 max_grad_norm=None, capturable=False):
         if level not in ("O2", "O3"):
             raise ValueError("level must be 'O2' or 'O3'")
+        if capturable and max_grad_norm is not None:
+            raise ValueError("capturable does not support max_grad_norm")
         self.params = list(params)
         for i, p in enumerate(self.params):
             _cuda(p, f"params[{i}]")
@@ -501,6 +563,15 @@ class Fp8AdamW:
         self._cast_key = None
         self._cast = None
         self._cast_step = None
+        self.capturable = capturable
+        self.state = StepState(lr, 1.0, 0, dev) if capturable else None
+
+    def set_lr(self, lr: float) -> None:
+        """The learning rate of the next step (on the device when
+        capturable)."""
+        self.lr = lr
+        if self.state is not None:
+            self.state.lr.fill_(float(lr))
 
     def _cast_plan(self, grads: Sequence[torch.Tensor]) -> CastPlan:
         key = tuple((g.data_ptr(), g.numel(), g.dtype) for g in grads)
@@ -520,6 +591,20 @@ class Fp8AdamW:
         if len(grads) != len(self.params):
             raise ValueError("one gradient per parameter")
         cast = self._cast_plan(grads)
+        if self.capturable:
+            if inv_loss_scale != 1.0:
+                raise ValueError("capturable: write inv_loss_scale into "
+                                 "self.state.inv_loss_scale")
+            # fused AdamW: one call; Adam-L2 or fused=False: the cast, then
+            # the step
+            if self.fused and not self.l2:
+                self._cast_step.step_dev(self.state, self.beta1, self.beta2,
+                                         self.eps, self.wd, found_inf_dev, stream)
+            else:
+                cast(stream)
+                self._plan.step_dev(self.state, self.beta1, self.beta2, self.eps,
+                                    self.wd, self.l2, found_inf_dev, stream)
+            return None
         t = self.step_count + 1
         if self.fused:
             found = self._cast_step(self.lr, self.beta1, self.beta2, self.eps,
@@ -538,6 +623,9 @@ class Fp8AdamW:
         return found
 
     def state_dict(self) -> Dict[str, object]:
+        if self.state is not None:
+            self.step_count = int(self.state.step.item())
+            self.lr = float(self.state.lr.item())
         d = {"step": self.step_count, "level": self.level,
              "grad_fmt": self.grad_fmt,
              "hparams": (self.lr, self.beta1, self.beta2, self.eps, self.wd),
@@ -556,6 +644,9 @@ class Fp8AdamW:
             raise ValueError("state dict does not match this optimizer")
         self.step_count = int(d["step"])
         self.lr, self.beta1, self.beta2, self.eps, self.wd = d["hparams"]
+        if self.state is not None:
+            self.state.step.fill_(self.step_count)
+            self.state.lr.fill_(float(self.lr))
         for dst, src in zip(self.m, d["m"]):
             dst.copy_(src)
         for dst, src in zip(self.v, d["v"]):

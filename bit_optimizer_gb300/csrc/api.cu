@@ -2,6 +2,7 @@
 // stream) workspace with its cached tensor and chunk tables, the per-call
 // scalars, and the kernel launches.
 #include <cmath>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -25,9 +26,13 @@ cudaError_t launch_step(const StepDesc* descs, const Chunk* chunks,
                         uint32_t nchunks_o3, const StepScratch& sc,
                         const StepScalars& s, uint32_t epoch,
                         uint32_t* found_dev, int grid_amax, int grid_update,
-                        int grid_w8, bool any_vs, cudaStream_t stream,
-                        LaunchMark mark);
-cudaError_t step_occupancy(int* amax_per_sm, int* update_per_sm, int* w8_per_sm);
+                        int grid_update_var, int grid_w8, bool any_vs,
+                        cudaStream_t stream, LaunchMark mark);
+cudaError_t step_occupancy(int* amax_per_sm, int* update_per_sm,
+                           int* update_var_per_sm, int* w8_per_sm);
+cudaError_t launch_step_scalars(DevState* state, float beta1, float beta2,
+                                float wd, bool l2, DevScalars* out, bool commit,
+                                cudaStream_t stream);
 cudaError_t launch_cast_amax(const CastDesc* descs, const Chunk* chunks,
                              uint32_t nchunks, unsigned long long* slots,
                              uint32_t epoch, int grid_amax, cudaStream_t stream,
@@ -49,8 +54,8 @@ cudaError_t launch_cast_step(const CastDesc* cdescs, const StepDesc* sdescs,
                              unsigned long long* gslots, const StepScratch& sc,
                              const StepScalars& s, uint32_t epoch, int fmt,
                              uint32_t* found_dev, int grid_amax, int grid_fused,
-                             int grid_update, int grid_w8, bool any_vs,
-                             cudaStream_t stream, LaunchMark mark);
+                             int grid_update, int grid_update_var, int grid_w8,
+                             bool any_vs, cudaStream_t stream, LaunchMark mark);
 cudaError_t cast_step_occupancy(int* per_sm);
 cudaError_t launch_reduce(const ReduceDesc* descs, const Chunk* chunks,
                           uint32_t nchunks, unsigned long long* slots,
@@ -83,9 +88,9 @@ cudaError_t launch_step_update(const StepDesc* descs, const Chunk* chunks,
                                uint32_t nchunks, const Chunk* chunks_o3,
                                uint32_t nchunks_o3, const StepScratch& sc,
                                const StepScalars& s, uint32_t epoch,
-                               uint32_t* found_dev, int grid_update, int grid_w8,
-                               bool any_vs, cudaStream_t stream,
-                               LaunchMark mark);
+                               uint32_t* found_dev, int grid_update,
+                               int grid_update_var, int grid_w8, bool any_vs,
+                               cudaStream_t stream, LaunchMark mark);
 cudaError_t grad_norm_occupancy(int* per_sm);
 
 namespace {
@@ -134,7 +139,7 @@ struct DevBuf {
 struct DeviceInfo {
   int sms = 0;
   int cast_amax = 0, cast_encode = 0;          // persistent grid sizes
-  int step_amax = 0, step_update = 0, step_w8 = 0;
+  int step_amax = 0, step_update = 0, step_update_var = 0, step_w8 = 0;
   int cast_step = 0;
   int reduce_amax = 0, reduce_amax_small = 0;
   int reduce_encode = 0, reduce_encode_small = 0;
@@ -154,6 +159,7 @@ struct Workspace {
   DevBuf slots;
   DevBuf saved_scales;       // n floats: m_scale before the step
   DevBuf norm_buf;           // gradient norm: 2n sum words, norm, clip
+  DevBuf dev_scalars;        // the *_dev calls' DevScalars
   // cast tables
   std::vector<fp8opt_cast_item> cast_key;
   DevBuf cast_descs, cast_chunks;
@@ -175,8 +181,9 @@ struct Workspace {
 
   void freeze() {
     frozen = true;
-    for (DevBuf* b : {&slots, &saved_scales, &norm_buf, &cast_descs, &cast_chunks,
-                      &step_descs, &step_chunks, &reduce_descs, &reduce_chunks})
+    for (DevBuf* b : {&slots, &saved_scales, &norm_buf, &dev_scalars, &cast_descs,
+                      &cast_chunks, &step_descs, &step_chunks, &reduce_descs,
+                      &reduce_chunks})
       b->frozen = true;
   }
 
@@ -184,6 +191,7 @@ struct Workspace {
     slots.release();
     saved_scales.release();
     norm_buf.release();
+    dev_scalars.release();
     cast_descs.release();
     cast_chunks.release();
     step_descs.release();
@@ -214,9 +222,11 @@ cudaError_t device_info(int dev, DeviceInfo** out) {
   if ((e = cast_occupancy(&a, &b)) != cudaSuccess) return e;
   info.cast_amax = info.sms * (a > 0 ? a : 1);
   info.cast_encode = info.sms * (b > 0 ? b : 1);
-  if ((e = step_occupancy(&a, &b, &c)) != cudaSuccess) return e;
+  int v = 0;
+  if ((e = step_occupancy(&a, &b, &v, &c)) != cudaSuccess) return e;
   info.step_amax = info.sms * (a > 0 ? a : 1);
   info.step_update = info.sms * (b > 0 ? b : 1);
+  info.step_update_var = info.sms * (v > 0 ? v : 1);
   info.step_w8 = info.sms * (c > 0 ? c : 1);
   if ((e = cast_step_occupancy(&a)) != cudaSuccess) return e;
   info.cast_step = info.sms * (a > 0 ? a : 1);
@@ -473,7 +483,60 @@ StepScalars make_scalars(float lr, float beta1, float beta2, float eps, float wd
   s.wd = wd;
   s.l2 = l2 ? 1 : 0;
   s.clip = nullptr;
+  s.dev = nullptr;
+  s.step_out = nullptr;
   return s;
+}
+
+static_assert(sizeof(fp8opt_step_state) == sizeof(DevState) &&
+                  offsetof(fp8opt_step_state, lr) == offsetof(DevState, lr) &&
+                  offsetof(fp8opt_step_state, inv_loss_scale) ==
+                      offsetof(DevState, inv_loss_scale) &&
+                  offsetof(fp8opt_step_state, step) == offsetof(DevState, step),
+              "fp8opt_step_state and DevState must share one layout");
+
+// The scalars of a device-resident step: the constants from the host, the
+// per-step values from the DevScalars the scalars kernel writes, and the
+// caller's step count to advance.
+StepScalars make_dev_scalars(float beta1, float beta2, float eps, float wd,
+                             bool l2, const DevScalars* dev, long long* step_out) {
+  StepScalars s = make_scalars(0.0f, beta1, beta2, eps, wd, 1, 1.0f, l2);
+  s.step_size = s.inv_sbc2 = s.ils = 0.0f;
+  s.decay = 1.0f;
+  s.dev = dev;
+  s.step_out = step_out;
+  return s;
+}
+
+int check_dev_state(const char* fn, const fp8opt_step_state* state) {
+  if (state == nullptr ||
+      (reinterpret_cast<uintptr_t>(state) & (alignof(fp8opt_step_state) - 1)) != 0)
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": state is NULL or misaligned");
+  return FP8OPT_OK;
+}
+
+// The workspace's DevScalars for a *_dev call.
+int dev_scalars_buf(const char* fn, Workspace* ws, DevScalars** out) {
+  cudaError_t e = ws->dev_scalars.reserve(sizeof(DevScalars));
+  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": workspace").c_str());
+  *out = static_cast<DevScalars*>(ws->dev_scalars.ptr);
+  return FP8OPT_OK;
+}
+
+// A *_dev call without chunks: the step is taken (nothing can be non-finite),
+// so the scalars kernel advances the step count itself.
+int empty_dev_step(const char* fn, fp8opt_step_state* state, float beta1,
+                   float beta2, float wd, bool l2, uint32_t* found_inf_dev,
+                   Workspace* ws, cudaStream_t stream) {
+  DevScalars* ds = nullptr;
+  int st = dev_scalars_buf(fn, ws, &ds);
+  if (st != FP8OPT_OK) return st;
+  cudaError_t e = launch_step_scalars(reinterpret_cast<DevState*>(state), beta1,
+                                      beta2, wd, l2, ds, true, stream);
+  if (e == cudaSuccess && found_inf_dev != nullptr)
+    e = cudaMemsetAsync(found_inf_dev, 0, sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
+  return FP8OPT_OK;
 }
 
 // The workspace's cast tables for this item list (uploaded when the list
@@ -894,8 +957,8 @@ int adam_step(const char* fn, bool l2, const fp8opt_param* params, int n,
     e = launch_step(c.descs, c.chunks, ws->step_nchunks,
                     c.chunks + ws->step_nchunks, ws->step_nchunks_o3, c.sc, s,
                     c.epoch, found_inf_dev, c.info->step_amax,
-                    c.info->step_update, c.info->step_w8, ws->step_any_vs,
-                    stream, launch_mark());
+                    c.info->step_update, c.info->step_update_var,
+                    c.info->step_w8, ws->step_any_vs, stream, launch_mark());
     if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
   }
   if (found_inf != nullptr || nr.norm != nullptr)
@@ -1051,7 +1114,8 @@ extern "C" int fp8_adam_step_finish(const fp8opt_param* params, int n, float lr,
   if (e == cudaSuccess)
     e = launch_step_update(c.descs, c.chunks, ws->step_nchunks,
                            c.chunks + ws->step_nchunks, ws->step_nchunks_o3, c.sc,
-                           s, c.epoch, found_dev, info->step_update, info->step_w8,
+                           s, c.epoch, found_dev, info->step_update,
+                           info->step_update_var, info->step_w8,
                            ws->step_any_vs, stream, launch_mark());
   if (e != cudaSuccess) return cuda_fail(e, "fp8_adam_step_finish: launch");
   return FP8OPT_OK;
@@ -1117,10 +1181,112 @@ extern "C" int fp8_cast_adamw_step(const fp8opt_cast_item* grads,
                        ws->step_nchunks, chunks + ws->step_nchunks,
                        ws->step_nchunks_o3, slots, sc, s, epoch, fmt,
                        found_inf_dev, info->cast_amax, info->cast_step,
-                       info->step_update, info->step_w8, ws->step_any_vs, stream,
-                       launch_mark());
+                       info->step_update, info->step_update_var,
+                       info->step_w8, ws->step_any_vs, stream, launch_mark());
   if (e != cudaSuccess) return cuda_fail(e, "fp8_cast_adamw_step: launch");
   if (found_inf != nullptr) return read_found(fn, sc.found, epoch, stream, found_inf);
+  return FP8OPT_OK;
+}
+
+extern "C" int fp8_adam_step_dev(const fp8opt_param* params, int n, float beta1,
+                                 float beta2, float eps, float wd, int l2,
+                                 fp8opt_step_state* state,
+                                 uint32_t* found_inf_dev, void* stream_ptr) {
+  const char* fn = "fp8_adam_step_dev";
+  int st = check_step_args(fn, params, n, 1);
+  if (st == FP8OPT_OK) st = check_dev_state(fn, state);
+  if (st == FP8OPT_OK && l2 != 0 && l2 != 1)
+    st = fail(FP8OPT_ERR_ARG, std::string(fn) + ": l2 must be 0 or 1");
+  if (st != FP8OPT_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (n == 0) {
+    int dev = 0;
+    DeviceInfo* info = nullptr;
+    if ((st = current_device_and_info(&dev, &info)) != FP8OPT_OK) return st;
+    return empty_dev_step(fn, state, beta1, beta2, wd, l2 != 0, found_inf_dev,
+                          workspace(dev, stream), stream);
+  }
+  StepCall c;
+  if ((st = setup_step(fn, params, n, stream_ptr, false, true, &c)) != FP8OPT_OK)
+    return st;
+  Workspace* ws = c.ws;
+  if (ws->step_nchunks == 0)
+    return empty_dev_step(fn, state, beta1, beta2, wd, l2 != 0, found_inf_dev, ws,
+                          stream);
+  DevScalars* ds = nullptr;
+  if ((st = dev_scalars_buf(fn, ws, &ds)) != FP8OPT_OK) return st;
+  const StepScalars s = make_dev_scalars(beta1, beta2, eps, wd, l2 != 0, ds,
+                                         reinterpret_cast<long long*>(&state->step));
+  cudaError_t e = launch_step_scalars(reinterpret_cast<DevState*>(state), beta1,
+                                      beta2, wd, l2 != 0, ds, false, stream);
+  if (e == cudaSuccess)
+    e = launch_step(c.descs, c.chunks, ws->step_nchunks,
+                    c.chunks + ws->step_nchunks, ws->step_nchunks_o3, c.sc, s,
+                    c.epoch, found_inf_dev, c.info->step_amax,
+                    c.info->step_update, c.info->step_update_var,
+                    c.info->step_w8, ws->step_any_vs, stream, launch_mark());
+  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
+  return FP8OPT_OK;
+}
+
+extern "C" int fp8_cast_adamw_step_dev(const fp8opt_cast_item* grads,
+                                       const fp8opt_param* params, int n, int fmt,
+                                       float beta1, float beta2, float eps,
+                                       float wd, fp8opt_step_state* state,
+                                       uint32_t* found_inf_dev, void* stream_ptr) {
+  const char* fn = "fp8_cast_adamw_step_dev";
+  int st = check_cast_args(fn, grads, n, fmt);
+  if (st == FP8OPT_OK) st = check_step_args(fn, params, n, 1);
+  if (st == FP8OPT_OK) st = check_takes_cast(fn, grads, params, n, fmt);
+  if (st == FP8OPT_OK) st = check_dev_state(fn, state);
+  if (st != FP8OPT_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  DeviceInfo* info = nullptr;
+  if ((st = current_device_and_info(&dev, &info)) != FP8OPT_OK) return st;
+  Workspace* ws = workspace(dev, stream);
+  if (n == 0)
+    return empty_dev_step(fn, state, beta1, beta2, wd, false, found_inf_dev, ws,
+                          stream);
+  if ((st = ensure_cast_tables(fn, ws, grads, n, stream)) != FP8OPT_OK) return st;
+  if ((st = ensure_step_tables(fn, ws, params, n, stream)) != FP8OPT_OK) return st;
+  if (ws->step_nchunks == 0)
+    return empty_dev_step(fn, state, beta1, beta2, wd, false, found_inf_dev, ws,
+                          stream);
+
+  // slots as in fp8_cast_adamw_step
+  uint32_t epoch = 0;
+  cudaError_t e = prepare_slots(ws, 4 * (size_t)n + 1, stream, &epoch);
+  if (e == cudaSuccess) e = ws->saved_scales.reserve(2 * (size_t)n * sizeof(float));
+  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": workspace").c_str());
+  DevScalars* ds = nullptr;
+  if ((st = dev_scalars_buf(fn, ws, &ds)) != FP8OPT_OK) return st;
+  unsigned long long* slots = static_cast<unsigned long long*>(ws->slots.ptr);
+  StepScratch sc;
+  sc.amax_m = slots + n;
+  sc.amax_w = slots + 2 * (size_t)n;
+  sc.amax_g = slots + 3 * (size_t)n;
+  sc.found = slots + 4 * (size_t)n;
+  sc.old_m_scale = static_cast<float*>(ws->saved_scales.ptr);
+  sc.old_v_bound = sc.old_m_scale + n;
+  const StepScalars s = make_dev_scalars(beta1, beta2, eps, wd, false, ds,
+                                         reinterpret_cast<long long*>(&state->step));
+  const Chunk* chunks = static_cast<const Chunk*>(ws->step_chunks.ptr);
+  e = launch_step_scalars(reinterpret_cast<DevState*>(state), beta1, beta2, wd,
+                          false, ds, false, stream);
+  if (e == cudaSuccess)
+    e = launch_cast_step(static_cast<const CastDesc*>(ws->cast_descs.ptr),
+                         static_cast<const StepDesc*>(ws->step_descs.ptr), chunks,
+                         ws->step_nchunks, chunks + ws->step_nchunks,
+                         ws->step_nchunks_o3, slots, sc, s, epoch, fmt,
+                         found_inf_dev, info->cast_amax, info->cast_step,
+                         info->step_update, info->step_update_var,
+                         info->step_w8, ws->step_any_vs, stream, launch_mark());
+  if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
   return FP8OPT_OK;
 }
 
@@ -1209,8 +1375,9 @@ extern "C" int fp8_cast_adam_step_clipped(
   if (e == cudaSuccess)
     e = launch_step(sdescs, schunks, ws->step_nchunks, schunks + ws->step_nchunks,
                     ws->step_nchunks_o3, sc, s, epoch, found_inf_dev,
-                    info->step_amax, info->step_update, info->step_w8,
-                    ws->step_any_vs, stream, mark);
+                    info->step_amax, info->step_update,
+                    info->step_update_var, info->step_w8, ws->step_any_vs,
+                    stream, mark);
   if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
   if (found_inf != nullptr || grad_norm != nullptr)
     return read_results(fn, sc.found, epoch, norm, stream, found_inf, grad_norm);

@@ -106,6 +106,8 @@ enum KernelId { kCastAmaxK = 0, kCastEncodeK, kStepAmaxK, kStepUpdateK,
 // is on; nullptr otherwise.
 typedef void (*LaunchMark)(int kernel, int end, cudaStream_t stream);
 
+struct DevScalars;
+
 // Per-call scalars of the AdamW step (computed on the host): the bias
 // corrections enter only through step_size = lr / (1 - beta1^t) and
 // inv_sbc2 = 1 / sqrt(1 - beta2^t), each evaluated in double and rounded once.
@@ -114,7 +116,34 @@ struct StepScalars {
   float wd;       // the L2 coefficient (used when l2)
   int32_t l2;     // Adam with L2 decay: g = fma(wd, w, g); decay is then 1
   const float* clip;  // device clip coefficient (k becomes k * clip), or NULL
+  // Device-resident step (the *_dev calls): step_size, inv_sbc2, decay and
+  // ils come from *dev instead, and the update kernel stores dev->t into
+  // *step_out when the step is taken.  NULL otherwise.
+  const DevScalars* dev;
+  long long* step_out;
 };
+
+// The caller's device-resident step values (fp8opt_step_state, same layout).
+struct DevState {
+  float lr;
+  float inv_loss_scale;
+  long long step;   // steps taken so far
+};
+
+// The per-step scalars of a *_dev call, made on the device from a DevState
+// by step_scalars_kernel with the same arithmetic as the host's, and the
+// step t they belong to.
+struct DevScalars {
+  float step_size, inv_sbc2, decay, ils;
+  long long t;
+};
+
+// inv_loss_scale of the call: from the host, or (DEVS) from the device.
+template <bool DEVS>
+__device__ __forceinline__ float step_ils(const StepScalars& s) {
+  if constexpr (DEVS) return __ldg(&s.dev->ils);
+  else return s.ils;
+}
 
 // A scaled second moment is stored as FP16 of v * kVTarget / bound.
 constexpr float kVTarget = 16384.0f;

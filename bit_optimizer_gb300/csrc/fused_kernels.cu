@@ -31,7 +31,8 @@ cudaError_t launch_step_update(const StepDesc* descs, const Chunk* chunks,
                                uint32_t nchunks, const Chunk* chunks_o3,
                                uint32_t nchunks_o3, const StepScratch& sc,
                                const StepScalars& s, uint32_t epoch,
-                               uint32_t* found_dev, int grid_update, int grid_w8,
+                               uint32_t* found_dev, int grid_update,
+                               int grid_update_var, int grid_w8,
                                bool any_vs, cudaStream_t stream,
                                LaunchMark mark);
 
@@ -171,8 +172,9 @@ __device__ __forceinline__ void cast_step_dispatch(const CastDesc& cd,
 }
 
 // At most 64 registers a thread: 4 resident CTAs per SM.  ANY_VS: some
-// tensor of the call has a scaled second moment.
-template <int FMT, bool ANY_VS>
+// tensor of the call has a scaled second moment.  DEVS: inv_loss_scale comes
+// from the device-resident step (StepScalars::dev).
+template <int FMT, bool ANY_VS, bool DEVS>
 __global__ void __launch_bounds__(kThreads, 4)
 cast_step_amax_kernel(const CastDesc* __restrict__ cdescs,
                       const StepDesc* __restrict__ sdescs,
@@ -194,7 +196,7 @@ cast_step_amax_kernel(const CastDesc* __restrict__ cdescs,
       sc.old_m_scale[ch.tensor] = ms;
       if (sd.v_bound != nullptr) sc.old_v_bound[ch.tensor] = *sd.v_bound;
     }
-    const float k = __fdiv_rn(s.ils, scale), minv = __frcp_rn(ms);
+    const float k = __fdiv_rn(step_ils<DEVS>(s), scale), minv = __frcp_rn(ms);
     const int64_t begin = (int64_t)ch.index * kChunkElems;
     const int64_t end = min(begin + kChunkElems, cd.numel);
     const bool checked = ab >= 0x7F800000u;
@@ -227,7 +229,8 @@ cudaError_t launch_cast_step(const CastDesc* cdescs, const StepDesc* sdescs,
                              unsigned long long* gslots, const StepScratch& sc,
                              const StepScalars& s, uint32_t epoch, int fmt,
                              uint32_t* found_dev, int grid_amax, int grid_fused,
-                             int grid_update, int grid_w8, bool any_vs,
+                             int grid_update, int grid_update_var, int grid_w8,
+                             bool any_vs,
                              cudaStream_t stream, LaunchMark mark) {
   if (nchunks == 0) {
     if (found_dev) return cudaMemsetAsync(found_dev, 0, sizeof(uint32_t), stream);
@@ -238,28 +241,34 @@ cudaError_t launch_cast_step(const CastDesc* cdescs, const StepDesc* sdescs,
   if (e != cudaSuccess) return e;
   const uint32_t g = grid_min((uint32_t)grid_fused, nchunks);
   if (mark) mark(kCastStepAmaxK, 0, stream);
-  if (fmt == kE4M3 && any_vs)
-    cast_step_amax_kernel<kE4M3, true><<<g, kThreads, 0, stream>>>(
-        cdescs, sdescs, chunks, nchunks, gslots, sc, s, epoch);
-  else if (fmt == kE4M3)
-    cast_step_amax_kernel<kE4M3, false><<<g, kThreads, 0, stream>>>(
-        cdescs, sdescs, chunks, nchunks, gslots, sc, s, epoch);
-  else if (any_vs)
-    cast_step_amax_kernel<kE5M2, true><<<g, kThreads, 0, stream>>>(
-        cdescs, sdescs, chunks, nchunks, gslots, sc, s, epoch);
-  else
-    cast_step_amax_kernel<kE5M2, false><<<g, kThreads, 0, stream>>>(
-        cdescs, sdescs, chunks, nchunks, gslots, sc, s, epoch);
+  const int v = (fmt == kE4M3 ? 0 : 4) | (any_vs ? 2 : 0) | (s.dev ? 1 : 0);
+  switch (v) {
+#define FP8OPT_CAST_STEP_CASE(FMT, VS, DEVS)                                 \
+  case (FMT == kE4M3 ? 0 : 4) | (VS ? 2 : 0) | (DEVS ? 1 : 0):               \
+    cast_step_amax_kernel<FMT, VS, DEVS><<<g, kThreads, 0, stream>>>(        \
+        cdescs, sdescs, chunks, nchunks, gslots, sc, s, epoch);              \
+    break;
+    FP8OPT_CAST_STEP_CASE(kE4M3, false, false)
+    FP8OPT_CAST_STEP_CASE(kE4M3, false, true)
+    FP8OPT_CAST_STEP_CASE(kE4M3, true, false)
+    FP8OPT_CAST_STEP_CASE(kE4M3, true, true)
+    FP8OPT_CAST_STEP_CASE(kE5M2, false, false)
+    FP8OPT_CAST_STEP_CASE(kE5M2, false, true)
+    FP8OPT_CAST_STEP_CASE(kE5M2, true, false)
+    FP8OPT_CAST_STEP_CASE(kE5M2, true, true)
+#undef FP8OPT_CAST_STEP_CASE
+  }
   if (mark) mark(kCastStepAmaxK, 1, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_step_update(sdescs, chunks, nchunks, chunks_o3, nchunks_o3, sc,
-                            s, epoch, found_dev, grid_update, grid_w8, any_vs,
+                            s, epoch, found_dev, grid_update, grid_update_var,
+                            grid_w8, any_vs,
                             stream, mark);
 }
 
 cudaError_t cast_step_occupancy(int* per_sm) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      per_sm, cast_step_amax_kernel<kE4M3, false>, kThreads, 0);
+      per_sm, cast_step_amax_kernel<kE4M3, false, false>, kThreads, 0);
 }
 
 }  // namespace fp8opt

@@ -35,6 +35,13 @@
 // Elements are processed in pairs with the paired fp32 instructions, which
 // round each lane like the scalar ones, so the first moment, its amax and its
 // scale are bit-identical to a scalar fp32 evaluation of the same lines.
+//
+// Device-resident step (DEVS instantiations, the *_dev calls): lr,
+// inv_loss_scale and the step count live in device memory.
+// step_scalars_kernel turns them into step_size, inv_sbc2, decay and ils with
+// the host's arithmetic.  The passes read those four from the device.  The
+// update stores the new step count unless found_inf skipped the step.  A
+// CUDA graph of such a call then serves every step.
 #include "fp8opt_internal.cuh"
 
 namespace fp8opt {
@@ -59,6 +66,14 @@ namespace {
 #ifndef FP8OPT_UPD_MIN_BLOCKS
 #define FP8OPT_UPD_MIN_BLOCKS 7
 #endif
+// The same for the scaled-second-moment, L2 and device-resident-step
+// instantiations.  These need a few more registers: at 7 CTAs/SM they spill
+// 8 to 52 bytes, at 6 they do not.  7 is still faster.  Measured on the O3
+// 1.3B step with the scaled second moment: 4.04 ms at 7 CTAs/SM, 4.13 at 6.
+// Measured on Adam-L2 over 350M: 1.127 ms at 7, 1.142 at 6.
+#ifndef FP8OPT_UPD_MIN_BLOCKS_VAR
+#define FP8OPT_UPD_MIN_BLOCKS_VAR 7
+#endif
 // Tiles ahead of the current one that the update and amax passes prefetch
 // into L2 (0: none).  Measured on the 6.7B list: the update pass is 7 %
 // slower with a prefetch one or two tiles ahead, and the amax pass 4 - 5 %
@@ -75,19 +90,45 @@ constexpr int kUpdGroups = FP8OPT_UPD_GROUPS;
 constexpr int kUpdThreads = FP8OPT_UPD_THREADS;
 constexpr int kW8Groups = 2;
 
+// Device-resident step (DEVS): the call's DevScalars, copied into shared
+// memory by thread 0 at kernel start (load_dev_scalars), so the passes read
+// them without holding a pointer.
+__shared__ DevScalars dev_sh;
+
+template <bool DEVS>
+__device__ __forceinline__ void load_dev_scalars(const StepScalars& s) {
+  if constexpr (DEVS) {
+    if (threadIdx.x == 0) dev_sh = *s.dev;
+    __syncthreads();
+  }
+}
+
+template <bool DEVS>
+__device__ __forceinline__ float ils_of(const StepScalars& s) {
+  if constexpr (DEVS) return dev_sh.ils;
+  else return s.ils;
+}
+
 // The scalar forms of the lines above (tails and unaligned tensors).
 __device__ __forceinline__ float m_new1(float mdec, float minv, float g,
                                         const StepScalars& s) {
   return __fmaf_rn(s.beta1, __fmul_rn(mdec, minv), __fmul_rn(s.omb1, g));
 }
 
+template <bool DEVS>
 __device__ __forceinline__ void adamw1(float g, float m, float vp, float wp,
                                        const StepScalars& s, float& v,
                                        float& w) {
   v = __fmaf_rn(s.beta2, vp, __fmul_rn(s.omb2, __fmul_rn(g, g)));
-  const float den = __fmaf_rn(__fsqrt_rn(v), s.inv_sbc2, s.eps);
-  const float u = __fdiv_rn(m, den);
-  w = __fmaf_rn(-s.step_size, u, __fmul_rn(wp, s.decay));
+  if constexpr (DEVS) {
+    const float den = __fmaf_rn(__fsqrt_rn(v), dev_sh.inv_sbc2, s.eps);
+    const float u = __fdiv_rn(m, den);
+    w = __fmaf_rn(-dev_sh.step_size, u, __fmul_rn(wp, dev_sh.decay));
+  } else {
+    const float den = __fmaf_rn(__fsqrt_rn(v), s.inv_sbc2, s.eps);
+    const float u = __fdiv_rn(m, den);
+    w = __fmaf_rn(-s.step_size, u, __fmul_rn(wp, s.decay));
+  }
 }
 
 // ------------------------------------------------------------ pass 1: amax
@@ -182,12 +223,13 @@ __device__ __forceinline__ void step_amax_dispatch(const StepDesc& d,
   }
 }
 
-template <bool L2>
+template <bool L2, bool DEVS>
 __global__ void __launch_bounds__(kThreads)
 step_amax_kernel(const StepDesc* __restrict__ descs,
                  const Chunk* __restrict__ chunks, uint32_t nchunks,
                  StepScratch sc, StepScalars s, uint32_t epoch) {
   __shared__ uint32_t red[kThreads / 32];
+  load_dev_scalars<DEVS>(s);
   for (uint32_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
     const Chunk ch = chunks[c];
     const StepDesc d = descs[ch.tensor];
@@ -196,7 +238,7 @@ step_amax_kernel(const StepDesc* __restrict__ descs,
       sc.old_m_scale[ch.tensor] = ms;
       if (d.v_bound != nullptr) sc.old_v_bound[ch.tensor] = *d.v_bound;
     }
-    float k = __fdiv_rn(s.ils, gs);
+    float k = __fdiv_rn(ils_of<DEVS>(s), gs);
     if (s.clip != nullptr) k = __fmul_rn(k, *s.clip);
     const float minv = __frcp_rn(ms);
     const int64_t begin = (int64_t)ch.index * kChunkElems;
@@ -228,6 +270,7 @@ struct UpdConsts {
       vinv2, vsc2;
 };
 
+template <bool DEVS>
 __device__ __forceinline__ UpdConsts upd_consts(float k, float minv, float msc,
                                                 float vinv, float vsc,
                                                 const StepScalars& s) {
@@ -238,10 +281,16 @@ __device__ __forceinline__ UpdConsts upd_consts(float k, float minv, float msc,
   c.omb1 = splat2(s.omb1);
   c.b2 = splat2(s.beta2);
   c.omb2 = splat2(s.omb2);
-  c.isbc2 = splat2(s.inv_sbc2);
+  if constexpr (DEVS) c.isbc2 = splat2(dev_sh.inv_sbc2);
+  else c.isbc2 = splat2(s.inv_sbc2);
   c.eps2 = splat2(s.eps);
-  c.nstep = splat2(-s.step_size);
-  c.decay = splat2(s.decay);
+  if constexpr (DEVS) {
+    c.nstep = splat2(-dev_sh.step_size);
+    c.decay = splat2(dev_sh.decay);
+  } else {
+    c.nstep = splat2(-s.step_size);
+    c.decay = splat2(s.decay);
+  }
   c.msc2 = splat2(msc);
   c.wd2 = splat2(s.wd);
   c.vinv2 = splat2(vinv);
@@ -293,7 +342,7 @@ __device__ __forceinline__ void update8(uint2 gc, uint2 mc, uint4 vh, uint4 wh,
 }
 
 // The update of this thread's share of [begin, end) from global memory.
-template <int GF, bool O3, bool MCHECK, bool VS, bool L2>
+template <int GF, bool O3, bool MCHECK, bool VS, bool L2, bool DEVS>
 __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
                               float k, float minv, float msc, float vinv,
                               float vsc, const StepScalars& s, uint32_t& hmax) {
@@ -301,7 +350,7 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
   const int tid = threadIdx.x;
   const bool vec = d.vec_ok != 0;
   // built here, so an instantiation keeps only the constants it uses
-  const UpdConsts c = upd_consts(k, minv, msc, vinv, vsc, s);
+  const UpdConsts c = upd_consts<DEVS>(k, minv, msc, vinv, vsc, s);
   // One thread asks L2 for the tile FP8OPT_UPD_PREFETCH tiles ahead (whole
   // tiles of 16-byte-aligned tensors only), so the loads below find their
   // lines on chip while the DRAM reads for later tiles are already running.
@@ -354,7 +403,7 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
           float vp = h_to_f(d.v[i]);
           if (VS) vp = __fmul_rn(vp, vinv);
           float v, w;
-          adamw1(g, m, vp, wp, s, v, w);
+          adamw1<DEVS>(g, m, vp, wp, s, v, w);
           const float mt = __fmul_rn(m, msc);
           d.m[i] = (uint8_t)(MCHECK ? enc1_checked<kE4M3>(mt)
                                     : (enc2<kE4M3>(mt, 0.0f) & 0xFFu));
@@ -368,7 +417,7 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
   }
 }
 
-template <int GF, bool O3, bool MCHECK, bool ANY_VS, bool L2>
+template <int GF, bool O3, bool MCHECK, bool ANY_VS, bool L2, bool DEVS>
 __device__ __forceinline__ void update_dispatch3(const StepDesc& d,
                                                  int64_t begin, int64_t end,
                                                  float k, float minv, float msc,
@@ -376,14 +425,14 @@ __device__ __forceinline__ void update_dispatch3(const StepDesc& d,
                                                  const StepScalars& s,
                                                  uint32_t& hmax) {
   if (ANY_VS && d.v_bound != nullptr)
-    thread_update<GF, O3, MCHECK, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv,
-                                              vsc, s, hmax);
+    thread_update<GF, O3, MCHECK, ANY_VS, L2, DEVS>(d, begin, end, k, minv, msc,
+                                                    vinv, vsc, s, hmax);
   else
-    thread_update<GF, O3, MCHECK, false, L2>(d, begin, end, k, minv, msc, vinv,
-                                             vsc, s, hmax);
+    thread_update<GF, O3, MCHECK, false, L2, DEVS>(d, begin, end, k, minv, msc,
+                                                   vinv, vsc, s, hmax);
 }
 
-template <int GF, bool O3, bool ANY_VS, bool L2>
+template <int GF, bool O3, bool ANY_VS, bool L2, bool DEVS>
 __device__ __forceinline__ void update_dispatch2(const StepDesc& d,
                                                  int64_t begin, int64_t end,
                                                  float k, float minv, float msc,
@@ -392,14 +441,14 @@ __device__ __forceinline__ void update_dispatch2(const StepDesc& d,
                                                  const StepScalars& s,
                                                  uint32_t& hmax) {
   if (mcheck)
-    update_dispatch3<GF, O3, true, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv,
-                                               vsc, s, hmax);
+    update_dispatch3<GF, O3, true, ANY_VS, L2, DEVS>(d, begin, end, k, minv, msc,
+                                                     vinv, vsc, s, hmax);
   else
-    update_dispatch3<GF, O3, false, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv,
-                                                vsc, s, hmax);
+    update_dispatch3<GF, O3, false, ANY_VS, L2, DEVS>(d, begin, end, k, minv, msc,
+                                                      vinv, vsc, s, hmax);
 }
 
-template <int GF, bool ANY_VS, bool L2>
+template <int GF, bool ANY_VS, bool L2, bool DEVS>
 __device__ __forceinline__ void update_dispatch(const StepDesc& d,
                                                 int64_t begin, int64_t end,
                                                 float k, float minv, float msc,
@@ -408,11 +457,11 @@ __device__ __forceinline__ void update_dispatch(const StepDesc& d,
                                                 const StepScalars& s,
                                                 uint32_t& hmax) {
   if (d.o3)
-    update_dispatch2<GF, true, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv, vsc,
-                                           mcheck, s, hmax);
+    update_dispatch2<GF, true, ANY_VS, L2, DEVS>(d, begin, end, k, minv, msc, vinv,
+                                                 vsc, mcheck, s, hmax);
   else
-    update_dispatch2<GF, false, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv, vsc,
-                                            mcheck, s, hmax);
+    update_dispatch2<GF, false, ANY_VS, L2, DEVS>(d, begin, end, k, minv, msc, vinv,
+                                                  vsc, mcheck, s, hmax);
 }
 
 __device__ __forceinline__ bool found_set(const StepScratch& sc, uint32_t epoch) {
@@ -424,21 +473,29 @@ __device__ __forceinline__ bool found_set(const StepScratch& sc, uint32_t epoch)
 // square root and division sequences.  ANY_VS: some tensor of the call has a
 // scaled second moment; L2: Adam with L2 decay.  Separate instantiations keep
 // the plain AdamW kernel free of the other variants' registers.
-template <bool ANY_VS, bool L2>
-__global__ void __launch_bounds__(kUpdThreads, FP8OPT_UPD_MIN_BLOCKS)
+template <bool ANY_VS, bool L2, bool DEVS>
+__global__ void __launch_bounds__(kUpdThreads, (ANY_VS || L2 || DEVS)
+                                                   ? FP8OPT_UPD_MIN_BLOCKS_VAR
+                                                   : FP8OPT_UPD_MIN_BLOCKS)
 step_update_kernel(const StepDesc* __restrict__ descs,
                    const Chunk* __restrict__ chunks, uint32_t nchunks,
                    StepScratch sc, StepScalars s, uint32_t epoch,
                    uint32_t* found_dev) {
   __shared__ uint32_t red[kUpdThreads / 32];
   const bool found = found_set(sc, epoch);
-  if (found_dev != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
-    *found_dev = found ? 1u : 0u;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (found_dev != nullptr) *found_dev = found ? 1u : 0u;
+    // the step count advances only when the step is taken
+    if constexpr (DEVS) {
+      if (!found) *s.step_out = s.dev->t;
+    }
+  }
   if (found) return;
+  load_dev_scalars<DEVS>(s);
   for (uint32_t r = blockIdx.x; r < nchunks; r += gridDim.x) {
     const Chunk ch = chunks[nchunks - 1 - r];
     const StepDesc d = descs[ch.tensor];
-    float k = __fdiv_rn(s.ils, *d.g_scale);
+    float k = __fdiv_rn(ils_of<DEVS>(s), *d.g_scale);
     if (s.clip != nullptr) k = __fmul_rn(k, *s.clip);
     const float minv = __frcp_rn(sc.old_m_scale[ch.tensor]);
     const uint32_t am = slot_value(sc.amax_m[ch.tensor], epoch);
@@ -458,14 +515,13 @@ step_update_kernel(const StepDesc* __restrict__ descs,
     const int64_t begin = (int64_t)ch.index * kChunkElems;
     const int64_t end = min(begin + kChunkElems, d.numel);
     const bool mcheck = am >= 0x7F800000u;
-    const UpdConsts c = upd_consts(k, minv, msc, vinv, vsc, s);
     uint32_t hmax = 0;
     if (d.g_fmt == kE4M3)
-      update_dispatch<kE4M3, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv, vsc,
-                                         mcheck, s, hmax);
+      update_dispatch<kE4M3, ANY_VS, L2, DEVS>(d, begin, end, k, minv, msc, vinv,
+                                               vsc, mcheck, s, hmax);
     else
-      update_dispatch<kE5M2, ANY_VS, L2>(d, begin, end, k, minv, msc, vinv, vsc,
-                                         mcheck, s, hmax);
+      update_dispatch<kE5M2, ANY_VS, L2, DEVS>(d, begin, end, k, minv, msc, vinv,
+                                               vsc, mcheck, s, hmax);
     if (d.o3) {   // uniform over the CTA
       uint32_t h = max(hmax & 0xFFFFu, hmax >> 16);
       h = block_max_u32<kUpdThreads>(h, red);
@@ -548,28 +604,37 @@ step_w8_kernel(const StepDesc* __restrict__ descs,
 }  // namespace
 
 // The update pass, then (for O3 chunks) the weight-copy pass.  any_vs: some
-// record has a scaled second moment.
+// record has a scaled second moment.  grid_update sizes the plain AdamW
+// instantiation, grid_update_var the scaled-v, L2 and device-resident ones.
 cudaError_t launch_step_update(const StepDesc* descs, const Chunk* chunks,
                                uint32_t nchunks, const Chunk* chunks_o3,
                                uint32_t nchunks_o3, const StepScratch& sc,
                                const StepScalars& s, uint32_t epoch,
-                               uint32_t* found_dev, int grid_update, int grid_w8,
+                               uint32_t* found_dev, int grid_update,
+                               int grid_update_var, int grid_w8,
                                bool any_vs, cudaStream_t stream,
                                LaunchMark mark) {
   if (mark) mark(kStepUpdateK, 0, stream);
-  const uint32_t g = grid_min((uint32_t)grid_update, nchunks);
-  if (any_vs && s.l2)
-    step_update_kernel<true, true><<<g, kUpdThreads, 0, stream>>>(
-        descs, chunks, nchunks, sc, s, epoch, found_dev);
-  else if (any_vs)
-    step_update_kernel<true, false><<<g, kUpdThreads, 0, stream>>>(
-        descs, chunks, nchunks, sc, s, epoch, found_dev);
-  else if (s.l2)
-    step_update_kernel<false, true><<<g, kUpdThreads, 0, stream>>>(
-        descs, chunks, nchunks, sc, s, epoch, found_dev);
-  else
-    step_update_kernel<false, false><<<g, kUpdThreads, 0, stream>>>(
-        descs, chunks, nchunks, sc, s, epoch, found_dev);
+  const bool dev = s.dev != nullptr;
+  const uint32_t g = grid_min(
+      (uint32_t)(any_vs || s.l2 || dev ? grid_update_var : grid_update), nchunks);
+  const int v = (any_vs ? 4 : 0) | (s.l2 ? 2 : 0) | (dev ? 1 : 0);
+  switch (v) {
+#define FP8OPT_UPDATE_CASE(VS, L2, DEVS)                                     \
+  case (VS ? 4 : 0) | (L2 ? 2 : 0) | (DEVS ? 1 : 0):                         \
+    step_update_kernel<VS, L2, DEVS><<<g, kUpdThreads, 0, stream>>>(         \
+        descs, chunks, nchunks, sc, s, epoch, found_dev);                    \
+    break;
+    FP8OPT_UPDATE_CASE(false, false, false)
+    FP8OPT_UPDATE_CASE(false, false, true)
+    FP8OPT_UPDATE_CASE(false, true, false)
+    FP8OPT_UPDATE_CASE(false, true, true)
+    FP8OPT_UPDATE_CASE(true, false, false)
+    FP8OPT_UPDATE_CASE(true, false, true)
+    FP8OPT_UPDATE_CASE(true, true, false)
+    FP8OPT_UPDATE_CASE(true, true, true)
+#undef FP8OPT_UPDATE_CASE
+  }
   if (mark) mark(kStepUpdateK, 1, stream);
   if (nchunks_o3 != 0) {
     if (mark) mark(kStepW8K, 0, stream);
@@ -588,12 +653,18 @@ cudaError_t launch_step_amax(const StepDesc* descs, const Chunk* chunks,
   if (nchunks == 0) return cudaSuccess;
   if (mark) mark(kStepAmaxK, 0, stream);
   const uint32_t ga = grid_min((uint32_t)grid_amax, nchunks);
-  if (s.l2)
-    step_amax_kernel<true><<<ga, kThreads, 0, stream>>>(descs, chunks, nchunks,
-                                                        sc, s, epoch);
+  if (s.l2 && s.dev)
+    step_amax_kernel<true, true><<<ga, kThreads, 0, stream>>>(descs, chunks,
+                                                              nchunks, sc, s, epoch);
+  else if (s.l2)
+    step_amax_kernel<true, false><<<ga, kThreads, 0, stream>>>(descs, chunks,
+                                                               nchunks, sc, s, epoch);
+  else if (s.dev)
+    step_amax_kernel<false, true><<<ga, kThreads, 0, stream>>>(descs, chunks,
+                                                               nchunks, sc, s, epoch);
   else
-    step_amax_kernel<false><<<ga, kThreads, 0, stream>>>(descs, chunks, nchunks,
-                                                         sc, s, epoch);
+    step_amax_kernel<false, false><<<ga, kThreads, 0, stream>>>(descs, chunks,
+                                                                nchunks, sc, s, epoch);
   if (mark) mark(kStepAmaxK, 1, stream);
   return cudaGetLastError();
 }
@@ -603,6 +674,7 @@ cudaError_t launch_step(const StepDesc* descs, const Chunk* chunks,
                         uint32_t nchunks_o3, const StepScratch& sc,
                         const StepScalars& s, uint32_t epoch,
                         uint32_t* found_dev, int grid_amax, int grid_update,
+                        int grid_update_var,
                         int grid_w8, bool any_vs, cudaStream_t stream,
                         LaunchMark mark) {
   if (nchunks == 0) {
@@ -613,18 +685,83 @@ cudaError_t launch_step(const StepDesc* descs, const Chunk* chunks,
                                    grid_amax, stream, mark);
   if (e != cudaSuccess) return e;
   return launch_step_update(descs, chunks, nchunks, chunks_o3, nchunks_o3, sc, s,
-                            epoch, found_dev, grid_update, grid_w8, any_vs,
+                            epoch, found_dev, grid_update, grid_update_var,
+                            grid_w8, any_vs,
                             stream, mark);
 }
 
+namespace {
+
+// beta^t in double by binary exponentiation, each product rounded to double:
+// the host's bias power, bit for bit.
+__device__ double bias_power(double b, long long t) {
+  double r = 1.0;
+  while (t > 0) {
+    if (t & 1) r = __dmul_rn(r, b);
+    b = __dmul_rn(b, b);
+    t >>= 1;
+  }
+  return r;
+}
+
+// One thread: the scalars of step t = state->step + 1 from the caller's
+// device-resident lr and inv_loss_scale, with the host's arithmetic (the
+// bias corrections in double, each result rounded to float once).  commit:
+// also store t (a call with no chunks, whose update pass does not run).
+__global__ void step_scalars_kernel(DevState* state, float beta1, float beta2,
+                                    float wd, int l2, DevScalars* out,
+                                    int commit) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  const long long t = state->step + 1;
+  const float lr = state->lr;
+  const double bc1 = __dsub_rn(1.0, bias_power((double)beta1, t));
+  const double bc2 = __dsub_rn(1.0, bias_power((double)beta2, t));
+  DevScalars d;
+  d.step_size = (float)__ddiv_rn((double)lr, bc1);
+  d.inv_sbc2 = (float)__ddiv_rn(1.0, __dsqrt_rn(bc2));
+  d.decay = l2 ? 1.0f : __fsub_rn(1.0f, __fmul_rn(lr, wd));
+  d.ils = state->inv_loss_scale;
+  d.t = t;
+  *out = d;
+  if (commit) state->step = t;
+}
+
+}  // namespace
+
+// Writes the scalars of the next step of `state` to `out` (one thread).
+cudaError_t launch_step_scalars(DevState* state, float beta1, float beta2,
+                                float wd, bool l2, DevScalars* out, bool commit,
+                                cudaStream_t stream) {
+  step_scalars_kernel<<<1, 32, 0, stream>>>(state, beta1, beta2, wd, l2 ? 1 : 0,
+                                            out, commit ? 1 : 0);
+  return cudaGetLastError();
+}
+
 cudaError_t step_occupancy(int* amax_per_sm, int* update_per_sm,
-                           int* w8_per_sm) {
+                           int* update_var_per_sm, int* w8_per_sm) {
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      amax_per_sm, step_amax_kernel<false>, kThreads, 0);
+      amax_per_sm, step_amax_kernel<false, false>, kThreads, 0);
   if (e != cudaSuccess) return e;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      update_per_sm, step_update_kernel<false, false>, kUpdThreads, 0);
+      update_per_sm, step_update_kernel<false, false, false>, kUpdThreads, 0);
   if (e != cudaSuccess) return e;
+  // the least of the instantiations that share grid_update_var
+  int lo = 0;
+  const void* vars[] = {
+      (const void*)step_update_kernel<false, false, true>,
+      (const void*)step_update_kernel<false, true, false>,
+      (const void*)step_update_kernel<false, true, true>,
+      (const void*)step_update_kernel<true, false, false>,
+      (const void*)step_update_kernel<true, false, true>,
+      (const void*)step_update_kernel<true, true, false>,
+      (const void*)step_update_kernel<true, true, true>};
+  for (const void* k : vars) {
+    int b = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, kUpdThreads, 0);
+    if (e != cudaSuccess) return e;
+    lo = (lo == 0 || b < lo) ? b : lo;
+  }
+  *update_var_per_sm = lo;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(w8_per_sm,
                                                        step_w8_kernel, kThreads, 0);
 }

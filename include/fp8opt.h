@@ -52,7 +52,9 @@
  * the device outputs.  What a capture fixes: the records, and the step's
  * scalars (lr, the bias corrections of `step`, inv_loss_scale, the clip
  * threshold); the cast and the reduction have none, so their replays are
- * exactly new calls.
+ * exactly new calls.  The *_dev step calls read lr, inv_loss_scale and the
+ * step count from device memory instead (fp8opt_step_state), so one captured
+ * graph of them serves every step of a training loop.
  *
  * Errors: every entry point returns FP8OPT_OK (0) or a negative status.  On an
  * argument error nothing is launched and no output is touched.  On a CUDA
@@ -253,6 +255,55 @@ FP8OPT_API int fp8_cast_adamw_step(const fp8opt_cast_item *grads,
                                    float wd, int64_t step, float inv_loss_scale,
                                    int *found_inf, uint32_t *found_inf_dev,
                                    void *stream);
+
+/*
+ * Device-resident step values for the *_dev calls (the graph-replayable form
+ * of the step: a captured call reads these at replay time, where the other
+ * step calls fix lr, the step's bias corrections and inv_loss_scale at
+ * capture).  Device memory, 8-byte aligned, owned by the caller:
+ *   lr              learning rate of the next step;
+ *   inv_loss_scale  1 / the GradScaler loss scale of the next step;
+ *   step            steps taken so far (>= 0).  A call computes the bias
+ *                   corrections of t = step + 1, in the arithmetic of
+ *                   fp8_adamw_step, and stores t back unless found_inf skips
+ *                   the step (GradScaler semantics: a skipped step does not
+ *                   count).
+ * The host reads none of these: values the host entry points would refuse
+ * (step < 0, a non-finite lr) are not checked.
+ */
+typedef struct {
+  float lr;
+  float inv_loss_scale;
+  int64_t step;
+} fp8opt_step_state;
+
+/*
+ * fp8_adam_step_dev: fp8_adamw_step (l2 = 0) or fp8_adam_step (l2 = 1) with lr,
+ * inv_loss_scale and the step count read from *state on the device (see
+ * fp8opt_step_state), so that the call can be captured once into a CUDA graph
+ * and replayed every step.  Results are bit-identical to the host-scalar call
+ * with the same values.  found_inf goes to found_inf_dev (device, may be
+ * NULL); there is no host output.  beta1, beta2, eps and wd are fixed per
+ * call as in fp8_adamw_step.  Errors: as fp8_adamw_step, plus FP8OPT_ERR_ARG
+ * when state is NULL or misaligned or l2 is not 0 or 1.
+ */
+FP8OPT_API int fp8_adam_step_dev(const fp8opt_param *params, int n, float beta1,
+                                 float beta2, float eps, float wd, int l2,
+                                 fp8opt_step_state *state,
+                                 uint32_t *found_inf_dev, void *stream);
+
+/*
+ * fp8_cast_adamw_step_dev: fp8_cast_adamw_step with lr, inv_loss_scale and the
+ * step count read from *state on the device, as fp8_adam_step_dev (AdamW
+ * only).  Arguments, results and errors otherwise those of
+ * fp8_cast_adamw_step, with found_inf in found_inf_dev only.
+ */
+FP8OPT_API int fp8_cast_adamw_step_dev(const fp8opt_cast_item *grads,
+                                       const fp8opt_param *params, int n,
+                                       int fmt, float beta1, float beta2,
+                                       float eps, float wd,
+                                       fp8opt_step_state *state,
+                                       uint32_t *found_inf_dev, void *stream);
 
 /*
  * fp8_grad_norm: the global L2 norm of the unscaled gradient of a step call

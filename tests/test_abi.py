@@ -62,6 +62,9 @@ int main(void) {
   F(fp8opt_reduce_item, stride); F(fp8opt_reduce_item, src_scale);
   F(fp8opt_reduce_item, codes); F(fp8opt_reduce_item, amax);
   F(fp8opt_reduce_item, scale);
+  printf("state %zu\n", sizeof(fp8opt_step_state));
+  F(fp8opt_step_state, lr); F(fp8opt_step_state, inv_loss_scale);
+  F(fp8opt_step_state, step);
   return 0;
 }''')
     exe = tmp_path / "layout"
@@ -73,10 +76,15 @@ int main(void) {
     assert int(got["cast"]) == C.sizeof(lib.CastItem)
     assert int(got["param"]) == C.sizeof(lib.Param)
     assert int(got["reduce"]) == C.sizeof(lib.ReduceItem)
+    # the 16-byte StepState buffer: float lr, float inv_loss_scale, int64 step
+    assert int(got["state"]) == 16
+    assert (int(got["fp8opt_step_state.lr"]),
+            int(got["fp8opt_step_state.inv_loss_scale"]),
+            int(got["fp8opt_step_state.step"])) == (0, 4, 8)
     classes = {"fp8opt_cast_item": lib.CastItem, "fp8opt_param": lib.Param,
                "fp8opt_reduce_item": lib.ReduceItem}
     for key, val in got.items():
-        if "." in key:
+        if "." in key and not key.startswith("fp8opt_step_state"):
             t, m = key.split(".")
             cls = classes[t]
             assert getattr(cls, m).offset == int(val), key
@@ -116,6 +124,36 @@ def test_argument_errors_need_no_gpu(lib):
     p[0].numel = 0
     assert L.fp8_adamw_step(p, 0, *args, 1, 1.0, C.byref(f), None, None) == lib.OK
     assert f.value == 0
+
+
+def test_device_step_argument_errors_need_no_gpu(lib):
+    L = lib.load()
+    p = (lib.Param * 1)()
+    item = (lib.CastItem * 1)()
+    state = (C.c_int64 * 2)()                     # 16 bytes, 8-aligned
+    hp = (0.9, 0.999, 1e-8, 0.0)
+    # state NULL or misaligned
+    assert L.fp8_adam_step_dev(p, 0, *hp, 0, None, None, None) == lib.ERR_ARG
+    assert "state" in L.fp8opt_last_error().decode()
+    assert L.fp8_adam_step_dev(p, 0, *hp, 0, C.addressof(state) + 4, None,
+                               None) == lib.ERR_ARG
+    # l2 must be 0 or 1
+    assert L.fp8_adam_step_dev(p, 0, *hp, 2, C.addressof(state), None,
+                               None) == lib.ERR_ARG
+    assert "l2" in L.fp8opt_last_error().decode()
+    # the records are checked as for fp8_adamw_step
+    p[0].g_fmt = 3
+    assert L.fp8_adam_step_dev(p, 1, *hp, 0, C.addressof(state), None,
+                               None) == lib.ERR_UNSUPPORTED
+    p[0].g_fmt = 0
+    assert L.fp8_adam_step_dev(p, -1, *hp, 0, C.addressof(state), None,
+                               None) == lib.ERR_ARG
+    assert L.fp8_cast_adamw_step_dev(item, p, 1, 7, *hp, C.addressof(state),
+                                     None, None) == lib.ERR_UNSUPPORTED
+    assert L.fp8_cast_adamw_step_dev(item, p, 0, 0, *hp, None, None,
+                                     None) == lib.ERR_ARG
+    # nothing was written to the state
+    assert list(state) == [0, 0]
 
 
 def test_fused_call_checks_that_the_step_takes_the_cast_outputs(lib):
