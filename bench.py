@@ -500,11 +500,12 @@ def reduce_configs(device, peak, ranks=(2, 8)):
 def other_configs(device, peak):
     """The remaining workloads, each timed on its own after the headline:
     the scaled cast of the 124M GPT-2 list (BF16 -> E4M3 and -> E5M2, 5 B per
-    element), the local FP8 reduction of 2 and 8 shards of that list, the O2 step on the 350M list (the inf cleared), the O3 step on
+    element), the local FP8 reduction of 2 and 8 shards of that list, the O2
+    step on the 350M list (the inf cleared; E4M3 and E5M2 gradients), the O3 step on
     the 1.3B list (20 B per param with the cast), the same with the scaled
     second moment, Adam with L2 decay on the 350M list, the 350M step clipped
     to a global gradient norm (and the norm pass alone), and the launch-bound
-    tiny list."""
+    tiny list, also as replays of a captured graph of the capturable step."""
     import dataclasses
     import torch
     import synth
@@ -530,6 +531,8 @@ def other_configs(device, peak):
     # (name, workload, reps, optimizer options, algorithmic bytes per param)
     runs = (
         ("o2_350m", synth.o2_350m, 20, {}, STEP_BYTES["O2"]),
+        # the same list with E5M2 gradient codes
+        ("o2_350m_e5m2", synth.o2_350m, 20, {"grad_fmt": "e5m2"}, STEP_BYTES["O2"]),
         ("o3_1p3b", synth.o3_1p3b, 10, {}, STEP_BYTES["O3"]),
         ("o3_1p3b_scaled_v", synth.o3_1p3b, 10, {"scaled_v": True},
          STEP_BYTES["O3"]),
@@ -543,7 +546,10 @@ def other_configs(device, peak):
     )
     for name, mk, reps, kw, bpp in runs:
         w = dataclasses.replace(mk(), inf_site=None)
-        params, grads, _, opt = build_state(w, device, **kw)
+        if "grad_fmt" in kw:
+            w = dataclasses.replace(w, grad_fmt=kw["grad_fmt"])
+        params, grads, _, opt = build_state(
+            w, device, **{k: v for k, v in kw.items() if k != "grad_fmt"})
         flag = torch.zeros(1, dtype=torch.int32, device=device)
         fn = lambda: opt.step(grads, w.inv_loss_scale, found_inf_dev=flag, sync=False)
         for _ in range(3):
@@ -566,7 +572,45 @@ def other_configs(device, peak):
                                      "bytes_per_param": 1}
         del params, grads, opt
         torch.cuda.empty_cache()
+    out["tiny_graph"] = tiny_graph(device, peak)
     return out
+
+
+def tiny_graph(device, peak):
+    """The tiny list's fused step as one replay of a captured CUDA graph:
+    the capturable optimizer reads lr, inv_loss_scale and the step count on
+    the device, so each replay is a real next step.  Shows the launch and
+    call overhead a graph removes from a launch-bound step."""
+    import dataclasses
+    import torch
+    import synth
+    import bit_optimizer_gb300 as bo
+    w = dataclasses.replace(synth.tiny(), inf_site=None)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        params, grads, _, opt = build_state(w, device, capturable=True)
+        flag = torch.zeros(1, dtype=torch.int32, device=device)
+        for _ in range(3):
+            opt.step(grads, found_inf_dev=flag, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        opt.step(grads, found_inf_dev=flag, stream=s)
+    for _ in range(3):
+        g.replay()
+    reps = 500
+    before = int(opt.state.step.item())
+    ms = _events_ms(g.replay, reps)
+    steps = int(opt.state.step.item()) - before
+    gbs = STEP_BYTES["O2"] * w.n_params / (ms * 1e-3) / 1e9
+    res = {"ms_per_step": ms, "Gparams/s": w.n_params / (ms * 1e-3) / 1e9,
+           "GB/s": gbs, "frac": gbs / peak, "level": w.level,
+           "params": w.n_params, "bytes_per_param": STEP_BYTES["O2"],
+           "steps_counted": steps, "capturable": True}
+    del g
+    torch.cuda.synchronize()
+    bo.release_stream(s)
+    return res
 
 
 def run_ours(args, wl):
