@@ -754,7 +754,10 @@ def run_ours(args, wl):
     if rank == 0 and world == 1 and not args.no_other_configs:
         del params, grads, flat, opt
         torch.cuda.empty_cache()
-        others = other_configs(device, peak)
+        try:
+            others = other_configs(device, peak)
+        except Exception as e:   # the headline line is printed regardless
+            others = {"error": f"{type(e).__name__}: {e}"[:300]}
 
     if rank == 0:
         line = {
