@@ -358,9 +358,40 @@ bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
 
-uint32_t chunks_of(int64_t numel) {
-  return numel == 0 ? 1u : (uint32_t)((numel + kChunkElems - 1) / kChunkElems);
+uint64_t chunks_of(int64_t numel, int shift) {
+  return numel == 0 ? 1u : (uint64_t)((numel + ((int64_t)1 << shift) - 1) >> shift);
 }
+
+// Chunk size of a list (as a shift): kChunkShift, halved down to min_shift
+// while the list has fewer than FP8OPT_CHUNKS_PER_SM chunks per SM.  A
+// persistent pass then runs several rounds of chunks on every SM, and its
+// last, partly filled round is a small part of it.  min_shift keeps a chunk
+// at least one full tile of the passes over the table.  numel(i) gives
+// tensor i's element count.  Only the cast's tables use it.  Measured on the
+// 124M list: the cast takes 0.0986 ms at 48 or 96 chunks per SM, and 0.1020
+// ms with 32768-element chunks.  The reduction (k = 8: 0.408 against 0.352
+// ms), the norm and the clipped step were slower with smaller chunks, whose
+// per-chunk prologue and CTA reduction then weigh more.  The O2 350M step
+// gained under 1 %, so the step's tables keep 32768-element chunks.
+#ifndef FP8OPT_CHUNKS_PER_SM
+#define FP8OPT_CHUNKS_PER_SM 48
+#endif
+template <class F>
+int chunk_shift_for(int n, F numel, int sms, int min_shift) {
+  int shift = kChunkShift;
+  const uint64_t target = (uint64_t)FP8OPT_CHUNKS_PER_SM * (uint64_t)sms;
+  while (shift > min_shift) {
+    uint64_t total = 0;
+    for (int i = 0; i < n && total < target; ++i) total += chunks_of(numel(i), shift);
+    if (total >= target) break;
+    --shift;
+  }
+  return shift;
+}
+
+// Smallest chunk shift of the cast's tables: a chunk holds at least one full
+// tile of the cast passes (8192 elements).
+constexpr int kMinShiftCast = 13;
 
 template <class T>
 bool same_list(const std::vector<T>& key, const T* items, int n) {
@@ -546,10 +577,17 @@ int ensure_cast_tables(const char* fn, Workspace* ws,
                        cudaStream_t stream) {
   if (ws->have_cast && same_list(ws->cast_key, items, n)) return FP8OPT_OK;
   if (capturing(stream) || ws->frozen) return refuse_capture(fn);
+  if ((uint32_t)n >= kMaxListTensors)
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": too many tensors");
+  DeviceInfo* info = nullptr;
+  cudaError_t ie = device_info(ws->device, &info);
+  if (ie != cudaSuccess) return cuda_fail(ie, (std::string(fn) + ": device query").c_str());
+  const int shift = chunk_shift_for(n, [&](int i) { return items[i].numel; },
+                                    info->sms, kMinShiftCast);
   std::vector<CastDesc> descs((size_t)n);
   std::vector<Chunk> chunks;
   size_t total = 0;
-  for (int i = 0; i < n; ++i) total += chunks_of(items[i].numel);
+  for (int i = 0; i < n; ++i) total += chunks_of(items[i].numel, shift);
   if (total > 0xFFFFFFFFull)
     return fail(FP8OPT_ERR_ARG, std::string(fn) + ": list too long");
   chunks.reserve(total);
@@ -563,8 +601,8 @@ int ensure_cast_tables(const char* fn, Workspace* ws,
     d.numel = it.numel;
     d.dtype = it.dtype;
     d.vec_ok = aligned(it.src, 16) && aligned(it.codes, 8);
-    for (uint32_t c = 0, nc = chunks_of(it.numel); c < nc; ++c)
-      chunks.push_back(Chunk{(uint32_t)i, c});
+    for (uint32_t c = 0, nc = (uint32_t)chunks_of(it.numel, shift); c < nc; ++c)
+      chunks.push_back(make_chunk((uint32_t)i, c, shift, it.numel));
   }
   ws->have_cast = false;
   cudaError_t e;
@@ -584,10 +622,13 @@ int ensure_step_tables(const char* fn, Workspace* ws, const fp8opt_param* params
                        int n, cudaStream_t stream) {
   if (ws->have_step && same_list(ws->step_key, params, n)) return FP8OPT_OK;
   if (capturing(stream) || ws->frozen) return refuse_capture(fn);
+  if ((uint32_t)n >= kMaxListTensors)
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": too many tensors");
+  const int shift = kChunkShift;
   std::vector<StepDesc> descs((size_t)n);
   std::vector<Chunk> chunks, chunks_o3;
   size_t total = 0;
-  for (int i = 0; i < n; ++i) total += 2 * (size_t)chunks_of(params[i].numel);
+  for (int i = 0; i < n; ++i) total += 2 * (size_t)chunks_of(params[i].numel, shift);
   if (total > 0xFFFFFFFFull)
     return fail(FP8OPT_ERR_ARG, std::string(fn) + ": list too long");
   for (int i = 0; i < n; ++i) {
@@ -608,9 +649,9 @@ int ensure_step_tables(const char* fn, Workspace* ws, const fp8opt_param* params
     d.o3 = p.w8_scale != nullptr;
     d.vec_ok = aligned(p.g, 8) && aligned(p.m, 8) && aligned(p.v, 16) &&
                aligned(p.w, 16) && (p.w8 == nullptr || aligned(p.w8, 8));
-    for (uint32_t c = 0, nc = chunks_of(p.numel); c < nc; ++c) {
-      chunks.push_back(Chunk{(uint32_t)i, c});
-      if (d.o3) chunks_o3.push_back(Chunk{(uint32_t)i, c});
+    for (uint32_t c = 0, nc = (uint32_t)chunks_of(p.numel, shift); c < nc; ++c) {
+      chunks.push_back(make_chunk((uint32_t)i, c, shift, p.numel));
+      if (d.o3) chunks_o3.push_back(make_chunk((uint32_t)i, c, shift, p.numel));
     }
   }
   const uint32_t nmain = (uint32_t)chunks.size();
@@ -661,10 +702,13 @@ int ensure_reduce_tables(const char* fn, Workspace* ws,
                          cudaStream_t stream) {
   if (ws->have_reduce && same_list(ws->reduce_key, items, n)) return FP8OPT_OK;
   if (capturing(stream) || ws->frozen) return refuse_capture(fn);
+  if ((uint32_t)n >= kMaxListTensors)
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": too many tensors");
+  const int shift = kChunkShift;
   std::vector<ReduceDesc> descs((size_t)n);
   std::vector<Chunk> chunks;
   size_t total = 0;
-  for (int i = 0; i < n; ++i) total += chunks_of(items[i].numel);
+  for (int i = 0; i < n; ++i) total += chunks_of(items[i].numel, shift);
   if (total > 0xFFFFFFFFull)
     return fail(FP8OPT_ERR_ARG, std::string(fn) + ": list too long");
   chunks.reserve(total);
@@ -680,8 +724,8 @@ int ensure_reduce_tables(const char* fn, Workspace* ws,
     d.stride = it.stride;
     d.vec_ok = aligned(it.src, 16) && aligned(it.codes, 16) && it.stride % 16 == 0;
     d.pad = 0;
-    for (uint32_t c = 0, nc = chunks_of(it.numel); c < nc; ++c)
-      chunks.push_back(Chunk{(uint32_t)i, c});
+    for (uint32_t c = 0, nc = (uint32_t)chunks_of(it.numel, shift); c < nc; ++c)
+      chunks.push_back(make_chunk((uint32_t)i, c, shift, it.numel));
   }
   ws->have_reduce = false;
   cudaError_t e;

@@ -122,8 +122,8 @@ cast_amax_kernel(const CastDesc* __restrict__ descs,
   for (uint32_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
     const Chunk ch = chunks[c];
     const CastDesc d = descs[ch.tensor];
-    const int64_t begin = (int64_t)ch.index * kChunkElems;
-    const int64_t end = min(begin + kChunkElems, d.numel);
+    const int64_t begin = ch.begin;
+    const int64_t end = begin + ch.len;
     const bool vec = d.vec_ok != 0;
     uint32_t mx;
     if (d.dtype == kF32)
@@ -243,12 +243,12 @@ __device__ __forceinline__ void encode_pass(const CastDesc* __restrict__ descs,
     const CastDesc d = descs[ch.tensor];
     const uint32_t ab = slot_value(slots[ch.tensor], epoch);
     const float scale = scale_from_amax_bits(ab, fp8_max_of<FMT>());
-    if (ch.index == 0 && threadIdx.x == 0) {
+    if (ch.begin == 0 && threadIdx.x == 0) {
       *d.amax_out = __uint_as_float(ab);
       *d.scale_out = scale;
     }
-    const int64_t begin = (int64_t)ch.index * kChunkElems;
-    const int64_t end = min(begin + kChunkElems, d.numel);
+    const int64_t begin = ch.begin;
+    const int64_t end = begin + ch.len;
     const bool checked = ab >= 0x7F800000u;
     SqAcc<FMT> acc;
     if (d.dtype == kF32)

@@ -1,10 +1,12 @@
 // Internal definitions shared by the libfp8opt kernels and the host layer.
 //
 // Work decomposition (multi-tensor chunk table): every tensor of a call is cut
-// into chunks of kChunkElems elements (the last chunk of a tensor may be
-// shorter; an empty tensor gets one empty chunk so that its per-tensor outputs
-// are still written).  The host builds the chunk table once per tensor list
-// and caches it on the device.  Each kernel is a persistent grid (a multiple
+// into chunks of 2^shift elements (the last chunk of a tensor may be shorter;
+// an empty tensor gets one empty chunk so that its per-tensor outputs are
+// still written).  The shift is kChunkShift (32768 elements), smaller in the
+// cast's tables of lists too short to give every SM several chunks; each
+// chunk carries its first element and length.  The host builds the chunk
+// table once per tensor list and caches it on the device.  Each kernel is a persistent grid (a multiple
 // of the SM count) whose CTAs stride over the chunk table; a CTA handles one
 // chunk at a time in tiles of kTileElems elements: thread t takes the 8-element
 // groups starting at tile + k * (kThreads * 8) + t * 8 for k = 0, 1, so every
@@ -27,7 +29,8 @@ namespace fp8opt {
 constexpr int kThreads = 256;                    // threads per CTA
 constexpr int kGroup = 8;                        // elements per vector group
 constexpr int kTileElems = kThreads * kGroup * 2;  // 4096 elements per tile
-constexpr int64_t kChunkElems = 32768;           // elements per chunk
+constexpr int kChunkShift = 15;                  // 32768 elements per chunk
+constexpr int64_t kChunkElems = (int64_t)1 << kChunkShift;
 
 constexpr int kE4M3 = 0;
 constexpr int kE5M2 = 1;
@@ -37,8 +40,24 @@ constexpr int kF16 = 2;
 
 struct Chunk {
   uint32_t tensor;  // index into the tensor table
-  uint32_t index;   // chunk number within the tensor
+  uint32_t len;     // elements in the chunk (0 for an empty tensor's chunk)
+  int64_t begin;    // first element; 0 marks a tensor's first chunk
 };
+
+// Most tensors one call takes.
+constexpr uint32_t kMaxListTensors = 1u << 30;
+
+// Chunk `index` of 2^shift elements of a tensor with numel elements.
+inline Chunk make_chunk(uint32_t tensor, uint32_t index, int shift,
+                        int64_t numel) {
+  Chunk c;
+  c.tensor = tensor;
+  c.begin = (int64_t)index << shift;
+  const int64_t rest = numel - c.begin;
+  const int64_t size = (int64_t)1 << shift;
+  c.len = (uint32_t)(rest < size ? (rest > 0 ? rest : 0) : size);
+  return c;
+}
 
 struct CastDesc {
   const void* src;

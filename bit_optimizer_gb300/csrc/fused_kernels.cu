@@ -190,15 +190,15 @@ cast_step_amax_kernel(const CastDesc* __restrict__ cdescs,
     const uint32_t ab = slot_value(gslots[ch.tensor], epoch);
     const float scale = scale_from_amax_bits(ab, fp8_max_of<FMT>());
     const float ms = *sd.m_scale;
-    if (ch.index == 0 && threadIdx.x == 0) {
+    if (ch.begin == 0 && threadIdx.x == 0) {
       *cd.amax_out = __uint_as_float(ab);
       *cd.scale_out = scale;
       sc.old_m_scale[ch.tensor] = ms;
       if (sd.v_bound != nullptr) sc.old_v_bound[ch.tensor] = *sd.v_bound;
     }
     const float k = __fdiv_rn(step_ils<DEVS>(s), scale), minv = __frcp_rn(ms);
-    const int64_t begin = (int64_t)ch.index * kChunkElems;
-    const int64_t end = min(begin + kChunkElems, cd.numel);
+    const int64_t begin = ch.begin;
+    const int64_t end = begin + ch.len;
     const bool checked = ab >= 0x7F800000u;
     uint32_t mx = 0, gx = 0, bad = 0;
     if (cd.dtype == kF32)

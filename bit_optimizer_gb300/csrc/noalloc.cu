@@ -19,7 +19,7 @@
 //     limit returns FP8OPT_ERR_LIMIT and launches nothing;
 //   * one copy of the array per device, held from the moment the library's
 //     device code is loaded on that device until the process exits
-//     (kScratchBytes, about 0.6 MB);
+//     (kScratchBytes, about 1.1 MB);
 //   * every call, on every stream of a device, uses the same array, and it
 //     keeps what the last call left there.  Each call clears the amax slots it
 //     needs before its kernels run, but calls whose GPU work overlaps (two
@@ -176,7 +176,8 @@ extern "C" int fp8_cast_scaled_noalloc(const fp8opt_cast_item* items, int n,
     d.dtype = it.dtype;
     d.vec_ok = aligned_to(it.src, 16) && aligned_to(it.codes, 8);
     const uint32_t chunks = it.numel == 0 ? 1u : (uint32_t)((it.numel + kChunkElems - 1) / kChunkElems);
-    for (uint32_t c = 0; c < chunks; ++c) h_chunks[nc++] = Chunk{(uint32_t)i, c};
+    for (uint32_t c = 0; c < chunks; ++c)
+      h_chunks[nc++] = make_chunk((uint32_t)i, c, kChunkShift, it.numel);
   }
   unsigned char* base = ds->scratch;
   unsigned long long* slots = reinterpret_cast<unsigned long long*>(base + kSlotsOffset);

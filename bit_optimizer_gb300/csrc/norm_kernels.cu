@@ -79,8 +79,8 @@ grad_norm_kernel(const StepDesc* __restrict__ descs,
   for (uint32_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
     const Chunk ch = chunks[c];
     const StepDesc d = descs[ch.tensor];
-    const int64_t begin = (int64_t)ch.index * kChunkElems;
-    const int64_t end = min(begin + kChunkElems, d.numel);
+    const int64_t begin = ch.begin;
+    const int64_t end = begin + ch.len;
     if (d.g_fmt == kE4M3)
       norm_chunk<kE4M3>(d, ch, begin, end, ils, sums, found, epoch, red64, red32);
     else

@@ -207,8 +207,8 @@ reduce_amax_kernel(const ReduceDesc* __restrict__ descs,
     const Chunk ch = chunks[c];
     const ReduceDesc d = descs[ch.tensor];
     load_reciprocals(d, k, r_s);
-    const int64_t begin = (int64_t)ch.index * kChunkElems;
-    const int64_t end = min(begin + kChunkElems, d.numel);
+    const int64_t begin = ch.begin;
+    const int64_t end = begin + ch.len;
     uint32_t mx = thread_reduce_amax<IN>(d, k, r_s, post, begin, end);
     mx = block_max_u32(mx, red);
     if (threadIdx.x == 0 && mx != 0)
@@ -241,8 +241,8 @@ reduce_amax_small_kernel(const ReduceDesc* __restrict__ descs,
     float r[K];
 #pragma unroll
     for (int j = 0; j < K; ++j) r[j] = r_s[j];
-    const int64_t begin = (int64_t)ch.index * kChunkElems;
-    const int64_t end = min(begin + kChunkElems, d.numel);
+    const int64_t begin = ch.begin;
+    const int64_t end = begin + ch.len;
     const bool vec = d.vec_ok != 0;
     uint32_t mx = 0;
 #pragma unroll 1
@@ -449,12 +449,12 @@ __device__ __forceinline__ void encode_pass(const ReduceDesc* __restrict__ descs
     load_reciprocals(d, k, r_s);
     const uint32_t ab = slot_value(slots[ch.tensor], epoch);
     const float scale = scale_from_amax_bits(ab, fp8_max_of<OUT>());
-    if (ch.index == 0 && threadIdx.x == 0) {
+    if (ch.begin == 0 && threadIdx.x == 0) {
       *d.amax_out = __uint_as_float(ab);
       *d.scale_out = scale;
     }
-    const int64_t begin = (int64_t)ch.index * kChunkElems;
-    const int64_t end = min(begin + kChunkElems, d.numel);
+    const int64_t begin = ch.begin;
+    const int64_t end = begin + ch.len;
     SqAcc<OUT> acc;
     if (ab >= 0x7F800000u)
       thread_reduce_encode<IN, OUT, true, SQ>(d, k, r_s, post, scale, begin, end, acc);

@@ -234,15 +234,15 @@ step_amax_kernel(const StepDesc* __restrict__ descs,
     const Chunk ch = chunks[c];
     const StepDesc d = descs[ch.tensor];
     const float gs = *d.g_scale, ms = *d.m_scale;
-    if (ch.index == 0 && threadIdx.x == 0) {
+    if (ch.begin == 0 && threadIdx.x == 0) {
       sc.old_m_scale[ch.tensor] = ms;
       if (d.v_bound != nullptr) sc.old_v_bound[ch.tensor] = *d.v_bound;
     }
     float k = __fdiv_rn(ils_of<DEVS>(s), gs);
     if (s.clip != nullptr) k = __fmul_rn(k, *s.clip);
     const float minv = __frcp_rn(ms);
-    const int64_t begin = (int64_t)ch.index * kChunkElems;
-    const int64_t end = min(begin + kChunkElems, d.numel);
+    const int64_t begin = ch.begin;
+    const int64_t end = begin + ch.len;
     uint32_t mx = 0, gx = 0, bad = 0;
     if (d.g_fmt == kE4M3)
       step_amax_dispatch<kE4M3, L2>(d, begin, end, k, minv, s, mx, gx, bad);
@@ -509,11 +509,11 @@ step_update_kernel(const StepDesc* __restrict__ descs,
                                     __fmul_rn(s.omb2, __fmul_rn(gmax, gmax)));
       vinv = __fmul_rn(b_old, 0x1p-14f);
       vsc = v_scale_from_bound(b_new);
-      if (ch.index == 0 && threadIdx.x == 0) *d.v_bound = b_new;
+      if (ch.begin == 0 && threadIdx.x == 0) *d.v_bound = b_new;
     }
-    if (ch.index == 0 && threadIdx.x == 0) *d.m_scale = msc;
-    const int64_t begin = (int64_t)ch.index * kChunkElems;
-    const int64_t end = min(begin + kChunkElems, d.numel);
+    if (ch.begin == 0 && threadIdx.x == 0) *d.m_scale = msc;
+    const int64_t begin = ch.begin;
+    const int64_t end = begin + ch.len;
     const bool mcheck = am >= 0x7F800000u;
     uint32_t hmax = 0;
     if (d.g_fmt == kE4M3)
@@ -588,12 +588,12 @@ step_w8_kernel(const StepDesc* __restrict__ descs,
     const StepDesc d = descs[ch.tensor];
     const uint32_t ab = slot_value(sc.amax_w[ch.tensor], epoch);
     const float scale = scale_from_amax_bits(ab, 448.0f);
-    if (ch.index == 0 && threadIdx.x == 0) {
+    if (ch.begin == 0 && threadIdx.x == 0) {
       *d.w8_amax = __uint_as_float(ab);
       *d.w8_scale = scale;
     }
-    const int64_t begin = (int64_t)ch.index * kChunkElems;
-    const int64_t end = min(begin + kChunkElems, d.numel);
+    const int64_t begin = ch.begin;
+    const int64_t end = begin + ch.len;
     if (ab >= 0x7F800000u)
       thread_w8<true>(d, begin, end, scale);
     else

@@ -204,7 +204,7 @@ FP8OPT_API int fp8_adamw_step(const fp8opt_param *params, int n, float lr, float
  * owns all device memory, or services that must not stall on or fail from an
  * allocation mid-step.  fp8_cast_scaled allocates its workspace on first use;
  * this entry point instead keeps its tensor table, chunk table and amax slots
- * in one fixed array compiled into the library (about 0.6 MB per device,
+ * in one fixed array compiled into the library (about 1.1 MB per device,
  * present on every device that loads the library, until the process exits),
  * and calls no cudaMalloc, cudaFree or other allocating routine.
  *
