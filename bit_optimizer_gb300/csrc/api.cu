@@ -377,9 +377,7 @@ uint64_t chunks_of(int64_t numel, int shift) {
 #define FP8OPT_CHUNKS_PER_SM 48
 #endif
 template <class F>
-int chunk_shift_for(int n, F numel, int sms, int min_shift) {
-  int shift = kChunkShift;
-  const uint64_t target = (uint64_t)FP8OPT_CHUNKS_PER_SM * (uint64_t)sms;
+int halve_chunks(int n, F numel, uint64_t target, int shift, int min_shift) {
   while (shift > min_shift) {
     uint64_t total = 0;
     for (int i = 0; i < n && total < target; ++i) total += chunks_of(numel(i), shift);
@@ -392,6 +390,28 @@ int chunk_shift_for(int n, F numel, int sms, int min_shift) {
 // Smallest chunk shift of the cast's tables: a chunk holds at least one full
 // tile of the cast passes (8192 elements).
 constexpr int kMinShiftCast = 13;
+// A tiny list (at most kTinyElems elements, any table) gets chunks of 2048
+// elements, the update pass's tile, so that its few thousand elements spread
+// over several SMs instead of one CTA per tensor walking its tiles in turn.
+// Passes whose tiles are larger take their scalar path there, which at a
+// few elements a thread costs little.  (Larger lists keep chunks of at least
+// one full tile of every pass, so their vector paths run.)
+constexpr int kMinShiftTiny = 11;
+constexpr int64_t kTinyElems = 65536;
+
+// The chunk shift of a table: tiny lists spread over the SMs; the cast's
+// tables (cast = true) also follow FP8OPT_CHUNKS_PER_SM; the others keep
+// kChunkShift.
+template <class F>
+int chunk_shift_for(int n, F numel, int sms, bool cast) {
+  int64_t elems = 0;
+  for (int i = 0; i < n && elems <= kTinyElems; ++i) elems += numel(i);
+  if (elems <= kTinyElems)
+    return halve_chunks(n, numel, (uint64_t)sms, kChunkShift, kMinShiftTiny);
+  if (!cast) return kChunkShift;
+  return halve_chunks(n, numel, (uint64_t)FP8OPT_CHUNKS_PER_SM * (uint64_t)sms,
+                      kChunkShift, kMinShiftCast);
+}
 
 template <class T>
 bool same_list(const std::vector<T>& key, const T* items, int n) {
@@ -583,7 +603,7 @@ int ensure_cast_tables(const char* fn, Workspace* ws,
   cudaError_t ie = device_info(ws->device, &info);
   if (ie != cudaSuccess) return cuda_fail(ie, (std::string(fn) + ": device query").c_str());
   const int shift = chunk_shift_for(n, [&](int i) { return items[i].numel; },
-                                    info->sms, kMinShiftCast);
+                                    info->sms, true);
   std::vector<CastDesc> descs((size_t)n);
   std::vector<Chunk> chunks;
   size_t total = 0;
@@ -624,7 +644,11 @@ int ensure_step_tables(const char* fn, Workspace* ws, const fp8opt_param* params
   if (capturing(stream) || ws->frozen) return refuse_capture(fn);
   if ((uint32_t)n >= kMaxListTensors)
     return fail(FP8OPT_ERR_ARG, std::string(fn) + ": too many tensors");
-  const int shift = kChunkShift;
+  DeviceInfo* info = nullptr;
+  cudaError_t ie = device_info(ws->device, &info);
+  if (ie != cudaSuccess) return cuda_fail(ie, (std::string(fn) + ": device query").c_str());
+  const int shift = chunk_shift_for(n, [&](int i) { return params[i].numel; },
+                                    info->sms, false);
   std::vector<StepDesc> descs((size_t)n);
   std::vector<Chunk> chunks, chunks_o3;
   size_t total = 0;
@@ -704,7 +728,11 @@ int ensure_reduce_tables(const char* fn, Workspace* ws,
   if (capturing(stream) || ws->frozen) return refuse_capture(fn);
   if ((uint32_t)n >= kMaxListTensors)
     return fail(FP8OPT_ERR_ARG, std::string(fn) + ": too many tensors");
-  const int shift = kChunkShift;
+  DeviceInfo* info = nullptr;
+  cudaError_t ie = device_info(ws->device, &info);
+  if (ie != cudaSuccess) return cuda_fail(ie, (std::string(fn) + ": device query").c_str());
+  const int shift = chunk_shift_for(n, [&](int i) { return items[i].numel; },
+                                    info->sms, false);
   std::vector<ReduceDesc> descs((size_t)n);
   std::vector<Chunk> chunks;
   size_t total = 0;
