@@ -24,7 +24,8 @@ EXPORTS = ("fp8_cast_scaled", "fp8_adamw_step", "fp8_adam_step",
            "fp8_adam_step_begin", "fp8_adam_step_finish",
            "fp8_cast_adam_step_clipped", "fp8_reduce_scaled_norm",
            "fp8_cast_scaled_noalloc", "fp8_adam_step_dev",
-           "fp8_cast_adamw_step_dev", "fp8opt_strerror",
+           "fp8_cast_adamw_step_dev", "fp8_cast_adam_step_clipped_dev",
+           "fp8opt_strerror",
            "fp8opt_last_error", "fp8opt_timing_enable", "fp8opt_timing_read",
            "fp8opt_release", "fp8opt_release_stream")
 KERNELS = ("cast_amax", "cast_encode", "step_amax", "step_update", "step_w8",
@@ -147,6 +148,11 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     L.fp8_cast_adamw_step_dev.argtypes = [
         C.POINTER(CastItem), C.POINTER(Param), C.c_int, C.c_int, C.c_float,
         C.c_float, C.c_float, C.c_float, C.c_void_p, C.c_void_p, C.c_void_p]
+    L.fp8_cast_adam_step_clipped_dev.restype = C.c_int
+    L.fp8_cast_adam_step_clipped_dev.argtypes = [
+        C.POINTER(CastItem), C.POINTER(Param), C.c_int, C.c_int, C.c_float,
+        C.c_float, C.c_float, C.c_float, C.c_int, C.c_float, C.c_void_p,
+        C.c_void_p, C.c_void_p, C.c_void_p]
     L.fp8opt_strerror.restype = C.c_char_p
     L.fp8opt_strerror.argtypes = [C.c_int]
     L.fp8opt_last_error.restype = C.c_char_p

@@ -474,17 +474,31 @@ class CastStepPlan:
 
 
     def step_dev(self, state: StepState, beta1, beta2, eps, wd,
-                 found_inf_dev: Optional[torch.Tensor] = None,
-                 stream=None) -> None:
-        """The cast and an AdamW step with lr, inv_loss_scale and the step
-        count read from ``state`` on the device (fp8_cast_adamw_step_dev);
-        capturable, never waits (see AdamWPlan.step_dev)."""
+                 found_inf_dev: Optional[torch.Tensor] = None, stream=None,
+                 l2=False, max_grad_norm=None,
+                 grad_norm_dev: Optional[torch.Tensor] = None) -> None:
+        """The cast and a step with lr, inv_loss_scale and the step count
+        read from ``state`` on the device: AdamW through
+        fp8_cast_adamw_step_dev; with l2, max_grad_norm or grad_norm_dev
+        through fp8_cast_adam_step_clipped_dev (the norm then in
+        grad_norm_dev, a float32 CUDA scalar, if given).  Capturable, never
+        waits (see AdamWPlan.step_dev)."""
         fdev = None
         if found_inf_dev is not None:
             fdev = _cuda(found_inf_dev, "found_inf_dev").data_ptr()
-        check(load().fp8_cast_adamw_step_dev(
+        if not l2 and max_grad_norm is None and grad_norm_dev is None:
+            check(load().fp8_cast_adamw_step_dev(
+                self.cast._items, self.step_plan._params, self.cast.n,
+                self.cast.fmt, beta1, beta2, eps, wd, state.ptr, fdev,
+                _stream_ptr(stream)))
+            return
+        ndev = (None if grad_norm_dev is None
+                else _slot_ptr(grad_norm_dev, 0, "grad_norm_dev"))
+        check(load().fp8_cast_adam_step_clipped_dev(
             self.cast._items, self.step_plan._params, self.cast.n, self.cast.fmt,
-            beta1, beta2, eps, wd, state.ptr, fdev, _stream_ptr(stream)))
+            beta1, beta2, eps, wd, 1 if l2 else 0,
+            0.0 if max_grad_norm is None else float(max_grad_norm), state.ptr,
+            ndev, fdev, _stream_ptr(stream)))
 
 
 # -------------------------------------------------------------- optimizer
@@ -512,8 +526,9 @@ class Fp8AdamW:
     (``self.state``, a StepState), so ``step`` can be captured into a CUDA
     graph once and replayed every step.  ``step`` then never waits: it returns
     None, takes inv_loss_scale from ``self.state`` (write it there) and
-    reports found_inf only through found_inf_dev.  Set the learning rate with
-    ``set_lr``.  Not with max_grad_norm.
+    reports found_inf only through found_inf_dev and, with max_grad_norm,
+    the norm only through ``grad_norm_dev``.  Set the learning rate with
+    ``set_lr``.  With max_grad_norm it needs ``fused``.
     """
 
     def __init__(self, params: Sequence[torch.Tensor], lr=1e-3,
@@ -522,8 +537,8 @@ class Fp8AdamW:
                  max_grad_norm=None, capturable=False):
         if level not in ("O2", "O3"):
             raise ValueError("level must be 'O2' or 'O3'")
-        if capturable and max_grad_norm is not None:
-            raise ValueError("capturable does not support max_grad_norm")
+        if capturable and max_grad_norm is not None and not fused:
+            raise ValueError("capturable with max_grad_norm needs fused=True")
         self.params = list(params)
         for i, p in enumerate(self.params):
             _cuda(p, f"params[{i}]")
@@ -565,6 +580,9 @@ class Fp8AdamW:
         self._cast_step = None
         self.capturable = capturable
         self.state = StepState(lr, 1.0, 0, dev) if capturable else None
+        self.grad_norm_dev = (torch.zeros(1, dtype=torch.float32, device=dev)
+                              if capturable and max_grad_norm is not None
+                              else None)
 
     def set_lr(self, lr: float) -> None:
         """The learning rate of the next step (on the device when
@@ -595,11 +613,14 @@ class Fp8AdamW:
             if inv_loss_scale != 1.0:
                 raise ValueError("capturable: write inv_loss_scale into "
                                  "self.state.inv_loss_scale")
-            # fused AdamW: one call; Adam-L2 or fused=False: the cast, then
-            # the step
-            if self.fused and not self.l2:
+            # fused: one call (AdamW, or Adam-L2 / clipping through the
+            # clipped form); fused=False: the cast, then the step
+            if self.fused:
                 self._cast_step.step_dev(self.state, self.beta1, self.beta2,
-                                         self.eps, self.wd, found_inf_dev, stream)
+                                         self.eps, self.wd, found_inf_dev, stream,
+                                         l2=self.l2,
+                                         max_grad_norm=self.max_grad_norm,
+                                         grad_norm_dev=self.grad_norm_dev)
             else:
                 cast(stream)
                 self._plan.step_dev(self.state, self.beta1, self.beta2, self.eps,

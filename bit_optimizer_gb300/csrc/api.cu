@@ -42,7 +42,8 @@ cudaError_t launch_cast_encode_sq(const CastDesc* descs, const Chunk* chunks,
                                   uint32_t epoch, int fmt, int grid_encode,
                                   unsigned long long* sums,
                                   unsigned long long* found, float ils,
-                                  cudaStream_t stream, LaunchMark mark);
+                                  const float* ils_dev, cudaStream_t stream,
+                                  LaunchMark mark);
 cudaError_t cast_encode_sq_occupancy(int* per_sm);
 cudaError_t launch_cast_encode(const CastDesc* descs, const Chunk* chunks,
                                uint32_t nchunks, const unsigned long long* slots,
@@ -68,6 +69,7 @@ cudaError_t reduce_occupancy(int* amax_per_sm, int* amax_small_per_sm,
 cudaError_t reduce_encode_sq_occupancy(int* per_sm);
 cudaError_t launch_grad_norm_terms(const StepDesc* descs, const Chunk* chunks,
                                    uint32_t nchunks, int n, float ils,
+                                   const float* ils_dev,
                                    unsigned long long* sums,
                                    unsigned long long* found, uint32_t epoch,
                                    double* terms, uint32_t* found_out, int grid,
@@ -1015,8 +1017,8 @@ int adam_step(const char* fn, bool l2, const fp8opt_param* params, int n,
   cudaError_t e = cudaSuccess;
   if (nr.on) {
     e = launch_grad_norm_terms(c.descs, c.chunks, ws->step_nchunks, n,
-                               inv_loss_scale, c.sums, c.sc.found, c.epoch,
-                               c.terms, nullptr, c.info->grad_norm, stream,
+                               inv_loss_scale, nullptr, c.sums, c.sc.found,
+                               c.epoch, c.terms, nullptr, c.info->grad_norm, stream,
                                launch_mark());
     if (e == cudaSuccess)
       e = launch_clip_coef(c.terms, n, c.sc.found, c.epoch, nullptr,
@@ -1089,7 +1091,7 @@ extern "C" int fp8_grad_norm_terms(const fp8opt_param* params, int n,
   if ((st = setup_step(fn, params, n, stream_ptr, true, true, &c)) != FP8OPT_OK)
     return st;
   cudaError_t e = launch_grad_norm_terms(
-      c.descs, c.chunks, c.ws->step_nchunks, n, inv_loss_scale, c.sums,
+      c.descs, c.chunks, c.ws->step_nchunks, n, inv_loss_scale, nullptr, c.sums,
       c.sc.found, c.epoch, terms_dev, found_dev, c.info->grad_norm, stream,
       launch_mark());
   if (e != cudaSuccess) return cuda_fail(e, "fp8_grad_norm_terms: launch");
@@ -1362,22 +1364,26 @@ extern "C" int fp8_cast_adamw_step_dev(const fp8opt_cast_item* grads,
   return FP8OPT_OK;
 }
 
-extern "C" int fp8_cast_adam_step_clipped(
-    const fp8opt_cast_item* grads, const fp8opt_param* params, int n, int fmt,
-    float lr, float beta1, float beta2, float eps, float wd, int64_t step,
-    float inv_loss_scale, int l2, float max_grad_norm, double* grad_norm,
-    float* grad_norm_dev, int* found_inf, uint32_t* found_inf_dev,
-    void* stream_ptr) {
-  const char* fn = "fp8_cast_adam_step_clipped";
+// fp8_cast_adam_step_clipped, and with state set its device-resident form
+// (lr, step and inv_loss_scale from *state; host outputs not allowed).
+static int cast_adam_clipped(const char* fn, const fp8opt_cast_item* grads,
+                             const fp8opt_param* params, int n, int fmt, float lr,
+                             float beta1, float beta2, float eps, float wd,
+                             int64_t step, float inv_loss_scale, int l2,
+                             float max_grad_norm, double* grad_norm,
+                             float* grad_norm_dev, int* found_inf,
+                             uint32_t* found_inf_dev, fp8opt_step_state* state,
+                             void* stream_ptr) {
   if (l2 != 0 && l2 != 1) return fail(FP8OPT_ERR_ARG, std::string(fn) + ": l2 must be 0 or 1");
   if (std::isnan(max_grad_norm))
     return fail(FP8OPT_ERR_ARG, std::string(fn) + ": max_grad_norm is NaN");
   int st = check_cast_args(fn, grads, n, fmt);
-  if (st == FP8OPT_OK) st = check_step_args(fn, params, n, step);
+  if (st == FP8OPT_OK) st = check_step_args(fn, params, n, state ? 1 : step);
   if (st == FP8OPT_OK) st = check_takes_cast(fn, grads, params, n, fmt);
+  if (st == FP8OPT_OK && state != nullptr) st = check_dev_state(fn, state);
   if (st != FP8OPT_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  if (n == 0) {
+  if (n == 0 && state == nullptr) {
     if (grad_norm != nullptr) *grad_norm = 0.0;
     if (grad_norm_dev != nullptr) {
       cudaError_t e = cudaMemsetAsync(grad_norm_dev, 0, sizeof(float), stream);
@@ -1385,16 +1391,35 @@ extern "C" int fp8_cast_adam_step_clipped(
     }
     return empty_step(fn, found_inf, found_inf_dev, stream);
   }
-  StepScalars s = make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale,
-                               l2 != 0);
 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0;
   DeviceInfo* info = nullptr;
   if ((st = current_device_and_info(&dev, &info)) != FP8OPT_OK) return st;
   Workspace* ws = workspace(dev, stream);
-  if ((st = ensure_cast_tables(fn, ws, grads, n, stream)) != FP8OPT_OK) return st;
-  if ((st = ensure_step_tables(fn, ws, params, n, stream)) != FP8OPT_OK) return st;
+  if (n > 0) {
+    if ((st = ensure_cast_tables(fn, ws, grads, n, stream)) != FP8OPT_OK) return st;
+    if ((st = ensure_step_tables(fn, ws, params, n, stream)) != FP8OPT_OK) return st;
+  }
+  if (state != nullptr && (n == 0 || ws->step_nchunks == 0)) {
+    if (grad_norm_dev != nullptr) {
+      cudaError_t e = cudaMemsetAsync(grad_norm_dev, 0, sizeof(float), stream);
+      if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": norm_dev").c_str());
+    }
+    return empty_dev_step(fn, state, beta1, beta2, wd, l2 != 0, found_inf_dev, ws,
+                          stream);
+  }
+  StepScalars s;
+  const float* ils_dev = nullptr;
+  DevScalars* ds = nullptr;
+  if (state != nullptr) {
+    if ((st = dev_scalars_buf(fn, ws, &ds)) != FP8OPT_OK) return st;
+    s = make_dev_scalars(beta1, beta2, eps, wd, l2 != 0, ds,
+                         reinterpret_cast<long long*>(&state->step));
+    ils_dev = &ds->ils;
+  } else {
+    s = make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale, l2 != 0);
+  }
 
   // slots: [0, n) gradient amax, then the step's [n, 4n + 1) (amax of m, of
   // the master, max |g|, found_inf); norm: sums, terms, norm, clip
@@ -1428,18 +1453,23 @@ extern "C" int fp8_cast_adam_step_clipped(
   // takes the plain encode pass)
   const bool want_norm = max_grad_norm > 0.0f || grad_norm != nullptr ||
                          grad_norm_dev != nullptr;
-  e = launch_cast_amax(cdescs, cchunks, ws->cast_nchunks, slots, epoch,
-                       info->cast_amax, stream, mark);
+  if (state != nullptr)
+    e = launch_step_scalars(reinterpret_cast<DevState*>(state), beta1, beta2, wd,
+                            l2 != 0, ds, false, stream);
+  if (e == cudaSuccess)
+    e = launch_cast_amax(cdescs, cchunks, ws->cast_nchunks, slots, epoch,
+                         info->cast_amax, stream, mark);
   if (e == cudaSuccess && want_norm)
     e = launch_cast_encode_sq(cdescs, cchunks, ws->cast_nchunks, slots, epoch, fmt,
                               info->cast_encode_sq, sums, sc.found,
-                              inv_loss_scale, stream, mark);
+                              inv_loss_scale, ils_dev, stream, mark);
   if (e == cudaSuccess && !want_norm)
     e = launch_cast_encode(cdescs, cchunks, ws->cast_nchunks, slots, epoch, fmt,
                            info->cast_encode, stream, mark);
   if (e == cudaSuccess && want_norm)
-    e = launch_grad_norm_terms(sdescs, schunks, 0, n, inv_loss_scale, sums,
-                               sc.found, epoch, terms, nullptr, 0, stream, mark);
+    e = launch_grad_norm_terms(sdescs, schunks, 0, n, inv_loss_scale, ils_dev,
+                               sums, sc.found, epoch, terms, nullptr, 0, stream,
+                               mark);
   if (e == cudaSuccess && want_norm)
     e = launch_clip_coef(terms, n, sc.found, epoch, nullptr, max_grad_norm, norm,
                          clip, grad_norm_dev, stream, mark);
@@ -1454,6 +1484,32 @@ extern "C" int fp8_cast_adam_step_clipped(
   if (found_inf != nullptr || grad_norm != nullptr)
     return read_results(fn, sc.found, epoch, norm, stream, found_inf, grad_norm);
   return FP8OPT_OK;
+}
+
+extern "C" int fp8_cast_adam_step_clipped(
+    const fp8opt_cast_item* grads, const fp8opt_param* params, int n, int fmt,
+    float lr, float beta1, float beta2, float eps, float wd, int64_t step,
+    float inv_loss_scale, int l2, float max_grad_norm, double* grad_norm,
+    float* grad_norm_dev, int* found_inf, uint32_t* found_inf_dev,
+    void* stream_ptr) {
+  return cast_adam_clipped("fp8_cast_adam_step_clipped", grads, params, n, fmt, lr,
+                           beta1, beta2, eps, wd, step, inv_loss_scale, l2,
+                           max_grad_norm, grad_norm, grad_norm_dev, found_inf,
+                           found_inf_dev, nullptr, stream_ptr);
+}
+
+extern "C" int fp8_cast_adam_step_clipped_dev(
+    const fp8opt_cast_item* grads, const fp8opt_param* params, int n, int fmt,
+    float beta1, float beta2, float eps, float wd, int l2, float max_grad_norm,
+    fp8opt_step_state* state, float* grad_norm_dev, uint32_t* found_inf_dev,
+    void* stream_ptr) {
+  const char* fn = "fp8_cast_adam_step_clipped_dev";
+  const int st = check_dev_state(fn, state);   // NULL would mean the host form
+  if (st != FP8OPT_OK) return st;
+  return cast_adam_clipped(fn, grads, params, n, fmt,
+                           0.0f, beta1, beta2, eps, wd, 1, 1.0f, l2,
+                           max_grad_norm, nullptr, grad_norm_dev, nullptr,
+                           found_inf_dev, state, stream_ptr);
 }
 
 extern "C" const char* fp8opt_strerror(int status) {

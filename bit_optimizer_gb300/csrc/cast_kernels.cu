@@ -147,6 +147,7 @@ struct SqOut {
   unsigned long long* sums;
   unsigned long long* found;
   float ils;
+  const float* ils_dev;   // inv_loss_scale in device memory instead, or NULL
 };
 
 // Encode this thread's share of [begin, end).  CHECKED when the tensor holds a
@@ -258,7 +259,8 @@ __device__ __forceinline__ void encode_pass(const CastDesc* __restrict__ descs,
     else
       encode_dispatch<kF16, FMT, SQ>(d, begin, end, scale, checked, acc);
     if (SQ)
-      sq_commit<FMT>(acc, ch.tensor, end > begin, __fdiv_rn(sq.ils, scale),
+      sq_commit<FMT>(acc, ch.tensor, end > begin,
+                     __fdiv_rn(sq.ils_dev != nullptr ? *sq.ils_dev : sq.ils, scale),
                      sq.sums, sq.found, epoch, red64, red32);
   }
 }
@@ -269,7 +271,7 @@ cast_encode_kernel(const CastDesc* __restrict__ descs,
                    const Chunk* __restrict__ chunks, uint32_t nchunks,
                    const unsigned long long* __restrict__ slots,
                    uint32_t epoch) {
-  const SqOut none = {nullptr, nullptr, 0.0f};
+  const SqOut none = {nullptr, nullptr, 0.0f, nullptr};
   encode_pass<FMT, false>(descs, chunks, nchunks, slots, epoch, none, nullptr,
                           nullptr);
 }
@@ -332,16 +334,18 @@ cudaError_t launch_cast_encode(const CastDesc* descs, const Chunk* chunks,
 
 // The encode pass alone (after launch_cast_amax), also summing the exact
 // squares of the codes it writes into sums (2n zeroed words) and setting the
-// found_inf slot `found` as a step with factor inv_loss_scale / scale would.
+// found_inf slot `found` as a step with factor inv_loss_scale / scale would
+// (inv_loss_scale read from ils_dev on the device when that is set).
 cudaError_t launch_cast_encode_sq(const CastDesc* descs, const Chunk* chunks,
                                   uint32_t nchunks, const unsigned long long* slots,
                                   uint32_t epoch, int fmt, int grid_encode,
                                   unsigned long long* sums,
                                   unsigned long long* found, float ils,
-                                  cudaStream_t stream, LaunchMark mark) {
+                                  const float* ils_dev, cudaStream_t stream,
+                                  LaunchMark mark) {
   if (nchunks == 0) return cudaSuccess;
   const uint32_t ge = grid_min((uint32_t)grid_encode, nchunks);
-  const SqOut sq = {sums, found, ils};
+  const SqOut sq = {sums, found, ils, ils_dev};
   if (mark) mark(kCastEncodeK, 0, stream);
   if (fmt == kE4M3)
     cast_encode_sq_kernel<kE4M3><<<ge, kThreads, 0, stream>>>(

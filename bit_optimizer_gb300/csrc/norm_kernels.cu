@@ -71,9 +71,11 @@ __device__ __forceinline__ void norm_chunk(const StepDesc& d, const Chunk& ch,
 
 __global__ void __launch_bounds__(kThreads, 5)
 grad_norm_kernel(const StepDesc* __restrict__ descs,
-                 const Chunk* __restrict__ chunks, uint32_t nchunks, float ils,
+                 const Chunk* __restrict__ chunks, uint32_t nchunks, float ils_h,
+                 const float* __restrict__ ils_dev,
                  unsigned long long* __restrict__ sums,
                  unsigned long long* __restrict__ found, uint32_t epoch) {
+  const float ils = ils_dev != nullptr ? *ils_dev : ils_h;
   __shared__ unsigned long long red64[2 * (kThreads / 32)];
   __shared__ uint32_t red32[kThreads / 32];
   for (uint32_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
@@ -92,6 +94,7 @@ grad_norm_kernel(const StepDesc* __restrict__ descs,
 // thread per record; block 0 also exports this call's found_inf.
 __global__ void __launch_bounds__(kThreads)
 grad_norm_terms_kernel(const StepDesc* __restrict__ descs, int n, float ils,
+                       const float* __restrict__ ils_dev,
                        const unsigned long long* __restrict__ sums,
                        const unsigned long long* __restrict__ found,
                        uint32_t epoch, double* __restrict__ terms,
@@ -99,7 +102,8 @@ grad_norm_terms_kernel(const StepDesc* __restrict__ descs, int n, float ils,
   const int t = blockIdx.x * kThreads + threadIdx.x;
   if (t < n) {
     const U128 s = {sums[2 * t], sums[2 * t + 1]};
-    const float k = __fdiv_rn(ils, *descs[t].g_scale);
+    const float k = __fdiv_rn(ils_dev != nullptr ? *ils_dev : ils,
+                              *descs[t].g_scale);
     terms[t] = norm_term(s, k);
   }
   if (found_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
@@ -157,9 +161,11 @@ __global__ void found_kernel(unsigned long long* __restrict__ slot, uint32_t epo
 
 // The norm pass and the per-record terms on `stream`.  sums: 2n zeroed words;
 // found: the call's found_inf slot; terms: n doubles out; found_out: the
-// call's found_inf as 0 / 1, or NULL.
+// call's found_inf as 0 / 1, or NULL.  ils_dev: inv_loss_scale in device
+// memory instead of ils, or NULL.
 cudaError_t launch_grad_norm_terms(const StepDesc* descs, const Chunk* chunks,
                                    uint32_t nchunks, int n, float ils,
+                                   const float* ils_dev,
                                    unsigned long long* sums,
                                    unsigned long long* found, uint32_t epoch,
                                    double* terms, uint32_t* found_out, int grid,
@@ -167,13 +173,13 @@ cudaError_t launch_grad_norm_terms(const StepDesc* descs, const Chunk* chunks,
   if (nchunks != 0) {
     if (mark) mark(kGradNormK, 0, stream);
     grad_norm_kernel<<<grid_min((uint32_t)grid, nchunks), kThreads, 0, stream>>>(
-        descs, chunks, nchunks, ils, sums, found, epoch);
+        descs, chunks, nchunks, ils, ils_dev, sums, found, epoch);
     if (mark) mark(kGradNormK, 1, stream);
   }
   if (n > 0) {
     if (mark) mark(kGradNormTermsK, 0, stream);
     grad_norm_terms_kernel<<<(n + kThreads - 1) / kThreads, kThreads, 0, stream>>>(
-        descs, n, ils, sums, found, epoch, terms, found_out);
+        descs, n, ils, ils_dev, sums, found, epoch, terms, found_out);
     if (mark) mark(kGradNormTermsK, 1, stream);
   }
   return cudaGetLastError();

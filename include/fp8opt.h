@@ -306,6 +306,22 @@ FP8OPT_API int fp8_cast_adamw_step_dev(const fp8opt_cast_item *grads,
                                        uint32_t *found_inf_dev, void *stream);
 
 /*
+ * fp8_cast_adam_step_clipped_dev: fp8_cast_adam_step_clipped with lr,
+ * inv_loss_scale and the step count read from *state on the device, as
+ * fp8_adam_step_dev: the capturable form of the clipped (and Adam-L2) fused
+ * step.  max_grad_norm is fixed per call like the betas.  The norm goes to
+ * grad_norm_dev (device float, may be NULL) and found_inf to found_inf_dev
+ * (may be NULL); there are no host outputs.  Arguments, results and errors
+ * otherwise those of fp8_cast_adam_step_clipped, plus FP8OPT_ERR_ARG when
+ * state is NULL or misaligned.
+ */
+FP8OPT_API int fp8_cast_adam_step_clipped_dev(
+    const fp8opt_cast_item *grads, const fp8opt_param *params, int n, int fmt,
+    float beta1, float beta2, float eps, float wd, int l2, float max_grad_norm,
+    fp8opt_step_state *state, float *grad_norm_dev, uint32_t *found_inf_dev,
+    void *stream);
+
+/*
  * fp8_grad_norm: the global L2 norm of the unscaled gradient of a step call
  * (the quantity torch.nn.utils.clip_grad_norm_ clips; the run script's
  * --clip-grad), without a step.  Element i of record t is g = decode(g code)

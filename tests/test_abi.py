@@ -152,6 +152,15 @@ def test_device_step_argument_errors_need_no_gpu(lib):
                                      None, None) == lib.ERR_UNSUPPORTED
     assert L.fp8_cast_adamw_step_dev(item, p, 0, 0, *hp, None, None,
                                      None) == lib.ERR_ARG
+    # the clipped form: state, l2 and the threshold are checked first
+    assert L.fp8_cast_adam_step_clipped_dev(item, p, 0, 0, *hp, 0, 1.0, None,
+                                            None, None, None) == lib.ERR_ARG
+    assert L.fp8_cast_adam_step_clipped_dev(item, p, 0, 0, *hp, 2, 1.0,
+                                            C.addressof(state), None, None,
+                                            None) == lib.ERR_ARG
+    assert L.fp8_cast_adam_step_clipped_dev(item, p, 0, 0, *hp, 0, float("nan"),
+                                            C.addressof(state), None, None,
+                                            None) == lib.ERR_ARG
     # nothing was written to the state
     assert list(state) == [0, 0]
 

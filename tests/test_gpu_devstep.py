@@ -100,7 +100,9 @@ def _assert_same(host, dev, p_host, p_dev):
 @pytest.mark.parametrize("kw", [dict(level="O2"),
                                 dict(level="O3", scaled_v=True),
                                 dict(level="O2", l2=True),
-                                dict(level="O2", fused=False)])
+                                dict(level="O2", fused=False),
+                                dict(level="O2", max_grad_norm=0.05),
+                                dict(level="O3", l2=True, max_grad_norm=0.05)])
 def test_dev_step_equals_host_step(bo, kw):
     wl = dataclasses.replace(
         synth.o2_6p7b_tail(n_layer=1, d=64, ffn=256, vocab=500, ctx=64, n_tail=20),
@@ -119,6 +121,9 @@ def test_dev_step_equals_host_step(bo, kw):
         torch.cuda.synchronize()
         assert dev.state.step.item() == t == host.step_count
         _assert_same(host, dev, p_host, p_dev)
+        if "max_grad_norm" in kw:
+            # the same norm, as a float on the device
+            assert dev.grad_norm_dev.item() == np.float32(host.last_grad_norm)
 
 
 def test_dev_step_graph_replays_follow_the_schedule(bo, stream):
@@ -226,3 +231,44 @@ def test_dev_step_state_dict_round_trip(bo):
     opt2.load_state_dict(d)
     assert opt2.state.step.item() == 2
     assert opt2.state.lr.item() == np.float32(3e-4)
+
+
+def test_clipped_dev_step_graph_replays(bo, stream):
+    """A captured clipped fused step (the norm and its coefficient depend on
+    the replayed inv_loss_scale) follows the host-scalar clipped steps."""
+    wl = dataclasses.replace(
+        synth.o2_350m(n_layer=1, d=64, ffn=256, vocab=300, ctx=32), inf_site=None)
+    s = stream
+    with torch.cuda.stream(s):
+        host, dev, p_host, p_dev = _host_and_dev_pair(bo, wl, max_grad_norm=0.02)
+        grads = [torch.empty(n, dtype=torch.bfloat16, device="cuda")
+                 for n in wl.numels]
+        flag = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+        lr, ils = schedule(1)
+        for i, g in enumerate(grads):
+            g.copy_(wl.grad(i, 1, "cuda"))
+        dev.set_lr(lr)
+        dev.state.inv_loss_scale.fill_(ils)
+        dev.step(grads, found_inf_dev=flag, stream=s)
+    s.synchronize()
+    host.lr = lr
+    assert host.step(grads, ils) == 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dev.step(grads, found_inf_dev=flag, stream=s)
+    for t in range(2, 6):
+        lr, ils = schedule(t)
+        with torch.cuda.stream(s):
+            for i, x in enumerate(grads):
+                x.copy_(wl.grad(i, t, "cuda"))
+            dev.set_lr(lr)
+            dev.state.inv_loss_scale.fill_(ils)
+            g.replay()
+        s.synchronize()
+        host.lr = lr
+        assert host.step(grads, ils) == 0
+        torch.cuda.synchronize()
+        assert flag.item() == 0 and dev.state.step.item() == t
+        assert host.last_grad_norm > 0.02           # the clip is active
+        assert dev.grad_norm_dev.item() == np.float32(host.last_grad_norm)
+        _assert_same(host, dev, p_host, p_dev)
