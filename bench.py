@@ -345,8 +345,9 @@ def cpu_baseline(wl, budget_s: float):
     entries, total = oracle_sample(wl, budget_s / 2 * cores, cores)
     times, used = oracle_parallel_times(wl, entries, 1, cores)
     secs = times[0]
+    import platform
     return {"value": total / secs / 1e9, "unit": UNIT, "cores": used,
-            "kind": "oracle",
+            "kind": "oracle", "machine": platform.machine(),
             "sample": f"1 cast+step over {_describe(wl, entries, total)}, "
                       f"{secs:.1f} s, split by tensor over {used} processes",
             "single_thread": {"value": total1 / secs1 / 1e9, "unit": UNIT,
@@ -374,7 +375,7 @@ def run_reference(args, wl):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": workload_desc(wl),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": used,
-                         "kind": "oracle",
+                         "kind": "oracle", "machine": __import__("platform").machine(),
                          "sample": f"each step: cast+step over "
                                    f"{_describe(wl, entries, total)}, split by "
                                    f"tensor over {used} processes, the step-1 "
