@@ -143,8 +143,9 @@ struct DeviceInfo {
   int cast_amax = 0, cast_encode = 0;          // persistent grid sizes
   int step_amax = 0, step_update = 0, step_update_var = 0, step_w8 = 0;
   int cast_step = 0;
-  int reduce_amax = 0, reduce_amax_small = 0;
-  int reduce_encode = 0, reduce_encode_small = 0;
+  int reduce_amax = 0, reduce_encode = 0;
+  // the k-specialised passes, for k <= 2, k = 4 and k = 8
+  int reduce_amax_small[3] = {0, 0, 0}, reduce_encode_small[3] = {0, 0, 0};
   int grad_norm = 0;
   int cast_encode_sq = 0, reduce_encode_sq = 0;
 };
@@ -232,12 +233,14 @@ cudaError_t device_info(int dev, DeviceInfo** out) {
   info.step_w8 = info.sms * (c > 0 ? c : 1);
   if ((e = cast_step_occupancy(&a)) != cudaSuccess) return e;
   info.cast_step = info.sms * (a > 0 ? a : 1);
-  int d = 0;
-  if ((e = reduce_occupancy(&a, &c, &b, &d)) != cudaSuccess) return e;
+  int as[3] = {0, 0, 0}, es[3] = {0, 0, 0};
+  if ((e = reduce_occupancy(&a, as, &b, es)) != cudaSuccess) return e;
   info.reduce_amax = info.sms * (a > 0 ? a : 1);
-  info.reduce_amax_small = info.sms * (c > 0 ? c : 1);
-  info.reduce_encode_small = info.sms * (d > 0 ? d : 1);
   info.reduce_encode = info.sms * (b > 0 ? b : 1);
+  for (int i = 0; i < 3; ++i) {
+    info.reduce_amax_small[i] = info.sms * (as[i] > 0 ? as[i] : 1);
+    info.reduce_encode_small[i] = info.sms * (es[i] > 0 ? es[i] : 1);
+  }
   if ((e = grad_norm_occupancy(&a)) != cudaSuccess) return e;
   info.grad_norm = info.sms * (a > 0 ? a : 1);
   if ((e = cast_encode_sq_occupancy(&a)) != cudaSuccess) return e;
@@ -868,12 +871,14 @@ int reduce_call(const char* fn, const fp8opt_reduce_item* items, int n, int k,
   unsigned long long* slots = static_cast<unsigned long long*>(ws->slots.ptr);
   ReduceNorm norm = {static_cast<unsigned long long*>(ws->norm_buf.ptr),
                      slots + n, ils, n, terms_dev, found_dev};
+  // the k-specialised passes' grids: k <= 2, k = 4, k = 8
+  const int ks = k <= 2 ? 0 : k == 4 ? 1 : k == 8 ? 2 : -1;
   e = launch_reduce(static_cast<const ReduceDesc*>(ws->reduce_descs.ptr),
                     static_cast<const Chunk*>(ws->reduce_chunks.ptr),
                     ws->reduce_nchunks, slots, epoch, k, in_fmt, out_fmt, post,
-                    k <= 2 ? info->reduce_amax_small : info->reduce_amax,
+                    ks >= 0 ? info->reduce_amax_small[ks] : info->reduce_amax,
                     with_norm ? info->reduce_encode_sq
-                    : k <= 2  ? info->reduce_encode_small
+                    : ks >= 0 ? info->reduce_encode_small[ks]
                               : info->reduce_encode,
                     with_norm ? &norm : nullptr, stream, launch_mark());
   if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());

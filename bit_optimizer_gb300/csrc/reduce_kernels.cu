@@ -12,7 +12,7 @@
 //                         again, code = encode(y * scale).  It walks the
 //                         chunk table backwards so the chunks the first pass
 //                         read last are still in L2.
-// Bytes per element: k (first pass) + k + 1 (encode).  With one or two
+// Bytes per element: k (first pass) + k + 1 (encode).  With 1, 2, 4 or 8
 // shards both passes run in forms specialised on k (reduce_amax_small_kernel,
 // reduce_encode_small_kernel).
 //
@@ -45,15 +45,32 @@ namespace {
 #ifndef FP8OPT_REDUCE_PREFETCH
 #define FP8OPT_REDUCE_PREFETCH 1
 #endif
-// The first pass for one or two shards: 16-code groups per thread per tile
-// and resident CTAs per SM.  Measured on the 124M list with two shards (the
-// whole reduction): 0.111 ms with two groups and 4 CTAs/SM, 0.113 with four
-// groups (3 or 4 CTAs/SM), 0.119 on the general kernel.
+// The passes specialised on k (1, 2, 4 or 8 shards): 16-code groups per
+// thread per tile and resident CTAs per SM for each k.  Measured on the 124M
+// list (the whole reduction):
+//   k = 2: 0.111 ms with two groups and 4 CTAs/SM, 0.113 with four groups,
+//          0.119 on the general kernel;
+//   k = 4: 0.175 ms with two groups at 4 CTAs/SM, 0.176 with one group,
+//          0.193 on the general kernel;
+//   k = 8: 0.316 ms with one group at 3 CTAs/SM, 0.321 at 4, 0.351 on the
+//          general kernel.
 #ifndef FP8OPT_RSMALL_GROUPS
 #define FP8OPT_RSMALL_GROUPS 2
 #endif
 #ifndef FP8OPT_RSMALL_MIN_BLOCKS
 #define FP8OPT_RSMALL_MIN_BLOCKS 4
+#endif
+#ifndef FP8OPT_RSMALL_G4
+#define FP8OPT_RSMALL_G4 2
+#endif
+#ifndef FP8OPT_RSMALL_MIN_BLOCKS_K4
+#define FP8OPT_RSMALL_MIN_BLOCKS_K4 4
+#endif
+#ifndef FP8OPT_RSMALL_G8
+#define FP8OPT_RSMALL_G8 1
+#endif
+#ifndef FP8OPT_RSMALL_MIN_BLOCKS_K8
+#define FP8OPT_RSMALL_MIN_BLOCKS_K8 3
 #endif
 
 constexpr int kRGroup = 16;    // codes per vector group (one 16-byte access)
@@ -216,22 +233,34 @@ reduce_amax_kernel(const ReduceDesc* __restrict__ descs,
   }
 }
 
-constexpr int kSGroups = FP8OPT_RSMALL_GROUPS;
-constexpr int64_t kSTile = (int64_t)kThreads * kRGroup * kSGroups;
+// Groups per thread per tile and CTAs per SM of the k-specialised passes.
+template <int K>
+__host__ __device__ constexpr int small_groups() {
+  return K <= 2 ? FP8OPT_RSMALL_GROUPS : K == 4 ? FP8OPT_RSMALL_G4 : FP8OPT_RSMALL_G8;
+}
+template <int K>
+__host__ __device__ constexpr int small_min_blocks() {
+  return K <= 2   ? FP8OPT_RSMALL_MIN_BLOCKS
+         : K == 4 ? FP8OPT_RSMALL_MIN_BLOCKS_K4
+                  : FP8OPT_RSMALL_MIN_BLOCKS_K8;
+}
 
-// The first pass for K = 1 or 2 shards.  Every shard's loads for all the
-// tile's groups are issued first. Each group's sum is then reduced to its max
-// at once, not kept for the encode.  A thread thus keeps K * kSGroups 16-byte
-// loads in flight in few registers, and four CTAs fit on an SM.  The sum is
-// the same expression as in reduce_groups, so y and its max are identical.
+// The first pass for K = 1, 2, 4 or 8 shards.  Every shard's loads for all
+// the tile's groups are issued first.  Each group's sum is then reduced to
+// its max at once, not kept for the encode.  A thread thus keeps
+// K * small_groups<K>() 16-byte loads in flight in few registers, so more
+// CTAs fit on an SM than the general kernel's three.  The sum is the same
+// expression as in reduce_groups, so y and its max are identical.
 template <int IN, int K>
-__global__ void __launch_bounds__(kThreads, FP8OPT_RSMALL_MIN_BLOCKS)
+__global__ void __launch_bounds__(kThreads, small_min_blocks<K>())
 reduce_amax_small_kernel(const ReduceDesc* __restrict__ descs,
                          const Chunk* __restrict__ chunks, uint32_t nchunks,
                          float post, unsigned long long* __restrict__ slots,
                          uint32_t epoch) {
   __shared__ uint32_t red[kThreads / 32];
   __shared__ float r_s[kMaxShards];
+  constexpr int kSGroups = small_groups<K>();
+  constexpr int64_t kSTile = (int64_t)kThreads * kRGroup * kSGroups;
   const int tid = threadIdx.x;
   const float2 pp = splat2(post);
   for (uint32_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
@@ -301,6 +330,12 @@ void launch_amax(uint32_t grid, const ReduceDesc* descs, const Chunk* chunks,
   else if (k == 2)
     reduce_amax_small_kernel<IN, 2><<<grid, kThreads, 0, stream>>>(
         descs, chunks, nchunks, post, slots, epoch);
+  else if (k == 4)
+    reduce_amax_small_kernel<IN, 4><<<grid, kThreads, 0, stream>>>(
+        descs, chunks, nchunks, post, slots, epoch);
+  else if (k == 8)
+    reduce_amax_small_kernel<IN, 8><<<grid, kThreads, 0, stream>>>(
+        descs, chunks, nchunks, post, slots, epoch);
   else
     reduce_amax_kernel<IN><<<grid, kThreads, 0, stream>>>(descs, chunks, nchunks,
                                                           k, post, slots, epoch);
@@ -368,13 +403,15 @@ __device__ void thread_reduce_encode(const ReduceDesc& d, int k,
   }
 }
 
-// The encode pass's vector path for K = 1 or 2 shards (finite amax): like
-// reduce_amax_small_kernel, all loads of the tile first, then each group is
-// summed, encoded and stored at once.
+// The encode pass's vector path for K = 1, 2, 4 or 8 shards (finite amax):
+// like reduce_amax_small_kernel, all loads of the tile first, then each
+// group is summed, encoded and stored at once.
 template <int IN, int OUT, int K>
 __device__ void thread_reduce_encode_small(const ReduceDesc& d, const float* r_s,
                                            float post, float scale,
                                            int64_t begin, int64_t end) {
+  constexpr int kSGroups = small_groups<K>();
+  constexpr int64_t kSTile = (int64_t)kThreads * kRGroup * kSGroups;
   const int tid = threadIdx.x;
   const bool vec = d.vec_ok != 0;
   const float2 pp = splat2(post);
@@ -433,8 +470,8 @@ struct RedSq {
   float ils;
 };
 
-// KS: 0, or the number of shards (1 or 2) the vector path is specialised on
-// (plain encode only).
+// KS: 0, or the number of shards (1, 2, 4 or 8) the vector path is
+// specialised on (plain encode only).
 template <int IN, int OUT, bool SQ, int KS>
 __device__ __forceinline__ void encode_pass(const ReduceDesc* __restrict__ descs,
                                             const Chunk* __restrict__ chunks,
@@ -482,7 +519,7 @@ reduce_encode_kernel(const ReduceDesc* __restrict__ descs,
 }
 
 template <int IN, int OUT, int K>
-__global__ void __launch_bounds__(kThreads, FP8OPT_RSMALL_MIN_BLOCKS)
+__global__ void __launch_bounds__(kThreads, small_min_blocks<K>())
 reduce_encode_small_kernel(const ReduceDesc* __restrict__ descs,
                            const Chunk* __restrict__ chunks, uint32_t nchunks,
                            float post, const unsigned long long* __restrict__ slots,
@@ -529,21 +566,23 @@ void launch_encode(uint32_t grid, const ReduceDesc* descs, const Chunk* chunks,
                    uint32_t nchunks, int k, float post,
                    const unsigned long long* slots, uint32_t epoch, int out_fmt,
                    const RedSq* sq, cudaStream_t stream) {
-  if (sq == nullptr && k <= 2) {
-    if (out_fmt == kE4M3) {
-      if (k == 1)
-        reduce_encode_small_kernel<IN, kE4M3, 1><<<grid, kThreads, 0, stream>>>(
-            descs, chunks, nchunks, post, slots, epoch);
-      else
-        reduce_encode_small_kernel<IN, kE4M3, 2><<<grid, kThreads, 0, stream>>>(
-            descs, chunks, nchunks, post, slots, epoch);
-    } else {
-      if (k == 1)
-        reduce_encode_small_kernel<IN, kE5M2, 1><<<grid, kThreads, 0, stream>>>(
-            descs, chunks, nchunks, post, slots, epoch);
-      else
-        reduce_encode_small_kernel<IN, kE5M2, 2><<<grid, kThreads, 0, stream>>>(
-            descs, chunks, nchunks, post, slots, epoch);
+  if (sq == nullptr && (k == 1 || k == 2 || k == 4 || k == 8)) {
+    const int v = (out_fmt == kE4M3 ? 0 : 4) | (k == 1 ? 0 : k == 2 ? 1 : k == 4 ? 2 : 3);
+    switch (v) {
+#define FP8OPT_ENCODE_SMALL_CASE(OUT, KI, K)                                 \
+  case (OUT == kE4M3 ? 0 : 4) | KI:                                          \
+    reduce_encode_small_kernel<IN, OUT, K><<<grid, kThreads, 0, stream>>>(   \
+        descs, chunks, nchunks, post, slots, epoch);                         \
+    break;
+      FP8OPT_ENCODE_SMALL_CASE(kE4M3, 0, 1)
+      FP8OPT_ENCODE_SMALL_CASE(kE4M3, 1, 2)
+      FP8OPT_ENCODE_SMALL_CASE(kE4M3, 2, 4)
+      FP8OPT_ENCODE_SMALL_CASE(kE4M3, 3, 8)
+      FP8OPT_ENCODE_SMALL_CASE(kE5M2, 0, 1)
+      FP8OPT_ENCODE_SMALL_CASE(kE5M2, 1, 2)
+      FP8OPT_ENCODE_SMALL_CASE(kE5M2, 2, 4)
+      FP8OPT_ENCODE_SMALL_CASE(kE5M2, 3, 8)
+#undef FP8OPT_ENCODE_SMALL_CASE
     }
   } else if (sq == nullptr) {
     if (out_fmt == kE4M3)
@@ -564,9 +603,9 @@ void launch_encode(uint32_t grid, const ReduceDesc* descs, const Chunk* chunks,
 
 }  // namespace
 
-// Launches both passes on `stream`; 1 <= k <= kMaxShards.  With k <= 2 the
-// grids are sized for the small-k kernels (the first pass, and the encode
-// pass when no norm is asked for).  With norm set,
+// Launches both passes on `stream`; 1 <= k <= kMaxShards.  With k in {1, 2,
+// 4, 8} the grids are sized for the k-specialised kernels (the first pass,
+// and the encode pass when no norm is asked for).  With norm set,
 // the encode pass also sums the exact squares of the codes it writes into
 // norm->sums (2n zeroed words; found_inf into norm->found), and a last kernel
 // writes each item's norm term and the found flag.
@@ -612,20 +651,31 @@ cudaError_t reduce_encode_sq_occupancy(int* per_sm) {
 }
 
 // Resident CTAs per SM of the reduction kernels: the first and the encode
-// pass, each in its general and its small-k form.
+// pass in their general form, and in the forms specialised on k for k <= 2,
+// k = 4 and k = 8 (amax_small and encode_small: three entries each).
 cudaError_t reduce_occupancy(int* amax_per_sm, int* amax_small_per_sm,
                              int* encode_per_sm, int* encode_small_per_sm) {
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       amax_per_sm, reduce_amax_kernel<kE4M3>, kThreads, 0);
   if (e != cudaSuccess) return e;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      amax_small_per_sm, reduce_amax_small_kernel<kE4M3, 2>, kThreads, 0);
-  if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      encode_small_per_sm, reduce_encode_small_kernel<kE4M3, kE4M3, 2>, kThreads, 0);
-  if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       encode_per_sm, reduce_encode_kernel<kE4M3, kE4M3>, kThreads, 0);
+  if (e != cudaSuccess) return e;
+  const void* amax_k[3] = {(const void*)reduce_amax_small_kernel<kE4M3, 2>,
+                           (const void*)reduce_amax_small_kernel<kE4M3, 4>,
+                           (const void*)reduce_amax_small_kernel<kE4M3, 8>};
+  const void* encode_k[3] = {(const void*)reduce_encode_small_kernel<kE4M3, kE4M3, 2>,
+                             (const void*)reduce_encode_small_kernel<kE4M3, kE4M3, 4>,
+                             (const void*)reduce_encode_small_kernel<kE4M3, kE4M3, 8>};
+  for (int i = 0; i < 3; ++i) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&amax_small_per_sm[i],
+                                                      amax_k[i], kThreads, 0);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&encode_small_per_sm[i],
+                                                      encode_k[i], kThreads, 0);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace fp8opt

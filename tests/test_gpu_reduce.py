@@ -89,7 +89,7 @@ def test_gpt_list_cast_shards(bo, k, in_fmt, out_fmt):
     assert compare(bo, shards, in_fmt, out_fmt, 1.0 / k) == 1.0
 
 
-@pytest.mark.parametrize("k", [1, 2, 3, 5, 64])
+@pytest.mark.parametrize("k", [1, 2, 3, 4, 5, 8, 64])
 def test_ragged_sizes_many_k(bo, k):
     sizes = [0, 1, 15, 16, 17, 4095, 8191, 8192, 8193, 32767, 32768, 32769, 100003]
     if k == 64:
@@ -98,7 +98,7 @@ def test_ragged_sizes_many_k(bo, k):
     assert compare(bo, shards, E4M3, E4M3, 1.0) == 1.0
 
 
-@pytest.mark.parametrize("k", [1, 2, 4])
+@pytest.mark.parametrize("k", [1, 2, 4, 8])
 def test_padded_stride_and_unaligned_stride(bo, k):
     shards = random_shards(np.random.default_rng(9), [5000, 40000, 33], k, E5M2)
     # stride numel + 16k: vector path where numel is a multiple of 16
