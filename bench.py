@@ -79,6 +79,9 @@ def parse():
     p.add_argument("--reduce-only", type=int, default=None, metavar="K",
                    help="time only the local FP8 reduction of K shards of the "
                         "124M list and print its line (profiling case)")
+    p.add_argument("--cast-only", default=None, choices=["e4m3", "e5m2"],
+                   help="time only the scaled cast of the 124M list to this "
+                        "format and print its line (profiling case)")
     return p.parse_args()
 
 
@@ -460,6 +463,33 @@ def _events_ms(fn, reps):
     return a.elapsed_time(b) / reps
 
 
+def cast_configs(device, peak, fmts=("e4m3", "e5m2")):
+    """The scaled cast of the 124M GPT-2 list (BF16 in, per-tensor
+    just-in-time scale): amax pass 2 B + encode pass 3 B per element."""
+    import torch
+    import synth
+    import bit_optimizer_gb300 as bo
+    out = {}
+    wl = synth.gpt2_cast()
+    srcs = bo.arena_views(wl.numels, torch.bfloat16, device)
+    for i, x in enumerate(srcs):
+        x.copy_(wl.grad(i, 1, device))
+    codes = bo.arena_views(wl.numels, torch.uint8, device)
+    amax = torch.empty(len(srcs), device=device)
+    scale = torch.empty(len(srcs), device=device)
+    for fmt in fmts:
+        plan = bo.CastPlan(srcs, codes, amax, scale, fmt)
+        for _ in range(3):
+            plan()
+        ms = _events_ms(plan, 20)
+        gbs = 5 * wl.n_params / (ms * 1e-3) / 1e9
+        out[f"cast_gpt2_124m_{fmt}"] = {"ms": ms, "GB/s": gbs, "frac": gbs / peak,
+                                        "bytes_per_elem": 5}
+    del srcs, codes
+    torch.cuda.empty_cache()
+    return out
+
+
 def reduce_configs(device, peak, ranks=(2, 8)):
     """The local FP8 reduction on the 124M GPT-2 list: k shards per tensor
     (each rank's BF16 gradient cast to E4M3 by the library, rows of a
@@ -511,23 +541,7 @@ def other_configs(device, peak):
     import torch
     import synth
     import bit_optimizer_gb300 as bo
-    out = {}
-    wl = synth.gpt2_cast()
-    srcs = bo.arena_views(wl.numels, torch.bfloat16, device)
-    for i, x in enumerate(srcs):
-        x.copy_(wl.grad(i, 1, device))
-    codes = bo.arena_views(wl.numels, torch.uint8, device)
-    amax = torch.empty(len(srcs), device=device)
-    scale = torch.empty(len(srcs), device=device)
-    for fmt in ("e4m3", "e5m2"):
-        plan = bo.CastPlan(srcs, codes, amax, scale, fmt)
-        for _ in range(3):
-            plan()
-        ms = _events_ms(plan, 20)
-        gbs = 5 * wl.n_params / (ms * 1e-3) / 1e9
-        out[f"cast_gpt2_124m_{fmt}"] = {"ms": ms, "GB/s": gbs, "frac": gbs / peak,
-                                        "bytes_per_elem": 5}
-    del srcs, codes
+    out = cast_configs(device, peak)
     out.update(reduce_configs(device, peak))
     # (name, workload, reps, optimizer options, algorithmic bytes per param)
     runs = (
@@ -867,6 +881,12 @@ def main():
         peak, _ = measured_peak()
         print(json.dumps(reduce_configs(torch.device("cuda", 0), peak,
                                         ranks=(args.reduce_only,))), flush=True)
+        return
+    if args.cast_only is not None:
+        import torch
+        peak, _ = measured_peak()
+        print(json.dumps(cast_configs(torch.device("cuda", 0), peak,
+                                      fmts=(args.cast_only,))), flush=True)
         return
     import dataclasses
     import synth
