@@ -3,14 +3,16 @@
 // Work decomposition (multi-tensor chunk table): every tensor of a call is cut
 // into chunks of 2^shift elements (the last chunk of a tensor may be shorter;
 // an empty tensor gets one empty chunk so that its per-tensor outputs are
-// still written).  The shift is kChunkShift (32768 elements), smaller in the
-// cast's tables of lists too short to give every SM several chunks; each
-// chunk carries its first element and length.  The host builds the chunk
-// table once per tensor list and caches it on the device.  Each kernel is a persistent grid (a multiple
-// of the SM count) whose CTAs stride over the chunk table; a CTA handles one
-// chunk at a time in tiles of kTileElems elements: thread t takes the 8-element
-// groups starting at tile + k * (kThreads * 8) + t * 8 for k = 0, 1, so every
-// load and store instruction of a warp touches one contiguous span.
+// still written).  The shift is kChunkShift (32768 elements); the host picks
+// a smaller one for the cast's tables of short lists and for every table of
+// a tiny list, and each chunk carries its first element and length.  The host
+// builds the chunk table once per tensor list and caches it on the device.
+// Each kernel is a persistent grid (a multiple of the SM count) whose CTAs
+// stride over the chunk table; a CTA handles one chunk at a time in tiles:
+// thread t of an N-thread CTA takes the groups of G elements starting at
+// tile + k * (N * G) + t * G, so every load and store instruction of a warp
+// touches one contiguous span.  Each pass sets its own N, G and groups per
+// tile.
 //
 // Per-tensor reductions (amax) and the found_inf flag live in 64-bit slots
 // tagged with a per-call epoch in the high word: a slot is current only when
@@ -28,7 +30,6 @@ namespace fp8opt {
 
 constexpr int kThreads = 256;                    // threads per CTA
 constexpr int kGroup = 8;                        // elements per vector group
-constexpr int kTileElems = kThreads * kGroup * 2;  // 4096 elements per tile
 constexpr int kChunkShift = 15;                  // 32768 elements per chunk
 constexpr int64_t kChunkElems = (int64_t)1 << kChunkShift;
 
