@@ -100,7 +100,8 @@ def workload_desc(wl):
         "level": wl.level,
         "grad_dtype": str(wl.grad_dtype).replace("torch.", ""),
         "grad_fmt": wl.grad_fmt,
-        "step": "fp8_cast_adamw_step (BF16 grads -> E4M3, then the AdamW step)",
+        "step": (f"fp8_cast_adamw_step ({str(wl.grad_dtype).replace('torch.', '')} "
+                 f"grads -> {wl.grad_fmt.upper()}, then the AdamW step)"),
         "bytes_per_param": STEP_BYTES[wl.level],
         "l2": "inputs larger than L2 (no flush needed)" if wl.n_params > 1e8
               else "inputs smaller than L2",
