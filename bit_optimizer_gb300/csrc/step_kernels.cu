@@ -385,9 +385,11 @@ __device__ void thread_update(const StepDesc& d, int64_t begin, int64_t end,
         uint4 vo, wo;
         update8<GF, O3, MCHECK, VS, L2>(gc[q], mc[q], vh[q], wh[q], c, mo, vo, wo,
                                         hmax);
-        *reinterpret_cast<uint2*>(d.m + i0) = mo;
-        *reinterpret_cast<uint4*>(d.v + i0) = vo;
-        *reinterpret_cast<uint4*>(d.w + i0) = wo;
+        // streaming stores (evict-first): the new state is not read again
+        // in this call.  Measured on the 6.7B list: 11.43 ms against 11.53.
+        __stcs(reinterpret_cast<uint2*>(d.m + i0), mo);
+        __stcs(reinterpret_cast<uint4*>(d.v + i0), vo);
+        __stcs(reinterpret_cast<uint4*>(d.w + i0), wo);
       }
     } else {
 #pragma unroll 1
