@@ -122,7 +122,7 @@ CASES = {
 
 
 @pytest.mark.parametrize("case,world", [(c, 2) for c in sorted(CASES)] +
-                         [("o3_clip", 3)])
+                         [("o3_clip", 3), ("o3_clip", 4)])
 def test_cpu_ranks_match_the_whole_pipeline(case, world, tmp_path):
     import torch.multiprocessing as mp
     cfg = CASES[case]
