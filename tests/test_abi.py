@@ -262,3 +262,24 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(TypeError):
         bo.CastPlan([torch.zeros(4)], [torch.zeros(4, dtype=torch.uint8)],
                     torch.zeros(1), torch.zeros(1))
+
+
+def test_step_state_views_match_the_c_layout(lib):
+    """StepState's lr, inv_loss_scale and step are views of one 16-byte
+    buffer at the offsets of fp8opt_step_state (checked here on a CPU
+    buffer)."""
+    import struct
+    import torch
+    from bit_optimizer_gb300.api import StepState
+    st = StepState(lr=3e-4, inv_loss_scale=2.0 ** -16, step=41, device="cpu")
+    raw = st.buf.numpy().tobytes()
+    assert len(raw) == 16
+    lr, ils, step = struct.unpack("<ffq", raw)
+    assert lr == struct.unpack("<f", struct.pack("<f", 3e-4))[0]
+    assert ils == 2.0 ** -16 and step == 41
+    st.step.add_(1)
+    st.lr.fill_(1e-3)
+    lr, ils, step = struct.unpack("<ffq", st.buf.numpy().tobytes())
+    assert step == 42 and lr == struct.unpack("<f", struct.pack("<f", 1e-3))[0]
+    assert st.step.dtype == torch.int64 and st.lr.dtype == torch.float32
+
