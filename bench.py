@@ -415,11 +415,19 @@ TRAFFIC_SUMMARY = "profiles/step_update_o2_1layer.md"
 
 
 def kernel_source_digest():
+    """First 16 hex digits of sha256 over the kernel sources with their
+    comments and whitespace removed: a comment edit leaves the kernels, and
+    so the recorded traffic, unchanged.  (The sources have no comment
+    markers inside string literals.)"""
     import hashlib
+    import re
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -77,8 +77,8 @@ namespace {
 // Tiles ahead of the current one that the update and amax passes prefetch
 // into L2 (0: none).  Measured on the 6.7B list: the update pass is 7 %
 // slower with a prefetch one or two tiles ahead, and the amax pass 4 - 5 %
-// slower, so both are off.  The amax pass (clipped 6.7B step, another
-// box): 2.13 ms with eight groups in flight, 2.21 with four, 2.26 with two.
+// slower, so both are off.  The amax pass (clipped 6.7B step, a separate
+// run): 2.13 ms with eight groups in flight, 2.21 with four, 2.26 with two.
 #ifndef FP8OPT_UPD_PREFETCH
 #define FP8OPT_UPD_PREFETCH 0
 #endif
