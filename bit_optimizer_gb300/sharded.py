@@ -134,7 +134,7 @@ class LibEngine:
         clip_coef(terms, max_grad_norm, clip, norm, found)
 
 
-# ----------------------------------------------------------------- driver
+# ------------------------------------------------------------ the step loop
 
 def _offsets(views, base) -> List[int]:
     """Element offsets of arena views in their base buffer."""

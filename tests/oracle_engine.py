@@ -1,6 +1,6 @@
 """The sharded step's arithmetic by the oracle, on host tensors: an engine
 with the methods of ``bit_optimizer_gb300.sharded.LibEngine``, so the sharded
-driver's host logic (partition, exchanges, skip, broadcasts) can run on CPU
+step loop's host logic (partition, exchanges, skip, broadcasts) can run on CPU
 ranks over gloo.  Test infrastructure only."""
 import math
 
