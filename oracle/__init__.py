@@ -27,19 +27,25 @@ _LIB_PATH = os.path.join(_HERE, "_build", "liboracle_fp8opt.so")
 _lib = None
 
 
+def compile_library(src: str, out: str) -> str:
+    """Compile a C source with the oracle's flags into the shared library
+    ``out`` (written atomically); return ``out``."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.check_call([
+        "gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
+        "-fno-fast-math", "-fno-finite-math-only", "-Wall", "-o", tmp, src,
+        "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle into a shared library (gcc); return its path."""
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
-    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.check_call([
-        "gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
-        "-fno-fast-math", "-fno-finite-math-only", "-Wall", "-o", tmp, _SRC,
-        "-lm"])
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    return compile_library(_SRC, _LIB_PATH)
 
 
 class Param(C.Structure):
@@ -53,9 +59,13 @@ class Param(C.Structure):
 
 
 def lib():
+    """The loaded oracle.  ``FP8OPT_ORACLE_LIB`` may name another build of
+    the same C source (the mutation test plants one mistake in a copy and
+    checks that the pins fail on it); otherwise the library ``build()``
+    makes."""
     global _lib
     if _lib is None:
-        L = C.CDLL(build())
+        L = C.CDLL(os.environ.get("FP8OPT_ORACLE_LIB") or build())
         L.oracle_fp8_decode.restype = C.c_float
         L.oracle_fp8_decode.argtypes = [C.c_uint8, C.c_int]
         L.oracle_fp8_encode.restype = C.c_uint8

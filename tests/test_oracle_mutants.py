@@ -1,0 +1,147 @@
+"""Mutation check of the oracle's pins.
+
+Each case plants one plausible mistake in a copy of the C oracle (a dropped
+term, a wrong operand, a missing clamp), builds that copy with the oracle's
+own flags under ``oracle/_build/mutants``, and runs the oracle's pin tests
+against it through ``FP8OPT_ORACLE_LIB``.  Every case must make at least one
+pin fail; a mistake that no pin catches would be a hole in the pins.  The
+unchanged source, built the same way, must pass them all, so a failure is
+the planted mistake's and not the harness's.  CPU only.
+"""
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "fp8opt_oracle.c")
+OUT = os.path.join(ROOT, "oracle", "_build", "mutants")
+
+PINS = ("codec", "cast", "step", "reduce", "clip")
+
+# (name, text in the oracle, planted replacement, pin file tried first)
+MUTANTS = [
+    # OCP 8-bit formats (TransformerEngine issue #131; the formats' definition)
+    ("round_half_away", "return rint(a / q) * q;", "return floor(a / q + 0.5) * q;",
+     "codec"),
+    ("no_saturation", "if (r > f->maxval) r = f->maxval;", "(void)0;", "codec"),
+    ("e4m3_max_480", "{3, 7, 448.0, 0},", "{3, 7, 480.0, 0},", "codec"),
+    ("subnormal_exponent", "v = ldexp((double)m, 1 - f->bias - f->mbits);",
+     "v = ldexp((double)m, -f->bias - f->mbits);", "codec"),
+    ("f16_overflow_saturates", "bits = (r > OR_HALF.maxval) ? 0x7C00u",
+     "bits = (r > OR_HALF.maxval) ? 0x7BFFu", "codec"),
+    ("e5m2_inf_to_nan", "return f->has_inf ? (neg ? 0xFC : 0x7C) : 0x7F;",
+     "return 0x7F;", "codec"),
+    # scaled cast, just-in-time per-tensor scale (MS-AMP O1)
+    ("amax_signed", "else if (fabsf(x) > a->fin) a->fin = fabsf(x);",
+     "else if (x > a->fin) a->fin = x;", "cast"),
+    ("scale_inverted", "float q = (float)OR_FMT[fmt].maxval / amax;",
+     "float q = amax / (float)OR_FMT[fmt].maxval;", "cast"),
+    ("nan_below_inf", "if (a->nan) return or_bits_f32(0x7FC00000u);\n    if (a->inf)",
+     "if (a->inf) return INFINITY;\n    if (a->nan)", "cast"),
+    ("cast_unscaled", "float t = x * scale;", "float t = x;", "cast"),
+    # AdamW / Adam step with FP8 m and FP16 v (MS-AMP O2 / O3; torch AdamW)
+    ("eps_inside_root", "float denom = fmaf(sqrtf(v), s.inv_sbc2, eps);",
+     "float denom = sqrtf(v * s.inv_sbc2 * s.inv_sbc2 + eps);", "step"),
+    ("no_sqrt", "float denom = fmaf(sqrtf(v), s.inv_sbc2, eps);",
+     "float denom = fmaf(v, s.inv_sbc2, eps);", "step"),
+    ("no_weight_decay", "float w = fmaf(-s.step_size, upd, wp * s.decay);",
+     "float w = fmaf(-s.step_size, upd, wp);", "step"),
+    ("no_first_bias_correction", "s.step_size = (float)((double)lr / bc1);",
+     "s.step_size = lr; (void)bc1;", "step"),
+    ("no_second_bias_correction", "s.inv_sbc2 = (float)(1.0 / sqrt(bc2));",
+     "s.inv_sbc2 = 1.0f; (void)bc2;", "step"),
+    ("bias_power_every_bit", "if (t & 1) r = r * b;", "r = r * b;", "step"),
+    ("no_unscale", "return inv_loss_scale / p->g_scale;",
+     "(void)inv_loss_scale; return 1.0f / p->g_scale;", "step"),
+    ("m_with_beta2", "return fmaf(beta1, mp, s->omb1 * g);",
+     "return fmaf(1.0f - s->omb2, mp, s->omb1 * g);", "step"),
+    ("v_with_beta1", "float v = fmaf(beta2, vp, s.omb2 * (g * g));",
+     "float v = fmaf(beta1, vp, s.omb1 * (g * g));", "step"),
+    ("m_not_dequantized", "float mp = oracle_fp8_decode(p->m[i], OR_E4M3) * minv;",
+     "float mp = oracle_fp8_decode(p->m[i], OR_E4M3); (void)minv;", "step"),
+    ("m_encoded_unscaled", "q->m[i] = oracle_fp8_encode(m * m_scale_new, OR_E4M3);",
+     "q->m[i] = oracle_fp8_encode(m, OR_E4M3);", "step"),
+    ("copy_amax_from_fp32", "if (q->w8) or_amax_add(&aw, oracle_f16_to_f32(q->w[i]));",
+     "if (q->w8) or_amax_add(&aw, w);", "step"),
+    ("found_inf_ignored", "if (!isfinite(or_grad(&p[t], k, i))) return 1;",
+     "(void)0;", "step"),
+    ("l2_term_dropped", "return l2 ? fmaf(wd, oracle_f16_to_f32(p->w[i]), g) : g;",
+     "(void)wd; return g;", "step"),
+    ("l2_also_decays", "s.decay = l2 ? 1.0f : 1.0f - lr * wd;",
+     "s.decay = 1.0f - lr * wd;", "step"),
+    ("scaled_v_not_rescaled", "if (scaled_v) vp = vp * vinv;", "(void)vinv;", "step"),
+    ("scaled_v_bound_forgets", "b_new = fmaf(beta2, *q->v_bound, s.omb2 * (gmax * gmax));",
+     "b_new = s.omb2 * (gmax * gmax);", "step"),
+    # local reduction of FP8 shards (MS-AMP O1, FP8 all-reduce)
+    ("reduce_divides", "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) * r[j];",
+     "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) / scales[j];",
+     "reduce"),
+    ("reduce_one_scale", "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) * r[j];",
+     "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) * r[0];",
+     "reduce"),
+    ("reduce_no_post", "y[i] = acc * post;", "y[i] = acc; (void)post;", "reduce"),
+    ("reduce_stride_as_numel", "src[(int64_t)j * stride + i]", "src[(int64_t)j * numel + i]",
+     "reduce"),
+    ("reduce_drops_last_shard", "for (int j = 1; j < k; ++j)\n            acc",
+     "for (int j = 1; j < k - 1; ++j)\n            acc", "reduce"),
+    # global gradient norm and clipping (torch clip_grad_norm_)
+    ("norm_sum_not_squared", "sum += (unsigned __int128)q * q;",
+     "sum += (unsigned __int128)q * 65536u;", "clip"),
+    ("norm_k_not_squared", "double kk = (double)k * (double)k;", "double kk = (double)k;",
+     "clip"),
+    ("norm_unit_dropped", "terms[t] = kk * ldexp((double)sum, -32);",
+     "terms[t] = kk * (double)sum;", "clip"),
+    ("clip_no_epsilon", "double c = (double)max_norm / (norm + 1e-6);",
+     "double c = (double)max_norm / norm;", "clip"),
+    ("clip_unclamped", "return c < 1.0 ? (float)c : 1.0f;", "return (float)c;", "clip"),
+    ("clip_unused", "if (clip != 1.0f) k = k * clip;", "(void)clip;", "clip"),
+]
+
+
+def _mutant_source(text, old, new):
+    assert text.count(old) == 1, f"planted text not unique in the oracle: {old!r}"
+    return text.replace(old, new)
+
+
+def _run_pins(lib_path, first):
+    order = [first] + [p for p in PINS if p != first]
+    files = [os.path.join("tests", f"test_oracle_{p}.py") for p in order]
+    env = dict(os.environ, FP8OPT_ORACLE_LIB=lib_path)
+    r = subprocess.run([sys.executable, "-m", "pytest", *files, "-x", "-q",
+                        "-p", "no:cacheprovider", "-m", "not gpu"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return r.returncode, r.stdout[-1500:] + r.stderr[-500:]
+
+
+def _build_and_run(name, text, first):
+    import oracle
+    src = os.path.join(OUT, f"{name}.c")
+    with open(src, "w") as f:
+        f.write(text)
+    lib = oracle.compile_library(src, os.path.join(OUT, f"lib{name}.so"))
+    return name, _run_pins(lib, first)
+
+
+def test_mutant_names_are_unique():
+    names = [m[0] for m in MUTANTS]
+    assert len(set(names)) == len(names)
+    assert all(m[3] in PINS for m in MUTANTS)
+
+
+def test_every_planted_mistake_fails_a_pin():
+    text = open(SRC).read()
+    jobs = [("control", text, "codec")]
+    jobs += [(name, _mutant_source(text, old, new), first)
+             for name, old, new, first in MUTANTS]
+    os.makedirs(OUT, exist_ok=True)
+    workers = max(1, min(8, os.cpu_count() or 1))
+    with ThreadPoolExecutor(workers) as ex:
+        results = dict(ex.map(lambda j: _build_and_run(*j), jobs))
+    rc, out = results.pop("control")
+    assert rc == 0, f"the unchanged oracle fails its pins:\n{out}"
+    survivors = {n: out for n, (rc, out) in results.items() if rc != 1}
+    assert not survivors, "planted mistakes no pin caught (or a harness error):\n" + \
+        "\n".join(f"--- {n} (rc {results[n][0]})\n{o}" for n, o in survivors.items())
