@@ -409,8 +409,10 @@ def build_state(wl, device, **opt_kw):
     return params, grads, flat, opt
 
 
+# the update kernel and the host code that sizes its grid and chunk table
 KERNEL_SOURCES = ("bit_optimizer_gb300/csrc/step_kernels.cu",
-                  "bit_optimizer_gb300/csrc/fp8opt_internal.cuh")
+                  "bit_optimizer_gb300/csrc/fp8opt_internal.cuh",
+                  "bit_optimizer_gb300/csrc/api.cu")
 TRAFFIC_SUMMARY = "profiles/step_update_o2_1layer.md"
 
 
