@@ -164,6 +164,31 @@ def test_clipped_step_with_found_inf_writes_nothing(orc):
             assert np.array_equal(getattr(a, f), getattr(b, f)), f
 
 
+def test_found_inf_is_decided_before_clipping(orc):
+    """torch's recipe unscales the gradients (finding any inf) before
+    clip_grad_norm_ runs: a gradient that overflows fp32 when unscaled skips
+    the step even where the clip coefficient would bring it back in range."""
+    rng = np.random.default_rng(14)
+    states = make_states(orc, [50, 70], rng)
+    s = states[0]
+    s.g[:] = 0
+    s.g[9] = 0x7E                                 # 448
+    s.g_scale = float(np.float32(2.0 ** -120))    # 448 * 2^120 > fp32 max
+    clip = 2.0 ** -8                              # 448 * 2^112 is finite
+    grads = [(tdec(x.g, x.g_fmt).float() * (np.float32(1.0) / np.float32(x.g_scale)))
+             for x in states]
+    flag = torch.zeros(1)
+    torch._amp_foreach_non_finite_check_and_unscale_(
+        grads, flag, torch.tensor(1.0, dtype=torch.float32))
+    assert flag.item() == 1
+    assert np.isfinite(np.float32(448.0) * (np.float32(2.0 ** 120) * np.float32(clip)))
+    before = [x.copy() for x in states]
+    assert orc.adam_step_coef(states, 1e-3, 0.9, 0.999, 1e-8, 0.01, 2, 1.0, clip) == 1
+    for a, b in zip(states, before):
+        for f in ("m", "v", "w", "m_scale"):
+            assert np.array_equal(getattr(a, f), getattr(b, f)), f
+
+
 def test_step_with_a_given_coefficient_is_the_clipped_step(orc):
     rng = np.random.default_rng(11)
     args = (1e-3, 0.9, 0.999, 1e-8, 0.01, 2, 1.0)

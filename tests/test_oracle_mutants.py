@@ -34,6 +34,16 @@ MUTANTS = [
      "bits = (r > OR_HALF.maxval) ? 0x7BFFu", "codec"),
     ("e5m2_inf_to_nan", "return f->has_inf ? (neg ? 0xFC : 0x7C) : 0x7F;",
      "return 0x7F;", "codec"),
+    ("e4m3_inf_saturates", "return f->has_inf ? (neg ? 0xFC : 0x7C) : 0x7F;",
+     "return f->has_inf ? (neg ? 0xFC : 0x7C) : (neg ? 0xFE : 0x7E);", "codec"),
+    ("e5m2_nan_decodes_inf",
+     "if (m != 0) return or_bits_f32(0x7FC00000u);\n        v = INFINITY;",
+     "v = INFINITY;", "codec"),
+    ("negative_zero_unsigned", "int neg = signbit(x) != 0;\n    if (isinf(x))",
+     "int neg = x < 0;\n    if (isinf(x))", "codec"),
+    ("f16_subnormal_unclamped",
+     "        lead = e - 1;\n        if (lead < emin) lead = emin;",
+     "        lead = e - 1;", "codec"),
     # scaled cast, just-in-time per-tensor scale (MS-AMP O1)
     ("amax_signed", "else if (fabsf(x) > a->fin) a->fin = fabsf(x);",
      "else if (x > a->fin) a->fin = x;", "cast"),
@@ -42,6 +52,11 @@ MUTANTS = [
     ("nan_below_inf", "if (a->nan) return or_bits_f32(0x7FC00000u);\n    if (a->inf)",
      "if (a->inf) return INFINITY;\n    if (a->nan)", "cast"),
     ("cast_unscaled", "float t = x * scale;", "float t = x;", "cast"),
+    ("tiny_amax_scale_unguarded", "if (!isfinite(q)) return 1.0f;\n    return q;",
+     "return q;", "cast"),
+    ("f16_source_as_bf16",
+     "default: return oracle_f16_to_f32(((const uint16_t *)src)[i]);",
+     "default: return oracle_bf16_to_f32(((const uint16_t *)src)[i]);", "cast"),
     # AdamW / Adam step with FP8 m and FP16 v (MS-AMP O2 / O3; torch AdamW)
     ("eps_inside_root", "float denom = fmaf(sqrtf(v), s.inv_sbc2, eps);",
      "float denom = sqrtf(v * s.inv_sbc2 * s.inv_sbc2 + eps);", "step"),
@@ -75,6 +90,19 @@ MUTANTS = [
     ("scaled_v_not_rescaled", "if (scaled_v) vp = vp * vinv;", "(void)vinv;", "step"),
     ("scaled_v_bound_forgets", "b_new = fmaf(beta2, *q->v_bound, s.omb2 * (gmax * gmax));",
      "b_new = s.omb2 * (gmax * gmax);", "step"),
+    ("m_scale_not_stored", "*q->m_scale = m_scale_new;", "(void)0;", "step"),
+    ("v_bound_not_stored", "if (scaled_v) *q->v_bound = b_new;", "(void)0;", "step"),
+    ("scaled_v_stored_unscaled",
+     "q->v[i] = oracle_f32_to_f16(scaled_v ? v * v_scale_new : v);",
+     "q->v[i] = oracle_f32_to_f16(v); (void)v_scale_new;", "step"),
+    ("w8_amax_reports_scale", "*q->w8_amax = amax_w;", "*q->w8_amax = w8_scale;", "step"),
+    ("w8_off_by_a_ulp",
+     "q->w8[i] = oracle_fp8_encode(oracle_f16_to_f32(q->w[i]) * w8_scale,",
+     "q->w8[i] = oracle_fp8_encode(oracle_f16_to_f32(q->w[i]) * w8_scale * 1.0009765625f,",
+     "step"),
+    ("l2_found_inf_after_decay", "if (!isfinite(or_grad(&p[t], k, i))) return 1;",
+     "if (!isfinite(or_grad_l2(&p[t], or_grad(&p[t], k, i), l2, wd, i))) return 1;",
+     "step"),
     # local reduction of FP8 shards (MS-AMP O1, FP8 all-reduce)
     ("reduce_divides", "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) * r[j];",
      "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) / scales[j];",
@@ -87,6 +115,9 @@ MUTANTS = [
      "reduce"),
     ("reduce_drops_last_shard", "for (int j = 1; j < k; ++j)\n            acc",
      "for (int j = 1; j < k - 1; ++j)\n            acc", "reduce"),
+    ("reduce_encodes_in_input_format",
+     "int rc = oracle_cast_scaled(y, OR_F32, numel, out_fmt,",
+     "int rc = oracle_cast_scaled(y, OR_F32, numel, in_fmt,", "reduce"),
     # global gradient norm and clipping (torch clip_grad_norm_)
     ("norm_sum_not_squared", "sum += (unsigned __int128)q * q;",
      "sum += (unsigned __int128)q * 65536u;", "clip"),
@@ -98,6 +129,17 @@ MUTANTS = [
      "double c = (double)max_norm / norm;", "clip"),
     ("clip_unclamped", "return c < 1.0 ? (float)c : 1.0f;", "return (float)c;", "clip"),
     ("clip_unused", "if (clip != 1.0f) k = k * clip;", "(void)clip;", "clip"),
+    ("norm_found_dropped",
+     "if (!isfinite(or_grad(&p[t], k, i))) { found = 1; continue; }",
+     "if (!isfinite(or_grad(&p[t], k, i))) { continue; }", "clip"),
+    ("norm_last_tensor_only", "for (int t = 0; t < n; ++t) total = total + terms[t];",
+     "for (int t = 0; t < n; ++t) total = terms[t];", "clip"),
+    ("clip_nonpositive_max", "if (!(max_norm > 0.0f)) return 1.0f;\n    double c",
+     "double c", "clip"),
+    ("found_inf_on_clipped_gradient",
+     "float k = or_grad_factor(&p[t], inv_loss_scale);\n        for (int64_t i = 0; i < p[t].numel; ++i)\n            if (!isfinite",
+     "float k = or_grad_factor(&p[t], inv_loss_scale) * clip;\n        for (int64_t i = 0; i < p[t].numel; ++i)\n            if (!isfinite",
+     "clip"),
 ]
 
 

@@ -188,6 +188,26 @@ def test_found_inf_matches_torch_gradscaler_check(orc, case):
                 assert np.array_equal(getattr(a, k), getattr(b, k))
 
 
+@pytest.mark.parametrize("l2", [False, True])
+def test_found_inf_looks_at_the_gradients_only(orc, l2):
+    """GradScaler's check runs over the unscaled gradients alone, before the
+    optimizer adds any decay term: an infinite weight with finite gradients
+    is no found_inf, in AdamW or in Adam-L2 mode, and the step runs."""
+    rng = np.random.default_rng(13)
+    states = make_states(orc, [40, 60], rng)
+    states[1].w[3] = 0x7C00                       # +inf FP16 weight
+    before = [s.copy() for s in states]
+    grads = [(tdec(s.g, s.g_fmt).float() * (np.float32(1.0) / np.float32(s.g_scale)))
+             for s in states]
+    flag = torch.zeros(1)
+    torch._amp_foreach_non_finite_check_and_unscale_(
+        grads, flag, torch.tensor(1.0, dtype=torch.float32))
+    assert flag.item() == 0
+    assert orc.adamw_step(states, 1e-3, 0.9, 0.999, 1e-8, 0.01, 2, 1.0, l2=l2) == 0
+    assert not np.isfinite(f16(states[1].w[3:4]).numpy()[0])
+    assert not np.array_equal(states[0].w, before[0].w)
+
+
 def test_empty_and_zero_tensors(orc):
     rng = np.random.default_rng(6)
     states = make_states(orc, [0, 16, 5], rng, fresh=True)
