@@ -393,7 +393,12 @@ FP8OPT_API int fp8_adam_step_clipped(const fp8opt_param *params, int n, float lr
  * fp8_adam_step_begin: the step's first pass over this rank's records
  * (found_inf, and the amax of each new first moment); found_dev (device
  * uint32, may be NULL) receives this rank's found_inf.  clip_dev: a device
- * fp32 clip coefficient (from fp8_clip_coef) or NULL for none.
+ * fp32 clip coefficient (from fp8_clip_coef) or NULL for none.  With a clip
+ * coefficient this pass tests the clipped gradient, so a gradient that
+ * overflows fp32 when unscaled but not once clipped is not flagged here; the
+ * GradScaler test of the unclipped gradient is fp8_grad_norm_terms's
+ * found_dev, which the clip coefficient's own sequence computes first and
+ * which belongs in found_in_dev.
  *
  * fp8_adam_step_finish: the rest of the step (update and O3 weight copy) of
  * the same records, skipped when this rank's found_inf or *found_in_dev (the
