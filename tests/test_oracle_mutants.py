@@ -44,6 +44,8 @@ MUTANTS = [
     ("f16_subnormal_unclamped",
      "        lead = e - 1;\n        if (lead < emin) lead = emin;",
      "        lead = e - 1;", "codec"),
+    ("f16_decode_subnormal", "v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);",
+     "codec"),
     # scaled cast, just-in-time per-tensor scale (MS-AMP O1)
     ("amax_signed", "else if (fabsf(x) > a->fin) a->fin = fabsf(x);",
      "else if (x > a->fin) a->fin = x;", "cast"),
@@ -57,6 +59,11 @@ MUTANTS = [
     ("f16_source_as_bf16",
      "default: return oracle_f16_to_f32(((const uint16_t *)src)[i]);",
      "default: return oracle_bf16_to_f32(((const uint16_t *)src)[i]);", "cast"),
+    ("cast_nonfinite_all_nan",
+     "if (!isfinite(x)) { codes[i] = oracle_fp8_encode(x, fmt); continue; }",
+     "if (!isfinite(x)) { codes[i] = 0x7F; continue; }", "cast"),
+    ("amax_ignores_inf", "else if (isinf(x)) a->inf = 1;", "else if (isinf(x)) (void)0;",
+     "cast"),
     # AdamW / Adam step with FP8 m and FP16 v (MS-AMP O2 / O3; torch AdamW)
     ("eps_inside_root", "float denom = fmaf(sqrtf(v), s.inv_sbc2, eps);",
      "float denom = sqrtf(v * s.inv_sbc2 * s.inv_sbc2 + eps);", "step"),
@@ -103,6 +110,34 @@ MUTANTS = [
     ("l2_found_inf_after_decay", "if (!isfinite(or_grad(&p[t], k, i))) return 1;",
      "if (!isfinite(or_grad_l2(&p[t], or_grad(&p[t], k, i), l2, wd, i))) return 1;",
      "step"),
+    ("decay_without_lr", "s.decay = l2 ? 1.0f : 1.0f - lr * wd;",
+     "s.decay = l2 ? 1.0f : 1.0f - wd;", "step"),
+    ("v_abs_not_square", "float v = fmaf(beta2, vp, s.omb2 * (g * g));",
+     "float v = fmaf(beta2, vp, s.omb2 * fabsf(g));", "step"),
+    ("m_amax_over_g", "or_amax_add(&am, or_m_new(q, minv, g, beta1, &s, i));",
+     "or_amax_add(&am, g);", "step"),
+    ("state_bytes_fp32_v",
+     "case 2: case 3: return (int)(sizeof(uint8_t) + sizeof(uint16_t));",
+     "case 2: case 3: return (int)(sizeof(uint8_t) + sizeof(float));", "step"),
+    ("scaled_v_gmax_before_l2", "if (scaled_v) or_amax_add(&ag, g);",
+     "if (scaled_v) or_amax_add(&ag, or_grad(q, k, i));", "step"),
+    ("m_scale_from_e5m2_max",
+     "float m_scale_new = oracle_scale_from_amax(or_amax_value(&am), OR_E4M3);",
+     "float m_scale_new = oracle_scale_from_amax(or_amax_value(&am), OR_E5M2);", "step"),
+    ("w8_scale_from_e5m2_max", "float w8_scale = oracle_scale_from_amax(amax_w, OR_E4M3);",
+     "float w8_scale = oracle_scale_from_amax(amax_w, OR_E5M2);", "step"),
+    ("v_target_2_15", "#define OR_V_TARGET 16384.0f", "#define OR_V_TARGET 32768.0f",
+     "step"),
+    ("vinv_2_15", "vinv = *q->v_bound * 0x1p-14f;", "vinv = *q->v_bound * 0x1p-15f;",
+     "step"),
+    ("grad_factor_times_scale", "return inv_loss_scale / p->g_scale;",
+     "return inv_loss_scale * p->g_scale;", "step"),
+    ("bias_power_squares_first", "if (t & 1) r = r * b;\n        b = b * b;",
+     "b = b * b;\n        if (t & 1) r = r * b;", "step"),
+    ("eps_scaled_by_correction", "float denom = fmaf(sqrtf(v), s.inv_sbc2, eps);",
+     "float denom = (sqrtf(v) + eps) * s.inv_sbc2;", "step"),
+    ("step_zero_allowed", "if (n < 0 || step < 1) return -1;\n    or_scalars",
+     "if (n < 0 || step < 0) return -1;\n    or_scalars", "step"),
     # local reduction of FP8 shards (MS-AMP O1, FP8 all-reduce)
     ("reduce_divides", "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) * r[j];",
      "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) / scales[j];",
@@ -118,6 +153,10 @@ MUTANTS = [
     ("reduce_encodes_in_input_format",
      "int rc = oracle_cast_scaled(y, OR_F32, numel, out_fmt,",
      "int rc = oracle_cast_scaled(y, OR_F32, numel, in_fmt,", "reduce"),
+    ("reduce_post_squared", "y[i] = acc * post;", "y[i] = acc * post * post;", "reduce"),
+    ("reduce_first_shard_skipped",
+     "float acc = oracle_fp8_decode(src[i], in_fmt) * r[0];", "float acc = 0.0f * r[0];",
+     "reduce"),
     # global gradient norm and clipping (torch clip_grad_norm_)
     ("norm_sum_not_squared", "sum += (unsigned __int128)q * q;",
      "sum += (unsigned __int128)q * 65536u;", "clip"),
@@ -140,6 +179,9 @@ MUTANTS = [
      "float k = or_grad_factor(&p[t], inv_loss_scale);\n        for (int64_t i = 0; i < p[t].numel; ++i)\n            if (!isfinite",
      "float k = or_grad_factor(&p[t], inv_loss_scale) * clip;\n        for (int64_t i = 0; i < p[t].numel; ++i)\n            if (!isfinite",
      "clip"),
+    ("norm_code_unit_halved", "uint64_t q = (uint64_t)ldexp(d, 16);",
+     "uint64_t q = (uint64_t)ldexp(d, 15);", "clip"),
+    ("norm_not_rooted", "*norm = sqrt(total);", "*norm = total;", "clip"),
 ]
 
 

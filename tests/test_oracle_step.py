@@ -376,16 +376,21 @@ def test_l2_mode_plain_v_matches_torch_adam(orc):
     assert ok >= 0.99
 
 
-def test_v_bound_holds_and_stays_below_fp16_overflow(orc):
+@pytest.mark.parametrize("l2", [False, True])
+def test_v_bound_holds_and_stays_below_fp16_overflow(orc, l2):
+    """The bound covers every element of v.  With L2 decay v accumulates the
+    decayed gradient g + wd * w, which here often outweighs g itself."""
     rng = np.random.default_rng(7)
     states = make_states_v(orc, [4096], rng, 1e-3, True)
     st = states[0]
+    wd = 0.1 if l2 else 0.0
     for t in range(1, 11):
         sigma = 10.0 ** rng.uniform(-6, -1)           # gradients jump around
         g, _, gs = orc.cast_scaled((rng.standard_normal(4096) * sigma)
                                    .astype(np.float32), F32, E4M3)
         st.g, st.g_scale = g, float(gs)
-        assert orc.adamw_step(states, 1e-3, 0.9, 0.999, 1e-8, 0.0, t, 1.0) == 0
+        assert orc.adamw_step(states, 1e-3, 0.9, 0.999, 1e-8, wd, t, 1.0,
+                              l2=l2) == 0
         codes = f16(st.v).numpy()
         assert codes.max() <= 16384 * (1 + 2.0 ** -9)   # far below 65504
         assert stored_v(st).max().item() <= st.v_bound[0] * (1 + 2.0 ** -9)
