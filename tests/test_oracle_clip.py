@@ -96,6 +96,27 @@ def test_clip_coefficient(orc):
     assert c * (123.0 + 1e-6) == pytest.approx(2.5, rel=1e-7)
 
 
+def test_clip_coefficient_is_torchs_rounded_once(orc):
+    """torch.nn.utils.clip_grad_norm_ in float64 scales every gradient by
+    min(1, max_norm / (norm + 1e-6)); a unit gradient element then holds that
+    coefficient exactly.  The oracle's coefficient is it rounded to float
+    once, for the norm torch returns."""
+    rng = np.random.default_rng(15)
+    clipped = 0
+    for _ in range(300):
+        g = torch.tensor(rng.standard_normal(37) * 10.0 ** rng.uniform(-3, 3),
+                         dtype=torch.float64)
+        max_norm = float(np.float32(10.0 ** rng.uniform(-3, 1)))
+        p1 = torch.zeros(37, dtype=torch.float64, requires_grad=True)
+        p2 = torch.zeros(1, dtype=torch.float64, requires_grad=True)
+        p1.grad, p2.grad = g.clone(), torch.ones(1, dtype=torch.float64)
+        norm = torch.nn.utils.clip_grad_norm_([p1, p2], max_norm).item()
+        coef = p2.grad.item()
+        assert orc.clip_coef(norm, max_norm) == np.float32(coef)
+        clipped += coef < 1.0
+    assert 50 < clipped < 300
+
+
 def torch_clipped_f64(st_list, lr, b1, b2, eps, wd, step, ils, max_norm, l2):
     """torch: dequantize, clip_grad_norm_ in float64, then one Adam / AdamW
     step per tensor from the dequantized state."""

@@ -46,6 +46,11 @@ MUTANTS = [
      "        lead = e - 1;", "codec"),
     ("f16_decode_subnormal", "v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);",
      "codec"),
+    ("f16_max_is_inf", "bits = (r > OR_HALF.maxval) ? 0x7C00u",
+     "bits = (r >= OR_HALF.maxval) ? 0x7C00u", "codec"),
+    ("e4m3_decode_top_codes_nan",
+     "if (!f->has_inf && e == eall && m == (1 << f->mbits) - 1)",
+     "if (!f->has_inf && e == eall && m >= (1 << f->mbits) - 2)", "codec"),
     # scaled cast, just-in-time per-tensor scale (MS-AMP O1)
     ("amax_signed", "else if (fabsf(x) > a->fin) a->fin = fabsf(x);",
      "else if (x > a->fin) a->fin = x;", "cast"),
@@ -138,6 +143,23 @@ MUTANTS = [
      "float denom = (sqrtf(v) + eps) * s.inv_sbc2;", "step"),
     ("step_zero_allowed", "if (n < 0 || step < 1) return -1;\n    or_scalars",
      "if (n < 0 || step < 0) return -1;\n    or_scalars", "step"),
+    ("first_bias_step_off_by_one",
+     "double bc1 = 1.0 - oracle_bias_power((double)beta1, step);",
+     "double bc1 = 1.0 - oracle_bias_power((double)beta1, step + 1);", "step"),
+    ("second_bias_step_off_by_one",
+     "double bc2 = 1.0 - oracle_bias_power((double)beta2, step);",
+     "double bc2 = 1.0 - oracle_bias_power((double)beta2, step + 1);", "step"),
+    ("second_correction_not_rooted", "s.inv_sbc2 = (float)(1.0 / sqrt(bc2));",
+     "s.inv_sbc2 = (float)(1.0 / bc2);", "step"),
+    ("w_store_truncates", "q->w[i] = oracle_f32_to_f16(w);",
+     "q->w[i] = (uint16_t)(oracle_f32_to_f16(w) & 0xFFFEu);", "step"),
+    ("v_store_truncates",
+     "q->v[i] = oracle_f32_to_f16(scaled_v ? v * v_scale_new : v);",
+     "q->v[i] = (uint16_t)(oracle_f32_to_f16(scaled_v ? v * v_scale_new : v) & 0xFFFEu);",
+     "step"),
+    ("m_scale_stale",
+     "float m_scale_new = oracle_scale_from_amax(or_amax_value(&am), OR_E4M3);",
+     "float m_scale_new = *q->m_scale; (void)am;", "step"),
     # local reduction of FP8 shards (MS-AMP O1, FP8 all-reduce)
     ("reduce_divides", "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) * r[j];",
      "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) / scales[j];",
@@ -157,6 +179,15 @@ MUTANTS = [
     ("reduce_first_shard_skipped",
      "float acc = oracle_fp8_decode(src[i], in_fmt) * r[0];", "float acc = 0.0f * r[0];",
      "reduce"),
+    ("reduce_accepts_short_stride",
+     "if (numel < 0 || k < 1 || k > 64 || stride < numel || in_fmt < 0 ||",
+     "if (numel < 0 || k < 1 || k > 64 || in_fmt < 0 ||", "reduce"),
+    ("reduce_accepts_no_shard",
+     "if (numel < 0 || k < 1 || k > 64 || stride < numel || in_fmt < 0 ||",
+     "if (numel < 0 || k < 0 || k > 64 || stride < numel || in_fmt < 0 ||", "reduce"),
+    ("cast_accepts_bad_dtype",
+     "if (numel < 0 || fmt < 0 || fmt > 1 || dtype < 0 || dtype > 2) return -1;",
+     "if (numel < 0 || fmt < 0 || fmt > 1 || dtype < 0) return -1;", "reduce"),
     # global gradient norm and clipping (torch clip_grad_norm_)
     ("norm_sum_not_squared", "sum += (unsigned __int128)q * q;",
      "sum += (unsigned __int128)q * 65536u;", "clip"),
@@ -182,6 +213,14 @@ MUTANTS = [
     ("norm_code_unit_halved", "uint64_t q = (uint64_t)ldexp(d, 16);",
      "uint64_t q = (uint64_t)ldexp(d, 15);", "clip"),
     ("norm_not_rooted", "*norm = sqrt(total);", "*norm = total;", "clip"),
+    ("norm_k_squared_in_float", "double kk = (double)k * (double)k;",
+     "double kk = (double)(k * k);", "clip"),
+    ("norm_terms_in_float", "terms[t] = kk * ldexp((double)sum, -32);",
+     "terms[t] = (float)(kk * ldexp((double)sum, -32));", "clip"),
+    ("norm_total_in_float", "for (int t = 0; t < n; ++t) total = total + terms[t];",
+     "for (int t = 0; t < n; ++t) total = (float)(total + terms[t]);", "clip"),
+    ("clip_coef_in_float", "double c = (double)max_norm / (norm + 1e-6);",
+     "double c = (double)(max_norm / (float)(norm + 1e-6));", "clip"),
 ]
 
 

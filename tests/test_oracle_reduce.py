@@ -154,3 +154,39 @@ def test_empty_tensor(orc):
     codes, amax, scale = orc.reduce_scaled(np.zeros((4, 0), np.uint8), [1.0] * 4,
                                            E4M3, E4M3)
     assert codes.size == 0 and amax == 0.0 and scale == 1.0
+
+
+def test_bad_arguments_are_refused(orc):
+    """Each C entry point refuses a malformed call with -1 before reading
+    anything (buffers here are large enough that a call which did read would
+    stay in bounds)."""
+    import ctypes as C
+    L = orc.lib()
+    buf = np.zeros(4096, np.uint8)
+    scales = np.ones(65, np.float32)
+    codes = np.zeros(4096, np.uint8)
+    amax = np.zeros(1, np.float32)
+    scale = np.zeros(1, np.float32)
+
+    def reduce(numel, stride, k, in_fmt=0, out_fmt=0):
+        return L.oracle_reduce_scaled(buf.ctypes.data, numel, stride,
+                                      scales.ctypes.data, k, in_fmt, out_fmt,
+                                      C.c_float(1.0), codes.ctypes.data,
+                                      amax.ctypes.data, scale.ctypes.data)
+
+    assert reduce(64, 64, 2) == 0
+    assert reduce(64, 63, 2) == -1           # shards overlap
+    assert reduce(64, 64, 0) == -1           # no shard
+    assert reduce(32, 32, 65) == -1          # more shards than the limit
+    assert reduce(-1, 64, 2) == -1
+    assert reduce(64, 64, 2, in_fmt=2) == -1
+    assert reduce(64, 64, 2, out_fmt=-1) == -1
+
+    def cast(numel, dtype, fmt=0):
+        return L.oracle_cast_scaled(buf.ctypes.data, dtype, numel, fmt,
+                                    codes.ctypes.data, amax.ctypes.data,
+                                    scale.ctypes.data)
+
+    assert cast(64, 0) == 0 and cast(64, 2) == 0
+    assert cast(64, 3) == -1 and cast(64, -1) == -1
+    assert cast(64, 0, fmt=2) == -1 and cast(-1, 0) == -1
