@@ -5,7 +5,8 @@ Tolerances (fixed by the library's specification):
 * FP8 codes: at most 1 code apart, at least 99.9% identical;
 * FP16 second moment and weights: at most 1 ulp apart;
 * FP16 master weights (O3): within 2e-3 relative.
-NaN codes / NaN halves must sit at the same positions.
+NaN codes / NaN halves must sit at the same positions, and E5M2 infinity
+codes must be identical.
 """
 import numpy as np
 import torch
@@ -39,6 +40,14 @@ def nan_code(c: np.ndarray, fmt: int) -> np.ndarray:
     return ((c & 0x7C) == 0x7C) & ((c & 0x03) != 0)
 
 
+def inf_code(c: np.ndarray, fmt: int) -> np.ndarray:
+    """Infinity codes (E5M2 only; E4M3 has none)."""
+    c = c.astype(np.int32)
+    if fmt == E4M3:
+        return np.zeros(c.shape, bool)
+    return (c & 0x7F) == 0x7C
+
+
 def _ord(x: np.ndarray, sign_bit: int) -> np.ndarray:
     x = x.astype(np.int64)
     mag = x & (sign_bit - 1)
@@ -53,7 +62,12 @@ def check_codes(got, ref, fmt=E4M3, name="codes", min_exact=CODE_MIN_EXACT):
         return 1.0
     nan = nan_code(ref, fmt)
     assert np.array_equal(nan, nan_code(got, fmt)), f"{name}: NaN codes differ"
-    d = np.abs(_ord(got, 0x80) - _ord(ref, 0x80))[~nan]
+    # E5M2 infinities come only from infinite values (finite ones saturate),
+    # so they are no rounding neighbour of the largest finite code
+    inf = inf_code(ref, fmt)
+    assert np.array_equal(inf, inf_code(got, fmt)) and np.array_equal(
+        got[inf], ref[inf]), f"{name}: infinity codes differ"
+    d = np.abs(_ord(got, 0x80) - _ord(ref, 0x80))[~(nan | inf)]
     assert d.size == 0 or d.max() <= 1, (
         f"{name}: codes {int(d.max())} apart at {np.flatnonzero(d > 1)[:5]}")
     exact = float(np.mean(got == ref))
