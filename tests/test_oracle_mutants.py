@@ -51,6 +51,16 @@ MUTANTS = [
     ("e4m3_decode_top_codes_nan",
      "if (!f->has_inf && e == eall && m == (1 << f->mbits) - 1)",
      "if (!f->has_inf && e == eall && m >= (1 << f->mbits) - 2)", "codec"),
+    ("fields_exponent_off", "return ((uint32_t)(lead + f->bias) << f->mbits) | M;",
+     "return ((uint32_t)(lead + f->bias + 1) << f->mbits) | M;", "codec"),
+    ("decode_exponent_off",
+     "v = ldexp(1.0 + ldexp((double)m, -f->mbits), e - f->bias);\n    }\n    return (float)(s ? -v : v);   /* exact",
+     "v = ldexp(1.0 + ldexp((double)m, -f->mbits), e - f->bias + 1);\n    }\n    return (float)(s ? -v : v);   /* exact",
+     "codec"),
+    ("e5m2_max_61440", "{2, 15, 57344.0, 1},", "{2, 15, 61440.0, 1},", "codec"),
+    ("f16_decode_nan_as_inf",
+     "if (m) return or_bits_f32(0x7FC00000u);\n        v = INFINITY;\n    } else if (e == 0) {\n        v = ldexp((double)m, -24);",
+     "v = INFINITY;\n    } else if (e == 0) {\n        v = ldexp((double)m, -24);", "codec"),
     # scaled cast, just-in-time per-tensor scale (MS-AMP O1)
     ("amax_signed", "else if (fabsf(x) > a->fin) a->fin = fabsf(x);",
      "else if (x > a->fin) a->fin = x;", "cast"),
@@ -69,6 +79,8 @@ MUTANTS = [
      "if (!isfinite(x)) { codes[i] = 0x7F; continue; }", "cast"),
     ("amax_ignores_inf", "else if (isinf(x)) a->inf = 1;", "else if (isinf(x)) (void)0;",
      "cast"),
+    ("bf16_shift_15", "return or_bits_f32((uint32_t)h << 16); }",
+     "return or_bits_f32((uint32_t)h << 15); }", "cast"),
     # AdamW / Adam step with FP8 m and FP16 v (MS-AMP O2 / O3; torch AdamW)
     ("eps_inside_root", "float denom = fmaf(sqrtf(v), s.inv_sbc2, eps);",
      "float denom = sqrtf(v * s.inv_sbc2 * s.inv_sbc2 + eps);", "step"),
@@ -160,6 +172,10 @@ MUTANTS = [
     ("m_scale_stale",
      "float m_scale_new = oracle_scale_from_amax(or_amax_value(&am), OR_E4M3);",
      "float m_scale_new = *q->m_scale; (void)am;", "step"),
+    ("v_scale_unguarded", "float q = OR_V_TARGET / b;\n    return isfinite(q) ? q : 1.0f;",
+     "float q = OR_V_TARGET / b;\n    return q;", "step"),
+    ("fp32_state_bytes_6", "case 0: case 1: return (int)(sizeof(float) + sizeof(float));",
+     "case 0: case 1: return (int)(sizeof(float) + sizeof(uint16_t));", "step"),
     # local reduction of FP8 shards (MS-AMP O1, FP8 all-reduce)
     ("reduce_divides", "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) * r[j];",
      "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) / scales[j];",
@@ -221,6 +237,8 @@ MUTANTS = [
      "for (int t = 0; t < n; ++t) total = (float)(total + terms[t]);", "clip"),
     ("clip_coef_in_float", "double c = (double)max_norm / (norm + 1e-6);",
      "double c = (double)(max_norm / (float)(norm + 1e-6));", "clip"),
+    ("norm_finite_on_found", "if (found != 0) { *norm = INFINITY; return found; }",
+     "if (found != 0) { *norm = sqrt(total); return found; }", "clip"),
 ]
 
 

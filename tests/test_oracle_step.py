@@ -397,6 +397,22 @@ def test_v_bound_holds_and_stays_below_fp16_overflow(orc, l2):
         assert codes.max() >= 16384 / 4096           # the bound is not loose
 
 
+def test_scaled_v_with_a_tiny_bound_stores_only_finite_values(orc):
+    """Gradients near 1e-17 give a bound B so small that 2^14 / B overflows
+    fp32.  Finite gradients must still leave finite state: torch's second
+    moment here is finite (and tiny), so no stored v or w may be inf or
+    NaN."""
+    rng = np.random.default_rng(16)
+    states = make_states_v(orc, [300], rng, 1e-3, True)
+    st = states[0]
+    st.g_scale = float(np.float32(2.0 ** 64))       # |g| <= 448 * 2^-64
+    assert orc.adamw_step(states, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0) == 0
+    b = float(st.v_bound[0])
+    assert 0.0 < b < 16384.0 / float(np.finfo(np.float32).max)
+    assert np.isfinite(f16(st.v).numpy()).all()
+    assert np.isfinite(f16(st.w).numpy()).all()
+
+
 def test_found_inf_leaves_v_bound_unchanged(orc):
     states = make_states_v(orc, [100], np.random.default_rng(8), 1e-3, True)
     assert orc.adamw_step(states, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0) == 0
