@@ -261,12 +261,36 @@ __device__ __forceinline__ uint2 enc8(const float (&x)[8]) {
   return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }
 
-// Any of the four bytes of w a non-finite code?  E4M3: low seven bits all
-// ones; E5M2: exponent field all ones.
+// The GradScaler test of a chunk of gradient codes as one comparison per
+// code.  |decode(code) * k| depends only on the code's magnitude (code &
+// 0x7F), and rounds monotonically in it; the non-finite codes (E4M3 0x7F,
+// E5M2 0x7C and above) are the format's largest magnitudes.  The magnitudes
+// whose unscaled value is not finite are therefore one upper range [T, 0x7F],
+// and overflow_threshold finds T by bisection over [0, first non-finite
+// magnitude].  T is 0 when k is not finite (0 * inf is NaN).
 template <int FMT>
-__device__ __forceinline__ uint32_t nonfinite_code_bytes(uint32_t w) {
-  if (FMT == kE4M3) return ((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
-  return ((w & 0x7C7C7C7Cu) + 0x04040404u) & 0x80808080u;
+__device__ __forceinline__ uint32_t overflow_threshold(float k) {
+  uint32_t lo = 0, hi = FMT == kE4M3 ? 0x7Fu : 0x7Cu;   // T lies in [lo, hi]
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi) >> 1;
+    if ((__float_as_uint(__fmul_rn(dec2<FMT>(mid).x, k)) & 0x7FFFFFFFu) >= 0x7F800000u)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  return lo;
+}
+
+// The per-byte addend of codes_at_least for threshold T (0 <= T <= 0x80).
+__device__ __forceinline__ uint32_t threshold_addend(uint32_t t) {
+  return (0x80u - t) * 0x01010101u;
+}
+
+// Bit 7 of each byte of w (four codes) whose magnitude is at least T, given
+// add = threshold_addend(T): a magnitude m <= 0x7F plus 0x80 - T reaches 0x80
+// exactly when m >= T, and never carries into the next byte.
+__device__ __forceinline__ uint32_t codes_at_least(uint32_t w, uint32_t add) {
+  return ((w & 0x7F7F7F7Fu) + add) & 0x80808080u;
 }
 
 // Eight codes in a uint2 -> eight floats.

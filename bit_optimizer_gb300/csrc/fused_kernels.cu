@@ -54,12 +54,14 @@ __device__ __forceinline__ uint32_t enc_pair(float2 t) {
 
 // This thread's share of [begin, end): encode, store the codes, and fold the
 // step's first pass into mx (max |m| bits), gx (max |g| bits, when GX: for a
-// scaled second moment) and bad (non-finite gradient).
-template <int DT, int FMT, bool CHECKED, bool SAFE, bool GX>
+// scaled second moment) and bad (non-finite gradient: a code magnitude at or
+// above the threshold whose addend is tadd, as in the unfused first pass).
+template <int DT, int FMT, bool CHECKED, bool GX>
 __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
                                  int64_t begin, int64_t end, float scale,
-                                 float k, float minv, const StepScalars& s,
-                                 uint32_t& mx, uint32_t& gx, uint32_t& bad) {
+                                 float k, float minv, uint32_t tadd,
+                                 const StepScalars& s, uint32_t& mx,
+                                 uint32_t& gx, uint32_t& bad) {
   constexpr int64_t kTile = (int64_t)kThreads * kGroup * kFusedGroups;
   const int tid = threadIdx.x;
   const bool vec = cd.vec_ok != 0 && sd.vec_ok != 0;
@@ -95,12 +97,10 @@ __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
           c[j] = enc_pair<FMT, CHECKED>(mul2(make_float2(x[q][2 * j], x[q][2 * j + 1]), sc2));
         const uint2 codes = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
         *reinterpret_cast<uint2*>(cd.codes + i0) = codes;
-        if (SAFE)
-          bad |= nonfinite_code_bytes<FMT>(codes.x) | nonfinite_code_bytes<FMT>(codes.y);
+        bad |= codes_at_least(codes.x, tadd) | codes_at_least(codes.y, tadd);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float2 g = mul2(dec2<FMT>(c[j]), k2);
-          if (!SAFE) bad |= nonfinite(g.x) | nonfinite(g.y);
           if (GX) gx = max(gx, max(abs_bits(g.x), abs_bits(g.y)));
           const float2 m = fma2(b1, mul2(dec2<kE4M3>(code_pair(mc[q], j)), minv2),
                                 mul2(omb1, g));
@@ -118,8 +118,8 @@ __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
           const uint32_t code = CHECKED ? enc1_checked<FMT>(t)
                                         : (enc2<FMT>(t, 0.0f) & 0xFFu);
           cd.codes[i] = (uint8_t)code;
+          bad |= codes_at_least(code, tadd);
           const float g = __fmul_rn(dec2<FMT>(code).x, k);
-          bad |= nonfinite(g);
           if (GX) gx = max(gx, abs_bits(g));
           const float mp = __fmul_rn(dec2<kE4M3>(sd.m[i]).x, minv);
           mx = max(mx, abs_bits(__fmaf_rn(s.beta1, mp, __fmul_rn(s.omb1, g))));
@@ -138,20 +138,12 @@ __device__ __forceinline__ void cast_step_dispatch2(const CastDesc& cd,
                                                     const StepScalars& s,
                                                     uint32_t& mx, uint32_t& gx,
                                                     uint32_t& bad) {
-  // As in the unfused step: when the largest finite code unscales to a finite
-  // value, every finite code does, and found_inf needs only the codes.
-  const bool safe = !nonfinite(__fmul_rn(fp8_max_of<FMT>(), k));
-  if (checked) {
-    if (safe)
-      thread_cast_step<DT, FMT, true, true, GX>(cd, sd, begin, end, scale, k, minv, s, mx, gx, bad);
-    else
-      thread_cast_step<DT, FMT, true, false, GX>(cd, sd, begin, end, scale, k, minv, s, mx, gx, bad);
-  } else {
-    if (safe)
-      thread_cast_step<DT, FMT, false, true, GX>(cd, sd, begin, end, scale, k, minv, s, mx, gx, bad);
-    else
-      thread_cast_step<DT, FMT, false, false, GX>(cd, sd, begin, end, scale, k, minv, s, mx, gx, bad);
-  }
+  // As in the unfused step: found_inf from the codes and the threshold of k.
+  const uint32_t tadd = threshold_addend(overflow_threshold<FMT>(k));
+  if (checked)
+    thread_cast_step<DT, FMT, true, GX>(cd, sd, begin, end, scale, k, minv, tadd, s, mx, gx, bad);
+  else
+    thread_cast_step<DT, FMT, false, GX>(cd, sd, begin, end, scale, k, minv, tadd, s, mx, gx, bad);
 }
 
 template <int DT, int FMT, bool ANY_VS>

@@ -133,15 +133,17 @@ __device__ __forceinline__ void adamw1(float g, float m, float vp, float wp,
 
 // ------------------------------------------------------------ pass 1: amax
 
-// SAFE: every finite gradient code unscales to a finite value (decided once
-// per chunk from the largest code), so found_inf only needs the codes.
+// found_inf is "some gradient code magnitude >= T" (overflow_threshold of
+// the unclipped factor, passed as its addend `tadd`), so it needs only the
+// codes, and a clip coefficient in k cannot hide an unscaled overflow.
 // L2: the gradient takes the decay term fma(wd, w, g) (so w is read too).
 // Besides the amax of the first moment (mx) this also reduces max |g| (gx)
 // when GX: the input of a scaled second moment's bound.
-template <int GF, bool SAFE, bool L2, bool GX>
+template <int GF, bool L2, bool GX>
 __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
-                                 float k, float minv, const StepScalars& s,
-                                 uint32_t& mx, uint32_t& gx, uint32_t& bad) {
+                                 float k, float minv, uint32_t tadd,
+                                 const StepScalars& s, uint32_t& mx,
+                                 uint32_t& gx, uint32_t& bad) {
   constexpr int64_t kTile = (int64_t)kThreads * kGroup * kAmaxGroups;
   const int tid = threadIdx.x;
   const bool vec = d.vec_ok != 0;
@@ -169,12 +171,10 @@ __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
       }
 #pragma unroll
       for (int q = 0; q < kAmaxGroups; ++q) {
-        if (SAFE)
-          bad |= nonfinite_code_bytes<GF>(gc[q].x) | nonfinite_code_bytes<GF>(gc[q].y);
+        bad |= codes_at_least(gc[q].x, tadd) | codes_at_least(gc[q].y, tadd);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           float2 g = mul2(dec2<GF>(code_pair(gc[q], j)), k2);
-          if (!SAFE) bad |= nonfinite(g.x) | nonfinite(g.y);
           if (L2) g = fma2(wd2, h2_to_f2(half_pair(wh[q], j)), g);
           if (GX) gx = max(gx, max(abs_bits(g.x), abs_bits(g.y)));
           const float2 m = fma2(b1, mul2(dec2<kE4M3>(code_pair(mc[q], j)), minv2),
@@ -189,8 +189,8 @@ __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
         for (int j = 0; j < kGroup; ++j) {
           const int64_t i = i0 + j;
           if (i >= end) break;
+          bad |= codes_at_least(d.g[i], tadd);
           float g = __fmul_rn(dec2<GF>(d.g[i]).x, k);
-          bad |= nonfinite(g);
           if (L2) g = __fmaf_rn(s.wd, h_to_f(d.w[i]), g);
           if (GX) gx = max(gx, abs_bits(g));
           mx = max(mx, abs_bits(m_new1(dec2<kE4M3>(d.m[i]).x, minv, g, s)));
@@ -200,27 +200,21 @@ __device__ void thread_step_amax(const StepDesc& d, int64_t begin, int64_t end,
   }
 }
 
+// k0: the unclipped factor inv_loss_scale / g_scale, which decides found_inf
+// (GradScaler unscales, and finds any inf, before the norm is clipped); k:
+// the factor the moments use (k0 times the clip coefficient, if any).
 template <int GF, bool L2>
 __device__ __forceinline__ void step_amax_dispatch(const StepDesc& d,
                                                    int64_t begin, int64_t end,
-                                                   float k, float minv,
+                                                   float k0, float k, float minv,
                                                    const StepScalars& s,
                                                    uint32_t& mx, uint32_t& gx,
                                                    uint32_t& bad) {
-  // The largest finite code gives the largest |g|; rounding is monotonic, so
-  // if that product is finite every finite code gives a finite g.
-  const bool safe = !nonfinite(__fmul_rn(fp8_max_of<GF>(), k));
-  if (d.v_bound != nullptr) {
-    if (safe)
-      thread_step_amax<GF, true, L2, true>(d, begin, end, k, minv, s, mx, gx, bad);
-    else
-      thread_step_amax<GF, false, L2, true>(d, begin, end, k, minv, s, mx, gx, bad);
-  } else {
-    if (safe)
-      thread_step_amax<GF, true, L2, false>(d, begin, end, k, minv, s, mx, gx, bad);
-    else
-      thread_step_amax<GF, false, L2, false>(d, begin, end, k, minv, s, mx, gx, bad);
-  }
+  const uint32_t tadd = threshold_addend(overflow_threshold<GF>(k0));
+  if (d.v_bound != nullptr)
+    thread_step_amax<GF, L2, true>(d, begin, end, k, minv, tadd, s, mx, gx, bad);
+  else
+    thread_step_amax<GF, L2, false>(d, begin, end, k, minv, tadd, s, mx, gx, bad);
 }
 
 template <bool L2, bool DEVS>
@@ -238,16 +232,16 @@ step_amax_kernel(const StepDesc* __restrict__ descs,
       sc.old_m_scale[ch.tensor] = ms;
       if (d.v_bound != nullptr) sc.old_v_bound[ch.tensor] = *d.v_bound;
     }
-    float k = __fdiv_rn(ils_of<DEVS>(s), gs);
-    if (s.clip != nullptr) k = __fmul_rn(k, *s.clip);
+    const float k0 = __fdiv_rn(ils_of<DEVS>(s), gs);
+    const float k = s.clip != nullptr ? __fmul_rn(k0, *s.clip) : k0;
     const float minv = __frcp_rn(ms);
     const int64_t begin = ch.begin;
     const int64_t end = begin + ch.len;
     uint32_t mx = 0, gx = 0, bad = 0;
     if (d.g_fmt == kE4M3)
-      step_amax_dispatch<kE4M3, L2>(d, begin, end, k, minv, s, mx, gx, bad);
+      step_amax_dispatch<kE4M3, L2>(d, begin, end, k0, k, minv, s, mx, gx, bad);
     else
-      step_amax_dispatch<kE5M2, L2>(d, begin, end, k, minv, s, mx, gx, bad);
+      step_amax_dispatch<kE5M2, L2>(d, begin, end, k0, k, minv, s, mx, gx, bad);
     mx = block_max_u32(mx, red);
     if (d.v_bound != nullptr) {   // uniform over the CTA
       gx = block_max_u32(gx, red);

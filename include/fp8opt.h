@@ -200,23 +200,25 @@ FP8OPT_API int fp8_adamw_step(const fp8opt_param *params, int n, float lr, float
 /*
  * fp8_cast_scaled_noalloc: fp8_cast_scaled for callers that must not allocate
  * device memory.  No counterpart in the MS-AMP pages: it exists for callers
- * such as code running under CUDA graph capture, runtimes whose pool allocator
- * owns all device memory, or services that must not stall on or fail from an
- * allocation mid-step.  fp8_cast_scaled allocates its workspace on first use;
- * this entry point instead keeps its tensor table, chunk table and amax slots
- * in one fixed array compiled into the library (about 1.1 MB per device,
- * present on every device that loads the library, until the process exits),
- * and calls no cudaMalloc, cudaFree or other allocating routine.
+ * such as runtimes whose pool allocator owns all device memory, or services
+ * that must not stall on or fail from an allocation mid-step.
+ * fp8_cast_scaled allocates its workspace on first use; this entry point
+ * instead keeps its tensor table, chunk table and amax slots in one fixed
+ * array compiled into the library (about 1.1 MB per device, present on every
+ * device that loads the library, until the process exits), and calls no
+ * cudaMalloc, cudaFree or other allocating routine.
  *
  * Same arguments, same results and same errors as fp8_cast_scaled, plus
  * FP8OPT_ERR_LIMIT (nothing launched) when n exceeds
  * FP8OPT_NOALLOC_MAX_TENSORS or the list needs more than
  * FP8OPT_NOALLOC_MAX_CHUNKS chunks.  The first call on each device sets the
- * entry point up for that device (it looks up the array's device address);
- * make that first call before any stream capture.  All calls on a device share
- * the one array, which keeps the previous call's contents; each call clears
- * what it needs zeroed, but calls whose GPU work overlaps (on different
- * streams, or from different host threads) race on the array: order them.
+ * entry point up for that device (it looks up the array's device address).
+ * Each call copies its tables from host arrays that the next call refills, so
+ * a stream that is capturing a CUDA graph is refused with FP8OPT_ERR_ARG and
+ * nothing enqueued.  All calls on a device share the one array, which keeps
+ * the previous call's contents; each call clears what it needs zeroed, but
+ * calls whose GPU work overlaps (on different streams, or from different host
+ * threads) race on the array: order them.
  */
 FP8OPT_API int fp8_cast_scaled_noalloc(const fp8opt_cast_item *items, int n,
                                        int fmt, void *stream);
@@ -393,12 +395,11 @@ FP8OPT_API int fp8_adam_step_clipped(const fp8opt_param *params, int n, float lr
  * fp8_adam_step_begin: the step's first pass over this rank's records
  * (found_inf, and the amax of each new first moment); found_dev (device
  * uint32, may be NULL) receives this rank's found_inf.  clip_dev: a device
- * fp32 clip coefficient (from fp8_clip_coef) or NULL for none.  With a clip
- * coefficient this pass tests the clipped gradient, so a gradient that
- * overflows fp32 when unscaled but not once clipped is not flagged here; the
- * GradScaler test of the unclipped gradient is fp8_grad_norm_terms's
- * found_dev, which the clip coefficient's own sequence computes first and
- * which belongs in found_in_dev.
+ * fp32 clip coefficient (from fp8_clip_coef) or NULL for none; it scales the
+ * gradient the moments see, while found_inf is still decided on the unclipped
+ * gradient (GradScaler unscales, and finds any inf, before the norm is
+ * clipped), so a gradient that overflows fp32 when unscaled skips the step
+ * even where the clip coefficient would bring it back in range.
  *
  * fp8_adam_step_finish: the rest of the step (update and O3 weight copy) of
  * the same records, skipped when this rank's found_inf or *found_in_dev (the

@@ -268,3 +268,121 @@ def test_fused_clipped_equals_the_two_calls(bo):
     for x, y in zip(oa.m + oa.v, ob.m + ob.v):
         assert torch.equal(x, y)
     assert torch.equal(oa.m_scale, ob.m_scale)
+
+
+# ------------- found_inf of the split step's first pass under a clip factor
+#
+# GradScaler unscales the gradients, and finds any inf, before
+# clip_grad_norm_ runs: a gradient that overflows fp32 when unscaled skips
+# the step even where the clip coefficient would bring it back in range.
+# With k0 = 2^121 an E4M3 code overflows exactly from magnitude 0x70 (128 *
+# 2^121 = 2^128) up, while 0x6F (120) stays finite; the clip coefficient
+# 2^-8 brings every code back in range.
+
+K0_EXP, CLIP = 121, 2.0 ** -8
+
+
+def boundary_states(top_code):
+    """Two tensors; tensor 0's gradient holds top_code (and smaller codes),
+    tensor 1 is ordinary; unscaled by k0 = 2^121 through g_scale."""
+    rng = np.random.default_rng(31)
+    out = []
+    for i, n in enumerate((5000, 3000)):
+        g = rng.integers(0, 0x40, n).astype(np.uint8) | \
+            (rng.integers(0, 2, n).astype(np.uint8) << 7)
+        if i == 0:
+            g[1234] = top_code
+            g[4321] = 0x6F
+        w = oracle.f32_to_f16((rng.standard_normal(n) * 0.02).astype(np.float32))
+        out.append(oracle.StepState(g, float(2.0 ** -K0_EXP) if i == 0 else 1.0,
+                                    np.zeros(n, np.uint8), 1.0,
+                                    np.zeros(n, np.uint16), w))
+    return out
+
+
+HP = (1e-3, 0.9, 0.999, 1e-8, 0.01, 1, 1.0)
+
+
+def assert_unchanged(gpu, states):
+    for i, s in enumerate(states):
+        assert np.array_equal(to_np_u8(gpu.m[i]), s.m)
+        assert np.array_equal(to_np_u16(gpu.v[i]), s.v)
+        assert np.array_equal(to_np_u16(gpu.w[i]), s.w)
+    check_f32_exact(gpu.m_scale.cpu().numpy()[:len(states)],
+                    [s.m_scale[0] for s in states], "m_scale")
+
+
+@pytest.mark.parametrize("top", [0x6F, 0x70, 0xF0, 0x7E])
+@pytest.mark.parametrize("finish", [False, True])
+def test_split_step_found_inf_is_unclipped(bo, top, finish):
+    states = boundary_states(top)
+    expect = 0 if top == 0x6F else 1
+    gpu = GpuState([s.copy() for s in states])
+    ref = [s.copy() for s in states]
+    assert oracle.adam_step_coef(ref, *HP, CLIP) == expect
+    clip = torch.full((1,), CLIP, device="cuda")
+    found = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    hp = HP + (False,)
+    gpu.plan.begin(hp, clip=clip, found=found)
+    torch.cuda.synchronize()
+    assert found.item() == expect
+    if finish:
+        out = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+        gpu.plan.finish(hp, clip=clip, found=out)
+        torch.cuda.synchronize()
+        assert out.item() == expect
+        if expect:
+            assert_unchanged(gpu, states)
+        else:
+            gpu.compare(ref)
+
+
+@pytest.mark.parametrize("top", [0x6F, 0x70])
+def test_clipped_step_found_inf_is_unclipped(bo, top):
+    """fp8_adam_step_clipped on the same gradients: the norm (+inf when
+    found_inf) and the state against the oracle's clipped step."""
+    states = boundary_states(top)
+    gpu = GpuState([s.copy() for s in states])
+    ref = [s.copy() for s in states]
+    f_ref, n_ref = oracle.adam_step_clipped(ref, *HP, 1.0)
+    assert f_ref == (0 if top == 0x6F else 1)
+    found = gpu.plan(*HP, found_inf_dev=gpu.found_dev, max_grad_norm=1.0)
+    assert found == f_ref == gpu.found_dev.item()
+    assert gpu.plan.last_grad_norm == n_ref
+    if f_ref:
+        assert_unchanged(gpu, states)
+    else:
+        gpu.compare(ref)
+
+
+def test_fused_clipped_found_inf_is_unclipped(bo):
+    """fp8_cast_adam_step_clipped: a float32 gradient near the fp32 maximum
+    casts to finite codes whose unscaled value (inv_loss_scale 4) overflows,
+    while the clipped one would not: found_inf = 1 and nothing written, as in
+    the oracle's cast followed by its clipped step."""
+    rng = np.random.default_rng(33)
+    grads = [torch.from_numpy((rng.standard_normal(n) * 1e-3).astype(np.float32))
+             for n in (4000, 2500)]
+    grads[1][77] = 2.0e38
+    ils = 4.0
+    states = fresh_states([torch.zeros(g.numel(), dtype=torch.float16) for g in grads],
+                          o3=False)
+    codes, _, scale = oracle_cast(grads, E4M3)
+    set_grads(states, codes, scale)
+    k1 = np.float32(np.float32(ils) / np.float32(scale[1]))
+    with np.errstate(over="ignore"):
+        assert codes[1][77] == 0x7E and not np.isfinite(np.float32(448.0) * k1)
+    ref = [s.copy() for s in states]
+    f_ref, n_ref = oracle.adam_step_clipped(ref, 1e-3, 0.9, 0.999, 1e-8, 0.01, 1,
+                                            ils, 1.0)
+    assert (f_ref, n_ref) == (1, math.inf)
+    gpu = GpuState([s.copy() for s in states])
+    srcs = [g.cuda() for g in grads]
+    amax = torch.zeros(2, device="cuda")
+    fused = bo.CastStepPlan(bo.CastPlan(srcs, gpu.g, amax, gpu.g_scale, "e4m3"),
+                            gpu.plan)
+    found = fused(1e-3, 0.9, 0.999, 1e-8, 0.01, 1, ils,
+                  found_inf_dev=gpu.found_dev, max_grad_norm=1.0)
+    assert found == 1 and gpu.found_dev.item() == 1
+    assert fused.last_grad_norm == math.inf
+    assert_unchanged(gpu, states)
