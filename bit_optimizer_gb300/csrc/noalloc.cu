@@ -3,15 +3,14 @@
 //
 // fp8_cast_scaled keeps its tensor table, chunk table and per-tensor amax
 // slots in a workspace it allocates with cudaMalloc on first use.  Some
-// callers cannot let a library do that: code running while a CUDA graph is
-// being captured (an allocation would break the capture), runtimes that hand
-// all device memory to their own pool allocator at start-up and forbid other
-// allocations, and services that must never stall on, or fail from, an
-// allocation in the middle of a step.  For them this entry point runs the
-// same two cast kernels with all of that scratch in one fixed-size array
-// compiled into the library (`g_noalloc_scratch` below), so a call allocates
-// nothing: no cudaMalloc, no cudaFree, no allocating library routine, and no
-// host heap either (the tables are staged in fixed host arrays).
+// callers cannot let a library do that: runtimes that hand all device memory
+// to their own pool allocator at start-up and forbid other allocations, and
+// services that must never stall on, or fail from, an allocation in the
+// middle of a step.  For them this entry point runs the same two cast kernels
+// with all of that scratch in one fixed-size array compiled into the library
+// (`g_noalloc_scratch` below), so a call allocates nothing: no cudaMalloc, no
+// cudaFree, no allocating library routine, and no host heap either (the
+// tables are staged in fixed host arrays).
 //
 // What that costs the caller:
 //   * fixed limits: at most kMaxTensors tensors and kMaxChunks chunks of
@@ -25,9 +24,12 @@
 //     needs before its kernels run, but calls whose GPU work overlaps (two
 //     streams, or two host threads) race on the array and can corrupt each
 //     other's results: order such calls on one stream, or with events;
+//   * each call copies its tables from host arrays that the next call
+//     refills, so a stream that is capturing work into a CUDA graph is
+//     refused (FP8OPT_ERR_ARG, nothing enqueued): a recorded copy would read
+//     whatever a later call left in those arrays;
 //   * the first call on each device does the set-up for that device (it asks
-//     the runtime for the array's device address and the kernels' occupancy),
-//     so make that first call before any stream capture.
+//     the runtime for the array's device address and the kernels' occupancy).
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -154,6 +156,14 @@ extern "C" int fp8_cast_scaled_noalloc(const fp8opt_cast_item* items, int n,
   }
   if (n == 0) return FP8OPT_OK;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess ||
+      cap != cudaStreamCaptureStatusNone)
+    return record_error(FP8OPT_ERR_ARG,
+                        "fp8_cast_scaled_noalloc: the stream is capturing a "
+                        "CUDA graph (or its capture state is unknown); the "
+                        "call copies its tables from host arrays that the "
+                        "next call refills, so it runs only uncaptured");
 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0;

@@ -1,11 +1,13 @@
 """fp8_cast_scaled_noalloc: the cast entry point for callers that must not
-allocate device memory (for example code under CUDA graph capture, or a
-runtime whose pool allocator owns all device memory).  It keeps its scratch in
-a fixed array inside the library, so these tests check, through the C ABI,
-that it returns what the allocating fp8_cast_scaled returns on the same
-inputs, on two calls in a row with different lists (the array keeps the
-previous call's contents, which must not leak into the next result), and that
-it refuses lists beyond its fixed limits before launching anything.
+allocate device memory (for example a runtime whose pool allocator owns all
+device memory, or a service that must not stall on an allocation mid-step).
+It keeps its scratch in a fixed array inside the library, so these tests
+check, through the C ABI, that it returns what the allocating fp8_cast_scaled
+returns on the same inputs, and what the oracle returns, on two calls in a row
+with different lists (the array keeps the previous call's contents, which
+must not leak into the next result); that it refuses lists beyond its fixed
+limits before launching anything; and that it refuses a stream that is
+capturing a CUDA graph without breaking that capture.
 
 The test allocates its own buffers with torch; only the entry point under
 test is forbidden to allocate.  Kept in a file of its own that is collected
@@ -16,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+from harness import oracle_cast
 from parity import check_codes, check_f32_exact, to_np_u8
 
 pytestmark = pytest.mark.gpu
@@ -81,6 +84,12 @@ def test_noalloc_matches_the_allocating_cast_on_two_calls():
         check_f32_exact(scale.cpu().numpy(), ref_scale.cpu().numpy()[:n], "scale")
         for i, (c, r) in enumerate(zip(codes, ref_codes)):
             check_codes(to_np_u8(c), to_np_u8(r), fmt, name=f"codes[{i}]")
+        # and against the oracle on the same values
+        o_codes, o_amax, o_scale = oracle_cast([x.cpu() for x in srcs], fmt)
+        check_f32_exact(amax.cpu().numpy(), o_amax, "amax (oracle)")
+        check_f32_exact(scale.cpu().numpy(), o_scale, "scale (oracle)")
+        for i, (c, r) in enumerate(zip(codes, o_codes)):
+            check_codes(to_np_u8(c), r, fmt, name=f"codes[{i}] (oracle)")
 
 
 def test_noalloc_refuses_lists_beyond_its_limits():
@@ -104,3 +113,37 @@ def test_noalloc_refuses_lists_beyond_its_limits():
     assert "chunks" in L.fp8opt_last_error().decode()
     torch.cuda.synchronize()
     assert bool((amax == -7.0).all()) and bool((scale == -7.0).all())
+
+
+def test_noalloc_refuses_a_capturing_stream():
+    """Its tables come from host arrays that the next call refills, so a
+    stream that is capturing a CUDA graph is refused with an argument error,
+    nothing is enqueued, and the caller's capture stays valid."""
+    import bit_optimizer_gb300 as bo
+    from bit_optimizer_gb300 import _lib
+    L = bo.load()
+    src = torch.randn(4096, device="cuda").to(torch.bfloat16)
+    code = torch.full((4096,), 0xA5, dtype=torch.uint8, device="cuda")
+    amax = torch.full((1,), -7.0, device="cuda")
+    scale = torch.full((1,), -7.0, device="cuda")
+    items = items_for(_lib, [src], [code], amax, scale)
+    x = torch.zeros(16, device="cuda")
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=side):
+        rc = L.fp8_cast_scaled_noalloc(items, 1, E4M3, side.cuda_stream)
+        x.add_(1.0)
+    assert rc == _lib.ERR_ARG
+    assert "capturing" in L.fp8opt_last_error().decode()
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert bool((x == 2.0).all())
+    assert bool((code == 0xA5).all()) and amax.item() == -7.0 and scale.item() == -7.0
+    # uncaptured, the same call runs
+    assert L.fp8_cast_scaled_noalloc(items, 1, E4M3, side.cuda_stream) == 0
+    side.synchronize()
+    _, o_amax, o_scale = oracle_cast([src.cpu()], E4M3)
+    check_f32_exact(amax.cpu().numpy(), o_amax, "amax")
+    check_f32_exact(scale.cpu().numpy(), o_scale, "scale")
