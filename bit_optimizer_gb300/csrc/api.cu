@@ -798,7 +798,11 @@ int empty_step(const char* fn, int* found_inf, uint32_t* found_inf_dev,
   return FP8OPT_OK;
 }
 
-// Waits for the stream and reads this call's found_inf word.
+// Waits for the stream and reads this call's found_inf word.  Called after
+// g_mu is released: the read blocks until the stream has run the call's
+// kernels, and other threads' calls on other streams must not wait for that.
+// The word stays valid meanwhile: only calls on this stream (one host thread
+// at a time) reuse this stream's workspace.
 int read_found(const char* fn, const unsigned long long* found, uint32_t epoch,
                cudaStream_t stream, int* out) {
   unsigned long long tag = 0;
@@ -915,7 +919,8 @@ struct NormReq {
   float* norm_dev = nullptr;   // device out, or NULL
 };
 
-// Waits for the stream and reads this call's found_inf word and norm.
+// Waits for the stream and reads this call's found_inf word and norm; called
+// after g_mu is released, as read_found.
 int read_results(const char* fn, const unsigned long long* found, uint32_t epoch,
                  const double* norm_dev, cudaStream_t stream, int* found_out,
                  double* norm_out) {
@@ -1014,7 +1019,7 @@ int adam_step(const char* fn, bool l2, const fp8opt_param* params, int n,
   StepScalars s =
       make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale, l2);
 
-  std::lock_guard<std::mutex> lock(g_mu);
+  std::unique_lock<std::mutex> lock(g_mu);
   StepCall c;
   if ((st = setup_step(fn, params, n, stream_ptr, nr.on, true, &c)) != FP8OPT_OK)
     return st;
@@ -1040,6 +1045,7 @@ int adam_step(const char* fn, bool l2, const fp8opt_param* params, int n,
                     c.info->step_w8, ws->step_any_vs, stream, launch_mark());
     if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
   }
+  lock.unlock();   // before any wait for the stream
   if (found_inf != nullptr || nr.norm != nullptr)
     return read_results(fn, c.sc.found, c.epoch, c.norm, stream, found_inf, nr.norm);
   return FP8OPT_OK;
@@ -1232,7 +1238,7 @@ extern "C" int fp8_cast_adamw_step(const fp8opt_cast_item* grads,
   const StepScalars s =
       make_scalars(lr, beta1, beta2, eps, wd, step, inv_loss_scale, false);
 
-  std::lock_guard<std::mutex> lock(g_mu);
+  std::unique_lock<std::mutex> lock(g_mu);
   int dev = 0;
   DeviceInfo* info = nullptr;
   if ((st = current_device_and_info(&dev, &info)) != FP8OPT_OK) return st;
@@ -1263,6 +1269,7 @@ extern "C" int fp8_cast_adamw_step(const fp8opt_cast_item* grads,
                        info->step_update, info->step_update_var,
                        info->step_w8, ws->step_any_vs, stream, launch_mark());
   if (e != cudaSuccess) return cuda_fail(e, "fp8_cast_adamw_step: launch");
+  lock.unlock();   // before any wait for the stream
   if (found_inf != nullptr) return read_found(fn, sc.found, epoch, stream, found_inf);
   return FP8OPT_OK;
 }
@@ -1397,7 +1404,7 @@ static int cast_adam_clipped(const char* fn, const fp8opt_cast_item* grads,
     return empty_step(fn, found_inf, found_inf_dev, stream);
   }
 
-  std::lock_guard<std::mutex> lock(g_mu);
+  std::unique_lock<std::mutex> lock(g_mu);
   int dev = 0;
   DeviceInfo* info = nullptr;
   if ((st = current_device_and_info(&dev, &info)) != FP8OPT_OK) return st;
@@ -1486,6 +1493,7 @@ static int cast_adam_clipped(const char* fn, const fp8opt_cast_item* grads,
                     info->step_update_var, info->step_w8, ws->step_any_vs,
                     stream, mark);
   if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
+  lock.unlock();   // before any wait for the stream
   if (found_inf != nullptr || grad_norm != nullptr)
     return read_results(fn, sc.found, epoch, norm, stream, found_inf, grad_norm);
   return FP8OPT_OK;
