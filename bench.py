@@ -79,6 +79,12 @@ def parse():
     p.add_argument("--reduce-only", type=int, default=None, metavar="K",
                    help="time only the local FP8 reduction of K shards of the "
                         "124M list and print its line (profiling case)")
+    p.add_argument("--record-traffic", default=None, metavar="CSV",
+                   help="write the step_update DRAM traffic record from an ncu "
+                        "raw-page CSV of a capture of this workload (no GPU "
+                        "needed), then exit")
+    p.add_argument("--capture-command", default="",
+                   help="with --record-traffic: the command the capture ran")
     p.add_argument("--cast-only", default=None, choices=["e4m3", "e5m2"],
                    help="time only the scaled cast of the 124M list to this "
                         "format and print its line (profiling case)")
@@ -413,7 +419,8 @@ def build_state(wl, device, **opt_kw):
 KERNEL_SOURCES = ("bit_optimizer_gb300/csrc/step_kernels.cu",
                   "bit_optimizer_gb300/csrc/fp8opt_internal.cuh",
                   "bit_optimizer_gb300/csrc/api.cu")
-TRAFFIC_SUMMARY = "profiles/step_update_o2_1layer.md"
+# written by --record-traffic from an ncu capture of step_update
+TRAFFIC_RECORD = "profiles/step_update_traffic.json"
 
 
 def kernel_source_digest():
@@ -434,20 +441,72 @@ def kernel_source_digest():
 
 
 def update_traffic_per_param():
-    """DRAM bytes per parameter of one step_update launch from the committed
-    ncu summary, or None when the kernel source changed since the capture."""
+    """DRAM bytes per parameter of one step_update launch from the recorded
+    ncu capture, or None when there is none or the kernel source changed
+    since it was taken."""
     try:
-        text = open(os.path.join(ROOT, TRAFFIC_SUMMARY)).read()
-    except OSError:
+        with open(os.path.join(ROOT, TRAFFIC_RECORD)) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    fields = dict(line.split(":", 1) for line in text.splitlines()
-                  if line.startswith(("traffic_bytes_per_param:", "source_digest:")))
-    if fields.get("source_digest", "").strip() != kernel_source_digest():
+    if rec.get("source_digest") != kernel_source_digest():
         return None
     try:
-        return float(fields["traffic_bytes_per_param"])
-    except (KeyError, ValueError):
+        return float(rec["traffic_bytes_per_param"])
+    except (KeyError, TypeError, ValueError):
         return None
+
+
+NCU_UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12,
+             "KB": 1e3, "MB": 1e6, "GB": 1e9, "nsecond": 1e-9, "usecond": 1e-6,
+             "msecond": 1e-3, "second": 1.0, "ns": 1e-9, "us": 1e-6,
+             "ms": 1e-3}
+
+
+def ncu_launches(csv_path, kernel="step_update"):
+    """The launches of `kernel` in an ncu raw-page CSV (ncu -i REP --page raw
+    --csv): per launch, DRAM bytes read and written and the duration in
+    seconds, converted from the units row."""
+    import csv
+    with open(csv_path, newline="") as f:
+        rows = [r for r in csv.reader(f) if r]
+    head = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+    names, units = rows[head], rows[head + 1]
+    col = {n: i for i, n in enumerate(names)}
+
+    def value(r, metric):
+        i = col[metric]
+        return float(r[i].replace(",", "")) * NCU_UNITS.get(units[i], 1.0)
+
+    out = []
+    for r in rows[head + 2:]:
+        if len(r) == len(names) and kernel in r[col["Kernel Name"]]:
+            out.append({"dram_read": value(r, "dram__bytes_read.sum"),
+                        "dram_write": value(r, "dram__bytes_write.sum"),
+                        "seconds": value(r, "gpu__time_duration.sum")})
+    return out
+
+
+def record_traffic(csv_path, wl, command):
+    """Writes TRAFFIC_RECORD from an ncu capture of step_update on workload
+    wl: DRAM bytes (read + write) per launch over wl's parameters, with the
+    current source digest."""
+    launches = ncu_launches(csv_path)
+    if not launches:
+        raise SystemExit(f"no step_update launch in {csv_path}")
+    rd = sum(x["dram_read"] for x in launches) / len(launches)
+    wr = sum(x["dram_write"] for x in launches) / len(launches)
+    us = sum(x["seconds"] for x in launches) / len(launches) * 1e6
+    rec = {"kernel": "step_update", "workload": wl.name, "params": wl.n_params,
+           "launches": len(launches), "dram_bytes_read": rd,
+           "dram_bytes_write": wr, "duration_us": us,
+           "traffic_bytes_per_param": round((rd + wr) / wl.n_params, 4),
+           "algorithmic_bytes_per_param": UPDATE_BYTES,
+           "source_digest": kernel_source_digest(), "command": command}
+    with open(os.path.join(ROOT, TRAFFIC_RECORD), "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    return rec
 
 
 def measured_peak():
@@ -907,6 +966,10 @@ def main():
     # a timed step must be a full update: a workload that seeds an inf (the
     # GradScaler skip case) is timed with that element cleared
     wl = dataclasses.replace(wl, inf_site=None)
+    if args.record_traffic is not None:
+        print(json.dumps(record_traffic(args.record_traffic, wl,
+                                        args.capture_command)), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args, wl)
     elif args.sharded:
