@@ -61,6 +61,22 @@ def oracle_step(states, wl, step, ils=None, l2=False):
                              l2=l2)
 
 
+def oracle_step_threads(states, wl, step, pool, workers):
+    """oracle_step over a long list on the host's cores: the tensors are
+    dealt, largest first, into `workers` groups of about equal size, and each
+    group is one oracle call in a thread of `pool` (ctypes releases the GIL).
+    With every gradient finite, each tensor's result is the one of a single
+    call over the whole list; returns the largest found_inf of the groups."""
+    groups = [[] for _ in range(workers)]
+    load = [0] * workers
+    for i in sorted(range(len(states)), key=lambda i: -states[i].numel):
+        j = load.index(min(load))
+        groups[j].append(states[i])
+        load[j] += states[i].numel
+    found = list(pool.map(lambda g: oracle_step(g, wl, step) if g else 0, groups))
+    return max(found)
+
+
 class GpuState:
     """The library's view of a list of oracle states, on the device."""
 

@@ -3,7 +3,9 @@ bench times.  Every tensor is resident and stepped by the library; the
 oracle follows a sample of whole tensors (all the small ones and the
 position embedding, and for the cast every tensor), and properties that hold
 at any size are checked on every tensor."""
+import concurrent.futures as cf
 import dataclasses
+import os
 
 import numpy as np
 import pytest
@@ -11,7 +13,7 @@ import torch
 
 import oracle
 import synth
-from harness import DeviceList, host_src, oracle_step
+from harness import DeviceList, host_src, oracle_step, oracle_step_threads
 from parity import (check_codes, check_f16, check_f32_exact, check_master,
                     to_np_u16, to_np_u8)
 
@@ -55,28 +57,34 @@ def test_cast_gpt2_124m_every_tensor(bo, fmt):
         check_codes(to_np_u8(codes[i]), rc, f, name=f"codes[{i}]")
 
 
-def lockstep_full(wl, steps, sample, first=1, fused=False, scaled_v=False):
+def lockstep_full(wl, steps, sample, first=1, fused=False, scaled_v=False,
+                  pool=None, workers=1):
     """Every tensor stepped by the library; the sampled ones start each step
     from the oracle's state.  fused: one fp8_cast_adamw_step call per step
-    (the bench's configuration), else fp8_cast_scaled then fp8_adamw_step."""
+    (the bench's configuration), else fp8_cast_scaled then fp8_adamw_step.
+    pool: a thread pool for the oracle's casts, steps and the comparisons
+    (workers threads), for samples of whole large lists."""
     dl = DeviceList(wl, scaled_v=scaled_v)
     states = {i: dl.fresh_oracle(i) for i in sample}
+    each = (lambda f, xs: list(pool.map(f, xs))) if pool else \
+        (lambda f, xs: [f(x) for x in xs])
     for t in range(first, first + steps):
         dl.gen_grads(t)
         if fused:
             for i in sample:
                 dl.put(i, states[i])
             f = dl.cast_step(t)
-            dl.check_cast(sample, states)
+            each(lambda i: dl.check_cast([i], states), sample)
         else:
             dl.cast_and_check(sample, states)
             for i in sample:
                 dl.put(i, states[i])
             f = dl.step(t)
-        f_ref = oracle_step([states[i] for i in sample], wl, t)
+        listed = [states[i] for i in sample]
+        f_ref = (oracle_step_threads(listed, wl, t, pool, workers) if pool
+                 else oracle_step(listed, wl, t))
         assert f == f_ref == 0
-        for i in sample:
-            dl.compare(i, states[i])
+        each(lambda i: dl.compare(i, states[i]), sample)
     return dl, states
 
 
@@ -114,11 +122,29 @@ def test_o2_350m_full_inf_skip_and_step(bo):
     dl.invariants()
 
 
-@pytest.mark.parametrize("fused", [False, True])
-def test_o3_1p3b_full(bo, fused):
+def test_o3_1p3b_full_two_calls(bo):
+    """The 1.3B O3 list through fp8_cast_scaled then fp8_adamw_step, with the
+    oracle on a sample of whole tensors."""
     wl = synth.o3_1p3b()
     sample = sample_of(wl, 6_000_000)
-    dl, _ = lockstep_full(wl, wl.warmup_steps + 1, sample, fused=fused)
+    dl, _ = lockstep_full(wl, wl.warmup_steps + 1, sample, fused=False)
+    dl.invariants()
+
+
+def test_o3_1p3b_every_tensor(bo):
+    """The 1.3B O3 list through the fused call (the bench's configuration),
+    with the oracle stepping every tensor from the same inputs: every
+    gradient code, m, v, master and weight-copy element and every scale of
+    all 292 tensors, including wte, qkv, fc and fc2, whose hundreds to
+    thousands of chunks merge their amax through atomics from many CTAs.
+    Three steps (two warm-up steps, then the measured one), so the moments
+    carry history."""
+    wl = synth.o3_1p3b()
+    workers = max(1, min(32, os.cpu_count() or 1))
+    sample = list(range(len(wl.shapes)))
+    with cf.ThreadPoolExecutor(workers) as pool:
+        dl, _ = lockstep_full(wl, wl.warmup_steps + 1, sample, fused=True,
+                              pool=pool, workers=workers)
     dl.invariants()
 
 
@@ -248,3 +274,55 @@ def test_cast_tensor_above_two_giga_elements(bo):
     idx = np.concatenate([np.arange(0, n, 9973), np.arange(n - 40000, n)])
     assert np.array_equal(got[torch.from_numpy(idx).cuda()].cpu().numpy(), rc[idx])
     assert int(got[n - 7].item()) == 0x7E
+
+
+def test_o3_step_tensor_above_two_giga_elements(bo):
+    """An O3 step over one tensor of 2^31 + 12345 elements (past 32-bit
+    indexing; 65537 chunks).  The oracle steps a sample of its elements (a
+    strided sample and the last 40,000, which straddle element 2^31) as a
+    tensor of its own.  First step from m = v = 0: this step's m is
+    (1 - beta1) * g, so with the one largest gradient code (448) planted in
+    the sample the tensor's m amax, and so its m scale, are the sample's;
+    with the one largest weight (1.0, far above the others' |w| < 0.2)
+    planted in the sample, the master's amax and the weight copy's scale are
+    the sample's too.  Every other element's result depends only on its own
+    inputs, so the sampled elements must match the oracle's sample: scales
+    and found_inf bit-exact, codes, v and weights within the tolerances."""
+    n = (1 << 31) + 12345
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(synth.tensor_seed(8, 0, "grad"))
+    g = torch.randint(0, 0x7E, (n,), generator=gen, device="cuda", dtype=torch.uint8)
+    g |= torch.randint(0, 2, (n,), generator=gen, device="cuda", dtype=torch.uint8) << 7
+    w = (torch.randn(n, generator=gen, device="cuda") * 0.02).clamp_(-0.19, 0.19)
+    w = w.to(torch.float16)
+    idx = np.concatenate([np.arange(0, n - 40000, 9973), np.arange(n - 40000, n)])
+    top_g, top_w = int(idx[len(idx) // 3]), int(idx[-3])
+    g[top_g] = 0xFE                         # -448: the largest |g|
+    w[top_w] = 1.0                          # the largest |master|
+    m = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    v = torch.zeros(n, dtype=torch.float16, device="cuda")
+    w8 = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    g_scale = torch.full((1,), 2.0 ** -4, device="cuda")
+    m_scale = torch.ones(1, device="cuda")
+    w8_scale = torch.ones(1, device="cuda")
+    w8_amax = torch.zeros(1, device="cuda")
+    sel = torch.from_numpy(idx).cuda()
+    st = oracle.StepState(to_np_u8(g[sel]), 2.0 ** -4, np.zeros(idx.size, np.uint8),
+                          1.0, np.zeros(idx.size, np.uint16), to_np_u16(w[sel]),
+                          o3=True)
+    plan = bo.AdamWPlan([g], g_scale, [m], m_scale, [v], [w], [w8], w8_scale,
+                        w8_amax)
+    found_dev = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    args = (1e-3, 0.9, 0.999, 1e-8, 0.01, 1, 0.5)
+    assert plan(*args, found_inf_dev=found_dev) == 0 and found_dev.item() == 0
+    assert oracle.adamw_step([st], *args) == 0
+    check_f32_exact(m_scale.cpu().numpy(), st.m_scale, "m_scale")
+    check_f32_exact(w8_scale.cpu().numpy(), st.w8_scale, "w8_scale")
+    check_f32_exact(w8_amax.cpu().numpy(), st.w8_amax, "w8_amax")
+    assert st.w8_amax[0] == np.float32(np.float16(w[top_w].item()))
+    check_codes(to_np_u8(m[sel]), st.m, name="m")
+    check_f16(to_np_u16(v[sel]), st.v, name="v")
+    check_master(to_np_u16(w[sel]), st.w, name="master")
+    check_f16(to_np_u16(w[sel]), st.w, name="w")
+    check_codes(to_np_u8(w8[sel]), st.w8, name="w8")
+    assert int(m[top_g].item()) == 0xFE      # the largest |m| on the maximum
