@@ -113,6 +113,23 @@ def lib():
         L.oracle_adam_step_coef.argtypes = [
             C.POINTER(Param), C.c_int, C.c_int, C.c_float, C.c_float, C.c_float,
             C.c_float, C.c_float, C.c_int64, C.c_float, C.c_float]
+        step_head = [C.POINTER(Param), C.c_int, C.c_int, C.c_float, C.c_float,
+                     C.c_float]
+        L.oracle_step_maxima.restype = C.c_int
+        L.oracle_step_maxima.argtypes = step_head + [
+            C.c_float, C.c_int64, C.c_float, C.c_float, C.c_void_p, C.c_void_p]
+        L.oracle_step_update.restype = C.c_int
+        L.oracle_step_update.argtypes = step_head + [
+            C.c_float, C.c_float, C.c_int64, C.c_float, C.c_float, C.c_void_p,
+            C.c_void_p, C.c_void_p]
+        L.oracle_weight_copy.restype = C.c_int
+        L.oracle_weight_copy.argtypes = [C.POINTER(Param), C.c_int, C.c_void_p]
+        L.oracle_reduce_scaled_given.restype = C.c_int
+        L.oracle_reduce_scaled_given.argtypes = [
+            C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_int, C.c_int,
+            C.c_int, C.c_float, C.c_float, C.c_void_p, C.c_void_p]
+        L.oracle_fp8_sq_sum.restype = None
+        L.oracle_fp8_sq_sum.argtypes = [C.c_void_p, C.c_int64, C.c_int, C.c_void_p]
         L.oracle_bias_power.restype = C.c_double
         L.oracle_bias_power.argtypes = [C.c_double, C.c_int64]
         L.oracle_v_scale_from_bound.restype = C.c_float
@@ -193,6 +210,36 @@ def cast_scaled(src: np.ndarray, dtype: int, fmt: int):
 
 
 # ---------------------------------------------------------- FP8 reduction
+
+def reduce_scaled_given(shards: np.ndarray, scales, in_fmt: int, out_fmt: int,
+                        post: float, amax: float, numel: int = None):
+    """reduce_scaled with the output scale taken from a given amax (a tensor
+    reduced in pieces takes the whole tensor's amax): returns (codes uint8,
+    scale float32 scalar)."""
+    sh = np.ascontiguousarray(shards, dtype=np.uint8)
+    assert sh.ndim == 2
+    k, stride = sh.shape
+    n = stride if numel is None else int(numel)
+    sc = np.ascontiguousarray(scales, dtype=np.float32).ravel()
+    assert sc.size == k
+    codes = np.empty(n, dtype=np.uint8)
+    scale = np.zeros(1, dtype=np.float32)
+    rc = lib().oracle_reduce_scaled_given(_ptr(sh), n, stride, _ptr(sc), k, in_fmt,
+                                          out_fmt, post, amax, _ptr(codes),
+                                          _ptr(scale))
+    if rc != 0:
+        raise ValueError(f"oracle_reduce_scaled_given rejected its arguments ({rc})")
+    return codes, scale[0]
+
+
+def fp8_sq_sum(codes: np.ndarray, fmt: int) -> int:
+    """The exact sum of the codes' squared values in units of 2^-32, as a
+    Python int (non-finite codes count 0)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8).ravel()
+    out = np.zeros(2, dtype=np.uint64)
+    lib().oracle_fp8_sq_sum(_ptr(c), c.size, fmt, _ptr(out))
+    return int(out[0]) | (int(out[1]) << 64)
+
 
 def reduce_scaled(shards: np.ndarray, scales, in_fmt: int, out_fmt: int,
                   post: float = 1.0, numel: int = None):
@@ -339,6 +386,50 @@ def adam_step_coef(states: Sequence[StepState], lr, beta1, beta2, eps, wd, step,
     if rc < 0:
         raise ValueError(f"oracle_adam_step_coef rejected its arguments ({rc})")
     return rc
+
+
+def step_maxima(states: Sequence[StepState], lr, beta1, beta2, wd, step,
+                inv_loss_scale, clip=1.0, l2=False):
+    """The step's first phase: (found_inf, amax_m, gmax), the per-record
+    amax of this step's first moment and max |g| (float32 arrays; not
+    written when found_inf).  Writes no state."""
+    n = len(states)
+    am = np.zeros(max(1, n), np.float32)
+    gm = np.zeros(max(1, n), np.float32)
+    rc = lib().oracle_step_maxima(_params(states), n, 1 if l2 else 0, lr, beta1,
+                                  beta2, wd, step, inv_loss_scale, clip,
+                                  _ptr(am), _ptr(gm))
+    if rc < 0:
+        raise ValueError(f"oracle_step_maxima rejected its arguments ({rc})")
+    return rc, am[:n], gm[:n]
+
+
+def step_update(states: Sequence[StepState], lr, beta1, beta2, eps, wd, step,
+                inv_loss_scale, amax_m, gmax, clip=1.0, l2=False):
+    """The step's second phase from the given per-record maxima (updates the
+    states in place); returns each record's new FP16 master amax."""
+    n = len(states)
+    am = np.ascontiguousarray(amax_m, np.float32)
+    gm = np.ascontiguousarray(gmax, np.float32)
+    assert am.size >= n and gm.size >= n
+    wm = np.zeros(max(1, n), np.float32)
+    rc = lib().oracle_step_update(_params(states), n, 1 if l2 else 0, lr, beta1,
+                                  beta2, eps, wd, step, inv_loss_scale, clip,
+                                  _ptr(am), _ptr(gm), _ptr(wm))
+    if rc < 0:
+        raise ValueError(f"oracle_step_update rejected its arguments ({rc})")
+    return wm[:n]
+
+
+def weight_copy(states: Sequence[StepState], master_amax) -> None:
+    """The step's third phase: each O3 record's FP8 weight copy from the
+    given master amax."""
+    n = len(states)
+    wm = np.ascontiguousarray(master_amax, np.float32)
+    assert wm.size >= n
+    rc = lib().oracle_weight_copy(_params(states), n, _ptr(wm))
+    if rc < 0:
+        raise ValueError(f"oracle_weight_copy rejected its arguments ({rc})")
 
 
 def grad_norm(states: Sequence[StepState], inv_loss_scale):

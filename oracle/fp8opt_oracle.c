@@ -240,6 +240,19 @@ static float or_load(const void *src, int dtype, int64_t i)
 
 /* ------------------------------------------------------------------- cast */
 
+/* The encode of a cast: each element multiplied by the scale in fp32 and
+ * encoded; a non-finite element keeps its own code. */
+static void or_cast_encode(const void *src, int dtype, int64_t numel, int fmt,
+                           float scale, uint8_t *codes)
+{
+    for (int64_t i = 0; i < numel; ++i) {
+        float x = or_load(src, dtype, i);
+        if (!isfinite(x)) { codes[i] = oracle_fp8_encode(x, fmt); continue; }
+        float t = x * scale;
+        codes[i] = oracle_fp8_encode(t, fmt);
+    }
+}
+
 /* Scaled FP8 cast of one tensor (weight gradients from wider types to FP8,
  * MS-AMP O1): amax over the tensor, scale = fp8_max / amax, then each element
  * is multiplied by the scale in fp32 and encoded.  Returns 0, or -1 on a bad
@@ -252,12 +265,7 @@ int oracle_cast_scaled(const void *src, int dtype, int64_t numel, int fmt,
     for (int64_t i = 0; i < numel; ++i) or_amax_add(&a, or_load(src, dtype, i));
     float amax = or_amax_value(&a);
     float scale = oracle_scale_from_amax(amax, fmt);
-    for (int64_t i = 0; i < numel; ++i) {
-        float x = or_load(src, dtype, i);
-        if (!isfinite(x)) { codes[i] = oracle_fp8_encode(x, fmt); continue; }
-        float t = x * scale;
-        codes[i] = oracle_fp8_encode(t, fmt);
-    }
+    or_cast_encode(src, dtype, numel, fmt, scale, codes);
     *amax_out = amax;
     *scale_out = scale;
     return 0;
@@ -357,9 +365,34 @@ static float or_grad_l2(const oracle_param *p, float g, int l2, float wd,
     return l2 ? fmaf(wd, oracle_f16_to_f32(p->w[i]), g) : g;
 }
 
-/* The step below with an optional gradient-clipping coefficient: clip != 1
- * multiplies each tensor's factor k (after the found_inf check, which uses the
- * unclipped k). */
+/* ------------------------------------------------------ step, by phases
+ *
+ * A step's per-tensor quantities are maxima over the tensor's elements: the
+ * amax of this step's fp32 first moment (its new scale), max |g| (a scaled
+ * second moment's bound) and, for O3, the amax of the new FP16 master (the
+ * weight copy's scale).  Everything else is elementwise.  The phases below
+ * compute the maxima, or take them as given: oracle_adam_step runs them in
+ * turn over whole tensors, and a tensor cut into pieces (element ranges with
+ * the tensor's scales and bounds) gives the same elements when every piece
+ * takes the whole tensor's maxima. */
+
+/* The phases' argument check: a list length and a step count (from 1). */
+static int or_bad_step(int n, int64_t step)
+{
+    return n < 0 || step < 1;
+}
+
+/* The factor the moments use: k = inv_loss_scale / g_scale, times the
+ * clip coefficient when the step clips (clip != 1).  found_inf is decided on
+ * the unclipped k. */
+static float or_step_factor(const oracle_param *p, float inv_loss_scale,
+                            float clip)
+{
+    float k = or_grad_factor(p, inv_loss_scale);
+    if (clip != 1.0f) k = k * clip;
+    return k;
+}
+
 static int or_adam_step(const oracle_param *p, int n, int l2, float lr,
                         float beta1, float beta2, float eps, float wd,
                         int64_t step, float inv_loss_scale, float clip);
@@ -375,11 +408,88 @@ int oracle_adam_step(const oracle_param *p, int n, int l2, float lr, float beta1
                         inv_loss_scale, 1.0f);
 }
 
-static int or_adam_step(const oracle_param *p, int n, int l2, float lr,
-                        float beta1, float beta2, float eps, float wd,
-                        int64_t step, float inv_loss_scale, float clip)
+/* One tensor's maxima: the amax of this step's fp32 first moment and, for a
+ * scaled second moment, max |g| (else 0). */
+static void or_tensor_maxima(const oracle_param *q, int l2, float beta1,
+                             float wd, const or_scalars *sc, float k,
+                             float *amax_m, float *gmax)
 {
-    if (n < 0 || step < 1) return -1;
+    const or_scalars s = *sc;
+    float minv = 1.0f / *q->m_scale;
+    int scaled_v = q->v_bound != NULL;
+    or_amax am = {0, 0, 0.0f}, ag = {0, 0, 0.0f};
+    for (int64_t i = 0; i < q->numel; ++i) {
+        float g = or_grad_l2(q, or_grad(q, k, i), l2, wd, i);
+        or_amax_add(&am, or_m_new(q, minv, g, beta1, &s, i));
+        if (scaled_v) or_amax_add(&ag, g);
+    }
+    *amax_m = or_amax_value(&am);
+    *gmax = or_amax_value(&ag);
+}
+
+/* One tensor's update from its given maxima: the first moment re-encoded
+ * with the scale of amax_m, v (scaled by the bound that gmax gives), the
+ * FP16 weight or master; returns the amax of the new FP16 master. */
+static float or_tensor_update(const oracle_param *q, int l2, float beta1,
+                              float beta2, float eps, float wd,
+                              const or_scalars *sc, float k, float amax_m,
+                              float gmax)
+{
+    const or_scalars s = *sc;
+    float minv = 1.0f / *q->m_scale;
+    int scaled_v = q->v_bound != NULL;
+    float m_scale_new = oracle_scale_from_amax(amax_m, OR_E4M3);
+    float vinv = 1.0f, b_new = 0.0f, v_scale_new = 1.0f;
+    if (scaled_v) {
+        vinv = *q->v_bound * 0x1p-14f;
+        b_new = fmaf(beta2, *q->v_bound, s.omb2 * (gmax * gmax));
+        v_scale_new = oracle_v_scale_from_bound(b_new);
+    }
+
+    or_amax aw = {0, 0, 0.0f};
+    for (int64_t i = 0; i < q->numel; ++i) {
+        float g = or_grad_l2(q, or_grad(q, k, i), l2, wd, i);
+        float m = or_m_new(q, minv, g, beta1, &s, i);
+        float vp = oracle_f16_to_f32(q->v[i]);
+        if (scaled_v) vp = vp * vinv;
+        float wp = oracle_f16_to_f32(q->w[i]);
+        float v = fmaf(beta2, vp, s.omb2 * (g * g));
+        float denom = fmaf(sqrtf(v), s.inv_sbc2, eps);
+        float upd = m / denom;
+        float w = fmaf(-s.step_size, upd, wp * s.decay);
+        q->m[i] = oracle_fp8_encode(m * m_scale_new, OR_E4M3);
+        q->v[i] = oracle_f32_to_f16(scaled_v ? v * v_scale_new : v);
+        q->w[i] = oracle_f32_to_f16(w);
+        if (q->w8) or_amax_add(&aw, oracle_f16_to_f32(q->w[i]));
+    }
+    *q->m_scale = m_scale_new;
+    if (scaled_v) *q->v_bound = b_new;
+    return or_amax_value(&aw);
+}
+
+/* One tensor's O3 FP8 weight copy, encoded from the FP16 master with the
+ * scale of the given master amax. */
+static void or_tensor_copy(const oracle_param *q, float amax_w)
+{
+    float w8_scale = oracle_scale_from_amax(amax_w, OR_E4M3);
+    for (int64_t i = 0; i < q->numel; ++i)
+        q->w8[i] = oracle_fp8_encode(oracle_f16_to_f32(q->w[i]) * w8_scale,
+                                     OR_E4M3);
+    *q->w8_scale = w8_scale;
+    *q->w8_amax = amax_w;
+}
+
+/* Phase 1: found_inf, the GradScaler check over every record (on the
+ * unscaled gradients, before any decay term and any clipping), and when it
+ * is clear each record's maxima (amax_m[t], gmax[t]; the factor k times
+ * clip).  Writes no state.  Returns 1 when found_inf (the maxima are then
+ * not written), 0, or -1 on a bad argument. */
+int oracle_step_maxima(const oracle_param *p, int n, int l2, float lr,
+                       float beta1, float beta2, float wd, int64_t step,
+                       float inv_loss_scale, float clip, float *amax_m,
+                       float *gmax)
+{
+    if (or_bad_step(n, step)) return -1;
     or_scalars s = or_make_scalars(lr, beta1, beta2, wd, step, l2);
 
     /* GradScaler check over every tensor before any state changes (on the
@@ -389,62 +499,63 @@ static int or_adam_step(const oracle_param *p, int n, int l2, float lr,
         for (int64_t i = 0; i < p[t].numel; ++i)
             if (!isfinite(or_grad(&p[t], k, i))) return 1;
     }
+    for (int t = 0; t < n; ++t)
+        or_tensor_maxima(&p[t], l2, beta1, wd, &s,
+                         or_step_factor(&p[t], inv_loss_scale, clip),
+                         &amax_m[t], &gmax[t]);
+    return 0;
+}
 
+/* Phase 2: each record's update from the given maxima (phase 1's, or the
+ * whole tensor's for a piece); master_amax[t] receives the amax of record
+ * t's new FP16 master (may be NULL).  Returns 0, or -1 on a bad argument. */
+int oracle_step_update(const oracle_param *p, int n, int l2, float lr,
+                       float beta1, float beta2, float eps, float wd,
+                       int64_t step, float inv_loss_scale, float clip,
+                       const float *amax_m, const float *gmax,
+                       float *master_amax)
+{
+    if (or_bad_step(n, step)) return -1;
+    or_scalars s = or_make_scalars(lr, beta1, beta2, wd, step, l2);
     for (int t = 0; t < n; ++t) {
-        const oracle_param *q = &p[t];
-        float k = or_grad_factor(q, inv_loss_scale);
-        if (clip != 1.0f) k = k * clip;
-        float minv = 1.0f / *q->m_scale;
-        int scaled_v = q->v_bound != NULL;
-
-        /* amax of this step's fp32 first moment -> its new scale; for a
-         * scaled second moment also max |g|. */
-        or_amax am = {0, 0, 0.0f}, ag = {0, 0, 0.0f};
-        for (int64_t i = 0; i < q->numel; ++i) {
-            float g = or_grad_l2(q, or_grad(q, k, i), l2, wd, i);
-            or_amax_add(&am, or_m_new(q, minv, g, beta1, &s, i));
-            if (scaled_v) or_amax_add(&ag, g);
-        }
-        float m_scale_new = oracle_scale_from_amax(or_amax_value(&am), OR_E4M3);
-        float vinv = 1.0f, b_new = 0.0f, v_scale_new = 1.0f;
-        if (scaled_v) {
-            float gmax = or_amax_value(&ag);
-            vinv = *q->v_bound * 0x1p-14f;
-            b_new = fmaf(beta2, *q->v_bound, s.omb2 * (gmax * gmax));
-            v_scale_new = oracle_v_scale_from_bound(b_new);
-        }
-
-        or_amax aw = {0, 0, 0.0f};
-        for (int64_t i = 0; i < q->numel; ++i) {
-            float g = or_grad_l2(q, or_grad(q, k, i), l2, wd, i);
-            float m = or_m_new(q, minv, g, beta1, &s, i);
-            float vp = oracle_f16_to_f32(q->v[i]);
-            if (scaled_v) vp = vp * vinv;
-            float wp = oracle_f16_to_f32(q->w[i]);
-            float v = fmaf(beta2, vp, s.omb2 * (g * g));
-            float denom = fmaf(sqrtf(v), s.inv_sbc2, eps);
-            float upd = m / denom;
-            float w = fmaf(-s.step_size, upd, wp * s.decay);
-            q->m[i] = oracle_fp8_encode(m * m_scale_new, OR_E4M3);
-            q->v[i] = oracle_f32_to_f16(scaled_v ? v * v_scale_new : v);
-            q->w[i] = oracle_f32_to_f16(w);
-            if (q->w8) or_amax_add(&aw, oracle_f16_to_f32(q->w[i]));
-        }
-        *q->m_scale = m_scale_new;
-        if (scaled_v) *q->v_bound = b_new;
-
-        /* O3: FP8 weight copy encoded from the FP16 master. */
-        if (q->w8) {
-            float amax_w = or_amax_value(&aw);
-            float w8_scale = oracle_scale_from_amax(amax_w, OR_E4M3);
-            for (int64_t i = 0; i < q->numel; ++i)
-                q->w8[i] = oracle_fp8_encode(oracle_f16_to_f32(q->w[i]) * w8_scale,
-                                             OR_E4M3);
-            *q->w8_scale = w8_scale;
-            *q->w8_amax = amax_w;
-        }
+        float aw = or_tensor_update(&p[t], l2, beta1, beta2, eps, wd, &s,
+                                    or_step_factor(&p[t], inv_loss_scale, clip),
+                                    amax_m[t], gmax[t]);
+        if (master_amax != NULL) master_amax[t] = aw;
     }
     return 0;
+}
+
+/* Phase 3: the O3 weight copy of each O3 record from the given master amax.
+ * Returns 0, or -1 on a bad argument. */
+int oracle_weight_copy(const oracle_param *p, int n, const float *master_amax)
+{
+    if (n < 0) return -1;
+    for (int t = 0; t < n; ++t)
+        if (p[t].w8) or_tensor_copy(&p[t], master_amax[t]);
+    return 0;
+}
+
+static int or_adam_step(const oracle_param *p, int n, int l2, float lr,
+                        float beta1, float beta2, float eps, float wd,
+                        int64_t step, float inv_loss_scale, float clip)
+{
+    if (or_bad_step(n, step)) return -1;
+    size_t bytes = (size_t)(n > 0 ? n : 1) * sizeof(float);
+    float *am = malloc(bytes), *gm = malloc(bytes), *wm = malloc(bytes);
+    int rc = -1;
+    if (am != NULL && gm != NULL && wm != NULL) {
+        rc = oracle_step_maxima(p, n, l2, lr, beta1, beta2, wd, step,
+                                inv_loss_scale, clip, am, gm);
+        if (rc == 0)
+            rc = oracle_step_update(p, n, l2, lr, beta1, beta2, eps, wd, step,
+                                    inv_loss_scale, clip, am, gm, wm);
+        if (rc == 0) rc = oracle_weight_copy(p, n, wm);
+    }
+    free(am);
+    free(gm);
+    free(wm);
+    return rc;
 }
 
 /* AdamW: oracle_adam_step with decoupled weight decay. */
@@ -466,28 +577,77 @@ int oracle_adamw_step(const oracle_param *p, int n, float lr, float beta1,
  * every product and sum rounded to fp32 on its own; then y is cast to out_fmt
  * exactly as oracle_cast_scaled casts an fp32 tensor.  Returns 0, or -1 on a
  * bad argument. */
-int oracle_reduce_scaled(const uint8_t *src, int64_t numel, int64_t stride,
-                         const float *scales, int k, int in_fmt, int out_fmt,
-                         float post, uint8_t *codes, float *amax_out,
-                         float *scale_out)
+static int or_reduce_values(const uint8_t *src, int64_t numel, int64_t stride,
+                            const float *scales, int k, int in_fmt, int out_fmt,
+                            float post, float *y)
 {
     if (numel < 0 || k < 1 || k > 64 || stride < numel || in_fmt < 0 ||
         in_fmt > 1 || out_fmt < 0 || out_fmt > 1)
         return -1;
     float r[64];
     for (int j = 0; j < k; ++j) r[j] = 1.0f / scales[j];
-    float *y = malloc((size_t)(numel > 0 ? numel : 1) * sizeof(float));
-    if (y == NULL) return -1;
     for (int64_t i = 0; i < numel; ++i) {
         float acc = oracle_fp8_decode(src[i], in_fmt) * r[0];
         for (int j = 1; j < k; ++j)
             acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) * r[j];
         y[i] = acc * post;
     }
-    int rc = oracle_cast_scaled(y, OR_F32, numel, out_fmt, codes, amax_out,
+    return 0;
+}
+
+int oracle_reduce_scaled(const uint8_t *src, int64_t numel, int64_t stride,
+                         const float *scales, int k, int in_fmt, int out_fmt,
+                         float post, uint8_t *codes, float *amax_out,
+                         float *scale_out)
+{
+    float *y = malloc((size_t)(numel > 0 ? numel : 1) * sizeof(float));
+    if (y == NULL) return -1;
+    int rc = or_reduce_values(src, numel, stride, scales, k, in_fmt, out_fmt,
+                              post, y);
+    if (rc == 0)
+        rc = oracle_cast_scaled(y, OR_F32, numel, out_fmt, codes, amax_out,
                                 scale_out);
     free(y);
     return rc;
+}
+
+/* The reduction above with its output scale taken from a given amax instead
+ * of the codes' own: scale = fp8_max(out_fmt) / amax with the cast's
+ * guards.  A tensor reduced in pieces (element ranges of every shard) gives
+ * the whole tensor's codes when each piece takes the whole tensor's amax,
+ * the largest of the pieces' own.  Returns 0, or -1 on a bad argument. */
+int oracle_reduce_scaled_given(const uint8_t *src, int64_t numel, int64_t stride,
+                               const float *scales, int k, int in_fmt,
+                               int out_fmt, float post, float amax,
+                               uint8_t *codes, float *scale_out)
+{
+    float *y = malloc((size_t)(numel > 0 ? numel : 1) * sizeof(float));
+    if (y == NULL) return -1;
+    int rc = or_reduce_values(src, numel, stride, scales, k, in_fmt, out_fmt,
+                              post, y);
+    if (rc == 0) {
+        *scale_out = oracle_scale_from_amax(amax, out_fmt);
+        or_cast_encode(y, OR_F32, numel, out_fmt, *scale_out, codes);
+    }
+    free(y);
+    return rc;
+}
+
+/* Exact sum of the squared values of n FP8 codes, in units of 2^-32, as a
+ * 128-bit integer: out[0] the low and out[1] the high 64 bits.  Every code
+ * value is a multiple of 2^-16, so each square is an integer count of
+ * 2^-32.  Non-finite codes count 0 (they set found_inf instead). */
+void oracle_fp8_sq_sum(const uint8_t *codes, int64_t n, int fmt, uint64_t *out)
+{
+    unsigned __int128 acc = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        float x = oracle_fp8_decode(codes[i], fmt);
+        if (!isfinite(x)) continue;
+        uint64_t r = (uint64_t)ldexp(fabs((double)x), 16);   /* exact */
+        acc += (unsigned __int128)r * r;
+    }
+    out[0] = (uint64_t)acc;
+    out[1] = (uint64_t)(acc >> 64);
 }
 
 /* ------------------------------------------------ gradient norm, clipping */

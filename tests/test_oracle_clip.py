@@ -247,3 +247,28 @@ def test_per_tensor_terms(orc):
     assert orc.grad_norm(states, 0.5) == (0, math.sqrt(total))
     states[1].g[3] = 0x7F
     assert orc.grad_norm_terms(states, 0.5)[0] == 1
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_exact_square_sum(orc, fmt):
+    """oracle_fp8_sq_sum against the sum of the decoded values' squares in
+    Python integers (each decoded value is a multiple of 2^-16), with the
+    non-finite codes left out; over pieces the sums add up to the whole's,
+    and k^2 * S * 2^-32, rounded once, is the oracle's norm term."""
+    rng = np.random.default_rng(44)
+    codes = rng.integers(0, 256, 20000).astype(np.uint8)
+    vals = orc.fp8_decode(codes, fmt)
+    expect = sum(int(abs(float(x)) * 65536) ** 2 for x in vals if np.isfinite(x))
+    s = orc.fp8_sq_sum(codes, fmt)
+    assert s == expect
+    cuts = [0, 5, 9999, 20000]
+    assert sum(orc.fp8_sq_sum(codes[a:b], fmt) for a, b in zip(cuts, cuts[1:])) == s
+    fin = codes.copy()
+    fin[~np.isfinite(vals)] = 0
+    st = orc.StepState(fin, 0.25, np.zeros(fin.size, np.uint8), 1.0,
+                       np.zeros(fin.size, np.uint16), np.zeros(fin.size, np.uint16),
+                       g_fmt=fmt)
+    found, terms = orc.grad_norm_terms([st], 0.5)
+    assert found == 0
+    k = float(np.float32(np.float32(0.5) / np.float32(0.25)))
+    assert terms[0] == (k * k) * (float(s) * 2.0 ** -32)

@@ -139,8 +139,8 @@ MUTANTS = [
     ("scaled_v_gmax_before_l2", "if (scaled_v) or_amax_add(&ag, g);",
      "if (scaled_v) or_amax_add(&ag, or_grad(q, k, i));", "step"),
     ("m_scale_from_e5m2_max",
-     "float m_scale_new = oracle_scale_from_amax(or_amax_value(&am), OR_E4M3);",
-     "float m_scale_new = oracle_scale_from_amax(or_amax_value(&am), OR_E5M2);", "step"),
+     "float m_scale_new = oracle_scale_from_amax(amax_m, OR_E4M3);",
+     "float m_scale_new = oracle_scale_from_amax(amax_m, OR_E5M2);", "step"),
     ("w8_scale_from_e5m2_max", "float w8_scale = oracle_scale_from_amax(amax_w, OR_E4M3);",
      "float w8_scale = oracle_scale_from_amax(amax_w, OR_E5M2);", "step"),
     ("v_target_2_15", "#define OR_V_TARGET 16384.0f", "#define OR_V_TARGET 32768.0f",
@@ -153,8 +153,8 @@ MUTANTS = [
      "b = b * b;\n        if (t & 1) r = r * b;", "step"),
     ("eps_scaled_by_correction", "float denom = fmaf(sqrtf(v), s.inv_sbc2, eps);",
      "float denom = (sqrtf(v) + eps) * s.inv_sbc2;", "step"),
-    ("step_zero_allowed", "if (n < 0 || step < 1) return -1;\n    or_scalars",
-     "if (n < 0 || step < 0) return -1;\n    or_scalars", "step"),
+    ("step_zero_allowed", "return n < 0 || step < 1;", "return n < 0 || step < 0;",
+     "step"),
     ("first_bias_step_off_by_one",
      "double bc1 = 1.0 - oracle_bias_power((double)beta1, step);",
      "double bc1 = 1.0 - oracle_bias_power((double)beta1, step + 1);", "step"),
@@ -170,12 +170,19 @@ MUTANTS = [
      "q->v[i] = (uint16_t)(oracle_f32_to_f16(scaled_v ? v * v_scale_new : v) & 0xFFFEu);",
      "step"),
     ("m_scale_stale",
-     "float m_scale_new = oracle_scale_from_amax(or_amax_value(&am), OR_E4M3);",
-     "float m_scale_new = *q->m_scale; (void)am;", "step"),
+     "float m_scale_new = oracle_scale_from_amax(amax_m, OR_E4M3);",
+     "float m_scale_new = *q->m_scale; (void)amax_m;", "step"),
     ("v_scale_unguarded", "float q = OR_V_TARGET / b;\n    return isfinite(q) ? q : 1.0f;",
      "float q = OR_V_TARGET / b;\n    return q;", "step"),
     ("fp32_state_bytes_6", "case 0: case 1: return (int)(sizeof(float) + sizeof(float));",
      "case 0: case 1: return (int)(sizeof(float) + sizeof(uint16_t));", "step"),
+    # the step by phases: pieces of a tensor with the tensor's maxima
+    ("copy_uses_first_record_amax",
+     "if (p[t].w8) or_tensor_copy(&p[t], master_amax[t]);",
+     "if (p[t].w8) or_tensor_copy(&p[t], master_amax[0]);", "step"),
+    ("update_master_amax_not_reported",
+     "if (master_amax != NULL) master_amax[t] = aw;",
+     "if (master_amax != NULL) master_amax[t] = 0.0f * aw;", "step"),
     # local reduction of FP8 shards (MS-AMP O1, FP8 all-reduce)
     ("reduce_divides", "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) * r[j];",
      "acc = acc + oracle_fp8_decode(src[(int64_t)j * stride + i], in_fmt) / scales[j];",
@@ -189,8 +196,8 @@ MUTANTS = [
     ("reduce_drops_last_shard", "for (int j = 1; j < k; ++j)\n            acc",
      "for (int j = 1; j < k - 1; ++j)\n            acc", "reduce"),
     ("reduce_encodes_in_input_format",
-     "int rc = oracle_cast_scaled(y, OR_F32, numel, out_fmt,",
-     "int rc = oracle_cast_scaled(y, OR_F32, numel, in_fmt,", "reduce"),
+     "rc = oracle_cast_scaled(y, OR_F32, numel, out_fmt,",
+     "rc = oracle_cast_scaled(y, OR_F32, numel, in_fmt,", "reduce"),
     ("reduce_post_squared", "y[i] = acc * post;", "y[i] = acc * post * post;", "reduce"),
     ("reduce_first_shard_skipped",
      "float acc = oracle_fp8_decode(src[i], in_fmt) * r[0];", "float acc = 0.0f * r[0];",
@@ -204,7 +211,13 @@ MUTANTS = [
     ("cast_accepts_bad_dtype",
      "if (numel < 0 || fmt < 0 || fmt > 1 || dtype < 0 || dtype > 2) return -1;",
      "if (numel < 0 || fmt < 0 || fmt > 1 || dtype < 0) return -1;", "reduce"),
+    ("reduce_given_amax_ignored", "*scale_out = oracle_scale_from_amax(amax, out_fmt);",
+     "*scale_out = oracle_scale_from_amax(448.0f, out_fmt); (void)amax;", "reduce"),
     # global gradient norm and clipping (torch clip_grad_norm_)
+    ("sq_sum_not_squared", "acc += (unsigned __int128)r * r;",
+     "acc += (unsigned __int128)r * 65536u;", "clip"),
+    ("sq_sum_unit_halved", "uint64_t r = (uint64_t)ldexp(fabs((double)x), 16);",
+     "uint64_t r = (uint64_t)ldexp(fabs((double)x), 15);", "clip"),
     ("norm_sum_not_squared", "sum += (unsigned __int128)q * q;",
      "sum += (unsigned __int128)q * 65536u;", "clip"),
     ("norm_k_not_squared", "double kk = (double)k * (double)k;", "double kk = (double)k;",

@@ -190,3 +190,28 @@ def test_bad_arguments_are_refused(orc):
     assert cast(64, 0) == 0 and cast(64, 2) == 0
     assert cast(64, 3) == -1 and cast(64, -1) == -1
     assert cast(64, 0, fmt=2) == -1 and cast(-1, 0) == -1
+
+
+def test_pieces_with_the_whole_amax_give_the_whole_reduction(orc):
+    """The reduction's only per-tensor quantity is the amax of the reduced
+    values: pieces (column ranges of every shard) reduced with the largest
+    of the pieces' own amax give the whole tensor's codes and scale."""
+    rng = np.random.default_rng(43)
+    k, n = 4, 5000
+    shards = rng.integers(0, 256, (k, n)).astype(np.uint8)
+    shards[(shards & 0x7F) == 0x7F] = 0x11            # finite codes only
+    scales = (2.0 ** rng.integers(-6, 7, k)).astype(np.float32)
+    for out_fmt in (orc.E4M3, orc.E5M2):
+        whole, amax, scale = orc.reduce_scaled(shards, scales, orc.E4M3, out_fmt,
+                                               1.0 / k)
+        cuts = [0, 1, 700, 701, 4096, n]
+        own = [orc.reduce_scaled(np.ascontiguousarray(shards[:, a:b]), scales,
+                                 orc.E4M3, out_fmt, 1.0 / k)[1]
+               for a, b in zip(cuts, cuts[1:])]
+        big = np.float32(max(own))
+        assert big == amax
+        for a, b in zip(cuts, cuts[1:]):
+            c, sc = orc.reduce_scaled_given(np.ascontiguousarray(shards[:, a:b]),
+                                            scales, orc.E4M3, out_fmt, 1.0 / k, big)
+            assert sc == scale
+            assert np.array_equal(c, whole[a:b])

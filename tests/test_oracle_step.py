@@ -440,3 +440,85 @@ def test_bias_power_is_beta_to_the_t(orc):
             got = Fraction(orc.bias_power(b, t))
             assert abs(got - exact) <= exact * Fraction(t, 2 ** 52)
     assert orc.bias_power(0.9, 0) == 1.0
+
+
+# ------------------------------------------------ the step of a tensor's pieces
+
+def piece_of(orc, st, a, b):
+    """Elements [a, b) of a state as a state of its own with the tensor's
+    scales and bound (copies)."""
+    p = orc.StepState(st.g[a:b], st.g_scale, st.m[a:b], st.m_scale[0], st.v[a:b],
+                      st.w[a:b], g_fmt=st.g_fmt, o3=st.w8 is not None,
+                      scaled_v=st.v_bound is not None,
+                      v_bound=st.v_bound[0] if st.v_bound is not None else 0.0)
+    return p
+
+
+def max_bits(values):
+    """The largest of float32 maxima in the amax order (NaN above +inf above
+    every finite value): as bit patterns of non-negative floats."""
+    b = np.asarray(values, np.float32).view(np.int32)
+    return np.int32(b.max()).view(np.float32)
+
+
+@pytest.mark.parametrize("o3,scaled_v,l2,clip", [
+    (False, False, False, 1.0), (True, False, False, 0.37),
+    (False, True, True, 1.0), (True, True, False, 0.5)])
+def test_pieces_with_the_whole_maxima_give_the_whole_step(orc, o3, scaled_v, l2,
+                                                          clip):
+    """A step's per-tensor quantities are maxima over the tensor's elements
+    (this step's first-moment amax, max |g| for the bound, the new master's
+    amax); everything else is elementwise.  So cutting every tensor into
+    pieces, taking phase 1 on the pieces, combining each tensor's maxima by
+    max, and running phases 2 and 3 on the pieces with the combined maxima
+    must reproduce the whole step on every element and every scale."""
+    rng = np.random.default_rng(41)
+    sizes = [1, 700, 4099, 300]
+    whole = make_states(orc, sizes, rng, o3=o3)
+    if scaled_v:
+        for st in whole:
+            st.v_bound = np.array([1e-6], np.float32)
+            st.v = (np.abs(rng.standard_normal(st.numel)) * 1000).astype(
+                np.float16).view(np.uint16)
+    hp = (1e-3, 0.9, 0.999, 1e-8, 0.01, 3, 0.5)
+    pieces, owner = [], []
+    for t, st in enumerate(whole):
+        cuts = sorted(set([0, st.numel] + list(rng.integers(0, st.numel + 1, 3))))
+        for a, b in zip(cuts, cuts[1:]):
+            pieces.append((t, a, b, piece_of(orc, st, a, b)))
+    ref = [s.copy() for s in whole]
+    assert orc.adam_step_coef(ref, *hp, clip, l2=l2) == 0
+    lr, b1, b2, eps, wd, step, ils = hp
+    ps = [p for _, _, _, p in pieces]
+    f, am, gm = orc.step_maxima(ps, lr, b1, b2, wd, step, ils, clip=clip, l2=l2)
+    assert f == 0
+    tam = [max_bits([am[i] for i, (t2, *_) in enumerate(pieces) if t2 == t])
+           for t in range(len(whole))]
+    tgm = [max_bits([gm[i] for i, (t2, *_) in enumerate(pieces) if t2 == t])
+           for t in range(len(whole))]
+    wm = orc.step_update(ps, lr, b1, b2, eps, wd, step, ils,
+                         [tam[t] for t, *_ in pieces], [tgm[t] for t, *_ in pieces],
+                         clip=clip, l2=l2)
+    twm = [max_bits([wm[i] for i, (t2, *_) in enumerate(pieces) if t2 == t])
+           for t in range(len(whole))]
+    orc.weight_copy(ps, [twm[t] for t, *_ in pieces])
+    for t, a, b, p in pieces:
+        r = ref[t]
+        assert np.array_equal(p.m, r.m[a:b]) and np.array_equal(p.v, r.v[a:b])
+        assert np.array_equal(p.w, r.w[a:b])
+        assert p.m_scale[0] == r.m_scale[0]
+        if o3:
+            assert np.array_equal(p.w8, r.w8[a:b])
+            assert p.w8_scale[0] == r.w8_scale[0] and p.w8_amax[0] == r.w8_amax[0]
+        if scaled_v:
+            assert p.v_bound[0] == r.v_bound[0]
+
+
+def test_phase_one_reports_found_inf_and_writes_nothing(orc):
+    rng = np.random.default_rng(42)
+    states = make_states(orc, [50, 60], rng)
+    states[1].g[7] = 0x7F
+    before = [s.copy() for s in states]
+    assert orc.step_maxima(states, 1e-3, 0.9, 0.999, 0.01, 1, 1.0)[0] == 1
+    for a, b in zip(states, before):
+        assert np.array_equal(a.m, b.m) and a.m_scale[0] == b.m_scale[0]
