@@ -25,6 +25,8 @@ EXPORTS = ("fp8_cast_scaled", "fp8_adamw_step", "fp8_adam_step",
            "fp8_cast_adam_step_clipped", "fp8_reduce_scaled_norm",
            "fp8_cast_scaled_noalloc", "fp8_adam_step_dev",
            "fp8_cast_adamw_step_dev", "fp8_cast_adam_step_clipped_dev",
+           "fp8_adam_step_copy", "fp8_reduce_scaled_begin",
+           "fp8_reduce_scaled_finish", "fp8_norm_terms_from_limbs",
            "fp8opt_strerror",
            "fp8opt_last_error", "fp8opt_timing_enable", "fp8opt_timing_read",
            "fp8opt_release", "fp8opt_release_stream")
@@ -118,10 +120,26 @@ def load(path: str = LIB_PATH) -> C.CDLL:
                  C.c_float, C.c_float, C.c_int64, C.c_float, C.c_int]
     L.fp8_adam_step_begin.restype = C.c_int
     L.fp8_adam_step_begin.argtypes = step_head + [C.c_void_p, C.c_void_p,
-                                                  C.c_void_p]
+                                                  C.c_void_p, C.c_void_p]
     L.fp8_adam_step_finish.restype = C.c_int
     L.fp8_adam_step_finish.argtypes = step_head + [C.c_void_p, C.c_void_p,
+                                                   C.c_void_p, C.c_void_p,
                                                    C.c_void_p, C.c_void_p]
+    L.fp8_adam_step_copy.restype = C.c_int
+    L.fp8_adam_step_copy.argtypes = [C.POINTER(Param), C.c_int, C.c_void_p,
+                                     C.c_void_p]
+    L.fp8_reduce_scaled_begin.restype = C.c_int
+    L.fp8_reduce_scaled_begin.argtypes = [C.POINTER(ReduceItem), C.c_int, C.c_int,
+                                          C.c_int, C.c_float, C.c_void_p,
+                                          C.c_void_p]
+    L.fp8_reduce_scaled_finish.restype = C.c_int
+    L.fp8_reduce_scaled_finish.argtypes = [
+        C.POINTER(ReduceItem), C.c_int, C.c_int, C.c_int, C.c_int, C.c_float,
+        C.c_void_p, C.c_float, C.c_void_p, C.c_void_p, C.c_void_p]
+    L.fp8_norm_terms_from_limbs.restype = C.c_int
+    L.fp8_norm_terms_from_limbs.argtypes = [C.c_void_p, C.c_void_p, C.c_int,
+                                            C.c_int, C.c_float, C.c_void_p,
+                                            C.c_void_p]
     L.fp8_cast_adam_step_clipped.restype = C.c_int
     L.fp8_cast_adam_step_clipped.argtypes = [
         C.POINTER(CastItem), C.POINTER(Param), C.c_int, C.c_int, C.c_float,

@@ -221,6 +221,30 @@ class ReducePlan:
             inv_loss_scale, _ptr_or_none(norm_terms, "norm_terms", torch.float64),
             _ptr_or_none(found, "found", torch.int32), _stream_ptr(stream)))
 
+    # The reduction split at its amax, for tensors reduced in pieces on
+    # several ranks (fp8_reduce_scaled_begin / _finish).  amax_bits: int32
+    # CUDA, one per item (fp32 bits); limbs: int64 CUDA, four per item;
+    # found: int32 CUDA scalar.  Neither waits for the stream.
+
+    def begin(self, amax_bits: torch.Tensor, stream=None) -> None:
+        if amax_bits.numel() < self.n:
+            raise ValueError("amax_bits needs one int32 per item")
+        check(load().fp8_reduce_scaled_begin(
+            self._items, self.n, self.k, self.in_fmt, self.post,
+            _ptr_or_none(amax_bits, "amax_bits", torch.int32), _stream_ptr(stream)))
+
+    def finish(self, amax_bits: torch.Tensor, inv_loss_scale: float = 1.0,
+               limbs: Optional[torch.Tensor] = None,
+               found: Optional[torch.Tensor] = None, stream=None) -> None:
+        if amax_bits.numel() < self.n or (limbs is not None and
+                                          limbs.numel() < 4 * self.n):
+            raise ValueError("amax_bits needs one int32 and limbs four int64 per item")
+        check(load().fp8_reduce_scaled_finish(
+            self._items, self.n, self.k, self.in_fmt, self.out_fmt, self.post,
+            _ptr_or_none(amax_bits, "amax_bits", torch.int32), inv_loss_scale,
+            _ptr_or_none(limbs, "limbs", torch.int64),
+            _ptr_or_none(found, "found", torch.int32), _stream_ptr(stream)))
+
 
 def fp8_reduce_scaled(shards: Sequence[torch.Tensor], scales, in_fmt="e4m3",
                       out_fmt="e4m3", post=1.0, codes=None, amax=None,
@@ -398,21 +422,44 @@ class AdamWPlan:
             _ptr_or_none(terms, "terms", torch.float64),
             _ptr_or_none(found, "found", torch.int32), _stream_ptr(stream)))
 
-    def begin(self, hp, clip=None, found=None, stream=None) -> None:
+    # maxima: int32 CUDA, 2n (begin: out, finish: in; the fp32 bits of each
+    # record's first-moment amax, then of its max |g|); master_amax: int32
+    # CUDA, n (finish: out, then copy: in), for records that are pieces of
+    # tensors cut across ranks.
+
+    def begin(self, hp, clip=None, found=None, stream=None,
+              maxima: Optional[torch.Tensor] = None) -> None:
         lr, b1, b2, eps, wd, step, ils, l2 = hp
+        if maxima is not None and maxima.numel() < 2 * self.n:
+            raise ValueError("maxima needs two int32 per record")
         check(load().fp8_adam_step_begin(
             self._params, self.n, lr, b1, b2, eps, wd, int(step), ils, int(l2),
             _ptr_or_none(clip, "clip", torch.float32),
-            _ptr_or_none(found, "found", torch.int32), _stream_ptr(stream)))
+            _ptr_or_none(found, "found", torch.int32),
+            _ptr_or_none(maxima, "maxima", torch.int32), _stream_ptr(stream)))
 
     def finish(self, hp, clip=None, found_in=None, found=None,
-               stream=None) -> None:
+               stream=None, maxima: Optional[torch.Tensor] = None,
+               master_amax: Optional[torch.Tensor] = None) -> None:
         lr, b1, b2, eps, wd, step, ils, l2 = hp
+        if (maxima is not None and maxima.numel() < 2 * self.n) or (
+                master_amax is not None and master_amax.numel() < self.n):
+            raise ValueError("maxima needs two and master_amax one int32 per record")
         check(load().fp8_adam_step_finish(
             self._params, self.n, lr, b1, b2, eps, wd, int(step), ils, int(l2),
             _ptr_or_none(clip, "clip", torch.float32),
             _ptr_or_none(found_in, "found_in", torch.int32),
-            _ptr_or_none(found, "found", torch.int32), _stream_ptr(stream)))
+            _ptr_or_none(found, "found", torch.int32),
+            _ptr_or_none(maxima, "maxima", torch.int32),
+            _ptr_or_none(master_amax, "master_amax", torch.int32),
+            _stream_ptr(stream)))
+
+    def copy(self, master_amax: torch.Tensor, stream=None) -> None:
+        if master_amax.numel() < self.n:
+            raise ValueError("master_amax needs one int32 per record")
+        check(load().fp8_adam_step_copy(
+            self._params, self.n, _ptr_or_none(master_amax, "master_amax", torch.int32),
+            _stream_ptr(stream)))
 
 
 def fp8_adamw_step(g, g_scale, m, m_scale, v, w, lr, beta1, beta2, eps, wd,
@@ -687,6 +734,23 @@ class Fp8AdamW:
     def state_bytes_per_param(level="O2") -> int:
         """Optimizer-state bytes per parameter: 1 (E4M3 m) + 2 (FP16 v)."""
         return 1 + 2
+
+
+def norm_terms_from_limbs(limbs: torch.Tensor, amax_bits: torch.Tensor, fmt,
+                          inv_loss_scale: float, terms: torch.Tensor,
+                          stream=None) -> None:
+    """fp8_norm_terms_from_limbs: the norm term of every tensor (float64 CUDA,
+    one per tensor) from its exact sum of squares as limbs (int64 CUDA, four
+    per tensor, possibly summed over ranks) and its reduced codes' amax
+    (int32 CUDA, fp32 bits, one per tensor)."""
+    n = terms.numel()
+    if limbs.numel() < 4 * n or amax_bits.numel() < n:
+        raise ValueError("limbs needs four int64 and amax_bits one int32 per term")
+    check(load().fp8_norm_terms_from_limbs(
+        _ptr_or_none(limbs, "limbs", torch.int64),
+        _ptr_or_none(amax_bits, "amax_bits", torch.int32), n, _fmt(fmt),
+        inv_loss_scale, _ptr_or_none(terms, "terms", torch.float64),
+        _stream_ptr(stream)))
 
 
 def clip_coef(terms: torch.Tensor, max_grad_norm: float, clip: torch.Tensor,

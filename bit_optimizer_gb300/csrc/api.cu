@@ -11,6 +11,8 @@
 #include <utility>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/fp8opt.h"
 #include "fp8opt_internal.cuh"
 
@@ -63,7 +65,18 @@ cudaError_t launch_reduce(const ReduceDesc* descs, const Chunk* chunks,
                           uint32_t epoch, int k, int in_fmt, int out_fmt,
                           float post, int grid_amax, int grid_encode,
                           const ReduceNorm* norm, cudaStream_t stream,
-                          LaunchMark mark);
+                          LaunchMark mark, int phase);
+cudaError_t launch_slots_export(const unsigned long long* slots, uint32_t epoch,
+                                int n, uint32_t* out, cudaStream_t stream);
+cudaError_t launch_slots_import(unsigned long long* slots, uint32_t epoch, int n,
+                                const uint32_t* in, cudaStream_t stream);
+cudaError_t launch_limbs_terms(const long long* limbs, const uint32_t* amax_bits,
+                               int n, int fmt, float ils, double* terms,
+                               cudaStream_t stream);
+cudaError_t launch_step_w8(const StepDesc* descs, const Chunk* chunks_o3,
+                           uint32_t nchunks_o3, const StepScratch& sc,
+                           uint32_t epoch, int grid_w8, cudaStream_t stream,
+                           LaunchMark mark);
 cudaError_t reduce_occupancy(int* amax_per_sm, int* amax_small_per_sm,
                              int* encode_per_sm, int* encode_small_per_sm);
 cudaError_t reduce_encode_sq_occupancy(int* per_sm);
@@ -173,6 +186,7 @@ struct Workspace {
   uint32_t step_nchunks = 0, step_nchunks_o3 = 0;
   bool step_any_vs = false;   // some record has a scaled second moment
   uint32_t begin_epoch = 0;   // epoch of an fp8_adam_step_begin awaiting its finish
+  uint32_t copy_epoch = 0;    // epoch of a finish awaiting its fp8_adam_step_copy
   // reduction tables
   std::vector<fp8opt_reduce_item> reduce_key;
   DevBuf reduce_descs, reduce_chunks;
@@ -340,7 +354,24 @@ void timing_mark(int kernel, int end, cudaStream_t stream) {
   }
 }
 
-LaunchMark launch_mark() { return g_timing.on ? timing_mark : nullptr; }
+// Every launch sits in an NVTX range named for its pass, so a profiler's
+// timeline (Nsight Systems, Nsight Compute's range filters) shows the passes
+// by name; without an attached tool a range costs one indirect call.  While
+// per-kernel timing is on, the range also holds the two events.
+void nvtx_mark(int kernel, int end, cudaStream_t) {
+  if (!end)
+    nvtxRangePushA(kKernelNames[kernel]);
+  else
+    nvtxRangePop();
+}
+
+void nvtx_timing_mark(int kernel, int end, cudaStream_t stream) {
+  if (!end) nvtx_mark(kernel, end, stream);
+  timing_mark(kernel, end, stream);
+  if (end) nvtx_mark(kernel, end, stream);
+}
+
+LaunchMark launch_mark() { return g_timing.on ? nvtx_timing_mark : nvtx_mark; }
 
 // Folds finished event pairs into the totals.
 cudaError_t timing_collect() {
@@ -844,18 +875,32 @@ extern "C" int fp8_cast_scaled(const fp8opt_cast_item* items, int n, int fmt,
 namespace fp8opt {
 namespace {
 
-// The reduction entry points; terms_dev set: also the norm terms of the
-// outputs (with found_dev, may be NULL).
+// What a reduction call runs: its passes (phase), the amax pass's per-item
+// values exported (amax_out) or the encode pass's imported (amax_in), and
+// the norm of the outputs (with_norm) as terms or as exact limbs, with
+// found_inf (found, may be NULL).
+struct ReduceReq {
+  int phase = kReduceBothPasses;
+  uint32_t* amax_out = nullptr;
+  const uint32_t* amax_in = nullptr;
+  bool with_norm = false;
+  float ils = 1.0f;
+  double* terms = nullptr;
+  long long* limbs = nullptr;
+  uint32_t* found = nullptr;
+};
+
+// The reduction entry points.
 int reduce_call(const char* fn, const fp8opt_reduce_item* items, int n, int k,
-                int in_fmt, int out_fmt, float post, bool with_norm, float ils,
-                double* terms_dev, uint32_t* found_dev, void* stream_ptr) {
+                int in_fmt, int out_fmt, float post, const ReduceReq& rq,
+                void* stream_ptr) {
   int st = check_reduce_args(fn, items, n, k, in_fmt, out_fmt);
   if (st != FP8OPT_OK) return st;
-  if (with_norm && n > 0 && terms_dev == nullptr)
+  if (rq.with_norm && n > 0 && rq.terms == nullptr && rq.limbs == nullptr)
     return fail(FP8OPT_ERR_ARG, std::string(fn) + ": terms_dev is NULL");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   if (n == 0)
-    return with_norm ? empty_step(fn, nullptr, found_dev, stream) : FP8OPT_OK;
+    return rq.with_norm ? empty_step(fn, nullptr, rq.found, stream) : FP8OPT_OK;
 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0;
@@ -868,23 +913,29 @@ int reduce_call(const char* fn, const fp8opt_reduce_item* items, int n, int k,
   uint32_t epoch = 0;
   cudaError_t e = prepare_slots(ws, (size_t)n + 1, stream, &epoch);
   const size_t sum_bytes = 2 * (size_t)n * sizeof(unsigned long long);
-  if (e == cudaSuccess && with_norm) e = ws->norm_buf.reserve(sum_bytes);
-  if (e == cudaSuccess && with_norm)
+  if (e == cudaSuccess && rq.with_norm) e = ws->norm_buf.reserve(sum_bytes);
+  if (e == cudaSuccess && rq.with_norm)
     e = cudaMemsetAsync(ws->norm_buf.ptr, 0, sum_bytes, stream);
   if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": workspace").c_str());
   unsigned long long* slots = static_cast<unsigned long long*>(ws->slots.ptr);
+  if (rq.amax_in != nullptr)
+    e = launch_slots_import(slots, epoch, n, rq.amax_in, stream);
   ReduceNorm norm = {static_cast<unsigned long long*>(ws->norm_buf.ptr),
-                     slots + n, ils, n, terms_dev, found_dev};
+                     slots + n, rq.ils, n, rq.terms, rq.found, rq.limbs};
   // the k-specialised passes' grids: k <= 2, k = 4, k = 8
   const int ks = k <= 2 ? 0 : k == 4 ? 1 : k == 8 ? 2 : -1;
-  e = launch_reduce(static_cast<const ReduceDesc*>(ws->reduce_descs.ptr),
-                    static_cast<const Chunk*>(ws->reduce_chunks.ptr),
-                    ws->reduce_nchunks, slots, epoch, k, in_fmt, out_fmt, post,
-                    ks >= 0 ? info->reduce_amax_small[ks] : info->reduce_amax,
-                    with_norm ? info->reduce_encode_sq
-                    : ks >= 0 ? info->reduce_encode_small[ks]
-                              : info->reduce_encode,
-                    with_norm ? &norm : nullptr, stream, launch_mark());
+  if (e == cudaSuccess)
+    e = launch_reduce(static_cast<const ReduceDesc*>(ws->reduce_descs.ptr),
+                      static_cast<const Chunk*>(ws->reduce_chunks.ptr),
+                      ws->reduce_nchunks, slots, epoch, k, in_fmt, out_fmt, post,
+                      ks >= 0 ? info->reduce_amax_small[ks] : info->reduce_amax,
+                      rq.with_norm ? info->reduce_encode_sq
+                      : ks >= 0 ? info->reduce_encode_small[ks]
+                                : info->reduce_encode,
+                      rq.with_norm ? &norm : nullptr, stream, launch_mark(),
+                      rq.phase);
+  if (e == cudaSuccess && rq.amax_out != nullptr)
+    e = launch_slots_export(slots, epoch, n, rq.amax_out, stream);
   if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
   return FP8OPT_OK;
 }
@@ -896,15 +947,72 @@ extern "C" int fp8_reduce_scaled(const fp8opt_reduce_item* items, int n, int k,
                                  int in_fmt, int out_fmt, float post,
                                  void* stream_ptr) {
   return reduce_call("fp8_reduce_scaled", items, n, k, in_fmt, out_fmt, post,
-                     false, 1.0f, nullptr, nullptr, stream_ptr);
+                     ReduceReq(), stream_ptr);
 }
 
 extern "C" int fp8_reduce_scaled_norm(const fp8opt_reduce_item* items, int n,
                                       int k, int in_fmt, int out_fmt, float post,
                                       float inv_loss_scale, double* terms_dev,
                                       uint32_t* found_dev, void* stream_ptr) {
+  ReduceReq rq;
+  rq.with_norm = true;
+  rq.ils = inv_loss_scale;
+  rq.terms = terms_dev;
+  rq.found = found_dev;
   return reduce_call("fp8_reduce_scaled_norm", items, n, k, in_fmt, out_fmt, post,
-                     true, inv_loss_scale, terms_dev, found_dev, stream_ptr);
+                     rq, stream_ptr);
+}
+
+extern "C" int fp8_reduce_scaled_begin(const fp8opt_reduce_item* items, int n,
+                                       int k, int in_fmt, float post,
+                                       uint32_t* amax_bits_dev, void* stream_ptr) {
+  if (n > 0 && amax_bits_dev == nullptr)
+    return fail(FP8OPT_ERR_ARG, "fp8_reduce_scaled_begin: amax_bits_dev is NULL");
+  ReduceReq rq;
+  rq.phase = kReduceAmaxPass;
+  rq.amax_out = amax_bits_dev;
+  return reduce_call("fp8_reduce_scaled_begin", items, n, k, in_fmt, in_fmt, post,
+                     rq, stream_ptr);
+}
+
+extern "C" int fp8_reduce_scaled_finish(const fp8opt_reduce_item* items, int n,
+                                        int k, int in_fmt, int out_fmt,
+                                        float post, const uint32_t* amax_bits_dev,
+                                        float inv_loss_scale, int64_t* limbs_dev,
+                                        uint32_t* found_dev, void* stream_ptr) {
+  if (n > 0 && amax_bits_dev == nullptr)
+    return fail(FP8OPT_ERR_ARG, "fp8_reduce_scaled_finish: amax_bits_dev is NULL");
+  if (found_dev != nullptr && limbs_dev == nullptr)
+    return fail(FP8OPT_ERR_ARG,
+                "fp8_reduce_scaled_finish: found_dev is given without limbs_dev");
+  ReduceReq rq;
+  rq.phase = kReduceEncodePass;
+  rq.amax_in = amax_bits_dev;
+  if (limbs_dev != nullptr) {
+    rq.with_norm = true;
+    rq.ils = inv_loss_scale;
+    rq.limbs = reinterpret_cast<long long*>(limbs_dev);
+    rq.found = found_dev;
+  }
+  return reduce_call("fp8_reduce_scaled_finish", items, n, k, in_fmt, out_fmt,
+                     post, rq, stream_ptr);
+}
+
+extern "C" int fp8_norm_terms_from_limbs(const int64_t* limbs_dev,
+                                         const uint32_t* amax_bits_dev, int n,
+                                         int fmt, float inv_loss_scale,
+                                         double* terms_dev, void* stream_ptr) {
+  if (n < 0 || (n > 0 && (limbs_dev == nullptr || amax_bits_dev == nullptr ||
+                          terms_dev == nullptr)))
+    return fail(FP8OPT_ERR_ARG,
+                "fp8_norm_terms_from_limbs: n < 0 or a NULL device array");
+  if (fmt != FP8OPT_E4M3 && fmt != FP8OPT_E5M2)
+    return fail(FP8OPT_ERR_UNSUPPORTED, "fp8_norm_terms_from_limbs: unknown format");
+  cudaError_t e = launch_limbs_terms(reinterpret_cast<const long long*>(limbs_dev),
+                                     amax_bits_dev, n, fmt, inv_loss_scale,
+                                     terms_dev, static_cast<cudaStream_t>(stream_ptr));
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_norm_terms_from_limbs: launch");
+  return FP8OPT_OK;
 }
 
 namespace fp8opt {
@@ -1141,7 +1249,7 @@ extern "C" int fp8_adam_step_begin(const fp8opt_param* params, int n, float lr,
                                    float beta1, float beta2, float eps, float wd,
                                    int64_t step, float inv_loss_scale, int l2,
                                    const float* clip_dev, uint32_t* found_dev,
-                                   void* stream_ptr) {
+                                   uint32_t* maxima_out, void* stream_ptr) {
   const char* fn = "fp8_adam_step_begin";
   int st = check_phase_args(fn, l2);
   if (st == FP8OPT_OK) st = check_step_args(fn, params, n, step);
@@ -1160,8 +1268,13 @@ extern "C" int fp8_adam_step_begin(const fp8opt_param* params, int n, float lr,
                                    launch_mark());
   if (e == cudaSuccess && found_dev != nullptr)
     e = launch_found(c.sc.found, c.epoch, nullptr, found_dev, stream, launch_mark());
+  if (e == cudaSuccess && maxima_out != nullptr)
+    e = launch_slots_export(c.sc.amax_m, c.epoch, n, maxima_out, stream);
+  if (e == cudaSuccess && maxima_out != nullptr)
+    e = launch_slots_export(c.sc.amax_g, c.epoch, n, maxima_out + n, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fp8_adam_step_begin: launch");
   c.ws->begin_epoch = c.epoch;
+  c.ws->copy_epoch = 0;
   return FP8OPT_OK;
 }
 
@@ -1170,7 +1283,9 @@ extern "C" int fp8_adam_step_finish(const fp8opt_param* params, int n, float lr,
                                     float wd, int64_t step, float inv_loss_scale,
                                     int l2, const float* clip_dev,
                                     const uint32_t* found_in_dev,
-                                    uint32_t* found_dev, void* stream_ptr) {
+                                    uint32_t* found_dev,
+                                    const uint32_t* maxima_in,
+                                    uint32_t* master_amax_out, void* stream_ptr) {
   const char* fn = "fp8_adam_step_finish";
   int st = check_phase_args(fn, l2);
   if (st == FP8OPT_OK) st = check_step_args(fn, params, n, step);
@@ -1196,13 +1311,55 @@ extern "C" int fp8_adam_step_finish(const fp8opt_param* params, int n, float lr,
   ws->begin_epoch = 0;
   cudaError_t e = launch_found(c.sc.found, c.epoch, found_in_dev, nullptr, stream,
                                launch_mark());
+  // the whole tensors' maxima, combined over the ranks holding their pieces
+  if (e == cudaSuccess && maxima_in != nullptr)
+    e = launch_slots_import(c.sc.amax_m, c.epoch, n, maxima_in, stream);
+  if (e == cudaSuccess && maxima_in != nullptr)
+    e = launch_slots_import(c.sc.amax_g, c.epoch, n, maxima_in + n, stream);
+  // with master_amax_out the O3 weight copy waits for fp8_adam_step_copy
+  const bool copy_now = master_amax_out == nullptr;
   if (e == cudaSuccess)
     e = launch_step_update(c.descs, c.chunks, ws->step_nchunks,
-                           c.chunks + ws->step_nchunks, ws->step_nchunks_o3, c.sc,
-                           s, c.epoch, found_dev, info->step_update,
-                           info->step_update_var, info->step_w8,
-                           ws->step_any_vs, stream, launch_mark());
+                           c.chunks + ws->step_nchunks,
+                           copy_now ? ws->step_nchunks_o3 : 0, c.sc, s, c.epoch,
+                           found_dev, info->step_update, info->step_update_var,
+                           info->step_w8, ws->step_any_vs, stream, launch_mark());
+  if (e == cudaSuccess && !copy_now)
+    e = launch_slots_export(c.sc.amax_w, c.epoch, n, master_amax_out, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fp8_adam_step_finish: launch");
+  ws->copy_epoch = copy_now ? 0 : c.epoch;
+  return FP8OPT_OK;
+}
+
+extern "C" int fp8_adam_step_copy(const fp8opt_param* params, int n,
+                                  const uint32_t* master_amax_in,
+                                  void* stream_ptr) {
+  const char* fn = "fp8_adam_step_copy";
+  int st = check_step_args(fn, params, n, 1);
+  if (st != FP8OPT_OK) return st;
+  if (n > 0 && master_amax_in == nullptr)
+    return fail(FP8OPT_ERR_ARG, std::string(fn) + ": master_amax_in is NULL");
+  if (n == 0) return FP8OPT_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  DeviceInfo* info = nullptr;
+  if ((st = current_device_and_info(&dev, &info)) != FP8OPT_OK) return st;
+  Workspace* ws = workspace(dev, stream);
+  if (!ws->have_step || !same_list(ws->step_key, params, n) ||
+      ws->copy_epoch == 0 || ws->copy_epoch != ws->epoch)
+    return fail(FP8OPT_ERR_ARG, std::string(fn) +
+                                    ": no fp8_adam_step_finish of this list with "
+                                    "master_amax_out is pending on this stream");
+  StepCall c;
+  if ((st = setup_step(fn, params, n, stream_ptr, false, false, &c)) != FP8OPT_OK)
+    return st;
+  ws->copy_epoch = 0;
+  cudaError_t e = launch_slots_import(c.sc.amax_w, c.epoch, n, master_amax_in, stream);
+  if (e == cudaSuccess)
+    e = launch_step_w8(c.descs, c.chunks + ws->step_nchunks, ws->step_nchunks_o3,
+                       c.sc, c.epoch, info->step_w8, stream, launch_mark());
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_adam_step_copy: launch");
   return FP8OPT_OK;
 }
 

@@ -105,8 +105,9 @@ struct ReduceDesc {
 constexpr int kMaxShards = 64;
 
 // The gradient norm of a reduction's outputs: 2n zeroed words of exact sums,
-// the call's found_inf slot, the inverse loss scale, n terms out and the
-// found flag out (may be NULL).
+// the call's found_inf slot, the inverse loss scale, n terms out (or, when
+// limbs is set, the exact sums as 4n limbs instead) and the found flag out
+// (may be NULL).
 struct ReduceNorm {
   unsigned long long* sums;
   unsigned long long* found;
@@ -114,7 +115,12 @@ struct ReduceNorm {
   int n;
   double* terms;
   uint32_t* found_out;
+  long long* limbs;
 };
+
+// Passes of a reduction call: the amax pass, the encode pass, or both.
+enum ReducePhase { kReduceAmaxPass = 1, kReduceEncodePass = 2,
+                   kReduceBothPasses = 3 };
 
 // Kernels, for the optional per-launch event timing.
 enum KernelId { kCastAmaxK = 0, kCastEncodeK, kStepAmaxK, kStepUpdateK,
@@ -261,38 +267,6 @@ __device__ __forceinline__ uint2 enc8(const float (&x)[8]) {
   return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }
 
-// The GradScaler test of a chunk of gradient codes as one comparison per
-// code.  |decode(code) * k| depends only on the code's magnitude (code &
-// 0x7F), and rounds monotonically in it; the non-finite codes (E4M3 0x7F,
-// E5M2 0x7C and above) are the format's largest magnitudes.  The magnitudes
-// whose unscaled value is not finite are therefore one upper range [T, 0x7F],
-// and overflow_threshold finds T by bisection over [0, first non-finite
-// magnitude].  T is 0 when k is not finite (0 * inf is NaN).
-template <int FMT>
-__device__ __forceinline__ uint32_t overflow_threshold(float k) {
-  uint32_t lo = 0, hi = FMT == kE4M3 ? 0x7Fu : 0x7Cu;   // T lies in [lo, hi]
-  while (lo < hi) {
-    const uint32_t mid = (lo + hi) >> 1;
-    if ((__float_as_uint(__fmul_rn(dec2<FMT>(mid).x, k)) & 0x7FFFFFFFu) >= 0x7F800000u)
-      hi = mid;
-    else
-      lo = mid + 1;
-  }
-  return lo;
-}
-
-// The per-byte addend of codes_at_least for threshold T (0 <= T <= 0x80).
-__device__ __forceinline__ uint32_t threshold_addend(uint32_t t) {
-  return (0x80u - t) * 0x01010101u;
-}
-
-// Bit 7 of each byte of w (four codes) whose magnitude is at least T, given
-// add = threshold_addend(T): a magnitude m <= 0x7F plus 0x80 - T reaches 0x80
-// exactly when m >= T, and never carries into the next byte.
-__device__ __forceinline__ uint32_t codes_at_least(uint32_t w, uint32_t add) {
-  return ((w & 0x7F7F7F7Fu) + add) & 0x80808080u;
-}
-
 // Eight codes in a uint2 -> eight floats.
 template <int FMT>
 __device__ __forceinline__ void dec8(uint2 c, float (&x)[8]) {
@@ -384,6 +358,40 @@ __device__ __forceinline__ uint32_t nonfinite(float x) {
 
 __device__ __forceinline__ uint32_t abs_bits(float x) {
   return __float_as_uint(x) & 0x7FFFFFFFu;
+}
+
+// The GradScaler test of a chunk of gradient codes as one comparison per
+// code.  |decode(code) * k| depends only on the code's magnitude (code &
+// 0x7F), and rounds monotonically in it; the non-finite codes (E4M3 0x7F,
+// E5M2 0x7C and above) are the format's largest magnitudes and never give a
+// finite product.  The magnitudes whose unscaled value is not finite are
+// therefore one upper range [T, 0x7F] (T is 0 when k is not finite: 0 * inf
+// is NaN), and overflow_threshold returns T: lane l of the warp tests
+// magnitudes l, l + 32, l + 64 and l + 96, and the lowest failing one is T
+// (0x7F always fails).  Every lane of the warp must call it; all get T.
+template <int FMT>
+__device__ __forceinline__ uint32_t overflow_threshold(float k) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const float2 a = dec2<FMT>(lane | ((lane + 32u) << 8));
+  const float2 b = dec2<FMT>((lane + 64u) | ((lane + 96u) << 8));
+  const uint32_t m0 = __ballot_sync(0xFFFFFFFFu, nonfinite(__fmul_rn(a.x, k)));
+  const uint32_t m1 = __ballot_sync(0xFFFFFFFFu, nonfinite(__fmul_rn(a.y, k)));
+  const uint32_t m2 = __ballot_sync(0xFFFFFFFFu, nonfinite(__fmul_rn(b.x, k)));
+  const uint32_t m3 = __ballot_sync(0xFFFFFFFFu, nonfinite(__fmul_rn(b.y, k)));
+  return m0 ? __ffs(m0) - 1u : m1 ? 31u + __ffs(m1)
+       : m2 ? 63u + __ffs(m2) : 95u + __ffs(m3);
+}
+
+// The per-byte addend of codes_at_least for threshold T (0 <= T <= 0x80).
+__device__ __forceinline__ uint32_t threshold_addend(uint32_t t) {
+  return (0x80u - t) * 0x01010101u;
+}
+
+// Bit 7 of each byte of w (four codes) whose magnitude is at least T, given
+// add = threshold_addend(T): a magnitude m <= 0x7F plus 0x80 - T reaches 0x80
+// exactly when m >= T, and never carries into the next byte.
+__device__ __forceinline__ uint32_t codes_at_least(uint32_t w, uint32_t add) {
+  return ((w & 0x7F7F7F7Fu) + add) & 0x80808080u;
 }
 
 // Two FP16 (one 32-bit word) <-> float2.
@@ -606,6 +614,88 @@ __device__ __forceinline__ void sq_commit(const SqAcc<FMT>& a, uint32_t t,
     const bool bad = FMT == kE4M3 ? cmax == 0x7Fu : cmax >= 0x7Cu;
     if (bad || nonfinite(__fmul_rn(dec2<FMT>(cmax).x, k)))
       atomicMax(found, slot_tag(epoch, 1u));
+  }
+}
+
+// The same exact sums through a shared-memory table of the integers r (r =
+// |value| * 2^9 for E4M3, |value| * 2^16 for E5M2; 0 for the non-finite
+// codes, which set found_inf instead), so that a code costs one byte
+// permutation, one shared load and one multiply-add.  Entry [mag][fmt * 32 +
+// lane] holds r of magnitude `mag` in format `fmt` for lane `lane`: the
+// lanes of a warp always read 32 different banks, whatever their codes.
+// __byte_perm(magnitudes, sq_lane_byte(), 0x5504 + 16 * j) is the byte
+// offset of code j's entry: magnitude j in byte 1 (mag * 256), the format
+// and lane in byte 0 (fmt * 128 + lane * 4).
+struct SqTable {
+  uint32_t r[128][64];   // 32 KB
+};
+
+// Fills the table (every thread of the CTA calls it; it ends with a CTA
+// barrier).
+__device__ __forceinline__ void sq_table_fill(SqTable& t) {
+  for (int i = threadIdx.x; i < 128 * 64; i += blockDim.x) {
+    const uint32_t mag = (uint32_t)i >> 6, e5 = ((uint32_t)i >> 5) & 1u;
+    const float v = e5 ? dec2<kE5M2>(mag).x * 65536.0f : dec2<kE4M3>(mag).x * 512.0f;
+    t.r[mag][i & 63] = (__float_as_uint(v) & 0x7FFFFFFFu) >= 0x7F800000u
+                           ? 0u : __float2uint_rn(v);
+  }
+  __syncthreads();
+}
+
+// Byte 0 of an entry's offset: the format's column block and this lane's
+// word within it.
+template <int FMT>
+__device__ __forceinline__ uint32_t sq_lane_byte() {
+  return (FMT == kE4M3 ? 0u : 128u) + 4u * (threadIdx.x & 31u);
+}
+
+// A thread's exact sums through the table, for either format (a CTA may
+// accumulate several chunks of one tensor before it commits).  E4M3 squares
+// are below 2^36, so the 64-bit sum holds 2^28 codes a thread.
+struct SqTab {
+  unsigned long long s4 = 0;   // E4M3: units of 2^-18
+  U128 s5 = {0ull, 0ull};      // E5M2: units of 2^-32
+
+  // wm: four code magnitudes (sign bits cleared); lb: sq_lane_byte<FMT>().
+  template <int FMT>
+  __device__ __forceinline__ void add_word(uint32_t wm, uint32_t lb,
+                                           const SqTable& t) {
+    const char* base = reinterpret_cast<const char*>(&t);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t r = *reinterpret_cast<const uint32_t*>(
+          base + __byte_perm(wm, lb, 0x5504u + 16u * j));
+      if (FMT == kE4M3)
+        s4 += (unsigned long long)r * r;
+      else
+        s5 = add64(s5, (unsigned long long)r * r);
+    }
+  }
+  // the sum in units of 2^-32 (both formats' parts)
+  __device__ __forceinline__ U128 sum() const {
+    return add128(U128{s4 << 14, s4 >> 50}, s5);
+  }
+};
+
+// End of a run of chunks of tensor t for a table-summing pass: the CTA's
+// exact sum goes to the tensor's 128-bit slot (as in sq_commit), and
+// found_inf is set when any thread saw a non-finite value (`bad`, from the
+// codes and the tensor's overflow threshold).  Every thread calls it.
+__device__ __forceinline__ void sq_commit_flag(const SqTab& a, uint32_t t,
+                                               bool nonempty, uint32_t bad,
+                                               unsigned long long* sums,
+                                               unsigned long long* found,
+                                               uint32_t epoch,
+                                               unsigned long long* red64) {
+  const U128 s = block_sum128(a.sum(), red64);
+  const int any_bad = __syncthreads_or(bad != 0);
+  if (threadIdx.x == 0 && nonempty) {
+    if (s.lo | s.hi) {
+      const unsigned long long old = atomicAdd(&sums[2 * t], s.lo);
+      const unsigned long long carry = old + s.lo < old ? 1ull : 0ull;
+      if (s.hi + carry) atomicAdd(&sums[2 * t + 1], s.hi + carry);
+    }
+    if (any_bad) atomicMax(found, slot_tag(epoch, 1u));
   }
 }
 

@@ -3,9 +3,10 @@
 // script's --clip-grad).
 //
 // grad_norm_kernel: a persistent grid over the step's chunk table; each
-// chunk's exact sum of squared code values (SqAcc, fp8opt_internal.cuh) goes
+// chunk's exact sum of squared code values (read from a shared-memory table
+// of the integer square roots: SqTable and SqTab, fp8opt_internal.cuh) goes
 // to its tensor's 128-bit slot, and found_inf is decided exactly as the
-// step's first pass does (sq_commit).
+// step's first pass does (the chunk's overflow threshold).
 //
 // grad_norm_terms_kernel: one thread per record, term_t = fl64(k_t^2 *
 // fl64(S_t) * 2^-32) (k_t^2 is exact in double).
@@ -22,24 +23,37 @@ namespace fp8opt {
 namespace {
 
 // 8-code groups per thread per tile, and resident CTAs per SM of the norm
-// pass.  Measured on the 350M list: 0.152 to 0.156 ms with eight groups at 5
-// CTAs/SM, 0.165 with four, 0.156 with sixteen (which spill at 5 CTAs/SM).
+// pass (each CTA holds the 32 KB table of the exact squares).
 #ifndef FP8OPT_NORM_GROUPS
 #define FP8OPT_NORM_GROUPS 8
 #endif
 #ifndef FP8OPT_NORM_MIN_BLOCKS
 #define FP8OPT_NORM_MIN_BLOCKS 5
 #endif
+// Tiles ahead of the current one that one thread of the CTA asks L2 for
+// (cp.async.bulk.prefetch.L2; 0: none).  A CTA walks one contiguous range of
+// the chunk table, so the next tiles are the next bytes of its range.
+#ifndef FP8OPT_NORM_PREFETCH
+#define FP8OPT_NORM_PREFETCH 0
+#endif
 constexpr int kNormGroups = FP8OPT_NORM_GROUPS;
 constexpr int64_t kNormTile = (int64_t)kThreads * kGroup * kNormGroups;
 
-// This thread's share of [begin, end) into acc.
+// This thread's share of [begin, end) into acc; bad collects the codes at
+// or above the tensor's overflow threshold (addend tadd).
 template <int GF>
 __device__ void thread_norm(const uint8_t* g, int64_t begin, int64_t end,
-                            bool vec, SqAcc<GF>& acc) {
+                            bool vec, uint32_t tadd, const SqTable& tab,
+                            SqTab& acc, uint32_t& bad) {
   const int tid = threadIdx.x;
+  const uint32_t lb = sq_lane_byte<GF>();
+  const bool pf = FP8OPT_NORM_PREFETCH > 0 && tid == 0 && vec && aligned16(g);
 #pragma unroll 1
   for (int64_t base = begin; base < end; base += kNormTile) {
+    if (pf) {
+      const int64_t ahead = base + FP8OPT_NORM_PREFETCH * kNormTile;
+      if (ahead + kNormTile <= end) prefetch_l2(g + ahead, (uint32_t)kNormTile);
+    }
     if (vec && base + kNormTile <= end) {
       uint2 c[kNormGroups];
 #pragma unroll
@@ -47,8 +61,10 @@ __device__ void thread_norm(const uint8_t* g, int64_t begin, int64_t end,
         c[q] = ld_once2(g + base + q * (kThreads * kGroup) + tid * kGroup);
 #pragma unroll
       for (int q = 0; q < kNormGroups; ++q) {
-        acc.add_word(c[q].x);
-        acc.add_word(c[q].y);
+        const uint32_t a = c[q].x & 0x7F7F7F7Fu, b = c[q].y & 0x7F7F7F7Fu;
+        bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
+        acc.add_word<GF>(a, lb, tab);
+        acc.add_word<GF>(b, lb, tab);
       }
     } else {
 #pragma unroll 1
@@ -57,27 +73,19 @@ __device__ void thread_norm(const uint8_t* g, int64_t begin, int64_t end,
         for (int e = 0; e < kGroup; ++e) {
           const int64_t i = i0 + e;
           if (i >= end) break;
-          acc.add_word(g[i]);
+          const uint32_t a = g[i] & 0x7Fu;
+          bad |= (a + tadd) & 0x80u;
+          acc.add_word<GF>(a, lb, tab);    // bytes 1..3 are zero: magnitude 0
         }
       }
     }
   }
 }
 
-template <int GF>
-__device__ __forceinline__ void norm_chunk(const StepDesc& d, const Chunk& ch,
-                                           int64_t begin, int64_t end, float ils,
-                                           unsigned long long* sums,
-                                           unsigned long long* found,
-                                           uint32_t epoch,
-                                           unsigned long long* red64,
-                                           uint32_t* red32) {
-  SqAcc<GF> acc;
-  thread_norm<GF>(d.g, begin, end, d.vec_ok != 0, acc);
-  const float k = __fdiv_rn(ils, *d.g_scale);
-  sq_commit<GF>(acc, ch.tensor, end > begin, k, sums, found, epoch, red64, red32);
-}
-
+// Each CTA takes one contiguous range of the chunk table (an equal share),
+// so a large tensor's chunks reach it as one run; a run adds to one
+// accumulator, which goes to the tensor's slot when the tensor changes: one
+// CTA reduction per run instead of one per chunk.
 __global__ void __launch_bounds__(kThreads, FP8OPT_NORM_MIN_BLOCKS)
 grad_norm_kernel(const StepDesc* __restrict__ descs,
                  const Chunk* __restrict__ chunks, uint32_t nchunks, float ils_h,
@@ -85,18 +93,41 @@ grad_norm_kernel(const StepDesc* __restrict__ descs,
                  unsigned long long* __restrict__ sums,
                  unsigned long long* __restrict__ found, uint32_t epoch) {
   const float ils = ils_dev != nullptr ? *ils_dev : ils_h;
+  __shared__ SqTable tab;
   __shared__ unsigned long long red64[2 * (kThreads / 32)];
-  __shared__ uint32_t red32[kThreads / 32];
-  for (uint32_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+  sq_table_fill(tab);
+  SqTab acc;
+  uint32_t bad = 0, tadd = 0, cur = 0xFFFFFFFFu;
+  bool nonempty = false;
+  const uint32_t c0 = (uint32_t)((uint64_t)blockIdx.x * nchunks / gridDim.x);
+  const uint32_t c1 = (uint32_t)((uint64_t)(blockIdx.x + 1) * nchunks / gridDim.x);
+  for (uint32_t c = c0; c < c1; ++c) {
     const Chunk ch = chunks[c];
     const StepDesc d = descs[ch.tensor];
+    if (ch.tensor != cur) {   // uniform over the CTA
+      if (cur != 0xFFFFFFFFu) {
+        sq_commit_flag(acc, cur, nonempty, bad, sums, found, epoch, red64);
+        acc = SqTab();
+        bad = 0;
+        nonempty = false;
+      }
+      cur = ch.tensor;
+      // found_inf exactly as the step's first pass decides it: some code at
+      // or above the overflow threshold of k = inv_loss_scale / g_scale
+      const float k = __fdiv_rn(ils, *d.g_scale);
+      tadd = threshold_addend(d.g_fmt == kE4M3 ? overflow_threshold<kE4M3>(k)
+                                               : overflow_threshold<kE5M2>(k));
+    }
     const int64_t begin = ch.begin;
     const int64_t end = begin + ch.len;
+    nonempty |= end > begin;
     if (d.g_fmt == kE4M3)
-      norm_chunk<kE4M3>(d, ch, begin, end, ils, sums, found, epoch, red64, red32);
+      thread_norm<kE4M3>(d.g, begin, end, d.vec_ok != 0, tadd, tab, acc, bad);
     else
-      norm_chunk<kE5M2>(d, ch, begin, end, ils, sums, found, epoch, red64, red32);
+      thread_norm<kE5M2>(d.g, begin, end, d.vec_ok != 0, tadd, tab, acc, bad);
   }
+  if (cur != 0xFFFFFFFFu)
+    sq_commit_flag(acc, cur, nonempty, bad, sums, found, epoch, red64);
 }
 
 // Per-record terms fl64(k^2 * fl64(S) * 2^-32) (k^2 is exact in double), one
@@ -166,7 +197,111 @@ __global__ void found_kernel(unsigned long long* __restrict__ slot, uint32_t epo
   if (out != nullptr) *out = f ? 1u : 0u;
 }
 
+// ---------------------------------------------- exchanges between ranks
+//
+// A tensor cut into pieces on several ranks has per-tensor quantities that
+// are maxima (an amax, max |g|) or exact sums over its pieces.  The calls
+// split at those quantities export each piece's value and import the
+// combined one: maxima as the fp32 bits of a non-negative value (their
+// unsigned order is the amax order: NaN 0x7FC00000 above +inf above every
+// finite value, so a MAX over ranks combines them), exact sums as four
+// 32-bit limbs held in int64 (a SUM over fewer than 2^31 ranks stays exact).
+
+// out[i] = this call's value in slot i (0 if the slot holds none).
+__global__ void slots_export_kernel(const unsigned long long* __restrict__ slots,
+                                    uint32_t epoch, int n,
+                                    uint32_t* __restrict__ out) {
+  const int i = blockIdx.x * kThreads + threadIdx.x;
+  if (i < n) out[i] = slot_value(slots[i], epoch);
+}
+
+// Slot i takes the given value as this call's.
+__global__ void slots_import_kernel(unsigned long long* __restrict__ slots,
+                                    uint32_t epoch, int n,
+                                    const uint32_t* __restrict__ in) {
+  const int i = blockIdx.x * kThreads + threadIdx.x;
+  if (i < n) slots[i] = slot_tag(epoch, in[i]);
+}
+
+// The exact 128-bit sums (sums[2i], sums[2i + 1]) as limbs[4i .. 4i + 3],
+// low limb first; block 0 also exports the call's found_inf.
+__global__ void sums_to_limbs_kernel(const unsigned long long* __restrict__ sums,
+                                     int n,
+                                     const unsigned long long* __restrict__ found,
+                                     uint32_t epoch, long long* __restrict__ limbs,
+                                     uint32_t* __restrict__ found_out) {
+  const int i = blockIdx.x * kThreads + threadIdx.x;
+  if (i < n) {
+    const unsigned long long lo = sums[2 * i], hi = sums[2 * i + 1];
+    limbs[4 * i] = (long long)(lo & 0xFFFFFFFFull);
+    limbs[4 * i + 1] = (long long)(lo >> 32);
+    limbs[4 * i + 2] = (long long)(hi & 0xFFFFFFFFull);
+    limbs[4 * i + 3] = (long long)(hi >> 32);
+  }
+  if (found_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
+    *found_out = slot_value(*found, epoch) != 0 ? 1u : 0u;
+}
+
+// terms[t] = the norm term of tensor t from its limbs summed over ranks (each
+// below 2^63; the top limb below 2^32) and the factor k = inv_loss_scale /
+// scale, scale = fp8_max / amax with the cast's guards (amax_bits[t]).
+__global__ void limbs_terms_kernel(const long long* __restrict__ limbs,
+                                   const uint32_t* __restrict__ amax_bits, int n,
+                                   float fp8_max, float ils,
+                                   double* __restrict__ terms) {
+  const int t = blockIdx.x * kThreads + threadIdx.x;
+  if (t >= n) return;
+  const unsigned long long l0 = (unsigned long long)limbs[4 * t];
+  const unsigned long long l1 = (unsigned long long)limbs[4 * t + 1];
+  const unsigned long long l2 = (unsigned long long)limbs[4 * t + 2];
+  const unsigned long long l3 = (unsigned long long)limbs[4 * t + 3];
+  U128 s = {l0, 0ull};
+  s = add128(s, U128{l1 << 32, l1 >> 32});
+  s = add128(s, U128{0ull, l2});
+  s = add128(s, U128{0ull, l3 << 32});
+  const float scale = scale_from_amax_bits(amax_bits[t], fp8_max);
+  terms[t] = norm_term(s, __fdiv_rn(ils, scale));
+}
+
 }  // namespace
+
+// Slot values of this call out to a device array, and back in.
+cudaError_t launch_slots_export(const unsigned long long* slots, uint32_t epoch,
+                                int n, uint32_t* out, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  slots_export_kernel<<<(n + kThreads - 1) / kThreads, kThreads, 0, stream>>>(
+      slots, epoch, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_slots_import(unsigned long long* slots, uint32_t epoch, int n,
+                                const uint32_t* in, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  slots_import_kernel<<<(n + kThreads - 1) / kThreads, kThreads, 0, stream>>>(
+      slots, epoch, n, in);
+  return cudaGetLastError();
+}
+
+// The exact sums of n records as limbs, and the call's found_inf (found_out,
+// may be NULL).
+cudaError_t launch_sums_to_limbs(const unsigned long long* sums, int n,
+                                 const unsigned long long* found, uint32_t epoch,
+                                 long long* limbs, uint32_t* found_out,
+                                 cudaStream_t stream) {
+  const int blocks = n > 0 ? (n + kThreads - 1) / kThreads : 1;
+  sums_to_limbs_kernel<<<blocks, kThreads, 0, stream>>>(sums, n, found, epoch,
+                                                        limbs, found_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_limbs_terms(const long long* limbs, const uint32_t* amax_bits,
+                               int n, int fmt, float ils, double* terms,
+                               cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  limbs_terms_kernel<<<(n + kThreads - 1) / kThreads, kThreads, 0, stream>>>(
+      limbs, amax_bits, n, fmt == kE4M3 ? 448.0f : 57344.0f, ils, terms);
+  return cudaGetLastError();
+}
 
 // The norm pass and the per-record terms on `stream`.  sums: 2n zeroed words;
 // found: the call's found_inf slot; terms: n doubles out; found_out: the

@@ -27,6 +27,11 @@
 
 namespace fp8opt {
 
+cudaError_t launch_sums_to_limbs(const unsigned long long* sums, int n,
+                                 const unsigned long long* found, uint32_t epoch,
+                                 long long* limbs, uint32_t* found_out,
+                                 cudaStream_t stream);
+
 namespace {
 
 // Tunables: 16-code groups per thread per tile, shards whose loads are issued
@@ -614,16 +619,19 @@ cudaError_t launch_reduce(const ReduceDesc* descs, const Chunk* chunks,
                           uint32_t epoch, int k, int in_fmt, int out_fmt,
                           float post, int grid_amax, int grid_encode,
                           const ReduceNorm* norm, cudaStream_t stream,
-                          LaunchMark mark) {
+                          LaunchMark mark, int phase) {
   if (nchunks == 0) return cudaSuccess;
   const uint32_t ga = grid_min((uint32_t)grid_amax, nchunks);
   const uint32_t ge = grid_min((uint32_t)grid_encode, nchunks);
-  if (mark) mark(kReduceAmaxK, 0, stream);
-  if (in_fmt == kE4M3)
-    launch_amax<kE4M3>(ga, descs, chunks, nchunks, k, post, slots, epoch, stream);
-  else
-    launch_amax<kE5M2>(ga, descs, chunks, nchunks, k, post, slots, epoch, stream);
-  if (mark) mark(kReduceAmaxK, 1, stream);
+  if (phase & kReduceAmaxPass) {
+    if (mark) mark(kReduceAmaxK, 0, stream);
+    if (in_fmt == kE4M3)
+      launch_amax<kE4M3>(ga, descs, chunks, nchunks, k, post, slots, epoch, stream);
+    else
+      launch_amax<kE5M2>(ga, descs, chunks, nchunks, k, post, slots, epoch, stream);
+    if (mark) mark(kReduceAmaxK, 1, stream);
+  }
+  if (!(phase & kReduceEncodePass)) return cudaGetLastError();
   if (mark) mark(kReduceEncodeK, 0, stream);
   RedSq sq;
   if (norm != nullptr) sq = RedSq{norm->sums, norm->found, norm->ils};
@@ -635,6 +643,12 @@ cudaError_t launch_reduce(const ReduceDesc* descs, const Chunk* chunks,
     launch_encode<kE5M2>(ge, descs, chunks, nchunks, k, post, slots, epoch,
                          out_fmt, sqp, stream);
   if (mark) mark(kReduceEncodeK, 1, stream);
+  if (norm != nullptr && norm->n > 0 && norm->limbs != nullptr) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_sums_to_limbs(norm->sums, norm->n, norm->found, epoch,
+                                norm->limbs, norm->found_out, stream);
+  }
   if (norm != nullptr && norm->n > 0) {
     if (mark) mark(kGradNormTermsK, 0, stream);
     reduce_terms_kernel<<<(norm->n + kThreads - 1) / kThreads, kThreads, 0, stream>>>(

@@ -641,6 +641,20 @@ cudaError_t launch_step_update(const StepDesc* descs, const Chunk* chunks,
   return cudaGetLastError();
 }
 
+// The O3 weight-copy pass alone, for an update pass launched without it
+// (the split step: the master's amax is combined over ranks in between).
+cudaError_t launch_step_w8(const StepDesc* descs, const Chunk* chunks_o3,
+                           uint32_t nchunks_o3, const StepScratch& sc,
+                           uint32_t epoch, int grid_w8, cudaStream_t stream,
+                           LaunchMark mark) {
+  if (nchunks_o3 == 0) return cudaSuccess;
+  if (mark) mark(kStepW8K, 0, stream);
+  step_w8_kernel<<<grid_min((uint32_t)grid_w8, nchunks_o3), kThreads, 0, stream>>>(
+      descs, chunks_o3, nchunks_o3, sc, epoch);
+  if (mark) mark(kStepW8K, 1, stream);
+  return cudaGetLastError();
+}
+
 // The first pass alone (found_inf, the amax of the new first moment, max |g|).
 cudaError_t launch_step_amax(const StepDesc* descs, const Chunk* chunks,
                              uint32_t nchunks, const StepScratch& sc,

@@ -1,26 +1,34 @@
 """Data-parallel sharding of the FP8 optimizer step (ZeRO-1 style).
 
 MS-AMP's O3 level keeps an FP16 master weight per parameter and an FP8 weight
-for forward/backward, and broadcasts the 8-bit weights (the "Optimization
-Level" page, O3 paragraph).  Here every rank owns the optimizer state (E4M3
-first moment, FP16 second moment, FP16 master) of a contiguous range of whole
-tensors, balanced by size; a step on each rank is
+for forward/backward, names ZeRO among the strategies it supports, and
+broadcasts the 8-bit weights (the "Optimization Level" page, O3 paragraph).
+Here the tensors of the list are laid end to end in one element space, each
+from a 256-element boundary, and rank r owns the optimizer state (E4M3 first
+moment, FP16 second moment, FP16 master) of the elements [r*S, (r+1)*S) of
+that space: every rank holds the same number of elements, and a tensor that
+crosses a segment boundary is cut into pieces on two or more ranks.  A step
+on each rank is
 
-  1. the FP8 cast of its local gradients, an all-to-all that brings every
-     tensor's codes from all ranks to its owner, and the FP8 mean of those
-     shards (with clipping, that reduction also gives the owned tensors' norm
-     terms and found_inf);
-  2. the step's first pass over its own tensors (``begin``), giving found_inf;
-  3. one exchange: found_inf MAX over ranks (and, with clipping, the per-tensor
-     norm terms, each held by exactly one rank, summed so every rank holds all
-     of them and takes the same norm and clip coefficient);
-  4. the update and the O3 weight copy of its own tensors (``finish``), skipped
-     on every rank when any rank found a non-finite gradient;
-  5. the E4M3 weight copies and their scales broadcast from their owners.
+  1. the FP8 cast of its local gradients of every tensor, one all-to-all that
+     sends every rank its segment of the codes, and an all-gather of the
+     per-tensor scales;
+  2. the FP8 mean of the ranks' shards of its pieces, in two passes: each
+     piece's amax, combined per tensor by MAX over ranks, then the encode with
+     the whole tensor's amax (with clipping, the encode also gives each
+     piece's exact sum of squares, combined per tensor by an exact SUM over
+     ranks, so that every rank takes the same norm and clip coefficient);
+  3. the step's first pass over its pieces; per tensor, the amax of the new
+     first moment and max |g| combined by MAX over ranks, with found_inf;
+  4. the update of its pieces with the whole tensors' maxima, skipped on every
+     rank when any rank found a non-finite gradient; for O3 the new masters'
+     amax combined by MAX, then the E4M3 weight copy;
+  5. one all-gather that returns every rank's segment of the new FP16 weights
+     (O2) or E4M3 weights (O3, their per-tensor scales combined by MAX).
 
-Because the partition is tensor-aligned, every per-tensor quantity (amax,
-scale, bound) is computed whole on one rank, and the result on every rank is
-the unsharded step's, bit for bit.
+Every per-tensor quantity is therefore the whole tensor's, and the result on
+every rank is the unsharded pipeline's, bit for bit.  On one rank a step is
+the cast and the step in one call (no exchange, no reduction).
 
 The collectives are torch.distributed calls on an initialised process group
 (NCCL between GPUs; gloo works for host-side tests).  The arithmetic is behind
@@ -31,51 +39,41 @@ from __future__ import annotations
 
 from typing import List, Optional, Sequence, Tuple
 
+ALIGN = 256   # elements: 256 B of codes, 512 B of FP16
 
-def partition(numels: Sequence[int], world: int) -> List[Tuple[int, int]]:
-    """Contiguous, tensor-aligned ranges [lo, hi) of the tensor list, one per
-    rank in rank order, that minimise the largest rank's element count (every
-    tensor of a step moves the same bytes per element, so this balances
-    bytes).  Ranks past the last tensor get empty ranges.  Deterministic:
-    every rank computes the same answer."""
+
+def layout(numels: Sequence[int], world: int, align: int = ALIGN):
+    """The element space of a tensor list for `world` ranks.
+
+    Returns (off, seg, pieces): tensor t starts at element off[t] (a multiple
+    of `align`; tensors follow one another in list order, each padded to a
+    multiple of `align`); every rank owns `seg` elements (a multiple of
+    `align`, world * seg covering the space), rank r the range [r*seg,
+    (r+1)*seg); pieces[r] lists rank r's (tensor, a, b), the tensor's
+    elements [a, b) inside that range, in tensor order.  An empty tensor is a
+    piece (t, 0, 0) of the rank whose range holds its offset, so that its
+    per-tensor outputs are written.  Deterministic: every rank computes the
+    same answer."""
     if world < 1:
         raise ValueError("world must be >= 1")
-    n = len(numels)
-    if any(x < 0 for x in numels):
+    if any(int(x) < 0 for x in numels):
         raise ValueError("negative numel")
-    # the smallest capacity whose greedy packing fits in `world` ranges
-    w = [max(int(x), 1) for x in numels]   # an empty tensor still has a record
-
-    def fits(cap):
-        parts, load = 1, 0
-        for x in w:
-            if x > cap:
-                return False
-            if load + x > cap:
-                parts += 1
-                load = x
-            else:
-                load += x
-        return parts <= world
-
-    lo, hi = max(w, default=1), max(sum(w), 1)
-    while lo < hi:
-        mid = (lo + hi) // 2
-        if fits(mid):
-            hi = mid
-        else:
-            lo = mid + 1
-    cap = lo
-    ranges, start, load = [], 0, 0
-    for i, x in enumerate(w):
-        if load + x > cap and i > start:
-            ranges.append((start, i))
-            start, load = i, 0
-        load += x
-    ranges.append((start, n))
-    while len(ranges) < world:
-        ranges.append((n, n))
-    return ranges
+    off, pos = [], 0
+    for x in numels:
+        off.append(pos)
+        pos += -(-int(x) // align) * align
+    share = -(-pos // world)
+    seg = max(align, -(-share // align) * align)
+    pieces: List[List[Tuple[int, int, int]]] = [[] for _ in range(world)]
+    for t, x in enumerate(numels):
+        x = int(x)
+        if x == 0:
+            pieces[min(off[t] // seg, world - 1)].append((t, 0, 0))
+            continue
+        for r in range(off[t] // seg, (off[t] + x - 1) // seg + 1):
+            pieces[r].append((t, max(0, r * seg - off[t]),
+                              min(x, (r + 1) * seg - off[t])))
+    return off, seg, pieces
 
 
 # ------------------------------------------------------------ collectives
@@ -95,16 +93,16 @@ class TorchDistComm:
         self._dist.all_to_all_single(out, inp, list(out_splits), list(in_splits),
                                      group=self.group)
 
+    def all_gather(self, out, inp):
+        """out = the ranks' inp, concatenated in rank order (inp may be this
+        rank's part of out)."""
+        self._dist.all_gather_into_tensor(out, inp, group=self.group)
+
     def all_reduce_sum(self, t):
         self._dist.all_reduce(t, op=self._dist.ReduceOp.SUM, group=self.group)
 
     def all_reduce_max(self, t):
         self._dist.all_reduce(t, op=self._dist.ReduceOp.MAX, group=self.group)
-
-    def broadcast(self, t, src):
-        self._dist.broadcast(t, src=self._dist.get_global_rank(self.group, src)
-                             if self.group is not None else src,
-                             group=self.group)
 
 
 # ------------------------------------------------------------------ engine
@@ -129,6 +127,14 @@ class LibEngine:
         return AdamWPlan(g, g_scale, m, m_scale, v, w, w8, w8_scale, w8_amax,
                          g_fmt, v_bound)
 
+    def make_cast_step(self, cast, step):
+        from .api import CastStepPlan
+        return CastStepPlan(cast, step)
+
+    def norm_terms_from_limbs(self, limbs, amax_bits, fmt, inv_loss_scale, terms):
+        from .api import norm_terms_from_limbs
+        norm_terms_from_limbs(limbs, amax_bits, fmt, inv_loss_scale, terms)
+
     def clip_coef(self, terms, max_grad_norm, clip, norm, found):
         from .api import clip_coef
         clip_coef(terms, max_grad_norm, clip, norm, found)
@@ -136,29 +142,22 @@ class LibEngine:
 
 # ------------------------------------------------------------ the step loop
 
-def _offsets(views, base) -> List[int]:
-    """Element offsets of arena views in their base buffer."""
-    isz = base.element_size()
-    return [(v.data_ptr() - base.data_ptr()) // isz for v in views]
-
-
 class ShardedFp8AdamW:
     """One rank of the data-parallel FP8 optimizer step (MS-AMP O2 / O3 with
-    ZeRO-1 sharding of the optimizer state).
+    ZeRO-1 sharding of the optimizer state over equal element ranges).
 
     weights: every tensor's FP16 weight (the same on every rank); they are
     copied into the optimizer's flat arena, whose views ``weights`` the
     forward pass uses (O2), or which holds the FP16 masters of this rank's
-    tensors (O3; the E4M3 copies of all tensors are ``w8`` / ``w8_scale``).
+    pieces (O3; the E4M3 copies of all tensors are ``w8`` / ``w8_scale``).
+    ``pieces`` lists this rank's (tensor, a, b); ``m``, ``v``, ``m_scale``
+    (and ``v_bound``) hold their optimizer state, one entry per piece.
 
     ``step(grads)`` takes this rank's local gradients of every tensor (BF16,
-    FP16 or FP32), casts them to FP8 (per-tensor just-in-time scales), sends
-    each tensor's codes to its owner (one all-to-all of the codes and one of
-    the scales), reduces the ranks' shards to their mean in FP8, and steps the
-    owned tensors.  found_inf is combined over ranks (every rank skips
-    together) and, with ``max_grad_norm``, the gradient is clipped to a
-    global L2 norm taken over every rank's tensors.  The owners then
-    broadcast the new FP16 weights (O2) or E4M3 weights and scales (O3).
+    FP16 or FP32) and runs the step of the module docstring; found_inf is
+    combined over ranks (every rank skips together) and, with
+    ``max_grad_norm``, the gradient is clipped to a global L2 norm taken over
+    every rank's pieces.
     """
 
     def __init__(self, weights: Sequence, comm, lr=1e-3, betas=(0.9, 0.999),
@@ -186,75 +185,91 @@ class ShardedFp8AdamW:
         self.numels = numels
         n = len(numels)
         self.n = n
-        self.ranges = partition(numels, self.world)
-        lo, hi = self.ranges[self.rank]
-        self.own = (lo, hi)
+        self.off, self.seg, self.layout_pieces = layout(numels, self.world)
+        self.pieces = self.layout_pieces[self.rank]
+        world, seg, off, rank = self.world, self.seg, self.off, self.rank
+        space = world * seg
         f32 = dict(dtype=torch.float32, device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
 
-        # every tensor: weights (O2) / masters (O3) and the local cast codes
-        self.weights, self._w_flat = arena_views(numels, torch.float16, dev,
-                                                 return_base=True)
+        # every tensor in the element space: FP16 weights (O2) / masters
+        # (O3), the local cast codes, and (O3) the E4M3 weight copies
+        self._w_flat = torch.zeros(space, dtype=torch.float16, device=dev)
+        self.weights = [self._w_flat[off[t]:off[t] + numels[t]] for t in range(n)]
         for dst, src in zip(self.weights, weights):
             dst.copy_(src.reshape(-1))
-        self._gc, self._gc_flat = arena_views(numels, torch.uint8, dev,
-                                              return_base=True)
+        self._gc_flat = torch.zeros(space, dtype=torch.uint8, device=dev)
+        self._gc = [self._gc_flat[off[t]:off[t] + numels[t]] for t in range(n)]
         self._g_amax = torch.zeros(max(n, 1), **f32)
         self._g_scale = torch.ones(max(n, 1), **f32)
-        # element offsets (the same in every uint8 / float16 arena: both pad
-        # each tensor to 256 bytes, i.e. 256 and 128 elements)
-        off8 = _offsets(self._gc, self._gc_flat) + [self._gc_flat.numel()]
-        off16 = _offsets(self.weights, self._w_flat) + [self._w_flat.numel()]
-        if n:
-            off8[-1] = off8[n - 1] + -(-numels[n - 1] // 256) * 256
-            off16[-1] = off16[n - 1] + -(-numels[n - 1] // 128) * 128
-        self._off8, self._off16 = off8, off16
-        self._bytes = [off8[b] - off8[a] for a, b in self.ranges]
-        self._counts = [b - a for a, b in self.ranges]
-        own_bytes = self._bytes[self.rank]
-        n_own = hi - lo
-
-        # the shards of this rank's tensors from every rank, and their scales
-        self._recv = torch.zeros(max(self.world * own_bytes, 1), dtype=torch.uint8,
-                                 device=dev)
-        self._recv_scale = torch.ones(max(self.world * n_own, 1), **f32)
-        self._scale_t = torch.ones((max(n_own, 1), self.world), **f32)
-        rows = self._recv[:self.world * own_bytes].view(self.world, own_bytes)
-        shards = [rows[:, off8[t] - off8[lo]: off8[t] - off8[lo] + numels[t]]
-                  for t in range(lo, hi)]
-        own_numels = numels[lo:hi]
-        self._g_own = arena_views(own_numels, torch.uint8, dev)
-        self._g_own_amax = torch.zeros(max(n_own, 1), **f32)
-        self._g_own_scale = torch.ones(max(n_own, 1), **f32)
-        self._reduce = self.engine.make_reduce(
-            shards, [self._scale_t[j] for j in range(n_own)], self._g_own,
-            self._g_own_amax, self._g_own_scale, grad_fmt, grad_fmt,
-            1.0 / self.world)
-
-        # this rank's optimizer state
-        self.m = arena_views(own_numels, torch.uint8, dev, fill=0)
-        self.v = arena_views(own_numels, torch.float16, dev, fill=0)
-        self.m_scale = torch.ones(max(n_own, 1), **f32)
-        self.v_bound = torch.zeros(max(n_own, 1), **f32) if scaled_v else None
-        if level == "O3":
-            self.w8, self._w8_flat = arena_views(numels, torch.uint8, dev, fill=0,
-                                                 return_base=True)
+        o3 = level == "O3"
+        if o3:
+            self._w8_flat = torch.zeros(space, dtype=torch.uint8, device=dev)
+            self.w8 = [self._w8_flat[off[t]:off[t] + numels[t]] for t in range(n)]
             self.w8_scale = torch.ones(max(n, 1), **f32)
             self.w8_amax = torch.zeros(max(n, 1), **f32)
-            w8_own = self.w8[lo:hi]
-            w8s, w8a = self.w8_scale[lo:max(hi, lo + 1)], self.w8_amax[lo:max(hi, lo + 1)]
         else:
             self.w8 = self.w8_scale = self.w8_amax = None
-            w8_own = w8s = w8a = None
+        self._found = torch.zeros(1, **i32)
+        self._found_out = torch.zeros(1, **i32)
+        self._cast_key = None
+        self._cast = None
+        self._fused, self._fused_for = None, None
+
+        pieces = self.pieces
+        npc = len(pieces)
+        sizes = [b - a for _, a, b in pieces]
+        self.m = arena_views(sizes, torch.uint8, dev, fill=0)
+        self.v = arena_views(sizes, torch.float16, dev, fill=0)
+        self.m_scale = torch.ones(max(npc, 1), **f32)
+        self.v_bound = torch.zeros(max(npc, 1), **f32) if scaled_v else None
+        w_pieces = [self._w_flat[off[t] + a:off[t] + b] for t, a, b in pieces]
+        if world == 1:
+            # one rank: the cast's codes and scales feed the step directly
+            self._step = self.engine.make_step(
+                self._gc, self._g_scale, self.m, self.m_scale, self.v, w_pieces,
+                self.w8 if o3 else None, self.w8_scale, self.w8_amax, grad_fmt,
+                self.v_bound)
+            return
+
+        self._piece_t = torch.tensor([t for t, _, _ in pieces] or [0],
+                                     dtype=torch.int64, device=dev)[:npc]
+        # every rank's codes of this rank's segment, and every rank's scales
+        self._recv = torch.zeros(space, dtype=torch.uint8, device=dev)
+        rows = self._recv.view(world, seg)
+        shards = [rows[:, off[t] + a - rank * seg:off[t] + b - rank * seg]
+                  for t, a, b in pieces]
+        self._scales_all = torch.ones(world * max(n, 1), **f32)
+        self._scales_t = torch.ones((max(n, 1), world), **f32)
+        self._g_own = arena_views(sizes, torch.uint8, dev)
+        self._g_own_amax = torch.zeros(max(npc, 1), **f32)
+        self._g_own_scale = torch.ones(max(npc, 1), **f32)
+        self._reduce = self.engine.make_reduce(
+            shards, [self._scales_t[t] for t, _, _ in pieces], self._g_own,
+            self._g_own_amax, self._g_own_scale, grad_fmt, grad_fmt, 1.0 / world)
+        if o3:
+            w8_pieces = [self._w8_flat[off[t] + a:off[t] + b] for t, a, b in pieces]
+            self._w8s_own = torch.ones(max(npc, 1), **f32)
+            self._w8a_own = torch.zeros(max(npc, 1), **f32)
+        else:
+            w8_pieces = self._w8s_own = self._w8a_own = None
         self._step = self.engine.make_step(
             self._g_own, self._g_own_scale, self.m, self.m_scale, self.v,
-            self.weights[lo:hi], w8_own, w8s, w8a, grad_fmt, self.v_bound)
-        self._found = torch.zeros(1, dtype=torch.int32, device=dev)
-        self._found_out = torch.zeros(1, dtype=torch.int32, device=dev)
+            w_pieces, w8_pieces, self._w8s_own, self._w8a_own, grad_fmt,
+            self.v_bound)
+        # exchange buffers: per piece (local) and per tensor (exchanged)
+        self._amax_local = torch.zeros(max(npc, 1), **i32)
+        self._amax_vec = torch.zeros(max(n, 1), **i32)
+        self._maxima_local = torch.zeros(2 * max(npc, 1), **i32)
+        self._maxima_vec = torch.zeros(2 * n + 1, **i32)
+        self._limbs_local = torch.zeros(4 * max(npc, 1), dtype=torch.int64, device=dev)
+        self._limbs_vec = torch.zeros(4 * n + 1, dtype=torch.int64, device=dev)
+        self._master_local = torch.zeros(max(npc, 1), **i32)
+        self._master_vec = torch.zeros(max(n, 1), **i32)
+        self._w8_vec = torch.zeros(2 * max(n, 1), **i32)
         self._terms = torch.zeros(max(n, 1), dtype=torch.float64, device=dev)
         self._norm = torch.zeros(1, dtype=torch.float64, device=dev)
         self._clip = torch.ones(1, **f32)
-        self._cast_key = None
-        self._cast = None
 
     def _cast_plan(self, grads):
         key = tuple((g.data_ptr(), g.numel(), g.dtype) for g in grads)
@@ -265,63 +280,118 @@ class ShardedFp8AdamW:
             self._cast_key = key
         return self._cast
 
+    def _max_over_ranks(self, local, vec, parts=1, flag=None):
+        """Per-tensor MAX over ranks of per-piece int32 values: `parts`
+        blocks of one value per piece in `local` go to their tensors' slots
+        in `vec` (zero elsewhere, below every value), the ranks' vectors are
+        combined by MAX in one collective, and each piece takes its tensor's
+        result back.  flag (an int32 scalar, optional) rides along in the
+        entry after the blocks and takes the MAX over ranks too."""
+        n, npc, idx = self.n, len(self.pieces), self._piece_t
+        vec.zero_()
+        for j in range(parts):
+            vec[j * n:(j + 1) * n].index_copy_(0, idx, local[j * npc:(j + 1) * npc])
+        if flag is not None:
+            vec[parts * n:parts * n + 1].copy_(flag)
+        self.comm.all_reduce_max(vec)
+        for j in range(parts):
+            local[j * npc:(j + 1) * npc].copy_(vec[j * n:(j + 1) * n].index_select(0, idx))
+        if flag is not None:
+            flag.copy_(vec[parts * n:parts * n + 1])
+
     def step(self, grads: Sequence, inv_loss_scale=1.0) -> int:
         """One data-parallel step from this rank's local gradients; returns
         found_inf (combined over ranks)."""
         if len(grads) != self.n:
             raise ValueError("one gradient per tensor")
-        lo, hi = self.own
-        comm, world = self.comm, self.world
+        if self.n == 0:
+            return 0
         t = self.step_count + 1
         hp = (self.lr, self.beta1, self.beta2, self.eps, self.wd, t,
               inv_loss_scale, self.l2)
-        # 1. FP8 cast of every local gradient
-        self._cast_plan(grads)()
-        # 2. each tensor's codes and scale to its owner
-        total = self._off8[self.n] if self.n else 0
-        comm.all_to_all(self._recv[:world * self._bytes[self.rank]],
-                        self._gc_flat[:total],
-                        [self._bytes[self.rank]] * world, self._bytes)
-        n_own = hi - lo
-        comm.all_to_all(self._recv_scale[:world * n_own], self._g_scale[:self.n],
-                        [n_own] * world, self._counts)
-        if n_own:
-            self._scale_t[:n_own].copy_(
-                self._recv_scale[:world * n_own].view(world, n_own).t())
-        # 3. the mean of the ranks' shards, re-encoded (with clipping, the
-        #    encode pass also gives the owned tensors' norm terms)
-        clip = None
-        if self.max_grad_norm is not None:
-            self._terms.zero_()
-            self._reduce(norm_terms=self._terms[lo:max(hi, lo + 1)],
-                         found=self._found, inv_loss_scale=inv_loss_scale)
-        else:
-            self._reduce()
-        # 4. found_inf (and the global norm) over ranks, then the step
-        if self.max_grad_norm is not None:
-            comm.all_reduce_sum(self._terms)
-            comm.all_reduce_max(self._found)
-            self.engine.clip_coef(self._terms[:self.n], self.max_grad_norm,
-                                  self._clip, self._norm, self._found)
-            clip = self._clip
-            self._step.begin(hp, clip, None)
-        else:
-            self._step.begin(hp, None, self._found)
-            comm.all_reduce_max(self._found)
-        self._step.finish(hp, clip, self._found, self._found_out)
-        # 5. the owners' new weights to every rank
-        for r, (a, b) in enumerate(self.ranges):
-            if a == b:
-                continue
-            if self.level == "O3":
-                comm.broadcast(self._w8_flat[self._off8[a]:self._off8[b]], r)
-                comm.broadcast(self.w8_scale[a:b], r)
-                comm.broadcast(self.w8_amax[a:b], r)
-            else:
-                comm.broadcast(self._w_flat[self._off16[a]:self._off16[b]], r)
-        found = int(self._found_out.item())
-        if self.max_grad_norm is not None:
-            self.last_grad_norm = float(self._norm.item())
+        cast = self._cast_plan(grads)
+        found = (self._step_one_rank(cast, hp) if self.world == 1
+                 else self._step_ranks(cast, hp))
         if found == 0:
             self.step_count = t
+        return found
+
+    def _step_one_rank(self, cast, hp) -> int:
+        if self._fused_for is not cast:
+            self._fused = self.engine.make_cast_step(cast, self._step)
+            self._fused_for = cast
+        lr, b1, b2, eps, wd, t, ils, l2 = hp
+        found = self._fused(lr, b1, b2, eps, wd, t, ils,
+                            found_inf_dev=self._found_out, l2=l2,
+                            max_grad_norm=self.max_grad_norm)
+        if self.max_grad_norm is not None:
+            self.last_grad_norm = self._fused.last_grad_norm
+        return int(found)
+
+    def _step_ranks(self, cast, hp) -> int:
+        import torch
+        comm, world, seg, rank, n = self.comm, self.world, self.seg, self.rank, self.n
+        npc = len(self.pieces)
+        ils = hp[6]
+        clipped = self.max_grad_norm is not None
+        # 1. FP8 cast of every local gradient; each rank's segment of the
+        #    codes to it; every rank's per-tensor scales to every rank
+        cast()
+        comm.all_to_all(self._recv, self._gc_flat, [seg] * world, [seg] * world)
+        comm.all_gather(self._scales_all[:world * n], self._g_scale[:n])
+        self._scales_t[:n].copy_(self._scales_all[:world * n].view(world, n).t())
+        # 2. the FP8 mean of the ranks' shards: pieces' amax, MAX per tensor,
+        #    then the encode (with clipping, the exact sums and found_inf)
+        self._reduce.begin(self._amax_local)
+        self._max_over_ranks(self._amax_local, self._amax_vec)
+        clip = None
+        self._found.zero_()
+        if clipped:
+            self._reduce.finish(self._amax_local, ils, self._limbs_local, self._found)
+            vec = self._limbs_vec
+            vec.zero_()
+            vec[:4 * n].view(n, 4).index_copy_(
+                0, self._piece_t, self._limbs_local[:4 * npc].view(npc, 4))
+            vec[4 * n:].copy_(self._found)
+            comm.all_reduce_sum(vec)
+            self._found.copy_((vec[4 * n:] != 0).to(torch.int32))
+            self.engine.norm_terms_from_limbs(vec[:4 * n], self._amax_vec[:n],
+                                              self.grad_fmt, ils, self._terms[:n])
+            self.engine.clip_coef(self._terms[:n], self.max_grad_norm, self._clip,
+                                  self._norm, self._found)
+            clip = self._clip
+        else:
+            self._reduce.finish(self._amax_local)
+        # 3. the first pass; the maxima and found_inf over ranks
+        found_local = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self._step.begin(hp, clip, found_local, maxima=self._maxima_local)
+        self._found.copy_(torch.maximum(found_local, self._found))
+        self._max_over_ranks(self._maxima_local, self._maxima_vec, parts=2,
+                             flag=self._found)
+        # 4. the update with the whole tensors' maxima; O3: the masters'
+        #    amax over ranks, then the weight copy
+        o3 = self.level == "O3"
+        self._step.finish(hp, clip, self._found, self._found_out,
+                          maxima=self._maxima_local,
+                          master_amax=self._master_local if o3 else None)
+        if o3:
+            self._max_over_ranks(self._master_local, self._master_vec)
+            self._step.copy(self._master_local)
+        # 5. every rank's segment of the new weights to every rank
+        if o3:
+            comm.all_gather(self._w8_flat, self._w8_flat[rank * seg:(rank + 1) * seg])
+            wv = self._w8_vec
+            wv.zero_()
+            if npc:
+                wv[:n].index_copy_(0, self._piece_t, self._w8s_own[:npc].view(torch.int32))
+                wv[n:2 * n].index_copy_(0, self._piece_t,
+                                        self._w8a_own[:npc].view(torch.int32))
+            comm.all_reduce_max(wv)
+            self.w8_scale[:n].copy_(wv[:n].view(torch.float32))
+            self.w8_amax[:n].copy_(wv[n:2 * n].view(torch.float32))
+        else:
+            comm.all_gather(self._w_flat, self._w_flat[rank * seg:(rank + 1) * seg])
+        found = int(self._found_out.item())
+        if clipped:
+            self.last_grad_norm = float(self._norm.item())
         return found

@@ -371,12 +371,16 @@ FP8OPT_API int fp8_adam_step_clipped(const fp8opt_param *params, int n, float lr
 
 /*
  * Sharded steps.  When each of several ranks (one per GPU) owns the optimizer
- * state of a disjoint set of whole tensors (ZeRO-1 style), a step needs one
- * exchange between ranks: found_inf must be combined (every rank skips if any
- * rank saw a non-finite gradient) and, with clipping, the global norm taken
- * over all ranks' tensors.  The calls below split the step at that exchange;
- * the caller runs the collective (e.g. NCCL) between them.  On one rank they
- * give exactly fp8_adamw_step / fp8_adam_step / fp8_adam_step_clipped.
+ * state of a disjoint part of the tensor list (ZeRO-1 style; a tensor may be
+ * cut into element ranges, pieces, on several ranks), a step needs
+ * exchanges between ranks: found_inf must be combined (every rank skips if
+ * any rank saw a non-finite gradient), with clipping the global norm taken
+ * over all ranks' tensors, and for a cut tensor its per-tensor maxima
+ * (the amax of the new first moment, max |g|, the new master's amax)
+ * combined over its pieces.  The calls below split the step at those
+ * exchanges; the caller runs the collectives (e.g. NCCL) between them.  On
+ * one rank they give exactly fp8_adamw_step / fp8_adam_step /
+ * fp8_adam_step_clipped.
  *
  * fp8_grad_norm_terms: for each of the n records, term_t = fl64(k_t^2 *
  * fl64(S_t)) with S_t the exact sum of squared code values (fp8_grad_norm's
@@ -400,13 +404,32 @@ FP8OPT_API int fp8_adam_step_clipped(const fp8opt_param *params, int n, float lr
  * gradient (GradScaler unscales, and finds any inf, before the norm is
  * clipped), so a gradient that overflows fp32 when unscaled skips the step
  * even where the clip coefficient would bring it back in range.
+ * maxima_out (device uint32[2n], may be NULL): each record's per-tensor
+ * maxima of this step, [0, n) the amax of the new first moment and [n, 2n)
+ * max |g| (0 without a scaled second moment), as fp32 bits (NaN as
+ * 0x7FC00000; the bits of these non-negative values order like the values,
+ * NaN above +inf).
  *
  * fp8_adam_step_finish: the rest of the step (update and O3 weight copy) of
  * the same records, skipped when this rank's found_inf or *found_in_dev (the
  * value combined over ranks; may be NULL) is nonzero; found_dev (may be NULL)
- * receives the combined flag.  It must follow fp8_adam_step_begin on the same
- * stream with the same records and the same hyperparameters, with no other
- * step, cast or norm call on that stream in between; otherwise FP8OPT_ERR_ARG
+ * receives the combined flag.  maxima_in (device uint32[2n], may be NULL):
+ * the maxima to use instead of this rank's own, in maxima_out's layout.  A
+ * record that is a piece of a tensor cut across ranks (an element range, with
+ * the tensor's scales and bound) gives the whole tensor's result on its
+ * elements when maxima_in holds the MAX over the pieces' maxima_out.
+ * master_amax_out (device uint32[n], may be NULL): the amax of each O3
+ * record's new FP16 master (fp32 bits); when it is given the O3 weight copy
+ * does not run here but in fp8_adam_step_copy, which must follow, so that
+ * the pieces' master amax can be combined first.  It must follow
+ * fp8_adam_step_begin on the same stream with the same records and the same
+ * hyperparameters, with no other step, cast or norm call on that stream in
+ * between; otherwise FP8OPT_ERR_ARG and nothing is launched.
+ *
+ * fp8_adam_step_copy: the O3 weight copy of the records of the preceding
+ * fp8_adam_step_finish (called with master_amax_out) from the given master
+ * amax master_amax_in (device uint32[n], fp32 bits: w8_scale = 448 / amax,
+ * with the cast's guards); skipped with the step.  Otherwise FP8OPT_ERR_ARG
  * and nothing is launched.
  *
  * Arguments otherwise as fp8_adamw_step; l2: 0 AdamW, 1 Adam with L2 decay.
@@ -422,14 +445,18 @@ FP8OPT_API int fp8_adam_step_begin(const fp8opt_param *params, int n, float lr,
                                    float beta1, float beta2, float eps, float wd,
                                    int64_t step, float inv_loss_scale, int l2,
                                    const float *clip_dev, uint32_t *found_dev,
-                                   void *stream);
+                                   uint32_t *maxima_out, void *stream);
 FP8OPT_API int fp8_adam_step_finish(const fp8opt_param *params, int n, float lr,
                                     float beta1, float beta2, float eps,
                                     float wd, int64_t step,
                                     float inv_loss_scale, int l2,
                                     const float *clip_dev,
                                     const uint32_t *found_in_dev,
-                                    uint32_t *found_dev, void *stream);
+                                    uint32_t *found_dev,
+                                    const uint32_t *maxima_in,
+                                    uint32_t *master_amax_out, void *stream);
+FP8OPT_API int fp8_adam_step_copy(const fp8opt_param *params, int n,
+                                  const uint32_t *master_amax_in, void *stream);
 
 /* Most shards one fp8_reduce_scaled call takes. */
 #define FP8OPT_MAX_SHARDS 64
@@ -510,6 +537,50 @@ FP8OPT_API int fp8_reduce_scaled_norm(const fp8opt_reduce_item *items, int n,
                                       int k, int in_fmt, int out_fmt, float post,
                                       float inv_loss_scale, double *terms_dev,
                                       uint32_t *found_dev, void *stream);
+
+/*
+ * fp8_reduce_scaled_begin and fp8_reduce_scaled_finish: fp8_reduce_scaled
+ * split at its one per-tensor quantity, the amax of the reduced values, for
+ * a tensor reduced in pieces on several ranks (each rank reduces an element
+ * range of every shard; the MS-AMP "Optimization Level" page's O3 paragraph
+ * names ZeRO, which cuts the optimizer's work across data-parallel ranks).
+ *
+ * begin: the amax pass; amax_bits_dev[i] (device uint32[n]) receives item i's
+ * amax as fp32 bits (NaN as 0x7FC00000; the bits of these non-negative values
+ * order like the values).  The caller combines the pieces of a tensor by MAX
+ * (e.g. an all-reduce of int32 maxima over ranks).
+ *
+ * finish: the encode pass with item i's amax taken from amax_bits_dev[i] (the
+ * combined value): codes, amax and scale exactly as fp8_reduce_scaled writes
+ * them for that amax, so the pieces of a tensor give its whole codes.
+ * limbs_dev (device int64[4n], may be NULL): item i's exact sum of the
+ * squared values of its output codes (fp8_grad_norm_terms' S, units of
+ * 2^-32) as four 32-bit limbs, low first (limbs_dev[4i + j] < 2^32), which a
+ * SUM over fewer than 2^31 ranks keeps exact; with it, found_dev (device
+ * uint32, may be NULL) receives whether some output code times
+ * inv_loss_scale / scale is not finite (the step's test).  found_dev without
+ * limbs_dev is FP8OPT_ERR_ARG.
+ *
+ * fp8_norm_terms_from_limbs: terms_dev[t] (device doubles) = the norm term
+ * fl64(k_t^2 * fl64(S_t * 2^-32)) of tensor t from its limbs (limbs_dev[4t ..
+ * 4t + 3], possibly summed over ranks: each below 2^63, the top one below
+ * 2^32) and k_t = inv_loss_scale / scale_t, scale_t = fp8_max(fmt) / amax_t
+ * with the cast's guards (amax_bits_dev[t]); the terms fp8_clip_coef sums.
+ *
+ * Arguments otherwise as fp8_reduce_scaled / fp8_reduce_scaled_norm.
+ */
+FP8OPT_API int fp8_reduce_scaled_begin(const fp8opt_reduce_item *items, int n,
+                                       int k, int in_fmt, float post,
+                                       uint32_t *amax_bits_dev, void *stream);
+FP8OPT_API int fp8_reduce_scaled_finish(const fp8opt_reduce_item *items, int n,
+                                        int k, int in_fmt, int out_fmt,
+                                        float post, const uint32_t *amax_bits_dev,
+                                        float inv_loss_scale, int64_t *limbs_dev,
+                                        uint32_t *found_dev, void *stream);
+FP8OPT_API int fp8_norm_terms_from_limbs(const int64_t *limbs_dev,
+                                         const uint32_t *amax_bits_dev, int n,
+                                         int fmt, float inv_loss_scale,
+                                         double *terms_dev, void *stream);
 
 /* Text of a status code (static storage). */
 FP8OPT_API const char *fp8opt_strerror(int status);

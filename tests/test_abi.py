@@ -283,3 +283,31 @@ def test_step_state_views_match_the_c_layout(lib):
     assert step == 42 and lr == struct.unpack("<f", struct.pack("<f", 1e-3))[0]
     assert st.step.dtype == torch.int64 and st.lr.dtype == torch.float32
 
+
+
+def test_split_step_and_reduction_argument_errors_need_no_gpu(lib):
+    """The calls that split the reduction and the step for tensors cut
+    across ranks refuse malformed calls before touching the GPU."""
+    L = lib.load()
+    it = (lib.ReduceItem * 1)()
+    assert L.fp8_reduce_scaled_begin(it, 1, 2, 0, 1.0, None, None) == lib.ERR_ARG
+    assert L.fp8_reduce_scaled_begin(it, 0, 2, 0, 1.0, None, None) == lib.OK
+    assert L.fp8_reduce_scaled_begin(it, -1, 2, 0, 1.0, 0x1000, None) == lib.ERR_ARG
+    assert L.fp8_reduce_scaled_finish(it, 1, 2, 0, 0, 1.0, None, 1.0, None, None,
+                                      None) == lib.ERR_ARG        # NULL amax bits
+    assert L.fp8_reduce_scaled_finish(it, 0, 2, 0, 0, 1.0, None, 1.0, None, 0x1000,
+                                      None) == lib.ERR_ARG        # found, no limbs
+    assert L.fp8_reduce_scaled_finish(it, 0, 2, 0, 5, 1.0, None, 1.0, None, None,
+                                      None) == lib.ERR_UNSUPPORTED
+    assert L.fp8_norm_terms_from_limbs(None, None, -1, 0, 1.0, None, None) == lib.ERR_ARG
+    assert L.fp8_norm_terms_from_limbs(None, None, 2, 0, 1.0, None, None) == lib.ERR_ARG
+    assert L.fp8_norm_terms_from_limbs(None, None, 0, 3, 1.0, None, None) == \
+        lib.ERR_UNSUPPORTED
+    assert L.fp8_norm_terms_from_limbs(None, None, 0, 0, 1.0, None, None) == lib.OK
+    p = (lib.Param * 1)()
+    assert L.fp8_adam_step_copy(p, -1, None, None) == lib.ERR_ARG
+    assert L.fp8_adam_step_copy(p, 0, None, None) == lib.OK
+    args = (1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+    assert L.fp8_adam_step_begin(p, 0, *args, 2, None, None, None, None) == lib.ERR_ARG
+    assert L.fp8_adam_step_finish(p, 0, *args, 2, None, None, None, None, None,
+                                  None) == lib.ERR_ARG

@@ -1,8 +1,11 @@
-"""The sharded data-parallel step on 2 CPU ranks over gloo, with the oracle as
-its engine: the tensor partition, the all-to-all of gradient codes and scales,
-the FP8 mean of the ranks' shards, found_inf combined over ranks, the global
-clip norm and the owners' weight broadcasts give, on every rank, the result of
-the same pipeline run whole in one process, bit for bit."""
+"""The sharded data-parallel step on CPU ranks over gloo, with the oracle as
+its engine: the element-space layout (tensors cut into pieces across ranks),
+the all-to-all of gradient codes, the all-gather of scales, the FP8 mean of the
+ranks' shards with each tensor's amax combined over its pieces, found_inf
+combined over ranks, the global clip norm from exact sums combined over
+ranks, the first moment's and the master's maxima combined over pieces, and
+the all-gather of the new weights give, on every rank, the result of the same
+pipeline run whole in one process, bit for bit."""
 import os
 import socket
 import sys
@@ -55,18 +58,17 @@ def worker(rank, world, port, cfg, out_dir):
     for t in range(1, cfg["steps"] + 1):
         found.append(opt.step(local_grads(wl, t, rank, cfg["inf_at"])))
         norms.append(opt.last_grad_norm if cfg["max_norm"] is not None else 0.0)
-    out = {"found": np.array(found), "norms": np.array(norms),
-           "ranges": np.array(opt.ranges)}
+    out = {"found": np.array(found), "norms": np.array(norms)}
     for i, w in enumerate(opt.weights):
         out[f"w{i}"] = w.view(torch.int16).numpy().copy()
     if cfg["level"] == "O3":
         out["w8_scale"] = opt.w8_scale.numpy().copy()
         for i, c in enumerate(opt.w8):
             out[f"w8_{i}"] = c.numpy().copy()
-    lo, hi = opt.own
-    for j in range(hi - lo):
-        out[f"m{lo + j}"] = opt.m[j].numpy().copy()
-        out[f"v{lo + j}"] = opt.v[j].view(torch.int16).numpy().copy()
+    out["pieces"] = np.array(opt.pieces, dtype=np.int64).reshape(-1, 3)
+    for j in range(len(opt.pieces)):
+        out[f"m_{j}"] = opt.m[j].numpy().copy()
+        out[f"v_{j}"] = opt.v[j].view(torch.int16).numpy().copy()
     np.savez(os.path.join(out_dir, f"rank{rank}.npz"), **out)
     dist.destroy_process_group()
 
@@ -92,10 +94,13 @@ def reference(cfg, world=2):
                 cs.append((c, s))
             casts.append(cs)
         for i in range(n):
-            codes, _, sc = oracle.reduce_scaled(
-                np.stack([casts[r][i][0] for r in range(world)]),
-                np.array([casts[r][i][1] for r in range(world)], np.float32),
-                oracle.E4M3, oracle.E4M3, 1.0 / world)
+            if world == 1:        # one rank: its cast feeds the step
+                codes, sc = casts[0][i]
+            else:
+                codes, _, sc = oracle.reduce_scaled(
+                    np.stack([casts[r][i][0] for r in range(world)]),
+                    np.array([casts[r][i][1] for r in range(world)], np.float32),
+                    oracle.E4M3, oracle.E4M3, 1.0 / world)
             states[i].g, states[i].g_scale = codes, float(sc)
         hp = (wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, step + 1, 1.0)
         if cfg["max_norm"] is not None:
@@ -122,7 +127,8 @@ CASES = {
 
 
 @pytest.mark.parametrize("case,world", [(c, 2) for c in sorted(CASES)] +
-                         [("o3_clip", 3), ("o3_clip", 4)])
+                         [("o3_clip", 1), ("o2", 1), ("o3_clip", 3),
+                          ("o3_clip", 4), ("o2_l2_scaled_v_clip", 4)])
 def test_cpu_ranks_match_the_whole_pipeline(case, world, tmp_path):
     import torch.multiprocessing as mp
     cfg = CASES[case]
@@ -140,44 +146,65 @@ def test_cpu_ranks_match_the_whole_pipeline(case, world, tmp_path):
             else:
                 assert np.array_equal(res[r][f"w8_{i}"], st.w8), (r, i)
                 assert res[r]["w8_scale"][i] == st.w8_scale[0]
-            if f"m{i}" in res[r]:
-                assert np.array_equal(res[r][f"m{i}"], st.m), (r, i)
-                assert np.array_equal(res[r][f"v{i}"].view(np.uint16), st.v), (r, i)
-                if cfg["level"] == "O3":
-                    assert np.array_equal(res[r][f"w{i}"].view(np.uint16), st.w)
-    # each tensor owned by exactly one rank, and every rank owns some
-    owned = [k for r in range(world) for k in res[r] if k.startswith("m")]
-    assert sorted(owned) == sorted(f"m{i}" for i in range(len(wl.shapes)))
-    assert all(any(k.startswith("m") for k in res[r]) for r in range(world))
+        for j, (t, a, b) in enumerate(res[r]["pieces"]):
+            st = states[t]
+            assert np.array_equal(res[r][f"m_{j}"], st.m[a:b]), (r, t)
+            assert np.array_equal(res[r][f"v_{j}"].view(np.uint16), st.v[a:b]), (r, t)
+            if cfg["level"] == "O3":       # the masters of the rank's pieces
+                assert np.array_equal(res[r][f"w{t}"].view(np.uint16)[a:b], st.w[a:b])
+    # every element owned by exactly one rank; some tensor cut across ranks
+    owner = {}
+    for r in range(world):
+        for t, a, b in res[r]["pieces"]:
+            owner.setdefault(int(t), []).append((int(a), int(b), r))
+    assert sorted(owner) == list(range(len(wl.shapes)))
+    for t, parts in owner.items():
+        parts.sort()
+        assert parts[0][0] == 0 and parts[-1][1] == wl.numels[t]
+        assert all(x[1] == y[0] for x, y in zip(parts, parts[1:]))
+    if world > 1:
+        assert any(len({r for *_, r in p}) > 1 for p in owner.values())
     if cfg["inf_at"] is not None:
         assert found[cfg["inf_at"][0] - 1] == 1 and sum(found) == 1
 
 
-def test_partition_is_balanced_and_contiguous():
-    from bit_optimizer_gb300.sharded import partition
+def test_layout_covers_every_element_once_and_balances():
+    from bit_optimizer_gb300.sharded import layout
     rng = np.random.default_rng(0)
-    for _ in range(200):
+    for _ in range(300):
         n = int(rng.integers(0, 40))
         numels = [int(x) for x in rng.integers(0, 10000, n)]
+        numels = [0 if rng.random() < 0.1 else x for x in numels]
         world = int(rng.integers(1, 9))
-        parts = partition(numels, world)
-        assert len(parts) == world
-        assert parts[0][0] == 0 and parts[-1][1] == n
-        for (a, b), (c, d) in zip(parts, parts[1:]):
-            assert b == c and a <= b
-        w = [max(x, 1) for x in numels]
-        best = max(sum(w[a:b]) for a, b in parts) if n else 0
-        # no contiguous split does better: brute force on small lists
-        if n <= 8:
-            import itertools
-            opt = None
-            for cuts in itertools.combinations_with_replacement(range(n + 1), world - 1):
-                bounds = [0, *cuts, n]
-                if any(x > y for x, y in zip(bounds, bounds[1:])):
-                    continue
-                m = max(sum(w[x:y]) for x, y in zip(bounds, bounds[1:]))
-                opt = m if opt is None else min(opt, m)
-            assert best == opt
+        off, seg, pieces = layout(numels, world)
+        assert len(pieces) == world and seg % 256 == 0
+        seen = {t: [] for t in range(n)}
+        for r, ps in enumerate(pieces):
+            for t, a, b in ps:
+                assert 0 <= a <= b <= numels[t] and a % 256 == 0
+                # inside the rank's range of the element space
+                assert r * seg <= off[t] + a and (b == a or off[t] + b <= (r + 1) * seg)
+                seen[t].append((a, b))
+            assert sum(b - a for _, a, b in ps) <= seg
+        for t in range(n):
+            parts = sorted(seen[t])
+            assert parts and parts[0][0] == 0 and parts[-1][1] == numels[t]
+            assert all(x[1] == y[0] for x, y in zip(parts, parts[1:]))
+            assert numels[t] > 0 or parts == [(0, 0)]
+        # offsets: in order, 256-element aligned, no overlap
+        for t in range(n - 1):
+            assert off[t] % 256 == 0 and off[t] + numels[t] <= off[t + 1]
+
+
+def test_layout_balance_on_the_350m_list_at_8_ranks():
+    """Equal segments: the busiest of 8 ranks holds at most 1.02x its share
+    of the 350M list's elements (whole tensors put wte's 51.5 M elements on
+    one rank: 1.158x)."""
+    from bit_optimizer_gb300.sharded import layout
+    wl = synth.o2_350m()
+    _, _, pieces = layout(wl.numels, 8)
+    loads = [sum(b - a for _, a, b in p) for p in pieces]
+    assert max(loads) <= 1.02 * sum(wl.numels) / 8
 
 
 class FailingEngine:
