@@ -509,6 +509,77 @@ def record_traffic(csv_path, wl, command):
     return rec
 
 
+# ------------------------------------------------------------- host side
+
+def device_host_numa_node(device_index):
+    """The host NUMA node closest to the GPU (cudaDevAttrHostNumaId), or
+    None when the runtime cannot say."""
+    import ctypes
+    for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+            break
+        except OSError:
+            continue
+    else:
+        return None
+    v = ctypes.c_int(-1)
+    if rt.cudaDeviceGetAttribute(ctypes.byref(v), 134, device_index) != 0:
+        return None
+    return v.value if v.value >= 0 else None
+
+
+def node_cpus(node):
+    """CPUs of a NUMA node that this process may run on (empty if unknown)."""
+    try:
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            text = f.read().strip()
+    except OSError:
+        return set()
+    cpus = set()
+    for part in filter(None, text.split(",")):
+        a, _, b = part.partition("-")
+        cpus.update(range(int(a), int(b or a) + 1))
+    return cpus & os.sched_getaffinity(0)
+
+
+def pinned_on_node(shape, dtype, node):
+    """A pinned host tensor allocated while this process runs on the CPUs of
+    NUMA node `node` (the default memory policy then places its pages
+    there), and the pages per node it actually got."""
+    import torch
+    cpus = node_cpus(node) if node is not None else set()
+    saved = os.sched_getaffinity(0)
+    if cpus:
+        os.sched_setaffinity(0, cpus)
+    try:
+        t = torch.empty(shape, dtype=dtype, pin_memory=True)
+        t.view(torch.uint8).zero_()               # touch every page
+    finally:
+        os.sched_setaffinity(0, saved)
+    return t, pages_by_node(t.data_ptr())
+
+
+def pages_by_node(addr):
+    """{node: pages} of the mapping that holds `addr`, from
+    /proc/self/maps and /proc/self/numa_maps (None if unreadable)."""
+    try:
+        with open("/proc/self/maps") as f:
+            start = next(int(a, 16) for a, b in
+                         (ln.split()[0].split("-") for ln in f)
+                         if int(a, 16) <= addr < int(b, 16))
+        with open("/proc/self/numa_maps") as f:
+            for ln in f:
+                fields = ln.split()
+                if int(fields[0], 16) == start:
+                    return {int(k[1:]): int(v) for k, v in
+                            (x.split("=", 1) for x in fields[2:] if "=" in x)
+                            if k.startswith("N") and k[1:].isdigit()}
+    except (OSError, StopIteration, ValueError):
+        return None
+    return None
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -771,9 +842,24 @@ def run_ours(args, wl):
         # found_inf back to the host.  Two device gradient arenas alternate:
         # step t+1's copy (on its own stream) overlaps step t's kernels, and
         # waits only until the step that last read its arena has finished.
-        host = torch.empty(flat.shape, dtype=flat.dtype, pin_memory=True)
+        numa = device_host_numa_node(local)
+        host, pages = pinned_on_node(flat.shape, flat.dtype, numa)
         host.copy_(flat)
         h2d = host.numel() * host.element_size()
+        # the link alone: one plain copy of the same pinned buffer into the
+        # same device arena, timed with events on a side stream (best of 2)
+        link_ms = None
+        link_stream = torch.cuda.Stream(device)
+        for _ in range(2):
+            la = torch.cuda.Event(enable_timing=True)
+            lb = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(link_stream):
+                la.record(link_stream)
+                flat.copy_(host, non_blocking=True)
+                lb.record(link_stream)
+            link_stream.synchronize()
+            t_ms = la.elapsed_time(lb)
+            link_ms = t_ms if link_ms is None else min(link_ms, t_ms)
         grads2, flat2 = bo.arena_views(wl.numels, wl.grad_dtype, device,
                                        return_base=True)
         bufs = [(grads, flat), (grads2, flat2)]
@@ -818,18 +904,31 @@ def run_ours(args, wl):
             torch.cuda.synchronize()
             return e0.elapsed_time(e1)
 
-        run(2)
+        # warm-up: as many steps as the headline's (at least 2, so that both
+        # arenas have been copied into and stepped)
+        run(max(2, args.warmup))
         barrier()
         k = max(1, args.e2e_steps)
+        e2e_clocks = ClockSampler(local)
+        e2e_clocks.start()
         ems = run(k) / k
         barrier()
+        e2e_clocks.stop()
         if world > 1:
             t = torch.tensor([ems], dtype=torch.float64, device=device)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             ems = float(t.item())
         e2e = {"value": world * n_params / (ems * 1e-3) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4,
-               "ms_per_step": ems, "steps": k}
+               "ms_per_step": ems, "steps": k,
+               # the host link measured alone in this run, and the bound it
+               # sets: the copy plus the device step (the overlapped loop
+               # can only approach the larger of the two)
+               "link_gbs": h2d / (link_ms * 1e-3) / 1e9, "link_copy_ms": link_ms,
+               "copy_plus_step_ms": link_ms + ms,
+               "clocks": e2e_clocks.summary(),
+               "host_buffer": {"device_host_numa_node": numa,
+                               "pages_by_node": pages}}
         del host
 
     cpu = None
@@ -928,16 +1027,22 @@ def run_sharded(args, wl):
     if rank == 0:
         desc = workload_desc(wl)
         desc["step"] = ("sharded data-parallel step: FP8 cast of each rank's "
-                        "gradients, FP8 all-to-all, FP8 mean, owners' step, "
-                        "weight broadcast (NCCL)")
-        lo, hi = opt.own
+                        "gradients, FP8 all-to-all, FP8 mean, owners' step "
+                        "over equal element ranges (tensors cut across ranks), "
+                        "weight all-gather (NCCL); one rank: the fused cast "
+                        "and step")
+        loads = [sum(b - a for _, a, b in p) for p in opt.layout_pieces]
         line = {
             "metric": METRIC, "value": wl.n_params / (ms * 1e-3) / 1e9,
             "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "strong", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": desc,
-            "partition_rank0": [lo, hi, sum(wl.numels[lo:hi])],
+            "shard_elements": {"per_rank_max": max(loads),
+                               "per_rank_mean": sum(loads) / world,
+                               "tensors_cut": sum(1 for t in range(len(wl.numels))
+                                                  if sum(1 for p in opt.layout_pieces
+                                                         for x in p if x[0] == t) > 1)},
             "clocks": sampler.summary(),
         }
         print(json.dumps(line), flush=True)

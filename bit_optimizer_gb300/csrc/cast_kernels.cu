@@ -153,15 +153,19 @@ struct SqOut {
 // Encode this thread's share of [begin, end).  CHECKED when the tensor holds a
 // non-finite element (its amax is not finite): those take the explicit
 // NaN / infinity codes; otherwise every product is finite.  SQ: also add the
-// codes written to acc.
+// exact squares of the codes written to acc (through the table tab) and
+// collect in bad the codes at or above the overflow threshold whose addend
+// is tadd (found_inf of a step with factor inv_loss_scale / scale).
 template <int DT, int FMT, bool CHECKED, bool SQ>
 __device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
                               int64_t end, bool vec, float scale,
-                              SqAcc<FMT>& acc) {
+                              const SqTable* tab, uint32_t tadd, SqTab& acc,
+                              uint32_t& bad) {
   constexpr int kEncGroups = SQ ? FP8OPT_ENCSQ_GROUPS : FP8OPT_ENC_GROUPS;
   constexpr int64_t kTile = (int64_t)kThreads * kGroup * kEncGroups;
   constexpr uint32_t kSrcBytes = DT == kF32 ? 4 : 2;
   const int tid = threadIdx.x;
+  const uint32_t lb = sq_lane_byte<FMT>();
   const bool pf = FP8OPT_ENC_PREFETCH > 0 && tid == 0 && vec && aligned16(src);
   for (int64_t base = begin; base < end; base += kTile) {
     if (pf) {
@@ -183,8 +187,10 @@ __device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
         const uint2 c = enc8<FMT, CHECKED>(x[k]);
         *reinterpret_cast<uint2*>(codes + i0) = c;
         if (SQ) {
-          acc.add_word(c.x);
-          acc.add_word(c.y);
+          const uint32_t a = c.x & 0x7F7F7F7Fu, b = c.y & 0x7F7F7F7Fu;
+          bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
+          acc.add_word<FMT>(a, lb, *tab);
+          acc.add_word<FMT>(b, lb, *tab);
         }
       }
     } else {
@@ -199,8 +205,10 @@ __device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
           const uint2 c = enc8<FMT, CHECKED>(x);
           *reinterpret_cast<uint2*>(codes + i0) = c;
           if (SQ) {
-            acc.add_word(c.x);
-            acc.add_word(c.y);
+            const uint32_t a = c.x & 0x7F7F7F7Fu, b = c.y & 0x7F7F7F7Fu;
+            bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
+            acc.add_word<FMT>(a, lb, *tab);
+            acc.add_word<FMT>(b, lb, *tab);
           }
         } else {
           for (int j = 0; j < kGroup; ++j) {
@@ -210,7 +218,10 @@ __device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
             const uint32_t c = CHECKED ? enc1_checked<FMT>(t)
                                        : (enc2<FMT>(t, 0.0f) & 0xFFu);
             codes[i] = (uint8_t)c;
-            if (SQ) acc.add_word(c);
+            if (SQ) {
+              bad |= ((c & 0x7Fu) + tadd) & 0x80u;
+              acc.add_word<FMT>(c & 0x7Fu, lb, *tab);
+            }
           }
         }
       }
@@ -222,12 +233,16 @@ template <int DT, int FMT, bool SQ>
 __device__ __forceinline__ void encode_dispatch(const CastDesc& d,
                                                 int64_t begin, int64_t end,
                                                 float scale, bool checked,
-                                                SqAcc<FMT>& acc) {
+                                                const SqTable* tab,
+                                                uint32_t tadd, SqTab& acc,
+                                                uint32_t& bad) {
   const bool vec = d.vec_ok != 0;
   if (checked)
-    thread_encode<DT, FMT, true, SQ>(d.src, d.codes, begin, end, vec, scale, acc);
+    thread_encode<DT, FMT, true, SQ>(d.src, d.codes, begin, end, vec, scale, tab,
+                                     tadd, acc, bad);
   else
-    thread_encode<DT, FMT, false, SQ>(d.src, d.codes, begin, end, vec, scale, acc);
+    thread_encode<DT, FMT, false, SQ>(d.src, d.codes, begin, end, vec, scale, tab,
+                                      tadd, acc, bad);
 }
 
 // One chunk-strided encode pass (SQ: with the exact squares of the codes).
@@ -237,8 +252,8 @@ __device__ __forceinline__ void encode_pass(const CastDesc* __restrict__ descs,
                                             uint32_t nchunks,
                                             const unsigned long long* __restrict__ slots,
                                             uint32_t epoch, const SqOut& sq,
-                                            unsigned long long* red64,
-                                            uint32_t* red32) {
+                                            const SqTable* tab,
+                                            unsigned long long* red64) {
   for (uint32_t r = blockIdx.x; r < nchunks; r += gridDim.x) {
     const Chunk ch = chunks[nchunks - 1 - r];
     const CastDesc d = descs[ch.tensor];
@@ -251,17 +266,20 @@ __device__ __forceinline__ void encode_pass(const CastDesc* __restrict__ descs,
     const int64_t begin = ch.begin;
     const int64_t end = begin + ch.len;
     const bool checked = ab >= 0x7F800000u;
-    SqAcc<FMT> acc;
+    SqTab acc;
+    uint32_t bad = 0, tadd = 0;
+    if (SQ)   // found_inf as the step decides it, from its factor
+      tadd = threshold_addend(overflow_threshold<FMT>(
+          __fdiv_rn(sq.ils_dev != nullptr ? *sq.ils_dev : sq.ils, scale)));
     if (d.dtype == kF32)
-      encode_dispatch<kF32, FMT, SQ>(d, begin, end, scale, checked, acc);
+      encode_dispatch<kF32, FMT, SQ>(d, begin, end, scale, checked, tab, tadd, acc, bad);
     else if (d.dtype == kBF16)
-      encode_dispatch<kBF16, FMT, SQ>(d, begin, end, scale, checked, acc);
+      encode_dispatch<kBF16, FMT, SQ>(d, begin, end, scale, checked, tab, tadd, acc, bad);
     else
-      encode_dispatch<kF16, FMT, SQ>(d, begin, end, scale, checked, acc);
+      encode_dispatch<kF16, FMT, SQ>(d, begin, end, scale, checked, tab, tadd, acc, bad);
     if (SQ)
-      sq_commit<FMT>(acc, ch.tensor, end > begin,
-                     __fdiv_rn(sq.ils_dev != nullptr ? *sq.ils_dev : sq.ils, scale),
-                     sq.sums, sq.found, epoch, red64, red32);
+      sq_commit_flag(acc, ch.tensor, end > begin, bad, sq.sums, sq.found, epoch,
+                     red64);
   }
 }
 
@@ -276,17 +294,19 @@ cast_encode_kernel(const CastDesc* __restrict__ descs,
                           nullptr);
 }
 
-// The encode pass with the exact squares (its sums and the found_inf test
-// need more registers; four CTAs per SM keep it free of spills).
+// The encode pass with the exact squares, read from the shared-memory table
+// of the integer square roots (SqTable; its sums and the found_inf test need
+// more registers; four CTAs per SM keep it free of spills).
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, FP8OPT_ENCSQ_MIN_BLOCKS)
 cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
                       const Chunk* __restrict__ chunks, uint32_t nchunks,
                       const unsigned long long* __restrict__ slots,
                       uint32_t epoch, SqOut sq) {
+  __shared__ SqTable tab;
   __shared__ unsigned long long red64[2 * (kThreads / 32)];
-  __shared__ uint32_t red32[kThreads / 32];
-  encode_pass<FMT, true>(descs, chunks, nchunks, slots, epoch, sq, red64, red32);
+  sq_table_fill(tab);
+  encode_pass<FMT, true>(descs, chunks, nchunks, slots, epoch, sq, &tab, red64);
 }
 
 }  // namespace

@@ -23,16 +23,20 @@ namespace fp8opt {
 namespace {
 
 // 8-code groups per thread per tile, and resident CTAs per SM of the norm
-// pass (each CTA holds the 32 KB table of the exact squares).
+// pass (each CTA holds the 32 KB table of the exact squares).  The pass is
+// bound by memory latency, so more bytes in flight per thread pay: measured
+// on the 6.7B list, 1.420 ms with sixteen groups at 4 CTAs/SM (63
+// registers), 1.449 with eight at 5 (48 registers).
 #ifndef FP8OPT_NORM_GROUPS
-#define FP8OPT_NORM_GROUPS 8
+#define FP8OPT_NORM_GROUPS 16
 #endif
 #ifndef FP8OPT_NORM_MIN_BLOCKS
-#define FP8OPT_NORM_MIN_BLOCKS 5
+#define FP8OPT_NORM_MIN_BLOCKS 4
 #endif
 // Tiles ahead of the current one that one thread of the CTA asks L2 for
 // (cp.async.bulk.prefetch.L2; 0: none).  A CTA walks one contiguous range of
 // the chunk table, so the next tiles are the next bytes of its range.
+// Measured slower (one tile ahead: 1.461 ms, two: 1.545 on the 6.7B list).
 #ifndef FP8OPT_NORM_PREFETCH
 #define FP8OPT_NORM_PREFETCH 0
 #endif
@@ -67,9 +71,18 @@ __device__ void thread_norm(const uint8_t* g, int64_t begin, int64_t end,
         acc.add_word<GF>(b, lb, tab);
       }
     } else {
+      // a partial tile: whole 8-code groups as vectors, the rest by code
 #pragma unroll 1
       for (int q = 0; q < kNormGroups; ++q) {
         const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
+        if (vec && i0 + kGroup <= end) {
+          const uint2 c = ld_once2(g + i0);
+          const uint32_t a = c.x & 0x7F7F7F7Fu, b = c.y & 0x7F7F7F7Fu;
+          bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
+          acc.add_word<GF>(a, lb, tab);
+          acc.add_word<GF>(b, lb, tab);
+          continue;
+        }
         for (int e = 0; e < kGroup; ++e) {
           const int64_t i = i0 + e;
           if (i >= end) break;
