@@ -65,6 +65,9 @@ def parse():
                    help="override the workload's layer count (profiling cases)")
     p.add_argument("--vocab", type=int, default=None,
                    help="override the workload's vocabulary (profiling cases)")
+    p.add_argument("--grad-fmt", default=None, choices=["e4m3", "e5m2"],
+                   help="override the workload's gradient code format "
+                        "(profiling case)")
     p.add_argument("--max-grad-norm", type=float, default=None,
                    help="clip the headline step to this global gradient norm "
                         "(fp8_cast_adam_step_clipped; profiling case)")
@@ -872,15 +875,18 @@ def run_ours(args, wl):
         clip = {"max_grad_norm": opt.max_grad_norm} if clip_kw else {}
 
         def run(k):
-            """k steps; returns their milliseconds between CUDA events: the
-            first copy's start on the copy stream and the last step's end."""
+            """k steps; returns their milliseconds between CUDA events (the
+            first copy's start on the copy stream and the last step's end)
+            and each step's copy duration on the copy stream."""
             copied = [torch.cuda.Event(), torch.cuda.Event()]
             done = [torch.cuda.Event(), torch.cuda.Event()]
-            e0 = torch.cuda.Event(enable_timing=True)
+            c0 = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+            c1 = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
             e1 = torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(copy_stream):
-                e0.record(copy_stream)
+                c0[0].record(copy_stream)
                 bufs[0][1].copy_(host, non_blocking=True)
+                c1[0].record(copy_stream)
                 copied[0].record(copy_stream)
             for t in range(k):
                 b, nb = t % 2, (t + 1) % 2
@@ -888,7 +894,9 @@ def run_ours(args, wl):
                     with torch.cuda.stream(copy_stream):
                         if t >= 1:
                             copy_stream.wait_event(done[nb])
+                        c0[t + 1].record(copy_stream)
                         bufs[nb][1].copy_(host, non_blocking=True)
+                        c1[t + 1].record(copy_stream)
                         copied[nb].record(copy_stream)
                 s = streams[b]
                 s.wait_event(copied[b])
@@ -902,7 +910,8 @@ def run_ours(args, wl):
                     raise RuntimeError("found_inf set on a finite workload")
             e1.record(streams[(k - 1) % 2])
             torch.cuda.synchronize()
-            return e0.elapsed_time(e1)
+            return (c0[0].elapsed_time(e1),
+                    [c0[t].elapsed_time(c1[t]) for t in range(k)])
 
         # warm-up: as many steps as the headline's (at least 2, so that both
         # arenas have been copied into and stepped)
@@ -911,7 +920,8 @@ def run_ours(args, wl):
         k = max(1, args.e2e_steps)
         e2e_clocks = ClockSampler(local)
         e2e_clocks.start()
-        ems = run(k) / k
+        total_ms, copies_ms = run(k)
+        ems = total_ms / k
         barrier()
         e2e_clocks.stop()
         if world > 1:
@@ -926,6 +936,10 @@ def run_ours(args, wl):
                # can only approach the larger of the two)
                "link_gbs": h2d / (link_ms * 1e-3) / 1e9, "link_copy_ms": link_ms,
                "copy_plus_step_ms": link_ms + ms,
+               # the same copies inside the loop: a shared host link shows
+               # here as copies far slower than link_copy_ms
+               "loop_copy_ms": {"median": statistics.median(copies_ms),
+                                "min": min(copies_ms), "max": max(copies_ms)},
                "clocks": e2e_clocks.summary(),
                "host_buffer": {"device_host_numa_node": numa,
                                "pages_by_node": pages}}
@@ -1071,6 +1085,8 @@ def main():
     # a timed step must be a full update: a workload that seeds an inf (the
     # GradScaler skip case) is timed with that element cleared
     wl = dataclasses.replace(wl, inf_site=None)
+    if args.grad_fmt is not None:
+        wl = dataclasses.replace(wl, grad_fmt=args.grad_fmt)
     if args.record_traffic is not None:
         print(json.dumps(record_traffic(args.record_traffic, wl,
                                         args.capture_command)), flush=True)

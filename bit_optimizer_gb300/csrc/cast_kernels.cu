@@ -245,15 +245,15 @@ __device__ __forceinline__ void encode_dispatch(const CastDesc& d,
                                       tadd, acc, bad);
 }
 
-// One chunk-strided encode pass (SQ: with the exact squares of the codes).
-template <int FMT, bool SQ>
+// One chunk-strided encode pass.
+template <int FMT>
 __device__ __forceinline__ void encode_pass(const CastDesc* __restrict__ descs,
                                             const Chunk* __restrict__ chunks,
                                             uint32_t nchunks,
                                             const unsigned long long* __restrict__ slots,
-                                            uint32_t epoch, const SqOut& sq,
-                                            const SqTable* tab,
-                                            unsigned long long* red64) {
+                                            uint32_t epoch) {
+  SqTab acc;          // unused without squares
+  uint32_t bad = 0;
   for (uint32_t r = blockIdx.x; r < nchunks; r += gridDim.x) {
     const Chunk ch = chunks[nchunks - 1 - r];
     const CastDesc d = descs[ch.tensor];
@@ -266,20 +266,15 @@ __device__ __forceinline__ void encode_pass(const CastDesc* __restrict__ descs,
     const int64_t begin = ch.begin;
     const int64_t end = begin + ch.len;
     const bool checked = ab >= 0x7F800000u;
-    SqTab acc;
-    uint32_t bad = 0, tadd = 0;
-    if (SQ)   // found_inf as the step decides it, from its factor
-      tadd = threshold_addend(overflow_threshold<FMT>(
-          __fdiv_rn(sq.ils_dev != nullptr ? *sq.ils_dev : sq.ils, scale)));
     if (d.dtype == kF32)
-      encode_dispatch<kF32, FMT, SQ>(d, begin, end, scale, checked, tab, tadd, acc, bad);
+      encode_dispatch<kF32, FMT, false>(d, begin, end, scale, checked, nullptr, 0,
+                                        acc, bad);
     else if (d.dtype == kBF16)
-      encode_dispatch<kBF16, FMT, SQ>(d, begin, end, scale, checked, tab, tadd, acc, bad);
+      encode_dispatch<kBF16, FMT, false>(d, begin, end, scale, checked, nullptr, 0,
+                                         acc, bad);
     else
-      encode_dispatch<kF16, FMT, SQ>(d, begin, end, scale, checked, tab, tadd, acc, bad);
-    if (SQ)
-      sq_commit_flag(acc, ch.tensor, end > begin, bad, sq.sums, sq.found, epoch,
-                     red64);
+      encode_dispatch<kF16, FMT, false>(d, begin, end, scale, checked, nullptr, 0,
+                                        acc, bad);
   }
 }
 
@@ -289,14 +284,122 @@ cast_encode_kernel(const CastDesc* __restrict__ descs,
                    const Chunk* __restrict__ chunks, uint32_t nchunks,
                    const unsigned long long* __restrict__ slots,
                    uint32_t epoch) {
-  const SqOut none = {nullptr, nullptr, 0.0f, nullptr};
-  encode_pass<FMT, false>(descs, chunks, nchunks, slots, epoch, none, nullptr,
-                          nullptr);
+  encode_pass<FMT>(descs, chunks, nchunks, slots, epoch);
 }
 
-// The encode pass with the exact squares, read from the shared-memory table
-// of the integer square roots (SqTable; its sums and the found_inf test need
-// more registers; four CTAs per SM keep it free of spills).
+// ------------------------------------ encode pass with the exact squares
+//
+// A full chunk of 16-bit elements (kChunkElems of them, vector loads, a
+// finite amax) is encoded as four tiles of kEncSqGroups 8-element groups per
+// thread, each tile's loads issued one tile ahead of its arithmetic (the
+// next chunk's first tile while this chunk's last is encoded), so that a
+// thread always has a tile in flight.  Other chunks take thread_encode, and
+// so do all chunks of E5M2 codes: their 128-bit sums leave too few registers
+// for two tiles in flight at four CTAs per SM.  A CTA's exact sum goes to
+// its tensor's slot when the next chunk it takes belongs to another tensor.
+constexpr int kEncSqGroups = FP8OPT_ENCSQ_GROUPS;
+constexpr int64_t kEncSqTile = (int64_t)kThreads * kGroup * kEncSqGroups;
+static_assert(kChunkElems % kEncSqTile == 0 && kChunkElems / kEncSqTile == 4,
+              "a full chunk is four tiles");
+
+struct EncTile {
+  uint4 h[kEncSqGroups];   // 8 16-bit elements per group
+};
+
+__device__ __forceinline__ void load_enc_tile(EncTile& t, const uint16_t* p) {
+#pragma unroll
+  for (int q = 0; q < kEncSqGroups; ++q)
+    t.h[q] = ld_once4(p + q * (kThreads * kGroup) + threadIdx.x * kGroup);
+}
+
+// Encodes a loaded tile (16-bit type DT, finite scale products) to codes at
+// c (the tile's first code), adding the exact squares to acc and the codes
+// at or above the overflow threshold (addend tadd) to bad.
+template <int DT, int FMT>
+__device__ __forceinline__ void enc_tile(const EncTile& t, uint8_t* c,
+                                         float scale, const SqTable& tab,
+                                         uint32_t tadd, SqTab& acc,
+                                         uint32_t& bad) {
+  const uint32_t lb = sq_lane_byte<FMT>();
+#pragma unroll
+  for (int q = 0; q < kEncSqGroups; ++q) {
+    float x[8];
+    if (DT == kF16) {
+      h8_to_f(t.h[q], x);
+    } else {
+      const uint32_t w[4] = {t.h[q].x, t.h[q].y, t.h[q].z, t.h[q].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[2 * j] = __uint_as_float(w[j] << 16);
+        x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = __fmul_rn(x[j], scale);
+    const uint2 code = enc8<FMT, false>(x);
+    *reinterpret_cast<uint2*>(c + q * (kThreads * kGroup) + threadIdx.x * kGroup) = code;
+    const uint32_t a = code.x & 0x7F7F7F7Fu, b = code.y & 0x7F7F7F7Fu;
+    bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
+    acc.add_word<FMT>(a, lb, tab);
+    acc.add_word<FMT>(b, lb, tab);
+  }
+}
+
+template <int FMT>
+__device__ __forceinline__ void enc_tile_dt(const EncTile& t, int dtype,
+                                            uint8_t* c, float scale,
+                                            const SqTable& tab, uint32_t tadd,
+                                            SqTab& acc, uint32_t& bad) {
+  if (dtype == kF16)
+    enc_tile<kF16, FMT>(t, c, scale, tab, tadd, acc, bad);
+  else
+    enc_tile<kBF16, FMT>(t, c, scale, tab, tadd, acc, bad);
+}
+
+// What the pass needs of a chunk, its tensor and the tensor's amax.
+struct EncChunk {
+  const void* src;
+  uint8_t* codes;
+  float* amax_out;
+  float* scale_out;
+  int64_t begin;
+  uint32_t len, tensor, ab;
+  int dtype;
+  bool vec;
+
+  // encoded by the tile pipeline
+  __device__ __forceinline__ bool tiled() const {
+    return vec && dtype != kF32 && len == (uint32_t)kChunkElems &&
+           ab < 0x7F800000u;
+  }
+  __device__ __forceinline__ const uint16_t* tile(int i) const {
+    return static_cast<const uint16_t*>(src) + begin + i * kEncSqTile;
+  }
+};
+
+__device__ __forceinline__ EncChunk enc_chunk(const CastDesc* descs,
+                                              const Chunk* chunks, uint32_t c,
+                                              const unsigned long long* slots,
+                                              uint32_t epoch) {
+  const Chunk ch = chunks[c];
+  const CastDesc& d = descs[ch.tensor];
+  EncChunk r;
+  r.src = d.src;
+  r.codes = d.codes;
+  r.amax_out = d.amax_out;
+  r.scale_out = d.scale_out;
+  r.begin = ch.begin;
+  r.len = ch.len;
+  r.tensor = ch.tensor;
+  r.ab = slot_value(slots[ch.tensor], epoch);
+  r.dtype = d.dtype;
+  r.vec = d.vec_ok != 0;
+  return r;
+}
+
+// The encode pass with the exact squares through the shared-memory table of
+// the integer square roots (SqTable).  It walks the chunk table backwards in
+// CTA strides, as the plain encode pass does.
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, FP8OPT_ENCSQ_MIN_BLOCKS)
 cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
@@ -305,8 +408,68 @@ cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
                       uint32_t epoch, SqOut sq) {
   __shared__ SqTable tab;
   __shared__ unsigned long long red64[2 * (kThreads / 32)];
+  if (blockIdx.x >= nchunks) return;   // uniform over the CTA
+  const float ils = sq.ils_dev != nullptr ? *sq.ils_dev : sq.ils;
+  constexpr bool kTiles = FMT == kE4M3;
+  uint32_t r = blockIdx.x;
+  EncChunk cur = enc_chunk(descs, chunks, nchunks - 1 - r, slots, epoch);
+  EncTile ta, tb;   // ta holds the current chunk's first tile if tiled
+  if (kTiles && cur.tiled()) load_enc_tile(ta, cur.tile(0));
   sq_table_fill(tab);
-  encode_pass<FMT, true>(descs, chunks, nchunks, slots, epoch, sq, &tab, red64);
+  SqTab acc;
+  uint32_t bad = 0, tadd = 0, tensor = 0xFFFFFFFFu;
+  bool nonempty = false;
+  float scale = 1.0f;
+  for (; r < nchunks; r += gridDim.x) {
+    const bool more = r + gridDim.x < nchunks;
+    EncChunk nxt = cur;
+    if (more) nxt = enc_chunk(descs, chunks, nchunks - 1 - (r + gridDim.x), slots, epoch);
+    if (cur.tensor != tensor) {   // uniform over the CTA
+      if (tensor != 0xFFFFFFFFu) {
+        sq_commit_flag(acc, tensor, nonempty, bad, sq.sums, sq.found, epoch, red64);
+        acc = SqTab();
+        bad = 0;
+        nonempty = false;
+      }
+      tensor = cur.tensor;
+      scale = scale_from_amax_bits(cur.ab, fp8_max_of<FMT>());
+      // found_inf as the step decides it, from its factor
+      tadd = threshold_addend(overflow_threshold<FMT>(__fdiv_rn(ils, scale)));
+    }
+    if (cur.begin == 0 && threadIdx.x == 0) {
+      *cur.amax_out = __uint_as_float(cur.ab);
+      *cur.scale_out = scale;
+    }
+    nonempty |= cur.len > 0;
+    const bool next_tiled = kTiles && more && nxt.tiled();
+    if (kTiles && cur.tiled()) {
+      uint8_t* c = cur.codes + cur.begin;
+      load_enc_tile(tb, cur.tile(1));
+      enc_tile_dt<FMT>(ta, cur.dtype, c, scale, tab, tadd, acc, bad);
+      load_enc_tile(ta, cur.tile(2));
+      enc_tile_dt<FMT>(tb, cur.dtype, c + kEncSqTile, scale, tab, tadd, acc, bad);
+      load_enc_tile(tb, cur.tile(3));
+      enc_tile_dt<FMT>(ta, cur.dtype, c + 2 * kEncSqTile, scale, tab, tadd, acc, bad);
+      if (next_tiled) load_enc_tile(ta, nxt.tile(0));
+      enc_tile_dt<FMT>(tb, cur.dtype, c + 3 * kEncSqTile, scale, tab, tadd, acc, bad);
+    } else {
+      if (next_tiled) load_enc_tile(ta, nxt.tile(0));
+      const CastDesc d = descs[cur.tensor];
+      const int64_t end = cur.begin + cur.len;
+      const bool checked = cur.ab >= 0x7F800000u;
+      if (d.dtype == kF32)
+        encode_dispatch<kF32, FMT, true>(d, cur.begin, end, scale, checked, &tab,
+                                         tadd, acc, bad);
+      else if (d.dtype == kBF16)
+        encode_dispatch<kBF16, FMT, true>(d, cur.begin, end, scale, checked, &tab,
+                                          tadd, acc, bad);
+      else
+        encode_dispatch<kF16, FMT, true>(d, cur.begin, end, scale, checked, &tab,
+                                         tadd, acc, bad);
+    }
+    cur = nxt;
+  }
+  sq_commit_flag(acc, tensor, nonempty, bad, sq.sums, sq.found, epoch, red64);
 }
 
 }  // namespace

@@ -22,83 +22,117 @@ namespace fp8opt {
 
 namespace {
 
-// 8-code groups per thread per tile, and resident CTAs per SM of the norm
-// pass (each CTA holds the 32 KB table of the exact squares).  The pass is
-// bound by memory latency, so more bytes in flight per thread pay: measured
-// on the 6.7B list, 1.420 ms with sixteen groups at 4 CTAs/SM (63
-// registers), 1.449 with eight at 5 (48 registers).
-#ifndef FP8OPT_NORM_GROUPS
-#define FP8OPT_NORM_GROUPS 16
-#endif
+// Resident CTAs per SM of the norm pass (each CTA holds the 32 KB table of
+// the exact squares).
 #ifndef FP8OPT_NORM_MIN_BLOCKS
 #define FP8OPT_NORM_MIN_BLOCKS 4
 #endif
-// Tiles ahead of the current one that one thread of the CTA asks L2 for
-// (cp.async.bulk.prefetch.L2; 0: none).  A CTA walks one contiguous range of
-// the chunk table, so the next tiles are the next bytes of its range.
-// Measured slower (one tile ahead: 1.461 ms, two: 1.545 on the 6.7B list).
-#ifndef FP8OPT_NORM_PREFETCH
-#define FP8OPT_NORM_PREFETCH 0
-#endif
-constexpr int kNormGroups = FP8OPT_NORM_GROUPS;
-constexpr int64_t kNormTile = (int64_t)kThreads * kGroup * kNormGroups;
+// A chunk is read as two half tiles of eight 8-code groups per thread.  The
+// pass is bound by memory latency, so each half's loads go out one half tile
+// ahead of its arithmetic: a chunk's second half is requested before its
+// first is summed, and the next chunk's first half before the second is
+// summed, so a thread always has a half tile in flight.
+constexpr int kHalfGroups = 8;
+constexpr int64_t kHalfTile = (int64_t)kThreads * kGroup * kHalfGroups;
+static_assert(2 * kHalfTile == kChunkElems, "a full chunk is two half tiles");
 
-// This thread's share of [begin, end) into acc; bad collects the codes at
-// or above the tensor's overflow threshold (addend tadd).
+struct HalfTile {
+  uint2 c[kHalfGroups];
+};
+
+// Issues the loads of the half tile at p (8-byte aligned, kHalfTile codes).
+__device__ __forceinline__ void load_half(HalfTile& h, const uint8_t* p) {
+#pragma unroll
+  for (int q = 0; q < kHalfGroups; ++q)
+    h.c[q] = ld_once2(p + q * (kThreads * kGroup) + threadIdx.x * kGroup);
+}
+
+// Adds a loaded half tile to acc; bad collects the codes at or above the
+// tensor's overflow threshold (addend tadd).
 template <int GF>
-__device__ void thread_norm(const uint8_t* g, int64_t begin, int64_t end,
-                            bool vec, uint32_t tadd, const SqTable& tab,
-                            SqTab& acc, uint32_t& bad) {
-  const int tid = threadIdx.x;
+__device__ __forceinline__ void sum_half(const HalfTile& h, uint32_t tadd,
+                                         const SqTable& tab, SqTab& acc,
+                                         uint32_t& bad) {
   const uint32_t lb = sq_lane_byte<GF>();
-  const bool pf = FP8OPT_NORM_PREFETCH > 0 && tid == 0 && vec && aligned16(g);
+#pragma unroll
+  for (int q = 0; q < kHalfGroups; ++q) {
+    const uint32_t a = h.c[q].x & 0x7F7F7F7Fu, b = h.c[q].y & 0x7F7F7F7Fu;
+    bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
+    acc.add_word<GF>(a, lb, tab);
+    acc.add_word<GF>(b, lb, tab);
+  }
+}
+
+__device__ __forceinline__ void sum_half_fmt(const HalfTile& h, int fmt,
+                                             uint32_t tadd, const SqTable& tab,
+                                             SqTab& acc, uint32_t& bad) {
+  if (fmt == kE4M3)
+    sum_half<kE4M3>(h, tadd, tab, acc, bad);
+  else
+    sum_half<kE5M2>(h, tadd, tab, acc, bad);
+}
+
+// This thread's share of a chunk that is not full ([begin, end) shorter than
+// kChunkElems, or codes without vector loads): whole 8-code groups as
+// vectors where they can be, the rest by code.
+template <int GF>
+__device__ void thread_norm_part(const uint8_t* g, int64_t begin, int64_t end,
+                                 bool vec, uint32_t tadd, const SqTable& tab,
+                                 SqTab& acc, uint32_t& bad) {
+  const uint32_t lb = sq_lane_byte<GF>();
 #pragma unroll 1
-  for (int64_t base = begin; base < end; base += kNormTile) {
-    if (pf) {
-      const int64_t ahead = base + FP8OPT_NORM_PREFETCH * kNormTile;
-      if (ahead + kNormTile <= end) prefetch_l2(g + ahead, (uint32_t)kNormTile);
+  for (int64_t i0 = begin + threadIdx.x * kGroup; i0 < end;
+       i0 += kThreads * kGroup) {
+    if (vec && i0 + kGroup <= end) {
+      const uint2 c = ld_once2(g + i0);
+      const uint32_t a = c.x & 0x7F7F7F7Fu, b = c.y & 0x7F7F7F7Fu;
+      bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
+      acc.add_word<GF>(a, lb, tab);
+      acc.add_word<GF>(b, lb, tab);
+      continue;
     }
-    if (vec && base + kNormTile <= end) {
-      uint2 c[kNormGroups];
-#pragma unroll
-      for (int q = 0; q < kNormGroups; ++q)
-        c[q] = ld_once2(g + base + q * (kThreads * kGroup) + tid * kGroup);
-#pragma unroll
-      for (int q = 0; q < kNormGroups; ++q) {
-        const uint32_t a = c[q].x & 0x7F7F7F7Fu, b = c[q].y & 0x7F7F7F7Fu;
-        bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
-        acc.add_word<GF>(a, lb, tab);
-        acc.add_word<GF>(b, lb, tab);
-      }
-    } else {
-      // a partial tile: whole 8-code groups as vectors, the rest by code
-#pragma unroll 1
-      for (int q = 0; q < kNormGroups; ++q) {
-        const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
-        if (vec && i0 + kGroup <= end) {
-          const uint2 c = ld_once2(g + i0);
-          const uint32_t a = c.x & 0x7F7F7F7Fu, b = c.y & 0x7F7F7F7Fu;
-          bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
-          acc.add_word<GF>(a, lb, tab);
-          acc.add_word<GF>(b, lb, tab);
-          continue;
-        }
-        for (int e = 0; e < kGroup; ++e) {
-          const int64_t i = i0 + e;
-          if (i >= end) break;
-          const uint32_t a = g[i] & 0x7Fu;
-          bad |= (a + tadd) & 0x80u;
-          acc.add_word<GF>(a, lb, tab);    // bytes 1..3 are zero: magnitude 0
-        }
-      }
+    for (int e = 0; e < kGroup && i0 + e < end; ++e) {
+      const uint32_t a = g[i0 + e] & 0x7Fu;
+      bad |= (a + tadd) & 0x80u;
+      acc.add_word<GF>(a, lb, tab);    // bytes 1..3 are zero: magnitude 0
     }
   }
+}
+
+// What the pass needs of a chunk and its tensor.
+struct NormChunk {
+  const uint8_t* g;
+  const float* g_scale;
+  int64_t begin;
+  uint32_t len, tensor;
+  int fmt;
+  bool vec;
+
+  __device__ __forceinline__ bool full() const {
+    return vec && len == (uint32_t)kChunkElems;
+  }
+};
+
+__device__ __forceinline__ NormChunk norm_chunk(const StepDesc* descs,
+                                                const Chunk* chunks, uint32_t c) {
+  const Chunk ch = chunks[c];
+  const StepDesc& d = descs[ch.tensor];
+  NormChunk r;
+  r.g = d.g;
+  r.g_scale = d.g_scale;
+  r.begin = ch.begin;
+  r.len = ch.len;
+  r.tensor = ch.tensor;
+  r.fmt = d.g_fmt;
+  r.vec = d.vec_ok != 0;
+  return r;
 }
 
 // Each CTA takes one contiguous range of the chunk table (an equal share),
 // so a large tensor's chunks reach it as one run; a run adds to one
 // accumulator, which goes to the tensor's slot when the tensor changes: one
-// CTA reduction per run instead of one per chunk.
+// CTA reduction per run instead of one per chunk.  The next chunk's record
+// is read while the current one is summed.
 __global__ void __launch_bounds__(kThreads, FP8OPT_NORM_MIN_BLOCKS)
 grad_norm_kernel(const StepDesc* __restrict__ descs,
                  const Chunk* __restrict__ chunks, uint32_t nchunks, float ils_h,
@@ -108,39 +142,52 @@ grad_norm_kernel(const StepDesc* __restrict__ descs,
   const float ils = ils_dev != nullptr ? *ils_dev : ils_h;
   __shared__ SqTable tab;
   __shared__ unsigned long long red64[2 * (kThreads / 32)];
-  sq_table_fill(tab);
-  SqTab acc;
-  uint32_t bad = 0, tadd = 0, cur = 0xFFFFFFFFu;
-  bool nonempty = false;
   const uint32_t c0 = (uint32_t)((uint64_t)blockIdx.x * nchunks / gridDim.x);
   const uint32_t c1 = (uint32_t)((uint64_t)(blockIdx.x + 1) * nchunks / gridDim.x);
+  if (c0 >= c1) return;   // uniform over the CTA
+  NormChunk cur = norm_chunk(descs, chunks, c0);
+  HalfTile a, b;          // a holds the current chunk's first half if full
+  if (cur.full()) load_half(a, cur.g + cur.begin);
+  sq_table_fill(tab);
+  SqTab acc;
+  uint32_t bad = 0, tadd = 0, tensor = 0xFFFFFFFFu;
+  bool nonempty = false;
   for (uint32_t c = c0; c < c1; ++c) {
-    const Chunk ch = chunks[c];
-    const StepDesc d = descs[ch.tensor];
-    if (ch.tensor != cur) {   // uniform over the CTA
-      if (cur != 0xFFFFFFFFu) {
-        sq_commit_flag(acc, cur, nonempty, bad, sums, found, epoch, red64);
+    const bool more = c + 1 < c1;
+    NormChunk nxt = cur;
+    if (more) nxt = norm_chunk(descs, chunks, c + 1);
+    if (cur.tensor != tensor) {   // uniform over the CTA
+      if (tensor != 0xFFFFFFFFu) {
+        sq_commit_flag(acc, tensor, nonempty, bad, sums, found, epoch, red64);
         acc = SqTab();
         bad = 0;
         nonempty = false;
       }
-      cur = ch.tensor;
+      tensor = cur.tensor;
       // found_inf exactly as the step's first pass decides it: some code at
       // or above the overflow threshold of k = inv_loss_scale / g_scale
-      const float k = __fdiv_rn(ils, *d.g_scale);
-      tadd = threshold_addend(d.g_fmt == kE4M3 ? overflow_threshold<kE4M3>(k)
+      const float k = __fdiv_rn(ils, *cur.g_scale);
+      tadd = threshold_addend(cur.fmt == kE4M3 ? overflow_threshold<kE4M3>(k)
                                                : overflow_threshold<kE5M2>(k));
     }
-    const int64_t begin = ch.begin;
-    const int64_t end = begin + ch.len;
-    nonempty |= end > begin;
-    if (d.g_fmt == kE4M3)
-      thread_norm<kE4M3>(d.g, begin, end, d.vec_ok != 0, tadd, tab, acc, bad);
-    else
-      thread_norm<kE5M2>(d.g, begin, end, d.vec_ok != 0, tadd, tab, acc, bad);
+    nonempty |= cur.len > 0;
+    const bool next_full = more && nxt.full();
+    if (cur.full()) {
+      load_half(b, cur.g + cur.begin + kHalfTile);
+      sum_half_fmt(a, cur.fmt, tadd, tab, acc, bad);
+      if (next_full) load_half(a, nxt.g + nxt.begin);
+      sum_half_fmt(b, cur.fmt, tadd, tab, acc, bad);
+    } else {
+      if (next_full) load_half(a, nxt.g + nxt.begin);
+      const int64_t end = cur.begin + cur.len;
+      if (cur.fmt == kE4M3)
+        thread_norm_part<kE4M3>(cur.g, cur.begin, end, cur.vec, tadd, tab, acc, bad);
+      else
+        thread_norm_part<kE5M2>(cur.g, cur.begin, end, cur.vec, tadd, tab, acc, bad);
+    }
+    cur = nxt;
   }
-  if (cur != 0xFFFFFFFFu)
-    sq_commit_flag(acc, cur, nonempty, bad, sums, found, epoch, red64);
+  sq_commit_flag(acc, tensor, nonempty, bad, sums, found, epoch, red64);
 }
 
 // Per-record terms fl64(k^2 * fl64(S) * 2^-32) (k^2 is exact in double), one
