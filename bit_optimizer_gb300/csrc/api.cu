@@ -46,7 +46,7 @@ cudaError_t launch_cast_encode_sq(const CastDesc* descs, const Chunk* chunks,
                                   unsigned long long* found, float ils,
                                   const float* ils_dev, cudaStream_t stream,
                                   LaunchMark mark);
-cudaError_t cast_encode_sq_occupancy(int* per_sm);
+cudaError_t cast_encode_sq_occupancy(int* per_sm);   // per_sm[2], per format
 cudaError_t launch_cast_encode(const CastDesc* descs, const Chunk* chunks,
                                uint32_t nchunks, const unsigned long long* slots,
                                uint32_t epoch, int fmt, int grid_encode,
@@ -160,7 +160,8 @@ struct DeviceInfo {
   // the k-specialised passes, for k <= 2, k = 4 and k = 8
   int reduce_amax_small[3] = {0, 0, 0}, reduce_encode_small[3] = {0, 0, 0};
   int grad_norm = 0;
-  int cast_encode_sq = 0, reduce_encode_sq = 0;
+  int cast_encode_sq[2] = {0, 0};   // per code format
+  int reduce_encode_sq = 0;
 };
 
 // Per-(device, stream) state.  The slot region holds only epoch-tagged
@@ -257,8 +258,10 @@ cudaError_t device_info(int dev, DeviceInfo** out) {
   }
   if ((e = grad_norm_occupancy(&a)) != cudaSuccess) return e;
   info.grad_norm = info.sms * (a > 0 ? a : 1);
-  if ((e = cast_encode_sq_occupancy(&a)) != cudaSuccess) return e;
-  info.cast_encode_sq = info.sms * (a > 0 ? a : 1);
+  int sq[2] = {0, 0};
+  if ((e = cast_encode_sq_occupancy(sq)) != cudaSuccess) return e;
+  for (int f = 0; f < 2; ++f)
+    info.cast_encode_sq[f] = info.sms * (sq[f] > 0 ? sq[f] : 1);
   if ((e = reduce_encode_sq_occupancy(&a)) != cudaSuccess) return e;
   info.reduce_encode_sq = info.sms * (a > 0 ? a : 1);
   *out = &(g_dev[dev] = info);
@@ -1630,7 +1633,7 @@ static int cast_adam_clipped(const char* fn, const fp8opt_cast_item* grads,
                          info->cast_amax, stream, mark);
   if (e == cudaSuccess && want_norm)
     e = launch_cast_encode_sq(cdescs, cchunks, ws->cast_nchunks, slots, epoch, fmt,
-                              info->cast_encode_sq, sums, sc.found,
+                              info->cast_encode_sq[fmt], sums, sc.found,
                               inv_loss_scale, ils_dev, stream, mark);
   if (e == cudaSuccess && !want_norm)
     e = launch_cast_encode(cdescs, cchunks, ws->cast_nchunks, slots, epoch, fmt,

@@ -30,6 +30,15 @@ namespace {
 #ifndef FP8OPT_ENCSQ_MIN_BLOCKS
 #define FP8OPT_ENCSQ_MIN_BLOCKS 4
 #endif
+// The same for E5M2 codes, whose 128-bit sums take more registers, and
+// whether their chunks go through the tile pipeline (1) or one tile at a
+// time (0).
+#ifndef FP8OPT_ENCSQ5_MIN_BLOCKS
+#define FP8OPT_ENCSQ5_MIN_BLOCKS 3
+#endif
+#ifndef FP8OPT_ENCSQ5_TILES
+#define FP8OPT_ENCSQ5_TILES 1
+#endif
 constexpr int kAmaxGroups = 4;
 
 // Tiles ahead of the current one the encode pass prefetches into L2 (0:
@@ -293,10 +302,10 @@ cast_encode_kernel(const CastDesc* __restrict__ descs,
 // finite amax) is encoded as four tiles of kEncSqGroups 8-element groups per
 // thread, each tile's loads issued one tile ahead of its arithmetic (the
 // next chunk's first tile while this chunk's last is encoded), so that a
-// thread always has a tile in flight.  Other chunks take thread_encode, and
-// so do all chunks of E5M2 codes: their 128-bit sums leave too few registers
-// for two tiles in flight at four CTAs per SM.  A CTA's exact sum goes to
-// its tensor's slot when the next chunk it takes belongs to another tensor.
+// thread always has a tile in flight.  Other chunks take thread_encode.  The
+// E5M2 instance runs fewer CTAs per SM: its 128-bit sums leave too few
+// registers for two tiles in flight at four.  A CTA's exact sum goes to its
+// tensor's slot when the next chunk it takes belongs to another tensor.
 constexpr int kEncSqGroups = FP8OPT_ENCSQ_GROUPS;
 constexpr int64_t kEncSqTile = (int64_t)kThreads * kGroup * kEncSqGroups;
 static_assert(kChunkElems % kEncSqTile == 0 && kChunkElems / kEncSqTile == 4,
@@ -401,7 +410,12 @@ __device__ __forceinline__ EncChunk enc_chunk(const CastDesc* descs,
 // the integer square roots (SqTable).  It walks the chunk table backwards in
 // CTA strides, as the plain encode pass does.
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, FP8OPT_ENCSQ_MIN_BLOCKS)
+constexpr int encsq_min_blocks() {
+  return FMT == kE4M3 ? FP8OPT_ENCSQ_MIN_BLOCKS : FP8OPT_ENCSQ5_MIN_BLOCKS;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, encsq_min_blocks<FMT>())
 cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
                       const Chunk* __restrict__ chunks, uint32_t nchunks,
                       const unsigned long long* __restrict__ slots,
@@ -410,7 +424,7 @@ cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
   __shared__ unsigned long long red64[2 * (kThreads / 32)];
   if (blockIdx.x >= nchunks) return;   // uniform over the CTA
   const float ils = sq.ils_dev != nullptr ? *sq.ils_dev : sq.ils;
-  constexpr bool kTiles = FMT == kE4M3;
+  constexpr bool kTiles = FMT == kE4M3 || FP8OPT_ENCSQ5_TILES != 0;
   uint32_t r = blockIdx.x;
   EncChunk cur = enc_chunk(descs, chunks, nchunks - 1 - r, slots, epoch);
   EncTile ta, tb;   // ta holds the current chunk's first tile if tiled
@@ -562,9 +576,13 @@ cudaError_t cast_occupancy(int* amax_per_sm, int* encode_per_sm) {
       encode_per_sm, cast_encode_kernel<kE4M3>, kThreads, 0);
 }
 
+// per_sm[f]: for codes of format f.
 cudaError_t cast_encode_sq_occupancy(int* per_sm) {
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm[kE4M3], cast_encode_sq_kernel<kE4M3>, kThreads, 0);
+  if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      per_sm, cast_encode_sq_kernel<kE4M3>, kThreads, 0);
+      &per_sm[kE5M2], cast_encode_sq_kernel<kE5M2>, kThreads, 0);
 }
 
 }  // namespace fp8opt
