@@ -695,9 +695,9 @@ def other_configs(device, peak):
         ("o3_1p3b", synth.o3_1p3b, 10, {}, STEP_BYTES["O3"]),
         ("o3_1p3b_scaled_v", synth.o3_1p3b, 10, {"scaled_v": True},
          STEP_BYTES["O3"]),
-        # Adam with L2 decay runs as two calls and its first pass reads w:
-        # cast 5 + first pass 4 + update 11
-        ("o2_350m_adam_l2", synth.o2_350m, 20, {"l2": True}, 20),
+        # Adam with L2 decay: its first pass also reads w; amax 2, the fused
+        # encode and first pass 2 + 1 + 2 + 1, update 11
+        ("o2_350m_adam_l2", synth.o2_350m, 20, {"l2": True}, 19),
         # clipping to a global norm, one call: gradient amax 2, encode with
         # the exact squares 3, first pass 2, update 11
         ("o2_350m_clip", synth.o2_350m, 20, {"max_grad_norm": 1.0}, 18),

@@ -1622,36 +1622,45 @@ static int cast_adam_clipped(const char* fn, const fp8opt_cast_item* grads,
   const Chunk* schunks = static_cast<const Chunk*>(ws->step_chunks.ptr);
   LaunchMark mark = launch_mark();
   // the norm only when it clips or is asked for (Adam with L2 decay alone
-  // takes the plain encode pass)
+  // takes the fused cast and step of fp8_cast_adamw_step)
   const bool want_norm = max_grad_norm > 0.0f || grad_norm != nullptr ||
                          grad_norm_dev != nullptr;
   if (state != nullptr)
     e = launch_step_scalars(reinterpret_cast<DevState*>(state), beta1, beta2, wd,
                             l2 != 0, ds, false, stream);
-  if (e == cudaSuccess)
-    e = launch_cast_amax(cdescs, cchunks, ws->cast_nchunks, slots, epoch,
-                         info->cast_amax, stream, mark);
-  if (e == cudaSuccess && want_norm)
-    e = launch_cast_encode_sq(cdescs, cchunks, ws->cast_nchunks, slots, epoch, fmt,
-                              info->cast_encode_sq[fmt], sums, sc.found,
-                              inv_loss_scale, ils_dev, stream, mark);
-  if (e == cudaSuccess && !want_norm)
-    e = launch_cast_encode(cdescs, cchunks, ws->cast_nchunks, slots, epoch, fmt,
-                           info->cast_encode, stream, mark);
-  if (e == cudaSuccess && want_norm)
-    e = launch_grad_norm_terms(sdescs, schunks, 0, n, inv_loss_scale, ils_dev,
-                               sums, sc.found, epoch, terms, nullptr, 0, stream,
-                               mark);
-  if (e == cudaSuccess && want_norm)
-    e = launch_clip_coef(terms, n, sc.found, epoch, nullptr, max_grad_norm, norm,
-                         clip, grad_norm_dev, stream, mark);
-  if (max_grad_norm > 0.0f) s.clip = clip;
-  if (e == cudaSuccess)
-    e = launch_step(sdescs, schunks, ws->step_nchunks, schunks + ws->step_nchunks,
-                    ws->step_nchunks_o3, sc, s, epoch, found_inf_dev,
-                    info->step_amax, info->step_update,
-                    info->step_update_var, info->step_w8, ws->step_any_vs,
-                    stream, mark);
+  if (!want_norm) {
+    // the cast's encode pass fused with the step's first pass (on the step's
+    // chunk table, as fp8_cast_adamw_step), then the update
+    if (e == cudaSuccess)
+      e = launch_cast_step(cdescs, sdescs, schunks, ws->step_nchunks,
+                           schunks + ws->step_nchunks, ws->step_nchunks_o3, slots,
+                           sc, s, epoch, fmt, found_inf_dev, info->cast_amax,
+                           info->cast_step, info->step_update,
+                           info->step_update_var, info->step_w8,
+                           ws->step_any_vs, stream, mark);
+  } else {
+    if (e == cudaSuccess)
+      e = launch_cast_amax(cdescs, cchunks, ws->cast_nchunks, slots, epoch,
+                           info->cast_amax, stream, mark);
+    if (e == cudaSuccess)
+      e = launch_cast_encode_sq(cdescs, cchunks, ws->cast_nchunks, slots, epoch,
+                                fmt, info->cast_encode_sq[fmt], sums, sc.found,
+                                inv_loss_scale, ils_dev, stream, mark);
+    if (e == cudaSuccess)
+      e = launch_grad_norm_terms(sdescs, schunks, 0, n, inv_loss_scale, ils_dev,
+                                 sums, sc.found, epoch, terms, nullptr, 0, stream,
+                                 mark);
+    if (e == cudaSuccess)
+      e = launch_clip_coef(terms, n, sc.found, epoch, nullptr, max_grad_norm, norm,
+                           clip, grad_norm_dev, stream, mark);
+    if (max_grad_norm > 0.0f) s.clip = clip;
+    if (e == cudaSuccess)
+      e = launch_step(sdescs, schunks, ws->step_nchunks, schunks + ws->step_nchunks,
+                      ws->step_nchunks_o3, sc, s, epoch, found_inf_dev,
+                      info->step_amax, info->step_update,
+                      info->step_update_var, info->step_w8, ws->step_any_vs,
+                      stream, mark);
+  }
   if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
   lock.unlock();   // before any wait for the stream
   if (found_inf != nullptr || grad_norm != nullptr)

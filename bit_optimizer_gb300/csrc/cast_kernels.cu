@@ -147,6 +147,94 @@ cast_amax_kernel(const CastDesc* __restrict__ descs,
   }
 }
 
+// ------------------------------------------- exact squares of the codes
+//
+// A thread's exact sum of squared code values, read through a shared-memory
+// table of integer roots (one byte permutation gives each code's entry).
+//   E4M3: SqTable's E4M3 columns, r = |value| * 2^9 below 2^18; r^2 summed
+//         in 64 bits in units of 2^-18.
+//   E5M2: Sq5Table, r = |value| * 2^16 below 2^32 split by the exponent field
+//         e: for e <= 16, r is below 2^18 and r^2 goes to `lo` (units of
+//         2^-32); for e >= 17, r is a multiple of 2^16 and (r / 2^16)^2,
+//         below 2^32, goes to `hi` (units of 1).  Each entry holds {r, 0} or
+//         {0, r / 2^16} for the lane reading it, so a code costs one 64-bit
+//         shared load and two multiply-adds instead of a 128-bit addition.
+// Both 64-bit sums hold at least 2^28 codes a thread.
+struct Sq5Table {
+  uint2 t[128][32];   // [magnitude][lane], 32 KB; rows of 256 bytes
+};
+
+__device__ __forceinline__ void sq5_table_fill(Sq5Table& t) {
+  for (int i = threadIdx.x; i < 128 * 32; i += blockDim.x) {
+    const uint32_t mag = (uint32_t)i >> 5, e = mag >> 2;
+    const float v = dec2<kE5M2>(mag).x * 65536.0f;
+    const uint32_t r = e == 31 ? 0u : __float2uint_rn(v);   // e == 31: inf, NaN
+    t.t[mag][i & 31] = e <= 16 ? make_uint2(r, 0u) : make_uint2(0u, r >> 16);
+  }
+  __syncthreads();
+}
+
+template <int FMT>
+struct SqSum;
+
+template <>
+struct SqSum<kE4M3> {
+  using Table = SqTable;
+  const SqTable* tab;
+  SqTab s;
+  __device__ __forceinline__ explicit SqSum(const SqTable* t) : tab(t) {}
+  // wm: four code magnitudes (sign bits cleared)
+  __device__ __forceinline__ void add_word(uint32_t wm) {
+    s.add_word<kE4M3>(wm, sq_lane_byte<kE4M3>(), *tab);
+  }
+  __device__ __forceinline__ U128 sum() const { return s.sum(); }
+  __device__ __forceinline__ void clear() { s = SqTab(); }
+};
+
+template <>
+struct SqSum<kE5M2> {
+  using Table = Sq5Table;
+  const Sq5Table* tab;
+  unsigned long long lo = 0, hi = 0;
+  __device__ __forceinline__ explicit SqSum(const Sq5Table* t) : tab(t) {}
+  __device__ __forceinline__ void add_word(uint32_t wm) {
+    const char* base = reinterpret_cast<const char*>(tab);
+    const uint32_t lb = 8u * (threadIdx.x & 31u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // byte 1: code j's magnitude (its row), byte 0: this lane's entry
+      const uint2 e = *reinterpret_cast<const uint2*>(
+          base + __byte_perm(wm, lb, 0x5504u + 16u * j));
+      lo += (unsigned long long)e.x * e.x;
+      hi += (unsigned long long)e.y * e.y;
+    }
+  }
+  // lo + hi * 2^32, in units of 2^-32
+  __device__ __forceinline__ U128 sum() const {
+    return add128(U128{lo, 0ull}, U128{hi << 32, hi >> 32});
+  }
+  __device__ __forceinline__ void clear() { lo = hi = 0; }
+};
+
+// sq_commit_flag of a thread's sum in units of 2^-32.
+__device__ __forceinline__ void sq_commit_sum(U128 sum, uint32_t t, bool nonempty,
+                                              uint32_t bad, unsigned long long* sums,
+                                              unsigned long long* found,
+                                              uint32_t epoch,
+                                              unsigned long long* red64) {
+  SqTab a;
+  a.s5 = sum;   // s4 stays 0: a.sum() is `sum`
+  sq_commit_flag(a, t, nonempty, bad, sums, found, epoch, red64);
+}
+
+template <int FMT>
+__device__ __forceinline__ void sq_table_fill_fmt(typename SqSum<FMT>::Table& t) {
+  if constexpr (FMT == kE4M3)
+    sq_table_fill(t);
+  else
+    sq5_table_fill(t);
+}
+
 // -------------------------------------------------------------- encode pass
 
 // Where an encode pass also sums the exact squares of the codes it writes
@@ -168,13 +256,12 @@ struct SqOut {
 template <int DT, int FMT, bool CHECKED, bool SQ>
 __device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
                               int64_t end, bool vec, float scale,
-                              const SqTable* tab, uint32_t tadd, SqTab& acc,
+                              uint32_t tadd, SqSum<FMT>& acc,
                               uint32_t& bad) {
   constexpr int kEncGroups = SQ ? FP8OPT_ENCSQ_GROUPS : FP8OPT_ENC_GROUPS;
   constexpr int64_t kTile = (int64_t)kThreads * kGroup * kEncGroups;
   constexpr uint32_t kSrcBytes = DT == kF32 ? 4 : 2;
   const int tid = threadIdx.x;
-  const uint32_t lb = sq_lane_byte<FMT>();
   const bool pf = FP8OPT_ENC_PREFETCH > 0 && tid == 0 && vec && aligned16(src);
   for (int64_t base = begin; base < end; base += kTile) {
     if (pf) {
@@ -198,8 +285,8 @@ __device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
         if (SQ) {
           const uint32_t a = c.x & 0x7F7F7F7Fu, b = c.y & 0x7F7F7F7Fu;
           bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
-          acc.add_word<FMT>(a, lb, *tab);
-          acc.add_word<FMT>(b, lb, *tab);
+          acc.add_word(a);
+          acc.add_word(b);
         }
       }
     } else {
@@ -216,8 +303,8 @@ __device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
           if (SQ) {
             const uint32_t a = c.x & 0x7F7F7F7Fu, b = c.y & 0x7F7F7F7Fu;
             bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
-            acc.add_word<FMT>(a, lb, *tab);
-            acc.add_word<FMT>(b, lb, *tab);
+            acc.add_word(a);
+            acc.add_word(b);
           }
         } else {
           for (int j = 0; j < kGroup; ++j) {
@@ -229,7 +316,7 @@ __device__ void thread_encode(const void* src, uint8_t* codes, int64_t begin,
             codes[i] = (uint8_t)c;
             if (SQ) {
               bad |= ((c & 0x7Fu) + tadd) & 0x80u;
-              acc.add_word<FMT>(c & 0x7Fu, lb, *tab);
+              acc.add_word(c & 0x7Fu);
             }
           }
         }
@@ -242,15 +329,14 @@ template <int DT, int FMT, bool SQ>
 __device__ __forceinline__ void encode_dispatch(const CastDesc& d,
                                                 int64_t begin, int64_t end,
                                                 float scale, bool checked,
-                                                const SqTable* tab,
-                                                uint32_t tadd, SqTab& acc,
+                                                uint32_t tadd, SqSum<FMT>& acc,
                                                 uint32_t& bad) {
   const bool vec = d.vec_ok != 0;
   if (checked)
-    thread_encode<DT, FMT, true, SQ>(d.src, d.codes, begin, end, vec, scale, tab,
+    thread_encode<DT, FMT, true, SQ>(d.src, d.codes, begin, end, vec, scale,
                                      tadd, acc, bad);
   else
-    thread_encode<DT, FMT, false, SQ>(d.src, d.codes, begin, end, vec, scale, tab,
+    thread_encode<DT, FMT, false, SQ>(d.src, d.codes, begin, end, vec, scale,
                                       tadd, acc, bad);
 }
 
@@ -261,7 +347,7 @@ __device__ __forceinline__ void encode_pass(const CastDesc* __restrict__ descs,
                                             uint32_t nchunks,
                                             const unsigned long long* __restrict__ slots,
                                             uint32_t epoch) {
-  SqTab acc;          // unused without squares
+  SqSum<FMT> acc(nullptr);   // unused without squares
   uint32_t bad = 0;
   for (uint32_t r = blockIdx.x; r < nchunks; r += gridDim.x) {
     const Chunk ch = chunks[nchunks - 1 - r];
@@ -276,14 +362,11 @@ __device__ __forceinline__ void encode_pass(const CastDesc* __restrict__ descs,
     const int64_t end = begin + ch.len;
     const bool checked = ab >= 0x7F800000u;
     if (d.dtype == kF32)
-      encode_dispatch<kF32, FMT, false>(d, begin, end, scale, checked, nullptr, 0,
-                                        acc, bad);
+      encode_dispatch<kF32, FMT, false>(d, begin, end, scale, checked, 0, acc, bad);
     else if (d.dtype == kBF16)
-      encode_dispatch<kBF16, FMT, false>(d, begin, end, scale, checked, nullptr, 0,
-                                         acc, bad);
+      encode_dispatch<kBF16, FMT, false>(d, begin, end, scale, checked, 0, acc, bad);
     else
-      encode_dispatch<kF16, FMT, false>(d, begin, end, scale, checked, nullptr, 0,
-                                        acc, bad);
+      encode_dispatch<kF16, FMT, false>(d, begin, end, scale, checked, 0, acc, bad);
   }
 }
 
@@ -326,10 +409,9 @@ __device__ __forceinline__ void load_enc_tile(EncTile& t, const uint16_t* p) {
 // at or above the overflow threshold (addend tadd) to bad.
 template <int DT, int FMT>
 __device__ __forceinline__ void enc_tile(const EncTile& t, uint8_t* c,
-                                         float scale, const SqTable& tab,
-                                         uint32_t tadd, SqTab& acc,
+                                         float scale, uint32_t tadd,
+                                         SqSum<FMT>& acc,
                                          uint32_t& bad) {
-  const uint32_t lb = sq_lane_byte<FMT>();
 #pragma unroll
   for (int q = 0; q < kEncSqGroups; ++q) {
     float x[8];
@@ -349,20 +431,20 @@ __device__ __forceinline__ void enc_tile(const EncTile& t, uint8_t* c,
     *reinterpret_cast<uint2*>(c + q * (kThreads * kGroup) + threadIdx.x * kGroup) = code;
     const uint32_t a = code.x & 0x7F7F7F7Fu, b = code.y & 0x7F7F7F7Fu;
     bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
-    acc.add_word<FMT>(a, lb, tab);
-    acc.add_word<FMT>(b, lb, tab);
+    acc.add_word(a);
+    acc.add_word(b);
   }
 }
 
 template <int FMT>
 __device__ __forceinline__ void enc_tile_dt(const EncTile& t, int dtype,
                                             uint8_t* c, float scale,
-                                            const SqTable& tab, uint32_t tadd,
-                                            SqTab& acc, uint32_t& bad) {
+                                            uint32_t tadd, SqSum<FMT>& acc,
+                                            uint32_t& bad) {
   if (dtype == kF16)
-    enc_tile<kF16, FMT>(t, c, scale, tab, tadd, acc, bad);
+    enc_tile<kF16, FMT>(t, c, scale, tadd, acc, bad);
   else
-    enc_tile<kBF16, FMT>(t, c, scale, tab, tadd, acc, bad);
+    enc_tile<kBF16, FMT>(t, c, scale, tadd, acc, bad);
 }
 
 // What the pass needs of a chunk, its tensor and the tensor's amax.
@@ -420,7 +502,7 @@ cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
                       const Chunk* __restrict__ chunks, uint32_t nchunks,
                       const unsigned long long* __restrict__ slots,
                       uint32_t epoch, SqOut sq) {
-  __shared__ SqTable tab;
+  __shared__ typename SqSum<FMT>::Table tab;
   __shared__ unsigned long long red64[2 * (kThreads / 32)];
   if (blockIdx.x >= nchunks) return;   // uniform over the CTA
   const float ils = sq.ils_dev != nullptr ? *sq.ils_dev : sq.ils;
@@ -429,8 +511,8 @@ cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
   EncChunk cur = enc_chunk(descs, chunks, nchunks - 1 - r, slots, epoch);
   EncTile ta, tb;   // ta holds the current chunk's first tile if tiled
   if (kTiles && cur.tiled()) load_enc_tile(ta, cur.tile(0));
-  sq_table_fill(tab);
-  SqTab acc;
+  sq_table_fill_fmt<FMT>(tab);
+  SqSum<FMT> acc(&tab);
   uint32_t bad = 0, tadd = 0, tensor = 0xFFFFFFFFu;
   bool nonempty = false;
   float scale = 1.0f;
@@ -440,8 +522,9 @@ cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
     if (more) nxt = enc_chunk(descs, chunks, nchunks - 1 - (r + gridDim.x), slots, epoch);
     if (cur.tensor != tensor) {   // uniform over the CTA
       if (tensor != 0xFFFFFFFFu) {
-        sq_commit_flag(acc, tensor, nonempty, bad, sq.sums, sq.found, epoch, red64);
-        acc = SqTab();
+        sq_commit_sum(acc.sum(), tensor, nonempty, bad, sq.sums, sq.found, epoch,
+                      red64);
+        acc.clear();
         bad = 0;
         nonempty = false;
       }
@@ -459,31 +542,31 @@ cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
     if (kTiles && cur.tiled()) {
       uint8_t* c = cur.codes + cur.begin;
       load_enc_tile(tb, cur.tile(1));
-      enc_tile_dt<FMT>(ta, cur.dtype, c, scale, tab, tadd, acc, bad);
+      enc_tile_dt<FMT>(ta, cur.dtype, c, scale, tadd, acc, bad);
       load_enc_tile(ta, cur.tile(2));
-      enc_tile_dt<FMT>(tb, cur.dtype, c + kEncSqTile, scale, tab, tadd, acc, bad);
+      enc_tile_dt<FMT>(tb, cur.dtype, c + kEncSqTile, scale, tadd, acc, bad);
       load_enc_tile(tb, cur.tile(3));
-      enc_tile_dt<FMT>(ta, cur.dtype, c + 2 * kEncSqTile, scale, tab, tadd, acc, bad);
+      enc_tile_dt<FMT>(ta, cur.dtype, c + 2 * kEncSqTile, scale, tadd, acc, bad);
       if (next_tiled) load_enc_tile(ta, nxt.tile(0));
-      enc_tile_dt<FMT>(tb, cur.dtype, c + 3 * kEncSqTile, scale, tab, tadd, acc, bad);
+      enc_tile_dt<FMT>(tb, cur.dtype, c + 3 * kEncSqTile, scale, tadd, acc, bad);
     } else {
       if (next_tiled) load_enc_tile(ta, nxt.tile(0));
       const CastDesc d = descs[cur.tensor];
       const int64_t end = cur.begin + cur.len;
       const bool checked = cur.ab >= 0x7F800000u;
       if (d.dtype == kF32)
-        encode_dispatch<kF32, FMT, true>(d, cur.begin, end, scale, checked, &tab,
+        encode_dispatch<kF32, FMT, true>(d, cur.begin, end, scale, checked,
                                          tadd, acc, bad);
       else if (d.dtype == kBF16)
-        encode_dispatch<kBF16, FMT, true>(d, cur.begin, end, scale, checked, &tab,
+        encode_dispatch<kBF16, FMT, true>(d, cur.begin, end, scale, checked,
                                           tadd, acc, bad);
       else
-        encode_dispatch<kF16, FMT, true>(d, cur.begin, end, scale, checked, &tab,
+        encode_dispatch<kF16, FMT, true>(d, cur.begin, end, scale, checked,
                                          tadd, acc, bad);
     }
     cur = nxt;
   }
-  sq_commit_flag(acc, tensor, nonempty, bad, sq.sums, sq.found, epoch, red64);
+  sq_commit_sum(acc.sum(), tensor, nonempty, bad, sq.sums, sq.found, epoch, red64);
 }
 
 }  // namespace

@@ -56,7 +56,9 @@ __device__ __forceinline__ uint32_t enc_pair(float2 t) {
 // step's first pass into mx (max |m| bits), gx (max |g| bits, when GX: for a
 // scaled second moment) and bad (non-finite gradient: a code magnitude at or
 // above the threshold whose addend is tadd, as in the unfused first pass).
-template <int DT, int FMT, bool CHECKED, bool GX>
+// L2 (Adam with L2 decay): the gradient takes the decay term fma(wd, w, g),
+// as in the unfused first pass, so the master weights are read too.
+template <int DT, int FMT, bool CHECKED, bool GX, bool L2>
 __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
                                  int64_t begin, int64_t end, float scale,
                                  float k, float minv, uint32_t tadd,
@@ -66,7 +68,7 @@ __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
   const int tid = threadIdx.x;
   const bool vec = cd.vec_ok != 0 && sd.vec_ok != 0;
   const float2 sc2 = splat2(scale), k2 = splat2(k), minv2 = splat2(minv),
-               b1 = splat2(s.beta1), omb1 = splat2(s.omb1);
+               b1 = splat2(s.beta1), omb1 = splat2(s.omb1), wd2 = splat2(s.wd);
   constexpr uint32_t kSrcBytes = DT == kF32 ? 4 : 2;
   const bool pf = FP8OPT_FUSED_PREFETCH > 0 && tid == 0 && vec &&
                   aligned16(cd.src) && aligned16(sd.m);
@@ -77,16 +79,19 @@ __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
         prefetch_l2(static_cast<const char*>(cd.src) + ahead * kSrcBytes,
                     (uint32_t)(kSrcBytes * kTile));
         prefetch_l2(sd.m + ahead, (uint32_t)kTile);
+        if (L2) prefetch_l2(sd.w + ahead, (uint32_t)(2 * kTile));
       }
     }
     if (vec && base + kTile <= end) {
       float x[kFusedGroups][8];
       uint2 mc[kFusedGroups];
+      uint4 wh[kFusedGroups];
 #pragma unroll
       for (int q = 0; q < kFusedGroups; ++q) {
         const int64_t i0 = base + q * (kThreads * kGroup) + tid * kGroup;
         load8<DT>(cd.src, i0, x[q]);
         mc[q] = ld_keep2(sd.m + i0);
+        if (L2) wh[q] = ld_keep4(sd.w + i0);
       }
 #pragma unroll
       for (int q = 0; q < kFusedGroups; ++q) {
@@ -100,7 +105,8 @@ __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
         bad |= codes_at_least(codes.x, tadd) | codes_at_least(codes.y, tadd);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float2 g = mul2(dec2<FMT>(c[j]), k2);
+          float2 g = mul2(dec2<FMT>(c[j]), k2);
+          if (L2) g = fma2(wd2, h2_to_f2(half_pair(wh[q], j)), g);
           if (GX) gx = max(gx, max(abs_bits(g.x), abs_bits(g.y)));
           const float2 m = fma2(b1, mul2(dec2<kE4M3>(code_pair(mc[q], j)), minv2),
                                 mul2(omb1, g));
@@ -119,7 +125,8 @@ __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
                                         : (enc2<FMT>(t, 0.0f) & 0xFFu);
           cd.codes[i] = (uint8_t)code;
           bad |= codes_at_least(code, tadd);
-          const float g = __fmul_rn(dec2<FMT>(code).x, k);
+          float g = __fmul_rn(dec2<FMT>(code).x, k);
+          if (L2) g = __fmaf_rn(s.wd, h_to_f(sd.w[i]), g);
           if (GX) gx = max(gx, abs_bits(g));
           const float mp = __fmul_rn(dec2<kE4M3>(sd.m[i]).x, minv);
           mx = max(mx, abs_bits(__fmaf_rn(s.beta1, mp, __fmul_rn(s.omb1, g))));
@@ -129,7 +136,7 @@ __device__ void thread_cast_step(const CastDesc& cd, const StepDesc& sd,
   }
 }
 
-template <int DT, int FMT, bool GX>
+template <int DT, int FMT, bool GX, bool L2>
 __device__ __forceinline__ void cast_step_dispatch2(const CastDesc& cd,
                                                     const StepDesc& sd,
                                                     int64_t begin, int64_t end,
@@ -141,12 +148,12 @@ __device__ __forceinline__ void cast_step_dispatch2(const CastDesc& cd,
   // As in the unfused step: found_inf from the codes and the threshold of k.
   const uint32_t tadd = threshold_addend(overflow_threshold<FMT>(k));
   if (checked)
-    thread_cast_step<DT, FMT, true, GX>(cd, sd, begin, end, scale, k, minv, tadd, s, mx, gx, bad);
+    thread_cast_step<DT, FMT, true, GX, L2>(cd, sd, begin, end, scale, k, minv, tadd, s, mx, gx, bad);
   else
-    thread_cast_step<DT, FMT, false, GX>(cd, sd, begin, end, scale, k, minv, tadd, s, mx, gx, bad);
+    thread_cast_step<DT, FMT, false, GX, L2>(cd, sd, begin, end, scale, k, minv, tadd, s, mx, gx, bad);
 }
 
-template <int DT, int FMT, bool ANY_VS>
+template <int DT, int FMT, bool ANY_VS, bool L2>
 __device__ __forceinline__ void cast_step_dispatch(const CastDesc& cd,
                                                    const StepDesc& sd,
                                                    int64_t begin, int64_t end,
@@ -156,17 +163,17 @@ __device__ __forceinline__ void cast_step_dispatch(const CastDesc& cd,
                                                    uint32_t& mx, uint32_t& gx,
                                                    uint32_t& bad) {
   if (ANY_VS && sd.v_bound != nullptr)
-    cast_step_dispatch2<DT, FMT, true>(cd, sd, begin, end, scale, k, minv, checked,
-                                       s, mx, gx, bad);
+    cast_step_dispatch2<DT, FMT, true, L2>(cd, sd, begin, end, scale, k, minv,
+                                           checked, s, mx, gx, bad);
   else
-    cast_step_dispatch2<DT, FMT, false>(cd, sd, begin, end, scale, k, minv, checked,
-                                        s, mx, gx, bad);
+    cast_step_dispatch2<DT, FMT, false, L2>(cd, sd, begin, end, scale, k, minv,
+                                            checked, s, mx, gx, bad);
 }
 
 // At most 64 registers a thread: 4 resident CTAs per SM.  ANY_VS: some
 // tensor of the call has a scaled second moment.  DEVS: inv_loss_scale comes
-// from the device-resident step (StepScalars::dev).
-template <int FMT, bool ANY_VS, bool DEVS>
+// from the device-resident step (StepScalars::dev).  L2: Adam with L2 decay.
+template <int FMT, bool ANY_VS, bool DEVS, bool L2>
 __global__ void __launch_bounds__(kThreads, 4)
 cast_step_amax_kernel(const CastDesc* __restrict__ cdescs,
                       const StepDesc* __restrict__ sdescs,
@@ -194,11 +201,11 @@ cast_step_amax_kernel(const CastDesc* __restrict__ cdescs,
     const bool checked = ab >= 0x7F800000u;
     uint32_t mx = 0, gx = 0, bad = 0;
     if (cd.dtype == kF32)
-      cast_step_dispatch<kF32, FMT, ANY_VS>(cd, sd, begin, end, scale, k, minv, checked, s, mx, gx, bad);
+      cast_step_dispatch<kF32, FMT, ANY_VS, L2>(cd, sd, begin, end, scale, k, minv, checked, s, mx, gx, bad);
     else if (cd.dtype == kBF16)
-      cast_step_dispatch<kBF16, FMT, ANY_VS>(cd, sd, begin, end, scale, k, minv, checked, s, mx, gx, bad);
+      cast_step_dispatch<kBF16, FMT, ANY_VS, L2>(cd, sd, begin, end, scale, k, minv, checked, s, mx, gx, bad);
     else
-      cast_step_dispatch<kF16, FMT, ANY_VS>(cd, sd, begin, end, scale, k, minv, checked, s, mx, gx, bad);
+      cast_step_dispatch<kF16, FMT, ANY_VS, L2>(cd, sd, begin, end, scale, k, minv, checked, s, mx, gx, bad);
     mx = block_max_u32(mx, red);
     if (ANY_VS && sd.v_bound != nullptr) {   // uniform over the CTA
       gx = block_max_u32(gx, red);
@@ -233,21 +240,26 @@ cudaError_t launch_cast_step(const CastDesc* cdescs, const StepDesc* sdescs,
   if (e != cudaSuccess) return e;
   const uint32_t g = grid_min((uint32_t)grid_fused, nchunks);
   if (mark) mark(kCastStepAmaxK, 0, stream);
-  const int v = (fmt == kE4M3 ? 0 : 4) | (any_vs ? 2 : 0) | (s.dev ? 1 : 0);
+  const int v = (s.l2 ? 8 : 0) | (fmt == kE4M3 ? 0 : 4) | (any_vs ? 2 : 0) |
+                (s.dev ? 1 : 0);
   switch (v) {
-#define FP8OPT_CAST_STEP_CASE(FMT, VS, DEVS)                                 \
-  case (FMT == kE4M3 ? 0 : 4) | (VS ? 2 : 0) | (DEVS ? 1 : 0):               \
-    cast_step_amax_kernel<FMT, VS, DEVS><<<g, kThreads, 0, stream>>>(        \
+#define FP8OPT_CAST_STEP_CASE(L2, FMT, VS, DEVS)                             \
+  case (L2 ? 8 : 0) | (FMT == kE4M3 ? 0 : 4) | (VS ? 2 : 0) | (DEVS ? 1 : 0): \
+    cast_step_amax_kernel<FMT, VS, DEVS, L2><<<g, kThreads, 0, stream>>>(    \
         cdescs, sdescs, chunks, nchunks, gslots, sc, s, epoch);              \
     break;
-    FP8OPT_CAST_STEP_CASE(kE4M3, false, false)
-    FP8OPT_CAST_STEP_CASE(kE4M3, false, true)
-    FP8OPT_CAST_STEP_CASE(kE4M3, true, false)
-    FP8OPT_CAST_STEP_CASE(kE4M3, true, true)
-    FP8OPT_CAST_STEP_CASE(kE5M2, false, false)
-    FP8OPT_CAST_STEP_CASE(kE5M2, false, true)
-    FP8OPT_CAST_STEP_CASE(kE5M2, true, false)
-    FP8OPT_CAST_STEP_CASE(kE5M2, true, true)
+#define FP8OPT_CAST_STEP_CASES(L2)                                           \
+    FP8OPT_CAST_STEP_CASE(L2, kE4M3, false, false)                           \
+    FP8OPT_CAST_STEP_CASE(L2, kE4M3, false, true)                            \
+    FP8OPT_CAST_STEP_CASE(L2, kE4M3, true, false)                            \
+    FP8OPT_CAST_STEP_CASE(L2, kE4M3, true, true)                             \
+    FP8OPT_CAST_STEP_CASE(L2, kE5M2, false, false)                           \
+    FP8OPT_CAST_STEP_CASE(L2, kE5M2, false, true)                            \
+    FP8OPT_CAST_STEP_CASE(L2, kE5M2, true, false)                            \
+    FP8OPT_CAST_STEP_CASE(L2, kE5M2, true, true)
+    FP8OPT_CAST_STEP_CASES(false)
+    FP8OPT_CAST_STEP_CASES(true)
+#undef FP8OPT_CAST_STEP_CASES
 #undef FP8OPT_CAST_STEP_CASE
   }
   if (mark) mark(kCastStepAmaxK, 1, stream);
@@ -260,7 +272,7 @@ cudaError_t launch_cast_step(const CastDesc* cdescs, const StepDesc* sdescs,
 
 cudaError_t cast_step_occupancy(int* per_sm) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      per_sm, cast_step_amax_kernel<kE4M3, false, false>, kThreads, 0);
+      per_sm, cast_step_amax_kernel<kE4M3, false, false, false>, kThreads, 0);
 }
 
 }  // namespace fp8opt

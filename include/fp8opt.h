@@ -509,7 +509,12 @@ FP8OPT_API int fp8_reduce_scaled(const fp8opt_reduce_item *items, int n, int k,
  * and decides found_inf, so the gradient norm costs no pass of its own (BF16
  * gradients, O2: 2 + 3 + 2 + 11 = 18 bytes per parameter, against 19 for the
  * two calls).  l2: 0 AdamW, 1 Adam with L2 decay; max_grad_norm <= 0 clips
- * nothing (the norm is still reported).  Results, found_inf semantics and
+ * nothing (the norm is still reported).  With max_grad_norm <= 0 and neither
+ * grad_norm nor grad_norm_dev there is no norm to take: the cast's encode
+ * pass is then fused with the step's first pass as in fp8_cast_adamw_step
+ * (Adam with L2 decay, O2: 2 + 6 + 11 = 19 bytes per parameter, the first
+ * pass reading the FP16 weights for the decay term).  Results, found_inf
+ * semantics and
  * errors are those of the two calls made in turn; params[i] must take
  * grads[i]'s output as for fp8_cast_adamw_step.
  */

@@ -267,10 +267,12 @@ def test_clipped_step_stays_in_bounds(lib, name, o3, l2):
 
 
 @pytest.mark.parametrize("name", list(LISTS))
-@pytest.mark.parametrize("clip", [None, 0.5])
+@pytest.mark.parametrize("clip", [None, 0.5, "l2"])
 def test_fused_cast_step_stays_in_bounds(lib, name, clip):
-    """fp8_cast_adamw_step (clip None) and fp8_cast_adam_step_clipped: the
-    cast's codes and scales are outputs the step then reads."""
+    """fp8_cast_adamw_step (clip None), fp8_cast_adam_step_clipped, and the
+    latter for Adam with L2 decay with no norm asked for ("l2": the fused
+    passes, the first one reading the weights): the cast's codes and scales
+    are outputs the step then reads."""
     Lib, _ = lib
     arena = Arena(7)
     rng = np.random.default_rng(8)
@@ -286,6 +288,10 @@ def test_fused_cast_step_stays_in_bounds(lib, name, clip):
     if clip is None:
         rc = Lib.fp8_cast_adamw_step(items, dev.params, n, E4M3, *HP, C.byref(found),
                                      ptr(found_dev), None)
+    elif clip == "l2":
+        rc = Lib.fp8_cast_adam_step_clipped(items, dev.params, n, E4M3, *HP, 1, 0.0,
+                                            None, None, C.byref(found),
+                                            ptr(found_dev), None)
     else:
         rc = Lib.fp8_cast_adam_step_clipped(items, dev.params, n, E4M3, *HP, 0, clip,
                                             C.byref(norm), ptr(norm_dev),
@@ -298,6 +304,9 @@ def test_fused_cast_step_stays_in_bounds(lib, name, clip):
         s.g, s.g_scale = np.ascontiguousarray(c), float(sc)
     if clip is None:
         assert oracle.adamw_step(ref, *HP) == 0
+    elif clip == "l2":
+        assert oracle.adamw_step(ref, *HP, l2=True) == 0
+        assert norm_dev.item() == -7.0   # no norm asked for: left as it was
     else:
         f_ref, n_ref = oracle.adam_step_clipped(ref, *HP, clip)
         assert f_ref == 0 and norm.value == n_ref

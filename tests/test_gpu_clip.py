@@ -224,6 +224,55 @@ def test_fused_clipped_long_tail(bo, l2):
     assert min(norms) > 0.05
 
 
+@pytest.mark.parametrize("o3,scaled_v,fmt", [(False, False, "e4m3"),
+                                              (True, True, "e5m2")])
+def test_fused_adam_l2_without_norm(bo, o3, scaled_v, fmt):
+    """Adam with L2 decay through fp8_cast_adam_step_clipped with no norm
+    asked for: the cast's encode pass fused with the step's first pass,
+    which reads the weights for the decay term.  Every code, scale and
+    state byte against the oracle's cast and then its step."""
+    wl = synth.o2_6p7b_tail(n_layer=1, d=128, ffn=512, vocab=3000, ctx=64,
+                            n_tail=30)
+    f = oracle.FMT[fmt]
+    states = fresh_states(wl.weights(), o3=o3, g_fmt=f, scaled_v=scaled_v)
+    gpu = GpuState([s.copy() for s in states])
+    srcs = [torch.zeros(x, dtype=wl.grad_dtype, device="cuda") for x in wl.numels]
+    amax = torch.zeros(len(states), device="cuda")
+    fused = bo.CastStepPlan(bo.CastPlan(srcs, gpu.g, amax, gpu.g_scale, fmt),
+                            gpu.plan)
+    for t in range(1, 4):
+        grads = wl.grads(t)
+        for d, h in zip(srcs, grads):
+            d.copy_(h)
+        codes, amax_ref, scale = oracle_cast(grads, f)
+        set_grads(states, codes, scale)
+        gpu.load_state(states)
+        f_ref = oracle.adamw_step(states, wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd,
+                                  t, wl.inv_loss_scale, l2=True)
+        found = fused(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.wd, t,
+                      wl.inv_loss_scale, found_inf_dev=gpu.found_dev, l2=True)
+        assert found == f_ref == 0
+        assert fused.last_grad_norm is None
+        assert np.array_equal(amax.cpu().numpy(), amax_ref)
+        for i, c in enumerate(codes):
+            assert np.array_equal(to_np_u8(gpu.g[i]), c)
+        gpu.compare(states)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+def test_fused_clipped_formats_and_sources(bo, fmt, dtype):
+    """Whole 32768-element chunks of 16-bit sources take the encode pass's
+    tile pipeline (E5M2 codes with their two-part sums), FP32 sources and
+    ragged ends the per-chunk path: every code, the norm and the state
+    against the oracle over three steps."""
+    wl = dataclasses.replace(
+        synth.o2_6p7b_tail(n_layer=1, d=128, ffn=512, vocab=3000, ctx=64,
+                           n_tail=30), grad_dtype=dtype)
+    _, _, norms = fused_clipped_lockstep(bo, wl, 3, 0.05, fmt=fmt)
+    assert min(norms) > 0.05
+
+
 def test_fused_clipped_o3_scaled_v_e5m2_unaligned(bo):
     wl = synth.o3_1p3b(n_layer=1, d=64, ffn=256, vocab=300, ctx=32)
     fused_clipped_lockstep(bo, wl, 2, 0.01, o3=True, scaled_v=True, fmt="e5m2",
