@@ -638,7 +638,8 @@ def reduce_configs(device, peak, ranks=(2, 8)):
     """The local FP8 reduction on the 124M GPT-2 list: k shards per tensor
     (each rank's BF16 gradient cast to E4M3 by the library, rows of a
     [k, numel] buffer with 16-byte row stride), reduced to their mean in E4M3;
-    2k + 1 bytes per element."""
+    2k + 1 bytes per element.  Each k is timed plain and with the norm terms
+    of its outputs."""
     import torch
     import synth
     import bit_optimizer_gb300 as bo
@@ -667,6 +668,20 @@ def reduce_configs(device, peak, ranks=(2, 8)):
         gbs = bpe * wl.n_params / (ms * 1e-3) / 1e9
         out[f"reduce_gpt2_124m_k{k}"] = {"ms": ms, "GB/s": gbs, "frac": gbs / peak,
                                          "bytes_per_elem": bpe, "shards": k}
+        # the same with the norm terms of the outputs (the sharded clipped
+        # step's reduction): the exact squares ride in the encode pass
+        terms = torch.empty(n_t, dtype=torch.float64, device=device)
+        found = torch.zeros(1, dtype=torch.int32, device=device)
+
+        def with_norm():
+            plan(norm_terms=terms, found=found, inv_loss_scale=1.0)
+        for _ in range(3):
+            with_norm()
+        ms = _events_ms(with_norm, 20)
+        gbs = bpe * wl.n_params / (ms * 1e-3) / 1e9
+        out[f"reduce_gpt2_124m_k{k}_norm"] = {"ms": ms, "GB/s": gbs,
+                                              "frac": gbs / peak,
+                                              "bytes_per_elem": bpe, "shards": k}
         del shards, codes
         torch.cuda.empty_cache()
     return out

@@ -79,7 +79,7 @@ cudaError_t launch_step_w8(const StepDesc* descs, const Chunk* chunks_o3,
                            LaunchMark mark);
 cudaError_t reduce_occupancy(int* amax_per_sm, int* amax_small_per_sm,
                              int* encode_per_sm, int* encode_small_per_sm);
-cudaError_t reduce_encode_sq_occupancy(int* per_sm);
+cudaError_t reduce_encode_sq_occupancy(int* per_sm, int* small_per_sm);
 cudaError_t launch_grad_norm_terms(const StepDesc* descs, const Chunk* chunks,
                                    uint32_t nchunks, int n, float ils,
                                    const float* ils_dev,
@@ -161,7 +161,7 @@ struct DeviceInfo {
   int reduce_amax_small[3] = {0, 0, 0}, reduce_encode_small[3] = {0, 0, 0};
   int grad_norm = 0;
   int cast_encode_sq[2] = {0, 0};   // per code format
-  int reduce_encode_sq = 0;
+  int reduce_encode_sq = 0, reduce_encode_sq_small[3] = {0, 0, 0};
 };
 
 // Per-(device, stream) state.  The slot region holds only epoch-tagged
@@ -262,8 +262,10 @@ cudaError_t device_info(int dev, DeviceInfo** out) {
   if ((e = cast_encode_sq_occupancy(sq)) != cudaSuccess) return e;
   for (int f = 0; f < 2; ++f)
     info.cast_encode_sq[f] = info.sms * (sq[f] > 0 ? sq[f] : 1);
-  if ((e = reduce_encode_sq_occupancy(&a)) != cudaSuccess) return e;
+  if ((e = reduce_encode_sq_occupancy(&a, es)) != cudaSuccess) return e;
   info.reduce_encode_sq = info.sms * (a > 0 ? a : 1);
+  for (int i = 0; i < 3; ++i)
+    info.reduce_encode_sq_small[i] = info.sms * (es[i] > 0 ? es[i] : 1);
   *out = &(g_dev[dev] = info);
   return cudaSuccess;
 }
@@ -932,7 +934,8 @@ int reduce_call(const char* fn, const fp8opt_reduce_item* items, int n, int k,
                       static_cast<const Chunk*>(ws->reduce_chunks.ptr),
                       ws->reduce_nchunks, slots, epoch, k, in_fmt, out_fmt, post,
                       ks >= 0 ? info->reduce_amax_small[ks] : info->reduce_amax,
-                      rq.with_norm ? info->reduce_encode_sq
+                      rq.with_norm ? (ks >= 0 ? info->reduce_encode_sq_small[ks]
+                                              : info->reduce_encode_sq)
                       : ks >= 0 ? info->reduce_encode_small[ks]
                                 : info->reduce_encode,
                       rq.with_norm ? &norm : nullptr, stream, launch_mark(),

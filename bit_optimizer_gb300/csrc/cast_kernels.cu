@@ -147,94 +147,6 @@ cast_amax_kernel(const CastDesc* __restrict__ descs,
   }
 }
 
-// ------------------------------------------- exact squares of the codes
-//
-// A thread's exact sum of squared code values, read through a shared-memory
-// table of integer roots (one byte permutation gives each code's entry).
-//   E4M3: SqTable's E4M3 columns, r = |value| * 2^9 below 2^18; r^2 summed
-//         in 64 bits in units of 2^-18.
-//   E5M2: Sq5Table, r = |value| * 2^16 below 2^32 split by the exponent field
-//         e: for e <= 16, r is below 2^18 and r^2 goes to `lo` (units of
-//         2^-32); for e >= 17, r is a multiple of 2^16 and (r / 2^16)^2,
-//         below 2^32, goes to `hi` (units of 1).  Each entry holds {r, 0} or
-//         {0, r / 2^16} for the lane reading it, so a code costs one 64-bit
-//         shared load and two multiply-adds instead of a 128-bit addition.
-// Both 64-bit sums hold at least 2^28 codes a thread.
-struct Sq5Table {
-  uint2 t[128][32];   // [magnitude][lane], 32 KB; rows of 256 bytes
-};
-
-__device__ __forceinline__ void sq5_table_fill(Sq5Table& t) {
-  for (int i = threadIdx.x; i < 128 * 32; i += blockDim.x) {
-    const uint32_t mag = (uint32_t)i >> 5, e = mag >> 2;
-    const float v = dec2<kE5M2>(mag).x * 65536.0f;
-    const uint32_t r = e == 31 ? 0u : __float2uint_rn(v);   // e == 31: inf, NaN
-    t.t[mag][i & 31] = e <= 16 ? make_uint2(r, 0u) : make_uint2(0u, r >> 16);
-  }
-  __syncthreads();
-}
-
-template <int FMT>
-struct SqSum;
-
-template <>
-struct SqSum<kE4M3> {
-  using Table = SqTable;
-  const SqTable* tab;
-  SqTab s;
-  __device__ __forceinline__ explicit SqSum(const SqTable* t) : tab(t) {}
-  // wm: four code magnitudes (sign bits cleared)
-  __device__ __forceinline__ void add_word(uint32_t wm) {
-    s.add_word<kE4M3>(wm, sq_lane_byte<kE4M3>(), *tab);
-  }
-  __device__ __forceinline__ U128 sum() const { return s.sum(); }
-  __device__ __forceinline__ void clear() { s = SqTab(); }
-};
-
-template <>
-struct SqSum<kE5M2> {
-  using Table = Sq5Table;
-  const Sq5Table* tab;
-  unsigned long long lo = 0, hi = 0;
-  __device__ __forceinline__ explicit SqSum(const Sq5Table* t) : tab(t) {}
-  __device__ __forceinline__ void add_word(uint32_t wm) {
-    const char* base = reinterpret_cast<const char*>(tab);
-    const uint32_t lb = 8u * (threadIdx.x & 31u);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      // byte 1: code j's magnitude (its row), byte 0: this lane's entry
-      const uint2 e = *reinterpret_cast<const uint2*>(
-          base + __byte_perm(wm, lb, 0x5504u + 16u * j));
-      lo += (unsigned long long)e.x * e.x;
-      hi += (unsigned long long)e.y * e.y;
-    }
-  }
-  // lo + hi * 2^32, in units of 2^-32
-  __device__ __forceinline__ U128 sum() const {
-    return add128(U128{lo, 0ull}, U128{hi << 32, hi >> 32});
-  }
-  __device__ __forceinline__ void clear() { lo = hi = 0; }
-};
-
-// sq_commit_flag of a thread's sum in units of 2^-32.
-__device__ __forceinline__ void sq_commit_sum(U128 sum, uint32_t t, bool nonempty,
-                                              uint32_t bad, unsigned long long* sums,
-                                              unsigned long long* found,
-                                              uint32_t epoch,
-                                              unsigned long long* red64) {
-  SqTab a;
-  a.s5 = sum;   // s4 stays 0: a.sum() is `sum`
-  sq_commit_flag(a, t, nonempty, bad, sums, found, epoch, red64);
-}
-
-template <int FMT>
-__device__ __forceinline__ void sq_table_fill_fmt(typename SqSum<FMT>::Table& t) {
-  if constexpr (FMT == kE4M3)
-    sq_table_fill(t);
-  else
-    sq5_table_fill(t);
-}
-
 // -------------------------------------------------------------- encode pass
 
 // Where an encode pass also sums the exact squares of the codes it writes

@@ -480,14 +480,13 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* smem) {
 //
 // Every E4M3 or E5M2 code's value is a multiple of 2^-16, so its square is an
 // integer count of 2^-32 and a tensor's sum of squares can be taken exactly:
-//   E4M3: r = |value| * 2^9 is an integer below 2^18 (taken exactly from the
-//         decoded float with one fused multiply-add against 2^23), r^2 below
-//         2^36 in units of 2^-18, summed in 64 bits per thread;
-//   E5M2: r = |value| * 2^16 below 2^32 from the code's fields, r^2 below
-//         2^64 in units of 2^-32, summed in 128 bits per thread.
+//   E4M3: r = |value| * 2^9 is an integer below 2^18, r^2 below 2^36 in
+//         units of 2^-18, summed in 64 bits per thread;
+//   E5M2: r = |value| * 2^16 is an integer below 2^32, r^2 below 2^64 in
+//         units of 2^-32, summed in 128 bits per thread (or, where a pass
+//         has one code format, as two 64-bit sums: SqSum<kE5M2>).
 // Integer sums are exact and order-free, so a norm built on them does not
-// depend on the kernel schedule.  A thread's share of one chunk (at most
-// kChunkElems / kThreads codes) keeps the E4M3 sum below 2^43.
+// depend on the kernel schedule.
 
 struct U128 {
   unsigned long long lo, hi;
@@ -530,94 +529,7 @@ __device__ __forceinline__ U128 block_sum128(U128 v, unsigned long long* smem) {
   return s;
 }
 
-// acc += r^2 over the four E4M3 codes of a word (sign bits cleared): the
-// decoded values are exact floats below 2^9, and v * 512 + 2^23 is an exact
-// float whose low 23 bits are the integer r.
-__device__ __forceinline__ void sq_e4m3(uint32_t w, unsigned long long& acc) {
-  const float2 a = dec2<kE4M3>(w & 0xFFFFu), b = dec2<kE4M3>(w >> 16);
-  const float2 ta = fma2(a, splat2(512.0f), splat2(8388608.0f));
-  const float2 tb = fma2(b, splat2(512.0f), splat2(8388608.0f));
-  const uint32_t r0 = __float_as_uint(ta.x) & 0x7FFFFFu;
-  const uint32_t r1 = __float_as_uint(ta.y) & 0x7FFFFFu;
-  const uint32_t r2 = __float_as_uint(tb.x) & 0x7FFFFFu;
-  const uint32_t r3 = __float_as_uint(tb.y) & 0x7FFFFFu;
-  acc += (unsigned long long)r0 * r0;
-  acc += (unsigned long long)r1 * r1;
-  acc += (unsigned long long)r2 * r2;
-  acc += (unsigned long long)r3 * r3;
-}
-
-// acc += r^2 over the four E5M2 codes of a word (sign bits cleared), with
-// r = (4 + m) << (e - 1) for exponent field e >= 1 and r = m for e = 0
-// (non-finite codes count 0; they set found_inf instead).
-__device__ __forceinline__ U128 sq_e5m2(uint32_t w, U128 acc) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t mag = (w >> (8 * j)) & 0x7Fu;
-    const uint32_t e = mag >> 2, m = mag & 3u;
-    const uint32_t r = e == 0 ? m : (e == 31 ? 0u : ((4u | m) << (e - 1)));
-    acc = add64(acc, (unsigned long long)r * r);
-  }
-  return acc;
-}
-
-// A thread's exact sum of squared code values (format FMT) and the largest
-// code magnitude it saw.  A non-finite code has the largest magnitudes of its
-// format (E4M3 0x7F, E5M2 0x7C and above), so the maximum also tells whether
-// one was seen.
-template <int FMT>
-struct SqAcc {
-  unsigned long long s4 = 0;   // E4M3: units of 2^-18
-  U128 s5 = {0ull, 0ull};      // E5M2: units of 2^-32
-  uint32_t vmax = 0;           // per-byte max of the magnitudes
-
-  __device__ __forceinline__ void add_word(uint32_t w) {
-    w &= 0x7F7F7F7Fu;
-    vmax = __vmaxu4(vmax, w);
-    if (FMT == kE4M3)
-      sq_e4m3(w, s4);
-    else
-      s5 = sq_e5m2(w, s5);
-  }
-  // the sum in units of 2^-32
-  __device__ __forceinline__ U128 sum() const {
-    if (FMT == kE4M3) return U128{s4 << 14, s4 >> 50};
-    return s5;
-  }
-  __device__ __forceinline__ uint32_t cmax() const {
-    return max(max(vmax & 0xFFu, (vmax >> 8) & 0xFFu),
-               max((vmax >> 16) & 0xFFu, vmax >> 24));
-  }
-};
-
-// End of a chunk of tensor t: the CTA's exact sum goes to the tensor's
-// 128-bit slot (sums[2t], sums[2t + 1]; the low word's carry to the high
-// word), and found_inf is set when a code is non-finite or the largest
-// |value| times k is not finite (the step's test on this chunk; the product
-// is monotone in |value|).  Every thread calls it.
-template <int FMT>
-__device__ __forceinline__ void sq_commit(const SqAcc<FMT>& a, uint32_t t,
-                                          bool nonempty, float k,
-                                          unsigned long long* sums,
-                                          unsigned long long* found,
-                                          uint32_t epoch,
-                                          unsigned long long* red64,
-                                          uint32_t* red32) {
-  const U128 s = block_sum128(a.sum(), red64);
-  const uint32_t cmax = block_max_u32(a.cmax(), red32);
-  if (threadIdx.x == 0 && nonempty) {
-    if (s.lo | s.hi) {
-      const unsigned long long old = atomicAdd(&sums[2 * t], s.lo);
-      const unsigned long long carry = old + s.lo < old ? 1ull : 0ull;
-      if (s.hi + carry) atomicAdd(&sums[2 * t + 1], s.hi + carry);
-    }
-    const bool bad = FMT == kE4M3 ? cmax == 0x7Fu : cmax >= 0x7Cu;
-    if (bad || nonfinite(__fmul_rn(dec2<FMT>(cmax).x, k)))
-      atomicMax(found, slot_tag(epoch, 1u));
-  }
-}
-
-// The same exact sums through a shared-memory table of the integers r (r =
+// The exact sums go through a shared-memory table of the integers r (r =
 // |value| * 2^9 for E4M3, |value| * 2^16 for E5M2; 0 for the non-finite
 // codes, which set found_inf instead), so that a code costs one byte
 // permutation, one shared load and one multiply-add.  Entry [mag][fmt * 32 +
@@ -697,6 +609,93 @@ __device__ __forceinline__ void sq_commit_flag(const SqTab& a, uint32_t t,
     }
     if (any_bad) atomicMax(found, slot_tag(epoch, 1u));
   }
+}
+
+// A thread's exact sum of squared code values for one code format (the
+// passes whose codes all have one format), read through a shared-memory
+// table of integer roots (one byte permutation gives each code's entry).
+//   E4M3: SqTable's E4M3 columns, r = |value| * 2^9 below 2^18; r^2 summed
+//         in 64 bits in units of 2^-18.
+//   E5M2: Sq5Table, r = |value| * 2^16 below 2^32 split by the exponent field
+//         e: for e <= 16, r is below 2^18 and r^2 goes to `lo` (units of
+//         2^-32); for e >= 17, r is a multiple of 2^16 and (r / 2^16)^2,
+//         below 2^32, goes to `hi` (units of 1).  Each entry holds {r, 0} or
+//         {0, r / 2^16} for the lane reading it, so a code costs one 64-bit
+//         shared load and two multiply-adds instead of a 128-bit addition.
+// Both 64-bit sums hold at least 2^28 codes a thread.
+struct Sq5Table {
+  uint2 t[128][32];   // [magnitude][lane], 32 KB; rows of 256 bytes
+};
+
+__device__ __forceinline__ void sq5_table_fill(Sq5Table& t) {
+  for (int i = threadIdx.x; i < 128 * 32; i += blockDim.x) {
+    const uint32_t mag = (uint32_t)i >> 5, e = mag >> 2;
+    const float v = dec2<kE5M2>(mag).x * 65536.0f;
+    const uint32_t r = e == 31 ? 0u : __float2uint_rn(v);   // e == 31: inf, NaN
+    t.t[mag][i & 31] = e <= 16 ? make_uint2(r, 0u) : make_uint2(0u, r >> 16);
+  }
+  __syncthreads();
+}
+
+template <int FMT>
+struct SqSum;
+
+template <>
+struct SqSum<kE4M3> {
+  using Table = SqTable;
+  const SqTable* tab;
+  SqTab s;
+  __device__ __forceinline__ explicit SqSum(const SqTable* t) : tab(t) {}
+  // wm: four code magnitudes (sign bits cleared)
+  __device__ __forceinline__ void add_word(uint32_t wm) {
+    s.add_word<kE4M3>(wm, sq_lane_byte<kE4M3>(), *tab);
+  }
+  __device__ __forceinline__ U128 sum() const { return s.sum(); }
+  __device__ __forceinline__ void clear() { s = SqTab(); }
+};
+
+template <>
+struct SqSum<kE5M2> {
+  using Table = Sq5Table;
+  const Sq5Table* tab;
+  unsigned long long lo = 0, hi = 0;
+  __device__ __forceinline__ explicit SqSum(const Sq5Table* t) : tab(t) {}
+  __device__ __forceinline__ void add_word(uint32_t wm) {
+    const char* base = reinterpret_cast<const char*>(tab);
+    const uint32_t lb = 8u * (threadIdx.x & 31u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // byte 1: code j's magnitude (its row), byte 0: this lane's entry
+      const uint2 e = *reinterpret_cast<const uint2*>(
+          base + __byte_perm(wm, lb, 0x5504u + 16u * j));
+      lo += (unsigned long long)e.x * e.x;
+      hi += (unsigned long long)e.y * e.y;
+    }
+  }
+  // lo + hi * 2^32, in units of 2^-32
+  __device__ __forceinline__ U128 sum() const {
+    return add128(U128{lo, 0ull}, U128{hi << 32, hi >> 32});
+  }
+  __device__ __forceinline__ void clear() { lo = hi = 0; }
+};
+
+// sq_commit_flag of a thread's sum in units of 2^-32.
+__device__ __forceinline__ void sq_commit_sum(U128 sum, uint32_t t, bool nonempty,
+                                              uint32_t bad, unsigned long long* sums,
+                                              unsigned long long* found,
+                                              uint32_t epoch,
+                                              unsigned long long* red64) {
+  SqTab a;
+  a.s5 = sum;   // s4 stays 0: a.sum() is `sum`
+  sq_commit_flag(a, t, nonempty, bad, sums, found, epoch, red64);
+}
+
+template <int FMT>
+__device__ __forceinline__ void sq_table_fill_fmt(typename SqSum<FMT>::Table& t) {
+  if constexpr (FMT == kE4M3)
+    sq_table_fill(t);
+  else
+    sq5_table_fill(t);
 }
 
 // Correctly rounded conversion of a 128-bit unsigned integer to double: the

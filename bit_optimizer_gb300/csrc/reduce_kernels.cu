@@ -50,6 +50,10 @@ namespace {
 #ifndef FP8OPT_REDUCE_PREFETCH
 #define FP8OPT_REDUCE_PREFETCH 1
 #endif
+// Resident CTAs per SM of the general encode pass with exact squares.
+#ifndef FP8OPT_REDUCE_SQ_MIN_BLOCKS
+#define FP8OPT_REDUCE_SQ_MIN_BLOCKS 2
+#endif
 // The passes specialised on k (1, 2, 4 or 8 shards): 16-code groups per
 // thread per tile and resident CTAs per SM for each k.  Measured on the 124M
 // list (the whole reduction):
@@ -361,11 +365,27 @@ __device__ __forceinline__ uint4 encode16(const float2 (&y)[8], float scale) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Sixteen codes written by an encode pass: their exact squares into acc, and
+// into bad the codes at or above the overflow threshold whose addend is tadd.
+template <int OUT>
+__device__ __forceinline__ void sq_add16(uint4 c, uint32_t tadd, SqSum<OUT>& acc,
+                                         uint32_t& bad) {
+  bad |= codes_at_least(c.x, tadd) | codes_at_least(c.y, tadd) |
+         codes_at_least(c.z, tadd) | codes_at_least(c.w, tadd);
+  acc.add_word(c.x & 0x7F7F7F7Fu);
+  acc.add_word(c.y & 0x7F7F7F7Fu);
+  acc.add_word(c.z & 0x7F7F7F7Fu);
+  acc.add_word(c.w & 0x7F7F7F7Fu);
+}
+
+// SQ: also add the exact squares of the codes written to acc and collect in
+// bad the codes at or above the overflow threshold whose addend is tadd.
 template <int IN, int OUT, bool CHECKED, bool SQ>
 __device__ void thread_reduce_encode(const ReduceDesc& d, int k,
                                      const float* r_s, float post, float scale,
                                      int64_t begin, int64_t end,
-                                     SqAcc<OUT>& acc) {
+                                     SqSum<OUT>& acc, uint32_t tadd,
+                                     uint32_t& bad) {
   const int tid = threadIdx.x;
   const bool vec = d.vec_ok != 0 && !CHECKED;
 #pragma unroll 1
@@ -382,12 +402,7 @@ __device__ void thread_reduce_encode(const ReduceDesc& d, int k,
       for (int g = 0; g < kRGroups; ++g) {
         const uint4 c = encode16<OUT>(y[g], scale);
         *reinterpret_cast<uint4*>(d.codes + i0[g]) = c;
-        if (SQ) {
-          acc.add_word(c.x);
-          acc.add_word(c.y);
-          acc.add_word(c.z);
-          acc.add_word(c.w);
-        }
+        if (SQ) sq_add16(c, tadd, acc, bad);
       }
     } else {
 #pragma unroll 1
@@ -401,7 +416,10 @@ __device__ void thread_reduce_encode(const ReduceDesc& d, int k,
           const uint32_t c = CHECKED ? enc1_checked<OUT>(t)
                                      : (enc2<OUT>(t, 0.0f) & 0xFFu);
           d.codes[i] = (uint8_t)c;
-          if (SQ) acc.add_word(c);
+          if (SQ) {
+            bad |= ((c & 0x7Fu) + tadd) & 0x80u;
+            acc.add_word(c & 0x7Fu);
+          }
         }
       }
     }
@@ -411,10 +429,12 @@ __device__ void thread_reduce_encode(const ReduceDesc& d, int k,
 // The encode pass's vector path for K = 1, 2, 4 or 8 shards (finite amax):
 // like reduce_amax_small_kernel, all loads of the tile first, then each
 // group is summed, encoded and stored at once.
-template <int IN, int OUT, int K>
+template <int IN, int OUT, int K, bool SQ>
 __device__ void thread_reduce_encode_small(const ReduceDesc& d, const float* r_s,
                                            float post, float scale,
-                                           int64_t begin, int64_t end) {
+                                           int64_t begin, int64_t end,
+                                           SqSum<OUT>& acc, uint32_t tadd,
+                                           uint32_t& bad) {
   constexpr int kSGroups = small_groups<K>();
   constexpr int64_t kSTile = (int64_t)kThreads * kRGroup * kSGroups;
   const int tid = threadIdx.x;
@@ -447,8 +467,10 @@ __device__ void thread_reduce_encode_small(const ReduceDesc& d, const float* r_s
         for (int j = 1; j < K; ++j) accum16<IN, false>(cv[j][g], r[j], y);
 #pragma unroll
         for (int q = 0; q < 8; ++q) y[q] = mul2(y[q], pp);
+        const uint4 c = encode16<OUT>(y, scale);
         *reinterpret_cast<uint4*>(d.codes + base + g * (kThreads * kRGroup) +
-                                  tid * kRGroup) = encode16<OUT>(y, scale);
+                                  tid * kRGroup) = c;
+        if (SQ) sq_add16(c, tadd, acc, bad);
       }
     } else {
 #pragma unroll 1
@@ -459,7 +481,12 @@ __device__ void thread_reduce_encode_small(const ReduceDesc& d, const float* r_s
           if (i >= end) break;
           const float t =
               __fmul_rn(reduce_one<IN>(d.src, d.stride, K, r_s, post, i), scale);
-          d.codes[i] = (uint8_t)(enc2<OUT>(t, 0.0f) & 0xFFu);
+          const uint32_t c = enc2<OUT>(t, 0.0f) & 0xFFu;
+          d.codes[i] = (uint8_t)c;
+          if (SQ) {
+            bad |= ((c & 0x7Fu) + tadd) & 0x80u;
+            acc.add_word(c & 0x7Fu);
+          }
         }
       }
     }
@@ -476,15 +503,19 @@ struct RedSq {
 };
 
 // KS: 0, or the number of shards (1, 2, 4 or 8) the vector path is
-// specialised on (plain encode only).
+// specialised on.  SQ: with the exact squares of the codes through the table
+// tab, committed to the tensor's slot per chunk, and found_inf from the
+// overflow threshold of k = inv_loss_scale / the output scale.
 template <int IN, int OUT, bool SQ, int KS>
 __device__ __forceinline__ void encode_pass(const ReduceDesc* __restrict__ descs,
                                             const Chunk* __restrict__ chunks,
                                             uint32_t nchunks, int k, float post,
                                             const unsigned long long* __restrict__ slots,
                                             uint32_t epoch, const RedSq& sq,
-                                            float* r_s, unsigned long long* red64,
-                                            uint32_t* red32) {
+                                            float* r_s,
+                                            const typename SqSum<OUT>::Table* tab,
+                                            unsigned long long* red64) {
+  SqSum<OUT> acc(tab);
   for (uint32_t r = blockIdx.x; r < nchunks; r += gridDim.x) {
     const Chunk ch = chunks[nchunks - 1 - r];
     const ReduceDesc d = descs[ch.tensor];
@@ -497,17 +528,23 @@ __device__ __forceinline__ void encode_pass(const ReduceDesc* __restrict__ descs
     }
     const int64_t begin = ch.begin;
     const int64_t end = begin + ch.len;
-    SqAcc<OUT> acc;
-    if (ab >= 0x7F800000u)
-      thread_reduce_encode<IN, OUT, true, SQ>(d, k, r_s, post, scale, begin, end, acc);
-    else if (KS > 0)
-      thread_reduce_encode_small<IN, OUT, (KS > 0 ? KS : 1)>(d, r_s, post, scale,
-                                                            begin, end);
-    else
-      thread_reduce_encode<IN, OUT, false, SQ>(d, k, r_s, post, scale, begin, end, acc);
+    uint32_t tadd = 0, bad = 0;
     if (SQ)
-      sq_commit<OUT>(acc, ch.tensor, end > begin, __fdiv_rn(sq.ils, scale),
-                     sq.sums, sq.found, epoch, red64, red32);
+      tadd = threshold_addend(overflow_threshold<OUT>(__fdiv_rn(sq.ils, scale)));
+    if (ab >= 0x7F800000u)
+      thread_reduce_encode<IN, OUT, true, SQ>(d, k, r_s, post, scale, begin, end,
+                                              acc, tadd, bad);
+    else if (KS > 0)
+      thread_reduce_encode_small<IN, OUT, (KS > 0 ? KS : 1), SQ>(
+          d, r_s, post, scale, begin, end, acc, tadd, bad);
+    else
+      thread_reduce_encode<IN, OUT, false, SQ>(d, k, r_s, post, scale, begin, end,
+                                               acc, tadd, bad);
+    if (SQ) {
+      sq_commit_sum(acc.sum(), ch.tensor, end > begin, bad, sq.sums, sq.found,
+                    epoch, red64);
+      acc.clear();
+    }
   }
 }
 
@@ -535,19 +572,25 @@ reduce_encode_small_kernel(const ReduceDesc* __restrict__ descs,
                                  none, r_s, nullptr, nullptr);
 }
 
-// (the exact squares need more registers than the plain pass: two CTAs per
-// SM keep it free of spills)
-template <int IN, int OUT>
-__global__ void __launch_bounds__(kThreads, 2)
+// The encode pass with the exact squares (table roots: SqSum), in the
+// general form and specialised on k = 1, 2, 4 or 8 (KS; 0: general).
+template <int KS>
+constexpr int reduce_sq_min_blocks() {
+  return KS > 0 ? small_min_blocks<KS>() : FP8OPT_REDUCE_SQ_MIN_BLOCKS;
+}
+
+template <int IN, int OUT, int KS>
+__global__ void __launch_bounds__(kThreads, reduce_sq_min_blocks<KS>())
 reduce_encode_sq_kernel(const ReduceDesc* __restrict__ descs,
                         const Chunk* __restrict__ chunks, uint32_t nchunks, int k,
                         float post, const unsigned long long* __restrict__ slots,
                         uint32_t epoch, RedSq sq) {
   __shared__ float r_s[kMaxShards];
+  __shared__ typename SqSum<OUT>::Table tab;
   __shared__ unsigned long long red64[2 * (kThreads / 32)];
-  __shared__ uint32_t red32[kThreads / 32];
-  encode_pass<IN, OUT, true, 0>(descs, chunks, nchunks, k, post, slots, epoch, sq,
-                                r_s, red64, red32);
+  sq_table_fill_fmt<OUT>(tab);
+  encode_pass<IN, OUT, true, KS>(descs, chunks, nchunks, KS > 0 ? KS : k, post,
+                                 slots, epoch, sq, r_s, &tab, red64);
 }
 
 // Per-item norm terms of the reduced tensors (k = ils / the output scale);
@@ -597,20 +640,33 @@ void launch_encode(uint32_t grid, const ReduceDesc* descs, const Chunk* chunks,
       reduce_encode_kernel<IN, kE5M2><<<grid, kThreads, 0, stream>>>(
           descs, chunks, nchunks, k, post, slots, epoch);
   } else {
-    if (out_fmt == kE4M3)
-      reduce_encode_sq_kernel<IN, kE4M3><<<grid, kThreads, 0, stream>>>(
-          descs, chunks, nchunks, k, post, slots, epoch, *sq);
-    else
-      reduce_encode_sq_kernel<IN, kE5M2><<<grid, kThreads, 0, stream>>>(
-          descs, chunks, nchunks, k, post, slots, epoch, *sq);
+    const int ki = k == 1 ? 1 : k == 2 ? 2 : k == 4 ? 3 : k == 8 ? 4 : 0;
+    const int v = (out_fmt == kE4M3 ? 0 : 8) | ki;
+    switch (v) {
+#define FP8OPT_ENCODE_SQ_CASE(OUT, KI, KS)                                   \
+  case (OUT == kE4M3 ? 0 : 8) | KI:                                          \
+    reduce_encode_sq_kernel<IN, OUT, KS><<<grid, kThreads, 0, stream>>>(     \
+        descs, chunks, nchunks, k, post, slots, epoch, *sq);                 \
+    break;
+      FP8OPT_ENCODE_SQ_CASE(kE4M3, 0, 0)
+      FP8OPT_ENCODE_SQ_CASE(kE4M3, 1, 1)
+      FP8OPT_ENCODE_SQ_CASE(kE4M3, 2, 2)
+      FP8OPT_ENCODE_SQ_CASE(kE4M3, 3, 4)
+      FP8OPT_ENCODE_SQ_CASE(kE4M3, 4, 8)
+      FP8OPT_ENCODE_SQ_CASE(kE5M2, 0, 0)
+      FP8OPT_ENCODE_SQ_CASE(kE5M2, 1, 1)
+      FP8OPT_ENCODE_SQ_CASE(kE5M2, 2, 2)
+      FP8OPT_ENCODE_SQ_CASE(kE5M2, 3, 4)
+      FP8OPT_ENCODE_SQ_CASE(kE5M2, 4, 8)
+#undef FP8OPT_ENCODE_SQ_CASE
+    }
   }
 }
 
 }  // namespace
 
 // Launches both passes on `stream`; 1 <= k <= kMaxShards.  With k in {1, 2,
-// 4, 8} the grids are sized for the k-specialised kernels (the first pass,
-// and the encode pass when no norm is asked for).  With norm set,
+// 4, 8} the grids are sized for the k-specialised kernels.  With norm set,
 // the encode pass also sums the exact squares of the codes it writes into
 // norm->sums (2n zeroed words; found_inf into norm->found), and a last kernel
 // writes each item's norm term and the found flag.
@@ -659,9 +715,21 @@ cudaError_t launch_reduce(const ReduceDesc* descs, const Chunk* chunks,
   return cudaGetLastError();
 }
 
-cudaError_t reduce_encode_sq_occupancy(int* per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      per_sm, reduce_encode_sq_kernel<kE4M3, kE4M3>, kThreads, 0);
+// Resident CTAs per SM of the encode pass with squares: general (per_sm)
+// and specialised on k for k <= 2, k = 4 and k = 8 (small_per_sm[3]).
+cudaError_t reduce_encode_sq_occupancy(int* per_sm, int* small_per_sm) {
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      per_sm, reduce_encode_sq_kernel<kE4M3, kE4M3, 0>, kThreads, 0);
+  if (e != cudaSuccess) return e;
+  const void* k[3] = {(const void*)reduce_encode_sq_kernel<kE4M3, kE4M3, 2>,
+                      (const void*)reduce_encode_sq_kernel<kE4M3, kE4M3, 4>,
+                      (const void*)reduce_encode_sq_kernel<kE4M3, kE4M3, 8>};
+  for (int i = 0; i < 3; ++i) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&small_per_sm[i], k[i],
+                                                      kThreads, 0);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // Resident CTAs per SM of the reduction kernels: the first and the encode

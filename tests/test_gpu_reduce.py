@@ -155,25 +155,30 @@ def test_repeated_calls_on_cached_tables(bo):
 
 
 
+@pytest.mark.parametrize("k", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("out_fmt", [E4M3, E5M2])
-def test_reduce_with_norm_terms(bo, out_fmt):
+def test_reduce_with_norm_terms(bo, out_fmt, k):
     """fp8_reduce_scaled_norm: the outputs of fp8_reduce_scaled plus each
     tensor's norm term of its output codes, bit-exact against the oracle's
-    terms of the oracle's reduction."""
-    shards = random_shards(np.random.default_rng(31 + out_fmt),
-                           [0, 17, 8193, 40000, 100003], 3, E4M3)
+    terms of the oracle's reduction (k = 1, 2, 4, 8 take the encode pass
+    specialised on k; the 100003-element tensor has whole 32768-element
+    chunks and a ragged end)."""
+    sizes = [0, 17, 8193, 40000, 100003, 98304]
+    shards = random_shards(np.random.default_rng(31 + out_fmt + 10 * k), sizes,
+                           k, E4M3)
     ils = 2.0 ** -3
     dev = [torch.from_numpy(c).cuda() for c, _ in shards]
     scales = torch.from_numpy(np.stack([s for _, s in shards])).cuda()
     codes = [torch.empty(c.shape[1], dtype=torch.uint8, device="cuda") for c, _ in shards]
-    amax, scale = torch.empty(5, device="cuda"), torch.empty(5, device="cuda")
-    terms = torch.full((5,), -1.0, dtype=torch.float64, device="cuda")
+    n_t = len(sizes)
+    amax, scale = torch.empty(n_t, device="cuda"), torch.empty(n_t, device="cuda")
+    terms = torch.full((n_t,), -1.0, dtype=torch.float64, device="cuda")
     found = torch.full((1,), 7, dtype=torch.int32, device="cuda")
     plan = bo.ReducePlan(dev, scales, codes, amax, scale, "e4m3",
-                         {E4M3: "e4m3", E5M2: "e5m2"}[out_fmt], 1.0 / 3)
+                         {E4M3: "e4m3", E5M2: "e5m2"}[out_fmt], 1.0 / k)
     plan(norm_terms=terms, found=found, inv_loss_scale=ils)
     torch.cuda.synchronize()
-    ref = [oracle.reduce_scaled(c, s, E4M3, out_fmt, 1.0 / 3) for c, s in shards]
+    ref = [oracle.reduce_scaled(c, s, E4M3, out_fmt, 1.0 / k) for c, s in shards]
     states = [oracle.StepState(rc, float(rs), np.zeros(rc.size, np.uint8), 1.0,
                                np.zeros(rc.size, np.uint16), np.zeros(rc.size, np.uint16),
                                g_fmt=out_fmt) for rc, _, rs in ref]
@@ -182,8 +187,15 @@ def test_reduce_with_norm_terms(bo, out_fmt):
     assert np.array_equal(terms.cpu().numpy(), tt)
     for c, (rc, ra, rs) in zip(codes, ref):
         assert np.array_equal(to_np_u8(c), rc)
+    # finite codes whose values overflow once unscaled: found_inf from the
+    # overflow threshold, as the oracle decides it
+    big = 2.0 ** 120
+    plan(norm_terms=terms, found=found, inv_loss_scale=big)
+    torch.cuda.synchronize()
+    f_big, _ = oracle.grad_norm_terms(states, big)
+    assert found.item() == f_big == 1
     # a NaN code in a shard: found_inf
-    shards[3][0][1, 5] = 0x7F
+    shards[3][0][k - 1, 5] = 0x7F
     dev[3].copy_(torch.from_numpy(shards[3][0]))
     plan(norm_terms=terms, found=found, inv_loss_scale=ils)
     torch.cuda.synchronize()
