@@ -415,7 +415,7 @@ cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
                       const unsigned long long* __restrict__ slots,
                       uint32_t epoch, SqOut sq) {
   __shared__ typename SqSum<FMT>::Table tab;
-  __shared__ unsigned long long red64[2 * (kThreads / 32)];
+  __shared__ SqRed red;
   if (blockIdx.x >= nchunks) return;   // uniform over the CTA
   const float ils = sq.ils_dev != nullptr ? *sq.ils_dev : sq.ils;
   constexpr bool kTiles = FMT == kE4M3 || FP8OPT_ENCSQ5_TILES != 0;
@@ -425,7 +425,7 @@ cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
   if (kTiles && cur.tiled()) load_enc_tile(ta, cur.tile(0));
   sq_table_fill_fmt<FMT>(tab);
   SqSum<FMT> acc(&tab);
-  uint32_t bad = 0, tadd = 0, tensor = 0xFFFFFFFFu;
+  uint32_t bad = 0, tadd = 0, tensor = 0xFFFFFFFFu, turn = 0;
   bool nonempty = false;
   float scale = 1.0f;
   for (; r < nchunks; r += gridDim.x) {
@@ -434,8 +434,8 @@ cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
     if (more) nxt = enc_chunk(descs, chunks, nchunks - 1 - (r + gridDim.x), slots, epoch);
     if (cur.tensor != tensor) {   // uniform over the CTA
       if (tensor != 0xFFFFFFFFu) {
-        sq_commit_sum(acc.sum(), tensor, nonempty, bad, sq.sums, sq.found, epoch,
-                      red64);
+        sq_commit(acc.sum(), bad, tensor, nonempty, sq.sums, sq.found, epoch, red,
+                  turn);
         acc.clear();
         bad = 0;
         nonempty = false;
@@ -478,7 +478,7 @@ cast_encode_sq_kernel(const CastDesc* __restrict__ descs,
     }
     cur = nxt;
   }
-  sq_commit_sum(acc.sum(), tensor, nonempty, bad, sq.sums, sq.found, epoch, red64);
+  sq_commit(acc.sum(), bad, tensor, nonempty, sq.sums, sq.found, epoch, red, turn);
 }
 
 }  // namespace

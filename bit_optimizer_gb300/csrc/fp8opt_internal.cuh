@@ -506,29 +506,6 @@ __device__ __forceinline__ U128 add64(U128 a, unsigned long long b) {
   return r;
 }
 
-// Sum over the CTA; the result is valid in thread 0.  Every thread calls it.
-// smem: 2 * kThreads / 32 words.
-__device__ __forceinline__ U128 block_sum128(U128 v, unsigned long long* smem) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    U128 w;
-    w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
-    w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
-    v = add128(v, w);
-  }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) {
-    smem[2 * warp] = v.lo;
-    smem[2 * warp + 1] = v.hi;
-  }
-  __syncthreads();
-  U128 s = {0ull, 0ull};
-  if (threadIdx.x == 0)
-    for (int i = 0; i < kThreads / 32; ++i) s = add128(s, U128{smem[2 * i], smem[2 * i + 1]});
-  return s;
-}
-
 // The exact sums go through a shared-memory table of the integers r (r =
 // |value| * 2^9 for E4M3, |value| * 2^16 for E5M2; 0 for the non-finite
 // codes, which set found_inf instead), so that a code costs one byte
@@ -589,19 +566,50 @@ struct SqTab {
   }
 };
 
+// Shared memory of sq_commit: each warp's partial sum and flag, in two
+// buffers used in turn.
+struct SqRed {
+  unsigned long long w[2][3 * (kThreads / 32)];
+};
+
 // End of a run of chunks of tensor t for a table-summing pass: the CTA's
-// exact sum goes to the tensor's 128-bit slot (as in sq_commit), and
-// found_inf is set when any thread saw a non-finite value (`bad`, from the
-// codes and the tensor's overflow threshold).  Every thread calls it.
-__device__ __forceinline__ void sq_commit_flag(const SqTab& a, uint32_t t,
-                                               bool nonempty, uint32_t bad,
-                                               unsigned long long* sums,
-                                               unsigned long long* found,
-                                               uint32_t epoch,
-                                               unsigned long long* red64) {
-  const U128 s = block_sum128(a.sum(), red64);
-  const int any_bad = __syncthreads_or(bad != 0);
+// exact sum (each thread's `sum`, in units of 2^-32) goes to the tensor's
+// 128-bit slot (sums[2t], sums[2t + 1]; the low word's carry goes to the
+// high word), and found_inf is set when any thread saw a non-finite value
+// (`bad`, from the codes and the tensor's overflow threshold).  Warps reduce
+// by shuffles; one CTA barrier then lets thread 0 add the warps' parts.  The
+// buffers alternate (turn), so a warp writing the next commit's part cannot
+// overtake thread 0's reading of this one: it first passes the barrier of
+// the commit in between, which thread 0 reaches only after its reads.
+// Every thread calls it, with the same nonempty and turn.
+__device__ __forceinline__ void sq_commit(U128 v, uint32_t bad, uint32_t t,
+                                          bool nonempty, unsigned long long* sums,
+                                          unsigned long long* found,
+                                          uint32_t epoch, SqRed& red,
+                                          uint32_t& turn) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    U128 w;
+    w.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
+    w.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
+    v = add128(v, w);
+  }
+  const bool wbad = __any_sync(0xFFFFFFFFu, bad != 0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned long long* buf = red.w[turn];
+  if (lane == 0) {
+    buf[3 * warp] = v.lo;
+    buf[3 * warp + 1] = v.hi;
+    buf[3 * warp + 2] = wbad ? 1ull : 0ull;
+  }
+  __syncthreads();
   if (threadIdx.x == 0 && nonempty) {
+    U128 s = {0ull, 0ull};
+    unsigned long long any_bad = 0;
+    for (int i = 0; i < kThreads / 32; ++i) {
+      s = add128(s, U128{buf[3 * i], buf[3 * i + 1]});
+      any_bad |= buf[3 * i + 2];
+    }
     if (s.lo | s.hi) {
       const unsigned long long old = atomicAdd(&sums[2 * t], s.lo);
       const unsigned long long carry = old + s.lo < old ? 1ull : 0ull;
@@ -609,6 +617,7 @@ __device__ __forceinline__ void sq_commit_flag(const SqTab& a, uint32_t t,
     }
     if (any_bad) atomicMax(found, slot_tag(epoch, 1u));
   }
+  turn ^= 1u;
 }
 
 // A thread's exact sum of squared code values for one code format (the
@@ -678,17 +687,6 @@ struct SqSum<kE5M2> {
   }
   __device__ __forceinline__ void clear() { lo = hi = 0; }
 };
-
-// sq_commit_flag of a thread's sum in units of 2^-32.
-__device__ __forceinline__ void sq_commit_sum(U128 sum, uint32_t t, bool nonempty,
-                                              uint32_t bad, unsigned long long* sums,
-                                              unsigned long long* found,
-                                              uint32_t epoch,
-                                              unsigned long long* red64) {
-  SqTab a;
-  a.s5 = sum;   // s4 stays 0: a.sum() is `sum`
-  sq_commit_flag(a, t, nonempty, bad, sums, found, epoch, red64);
-}
 
 template <int FMT>
 __device__ __forceinline__ void sq_table_fill_fmt(typename SqSum<FMT>::Table& t) {

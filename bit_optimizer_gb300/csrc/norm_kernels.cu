@@ -141,7 +141,7 @@ grad_norm_kernel(const StepDesc* __restrict__ descs,
                  unsigned long long* __restrict__ found, uint32_t epoch) {
   const float ils = ils_dev != nullptr ? *ils_dev : ils_h;
   __shared__ SqTable tab;
-  __shared__ unsigned long long red64[2 * (kThreads / 32)];
+  __shared__ SqRed red;
   const uint32_t c0 = (uint32_t)((uint64_t)blockIdx.x * nchunks / gridDim.x);
   const uint32_t c1 = (uint32_t)((uint64_t)(blockIdx.x + 1) * nchunks / gridDim.x);
   if (c0 >= c1) return;   // uniform over the CTA
@@ -150,7 +150,7 @@ grad_norm_kernel(const StepDesc* __restrict__ descs,
   if (cur.full()) load_half(a, cur.g + cur.begin);
   sq_table_fill(tab);
   SqTab acc;
-  uint32_t bad = 0, tadd = 0, tensor = 0xFFFFFFFFu;
+  uint32_t bad = 0, tadd = 0, tensor = 0xFFFFFFFFu, turn = 0;
   bool nonempty = false;
   for (uint32_t c = c0; c < c1; ++c) {
     const bool more = c + 1 < c1;
@@ -158,7 +158,7 @@ grad_norm_kernel(const StepDesc* __restrict__ descs,
     if (more) nxt = norm_chunk(descs, chunks, c + 1);
     if (cur.tensor != tensor) {   // uniform over the CTA
       if (tensor != 0xFFFFFFFFu) {
-        sq_commit_flag(acc, tensor, nonempty, bad, sums, found, epoch, red64);
+        sq_commit(acc.sum(), bad, tensor, nonempty, sums, found, epoch, red, turn);
         acc = SqTab();
         bad = 0;
         nonempty = false;
@@ -187,7 +187,7 @@ grad_norm_kernel(const StepDesc* __restrict__ descs,
     }
     cur = nxt;
   }
-  sq_commit_flag(acc, tensor, nonempty, bad, sums, found, epoch, red64);
+  sq_commit(acc.sum(), bad, tensor, nonempty, sums, found, epoch, red, turn);
 }
 
 // Per-record terms fl64(k^2 * fl64(S) * 2^-32) (k^2 is exact in double), one

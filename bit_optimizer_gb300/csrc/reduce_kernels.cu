@@ -514,8 +514,9 @@ __device__ __forceinline__ void encode_pass(const ReduceDesc* __restrict__ descs
                                             uint32_t epoch, const RedSq& sq,
                                             float* r_s,
                                             const typename SqSum<OUT>::Table* tab,
-                                            unsigned long long* red64) {
+                                            SqRed* red) {
   SqSum<OUT> acc(tab);
+  uint32_t turn = 0;
   for (uint32_t r = blockIdx.x; r < nchunks; r += gridDim.x) {
     const Chunk ch = chunks[nchunks - 1 - r];
     const ReduceDesc d = descs[ch.tensor];
@@ -541,8 +542,8 @@ __device__ __forceinline__ void encode_pass(const ReduceDesc* __restrict__ descs
       thread_reduce_encode<IN, OUT, false, SQ>(d, k, r_s, post, scale, begin, end,
                                                acc, tadd, bad);
     if (SQ) {
-      sq_commit_sum(acc.sum(), ch.tensor, end > begin, bad, sq.sums, sq.found,
-                    epoch, red64);
+      sq_commit(acc.sum(), bad, ch.tensor, end > begin, sq.sums, sq.found, epoch,
+                *red, turn);
       acc.clear();
     }
   }
@@ -587,10 +588,10 @@ reduce_encode_sq_kernel(const ReduceDesc* __restrict__ descs,
                         uint32_t epoch, RedSq sq) {
   __shared__ float r_s[kMaxShards];
   __shared__ typename SqSum<OUT>::Table tab;
-  __shared__ unsigned long long red64[2 * (kThreads / 32)];
+  __shared__ SqRed red;
   sq_table_fill_fmt<OUT>(tab);
   encode_pass<IN, OUT, true, KS>(descs, chunks, nchunks, KS > 0 ? KS : k, post,
-                                 slots, epoch, sq, r_s, &tab, red64);
+                                 slots, epoch, sq, r_s, &tab, &red);
 }
 
 // Per-item norm terms of the reduced tensors (k = ils / the output scale);
