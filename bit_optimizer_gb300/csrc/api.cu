@@ -86,7 +86,7 @@ cudaError_t launch_grad_norm_terms(const StepDesc* descs, const Chunk* chunks,
                                    unsigned long long* sums,
                                    unsigned long long* found, uint32_t epoch,
                                    double* terms, uint32_t* found_out, int grid,
-                                   cudaStream_t stream, LaunchMark mark);
+                                   int fmts, cudaStream_t stream, LaunchMark mark);
 cudaError_t launch_clip_coef(const double* terms, int n,
                              const unsigned long long* found_slot, uint32_t epoch,
                              const uint32_t* found_flag, float max_norm,
@@ -186,6 +186,7 @@ struct Workspace {
   DevBuf step_descs, step_chunks;
   uint32_t step_nchunks = 0, step_nchunks_o3 = 0;
   bool step_any_vs = false;   // some record has a scaled second moment
+  int step_fmts = 0;          // bit f: some record has gradient codes of format f
   uint32_t begin_epoch = 0;   // epoch of an fp8_adam_step_begin awaiting its finish
   uint32_t copy_epoch = 0;    // epoch of a finish awaiting its fp8_adam_step_copy
   // reduction tables
@@ -733,7 +734,11 @@ int ensure_step_tables(const char* fn, Workspace* ws, const fp8opt_param* params
   ws->step_nchunks = nmain;
   ws->step_nchunks_o3 = no3;
   ws->step_any_vs = false;
-  for (int i = 0; i < n; ++i) ws->step_any_vs |= params[i].v_bound != nullptr;
+  ws->step_fmts = 0;
+  for (int i = 0; i < n; ++i) {
+    ws->step_any_vs |= params[i].v_bound != nullptr;
+    ws->step_fmts |= 1 << params[i].g_fmt;
+  }
   ws->have_step = true;
   return FP8OPT_OK;
 }
@@ -1142,8 +1147,8 @@ int adam_step(const char* fn, bool l2, const fp8opt_param* params, int n,
   if (nr.on) {
     e = launch_grad_norm_terms(c.descs, c.chunks, ws->step_nchunks, n,
                                inv_loss_scale, nullptr, c.sums, c.sc.found,
-                               c.epoch, c.terms, nullptr, c.info->grad_norm, stream,
-                               launch_mark());
+                               c.epoch, c.terms, nullptr, c.info->grad_norm,
+                               ws->step_fmts, stream, launch_mark());
     if (e == cudaSuccess)
       e = launch_clip_coef(c.terms, n, c.sc.found, c.epoch, nullptr,
                            run_step ? nr.max_norm : 0.0f, c.norm, c.clip,
@@ -1217,8 +1222,8 @@ extern "C" int fp8_grad_norm_terms(const fp8opt_param* params, int n,
     return st;
   cudaError_t e = launch_grad_norm_terms(
       c.descs, c.chunks, c.ws->step_nchunks, n, inv_loss_scale, nullptr, c.sums,
-      c.sc.found, c.epoch, terms_dev, found_dev, c.info->grad_norm, stream,
-      launch_mark());
+      c.sc.found, c.epoch, terms_dev, found_dev, c.info->grad_norm,
+      c.ws->step_fmts, stream, launch_mark());
   if (e != cudaSuccess) return cuda_fail(e, "fp8_grad_norm_terms: launch");
   return FP8OPT_OK;
 }
@@ -1651,8 +1656,8 @@ static int cast_adam_clipped(const char* fn, const fp8opt_cast_item* grads,
                                 inv_loss_scale, ils_dev, stream, mark);
     if (e == cudaSuccess)
       e = launch_grad_norm_terms(sdescs, schunks, 0, n, inv_loss_scale, ils_dev,
-                                 sums, sc.found, epoch, terms, nullptr, 0, stream,
-                                 mark);
+                                 sums, sc.found, epoch, terms, nullptr, 0,
+                                 ws->step_fmts, stream, mark);
     if (e == cudaSuccess)
       e = launch_clip_coef(terms, n, sc.found, epoch, nullptr, max_grad_norm, norm,
                            clip, grad_norm_dev, stream, mark);

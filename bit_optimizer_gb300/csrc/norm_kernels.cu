@@ -47,39 +47,72 @@ __device__ __forceinline__ void load_half(HalfTile& h, const uint8_t* p) {
     h.c[q] = ld_once2(p + q * (kThreads * kGroup) + threadIdx.x * kGroup);
 }
 
+// A thread's exact sums in the norm pass.  kNormAny: a list of either code
+// format, per tensor, through SqTable (E5M2 squares in 128 bits).
+// kNormE5M2: every tensor has E5M2 codes, through SqSum<kE5M2> (two 64-bit
+// sums, a 64-bit table entry per code).
+constexpr int kNormAny = 0;
+constexpr int kNormE5M2 = 1;
+
+template <int MODE>
+struct NormAcc;
+
+template <>
+struct NormAcc<kNormAny> {
+  using Table = SqTable;
+  const SqTable* tab;
+  SqTab s;
+  __device__ __forceinline__ explicit NormAcc(const SqTable* t) : tab(t) {}
+  template <int GF>
+  __device__ __forceinline__ void add(uint32_t wm) {
+    s.add_word<GF>(wm, sq_lane_byte<GF>(), *tab);
+  }
+  __device__ __forceinline__ U128 sum() const { return s.sum(); }
+  __device__ __forceinline__ void clear() { s = SqTab(); }
+};
+
+template <>
+struct NormAcc<kNormE5M2> {
+  using Table = Sq5Table;
+  SqSum<kE5M2> s;
+  __device__ __forceinline__ explicit NormAcc(const Sq5Table* t) : s(t) {}
+  template <int GF>
+  __device__ __forceinline__ void add(uint32_t wm) { s.add_word(wm); }
+  __device__ __forceinline__ U128 sum() const { return s.sum(); }
+  __device__ __forceinline__ void clear() { s.clear(); }
+};
+
 // Adds a loaded half tile to acc; bad collects the codes at or above the
 // tensor's overflow threshold (addend tadd).
-template <int GF>
+template <int GF, class Acc>
 __device__ __forceinline__ void sum_half(const HalfTile& h, uint32_t tadd,
-                                         const SqTable& tab, SqTab& acc,
-                                         uint32_t& bad) {
-  const uint32_t lb = sq_lane_byte<GF>();
+                                         Acc& acc, uint32_t& bad) {
 #pragma unroll
   for (int q = 0; q < kHalfGroups; ++q) {
     const uint32_t a = h.c[q].x & 0x7F7F7F7Fu, b = h.c[q].y & 0x7F7F7F7Fu;
     bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
-    acc.add_word<GF>(a, lb, tab);
-    acc.add_word<GF>(b, lb, tab);
+    acc.template add<GF>(a);
+    acc.template add<GF>(b);
   }
 }
 
+template <int MODE>
 __device__ __forceinline__ void sum_half_fmt(const HalfTile& h, int fmt,
-                                             uint32_t tadd, const SqTable& tab,
-                                             SqTab& acc, uint32_t& bad) {
-  if (fmt == kE4M3)
-    sum_half<kE4M3>(h, tadd, tab, acc, bad);
+                                             uint32_t tadd, NormAcc<MODE>& acc,
+                                             uint32_t& bad) {
+  if (MODE == kNormAny && fmt == kE4M3)
+    sum_half<kE4M3>(h, tadd, acc, bad);
   else
-    sum_half<kE5M2>(h, tadd, tab, acc, bad);
+    sum_half<kE5M2>(h, tadd, acc, bad);
 }
 
 // This thread's share of a chunk that is not full ([begin, end) shorter than
 // kChunkElems, or codes without vector loads): whole 8-code groups as
 // vectors where they can be, the rest by code.
-template <int GF>
+template <int GF, class Acc>
 __device__ void thread_norm_part(const uint8_t* g, int64_t begin, int64_t end,
-                                 bool vec, uint32_t tadd, const SqTable& tab,
-                                 SqTab& acc, uint32_t& bad) {
-  const uint32_t lb = sq_lane_byte<GF>();
+                                 bool vec, uint32_t tadd, Acc& acc,
+                                 uint32_t& bad) {
 #pragma unroll 1
   for (int64_t i0 = begin + threadIdx.x * kGroup; i0 < end;
        i0 += kThreads * kGroup) {
@@ -87,14 +120,14 @@ __device__ void thread_norm_part(const uint8_t* g, int64_t begin, int64_t end,
       const uint2 c = ld_once2(g + i0);
       const uint32_t a = c.x & 0x7F7F7F7Fu, b = c.y & 0x7F7F7F7Fu;
       bad |= ((a + tadd) | (b + tadd)) & 0x80808080u;
-      acc.add_word<GF>(a, lb, tab);
-      acc.add_word<GF>(b, lb, tab);
+      acc.template add<GF>(a);
+      acc.template add<GF>(b);
       continue;
     }
     for (int e = 0; e < kGroup && i0 + e < end; ++e) {
       const uint32_t a = g[i0 + e] & 0x7Fu;
       bad |= (a + tadd) & 0x80u;
-      acc.add_word<GF>(a, lb, tab);    // bytes 1..3 are zero: magnitude 0
+      acc.template add<GF>(a);    // bytes 1..3 are zero: magnitude 0
     }
   }
 }
@@ -132,7 +165,9 @@ __device__ __forceinline__ NormChunk norm_chunk(const StepDesc* descs,
 // so a large tensor's chunks reach it as one run; a run adds to one
 // accumulator, which goes to the tensor's slot when the tensor changes: one
 // CTA reduction per run instead of one per chunk.  The next chunk's record
-// is read while the current one is summed.
+// is read while the current one is summed.  MODE: kNormAny, or kNormE5M2
+// when every tensor of the call has E5M2 codes.
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, FP8OPT_NORM_MIN_BLOCKS)
 grad_norm_kernel(const StepDesc* __restrict__ descs,
                  const Chunk* __restrict__ chunks, uint32_t nchunks, float ils_h,
@@ -140,7 +175,7 @@ grad_norm_kernel(const StepDesc* __restrict__ descs,
                  unsigned long long* __restrict__ sums,
                  unsigned long long* __restrict__ found, uint32_t epoch) {
   const float ils = ils_dev != nullptr ? *ils_dev : ils_h;
-  __shared__ SqTable tab;
+  __shared__ typename NormAcc<MODE>::Table tab;
   __shared__ SqRed red;
   const uint32_t c0 = (uint32_t)((uint64_t)blockIdx.x * nchunks / gridDim.x);
   const uint32_t c1 = (uint32_t)((uint64_t)(blockIdx.x + 1) * nchunks / gridDim.x);
@@ -148,8 +183,11 @@ grad_norm_kernel(const StepDesc* __restrict__ descs,
   NormChunk cur = norm_chunk(descs, chunks, c0);
   HalfTile a, b;          // a holds the current chunk's first half if full
   if (cur.full()) load_half(a, cur.g + cur.begin);
-  sq_table_fill(tab);
-  SqTab acc;
+  if constexpr (MODE == kNormAny)
+    sq_table_fill(tab);
+  else
+    sq5_table_fill(tab);
+  NormAcc<MODE> acc(&tab);
   uint32_t bad = 0, tadd = 0, tensor = 0xFFFFFFFFu, turn = 0;
   bool nonempty = false;
   for (uint32_t c = c0; c < c1; ++c) {
@@ -159,7 +197,7 @@ grad_norm_kernel(const StepDesc* __restrict__ descs,
     if (cur.tensor != tensor) {   // uniform over the CTA
       if (tensor != 0xFFFFFFFFu) {
         sq_commit(acc.sum(), bad, tensor, nonempty, sums, found, epoch, red, turn);
-        acc = SqTab();
+        acc.clear();
         bad = 0;
         nonempty = false;
       }
@@ -167,23 +205,24 @@ grad_norm_kernel(const StepDesc* __restrict__ descs,
       // found_inf exactly as the step's first pass decides it: some code at
       // or above the overflow threshold of k = inv_loss_scale / g_scale
       const float k = __fdiv_rn(ils, *cur.g_scale);
-      tadd = threshold_addend(cur.fmt == kE4M3 ? overflow_threshold<kE4M3>(k)
-                                               : overflow_threshold<kE5M2>(k));
+      tadd = threshold_addend(MODE == kNormAny && cur.fmt == kE4M3
+                                  ? overflow_threshold<kE4M3>(k)
+                                  : overflow_threshold<kE5M2>(k));
     }
     nonempty |= cur.len > 0;
     const bool next_full = more && nxt.full();
     if (cur.full()) {
       load_half(b, cur.g + cur.begin + kHalfTile);
-      sum_half_fmt(a, cur.fmt, tadd, tab, acc, bad);
+      sum_half_fmt<MODE>(a, cur.fmt, tadd, acc, bad);
       if (next_full) load_half(a, nxt.g + nxt.begin);
-      sum_half_fmt(b, cur.fmt, tadd, tab, acc, bad);
+      sum_half_fmt<MODE>(b, cur.fmt, tadd, acc, bad);
     } else {
       if (next_full) load_half(a, nxt.g + nxt.begin);
       const int64_t end = cur.begin + cur.len;
-      if (cur.fmt == kE4M3)
-        thread_norm_part<kE4M3>(cur.g, cur.begin, end, cur.vec, tadd, tab, acc, bad);
+      if (MODE == kNormAny && cur.fmt == kE4M3)
+        thread_norm_part<kE4M3>(cur.g, cur.begin, end, cur.vec, tadd, acc, bad);
       else
-        thread_norm_part<kE5M2>(cur.g, cur.begin, end, cur.vec, tadd, tab, acc, bad);
+        thread_norm_part<kE5M2>(cur.g, cur.begin, end, cur.vec, tadd, acc, bad);
     }
     cur = nxt;
   }
@@ -366,18 +405,24 @@ cudaError_t launch_limbs_terms(const long long* limbs, const uint32_t* amax_bits
 // The norm pass and the per-record terms on `stream`.  sums: 2n zeroed words;
 // found: the call's found_inf slot; terms: n doubles out; found_out: the
 // call's found_inf as 0 / 1, or NULL.  ils_dev: inv_loss_scale in device
-// memory instead of ils, or NULL.
+// memory instead of ils, or NULL.  fmts: bit f set when some record has
+// codes of format f.
 cudaError_t launch_grad_norm_terms(const StepDesc* descs, const Chunk* chunks,
                                    uint32_t nchunks, int n, float ils,
                                    const float* ils_dev,
                                    unsigned long long* sums,
                                    unsigned long long* found, uint32_t epoch,
                                    double* terms, uint32_t* found_out, int grid,
-                                   cudaStream_t stream, LaunchMark mark) {
+                                   int fmts, cudaStream_t stream, LaunchMark mark) {
   if (nchunks != 0) {
     if (mark) mark(kGradNormK, 0, stream);
-    grad_norm_kernel<<<grid_min((uint32_t)grid, nchunks), kThreads, 0, stream>>>(
-        descs, chunks, nchunks, ils, ils_dev, sums, found, epoch);
+    const uint32_t g = grid_min((uint32_t)grid, nchunks);
+    if (fmts == (1 << kE5M2))
+      grad_norm_kernel<kNormE5M2><<<g, kThreads, 0, stream>>>(
+          descs, chunks, nchunks, ils, ils_dev, sums, found, epoch);
+    else
+      grad_norm_kernel<kNormAny><<<g, kThreads, 0, stream>>>(
+          descs, chunks, nchunks, ils, ils_dev, sums, found, epoch);
     if (mark) mark(kGradNormK, 1, stream);
   }
   if (n > 0) {
@@ -414,8 +459,8 @@ cudaError_t launch_found(unsigned long long* slot, uint32_t epoch,
 }
 
 cudaError_t grad_norm_occupancy(int* per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, grad_norm_kernel,
-                                                       kThreads, 0);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      per_sm, grad_norm_kernel<kNormAny>, kThreads, 0);
 }
 
 }  // namespace fp8opt

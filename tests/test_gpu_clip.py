@@ -52,6 +52,25 @@ def test_grad_norm_bit_exact(bo, fmt, ils):
     assert norm == rn, (norm, rn)
 
 
+def test_grad_norm_mixed_formats(bo):
+    """A list whose tensors alternate E4M3 and E5M2 codes (runs of one
+    tensor's chunks, whole chunks and ragged ends, in both formats within
+    one CTA's range): the norm bit-exact against the oracle."""
+    wl = synth.o2_6p7b_tail(n_layer=1, d=128, ffn=512, vocab=3000, ctx=64,
+                            n_tail=40)
+    grads = wl.grads(1)
+    fmts = [E4M3 if i % 2 == 0 else E5M2 for i in range(len(grads))]
+    states = fresh_states(wl.weights(), o3=False)
+    for i, (s, g) in enumerate(zip(states, grads)):
+        codes, _, scale = oracle_cast([g], fmts[i])
+        s.g_fmt = fmts[i]
+        set_grads([s], codes, scale)
+    gpu = GpuState([s.copy() for s in states])
+    for ils in (1.0, 0.37):
+        found, norm = gpu_norm(gpu, ils)
+        assert (found, norm) == oracle.grad_norm(states, ils)
+
+
 def test_grad_norm_exactness_case(bo):
     """One E5M2 maximum and 4096 minimum subnormals: only an exact sum keeps
     the small squares (the oracle's exactness pin, on the GPU)."""
