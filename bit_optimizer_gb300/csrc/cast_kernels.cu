@@ -401,8 +401,10 @@ __device__ __forceinline__ EncChunk enc_chunk(const CastDesc* descs,
 }
 
 // The encode pass with the exact squares through the shared-memory table of
-// the integer square roots (SqTable).  It walks the chunk table backwards in
-// CTA strides, as the plain encode pass does.
+// the integer square roots (SqSum<FMT>: SqTable for E4M3, Sq5Table for
+// E5M2).  It walks the chunk table backwards in CTA strides, as the plain
+// encode pass does; chunks of one tensor are adjacent in the table, so a
+// tensor's chunks reach a CTA as one run.
 template <int FMT>
 constexpr int encsq_min_blocks() {
   return FMT == kE4M3 ? FP8OPT_ENCSQ_MIN_BLOCKS : FP8OPT_ENCSQ5_MIN_BLOCKS;

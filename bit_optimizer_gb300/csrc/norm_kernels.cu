@@ -2,11 +2,13 @@
 // coefficient that follows from it (torch.nn.utils.clip_grad_norm_, the run
 // script's --clip-grad).
 //
-// grad_norm_kernel: a persistent grid over the step's chunk table; each
-// chunk's exact sum of squared code values (read from a shared-memory table
-// of the integer square roots: SqTable and SqTab, fp8opt_internal.cuh) goes
-// to its tensor's 128-bit slot, and found_inf is decided exactly as the
-// step's first pass does (the chunk's overflow threshold).
+// grad_norm_kernel: a persistent grid over the step's chunk table, each CTA
+// walking one contiguous range of it; the exact sum of squared code values
+// of each run of one tensor's chunks (read from a shared-memory table of the
+// integer square roots: SqTable and SqTab, or for an all-E5M2 list Sq5Table
+// and SqSum, fp8opt_internal.cuh) goes to the tensor's 128-bit slot, and
+// found_inf is decided exactly as the step's first pass does (the tensor's
+// overflow threshold).
 //
 // grad_norm_terms_kernel: one thread per record, term_t = fl64(k_t^2 *
 // fl64(S_t) * 2^-32) (k_t^2 is exact in double).
