@@ -159,6 +159,22 @@ def test_o2_6p7b_tail_full_10_steps(bo):
     assert dl.m_scale[zero].item() == 1.0 and not bool(dl.m[zero].any().item())
 
 
+def test_o2_6p7b_tail_every_tensor(bo):
+    """The 6.7B long-tail list through the fused call (the bench's workload
+    and configuration), with the oracle stepping all 589 tensors from the
+    same inputs: every gradient code, m, v and weight element and every scale
+    of 6.66 G parameters, over two steps so the moments carry history.  About
+    40 GB of host memory for the oracle's state and 3 to 4 minutes on a
+    16-core host."""
+    wl = synth.o2_6p7b_tail()
+    workers = max(1, min(32, os.cpu_count() or 1))
+    sample = list(range(len(wl.shapes)))
+    with cf.ThreadPoolExecutor(workers) as pool:
+        dl, _ = lockstep_full(wl, 2, sample, fused=True, pool=pool,
+                              workers=workers)
+    dl.invariants()
+
+
 def test_o2_6p7b_tail_full_scaled_v(bo):
     """The long-tail list with the scaled second moment, through the fused
     call, 3 steps."""
