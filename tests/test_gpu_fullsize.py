@@ -76,7 +76,9 @@ def lockstep_full(wl, steps, sample, first=1, fused=False, scaled_v=False,
             f = dl.cast_step(t)
             each(lambda i: dl.check_cast([i], states), sample)
         else:
-            dl.cast_and_check(sample, states)
+            dl.cast()
+            torch.cuda.synchronize()
+            each(lambda i: dl.check_cast([i], states), sample)
             for i in sample:
                 dl.put(i, states[i])
             f = dl.step(t)
@@ -89,36 +91,50 @@ def lockstep_full(wl, steps, sample, first=1, fused=False, scaled_v=False,
 
 
 def test_o2_350m_full_inf_skip_and_step(bo):
+    """The 350M list, every tensor against the oracle: the warm-up steps, a
+    step whose gradients hold one +inf (nothing may change), and the same
+    step with the inf cleared."""
     wl = synth.o2_350m()
     clean = dataclasses.replace(wl, inf_site=None)
-    sample = sample_of(wl, 3_000_000)
-    assert wl.inf_site[0] in sample
-    dl, states = lockstep_full(clean, wl.warmup_steps, sample)
-    t = wl.warmup_steps + 1
-    # the measured step's gradients hold one +inf: nothing may change
-    dl.gen_grads(t, wl)
-    dl.cast_and_check(sample, states)
-    for i in sample:
-        dl.put(i, states[i])
-    sums = [(x.sum(dtype=torch.int64).item(), x.numel()) for x in dl.m]
-    vsum = [x.view(torch.int16).sum(dtype=torch.int64).item() for x in dl.v]
-    wsum = [x.view(torch.int16).sum(dtype=torch.int64).item() for x in dl.w]
-    mscale = dl.m_scale.clone()
-    assert oracle_step([states[i] for i in sample], wl, t) == 1
-    assert dl.step(t) == 1 and dl.found_dev.item() == 1
-    assert sums == [(x.sum(dtype=torch.int64).item(), x.numel()) for x in dl.m]
-    assert vsum == [x.view(torch.int16).sum(dtype=torch.int64).item() for x in dl.v]
-    assert wsum == [x.view(torch.int16).sum(dtype=torch.int64).item() for x in dl.w]
-    assert torch.equal(mscale, dl.m_scale)
-    # the same step with the inf cleared
-    dl.gen_grads(t, clean)
-    dl.cast_and_check(sample, states)
-    for i in sample:
-        dl.put(i, states[i])
-    assert oracle_step([states[i] for i in sample], wl, t) == 0
-    assert dl.step(t) == 0
-    for i in sample:
-        dl.compare(i, states[i])
+    sample = list(range(len(wl.shapes)))
+    workers = max(1, min(32, os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(workers) as pool:
+        dl, states = lockstep_full(clean, wl.warmup_steps, sample, pool=pool,
+                                   workers=workers)
+        t = wl.warmup_steps + 1
+        listed = [states[i] for i in sample]
+        # the measured step's gradients hold one +inf: nothing may change
+        dl.gen_grads(t, wl)
+        dl.cast()
+        torch.cuda.synchronize()
+        list(pool.map(lambda i: dl.check_cast([i], states), sample))
+        for i in sample:
+            dl.put(i, states[i])
+        sums = [(x.sum(dtype=torch.int64).item(), x.numel()) for x in dl.m]
+        vsum = [x.view(torch.int16).sum(dtype=torch.int64).item() for x in dl.v]
+        wsum = [x.view(torch.int16).sum(dtype=torch.int64).item() for x in dl.w]
+        mscale = dl.m_scale.clone()
+        # found_inf is the maximum over the oracle's groups (the inf is in
+        # one); the groups without it would step, so they run on copies
+        probe = [st.copy() for st in listed]
+        assert oracle_step_threads(probe, wl, t, pool, workers) == 1
+        del probe
+        assert dl.step(t) == 1 and dl.found_dev.item() == 1
+        assert sums == [(x.sum(dtype=torch.int64).item(), x.numel()) for x in dl.m]
+        assert vsum == [x.view(torch.int16).sum(dtype=torch.int64).item() for x in dl.v]
+        assert wsum == [x.view(torch.int16).sum(dtype=torch.int64).item() for x in dl.w]
+        assert torch.equal(mscale, dl.m_scale)
+        # the same step with the inf cleared
+        dl.gen_grads(t, clean)
+        dl.cast()
+        torch.cuda.synchronize()
+        list(pool.map(lambda i: dl.check_cast([i], states), sample))
+        for i in sample:
+            dl.put(i, states[i])
+        listed = [states[i] for i in sample]
+        assert oracle_step_threads(listed, wl, t, pool, workers) == 0
+        assert dl.step(t) == 0
+        list(pool.map(lambda i: dl.compare(i, states[i]), sample))
     dl.invariants()
 
 
