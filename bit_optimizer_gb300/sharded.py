@@ -271,6 +271,60 @@ class ShardedFp8AdamW:
         self._norm = torch.zeros(1, dtype=torch.float64, device=dev)
         self._clip = torch.ones(1, **f32)
 
+    def state_dict(self) -> dict:
+        """This rank's optimizer state: its pieces' E4M3 first moments, FP16
+        second moments, their scales (and second-moment bounds); for O3 the
+        FP16 masters of its pieces and every tensor's E4M3 weight copy with
+        its scale and amax; the step count and hyperparameters; and the
+        layout the state belongs to (ranks, this rank, the tensors' sizes),
+        which load_state_dict checks.  The O2 weights are the model's: every
+        rank holds all of them after a step."""
+        d = {"step": self.step_count, "level": self.level,
+             "grad_fmt": self.grad_fmt,
+             "hparams": (self.lr, self.beta1, self.beta2, self.eps, self.wd),
+             "l2": self.l2, "max_grad_norm": self.max_grad_norm,
+             "world": self.world, "rank": self.rank,
+             "numels": list(self.numels), "pieces": list(self.pieces),
+             "m": [t.clone() for t in self.m], "v": [t.clone() for t in self.v],
+             "m_scale": self.m_scale.clone(),
+             "v_bound": None if self.v_bound is None else self.v_bound.clone()}
+        if self.level == "O3":
+            off = self.off
+            d["master"] = [self._w_flat[off[t] + a:off[t] + b].clone()
+                           for t, a, b in self.pieces]
+            d["w8"] = [t.clone() for t in self.w8]
+            d["w8_scale"] = self.w8_scale.clone()
+            d["w8_amax"] = self.w8_amax.clone()
+        return d
+
+    def load_state_dict(self, d: dict) -> None:
+        """Restores a state_dict of the same rank of the same layout (level,
+        number of ranks, tensor sizes); raises ValueError otherwise."""
+        if (d["level"] != self.level or d["world"] != self.world or
+                d["rank"] != self.rank or list(d["numels"]) != self.numels or
+                [tuple(p) for p in d["pieces"]] != [tuple(p) for p in self.pieces]):
+            raise ValueError("state dict does not match this optimizer's level, "
+                             "ranks or tensors")
+        if (d.get("v_bound") is None) != (self.v_bound is None):
+            raise ValueError("state dict and optimizer differ in scaled_v")
+        self.step_count = int(d["step"])
+        self.lr, self.beta1, self.beta2, self.eps, self.wd = d["hparams"]
+        for dst, src in zip(self.m, d["m"]):
+            dst.copy_(src)
+        for dst, src in zip(self.v, d["v"]):
+            dst.copy_(src)
+        self.m_scale.copy_(d["m_scale"])
+        if self.v_bound is not None:
+            self.v_bound.copy_(d["v_bound"])
+        if self.level == "O3":
+            off = self.off
+            for (t, a, b), src in zip(self.pieces, d["master"]):
+                self._w_flat[off[t] + a:off[t] + b].copy_(src)
+            for dst, src in zip(self.w8, d["w8"]):
+                dst.copy_(src)
+            self.w8_scale.copy_(d["w8_scale"])
+            self.w8_amax.copy_(d["w8_amax"])
+
     def _cast_plan(self, grads):
         key = tuple((g.data_ptr(), g.numel(), g.dtype) for g in grads)
         if key != self._cast_key:

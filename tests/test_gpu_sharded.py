@@ -181,3 +181,78 @@ def test_sharded_equals_whole_and_oracle(bo, case, world):
         check_f16(to_np_u16(whole["w"][i]), st.w, name=f"w[{i}]")
         if cfg["level"] == "O3":
             check_codes(to_np_u8(whole["w8"][i]), st.w8, name=f"w8[{i}]")
+
+
+def _state_bytes(opt):
+    out = {"m_scale": opt.m_scale.clone()}
+    for j, (t, a, b) in enumerate(opt.pieces):
+        out[f"m{j}"] = opt.m[j].clone()
+        out[f"v{j}"] = opt.v[j].clone()
+        out[f"w{j}"] = opt.weights[t][a:b].clone()
+    if opt.v_bound is not None:
+        out["v_bound"] = opt.v_bound.clone()
+    if opt.level == "O2":
+        for i, w in enumerate(opt.weights):
+            out[f"W{i}"] = w.clone()
+    else:
+        out["w8_scale"] = opt.w8_scale.clone()
+        out["w8_amax"] = opt.w8_amax.clone()
+        for i, c in enumerate(opt.w8):
+            out[f"w8_{i}"] = c.clone()
+    return out
+
+
+@pytest.mark.parametrize("case,world", [("o2", 2), ("o3_clip", 3),
+                                        ("o2_l2_scaled_v_clip", 2), ("o3_clip", 1)])
+def test_sharded_checkpoint_resume_on_the_gpu(bo, case, world):
+    """ShardedFp8AdamW.state_dict / load_state_dict through the library:
+    two steps, a checkpoint (through torch.save), a third step; a fresh
+    optimizer built from the model's weights and loaded from the checkpoint
+    takes the same third step, byte for byte, on every rank."""
+    import io
+    from bit_optimizer_gb300.sharded import ShardedFp8AdamW
+    cfg = CASES[case]
+    wl = workload()
+    shared = {"slots": [None] * world, "barrier": threading.Barrier(world)}
+    results, errors = [None] * world, []
+
+    def rank_main(rank):
+        try:
+            with torch.cuda.stream(torch.cuda.Stream()):
+                kw = dict(lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
+                          weight_decay=wl.wd, level=cfg["level"], l2=cfg["l2"],
+                          scaled_v=cfg["scaled_v"], max_grad_norm=cfg["max_norm"])
+                comm = ThreadComm(rank, world, shared)
+                opt = ShardedFp8AdamW([w.cuda() for w in wl.weights()], comm, **kw)
+                for t in (1, 2):
+                    opt.step([g.cuda() for g in local_grads(wl, t, rank)])
+                buf = io.BytesIO()
+                torch.save(opt.state_dict(), buf)
+                model = [w.clone() for w in opt.weights]
+                grads3 = [g.cuda() for g in local_grads(wl, 3, rank)]
+                opt.step(grads3)
+                first = _state_bytes(opt)
+                again = ShardedFp8AdamW(
+                    model if cfg["level"] == "O2" else [w.cuda() for w in wl.weights()],
+                    comm, **kw)
+                buf.seek(0)
+                again.load_state_dict(torch.load(buf))
+                again.step(grads3)
+                torch.cuda.current_stream().synchronize()
+                results[rank] = (first, _state_bytes(again), again.step_count)
+        except BaseException as e:   # surface a rank's failure in the test
+            errors.append(e)
+            shared["barrier"].abort()
+
+    threads = [threading.Thread(target=rank_main, args=(r,)) for r in range(world)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    if errors:
+        raise errors[0]
+    for first, second, steps in results:
+        assert steps == 3
+        assert sorted(first) == sorted(second)
+        for k in first:
+            assert torch.equal(first[k], second[k]), k

@@ -168,6 +168,92 @@ def test_cpu_ranks_match_the_whole_pipeline(case, world, tmp_path):
         assert found[cfg["inf_at"][0] - 1] == 1 and sum(found) == 1
 
 
+def _dump(opt):
+    """Every state byte of a sharded optimizer, as numpy arrays."""
+    out = {"m_scale": opt.m_scale.numpy().copy(),
+           "pieces": np.array(opt.pieces, dtype=np.int64).reshape(-1, 3)}
+    for i, w in enumerate(opt.weights):
+        out[f"w{i}"] = w.view(torch.int16).numpy().copy()
+    for j in range(len(opt.pieces)):
+        out[f"m_{j}"] = opt.m[j].numpy().copy()
+        out[f"v_{j}"] = opt.v[j].view(torch.int16).numpy().copy()
+    if opt.v_bound is not None:
+        out["v_bound"] = opt.v_bound.numpy().copy()
+    if opt.level == "O3":
+        out["w8_scale"] = opt.w8_scale.numpy().copy()
+        out["w8_amax"] = opt.w8_amax.numpy().copy()
+        for i, c in enumerate(opt.w8):
+            out[f"w8_{i}"] = c.numpy().copy()
+    return out
+
+
+def resume_worker(rank, world, port, cfg, out_dir):
+    """Two steps, a checkpoint (through torch.save), a third step; then a
+    fresh optimizer built from the weights a model checkpoint would hold,
+    the checkpoint loaded, and the same third step."""
+    sys.path[:0] = [ROOT, HERE]
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    import torch.distributed as dist
+    from bit_optimizer_gb300.sharded import ShardedFp8AdamW, TorchDistComm
+    from oracle_engine import OracleEngine
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    wl = workload()
+    kw = dict(lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps,
+              weight_decay=wl.wd, level=cfg["level"], l2=cfg["l2"],
+              scaled_v=cfg["scaled_v"], max_grad_norm=cfg["max_norm"],
+              engine=OracleEngine(), device="cpu")
+    opt = ShardedFp8AdamW(wl.weights(), TorchDistComm(), **kw)
+    for t in (1, 2):
+        opt.step(local_grads(wl, t, rank))
+    path = os.path.join(out_dir, f"ckpt{rank}.pt")
+    torch.save(opt.state_dict(), path)
+    model = [w.clone() for w in opt.weights]     # O2: the model's weights
+    opt.step(local_grads(wl, 3, rank))
+    first = _dump(opt)
+    again = ShardedFp8AdamW(model if cfg["level"] == "O2" else wl.weights(),
+                            TorchDistComm(), **kw)
+    again.load_state_dict(torch.load(path))
+    assert again.step_count == 2
+    again.step(local_grads(wl, 3, rank))
+    second = _dump(again)
+    np.savez(os.path.join(out_dir, f"first{rank}.npz"), **first)
+    np.savez(os.path.join(out_dir, f"second{rank}.npz"), **second)
+    # a checkpoint of another rank, or of another layout, is refused
+    other = torch.load(os.path.join(out_dir, f"ckpt{rank}.pt"))
+    other["rank"] = (rank + 1) % max(world, 2)
+    try:
+        again.load_state_dict(other)
+        refused = 0
+    except ValueError:
+        refused = 1
+    np.save(os.path.join(out_dir, f"refused{rank}.npy"), np.array([refused]))
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("case,world", [("o2", 2), ("o3_clip", 2),
+                                        ("o2_l2_scaled_v_clip", 3), ("o3_clip", 1)])
+def test_checkpoint_resume_is_bit_identical(case, world, tmp_path):
+    """ShardedFp8AdamW.state_dict / load_state_dict: a run resumed from a
+    checkpoint takes the same step, byte for byte, on every rank."""
+    import torch.multiprocessing as mp
+    cfg = CASES[case]
+    mp.spawn(resume_worker, args=(world, free_port(), cfg, str(tmp_path)),
+             nprocs=world, join=True)
+    for r in range(world):
+        a = dict(np.load(tmp_path / f"first{r}.npz"))
+        b = dict(np.load(tmp_path / f"second{r}.npz"))
+        assert sorted(a) == sorted(b)
+        for k in a:
+            if cfg["level"] == "O3" and k.startswith("w") and k[1:].isdigit():
+                continue          # O3 keeps only its pieces' masters (below)
+            assert np.array_equal(a[k], b[k]), (r, k)
+        if cfg["level"] == "O3":
+            for t, lo, hi in a["pieces"]:
+                assert np.array_equal(a[f"w{t}"][lo:hi], b[f"w{t}"][lo:hi]), (r, t)
+        assert int(np.load(tmp_path / f"refused{r}.npy")[0]) == 1
+
+
 def test_layout_covers_every_element_once_and_balances():
     from bit_optimizer_gb300.sharded import layout
     rng = np.random.default_rng(0)
