@@ -11,8 +11,8 @@
  * gradients in FP8; O2 keeps the Adam/AdamW first moment in FP8 and the second
  * moment in FP16 with FP16 weights; O3 adds an FP16 master weight and an FP8
  * regular weight (the level table).  MS-AMP README, "Usage": the GradScaler
- * loop (scale, backward, step) and "Recognized optimizers are torch.optim.Adam
- * and torch.optim.AdamW".  TransformerEngine issue #131: the two FP8 formats
+ * loop (scale, backward, step), and the two torch optimizers it supports,
+ * Adam and AdamW.  TransformerEngine issue #131: the two FP8 formats
  * E4M3 and E5M2.  The pages give neither bit layouts nor a scaling rule nor an
  * update order; the readings used here are:
  *   - E4M3 / E5M2 are the OCP 8-bit floating-point formats (E4M3: bias 7, no
