@@ -39,6 +39,10 @@ def test_our_arm_line():
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] == 4
+    # the link measured alone and the loop's own copies, beside the loop
+    assert e["link_copy_ms"] > 0 and e["link_gbs"] > 0
+    lc = e["loop_copy_ms"]
+    assert 0 < lc["min"] <= lc["median"] <= lc["max"]
     c = d["cpu_baseline"]
     assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0
     assert d["gpu_launches"] == 3 * d["steps"]      # cast amax, fused pass, update
