@@ -87,6 +87,14 @@ cudaError_t launch_grad_norm_terms(const StepDesc* descs, const Chunk* chunks,
                                    unsigned long long* found, uint32_t epoch,
                                    double* terms, uint32_t* found_out, int grid,
                                    int fmts, cudaStream_t stream, LaunchMark mark);
+cudaError_t launch_norm_finish(const StepDesc* descs, int n, float ils,
+                               const float* ils_dev,
+                               const unsigned long long* sums,
+                               const unsigned long long* found_slot,
+                               uint32_t epoch, double* terms, float max_norm,
+                               double* norm_out, float* clip_out,
+                               float* user_norm, cudaStream_t stream,
+                               LaunchMark mark);
 cudaError_t launch_clip_coef(const double* terms, int n,
                              const unsigned long long* found_slot, uint32_t epoch,
                              const uint32_t* found_flag, float max_norm,
@@ -1145,14 +1153,16 @@ int adam_step(const char* fn, bool l2, const fp8opt_param* params, int n,
   Workspace* ws = c.ws;
   cudaError_t e = cudaSuccess;
   if (nr.on) {
-    e = launch_grad_norm_terms(c.descs, c.chunks, ws->step_nchunks, n,
+    // the norm pass, then the terms, norm and clip coefficient in one launch
+    e = launch_grad_norm_terms(c.descs, c.chunks, ws->step_nchunks, 0,
                                inv_loss_scale, nullptr, c.sums, c.sc.found,
                                c.epoch, c.terms, nullptr, c.info->grad_norm,
                                ws->step_fmts, stream, launch_mark());
     if (e == cudaSuccess)
-      e = launch_clip_coef(c.terms, n, c.sc.found, c.epoch, nullptr,
-                           run_step ? nr.max_norm : 0.0f, c.norm, c.clip,
-                           nr.norm_dev, stream, launch_mark());
+      e = launch_norm_finish(c.descs, n, inv_loss_scale, nullptr, c.sums,
+                             c.sc.found, c.epoch, c.terms,
+                             run_step ? nr.max_norm : 0.0f, c.norm, c.clip,
+                             nr.norm_dev, stream, launch_mark());
     if (e != cudaSuccess) return cuda_fail(e, (std::string(fn) + ": launch").c_str());
     if (nr.max_norm > 0.0f) s.clip = c.clip;
   }
@@ -1655,12 +1665,9 @@ static int cast_adam_clipped(const char* fn, const fp8opt_cast_item* grads,
                                 fmt, info->cast_encode_sq[fmt], sums, sc.found,
                                 inv_loss_scale, ils_dev, stream, mark);
     if (e == cudaSuccess)
-      e = launch_grad_norm_terms(sdescs, schunks, 0, n, inv_loss_scale, ils_dev,
-                                 sums, sc.found, epoch, terms, nullptr, 0,
-                                 ws->step_fmts, stream, mark);
-    if (e == cudaSuccess)
-      e = launch_clip_coef(terms, n, sc.found, epoch, nullptr, max_grad_norm, norm,
-                           clip, grad_norm_dev, stream, mark);
+      e = launch_norm_finish(sdescs, n, inv_loss_scale, ils_dev, sums, sc.found,
+                             epoch, terms, max_grad_norm, norm, clip,
+                             grad_norm_dev, stream, mark);
     if (max_grad_norm > 0.0f) s.clip = clip;
     if (e == cudaSuccess)
       e = launch_step(sdescs, schunks, ws->step_nchunks, schunks + ws->step_nchunks,

@@ -251,38 +251,69 @@ grad_norm_terms_kernel(const StepDesc* __restrict__ descs, int n, float ils,
     *found_out = slot_value(*found, epoch) != 0 ? 1u : 0u;
 }
 
-// One CTA: total = sum of the terms in order, norm = sqrt(total) (+inf when
-// found_inf is set in the slot or in found_flag), clip coefficient.
+// total = the terms summed in record order in double (one thread; the
+// additions are a dependent chain, so the terms are read eight at a time
+// ahead of it), norm = sqrt(total) (+inf when found_inf is set in the slot
+// or in found_flag), clip coefficient.  Thread 0 only.
+__device__ __forceinline__ void finish_norm(const double* terms, int n, bool inf,
+                                            float max_norm, double* norm_out,
+                                            float* clip_out, float* user_norm) {
+  double total = 0.0;
+  int i = 0;
+  for (; i + 8 <= n; i += 8) {
+    double x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = terms[i + j];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) total = __dadd_rn(total, x[j]);
+  }
+  for (; i < n; ++i) total = __dadd_rn(total, terms[i]);
+  const double norm = inf ? __longlong_as_double(0x7FF0000000000000ll)
+                          : __dsqrt_rn(total);
+  float clip = 1.0f;
+  if (!inf && max_norm > 0.0f) {
+    const double c = __ddiv_rn((double)max_norm, __dadd_rn(norm, 1e-6));
+    if (c < 1.0) clip = __double2float_rn(c);
+  }
+  if (norm_out != nullptr) *norm_out = norm;
+  if (clip_out != nullptr) *clip_out = clip;
+  if (user_norm != nullptr) *user_norm = __double2float_rn(norm);
+}
+
+// One CTA: the norm and clip coefficient from n given terms (finish_norm).
 __global__ void __launch_bounds__(kThreads)
 clip_coef_kernel(const double* __restrict__ terms, int n,
                  const unsigned long long* __restrict__ found_slot,
                  uint32_t epoch, const uint32_t* __restrict__ found_flag,
                  float max_norm, double* __restrict__ norm_out,
                  float* __restrict__ clip_out, float* __restrict__ user_norm) {
-  __shared__ double term[kThreads];
+  if (threadIdx.x != 0) return;
   const bool inf = (found_slot != nullptr && slot_value(*found_slot, epoch) != 0) ||
                    (found_flag != nullptr && *found_flag != 0);
-  double total = 0.0;
-  for (int t0 = 0; t0 < n; t0 += kThreads) {
-    const int t = t0 + threadIdx.x;
-    if (t < n) term[threadIdx.x] = terms[t];
-    __syncthreads();
-    if (threadIdx.x == 0)
-      for (int i = 0; i < kThreads && t0 + i < n; ++i) total = __dadd_rn(total, term[i]);
-    __syncthreads();
+  finish_norm(terms, n, inf, max_norm, norm_out, clip_out, user_norm);
+}
+
+// One CTA: the records' terms as grad_norm_terms_kernel writes them (every
+// thread a share of the records), then, after the CTA barrier that makes
+// them visible, the norm and clip coefficient from them (finish_norm).
+// terms is written and read here, so it is neither const nor restrict.
+__global__ void __launch_bounds__(kThreads)
+norm_finish_kernel(const StepDesc* __restrict__ descs, int n, float ils,
+                   const float* __restrict__ ils_dev,
+                   const unsigned long long* __restrict__ sums,
+                   const unsigned long long* __restrict__ found_slot,
+                   uint32_t epoch, double* terms, float max_norm,
+                   double* __restrict__ norm_out, float* __restrict__ clip_out,
+                   float* __restrict__ user_norm) {
+  const float k_ils = ils_dev != nullptr ? *ils_dev : ils;
+  for (int t = threadIdx.x; t < n; t += blockDim.x) {
+    const U128 s = {sums[2 * t], sums[2 * t + 1]};
+    terms[t] = norm_term(s, __fdiv_rn(k_ils, *descs[t].g_scale));
   }
-  if (threadIdx.x == 0) {
-    const double norm = inf ? __longlong_as_double(0x7FF0000000000000ll)
-                            : __dsqrt_rn(total);
-    float clip = 1.0f;
-    if (!inf && max_norm > 0.0f) {
-      const double c = __ddiv_rn((double)max_norm, __dadd_rn(norm, 1e-6));
-      if (c < 1.0) clip = __double2float_rn(c);
-    }
-    if (norm_out != nullptr) *norm_out = norm;
-    if (clip_out != nullptr) *clip_out = clip;
-    if (user_norm != nullptr) *user_norm = __double2float_rn(norm);
-  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    finish_norm(terms, n, slot_value(*found_slot, epoch) != 0, max_norm, norm_out,
+                clip_out, user_norm);
 }
 
 // Writes a call's found_inf slot as 0 / 1 (out), after merging in an outside
@@ -446,6 +477,25 @@ cudaError_t launch_clip_coef(const double* terms, int n,
   clip_coef_kernel<<<1, kThreads, 0, stream>>>(terms, n, found_slot, epoch,
                                                found_flag, max_norm, norm_out,
                                                clip_out, user_norm);
+  if (mark) mark(kClipCoefK, 1, stream);
+  return cudaGetLastError();
+}
+
+// The records' terms, the norm and the clip coefficient in one launch (see
+// norm_finish_kernel): after the norm pass, in place of the terms kernel and
+// launch_clip_coef.
+cudaError_t launch_norm_finish(const StepDesc* descs, int n, float ils,
+                               const float* ils_dev,
+                               const unsigned long long* sums,
+                               const unsigned long long* found_slot,
+                               uint32_t epoch, double* terms, float max_norm,
+                               double* norm_out, float* clip_out,
+                               float* user_norm, cudaStream_t stream,
+                               LaunchMark mark) {
+  if (mark) mark(kClipCoefK, 0, stream);
+  norm_finish_kernel<<<1, kThreads, 0, stream>>>(descs, n, ils, ils_dev, sums,
+                                                 found_slot, epoch, terms, max_norm,
+                                                 norm_out, clip_out, user_norm);
   if (mark) mark(kClipCoefK, 1, stream);
   return cudaGetLastError();
 }
