@@ -304,10 +304,11 @@ def test_fused_clipped_threshold_above_norm_and_zero(bo):
     fused_clipped_lockstep(bo, wl, 2, 0.0)      # measures only
 
 
-def test_fused_clipped_inf_in_a_gradient_skips(bo):
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fused_clipped_inf_in_a_gradient_skips(bo, fmt):
     wl = dataclasses.replace(synth.o2_350m(n_layer=1, d=64, ffn=256, vocab=300,
                                            ctx=32), inf_site=(3, 17))
-    gpu, states, norms = fused_clipped_lockstep(bo, wl, 1, 0.1)
+    gpu, states, norms = fused_clipped_lockstep(bo, wl, 1, 0.1, fmt=fmt)
     assert norms == [math.inf]
     for i, s in enumerate(states):
         assert np.array_equal(to_np_u8(gpu.m[i]), s.m)
