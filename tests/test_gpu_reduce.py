@@ -107,6 +107,18 @@ def test_padded_stride_and_unaligned_stride(bo, k):
     assert compare(bo, shards, E5M2, E4M3, 0.25, pad=3) == 1.0
 
 
+@pytest.mark.parametrize("k", [1, 2, 8])
+@pytest.mark.parametrize("post", [0.0, -0.75, 3e37, 1e-40, float("inf")])
+def test_post_factors(bo, k, post):
+    """Zero, negative, overflowing, subnormal-making and infinite post
+    factors: amax, scale and codes against the oracle, in the passes
+    specialised on k = 1, 2 and 8."""
+    shards = random_shards(np.random.default_rng(50 + k), [0, 17, 40000, 100003],
+                           k, E4M3)
+    assert compare(bo, shards, E4M3, E4M3, post) >= 0.999
+    assert compare(bo, shards, E4M3, E5M2, post) >= 0.999
+
+
 def test_in_place_into_the_first_shard(bo):
     shards = random_shards(np.random.default_rng(4), [70000, 8192, 100], 3, E4M3)
     assert compare(bo, shards, E4M3, E4M3, 1.0, in_place=True) == 1.0
